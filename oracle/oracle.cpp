@@ -1,0 +1,489 @@
+// fp64 CPU oracle for block-sparse decode attention over a paged, head-major KV cache.
+//
+// TEST INFRASTRUCTURE ONLY.  Nothing in the library calls this code; only the tests, the
+// smoke check and the bench's CPU-baseline leg load it.  It shares no code, header, table or
+// helper with the CUDA path: it reads the same seeded inputs (bf16 bit patterns, int32
+// tables) and computes every step with plain loops in double precision, in the order the
+// pages state them, so that a reader can check it against the pages by eye.
+//
+// Sources (web pages, cited by title and section):
+//   [NOSA]  "NOSA: Native and Offloadable Sparse Attention" (technical summary), section
+//           "Method 1: the NOSA algorithm" (dual selection, locality guarantee, block-wise
+//           implementation, ED-DMA) and "Method 2: the NOSI system" (set-difference).
+//   [Spin]  "Unifying Sparse Attention with Hierarchical Memory for Scalable Long-Context LLM
+//           Serving", section 2B "Dynamic, locality-aware KV management" (bucketed LRU with
+//           64 recency buckets; per-head physical pages).
+//   [Lazy]  "LazyAttention" (technical summary), sections "Core idea: deferred positional
+//           encoding", "Technical implementation 2. Decoding" and "Mathematical equivalence".
+//   [FA]    "How KV sparsity achieves 1.5x acceleration for vLLM" (Novita AI), section
+//           "2. Attention modification" (softmax attention, rowmax / l statistics).
+//
+// Readings of points the pages leave open (each also listed in the design notes):
+//   R1 pooling averages keys inside each 16-token sub-block; the max is over the sub-block
+//      *scores*; the GQA group's scores are summed before the max.
+//   R2 the page holding the newest token (the local page) is always attended, outside the
+//      budget, and is never a candidate; candidates are the complete pages before it.
+//   R3 eviction scores are per page and ranked directly (pre-exp); exp is never applied.
+//   R4 Gamma_e candidates are the pages still alive; unselected candidates die forever;
+//      Gamma_q ranks all complete pages outside E (evicted pages allowed).
+//   R5 total order for ranking: score descending, then page index ascending.
+//   R6 RoPE is the half-split ("rotate-half") form over pairs (x_i, x_{i+64}),
+//      theta_i = theta^(-2i/128); stored keys carry only their document-local rotation.
+//   R7 packed page word: phys[0:18) | (valid-1)[18:24) | doc slot[24:32).
+//   R8 LRU: bucket = min(63, (t - ts) / W); empty slots are bucket 63; hits are touched
+//      first; victims are untouched slots in (bucket desc, slot asc) order.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <thread>
+#include <vector>
+
+namespace {
+
+constexpr int kD = 128;       // head dimension
+constexpr int kPage = 64;     // tokens per page (one selection block)
+constexpr int kSub = 16;      // tokens per pooling sub-block
+constexpr int kNSub = kPage / kSub;
+const double kNegInf = -std::numeric_limits<double>::infinity();
+
+// bf16 bit pattern -> exact double (a bf16 is the upper half of an IEEE binary32).
+double from_bf16(uint16_t h) {
+  uint32_t u = static_cast<uint32_t>(h) << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return static_cast<double>(f);
+}
+
+const uint16_t* row_ptr(const uint16_t* plane, int64_t phys, int t) {
+  return plane + (phys * kPage + t) * kD;
+}
+
+template <class F>
+void for_units(int n_units, int nthreads, F f) {
+  if (nthreads <= 0) nthreads = static_cast<int>(std::max(1u, std::thread::hardware_concurrency()));
+  nthreads = std::max(1, std::min(nthreads, n_units));
+  std::atomic<int> next{0};
+  auto work = [&] {
+    for (int i = next.fetch_add(1); i < n_units; i = next.fetch_add(1)) f(i);
+  };
+  if (nthreads == 1) { work(); return; }
+  std::vector<std::thread> th;
+  for (int t = 0; t < nthreads; ++t) th.emplace_back(work);
+  for (auto& x : th) x.join();
+}
+
+// Ranking under R5: true when (a_score, a_page) comes before (b_score, b_page).
+bool ranks_before(double as, int ap, double bs, int bp) {
+  if (as != bs) return as > bs;
+  return ap < bp;
+}
+
+// Top-k of `cand` (page ids) under R5 by the score array `sc`, by a plain full sort.
+std::vector<int> top_k(const std::vector<int>& cand, const double* sc, int k) {
+  std::vector<int> v = cand;
+  std::sort(v.begin(), v.end(), [&](int a, int b) { return ranks_before(sc[a], a, sc[b], b); });
+  if (static_cast<int>(v.size()) > k) v.resize(k);
+  return v;
+}
+
+}  // namespace
+
+extern "C" {
+
+// ---------------------------------------------------------------- packed page word (R7)
+// [Lazy] "Technical implementation 2. Decoding": block id and offset are bit-packed into a
+// single register-sized word.  Returns 0 on success, -1 if a field is out of range.
+int orc_meta_pack(int32_t phys, int32_t valid, int32_t slot, uint32_t* word) {
+  if (phys < 0 || phys >= (1 << 18) || valid < 1 || valid > 64 || slot < 0 || slot > 255) return -1;
+  *word = static_cast<uint32_t>(phys) | (static_cast<uint32_t>(valid - 1) << 18) |
+          (static_cast<uint32_t>(slot) << 24);
+  return 0;
+}
+
+void orc_meta_unpack(uint32_t word, int32_t* phys, int32_t* valid, int32_t* slot) {
+  *phys = static_cast<int32_t>(word & 0x3FFFFu);
+  *valid = static_cast<int32_t>((word >> 18) & 0x3Fu) + 1;
+  *slot = static_cast<int32_t>(word >> 24);
+}
+
+// ---------------------------------------------------------------- A-1 sub-block means
+// [NOSA] "Block-wise implementation": first stage of the two-stage pooling, the mean of the
+// keys inside each sub-block.  `valid` tokens of the 64-token page hold data; sub-block j
+// covers tokens [16j, 16j+16) and averages its cnt[j] valid rows (mean = 0 when cnt[j] = 0).
+void orc_page_means(const uint16_t* page, int valid, double* mean, int32_t* cnt) {
+  for (int j = 0; j < kNSub; ++j) {
+    const int lo = j * kSub, hi = std::min(valid, lo + kSub);
+    const int c = std::max(0, hi - lo);
+    cnt[j] = c;
+    for (int d = 0; d < kD; ++d) {
+      double s = 0.0;
+      for (int t = lo; t < hi; ++t) s += from_bf16(page[t * kD + d]);
+      mean[j * kD + d] = c > 0 ? s / c : 0.0;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- A-2 block scores
+// [NOSA] "Block-wise implementation" (two-stage pooling: mean inside sub-blocks, then max to
+// the block) with reading R1 for the GQA group:
+//   s[p] = max_j  sum_g  (q_g . mean_{p,j}) / sqrt(128)
+// for every complete page p before the local page (R2); every other entry is -inf.
+// q: G rows of 128 bf16; kplane: the pool plane of this kv head, [n_phys][64][128].
+void orc_score_unit(const uint16_t* q, int G, const uint16_t* kplane, const int32_t* pt_row,
+                    int seq_len, int np_out, double* s) {
+  const int local = (seq_len - 1) / kPage;
+  std::vector<double> mean(kNSub * kD);
+  int32_t cnt[kNSub];
+  const double inv_sqrt_d = 1.0 / std::sqrt(static_cast<double>(kD));
+  for (int p = 0; p < np_out; ++p) {
+    if (p >= local) { s[p] = kNegInf; continue; }
+    orc_page_means(row_ptr(kplane, pt_row[p], 0), kPage, mean.data(), cnt);
+    double best = kNegInf;
+    for (int j = 0; j < kNSub; ++j) {
+      double sum_g = 0.0;
+      for (int g = 0; g < G; ++g) {
+        double dot = 0.0;
+        for (int d = 0; d < kD; ++d) dot += from_bf16(q[g * kD + d]) * mean[j * kD + d];
+        sum_g += dot;
+      }
+      best = std::max(best, sum_g * inv_sqrt_d);
+    }
+    s[p] = best;
+  }
+}
+
+// ---------------------------------------------------------------- A-3 selection
+// [NOSA] "Dual-selection mechanism", "Locality guarantee" and "ED-DMA", with readings R2-R5:
+//   candidates C = complete pages 0 .. local-1
+//   A = pages of C still alive;  E = top-k_e of A by eviction score (pre-exp, never exp'ed)
+//   every page of A outside E dies (alive = 0) and can never enter E again
+//   Q = top-k_q of C \ E by query score;  output = sort(E u Q) then the local page.
+// alive: one byte per logical page (1 = alive); sel has room for k_e + k_q + 1 entries and
+// unused entries are set to -1.
+void orc_select_unit(const double* s, const double* e, uint8_t* alive, int np, int seq_len,
+                     int k_q, int k_e, int32_t* sel, int32_t* n_sel) {
+  const int local = (seq_len - 1) / kPage;
+  const int n_cand = std::min(local, np);
+  std::vector<int> A, rest;
+  for (int p = 0; p < n_cand; ++p)
+    if (alive[p]) A.push_back(p);
+  std::vector<int> E = top_k(A, e, k_e);
+  std::vector<uint8_t> inE(np, 0);
+  for (int p : E) inE[p] = 1;
+  for (int p : A)
+    if (!inE[p]) alive[p] = 0;
+  for (int p = 0; p < n_cand; ++p)
+    if (!inE[p]) rest.push_back(p);
+  std::vector<int> Q = top_k(rest, s, k_q);
+  std::vector<int> R = E;
+  R.insert(R.end(), Q.begin(), Q.end());
+  std::sort(R.begin(), R.end());
+  const int stride = k_e + k_q + 1;
+  for (int i = 0; i < stride; ++i) sel[i] = -1;
+  for (size_t i = 0; i < R.size(); ++i) sel[i] = R[i];
+  sel[R.size()] = local;
+  *n_sel = static_cast<int32_t>(R.size()) + 1;
+}
+
+// ---------------------------------------------------------------- A-4 attention
+// [FA] "2. Attention modification": softmax attention written as the plain two-pass form
+//   z_t = q . k_t / sqrt(128),  m = max z,  l = sum exp(z_t - m),
+//   O = sum exp(z_t - m) v_t / l,  LSE = m + log l   (natural log)
+// over every valid token of the listed pages (page i has valid[i] tokens).
+// out: G x 128, lse: G.  With no tokens at all, out = 0 and lse = -inf.
+void orc_attn_unit(const uint16_t* q, int G, const uint16_t* kplane, const uint16_t* vplane,
+                   const int32_t* phys, const int32_t* valid, int n_pages, double* out, double* lse) {
+  const double inv_sqrt_d = 1.0 / std::sqrt(static_cast<double>(kD));
+  std::vector<double> z;
+  for (int g = 0; g < G; ++g) {
+    z.clear();
+    for (int i = 0; i < n_pages; ++i)
+      for (int t = 0; t < valid[i]; ++t) {
+        const uint16_t* k = row_ptr(kplane, phys[i], t);
+        double dot = 0.0;
+        for (int d = 0; d < kD; ++d) dot += from_bf16(q[g * kD + d]) * from_bf16(k[d]);
+        z.push_back(dot * inv_sqrt_d);
+      }
+    if (z.empty()) {
+      for (int d = 0; d < kD; ++d) out[g * kD + d] = 0.0;
+      lse[g] = kNegInf;
+      continue;
+    }
+    const double m = *std::max_element(z.begin(), z.end());
+    double l = 0.0;
+    for (double x : z) l += std::exp(x - m);
+    for (int d = 0; d < kD; ++d) out[g * kD + d] = 0.0;
+    size_t idx = 0;
+    for (int i = 0; i < n_pages; ++i)
+      for (int t = 0; t < valid[i]; ++t, ++idx) {
+        const double w = std::exp(z[idx] - m) / l;
+        const uint16_t* v = row_ptr(vplane, phys[i], t);
+        for (int d = 0; d < kD; ++d) out[g * kD + d] += w * from_bf16(v[d]);
+      }
+    lse[g] = m + std::log(l);
+  }
+}
+
+// ---------------------------------------------------------------- A-5 lazy RoPE
+// RoPE rotation by position `pos` (reading R6): for i < 64, with a_i = pos * theta^(-2i/128),
+//   y_i = x_i cos a_i - x_{i+64} sin a_i,   y_{i+64} = x_{i+64} cos a_i + x_i sin a_i.
+void orc_rope(const double* x, double pos, double theta, double* y) {
+  for (int i = 0; i < kD / 2; ++i) {
+    const double a = pos * std::pow(theta, -2.0 * i / kD);
+    const double c = std::cos(a), s = std::sin(a);
+    y[i] = x[i] * c - x[i + kD / 2] * s;
+    y[i + kD / 2] = x[i + kD / 2] * c + x[i] * s;
+  }
+}
+
+// [Lazy] "Mathematical equivalence", materialised side: the query at position qpos is rotated
+// by R(qpos); each stored key of document slot i (placed at token offset doc_pos[i]) is copied
+// and rotated by R(doc_pos[i]) (it already carries its document-local rotation), then plain
+// softmax attention runs on the rotated copies.
+void orc_attn_materialised_unit(const uint16_t* q, int G, const uint16_t* kplane,
+                                const uint16_t* vplane, const int32_t* phys, const int32_t* valid,
+                                const int32_t* slot, int n_pages, int32_t qpos,
+                                const int32_t* doc_pos, double theta, double* out, double* lse) {
+  const double inv_sqrt_d = 1.0 / std::sqrt(static_cast<double>(kD));
+  std::vector<double> keys;  // rotated copies, one row per valid token
+  std::vector<int> page_of, tok_of;
+  double kin[kD], krot[kD];
+  for (int i = 0; i < n_pages; ++i)
+    for (int t = 0; t < valid[i]; ++t) {
+      const uint16_t* k = row_ptr(kplane, phys[i], t);
+      for (int d = 0; d < kD; ++d) kin[d] = from_bf16(k[d]);
+      orc_rope(kin, static_cast<double>(doc_pos[slot[i]]), theta, krot);
+      keys.insert(keys.end(), krot, krot + kD);
+      page_of.push_back(i);
+      tok_of.push_back(t);
+    }
+  const size_t n = page_of.size();
+  double qin[kD], qrot[kD];
+  std::vector<double> z(n);
+  for (int g = 0; g < G; ++g) {
+    for (int d = 0; d < kD; ++d) qin[d] = from_bf16(q[g * kD + d]);
+    orc_rope(qin, static_cast<double>(qpos), theta, qrot);
+    for (int d = 0; d < kD; ++d) out[g * kD + d] = 0.0;
+    if (n == 0) { lse[g] = kNegInf; continue; }
+    for (size_t r = 0; r < n; ++r) {
+      double dot = 0.0;
+      for (int d = 0; d < kD; ++d) dot += qrot[d] * keys[r * kD + d];
+      z[r] = dot * inv_sqrt_d;
+    }
+    const double m = *std::max_element(z.begin(), z.end());
+    double l = 0.0;
+    for (double x : z) l += std::exp(x - m);
+    for (size_t r = 0; r < n; ++r) {
+      const double w = std::exp(z[r] - m) / l;
+      const uint16_t* v = row_ptr(vplane, phys[page_of[r]], tok_of[r]);
+      for (int d = 0; d < kD; ++d) out[g * kD + d] += w * from_bf16(v[d]);
+    }
+    lse[g] = m + std::log(l);
+  }
+}
+
+// [Lazy] "Technical implementation 2. Decoding", lazy side: keys are used as stored; the query
+// is rotated once per document by the relative offset qpos - doc_pos[slot] and that rotated
+// query scores every key of the document.
+void orc_attn_lazy_unit(const uint16_t* q, int G, const uint16_t* kplane, const uint16_t* vplane,
+                        const int32_t* phys, const int32_t* valid, const int32_t* slot, int n_pages,
+                        int32_t qpos, const int32_t* doc_pos, double theta, double* out,
+                        double* lse) {
+  const double inv_sqrt_d = 1.0 / std::sqrt(static_cast<double>(kD));
+  double qin[kD], qrot[kD];
+  std::vector<double> z;
+  for (int g = 0; g < G; ++g) {
+    for (int d = 0; d < kD; ++d) qin[d] = from_bf16(q[g * kD + d]);
+    z.clear();
+    int cur_slot = -1;
+    for (int i = 0; i < n_pages; ++i) {
+      if (slot[i] != cur_slot) {
+        cur_slot = slot[i];
+        orc_rope(qin, static_cast<double>(qpos) - doc_pos[cur_slot], theta, qrot);
+      }
+      for (int t = 0; t < valid[i]; ++t) {
+        const uint16_t* k = row_ptr(kplane, phys[i], t);
+        double dot = 0.0;
+        for (int d = 0; d < kD; ++d) dot += qrot[d] * from_bf16(k[d]);
+        z.push_back(dot * inv_sqrt_d);
+      }
+    }
+    for (int d = 0; d < kD; ++d) out[g * kD + d] = 0.0;
+    if (z.empty()) { lse[g] = kNegInf; continue; }
+    const double m = *std::max_element(z.begin(), z.end());
+    double l = 0.0;
+    for (double x : z) l += std::exp(x - m);
+    size_t idx = 0;
+    for (int i = 0; i < n_pages; ++i)
+      for (int t = 0; t < valid[i]; ++t, ++idx) {
+        const double w = std::exp(z[idx] - m) / l;
+        const uint16_t* v = row_ptr(vplane, phys[i], t);
+        for (int d = 0; d < kD; ++d) out[g * kD + d] += w * from_bf16(v[d]);
+      }
+    lse[g] = m + std::log(l);
+  }
+}
+
+// ---------------------------------------------------------------- A-6 set-difference
+// [NOSA] "Method 2: NOSI", optimised memory layout: the blocks to swap in are the selected
+// blocks that are not GPU-resident.  missing = sel \ resident (ascending, sel ascending);
+// slot[i] = the resident slot holding sel[i], or -1.  resident holds -1 for empty slots.
+// missing and slot have `stride` entries; those past the results are set to -1.
+void orc_setdiff_unit(const int32_t* resident, int n_slots, const int32_t* sel, int n_sel,
+                      int stride, int32_t* missing, int32_t* n_missing, int32_t* slot) {
+  for (int i = 0; i < stride; ++i) missing[i] = slot[i] = -1;
+  int m = 0;
+  for (int i = 0; i < n_sel; ++i) {
+    int found = -1;
+    for (int s = 0; s < n_slots; ++s)
+      if (resident[s] >= 0 && resident[s] == sel[i]) { found = s; break; }
+    slot[i] = found;
+    if (found < 0) missing[m++] = sel[i];
+  }
+  *n_missing = m;
+}
+
+// ---------------------------------------------------------------- A-7 bucketed LRU
+// [Spin] 2B "Bucketed LRU policy": resident pages are grouped into 64 recency buckets by
+// their timestamps and evicted a bucket at a time, oldest first (reading R8):
+//   1. every hit slot (slot[i] >= 0) is touched: ts = t
+//   2. bucket(s) = 63 for an empty slot, else min(63, (t - ts[s]) / W); hist counts all slots
+//   3. victims: the n_missing untouched slots first in (bucket desc, slot asc) order
+//   4. missing[i] is installed in victims[i] with ts = t
+// victims has `stride` entries; unused entries are -1.
+void orc_lru_unit(int32_t* resident, int32_t* ts, int n_slots, const int32_t* slot, int n_sel,
+                  const int32_t* missing, int n_missing, int32_t t, int W, int stride,
+                  int32_t* victims, int32_t* hist) {
+  std::vector<uint8_t> touched(n_slots, 0);
+  for (int i = 0; i < n_sel; ++i)
+    if (slot[i] >= 0) { ts[slot[i]] = t; touched[slot[i]] = 1; }
+  std::vector<int> bucket(n_slots);
+  for (int b = 0; b < 64; ++b) hist[b] = 0;
+  for (int s = 0; s < n_slots; ++s) {
+    if (resident[s] < 0) {
+      bucket[s] = 63;
+    } else {
+      const int64_t age = static_cast<int64_t>(t) - ts[s];
+      bucket[s] = static_cast<int>(std::min<int64_t>(63, age / W));
+    }
+    hist[bucket[s]] += 1;
+  }
+  std::vector<int> order;
+  for (int s = 0; s < n_slots; ++s)
+    if (!touched[s]) order.push_back(s);
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return bucket[a] > bucket[b]; });
+  for (int i = 0; i < stride; ++i) victims[i] = -1;
+  for (int i = 0; i < n_missing && i < static_cast<int>(order.size()); ++i) {
+    victims[i] = order[i];
+    resident[order[i]] = missing[i];
+    ts[order[i]] = t;
+  }
+}
+
+// ---------------------------------------------------------------- batch drivers
+// The same functions applied to a list of (request, kv head) units, one unit per task on a
+// pool of `nthreads` threads (0 = all hardware threads).  Unit u = b * Hk + h.  Pools are
+// [Hk][n_phys][64][128]; q is [B][Hq][128]; kv head h serves query heads h*G .. h*G+G-1.
+
+void orc_score_batch(int B, int Hq, int Hk, const uint16_t* q, const uint16_t* kpool, int64_t n_phys,
+                     const int32_t* page_table, int np_max, const int32_t* seq_len,
+                     const int32_t* units, int n_units, double* s, int nthreads) {
+  (void)B;
+  const int G = Hq / Hk;
+  for_units(n_units, nthreads, [&](int i) {
+    const int u = units[i], b = u / Hk, h = u % Hk;
+    orc_score_unit(q + (static_cast<int64_t>(b) * Hq + h * G) * kD, G,
+                   kpool + static_cast<int64_t>(h) * n_phys * kPage * kD,
+                   page_table + static_cast<int64_t>(b) * np_max, seq_len[b], np_max,
+                   s + static_cast<int64_t>(u) * np_max);
+  });
+}
+
+void orc_select_batch(int Hk, const double* s, const double* e, uint8_t* alive, int np_max,
+                      const int32_t* seq_len, int k_q, int k_e, int32_t* sel, int32_t* n_sel,
+                      const int32_t* units, int n_units, int nthreads) {
+  const int stride = k_e + k_q + 1;
+  for_units(n_units, nthreads, [&](int i) {
+    const int u = units[i], b = u / Hk;
+    const int64_t o = static_cast<int64_t>(u) * np_max;
+    orc_select_unit(s + o, e + o, alive + o, np_max, seq_len[b], k_q, k_e,
+                    sel + static_cast<int64_t>(u) * stride, n_sel + u);
+  });
+}
+
+void orc_sparse_attn_batch(int B, int Hq, int Hk, const uint16_t* q, const uint16_t* kpool,
+                           const uint16_t* vpool, int64_t n_phys, const int32_t* page_table,
+                           int np_max, const int32_t* sel, const int32_t* n_sel, int sel_stride,
+                           const int32_t* seq_len, const int32_t* units, int n_units, double* out,
+                           double* lse, int nthreads) {
+  (void)B;
+  const int G = Hq / Hk;
+  for_units(n_units, nthreads, [&](int i) {
+    const int u = units[i], b = u / Hk, h = u % Hk;
+    const int n = n_sel[u];
+    std::vector<int32_t> phys(n), valid(n);
+    for (int j = 0; j < n; ++j) {
+      const int p = sel[static_cast<int64_t>(u) * sel_stride + j];
+      phys[j] = page_table[static_cast<int64_t>(b) * np_max + p];
+      valid[j] = std::min(kPage, seq_len[b] - kPage * p);
+    }
+    const int64_t plane = static_cast<int64_t>(h) * n_phys * kPage * kD;
+    const int64_t qo = (static_cast<int64_t>(b) * Hq + h * G);
+    orc_attn_unit(q + qo * kD, G, kpool + plane, vpool + plane, phys.data(), valid.data(), n,
+                  out + qo * kD, lse + qo);
+  });
+}
+
+// Lazy-RoPE batch.  phys/valid/slot are [B][meta_heads][np_max] (meta_heads = 1 shares one page
+// list across kv heads, or Hk); doc_pos is [B][max_docs].  materialise != 0 runs the
+// materialised form, else the lazy form.
+void orc_lazy_attn_batch(int B, int Hq, int Hk, const uint16_t* q, const uint16_t* kpool,
+                         const uint16_t* vpool, int64_t n_phys, const int32_t* phys,
+                         const int32_t* valid, const int32_t* slot, int meta_heads,
+                         const int32_t* n_pages, int np_max, const int32_t* qpos,
+                         const int32_t* doc_pos, int max_docs, double theta, int materialise,
+                         const int32_t* units, int n_units, double* out, double* lse, int nthreads) {
+  (void)B;
+  const int G = Hq / Hk;
+  for_units(n_units, nthreads, [&](int i) {
+    const int u = units[i], b = u / Hk, h = u % Hk;
+    const int mh = meta_heads == 1 ? 0 : h;
+    const int64_t mo = (static_cast<int64_t>(b) * meta_heads + mh) * np_max;
+    const int64_t plane = static_cast<int64_t>(h) * n_phys * kPage * kD;
+    const int64_t qo = (static_cast<int64_t>(b) * Hq + h * G);
+    const int32_t* dp = doc_pos + static_cast<int64_t>(b) * max_docs;
+    if (materialise)
+      orc_attn_materialised_unit(q + qo * kD, G, kpool + plane, vpool + plane, phys + mo, valid + mo,
+                                 slot + mo, n_pages[b], qpos[b], dp, theta, out + qo * kD, lse + qo);
+    else
+      orc_attn_lazy_unit(q + qo * kD, G, kpool + plane, vpool + plane, phys + mo, valid + mo,
+                         slot + mo, n_pages[b], qpos[b], dp, theta, out + qo * kD, lse + qo);
+  });
+}
+
+void orc_setdiff_batch(const int32_t* resident, int n_slots, const int32_t* sel, const int32_t* n_sel,
+                       int sel_stride, int n_units, int32_t* missing, int32_t* n_missing,
+                       int32_t* slot, int nthreads) {
+  for_units(n_units, nthreads, [&](int u) {
+    const int64_t so = static_cast<int64_t>(u) * sel_stride;
+    orc_setdiff_unit(resident + static_cast<int64_t>(u) * n_slots, n_slots, sel + so, n_sel[u],
+                     sel_stride, missing + so, n_missing + u, slot + so);
+  });
+}
+
+void orc_lru_batch(int32_t* resident, int32_t* ts, int n_slots, const int32_t* slot,
+                   const int32_t* n_sel, const int32_t* missing, const int32_t* n_missing,
+                   int sel_stride, int n_units, int32_t t, int W, int32_t* victims, int32_t* hist,
+                   int nthreads) {
+  for_units(n_units, nthreads, [&](int u) {
+    const int64_t so = static_cast<int64_t>(u) * sel_stride;
+    const int64_t ro = static_cast<int64_t>(u) * n_slots;
+    orc_lru_unit(resident + ro, ts + ro, n_slots, slot + so, n_sel[u], missing + so, n_missing[u], t,
+                 W, sel_stride, victims + so, hist + static_cast<int64_t>(u) * 64);
+  });
+}
+
+}  // extern "C"

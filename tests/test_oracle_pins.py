@@ -1,0 +1,418 @@
+"""Pins for the fp64 oracle, against things other than the oracle itself.
+
+Each pin is chosen so that a plausible slip in the oracle fails at least one of them:
+
+* page word      -- exhaustive per-field round trip, fixed known words, range rejection.
+* sub-block mean -- closed form on integer-valued keys; numpy mean; partial / empty sub-blocks.
+* block score    -- pooling linearity (the mean of the token scores of a sub-block equals the
+                    score of its mean key), brute force in numpy over all pages; a constructed
+                    page whose best sub-block is known; -inf at and after the local page.
+* selection      -- the defining property of a top-k under (score desc, page asc), tie cases,
+                    alive-bit updates, padding; the NOSA locality bound gamma(t) >= k_e/k and
+                    "an evicted page never re-enters" over random trajectories that cross page
+                    boundaries; sparse == dense when the budget covers every page.
+* attention      -- scipy logsumexp/softmax; identical keys give the mean of V; a single token;
+                    page-order invariance; the split/merge identity of the LSE statistics.
+* RoPE / lazy    -- R(0) = I, R(a)R(b) = R(a+b), norm preservation, the theta_0 = 1 pair,
+                    dependence on n - m only, lazy == materialised, P = 0 reduces to plain
+                    attention.
+* set-difference -- Python sets.
+* bucketed LRU   -- bucket-by-bucket brute force, plus invariants (victims distinct, untouched,
+                    all selected pages resident afterwards, histogram sums to the slot count).
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+from scipy.special import logsumexp, softmax
+
+import gen
+import oracle
+
+D, PAGE = 128, 64
+
+
+def bf(x):
+    return gen.f32_to_bf16(np.asarray(x, np.float32))
+
+
+def f(x):
+    return gen.bf16_to_f32(x).astype(np.float64)
+
+
+# ------------------------------------------------------------------------------ page word
+
+def test_meta_known_words():
+    assert oracle.meta_pack(0, 1, 0) == 0
+    assert oracle.meta_pack(1, 64, 0) == 0x00FC0001
+    assert oracle.meta_pack(0x3FFFF, 64, 255) == 0xFFFFFFFF
+    assert oracle.meta_pack(5, 2, 3) == (5 | (1 << 18) | (3 << 24))
+
+
+@pytest.mark.parametrize("field", ["phys", "valid", "slot"])
+def test_meta_roundtrip_each_field_exhaustive(field):
+    rng = np.random.default_rng(1)
+    ranges = {"phys": range(1 << 18), "valid": range(1, 65), "slot": range(256)}
+    others = {k: int(rng.integers(r.start, r.stop)) for k, r in ranges.items()}
+    for v in ranges[field]:
+        args = dict(others)
+        args[field] = v
+        w = oracle.meta_pack(args["phys"], args["valid"], args["slot"])
+        assert oracle.meta_unpack(w) == (args["phys"], args["valid"], args["slot"])
+
+
+def test_meta_roundtrip_random_and_rejects():
+    rng = np.random.default_rng(2)
+    for _ in range(3000):
+        p, v, s = int(rng.integers(0, 1 << 18)), int(rng.integers(1, 65)), int(rng.integers(0, 256))
+        assert oracle.meta_unpack(oracle.meta_pack(p, v, s)) == (p, v, s)
+    for bad in [(-1, 1, 0), (1 << 18, 1, 0), (0, 0, 0), (0, 65, 0), (0, 1, 256), (0, 1, -1)]:
+        with pytest.raises(ValueError):
+            oracle.meta_pack(*bad)
+
+
+# ------------------------------------------------------------------------------ pooling
+
+def test_page_means_closed_form():
+    t = np.arange(PAGE)[:, None]
+    page = bf(np.broadcast_to((t % 16) - 7.0, (PAGE, D)))     # each sub-block holds -7..8
+    mean, cnt = oracle.page_means(page, 64)
+    assert cnt.tolist() == [16, 16, 16, 16]
+    assert np.all(mean == 0.5)
+    mean, cnt = oracle.page_means(page, 40)                    # rows 32..39 hold -7..0
+    assert cnt.tolist() == [16, 16, 8, 0]
+    assert np.all(mean[:2] == 0.5) and np.all(mean[2] == -3.5) and np.all(mean[3] == 0.0)
+
+
+def test_page_means_numpy():
+    page = gen.rows_bf16(3, 1, PAGE)
+    mean, _ = oracle.page_means(page, 64)
+    ref = f(page).reshape(4, 16, D).mean(axis=1)
+    assert np.allclose(mean, ref, rtol=0, atol=1e-12)
+
+
+def _scores_bruteforce(q, kplane, pt_row, L, np_out):
+    """Pooled token scores: for each sub-block, the mean over its 16 tokens of
+    sum_g q_g . k_t / sqrt(d); then the max over the 4 sub-blocks."""
+    local = (L - 1) // PAGE
+    out = np.full(np_out, -np.inf)
+    qf = f(q)
+    for p in range(min(local, np_out)):
+        keys = f(kplane[pt_row[p]])                  # 64 x 128
+        tok = (keys @ qf.T).sum(axis=1) / math.sqrt(D)    # per-token group score
+        out[p] = tok.reshape(4, 16).mean(axis=1).max()
+    return out
+
+
+def test_score_unit_pooling_linearity_bruteforce():
+    w = gen.sparse_workload(1, 8, 2, 1000, 4, 4, seed=11, outlier_p=0.05)
+    for h in range(2):
+        q = w["q"][0, h * 4:(h + 1) * 4]
+        s = oracle.score_unit(q, w["k_pool"][h], w["page_table"][0], 1000, w["np_max"])
+        ref = _scores_bruteforce(q, w["k_pool"][h], w["page_table"][0], 1000, w["np_max"])
+        assert np.array_equal(np.isinf(s), np.isinf(ref))
+        fin = np.isfinite(ref)
+        assert np.allclose(s[fin], ref[fin], rtol=1e-12, atol=1e-12)
+    # local page = (1000-1)//64 = 15; pages 15.. are not candidates
+    assert np.isinf(s[15:]).all() and np.isfinite(s[:15]).all()
+
+
+def test_score_unit_picks_best_subblock_and_sums_group():
+    # one page; sub-block 2 has mean +1 on dim 0, the others -1; q_g = e_0 for both heads
+    page = np.full((PAGE, D), 0.0, np.float32)
+    page[:, 0] = -1.0
+    page[32:48, 0] = 1.0
+    kplane = bf(page)[None]                         # n_phys = 1
+    q = bf(np.eye(1, D, 0).repeat(2, 0))            # G = 2, both e_0
+    s = oracle.score_unit(q, kplane, np.array([0, 0], np.int32), 2 * PAGE, 2)
+    assert s[0] == pytest.approx(2.0 / math.sqrt(D), abs=1e-15)   # (1 + 1) / sqrt(128)
+    assert s[1] == -np.inf
+
+
+# ------------------------------------------------------------------------------ selection
+
+def _assert_topk(chosen, pool, sc, k):
+    chosen, pool = set(chosen), set(pool)
+    assert chosen <= pool and len(chosen) == min(k, len(pool))
+    for a in chosen:
+        for b in pool - chosen:
+            assert (sc[a] > sc[b]) or (sc[a] == sc[b] and a < b)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_select_topk_definition_with_ties(seed):
+    rng = np.random.default_rng(seed)
+    npg = int(rng.integers(3, 40))
+    L = int(rng.integers(1, npg * PAGE + 1))
+    local = (L - 1) // PAGE
+    s = rng.integers(-3, 4, npg).astype(np.float64)      # many ties
+    e = rng.integers(-3, 4, npg).astype(np.float64)
+    alive = (rng.random(npg) < 0.7).astype(np.uint8)
+    k_q, k_e = int(rng.integers(0, 6)), int(rng.integers(0, 6))
+    sel, n, alive2 = oracle.select_unit(s, e, alive, L, k_q, k_e)
+    cand = list(range(min(local, npg)))
+    A = [p for p in cand if alive[p]]
+    E = [p for p in A if alive2[p]]
+    _assert_topk(E, A, e, k_e)
+    # unselected alive candidates die; non-candidates keep their bit
+    assert all(alive2[p] == 0 for p in set(A) - set(E))
+    assert np.array_equal(alive2[min(local, npg):], alive[min(local, npg):])
+    R = [int(x) for x in sel[:n - 1]]
+    Q = sorted(set(R) - set(E))
+    _assert_topk(Q, [p for p in cand if p not in E], s, k_q)
+    assert R == sorted(R) and sel[n - 1] == local and (sel[n:] == -1).all()
+    assert len(R) == len(set(R)) == len(E) + len(Q)
+
+
+def _run_traj(seed, L0, steps, k_e, k_q, npg):
+    rng = np.random.default_rng(seed)
+    e = rng.normal(size=npg)
+    alive = np.ones(npg, np.uint8)
+    prev_S, dead = None, set()
+    k = k_e + k_q
+    gammas = []
+    for t in range(steps):
+        L = L0 + t + 1
+        e = e + 0.1 * rng.normal(size=npg)
+        s = rng.normal(size=npg)
+        before = alive.copy()
+        sel, n, alive = oracle.select_unit(s, e, alive, L, k_q, k_e)
+        local = (L - 1) // PAGE
+        E = {p for p in range(local) if alive[p]}
+        assert not (E & dead), "an evicted page re-entered the eviction-head set"
+        assert all(before[p] for p in E)
+        dead |= {p for p in range(local) if before[p] and not alive[p]}
+        R = set(int(x) for x in sel[:n - 1])
+        S = R | {local}
+        if prev_S is not None and local >= k:
+            gamma = len(R & prev_S) / k
+            gammas.append(gamma)
+            assert gamma >= k_e / k - 1e-12
+        prev_S = S
+    return gammas
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_locality_and_monotone_eviction_across_page_boundaries(seed):
+    # 150 steps starting 20 tokens before a page boundary: crosses 3 boundaries
+    g = _run_traj(seed, L0=40 * PAGE - 20, steps=150, k_e=12, k_q=4, npg=45)
+    assert len(g) == 149 and min(g) >= 0.75
+
+
+def test_locality_small_budgets():
+    _run_traj(9, L0=10 * PAGE - 3, steps=200, k_e=3, k_q=5, npg=15)
+
+
+# ------------------------------------------------------------------------------ attention
+
+def _dense_ref(q, kplane, vplane, phys, valid):
+    keys = np.concatenate([f(kplane[p, :v]) for p, v in zip(phys, valid)])
+    vals = np.concatenate([f(vplane[p, :v]) for p, v in zip(phys, valid)])
+    z = f(q) @ keys.T / math.sqrt(D)
+    return softmax(z, axis=1) @ vals, logsumexp(z, axis=1)
+
+
+def test_attn_scipy_bruteforce():
+    w = gen.sparse_workload(1, 8, 2, 700, 4, 4, seed=5, outlier_p=0.05)
+    phys = w["page_table"][0, [0, 3, 5, 10]]
+    valid = np.array([64, 64, 64, 700 - 640], np.int32)
+    q = w["q"][0, :4]
+    out, lse = oracle.attn_unit(q, w["k_pool"][0], w["v_pool"][0], phys, valid)
+    ro, rl = _dense_ref(q, w["k_pool"][0], w["v_pool"][0], phys, valid)
+    assert np.allclose(out, ro, atol=1e-12) and np.allclose(lse, rl, atol=1e-12)
+
+
+def test_attn_identical_keys_and_single_token():
+    kplane = bf(np.tile(gen.normal_f32(0, 1, D), (2, PAGE, 1)))     # all keys the same
+    vplane = gen.rows_bf16(0, 2, 2 * PAGE).reshape(2, PAGE, D)
+    q = gen.rows_bf16(0, 3, 3)
+    out, lse = oracle.attn_unit(q, kplane, vplane, [0, 1], [64, 30])
+    vals = np.concatenate([f(vplane[0]), f(vplane[1, :30])])
+    assert np.allclose(out, vals.mean(0)[None], atol=1e-12)
+    z = f(q) @ f(kplane[0, 0]) / math.sqrt(D)
+    assert np.allclose(lse, z + math.log(94), atol=1e-12)
+    out1, lse1 = oracle.attn_unit(q, kplane, vplane, [1], [1])
+    assert np.allclose(out1, f(vplane[1, 0])[None], atol=0) and np.allclose(lse1, z, atol=1e-13)
+    out0, lse0 = oracle.attn_unit(q, kplane, vplane, [], [])
+    assert (out0 == 0).all() and (lse0 == -np.inf).all()
+
+
+def test_attn_page_order_invariance_and_lse_merge():
+    w = gen.sparse_workload(1, 4, 1, 64 * 9, 2, 2, seed=8)
+    K, V, q = w["k_pool"][0], w["v_pool"][0], w["q"][0]
+    phys = w["page_table"][0]
+    valid = np.full(9, 64, np.int32)
+    o, l = oracle.attn_unit(q, K, V, phys, valid)
+    perm = np.random.default_rng(0).permutation(9)
+    o2, l2 = oracle.attn_unit(q, K, V, phys[perm], valid[perm])
+    assert np.allclose(o, o2, atol=1e-13) and np.allclose(l, l2, atol=1e-13)
+    oa, la = oracle.attn_unit(q, K, V, phys[:4], valid[:4])
+    ob, lb = oracle.attn_unit(q, K, V, phys[4:], valid[4:])
+    lm = np.logaddexp(la, lb)
+    om = oa * np.exp(la - lm)[:, None] + ob * np.exp(lb - lm)[:, None]
+    assert np.allclose(om, o, atol=1e-12) and np.allclose(lm, l, atol=1e-12)
+
+
+def test_sparse_equals_dense_when_budget_covers_everything():
+    w = gen.sparse_workload(1, 8, 2, 64 * 6 + 10, 8, 8, seed=4)
+    s = oracle.score_batch(w["q"], w["k_pool"], w["page_table"], w["seq_len"])
+    sel, n_sel, _ = oracle.select_batch(s, w["evict"], np.ones_like(w["evict"], np.uint8),
+                                        w["seq_len"], 8, 8)
+    assert (n_sel == 7).all() and (sel[..., :7] == np.arange(7)).all()
+    out, lse = oracle.sparse_attn_batch(w["q"], w["k_pool"], w["v_pool"], w["page_table"], sel,
+                                        n_sel, w["seq_len"])
+    for h in range(2):
+        ro, rl = _dense_ref(w["q"][0, 4 * h:4 * h + 4], w["k_pool"][h], w["v_pool"][h],
+                            w["page_table"][0, :7], [64] * 6 + [10])
+        assert np.allclose(out[0, 4 * h:4 * h + 4], ro, atol=1e-12)
+        assert np.allclose(lse[0, 4 * h:4 * h + 4], rl, atol=1e-12)
+
+
+# ------------------------------------------------------------------------------ RoPE / lazy
+
+def test_rope_identities():
+    x = gen.normal_f64(1, 1, D)
+    th = 500000.0
+    assert np.allclose(oracle.rope(x, 0, th), x, atol=0)
+    a, b = 1234.0, -567.0
+    assert np.allclose(oracle.rope(oracle.rope(x, a, th), b, th), oracle.rope(x, a + b, th), atol=1e-10)
+    assert abs(np.linalg.norm(oracle.rope(x, 98765.0, th)) - np.linalg.norm(x)) < 1e-11
+    # dimension pair 0 has frequency theta^0 = 1: e_0 -> (cos p) e_0 + (sin p) e_64
+    e0 = np.eye(1, D, 0)[0]
+    y = oracle.rope(e0, 2.0, th)
+    assert y[0] == pytest.approx(math.cos(2.0), abs=1e-15)
+    assert y[64] == pytest.approx(math.sin(2.0), abs=1e-15)
+    assert np.count_nonzero(y) == 2
+    # the last pair turns slowest: theta^(-126/128)
+    e63 = np.eye(1, D, 63)[0]
+    y = oracle.rope(e63, 1e5, th)
+    ang = 1e5 * th ** (-126 / 128)
+    assert y[63] == pytest.approx(math.cos(ang), abs=1e-12)
+    assert y[127] == pytest.approx(math.sin(ang), abs=1e-12)
+
+
+def test_rope_scores_depend_on_offset_only():
+    q, k = gen.normal_f64(2, 1, D), gen.normal_f64(2, 2, D)
+    th = 500000.0
+    base = oracle.rope(q, 40000, th) @ oracle.rope(k, 1000, th)
+    for n, m in [(39000, 0), (45000, 6000), (100000, 61000)]:
+        assert oracle.rope(q, n, th) @ oracle.rope(k, m, th) == pytest.approx(base, abs=1e-9)
+
+
+def _lazy_case(seed):
+    w = gen.lazy_rag(seed=seed, B=2, Hq=4, Hk=2, n_docs=6, docs_per_req=3, min_len=70, max_len=200,
+                     theta=500000.0)
+    return w
+
+
+def test_lazy_equals_materialised():
+    w = _lazy_case(3)
+    om, lm = oracle.lazy_attn_batch(w["q"], w["k_pool"], w["v_pool"], w["phys"], w["valid"],
+                                    w["slot"], w["n_pages"], w["qpos"], w["doc_pos"], w["theta"],
+                                    materialise=True)
+    ol, ll = oracle.lazy_attn_batch(w["q"], w["k_pool"], w["v_pool"], w["phys"], w["valid"],
+                                    w["slot"], w["n_pages"], w["qpos"], w["doc_pos"], w["theta"],
+                                    materialise=False)
+    assert np.abs(om - ol).max() <= 1e-12 and np.abs(lm - ll).max() <= 1e-12
+
+
+def test_lazy_single_doc_at_query_reduces_to_plain_attention():
+    # one document placed at offset P with the query at n = P: relative offset 0, R(0) = I
+    w = _lazy_case(4)
+    b, n = 0, int(w["n_pages"][0])
+    first = w["slot"][b, :n] == 0
+    phys, valid = w["phys"][b, :n][first], w["valid"][b, :n][first]
+    slot = np.zeros(len(phys), np.int32)
+    for P in (0, 777):
+        out, lse = oracle.attn_lazy_unit(w["q"][b, :2], w["k_pool"][0], w["v_pool"][0], phys, valid,
+                                         slot, P, [P], w["theta"])
+        ro, rl = oracle.attn_unit(w["q"][b, :2], w["k_pool"][0], w["v_pool"][0], phys, valid)
+        assert np.allclose(out, ro, atol=1e-13) and np.allclose(lse, rl, atol=1e-13)
+
+
+def test_lazy_differs_from_unrotated_when_offsets_nonzero():
+    # guards against a rotation that silently does nothing
+    w = _lazy_case(5)
+    b, n = 1, int(w["n_pages"][1])
+    out, _ = oracle.attn_lazy_unit(w["q"][b, :2], w["k_pool"][0], w["v_pool"][0], w["phys"][b, :n],
+                                   w["valid"][b, :n], w["slot"][b, :n], w["qpos"][b],
+                                   w["doc_pos"][b], w["theta"])
+    ro, _ = oracle.attn_unit(w["q"][b, :2], w["k_pool"][0], w["v_pool"][0], w["phys"][b, :n],
+                             w["valid"][b, :n])
+    assert np.abs(out - ro).max() > 1e-3
+
+
+# ------------------------------------------------------------------------------ set-difference
+
+@pytest.mark.parametrize("seed", range(6))
+def test_setdiff_python_sets(seed):
+    rng = np.random.default_rng(seed)
+    n_slots, stride = 40, 12
+    resident = np.full(n_slots, -1, np.int32)
+    ids = rng.choice(100, size=int(rng.integers(0, n_slots)), replace=False)
+    pos = rng.choice(n_slots, size=len(ids), replace=False)
+    resident[pos] = ids
+    n_sel = int(rng.integers(0, stride + 1))
+    sel = np.full(stride, -1, np.int32)
+    sel[:n_sel] = np.sort(rng.choice(100, size=n_sel, replace=False))
+    missing, nm, slot = oracle.setdiff_unit(resident, sel, n_sel, stride)
+    want = sorted(set(sel[:n_sel].tolist()) - set(resident.tolist()))
+    assert missing[:nm].tolist() == want and (missing[nm:] == -1).all()
+    for i in range(n_sel):
+        if sel[i] in set(resident.tolist()):
+            assert resident[slot[i]] == sel[i]
+        else:
+            assert slot[i] == -1
+    assert (slot[n_sel:] == -1).all()
+
+
+# ------------------------------------------------------------------------------ bucketed LRU
+
+def _lru_bruteforce(resident, ts, slot, n_sel, missing, n_missing, t, W):
+    resident, ts = resident.copy(), ts.copy()
+    hits = {int(s) for s in slot[:n_sel] if s >= 0}
+    for s in hits:
+        ts[s] = t
+    bucket = [63 if resident[s] < 0 else min(63, (int(t) - int(ts[s])) // W) for s in range(len(ts))]
+    order = []
+    for b in range(63, -1, -1):                 # oldest bucket first, slots ascending inside
+        order += [s for s in range(len(ts)) if bucket[s] == b and s not in hits]
+    victims = order[:n_missing]
+    for i, s in enumerate(victims):
+        resident[s] = missing[i]
+        ts[s] = t
+    hist = np.bincount(bucket, minlength=64)
+    return resident, ts, victims, hist
+
+
+@pytest.mark.parametrize("W", [1, 3])
+def test_lru_bruteforce_trajectory(W):
+    rng = np.random.default_rng(W)
+    n_slots, stride = 24, 7
+    resident = np.full(n_slots, -1, np.int32)
+    ts = np.full(n_slots, np.iinfo(np.int32).min, np.int32)
+    for t in range(60):
+        n_sel = int(rng.integers(1, stride + 1))
+        sel = np.full(stride, -1, np.int32)
+        sel[:n_sel] = np.sort(rng.choice(40, size=n_sel, replace=False))
+        missing, nm, slot = oracle.setdiff_unit(resident, sel, n_sel, stride)
+        r2, t2, vic, hist = oracle.lru_unit(resident, ts, slot, n_sel, missing, nm, t, W, stride)
+        br, bt, bv, bh = _lru_bruteforce(resident, ts, slot, n_sel, missing, nm, t, W)
+        assert np.array_equal(r2, br) and np.array_equal(t2, bt)
+        assert vic[:nm].tolist() == bv and (vic[nm:] == -1).all()
+        assert np.array_equal(hist, bh) and hist.sum() == n_slots
+        assert len(set(vic[:nm].tolist())) == nm
+        assert set(sel[:n_sel].tolist()) <= set(r2.tolist())
+        assert all(t2[s] == t for s in range(n_slots) if r2[s] in set(sel[:n_sel].tolist()))
+        resident, ts = r2, t2
+
+
+def test_lru_empty_slots_are_oldest():
+    resident = np.array([5, -1, 7, -1], np.int32)
+    ts = np.array([0, np.iinfo(np.int32).min, 1, np.iinfo(np.int32).min], np.int32)
+    r, t, vic, hist = oracle.lru_unit(resident, ts, [-1, -1], 2, [8, 9], 2, 2, 1, 2)
+    assert vic.tolist() == [1, 3] and r.tolist() == [5, 8, 7, 9] and hist[63] == 2
+    r, t, vic, hist = oracle.lru_unit(r, t, [-1, -1, -1], 3, [10, 11, 12], 3, 3, 1, 3)
+    # ages now: slot0 3, slot1 1, slot2 2, slot3 1 -> order 0, 2, 1
+    assert vic.tolist() == [0, 2, 1] and hist[3] == 1 and hist[2] == 1 and hist[1] == 2

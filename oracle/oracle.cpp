@@ -30,8 +30,8 @@
 //   R6 RoPE is the half-split ("rotate-half") form over pairs (x_i, x_{i+64}),
 //      theta_i = theta^(-2i/128); stored keys carry only their document-local rotation.
 //   R7 packed page word: phys[0:18) | (valid-1)[18:24) | doc slot[24:32).
-//   R8 LRU: bucket = min(63, (t - ts) / W); empty slots are bucket 63; hits are touched
-//      first; victims are untouched slots in (bucket desc, slot asc) order.
+//   R8 LRU: bucket = min(63, max(0, t - ts) / W); empty slots are bucket 63; hits are
+//      touched first; victims are untouched slots in (bucket desc, slot asc) order.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -350,7 +350,8 @@ void orc_setdiff_unit(const int32_t* resident, int n_slots, const int32_t* sel, 
 // [Spin] 2B "Bucketed LRU policy": resident pages are grouped into 64 recency buckets by
 // their timestamps and evicted a bucket at a time, oldest first (reading R8):
 //   1. every hit slot (slot[i] >= 0) is touched: ts = t
-//   2. bucket(s) = 63 for an empty slot, else min(63, (t - ts[s]) / W); hist counts all slots
+//   2. bucket(s) = 63 for an empty slot, else min(63, (t - ts[s]) / W), where a timestamp
+//      later than t counts as age 0; hist counts all slots
 //   3. victims: the n_missing untouched slots first in (bucket desc, slot asc) order
 //   4. missing[i] is installed in victims[i] with ts = t
 // victims has `stride` entries; unused entries are -1.
@@ -366,7 +367,7 @@ void orc_lru_unit(int32_t* resident, int32_t* ts, int n_slots, const int32_t* sl
     if (resident[s] < 0) {
       bucket[s] = 63;
     } else {
-      const int64_t age = static_cast<int64_t>(t) - ts[s];
+      const int64_t age = std::max<int64_t>(0, static_cast<int64_t>(t) - ts[s]);
       bucket[s] = static_cast<int>(std::min<int64_t>(63, age / W));
     }
     hist[bucket[s]] += 1;

@@ -1,0 +1,240 @@
+/*
+ * spkv.h -- C ABI of the GB300 (sm_103a) block-sparse paged-KV decode library.
+ *
+ * One decode step over a paged, head-major KV cache runs as
+ *
+ *   paged_kv_append      write the new token's K/V rows, refresh the pooled-key summaries
+ *   score_blocks         block scores from the pooled keys (two-stage pooling)
+ *   select_topk          per-KV-head top-k pages: eviction-head budget k_e + query budget k_q
+ *   resident_setdiff     selected pages that are not resident (swap-in list)
+ *   lru_bucket_update    64-bucket LRU recency update and victim choice
+ *   sparse_decode_attn   split-K flash decoding over the selected pages
+ *   lazy_rope_decode_attn  the same with deferred RoPE (query rotated once per document)
+ *
+ * Sources (web pages, cited by title and section):
+ *   [NOSA] "NOSA: Native and Offloadable Sparse Attention", sections "Method 1: the NOSA
+ *          algorithm" and "Method 2: the NOSI system".
+ *   [Spin] "Unifying Sparse Attention with Hierarchical Memory for Scalable Long-Context LLM
+ *          Serving", section 2A "Unified partition abstraction" and 2B "Dynamic,
+ *          locality-aware KV management".
+ *   [Lazy] "LazyAttention", sections "Core idea: deferred positional encoding",
+ *          "Technical implementation 2. Decoding" and "Mathematical equivalence".
+ *   [FA]   "How KV sparsity achieves 1.5x acceleration for vLLM" (Novita AI), section
+ *          "2. Attention modification".
+ *
+ * Conventions for every entry point
+ *   - Pointers named "device" are CUDA device memory owned by the caller (for example
+ *     allocated by PyTorch); the library never frees them.  Host pointers are marked "host".
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream) and
+ *     never synchronise, except spkv_get_device_error.
+ *   - Argument errors are detected on the host before any launch and return SPKV_EINVAL.
+ *     A failed launch returns SPKV_ECUDA.  No C++ exception crosses this boundary.
+ *   - Malformed *device* data (a page id, physical page or slot out of range) never faults:
+ *     the kernel skips the entry and sets a bit in the handle's device error word, which
+ *     spkv_get_device_error reports (bits SPKV_DEVERR_*).
+ *   - Fixed shapes: head_dim 128, page 64 tokens, pooling sub-block 16 tokens, group size
+ *     G = Hq / Hk with 1 <= G <= 16.  Other values return SPKV_EUNSUPPORTED.
+ *   - bf16 is IEEE bfloat16; accumulation is fp32.
+ *   - A handle serves one stream at a time; calls on one handle must not overlap on the GPU.
+ *   - "unit" = one (request b, kv head h) pair, u = b * Hk + h.
+ */
+#ifndef SPKV_H_
+#define SPKV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum spkv_status {
+  SPKV_OK = 0,
+  SPKV_EINVAL = -1,        /* bad argument, detected on the host, nothing launched */
+  SPKV_ENOMEM = -2,        /* device or host allocation failed (create only) */
+  SPKV_ECUDA = -3,         /* a CUDA call or kernel launch failed */
+  SPKV_EDEVICE = -4,       /* the device error word was non-zero (spkv_get_device_error) */
+  SPKV_ETIMEOUT = -5,      /* a bounded wait inside a kernel gave up (never in a correct run) */
+  SPKV_EUNSUPPORTED = -6   /* shape outside the fixed sizes listed above */
+};
+
+/* Bits of the device error word. */
+#define SPKV_DEVERR_PAGE_ID 1u      /* logical page id outside [0, np_max) or past seq_len */
+#define SPKV_DEVERR_PHYS 2u         /* physical page id outside [0, n_phys_pages) */
+#define SPKV_DEVERR_SLOT 4u         /* resident slot / doc slot outside its table */
+#define SPKV_DEVERR_ORDER 8u        /* selected list not strictly ascending, or duplicate resident id */
+#define SPKV_DEVERR_CAPACITY 16u    /* more missing pages than evictable slots */
+#define SPKV_DEVERR_TIMEOUT 32u     /* a bounded intra-CTA wait gave up (reported as SPKV_ETIMEOUT) */
+
+typedef struct spkv_cache* spkv_cache_t; /* opaque, library-owned */
+
+/* Description of a paged KV cache.  All buffers are caller-owned device memory.
+ *   k_pool, v_pool : bf16 [n_kv_heads][n_phys_pages][64][128]; one page of one head is
+ *                    16 KiB contiguous ([Spin] 2B "per-head physical pages").  16-byte aligned.
+ *   ksum           : fp32 [n_kv_heads][n_phys_pages][4][128]; per page and sub-block, the sum
+ *                    of the valid keys (the library writes it; mean = ksum / count).
+ *   page_cnt       : int32 [n_phys_pages]; valid tokens held by each physical page.  Read by
+ *                    paged_kv_create, updated by paged_kv_append.
+ *   max_units      : the largest B * n_kv_heads any call on this handle will use (sizes the
+ *                    split-K workspace); 0 means 4096.
+ */
+typedef struct {
+  int32_t n_kv_heads;
+  int32_t head_dim;     /* must be 128 */
+  int32_t page_tokens;  /* must be 64 */
+  int32_t subblock;     /* must be 16 */
+  int64_t n_phys_pages;
+  void* k_pool;
+  void* v_pool;
+  float* ksum;
+  int32_t* page_cnt;
+  int32_t max_units;
+} spkv_desc;
+
+/* Creates a handle for the pool described by *desc (the struct is copied; the buffers are
+ * not) and builds the pooled-key summaries of every physical page from page_cnt:
+ *   ksum[h][p][j][:] = sum of K[h][p][t][:] over t in [16j, min(16j+16, page_cnt[p])).
+ * [NOSA] "Method 1", block-wise implementation (first pooling stage: sub-block means);
+ * [NOSA] "Method 2: NOSI", kernel fusion (pooling is produced when K is written, not per step).
+ * Allocates the handle, a split-K workspace and the device error word (SPKV_ENOMEM on
+ * failure).  *out receives the handle.  The summary build is enqueued on `stream`. */
+int paged_kv_create(const spkv_desc* desc, void* stream, spkv_cache_t* out);
+
+/* Appends n_rows tokens.  Row i writes K and V of all heads at token slot tok_in_page[i]
+ * of physical page phys_page[i]:
+ *   k_new, v_new : device bf16 [n_rows][n_kv_heads][128]
+ *   phys_page, tok_in_page : device int32 [n_rows]
+ * then sets page_cnt[p] = max(page_cnt[p], tok + 1) and recomputes the touched sub-block
+ * sums from the pool in a fixed order (bitwise the same as paged_kv_create).  Rows of one
+ * call must name distinct (page, token) slots; pages are filled in token order.
+ * Out-of-range ids are skipped (SPKV_DEVERR_PHYS / SPKV_DEVERR_PAGE_ID).
+ * [NOSA] "Method 2: NOSI", kernel fusion; [NOSA] "Method 1", block-wise implementation. */
+int paged_kv_append(spkv_cache_t cache, const int32_t* phys_page, const int32_t* tok_in_page,
+                    const void* k_new, const void* v_new, int n_rows, void* stream);
+
+/* Block scores, [NOSA] "Method 1", block-wise implementation (two-stage pooling: mean over
+ * each 16-token sub-block, max over the 4 sub-blocks of the page) and dual selection
+ * (query-aware part).  For unit (b, h) and every complete page p before the local page
+ * l_b = (seq_len[b] - 1) / 64:
+ *   scores[b][h][p] = max_j (sum_g q[b][h*G+g]) . ksum[h][page_table[b][p]][j] / (16 sqrt(128))
+ * i.e. the sub-block scores of the G query heads of the group are summed before the max.
+ * Entries p >= l_b are -inf.
+ *   q          : device bf16 [B][Hq][128]
+ *   page_table : device int32 [B][np_max], physical page of each logical page
+ *   seq_len    : device int32 [B], tokens in each request's context (>= 1)
+ *   scores     : device fp32 [B][n_kv_heads][np_max] (output) */
+int score_blocks(spkv_cache_t cache, const void* q, int B, int Hq, const int32_t* page_table,
+                 int np_max, const int32_t* seq_len, float* scores, void* stream);
+
+/* Dual top-k page selection, [NOSA] "Method 1": dual selection (Gamma_q query-aware,
+ * Gamma_e query-agnostic eviction head), locality guarantee, ED-DMA (pages are ranked on the
+ * pre-exp eviction scores; exp is never applied).  Per unit, with candidates C = complete
+ * pages 0 .. l_b - 1 (the local page l_b is always attended, outside the budget):
+ *   E = top-k_e of {p in C : alive bit set} by evict_scores;
+ *   every alive candidate outside E has its alive bit cleared (it can never enter E again);
+ *   Q = top-k_q of C \ E by q_scores (evicted pages may enter Q);
+ *   sel = ascending(E u Q), then l_b;  n_sel = |E u Q| + 1;  unused entries = -1.
+ * Ranking is a total order: score descending, then page id ascending (-0.0 equals +0.0).
+ *   q_scores, evict_scores : device fp32 [B][n_kv_heads][np_max]; must not be NaN
+ *   alive      : device uint32 [B][n_kv_heads][ceil(np_max/32)] bitmask, bit p%32 of word
+ *                p/32 (in/out); bits of non-candidate pages are left as they are, so a page
+ *                becomes a candidate alive when it completes
+ *   sel        : device int32 [B][n_kv_heads][k_e + k_q + 1] (output)
+ *   n_sel      : device int32 [B][n_kv_heads] (output)
+ * np_max <= 32768. */
+int select_topk(spkv_cache_t cache, const float* q_scores, const float* evict_scores,
+                uint32_t* alive, int B, int np_max, const int32_t* seq_len, int k_q, int k_e,
+                int32_t* sel, int32_t* n_sel, void* stream);
+
+/* Sparse decode attention over the selected pages (split-K flash decoding), [FA] "2.
+ * Attention modification" (one-pass online softmax with rowmax / l, which are also
+ * returned).  For query head g of unit (b, h):
+ *   out[b][h*G+g][:] = sum_t softmax_t(q . k_t / sqrt(128)) v_t
+ *   lse[b][h*G+g]    = log sum_t exp(q . k_t / sqrt(128))          (natural log)
+ * over the tokens of pages sel[u][0 .. n_sel[u]); page p holds min(64, seq_len[b] - 64 p)
+ * valid tokens (rows past that are never read into the result, even if they hold NaN).
+ *   q          : device bf16 [B][Hq][128]
+ *   page_table : device int32 [B][np_max]
+ *   sel, n_sel : device int32 [B][n_kv_heads][sel_stride], [B][n_kv_heads]
+ *   seq_len    : device int32 [B]
+ *   out        : device fp32 [B][Hq][128];  lse: device fp32 [B][Hq]
+ * A unit with no pages gets out = 0 and lse = -inf. */
+int sparse_decode_attn(spkv_cache_t cache, const void* q, int B, int Hq, const int32_t* page_table,
+                       int np_max, const int32_t* sel, const int32_t* n_sel, int sel_stride,
+                       const int32_t* seq_len, float* out, float* lse, void* stream);
+
+/* Decode attention with deferred RoPE, [Lazy] "Core idea" (keys are stored without their
+ * placement position), "Technical implementation 2. Decoding" (the query is rotated only when
+ * the relative offset changes, i.e. once per document; block id and offset bit-packed in one
+ * word) and "Mathematical equivalence" (scores depend only on n - m).
+ * Each page word (see spkv_pack_page_words) gives a physical page, its valid token count and
+ * a document slot i; with P_i = doc_pos[b][i] and n = qpos[b] the page's keys are scored with
+ * R(n - P_i) q, where R is the half-split RoPE rotation over pairs (x_j, x_{j+64}) with
+ * frequencies theta^(-2j/128).  Stored keys carry only their document-local rotation.
+ *   q        : device bf16 [B][Hq][128], not rotated
+ *   qpos     : device int32 [B]
+ *   meta     : device uint32 [B][meta_heads][np_max]; meta_heads is 1 (one page list shared
+ *              by all kv heads) or n_kv_heads
+ *   n_pages  : device int32 [B], pages of each request's list
+ *   doc_pos  : device int32 [B][max_docs]
+ *   out, lse : as sparse_decode_attn. */
+int lazy_rope_decode_attn(spkv_cache_t cache, const void* q, int B, int Hq, const int32_t* qpos,
+                          const uint32_t* meta, int meta_heads, const int32_t* n_pages, int np_max,
+                          const int32_t* doc_pos, int max_docs, float theta, float* out,
+                          float* lse, void* stream);
+
+/* Set-difference of selected vs GPU-resident pages, [NOSA] "Method 2: NOSI", optimised
+ * memory layout (custom kernel computing set differences for block swapping).  Per unit:
+ *   missing = sel[0..n_sel) \ resident (ascending), n_missing = its size;
+ *   slot[i] = index s with resident[s] == sel[i], or -1.  Entries past the results are -1.
+ *   resident : device int32 [n_units][n_slots], -1 = empty, no duplicate ids
+ *   sel      : device int32 [n_units][sel_stride], strictly ascending in [0, n_sel)
+ *   missing, slot : device int32 [n_units][sel_stride];  n_missing: device int32 [n_units]
+ * n_slots <= 16384, sel_stride <= 4096. */
+int resident_setdiff(spkv_cache_t cache, const int32_t* resident, int n_slots, const int32_t* sel,
+                     const int32_t* n_sel, int sel_stride, int n_units, int32_t* missing,
+                     int32_t* n_missing, int32_t* slot, void* stream);
+
+/* Bucketed LRU update, [Spin] 2B "bucketed LRU policy" (pages grouped into 64 recency
+ * buckets by timestamp; eviction without a global sort).  Per unit, at time t_now:
+ *   1. ts[s] = t_now for every hit slot s = slot[i] >= 0;
+ *   2. bucket(s) = 63 if resident[s] < 0, else min(63, max(0, t_now - ts[s]) / bucket_width);
+ *      hist[u][b] = number of slots in bucket b (all slots, after step 1);
+ *   3. victims[0 .. n_missing) = untouched slots in order (bucket desc, slot asc);
+ *   4. resident[victims[i]] = missing[i], ts[victims[i]] = t_now.
+ *   resident, ts : device int32 [n_units][n_slots] (in/out); an empty slot's ts is ignored
+ *   slot, missing: device int32 [n_units][sel_stride]; n_sel, n_missing: device int32 [n_units]
+ *   victims      : device int32 [n_units][sel_stride] (output, -1 past n_missing)
+ *   hist         : device int32 [n_units][64] (output)
+ * bucket_width >= 1, n_slots <= 16384. */
+int lru_bucket_update(spkv_cache_t cache, int32_t* resident, int32_t* ts, int n_slots,
+                      const int32_t* slot, const int32_t* n_sel, const int32_t* missing,
+                      const int32_t* n_missing, int sel_stride, int n_units, int32_t t_now,
+                      int bucket_width, int32_t* victims, int32_t* hist, void* stream);
+
+/* Packs page words for lazy_rope_decode_attn on the host ([Lazy] "Technical implementation
+ * 2. Decoding", bit-packed block id and offset):
+ *   word = phys | (valid - 1) << 18 | doc_slot << 24,
+ * with phys < 2^18, 1 <= valid <= 64, doc_slot < 256.  Host arrays of length n.
+ * Returns SPKV_EINVAL (and stops) at the first field out of range. */
+int spkv_pack_page_words(const int32_t* phys, const int32_t* valid, const int32_t* doc_slot,
+                         int64_t n, uint32_t* words);
+
+/* Waits for `stream`, then reads and clears the handle's device error word into *bits.
+ * Returns SPKV_OK when it was zero, SPKV_EDEVICE otherwise (SPKV_ECUDA if the wait failed). */
+int spkv_get_device_error(spkv_cache_t cache, void* stream, uint32_t* bits);
+
+/* Frees the handle and what it allocated (not the caller's buffers).  The caller must make
+ * sure no call on the handle is still running. */
+int paged_kv_destroy(spkv_cache_t cache);
+
+/* Number of SMs the handle's kernels size their grids for (the device's SM count). */
+int spkv_sm_count(spkv_cache_t cache);
+
+/* A static string naming a status code. */
+const char* spkv_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPKV_H_ */

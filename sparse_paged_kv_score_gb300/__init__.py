@@ -1,0 +1,206 @@
+"""Block-sparse decode attention over a paged, head-major KV cache, for NVIDIA GB300 (sm_103a).
+
+A thin Python binding over the C ABI of ``libspkv.so`` (``include/spkv.h``).  Each function
+has the name of the C entry point it calls and only marshals arguments: it checks dtypes,
+devices and shapes of the torch tensors, then passes raw pointers, sizes and the current CUDA
+stream.  Every step of the decode path runs in the library's own CUDA kernels; nothing here
+computes.  Outputs are caller-allocated tensors, filled in place.
+
+    cache = paged_kv_create(k_pool, v_pool, ksum, page_cnt)
+    score_blocks(cache, q, page_table, seq_len, scores)
+    select_topk(cache, scores, evict, alive, seq_len, k_q, k_e, sel, n_sel)
+    resident_setdiff(cache, resident, sel, n_sel, missing, n_missing, slot)
+    lru_bucket_update(cache, resident, ts, slot, n_sel, missing, n_missing, t, 1, victims, hist)
+    sparse_decode_attn(cache, q, page_table, sel, n_sel, seq_len, out, lse)
+    lazy_rope_decode_attn(cache, q, qpos, meta, n_pages, doc_pos, theta, out, lse)
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from ._abi import DEVERR, SpkvDesc, SpkvError, check, load
+
+__all__ = ["PagedKVCache", "paged_kv_create", "paged_kv_append", "score_blocks", "select_topk",
+           "sparse_decode_attn", "lazy_rope_decode_attn", "resident_setdiff", "lru_bucket_update",
+           "pack_page_words", "get_device_error", "SpkvError", "DEVERR", "load"]
+
+HEAD_DIM, PAGE, SUBBLOCK = 128, 64, 16
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _t(x: torch.Tensor, dtype, name: str, shape=None) -> int:
+    if not isinstance(x, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if x.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {x.dtype}")
+    if not x.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not x.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if shape is not None and tuple(x.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(x.shape)}")
+    return x.data_ptr()
+
+
+class PagedKVCache:
+    """Owns one library handle (``spkv_cache_t``) for a caller-owned pool."""
+
+    def __init__(self, k_pool, v_pool, ksum, page_cnt, max_units: int = 0, stream=None):
+        Hk, n_phys = k_pool.shape[0], k_pool.shape[1]
+        shp = (Hk, n_phys, PAGE, HEAD_DIM)
+        self.desc = SpkvDesc(Hk, HEAD_DIM, PAGE, SUBBLOCK, n_phys,
+                             _t(k_pool, torch.bfloat16, "k_pool", shp),
+                             _t(v_pool, torch.bfloat16, "v_pool", shp),
+                             _t(ksum, torch.float32, "ksum", (Hk, n_phys, 4, HEAD_DIM)),
+                             _t(page_cnt, torch.int32, "page_cnt", (n_phys,)), int(max_units))
+        self.n_kv_heads, self.n_phys = Hk, n_phys
+        self.tensors = (k_pool, v_pool, ksum, page_cnt)   # keep the buffers alive
+        h = ctypes.c_void_p()
+        check("paged_kv_create", load().paged_kv_create(ctypes.byref(self.desc), _stream(stream),
+                                                        ctypes.byref(h)))
+        self.handle = h
+
+    @property
+    def sm_count(self) -> int:
+        return load().spkv_sm_count(self.handle)
+
+    def close(self):
+        if self.handle:
+            torch.cuda.synchronize()
+            check("paged_kv_destroy", load().paged_kv_destroy(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            if self.handle:
+                load().paged_kv_destroy(self.handle)
+                self.handle = None
+        except Exception:
+            pass
+
+
+def paged_kv_create(k_pool, v_pool, ksum, page_cnt, max_units: int = 0, stream=None) -> PagedKVCache:
+    return PagedKVCache(k_pool, v_pool, ksum, page_cnt, max_units, stream)
+
+
+def paged_kv_append(cache: PagedKVCache, phys_page, tok_in_page, k_new, v_new, stream=None):
+    n = phys_page.shape[0]
+    shp = (n, cache.n_kv_heads, HEAD_DIM)
+    check("paged_kv_append", load().paged_kv_append(
+        cache.handle, _t(phys_page, torch.int32, "phys_page", (n,)),
+        _t(tok_in_page, torch.int32, "tok_in_page", (n,)), _t(k_new, torch.bfloat16, "k_new", shp),
+        _t(v_new, torch.bfloat16, "v_new", shp), n, _stream(stream)))
+
+
+def score_blocks(cache: PagedKVCache, q, page_table, seq_len, scores, stream=None):
+    B, Hq = q.shape[0], q.shape[1]
+    np_max = page_table.shape[1]
+    check("score_blocks", load().score_blocks(
+        cache.handle, _t(q, torch.bfloat16, "q", (B, Hq, HEAD_DIM)), B, Hq,
+        _t(page_table, torch.int32, "page_table", (B, np_max)), np_max,
+        _t(seq_len, torch.int32, "seq_len", (B,)),
+        _t(scores, torch.float32, "scores", (B, cache.n_kv_heads, np_max)), _stream(stream)))
+
+
+def select_topk(cache: PagedKVCache, q_scores, evict_scores, alive, seq_len, k_q: int, k_e: int, sel,
+                n_sel, stream=None):
+    B, Hk, np_max = q_scores.shape
+    stride = k_q + k_e + 1
+    check("select_topk", load().select_topk(
+        cache.handle, _t(q_scores, torch.float32, "q_scores", (B, Hk, np_max)),
+        _t(evict_scores, torch.float32, "evict_scores", (B, Hk, np_max)),
+        _t(alive, torch.int32, "alive", (B, Hk, (np_max + 31) // 32)), B, np_max,
+        _t(seq_len, torch.int32, "seq_len", (B,)), int(k_q), int(k_e),
+        _t(sel, torch.int32, "sel", (B, Hk, stride)), _t(n_sel, torch.int32, "n_sel", (B, Hk)),
+        _stream(stream)))
+
+
+def sparse_decode_attn(cache: PagedKVCache, q, page_table, sel, n_sel, seq_len, out, lse, stream=None):
+    B, Hq = q.shape[0], q.shape[1]
+    np_max = page_table.shape[1]
+    stride = sel.shape[2]
+    check("sparse_decode_attn", load().sparse_decode_attn(
+        cache.handle, _t(q, torch.bfloat16, "q", (B, Hq, HEAD_DIM)), B, Hq,
+        _t(page_table, torch.int32, "page_table", (B, np_max)), np_max,
+        _t(sel, torch.int32, "sel", (B, cache.n_kv_heads, stride)),
+        _t(n_sel, torch.int32, "n_sel", (B, cache.n_kv_heads)), stride,
+        _t(seq_len, torch.int32, "seq_len", (B,)), _t(out, torch.float32, "out", (B, Hq, HEAD_DIM)),
+        _t(lse, torch.float32, "lse", (B, Hq)), _stream(stream)))
+
+
+def lazy_rope_decode_attn(cache: PagedKVCache, q, qpos, meta, n_pages, doc_pos, theta: float, out, lse,
+                          stream=None):
+    """meta: int32 tensor holding the uint32 page words, [B][meta_heads][np_max] or [B][np_max]."""
+    B, Hq = q.shape[0], q.shape[1]
+    if meta.dim() == 2:
+        meta = meta.unsqueeze(1)
+    meta_heads, np_max = meta.shape[1], meta.shape[2]
+    max_docs = doc_pos.shape[1]
+    check("lazy_rope_decode_attn", load().lazy_rope_decode_attn(
+        cache.handle, _t(q, torch.bfloat16, "q", (B, Hq, HEAD_DIM)), B, Hq,
+        _t(qpos, torch.int32, "qpos", (B,)), _t(meta, torch.int32, "meta", (B, meta_heads, np_max)),
+        meta_heads, _t(n_pages, torch.int32, "n_pages", (B,)), np_max,
+        _t(doc_pos, torch.int32, "doc_pos", (B, max_docs)), max_docs, float(theta),
+        _t(out, torch.float32, "out", (B, Hq, HEAD_DIM)), _t(lse, torch.float32, "lse", (B, Hq)),
+        _stream(stream)))
+
+
+def resident_setdiff(cache: PagedKVCache, resident, sel, n_sel, missing, n_missing, slot, stream=None):
+    n_units, n_slots = resident.shape
+    stride = sel.shape[-1]
+    for name, x, want in (("sel", sel, n_units * stride), ("n_sel", n_sel, n_units),
+                          ("missing", missing, n_units * stride), ("n_missing", n_missing, n_units),
+                          ("slot", slot, n_units * stride)):
+        if x.numel() != want:
+            raise ValueError(f"{name}: expected {want} elements")
+    check("resident_setdiff", load().resident_setdiff(
+        cache.handle, _t(resident, torch.int32, "resident"), n_slots,
+        _t(sel, torch.int32, "sel"), _t(n_sel, torch.int32, "n_sel"), stride, n_units,
+        _t(missing, torch.int32, "missing"), _t(n_missing, torch.int32, "n_missing"),
+        _t(slot, torch.int32, "slot"), _stream(stream)))
+
+
+def lru_bucket_update(cache: PagedKVCache, resident, ts, slot, n_sel, missing, n_missing, t_now: int,
+                      bucket_width: int, victims, hist, stream=None):
+    n_units, n_slots = resident.shape
+    stride = slot.shape[-1]
+    for name, x, want in (("ts", ts, n_units * n_slots), ("slot", slot, n_units * stride),
+                          ("n_sel", n_sel, n_units), ("missing", missing, n_units * stride),
+                          ("n_missing", n_missing, n_units), ("victims", victims, n_units * stride),
+                          ("hist", hist, n_units * 64)):
+        if x.numel() != want:
+            raise ValueError(f"{name}: expected {want} elements")
+    check("lru_bucket_update", load().lru_bucket_update(
+        cache.handle, _t(resident, torch.int32, "resident"), _t(ts, torch.int32, "ts"), n_slots,
+        _t(slot, torch.int32, "slot"), _t(n_sel, torch.int32, "n_sel"),
+        _t(missing, torch.int32, "missing"), _t(n_missing, torch.int32, "n_missing"), stride, n_units,
+        int(t_now), int(bucket_width), _t(victims, torch.int32, "victims"),
+        _t(hist, torch.int32, "hist"), _stream(stream)))
+
+
+def pack_page_words(phys, valid, doc_slot) -> np.ndarray:
+    """Host helper: packs page words (uint32) for lazy_rope_decode_attn via the C ABI."""
+    phys = np.ascontiguousarray(phys, np.int32)
+    valid = np.ascontiguousarray(valid, np.int32)
+    doc_slot = np.ascontiguousarray(doc_slot, np.int32)
+    if not (phys.shape == valid.shape == doc_slot.shape):
+        raise ValueError("phys, valid and doc_slot must have the same shape")
+    out = np.empty(phys.shape, np.uint32)
+    check("spkv_pack_page_words", load().spkv_pack_page_words(
+        phys.ctypes.data, valid.ctypes.data, doc_slot.ctypes.data, phys.size, out.ctypes.data))
+    return out
+
+
+def get_device_error(cache: PagedKVCache, stream=None):
+    """Waits for the stream; returns (status, bits) of the device error word and clears it."""
+    bits = ctypes.c_uint32(0)
+    st = load().spkv_get_device_error(cache.handle, _stream(stream), ctypes.byref(bits))
+    return st, int(bits.value)

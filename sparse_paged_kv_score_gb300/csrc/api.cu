@@ -1,0 +1,281 @@
+// Host side of the C ABI declared in include/spkv.h: argument checks, the handle, tensor-map
+// encoding and kernel launches.  No entry point synchronises except spkv_get_device_error.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "internal.h"
+
+using spkv::AttnParams;
+
+namespace {
+
+constexpr int kMaxGroup = 16;
+constexpr int kMaxUnitsDefault = 4096;
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? SPKV_OK : SPKV_ECUDA; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// Pool [n_page_heads][64 tok][128 d] bf16 as a 3-D tensor (d, tok, page-head); box 64 x 64 x 1
+// with 128-byte swizzle (a 128-byte row of the box is one token's 64 dims).
+bool encode_pool(CUtensorMap* m, void* base, int64_t n_page_heads) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {128, 64, static_cast<cuuint64_t>(n_page_heads)};
+  cuuint64_t strides[2] = {256, 16384};
+  cuuint32_t box[3] = {64, 64, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int check_group(spkv_cache_t c, int B, int Hq) {
+  if (!c || B < 0 || Hq <= 0) return SPKV_EINVAL;
+  const int Hk = c->d.n_kv_heads;
+  if (Hq % Hk != 0) return SPKV_EINVAL;
+  const int G = Hq / Hk;
+  if (G < 1 || G > kMaxGroup) return SPKV_EUNSUPPORTED;
+  if (int64_t(B) * Hk > c->max_units) return SPKV_EINVAL;
+  return SPKV_OK;
+}
+
+void fill_common(AttnParams& p, spkv_cache_t c, const void* q, int B, int Hq, float* out, float* lse) {
+  std::memset(&p, 0, sizeof(p));
+  p.q = q;
+  p.out = out;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hk = c->d.n_kv_heads;
+  p.G = Hq / p.Hk;
+  p.n_phys = c->d.n_phys_pages;
+  p.err = c->dev_err;
+  p.ws_m = c->ws_m;
+  p.ws_l = c->ws_l;
+  p.ws_o = c->ws_o;
+  p.ws_cnt = c->ws_cnt;
+  p.scale_log2 = static_cast<float>(1.4426950408889634074 / std::sqrt(128.0));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* spkv_status_string(int s) {
+  switch (s) {
+    case SPKV_OK: return "SPKV_OK";
+    case SPKV_EINVAL: return "SPKV_EINVAL: invalid argument";
+    case SPKV_ENOMEM: return "SPKV_ENOMEM: allocation failed";
+    case SPKV_ECUDA: return "SPKV_ECUDA: CUDA call or launch failed";
+    case SPKV_EDEVICE: return "SPKV_EDEVICE: device data out of range (see error bits)";
+    case SPKV_ETIMEOUT: return "SPKV_ETIMEOUT: a bounded device wait gave up";
+    case SPKV_EUNSUPPORTED: return "SPKV_EUNSUPPORTED: shape outside the supported sizes";
+    default: return "unknown status";
+  }
+}
+
+int paged_kv_create(const spkv_desc* desc, void* stream, spkv_cache_t* out) {
+  if (!desc || !out) return SPKV_EINVAL;
+  *out = nullptr;
+  const spkv_desc& d = *desc;
+  if (d.head_dim != 128 || d.page_tokens != 64 || d.subblock != 16) return SPKV_EUNSUPPORTED;
+  if (d.n_kv_heads <= 0 || d.n_phys_pages <= 0 || d.max_units < 0) return SPKV_EINVAL;
+  if (!d.k_pool || !d.v_pool || !d.ksum || !d.page_cnt) return SPKV_EINVAL;
+  if (!aligned(d.k_pool, 16) || !aligned(d.v_pool, 16) || !aligned(d.ksum, 16)) return SPKV_EINVAL;
+  const int64_t n_ph = int64_t(d.n_kv_heads) * d.n_phys_pages;
+  if (n_ph >= (int64_t(1) << 31)) return SPKV_EUNSUPPORTED;
+
+  spkv_cache* c = new (std::nothrow) spkv_cache();
+  if (!c) return SPKV_ENOMEM;
+  c->d = d;
+  c->max_units = d.max_units > 0 ? d.max_units : kMaxUnitsDefault;
+  if (cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+    delete c;
+    return SPKV_ECUDA;
+  }
+  c->attn_grid = c->sm_count;
+  if (!encode_pool(&c->tmap_k, d.k_pool, n_ph) || !encode_pool(&c->tmap_v, d.v_pool, n_ph)) {
+    delete c;
+    return SPKV_ECUDA;
+  }
+  c->ws_slots = int64_t(c->attn_grid) + c->max_units;
+  bool ok = cudaMalloc(&c->dev_err, sizeof(uint32_t)) == cudaSuccess &&
+            cudaMalloc(&c->ws_m, sizeof(float) * 16 * c->ws_slots) == cudaSuccess &&
+            cudaMalloc(&c->ws_l, sizeof(float) * 16 * c->ws_slots) == cudaSuccess &&
+            cudaMalloc(&c->ws_o, sizeof(float) * 16 * 128 * c->ws_slots) == cudaSuccess &&
+            cudaMalloc(&c->ws_cnt, sizeof(int32_t) * c->max_units) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    paged_kv_destroy(c);
+    return SPKV_ENOMEM;
+  }
+  cudaStream_t st = as_stream(stream);
+  if (cudaMemsetAsync(c->dev_err, 0, sizeof(uint32_t), st) != cudaSuccess ||
+      cudaMemsetAsync(c->ws_cnt, 0, sizeof(int32_t) * c->max_units, st) != cudaSuccess ||
+      spkv::launch_summary_build(c, st) != cudaSuccess) {
+    paged_kv_destroy(c);
+    return SPKV_ECUDA;
+  }
+  *out = c;
+  return SPKV_OK;
+}
+
+int paged_kv_destroy(spkv_cache_t c) {
+  if (!c) return SPKV_EINVAL;
+  cudaFree(c->dev_err);
+  cudaFree(c->ws_m);
+  cudaFree(c->ws_l);
+  cudaFree(c->ws_o);
+  cudaFree(c->ws_cnt);
+  delete c;
+  return SPKV_OK;
+}
+
+int spkv_sm_count(spkv_cache_t c) { return c ? c->sm_count : SPKV_EINVAL; }
+
+int paged_kv_append(spkv_cache_t c, const int32_t* phys_page, const int32_t* tok_in_page, const void* k_new,
+                    const void* v_new, int n_rows, void* stream) {
+  if (!c || n_rows < 0) return SPKV_EINVAL;
+  if (n_rows == 0) return SPKV_OK;
+  if (!phys_page || !tok_in_page || !k_new || !v_new || !aligned(k_new, 4) || !aligned(v_new, 4)) return SPKV_EINVAL;
+  return status_of(spkv::launch_append(c, phys_page, tok_in_page, k_new, v_new, n_rows, as_stream(stream)));
+}
+
+int score_blocks(spkv_cache_t c, const void* q, int B, int Hq, const int32_t* page_table, int np_max,
+                 const int32_t* seq_len, float* scores, void* stream) {
+  int st = check_group(c, B, Hq);
+  if (st != SPKV_OK) return st;
+  if (B == 0) return SPKV_OK;
+  if (!q || !page_table || !seq_len || !scores || np_max <= 0 || !aligned(q, 4)) return SPKV_EINVAL;
+  return status_of(spkv::launch_score(c, q, B, Hq, page_table, np_max, seq_len, scores, as_stream(stream)));
+}
+
+int select_topk(spkv_cache_t c, const float* q_scores, const float* evict_scores, uint32_t* alive, int B, int np_max,
+                const int32_t* seq_len, int k_q, int k_e, int32_t* sel, int32_t* n_sel, void* stream) {
+  if (!c || B < 0) return SPKV_EINVAL;
+  if (int64_t(B) * c->d.n_kv_heads > 65535) return SPKV_EINVAL;
+  if (B == 0) return SPKV_OK;
+  if (!q_scores || !evict_scores || !alive || !seq_len || !sel || !n_sel) return SPKV_EINVAL;
+  if (np_max <= 0 || np_max > 32768 || k_q < 0 || k_e < 0 || k_q + k_e + 1 > 4096) return SPKV_EINVAL;
+  return status_of(spkv::launch_select(c, q_scores, evict_scores, alive, B, np_max, seq_len, k_q, k_e, sel, n_sel,
+                                       as_stream(stream)));
+}
+
+int sparse_decode_attn(spkv_cache_t c, const void* q, int B, int Hq, const int32_t* page_table, int np_max,
+                       const int32_t* sel, const int32_t* n_sel, int sel_stride, const int32_t* seq_len, float* out,
+                       float* lse, void* stream) {
+  int st = check_group(c, B, Hq);
+  if (st != SPKV_OK) return st;
+  if (B == 0) return SPKV_OK;
+  if (!q || !page_table || !sel || !n_sel || !seq_len || !out || !lse || np_max <= 0 || sel_stride <= 0 ||
+      !aligned(q, 4))
+    return SPKV_EINVAL;
+  AttnParams p;
+  fill_common(p, c, q, B, Hq, out, lse);
+  p.page_table = page_table;
+  p.np_max = np_max;
+  p.sel = sel;
+  p.n_sel = n_sel;
+  p.sel_stride = sel_stride;
+  p.seq_len = seq_len;
+  const int64_t t_max = int64_t(B) * c->d.n_kv_heads * sel_stride;
+  const int grid = static_cast<int>(t_max < c->attn_grid ? t_max : c->attn_grid);
+  return status_of(spkv::launch_attn(c, p, false, grid, as_stream(stream)));
+}
+
+int lazy_rope_decode_attn(spkv_cache_t c, const void* q, int B, int Hq, const int32_t* qpos, const uint32_t* meta,
+                          int meta_heads, const int32_t* n_pages, int np_max, const int32_t* doc_pos, int max_docs,
+                          float theta, float* out, float* lse, void* stream) {
+  int st = check_group(c, B, Hq);
+  if (st != SPKV_OK) return st;
+  if (B == 0) return SPKV_OK;
+  if (!q || !qpos || !meta || !n_pages || !doc_pos || !out || !lse || np_max <= 0 || max_docs <= 0 ||
+      !aligned(q, 4))
+    return SPKV_EINVAL;
+  if (meta_heads != 1 && meta_heads != c->d.n_kv_heads) return SPKV_EINVAL;
+  if (!(theta > 1.0f) || !std::isfinite(theta)) return SPKV_EINVAL;
+  AttnParams p;
+  fill_common(p, c, q, B, Hq, out, lse);
+  p.np_max = np_max;
+  p.qpos = qpos;
+  p.meta = meta;
+  p.meta_heads = meta_heads;
+  p.n_pages = n_pages;
+  p.doc_pos = doc_pos;
+  p.max_docs = max_docs;
+  // turns per position of pair j: theta^(-2j/128) / (2 pi), as a 2^-64 fixed-point fraction
+  for (int j = 0; j < 64; ++j) {
+    const double f = std::pow(static_cast<double>(theta), -2.0 * j / 128.0) / (2.0 * 3.14159265358979323846);
+    p.phase_inc[j] = static_cast<uint64_t>(std::ldexp(f, 64));
+  }
+  const int64_t t_max = int64_t(B) * c->d.n_kv_heads * np_max;
+  const int grid = static_cast<int>(t_max < c->attn_grid ? t_max : c->attn_grid);
+  return status_of(spkv::launch_attn(c, p, true, grid, as_stream(stream)));
+}
+
+int resident_setdiff(spkv_cache_t c, const int32_t* resident, int n_slots, const int32_t* sel, const int32_t* n_sel,
+                     int sel_stride, int n_units, int32_t* missing, int32_t* n_missing, int32_t* slot, void* stream) {
+  if (!c || n_units < 0) return SPKV_EINVAL;
+  if (n_units == 0) return SPKV_OK;
+  if (!resident || !sel || !n_sel || !missing || !n_missing || !slot) return SPKV_EINVAL;
+  if (n_slots <= 0 || n_slots > 16384 || sel_stride <= 0 || sel_stride > 4096 || n_units > 65535) return SPKV_EINVAL;
+  return status_of(spkv::launch_setdiff(c->dev_err, resident, n_slots, sel, n_sel, sel_stride, n_units, missing,
+                                        n_missing, slot, as_stream(stream)));
+}
+
+int lru_bucket_update(spkv_cache_t c, int32_t* resident, int32_t* ts, int n_slots, const int32_t* slot,
+                      const int32_t* n_sel, const int32_t* missing, const int32_t* n_missing, int sel_stride,
+                      int n_units, int32_t t_now, int bucket_width, int32_t* victims, int32_t* hist, void* stream) {
+  if (!c || n_units < 0) return SPKV_EINVAL;
+  if (n_units == 0) return SPKV_OK;
+  if (!resident || !ts || !slot || !n_sel || !missing || !n_missing || !victims || !hist) return SPKV_EINVAL;
+  if (n_slots <= 0 || n_slots > 16384 || sel_stride <= 0 || sel_stride > 4096 || n_units > 65535 || bucket_width < 1)
+    return SPKV_EINVAL;
+  return status_of(spkv::launch_lru(c->dev_err, resident, ts, n_slots, slot, n_sel, missing, n_missing, sel_stride,
+                                    n_units, t_now, bucket_width, victims, hist, as_stream(stream)));
+}
+
+int spkv_pack_page_words(const int32_t* phys, const int32_t* valid, const int32_t* doc_slot, int64_t n,
+                         uint32_t* words) {
+  if (n < 0 || (n > 0 && (!phys || !valid || !doc_slot || !words))) return SPKV_EINVAL;
+  for (int64_t i = 0; i < n; ++i) {
+    if (phys[i] < 0 || phys[i] >= (1 << 18) || valid[i] < 1 || valid[i] > 64 || doc_slot[i] < 0 || doc_slot[i] > 255)
+      return SPKV_EINVAL;
+    words[i] = static_cast<uint32_t>(phys[i]) | (static_cast<uint32_t>(valid[i] - 1) << 18) |
+               (static_cast<uint32_t>(doc_slot[i]) << 24);
+  }
+  return SPKV_OK;
+}
+
+int spkv_get_device_error(spkv_cache_t c, void* stream, uint32_t* bits) {
+  if (!c || !bits) return SPKV_EINVAL;
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return SPKV_ECUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, c->dev_err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return SPKV_ECUDA;
+  if (v && cudaMemset(c->dev_err, 0, sizeof(v)) != cudaSuccess) return SPKV_ECUDA;
+  *bits = v;
+  if (v & SPKV_DEVERR_TIMEOUT) return SPKV_ETIMEOUT;
+  return v ? SPKV_EDEVICE : SPKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,563 @@
+// Split-K flash decoding over a list of KV pages per (request, kv head) unit, in two forms:
+//   sparse : the page list is a selected subset (logical page ids -> page table), plain scores
+//   lazy   : the page list is packed page words; the query is rotated with RoPE by the offset
+//            between the query position and the page's document, once per document switch
+//
+// Computation: [FA] "How KV sparsity achieves 1.5x acceleration for vLLM", section "2. Attention
+// modification": one pass over KV blocks with a running max, a running sum l and an output
+// accumulator, O / l at the end; rowmax and l are kept and returned as LSE.  Lazy form:
+// [LazyAttention] "Technical implementation 2. Decoding" and "Mathematical equivalence".
+//
+// GB300 design (one CTA per SM, persistent):
+//   * Work balance: the pages of all units form one sequence of T pages; CTA i takes pages
+//     [i*T/N, (i+1)*T/N).  A unit split over several CTAs leaves one fp32 partial
+//     (max, sum, unnormalised O) per CTA in a workspace slot (unit + cta); the last CTA to
+//     finish a unit (atomic arrival counter, no waiting) merges the partials.
+//   * Data movement: a producer warp streams each page's K and V (2 x 16 KiB, head-major, one
+//     contiguous page each) with TMA tensor loads (128B swizzle) into a ring of shared-memory
+//     stages, completed on mbarriers; consumers release stages on a second barrier.
+//   * Math: four consumer warps each take 16 of the 64 tokens of every page.  Q.K^T runs on
+//     mma.sync m16n8k16 with the 16 keys as M and the GQA group (padded to 8) as N, so the
+//     group of G <= 8 query heads shares one tensor-core tile; P^T goes from the accumulator
+//     layout to the B-operand layout with movmatrix; P.V runs with V^T (ldmatrix.trans) as A.
+//     P is split into bf16 hi + lo parts (two MMAs) so the weights keep ~17 bits.
+#include <math_constants.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace spkv {
+namespace {
+
+constexpr int kConsumers = 4;
+constexpr int kThreads = (kConsumers + 1) * 32;
+constexpr int kBoxBytes = 8192;                // 64 tokens x 64 dims x bf16
+constexpr int kStageBytes = 4 * kBoxBytes;     // K (2 boxes) + V (2 boxes) of one page-head
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct __align__(16) StageMeta {
+  int unit;     // unit of this page
+  int valid;    // valid tokens (0 = skip the page)
+  int rel;      // lazy: query position - document offset
+  int ustart;   // position of the unit's first page in the global page sequence
+  int ucount;   // pages of the unit
+  int pad0, pad1, pad2;
+};
+
+template <int NT>
+struct Smem {
+  static constexpr int kG = NT * 8;
+  // combine area (one per consumer warp)
+  float cm[kConsumers][kG];
+  float cl[kConsumers][kG];
+  float co[kConsumers][kG][kHeadDim];
+  uint64_t full[8];
+  uint64_t empty[8];
+  StageMeta meta[8];
+  int scan[kThreads];
+  int u0, p0;
+  int last;
+};
+
+template <int NT, int STAGES>
+constexpr size_t smem_bytes() {
+  return 1024 /*align slack*/ + size_t(STAGES) * kStageBytes + sizeof(Smem<NT>);
+}
+
+__device__ __forceinline__ int unit_count(const AttnParams& p, bool lazy, int u) {
+  if (lazy) {
+    const int n = p.n_pages[u / p.Hk];
+    return n < 0 ? 0 : (n > p.np_max ? p.np_max : n);
+  }
+  const int n = p.n_sel[u];
+  return n < 0 ? 0 : (n > p.sel_stride ? p.sel_stride : n);
+}
+
+// CTA whose page range contains global page position x (ranges [i*T/N, (i+1)*T/N), T >= N).
+__device__ __forceinline__ int cta_of(int64_t x, int64_t T, int64_t N) {
+  return static_cast<int>(((x + 1) * N - 1) / T);
+}
+
+// Swizzled shared address of the 16-byte chunk `chunk` (0..15 across the 128 dims) of token
+// row `row` inside one K or V page image made of two 128B-swizzled 64x64 boxes.
+__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk) {
+  return base + ((chunk >> 3) * kBoxBytes) + row * 128 + ((((chunk & 7) ^ (row & 7))) << 4);
+}
+
+template <int NT, bool LAZY, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                      const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem<NT>& S = *reinterpret_cast<Smem<NT>*>(stages + size_t(STAGES) * kStageBytes);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int U = p.B * p.Hk;
+
+  // ---- 1. global page sequence: T = sum of unit counts; find this CTA's first unit
+  const int c0 = static_cast<int>(int64_t(tid) * U / kThreads);
+  const int c1 = static_cast<int>(int64_t(tid + 1) * U / kThreads);
+  int csum = 0;
+  for (int u = c0; u < c1; ++u) csum += unit_count(p, LAZY, u);
+  // block exclusive scan of csum
+  int x = csum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) S.scan[warp] = x;
+  __syncthreads();
+  int wbase = 0, T = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    if (w < warp) wbase += S.scan[w];
+    T += S.scan[w];
+  }
+  const int cpre = wbase + x - csum;  // exclusive prefix of this thread's chunk
+
+  // units with no pages get out = 0, lse = -inf (spread over the CTAs)
+  for (int u = blockIdx.x; u < U; u += gridDim.x) {
+    if (unit_count(p, LAZY, u) != 0) continue;
+    const int b = u / p.Hk, h = u % p.Hk;
+    for (int i = tid; i < p.G * kHeadDim; i += kThreads)
+      p.out[(int64_t(b) * p.Hq + h * p.G) * kHeadDim + i] = 0.f;
+    if (tid < p.G) p.lse[int64_t(b) * p.Hq + h * p.G + tid] = -CUDART_INF_F;
+  }
+
+  const int64_t N = T < static_cast<int>(gridDim.x) ? T : gridDim.x;
+  if (static_cast<int64_t>(blockIdx.x) >= N) return;
+  const int64_t lo = int64_t(blockIdx.x) * T / N;
+  const int64_t hi = int64_t(blockIdx.x + 1) * T / N;
+  if (csum > 0 && lo >= cpre && lo < cpre + csum) {
+    int acc = cpre;
+    for (int u = c0; u < c1; ++u) {
+      const int n = unit_count(p, LAZY, u);
+      if (lo < acc + n) {
+        S.u0 = u;
+        S.p0 = acc;
+        break;
+      }
+      acc += n;
+    }
+  }
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], kConsumers);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int n_local = static_cast<int>(hi - lo);
+
+  if (warp == kConsumers) {
+    // ================================================================ producer warp
+    int u = S.u0, ustart = S.p0, ucnt = unit_count(p, LAZY, u);
+    const uint64_t pol = LAZY ? l2_policy_evict_normal() : l2_policy_evict_first();
+    bool ok = true;
+    for (int64_t j0 = lo; j0 < hi && ok; j0 += 32) {
+      const int64_t xpos = j0 + lane;
+      const bool need = xpos < hi;
+      int my_u = -1, my_k = 0, my_us = 0, my_uc = 0;
+      while (true) {
+        if (need && my_u < 0 && xpos < int64_t(ustart) + ucnt) {
+          my_u = u;
+          my_k = static_cast<int>(xpos - ustart);
+          my_us = ustart;
+          my_uc = ucnt;
+        }
+        if (!__any_sync(0xffffffffu, need && my_u < 0)) break;
+        if (u >= U - 1) break;  // cannot happen: every position < T lies in a unit
+        ustart += ucnt;
+        do {
+          ++u;
+          ucnt = unit_count(p, LAZY, u);
+        } while (ucnt == 0 && u < U - 1);
+      }
+      // page info of position xpos
+      int phys = 0, valid = 0, rel = 0, head = 0;
+      if (need && my_u >= 0) {
+        const int b = my_u / p.Hk;
+        head = my_u % p.Hk;
+        uint32_t bad = 0;
+        if (!LAZY) {
+          const int lp = p.sel[int64_t(my_u) * p.sel_stride + my_k];
+          if (lp < 0 || lp >= p.np_max) {
+            bad |= SPKV_DEVERR_PAGE_ID;
+          } else {
+            const int v = min(kPageTokens, p.seq_len[b] - kPageTokens * lp);
+            const int ph = p.page_table[int64_t(b) * p.np_max + lp];
+            if (v <= 0) bad |= SPKV_DEVERR_PAGE_ID;
+            else if (ph < 0 || ph >= p.n_phys) bad |= SPKV_DEVERR_PHYS;
+            else { phys = ph; valid = v; }
+          }
+        } else {
+          const int mh = p.meta_heads == 1 ? 0 : head;
+          const uint32_t w = p.meta[(int64_t(b) * p.meta_heads + mh) * p.np_max + my_k];
+          const int ph = static_cast<int>(w & 0x3FFFFu);
+          const int v = static_cast<int>((w >> 18) & 63u) + 1;
+          const int sl = static_cast<int>(w >> 24);
+          if (ph >= p.n_phys) bad |= SPKV_DEVERR_PHYS;
+          else if (sl >= p.max_docs) bad |= SPKV_DEVERR_SLOT;
+          else {
+            phys = ph;
+            valid = v;
+            rel = p.qpos[b] - p.doc_pos[int64_t(b) * p.max_docs + sl];
+          }
+        }
+        flag_error(p.err, bad);
+      }
+      const int cnt = static_cast<int>(hi - j0 < 32 ? hi - j0 : 32);
+      for (int i = 0; i < cnt; ++i) {
+        const int jl = static_cast<int>(j0 - lo) + i;
+        const int s = jl % STAGES;
+        const int bu = __shfl_sync(0xffffffffu, my_u, i);
+        const int bv = __shfl_sync(0xffffffffu, valid, i);
+        const int bp = __shfl_sync(0xffffffffu, phys, i);
+        const int br = __shfl_sync(0xffffffffu, rel, i);
+        const int bs = __shfl_sync(0xffffffffu, my_us, i);
+        const int bc = __shfl_sync(0xffffffffu, my_uc, i);
+        const int bh = __shfl_sync(0xffffffffu, head, i);
+        if (jl >= STAGES) {
+          if (!mbar_wait(&S.empty[s], ((jl / STAGES) - 1) & 1)) {
+            if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
+            ok = false;
+            break;
+          }
+        }
+        if (lane == 0) {
+          StageMeta m;
+          m.unit = bu;
+          m.valid = bv;
+          m.rel = br;
+          m.ustart = bs;
+          m.ucount = bc;
+          m.pad0 = m.pad1 = m.pad2 = 0;
+          S.meta[s] = m;
+          if (bv > 0) {
+            mbar_arrive_expect_tx(&S.full[s], kStageBytes);
+            uint8_t* dst = stages + size_t(s) * kStageBytes;
+            const int z = static_cast<int>(int64_t(bh) * p.n_phys + bp);
+            tma_load_3d(dst, &tmk, &S.full[s], 0, 0, z, pol);
+            tma_load_3d(dst + kBoxBytes, &tmk, &S.full[s], 64, 0, z, pol);
+            tma_load_3d(dst + 2 * kBoxBytes, &tmv, &S.full[s], 0, 0, z, pol);
+            tma_load_3d(dst + 3 * kBoxBytes, &tmv, &S.full[s], 64, 0, z, pol);
+          } else {
+            mbar_arrive(&S.full[s]);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    // Before leaving, make sure no TMA copy issued by this CTA is still in flight.
+    const int first = n_local > STAGES ? n_local - STAGES : 0;
+    for (int jl = first; jl < n_local; ++jl) mbar_wait(&S.full[jl % STAGES], (jl / STAGES) & 1);
+    return;
+  }
+
+  // ================================================================== consumer warps
+  const int r = lane >> 2, c = lane & 3;
+  const int t0 = warp * 16;
+  const float scale = p.scale_log2;
+
+  float m[NT][2], lsum[NT][2];
+  float O[8][NT][4];
+  uint32_t qh[8][NT][2];                  // B fragments of q (bf16 hi part)
+  uint32_t ql[LAZY ? 8 : 1][NT][2];       // lazy: bf16 lo part of the rotated query
+  uint32_t qraw[LAZY ? 8 : 1][NT][2];     // lazy: unrotated query
+  int cur_u = -1, cur_us = 0, cur_uc = 0, cur_rel = 0;
+  bool have_rel = false;
+
+  auto reset_state = [&]() {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m[nt][0] = m[nt][1] = -CUDART_INF_F;
+      lsum[nt][0] = lsum[nt][1] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) O[j][nt][e] = 0.f;
+    }
+  };
+
+  auto load_q = [&](int u) {
+    const int b = u / p.Hk, h = u % p.Hk;
+    const uint32_t* qw = reinterpret_cast<const uint32_t*>(p.q);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int g = nt * 8 + r;
+      const bool live = g < p.G;
+      const int64_t row = (int64_t(b) * p.Hq + h * p.G + (live ? g : 0)) * (kHeadDim / 2);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t w0 = live ? qw[row + ks * 8 + c] : 0u;
+        const uint32_t w1 = live ? qw[row + ks * 8 + c + 4] : 0u;
+        if (LAZY) {
+          qraw[LAZY ? ks : 0][nt][0] = w0;
+          qraw[LAZY ? ks : 0][nt][1] = w1;
+        } else {
+          qh[ks][nt][0] = w0;
+          qh[ks][nt][1] = w1;
+        }
+      }
+    }
+  };
+
+  // Lazy form: q_rot = R(rel) q for this thread's 32 dims, split into bf16 hi + lo.  The
+  // angle of pair i is rel * theta_i; its fraction of a turn is formed exactly modulo 1 as a
+  // 64-bit fixed-point product (phase accumulator), so the angle handed to __sincosf lies in
+  // [-pi, pi) with ~1e-9 rad error however large rel * theta_i is.
+  auto rotate_q = [&](int rel) {
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+      for (int wi = 0; wi < 2; ++wi) {
+        float sn[2], cs[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int i = 16 * ks + 2 * c + 8 * wi + e;   // pair index: dims i and i + 64
+          const uint64_t ph = static_cast<uint64_t>(static_cast<int64_t>(rel)) * p.phase_inc[i];
+          const float ang = static_cast<float>(static_cast<int32_t>(ph >> 32)) * 1.4629180792671596e-09f;
+          __sincosf(ang, &sn[e], &cs[e]);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint32_t wx = qraw[LAZY ? ks : 0][nt][wi], wy = qraw[LAZY ? ks + 4 : 0][nt][wi];
+          const float x0 = bf16lo_to_f32(wx), x1 = bf16hi_to_f32(wx);
+          const float y0 = bf16lo_to_f32(wy), y1 = bf16hi_to_f32(wy);
+          float xh0, xl0, xh1, xl1, yh0, yl0, yh1, yl1;
+          split_bf16(x0 * cs[0] - y0 * sn[0], xh0, xl0);
+          split_bf16(x1 * cs[1] - y1 * sn[1], xh1, xl1);
+          split_bf16(y0 * cs[0] + x0 * sn[0], yh0, yl0);
+          split_bf16(y1 * cs[1] + x1 * sn[1], yh1, yl1);
+          qh[ks][nt][wi] = pack_bf16x2(xh0, xh1);
+          ql[LAZY ? ks : 0][nt][wi] = pack_bf16x2(xl0, xl1);
+          qh[ks + 4][nt][wi] = pack_bf16x2(yh0, yh1);
+          ql[LAZY ? ks + 4 : 0][nt][wi] = pack_bf16x2(yl0, yl1);
+        }
+      }
+    }
+  };
+
+  // Merge the four warps' states for unit u and write the result or a split-K partial.
+  auto flush = [&](int u, int ustart, int ucount) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        float l = lsum[nt][cc];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        if (r == 0) {
+          S.cm[warp][nt * 8 + 2 * c + cc] = m[nt][cc];
+          S.cl[warp][nt * 8 + 2 * c + cc] = l;
+        }
+      }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          S.co[warp][nt * 8 + 2 * c + (e & 1)][16 * j + r + ((e >> 1) << 3)] = O[j][nt][e];
+    named_bar_sync(1, kConsumers * 32);
+
+    const int b = u / p.Hk, h = u % p.Hk;
+    const int d = tid;  // 0..127
+    const int first = cta_of(ustart, T, N);
+    const int nparts = cta_of(int64_t(ustart) + ucount - 1, T, N) - first + 1;
+    const int64_t orow = int64_t(b) * p.Hq + h * p.G;
+    const int64_t slot = int64_t(u) + blockIdx.x;
+    for (int g = 0; g < p.G; ++g) {
+      float M = -CUDART_INF_F;
+#pragma unroll
+      for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, S.cm[w][g]);
+      float L = 0.f, acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumers; ++w) {
+        const float mw = S.cm[w][g];
+        const float fw = mw == -CUDART_INF_F ? 0.f : exp2f(mw - M);
+        L += fw * S.cl[w][g];
+        acc += fw * S.co[w][g][d];
+      }
+      if (nparts == 1) {
+        p.out[(orow + g) * kHeadDim + d] = L > 0.f ? acc / L : 0.f;
+        if (d == 0) p.lse[orow + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
+      } else {
+        p.ws_o[(slot * 16 + g) * kHeadDim + d] = acc;
+        if (d == 0) {
+          p.ws_m[slot * 16 + g] = M;
+          p.ws_l[slot * 16 + g] = L;
+        }
+      }
+    }
+    if (nparts > 1) {
+      __threadfence();
+      named_bar_sync(1, kConsumers * 32);
+      if (tid == 0) S.last = (atomicAdd(&p.ws_cnt[u], 1) == nparts - 1);
+      named_bar_sync(1, kConsumers * 32);
+      if (S.last) {
+        __threadfence();
+        for (int g = 0; g < p.G; ++g) {
+          float M = -CUDART_INF_F;
+          for (int i = 0; i < nparts; ++i) M = fmaxf(M, __ldcg(&p.ws_m[(int64_t(u) + first + i) * 16 + g]));
+          float L = 0.f, acc = 0.f;
+          for (int i = 0; i < nparts; ++i) {
+            const int64_t sl = int64_t(u) + first + i;
+            const float mw = __ldcg(&p.ws_m[sl * 16 + g]);
+            const float fw = mw == -CUDART_INF_F ? 0.f : exp2f(mw - M);
+            L += fw * __ldcg(&p.ws_l[sl * 16 + g]);
+            acc += fw * __ldcg(&p.ws_o[(sl * 16 + g) * kHeadDim + d]);
+          }
+          p.out[(orow + g) * kHeadDim + d] = L > 0.f ? acc / L : 0.f;
+          if (d == 0) p.lse[orow + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
+        }
+        if (tid == 0) p.ws_cnt[u] = 0;
+      }
+    }
+    named_bar_sync(1, kConsumers * 32);
+  };
+
+  reset_state();
+  const uint32_t stage0 = smem_u32(stages);
+  for (int jl = 0; jl < n_local; ++jl) {
+    const int s = jl % STAGES;
+    if (!mbar_wait(&S.full[s], (jl / STAGES) & 1)) {
+      if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
+      break;
+    }
+    const StageMeta mt = S.meta[s];
+    if (mt.unit < 0) {  // defensive: a position the producer could not place
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[s]);
+      continue;
+    }
+    if (mt.unit != cur_u) {
+      if (cur_u >= 0) flush(cur_u, cur_us, cur_uc);
+      cur_u = mt.unit;
+      cur_us = mt.ustart;
+      cur_uc = mt.ucount;
+      reset_state();
+      load_q(cur_u);
+      have_rel = false;
+    }
+    if (mt.valid > t0) {
+      if (LAZY && (!have_rel || mt.rel != cur_rel)) {
+        rotate_q(mt.rel);
+        cur_rel = mt.rel;
+        have_rel = true;
+      }
+      const uint32_t kb = stage0 + s * kStageBytes;
+      const uint32_t vb = kb + 2 * kBoxBytes;
+      // ---- S^T = K q^T for my 16 keys
+      float acc[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+      const int krow = t0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        uint32_t a[4];
+        ldsm_x4(swz(kb, krow, 2 * ks + (lane >> 4)), a);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma_bf16_16816(acc[nt], a, qh[ks][nt][0], qh[ks][nt][1]);
+          if (LAZY) mma_bf16_16816(acc[nt], a, ql[LAZY ? ks : 0][nt][0], ql[LAZY ? ks : 0][nt][1]);
+        }
+      }
+      // ---- online softmax (log2 domain) on my 16 rows
+      const bool row0_ok = t0 + r < mt.valid, row1_ok = t0 + r + 8 < mt.valid;
+      uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float sv[4];
+        sv[0] = row0_ok ? acc[nt][0] * scale : -CUDART_INF_F;
+        sv[1] = row0_ok ? acc[nt][1] * scale : -CUDART_INF_F;
+        sv[2] = row1_ok ? acc[nt][2] * scale : -CUDART_INF_F;
+        sv[3] = row1_ok ? acc[nt][3] * scale : -CUDART_INF_F;
+        float pv[4];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          float mx = fmaxf(sv[cc], sv[cc + 2]);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float mnew = fmaxf(m[nt][cc], mx);
+          const float alpha = exp2f(m[nt][cc] - mnew);
+          m[nt][cc] = mnew;
+          pv[cc] = exp2f(sv[cc] - mnew);
+          pv[cc + 2] = exp2f(sv[cc + 2] - mnew);
+          lsum[nt][cc] = lsum[nt][cc] * alpha + pv[cc] + pv[cc + 2];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            O[j][nt][cc] *= alpha;
+            O[j][nt][cc + 2] *= alpha;
+          }
+        }
+        float h0, l0, h1, l1, h2, l2, h3, l3;
+        split_bf16(pv[0], h0, l0);
+        split_bf16(pv[1], h1, l1);
+        split_bf16(pv[2], h2, l2);
+        split_bf16(pv[3], h3, l3);
+        bh[nt][0] = movmatrix_trans(pack_bf16x2(h0, h1));
+        bh[nt][1] = movmatrix_trans(pack_bf16x2(h2, h3));
+        bl[nt][0] = movmatrix_trans(pack_bf16x2(l0, l1));
+        bl[nt][1] = movmatrix_trans(pack_bf16x2(l2, l3));
+      }
+      // ---- O^T += V^T P^T for my 16 keys
+      const bool partial = mt.valid < t0 + 16;
+      uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
+      if (partial) {
+        const int ta = t0 + 2 * c, tb = t0 + 8 + 2 * c;
+        mlo = (ta < mt.valid ? 0x0000FFFFu : 0u) | (ta + 1 < mt.valid ? 0xFFFF0000u : 0u);
+        mhi = (tb < mt.valid ? 0x0000FFFFu : 0u) | (tb + 1 < mt.valid ? 0xFFFF0000u : 0u);
+      }
+      const int vrow = t0 + (lane & 7) + ((lane >> 4) & 1) * 8;
+      const int vsel = (lane >> 3) & 1;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t a[4];
+        ldsm_x4_trans(swz(vb, vrow, 2 * j + vsel), a);
+        a[0] &= mlo;
+        a[1] &= mlo;
+        a[2] &= mhi;
+        a[3] &= mhi;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma_bf16_16816(O[j][nt], a, bh[nt][0], bh[nt][1]);
+          mma_bf16_16816(O[j][nt], a, bl[nt][0], bl[nt][1]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[s]);
+  }
+  if (cur_u >= 0) flush(cur_u, cur_us, cur_uc);
+}
+
+template <int NT, bool LAZY, int STAGES>
+cudaError_t launch_one(const spkv_cache* c, const AttnParams& p, int grid, cudaStream_t st) {
+  auto kern = attn_split_kernel<NT, LAZY, STAGES>;
+  const size_t smem = smem_bytes<NT, STAGES>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, smem, st>>>(c->tmap_k, c->tmap_v, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t attn_smem_bytes(int G, bool lazy) {
+  (void)lazy;
+  return G <= 8 ? smem_bytes<1, 6>() : smem_bytes<2, 5>();
+}
+
+cudaError_t launch_attn(const spkv_cache* c, const AttnParams& p, bool lazy, int grid, cudaStream_t st) {
+  if (p.G <= 8) {
+    return lazy ? launch_one<1, true, 6>(c, p, grid, st) : launch_one<1, false, 6>(c, p, grid, st);
+  }
+  return lazy ? launch_one<2, true, 5>(c, p, grid, st) : launch_one<2, false, 5>(c, p, grid, st);
+}
+
+}  // namespace spkv

@@ -1,0 +1,78 @@
+// Host-side handle and the launch functions each kernel file exports to api.cu.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/spkv.h"
+
+struct spkv_cache {
+  spkv_desc d;
+  int device = 0;
+  int sm_count = 0;
+  CUtensorMap tmap_k;   // K pool as [Hk*n_phys][64 tok][128 d] bf16, box 64x64, 128B swizzle
+  CUtensorMap tmap_v;
+  uint32_t* dev_err = nullptr;   // device error word
+  float* ws_m = nullptr;         // split-K partial row max   [slots][16]
+  float* ws_l = nullptr;         // split-K partial row sum   [slots][16]
+  float* ws_o = nullptr;         // split-K partial outputs   [slots][16][128]
+  int32_t* ws_cnt = nullptr;     // per-unit arrival counters [max_units], kept at 0 between calls
+  int64_t ws_slots = 0;
+  int32_t max_units = 0;
+  int attn_grid = 0;             // CTAs of the split-K attention kernel (one per SM)
+};
+
+namespace spkv {
+
+// Parameters of the split-K attention kernel (sparse and lazy forms).
+struct AttnParams {
+  const void* q;
+  float* out;
+  float* lse;
+  int B, Hq, Hk, G;
+  int64_t n_phys;
+  uint32_t* err;
+  float* ws_m;
+  float* ws_l;
+  float* ws_o;
+  int32_t* ws_cnt;
+  // sparse form
+  const int32_t* page_table;
+  int np_max;
+  const int32_t* sel;
+  const int32_t* n_sel;
+  int sel_stride;
+  const int32_t* seq_len;
+  // lazy form
+  const int32_t* qpos;
+  const uint32_t* meta;
+  int meta_heads;
+  const int32_t* n_pages;
+  const int32_t* doc_pos;
+  int max_docs;
+  float scale_log2;              // log2(e) / sqrt(128)
+  uint64_t phase_inc[64];        // RoPE pair j: turns per position, 2^-64 fixed point
+};
+
+cudaError_t launch_summary_build(const spkv_cache* c, cudaStream_t st);
+cudaError_t launch_append(const spkv_cache* c, const int32_t* phys, const int32_t* tok, const void* k_new,
+                          const void* v_new, int n_rows, cudaStream_t st);
+cudaError_t launch_score(const spkv_cache* c, const void* q, int B, int Hq, const int32_t* page_table,
+                         int np_max, const int32_t* seq_len, float* scores, cudaStream_t st);
+cudaError_t launch_select(const spkv_cache* c, const float* qs, const float* es, uint32_t* alive, int B,
+                          int np_max, const int32_t* seq_len, int k_q, int k_e, int32_t* sel, int32_t* n_sel,
+                          cudaStream_t st);
+cudaError_t launch_attn(const spkv_cache* c, const AttnParams& p, bool lazy, int grid, cudaStream_t st);
+cudaError_t launch_setdiff(uint32_t* err, const int32_t* resident, int n_slots, const int32_t* sel,
+                           const int32_t* n_sel, int sel_stride, int n_units, int32_t* missing,
+                           int32_t* n_missing, int32_t* slot, cudaStream_t st);
+cudaError_t launch_lru(uint32_t* err, int32_t* resident, int32_t* ts, int n_slots, const int32_t* slot,
+                       const int32_t* n_sel, const int32_t* missing, const int32_t* n_missing, int sel_stride,
+                       int n_units, int32_t t_now, int bucket_width, int32_t* victims, int32_t* hist,
+                       cudaStream_t st);
+
+// Shared-memory bytes the attention kernel needs for a group size (used for limits checks).
+size_t attn_smem_bytes(int G, bool lazy);
+
+}  // namespace spkv

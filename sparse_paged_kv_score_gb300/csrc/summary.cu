@@ -1,0 +1,109 @@
+// Pooled-key summaries (first pooling stage) and token append.
+//
+// [NOSA] "NOSA: Native and Offloadable Sparse Attention", section "Method 1", block-wise
+// implementation: the selection score pools keys by their mean inside 16-token sub-blocks.
+// [NOSA] section "Method 2: NOSI", kernel fusion: pooling is produced where K is written.
+// We keep the fp32 *sum* of each sub-block's valid keys (mean = sum / count), written in a fixed
+// token order so that a create and any sequence of appends give bitwise the same sums.
+#include "common.cuh"
+#include "internal.h"
+
+namespace spkv {
+namespace {
+
+// Sum of the valid rows of sub-block j of one page-head for dims 2i, 2i+1 (fixed order).
+__device__ __forceinline__ float2 subblock_sum(const uint32_t* page_words, int j, int cnt, int i) {
+  float s0 = 0.f, s1 = 0.f;
+  const int hi = min(kSubblock * (j + 1), cnt);
+  for (int t = kSubblock * j; t < hi; ++t) {
+    const uint32_t w = page_words[t * (kHeadDim / 2) + i];
+    s0 += bf16lo_to_f32(w);
+    s1 += bf16hi_to_f32(w);
+  }
+  return make_float2(s0, s1);
+}
+
+// One group of 64 threads per page-head; thread i owns dims 2i, 2i+1.
+__global__ void __launch_bounds__(256) summary_build_kernel(const uint32_t* __restrict__ kpool, float* __restrict__ ksum,
+                                                            const int32_t* __restrict__ page_cnt, int64_t n_ph,
+                                                            int64_t n_phys) {
+  const int64_t ph = int64_t(blockIdx.x) * 4 + threadIdx.x / 64;
+  if (ph >= n_ph) return;
+  const int i = threadIdx.x % 64;
+  const int cnt = max(0, min(kPageTokens, page_cnt[ph % n_phys]));
+  const uint32_t* pw = kpool + ph * (kPageTokens * kHeadDim / 2);
+  float2* out = reinterpret_cast<float2*>(ksum + ph * kNSub * kHeadDim);
+#pragma unroll
+  for (int j = 0; j < kNSub; ++j) out[j * (kHeadDim / 2) + i] = subblock_sum(pw, j, cnt, i);
+}
+
+// Writes row r of every head into the pool and raises page_cnt.  One 64-thread group per
+// (row, head).
+__global__ void __launch_bounds__(256) append_write_kernel(uint32_t* __restrict__ kpool, uint32_t* __restrict__ vpool,
+                                                           int32_t* __restrict__ page_cnt, const int32_t* __restrict__ phys,
+                                                           const int32_t* __restrict__ tok, const uint32_t* __restrict__ k_new,
+                                                           const uint32_t* __restrict__ v_new, int n_rows, int Hk,
+                                                           int64_t n_phys, uint32_t* err) {
+  const int64_t item = int64_t(blockIdx.x) * 4 + threadIdx.x / 64;
+  if (item >= int64_t(n_rows) * Hk) return;
+  const int row = static_cast<int>(item / Hk), h = static_cast<int>(item % Hk);
+  const int i = threadIdx.x % 64;
+  const int p = phys[row], t = tok[row];
+  if (p < 0 || p >= n_phys || t < 0 || t >= kPageTokens) {
+    if (i == 0 && h == 0) flag_error(err, (p < 0 || p >= n_phys) ? SPKV_DEVERR_PHYS : SPKV_DEVERR_PAGE_ID);
+    return;
+  }
+  const int64_t dst = ((int64_t(h) * n_phys + p) * kPageTokens + t) * (kHeadDim / 2) + i;
+  const int64_t src = (int64_t(row) * Hk + h) * (kHeadDim / 2) + i;
+  kpool[dst] = k_new[src];
+  vpool[dst] = v_new[src];
+  if (i == 0 && h == 0) atomicMax(&page_cnt[p], t + 1);
+}
+
+// Recomputes the sub-block sum that row r touched, for every head.
+__global__ void __launch_bounds__(256) append_sum_kernel(const uint32_t* __restrict__ kpool, float* __restrict__ ksum,
+                                                         const int32_t* __restrict__ page_cnt,
+                                                         const int32_t* __restrict__ phys, const int32_t* __restrict__ tok,
+                                                         int n_rows, int Hk, int64_t n_phys) {
+  const int64_t item = int64_t(blockIdx.x) * 4 + threadIdx.x / 64;
+  if (item >= int64_t(n_rows) * Hk) return;
+  const int row = static_cast<int>(item / Hk), h = static_cast<int>(item % Hk);
+  const int i = threadIdx.x % 64;
+  const int p = phys[row], t = tok[row];
+  if (p < 0 || p >= n_phys || t < 0 || t >= kPageTokens) return;
+  const int j = t / kSubblock;
+  const int cnt = max(0, min(kPageTokens, page_cnt[p]));
+  const int64_t ph = int64_t(h) * n_phys + p;
+  const uint32_t* pw = kpool + ph * (kPageTokens * kHeadDim / 2);
+  reinterpret_cast<float2*>(ksum + (ph * kNSub + j) * kHeadDim)[i] = subblock_sum(pw, j, cnt, i);
+}
+
+}  // namespace
+
+cudaError_t launch_summary_build(const spkv_cache* c, cudaStream_t st) {
+  const int64_t n_ph = int64_t(c->d.n_kv_heads) * c->d.n_phys_pages;
+  if (n_ph == 0) return cudaSuccess;
+  const int64_t blocks = (n_ph + 3) / 4;
+  summary_build_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+      static_cast<const uint32_t*>(c->d.k_pool), c->d.ksum, c->d.page_cnt, n_ph, c->d.n_phys_pages);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(const spkv_cache* c, const int32_t* phys, const int32_t* tok, const void* k_new,
+                          const void* v_new, int n_rows, cudaStream_t st) {
+  if (n_rows == 0) return cudaSuccess;
+  const int Hk = c->d.n_kv_heads;
+  const int64_t blocks = (int64_t(n_rows) * Hk + 3) / 4;
+  append_write_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+      static_cast<uint32_t*>(c->d.k_pool), static_cast<uint32_t*>(c->d.v_pool), c->d.page_cnt, phys, tok,
+      static_cast<const uint32_t*>(k_new), static_cast<const uint32_t*>(v_new), n_rows, Hk, c->d.n_phys_pages,
+      c->dev_err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  append_sum_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<const uint32_t*>(c->d.k_pool),
+                                                                     c->d.ksum, c->d.page_cnt, phys, tok, n_rows, Hk,
+                                                                     c->d.n_phys_pages);
+  return cudaGetLastError();
+}
+
+}  // namespace spkv

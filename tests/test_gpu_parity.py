@@ -1,0 +1,373 @@
+"""GPU parity: every kernel, called through the C ABI, against the fp64 oracle on seeded inputs.
+
+Acceptance (attention): max |dO| <= 1e-2 and mean |dO| <= 1e-3 against the fp64 oracle on the
+same bf16 inputs, LSE within 1e-3.  Selection, set-difference and LRU: bit-exact when both
+sides rank the same fp32 scores; against fp64 oracle scores, differences are allowed only among
+pages within 1e-5 relative of the k-th score.  Block scores: within an fp32 summation bound
+derived from the operand magnitudes (2e-5 x sum |q_sum| |mean|, about twice the worst-case
+rounding of the 16 + 128 + G term sums).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+import sparse_paged_kv_score_gb300 as spkv
+from helpers import (DEV, Dev, alive_bits_to_bytes, alive_bytes_to_bits, attn_errors, bf, f32, i32,
+                     u32_as_i32)
+
+pytestmark = pytest.mark.gpu
+
+ATTN_MAX, ATTN_MEAN, LSE_TOL = 1e-2, 1e-3, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from sparse_paged_kv_score_gb300 import build
+    build.build()
+    spkv.load()
+
+
+def f64(bits):
+    return gen.bf16_to_f32(bits).astype(np.float64)
+
+
+# ------------------------------------------------------------------ summaries / append
+
+def test_summaries_match_oracle_means():
+    w = gen.sparse_workload(2, 8, 2, 64 * 5 + 37, 4, 4, seed=3)   # last page holds 37 tokens
+    d = Dev(w)
+    ks = d.ksum.cpu().numpy()
+    cnt = gen.page_counts(w)
+    for h in range(2):
+        for p in range(w["n_phys"]):
+            mean, c = oracle.page_means(w["k_pool"][h, p], cnt[p])
+            assert np.allclose(ks[h, p], mean * c[:, None], rtol=0, atol=2e-5)
+    assert d.errors() == (0, 0)
+    d.close()
+
+
+def test_append_equals_rebuild():
+    B, Hk = 3, 2
+    w = gen.sparse_workload(B, 8, Hk, 64 * 3 - 2, 4, 4, seed=5, extra_tokens=70)
+    d = Dev(w)
+    L = w["seq_len"].copy()
+    for step in range(4):      # crosses the page boundary at 192
+        phys = np.array([w["page_table"][b, L[b] // 64] for b in range(B)], np.int32)
+        tok = (L % 64).astype(np.int32)
+        kn = gen.rows_bf16(9, 100 + step, B * Hk).reshape(B, Hk, 128)
+        vn = gen.rows_bf16(9, 200 + step, B * Hk).reshape(B, Hk, 128)
+        spkv.paged_kv_append(d.cache, i32(phys), i32(tok), bf(kn), bf(vn))
+        for b in range(B):
+            w["k_pool"][:, phys[b], tok[b]] = kn[b]
+            w["v_pool"][:, phys[b], tok[b]] = vn[b]
+        L += 1
+    torch.cuda.synchronize()
+    w["seq_len"] = L
+    assert np.array_equal(d.k_pool.view(torch.int16).cpu().numpy().view(np.uint16), w["k_pool"])
+    assert np.array_equal(d.v_pool.view(torch.int16).cpu().numpy().view(np.uint16), w["v_pool"])
+    assert np.array_equal(d.cnt.cpu().numpy(), gen.page_counts(w))
+    fresh = Dev(w)      # summary build from scratch on the updated pool
+    assert torch.equal(d.ksum, fresh.ksum), "append and create must give bitwise equal sums"
+    assert d.errors() == (0, 0)
+    d.close()
+    fresh.close()
+
+
+# ------------------------------------------------------------------ block scores
+
+def _score_bound(w):
+    q = f64(w["q"])
+    B, Hk, G = w["B"], w["Hk"], w["G"]
+    bound = np.zeros((B, Hk, w["np_max"]))
+    for b in range(B):
+        for h in range(Hk):
+            qs = np.abs(q[b, h * G:(h + 1) * G].sum(0))
+            for p in range(w["np_max"]):
+                keys = f64(w["k_pool"][h, w["page_table"][b, p]])
+                m = np.abs(keys.reshape(4, 16, 128).mean(1))
+                bound[b, h, p] = 2e-5 * (m @ qs).max() / math.sqrt(128) + 1e-7
+    return bound
+
+
+@pytest.mark.parametrize("which", ["tiny", "mid"])
+def test_score_blocks_vs_oracle(which):
+    w = gen.tiny() if which == "tiny" else gen.sparse_workload(3, 32, 8, 64 * 40 + 5, 8, 8, seed=7,
+                                                                outlier_p=0.01)
+    d = Dev(w)
+    s = d.scores().cpu().numpy().astype(np.float64)
+    ref = oracle.score_batch(w["q"], w["k_pool"], w["page_table"], w["seq_len"])
+    assert np.array_equal(np.isinf(s), np.isinf(ref))
+    fin = np.isfinite(ref)
+    bound = _score_bound(w)
+    assert (np.abs(s - ref)[fin] <= bound[fin]).all(), np.abs(s - ref)[fin].max()
+    assert d.errors() == (0, 0)
+    d.close()
+
+
+# ------------------------------------------------------------------ selection
+
+def _check_select_bitexact(d, s_dev, e_np, alive_dev, k_q, k_e):
+    alive_before = alive_bits_to_bytes(alive_dev.cpu().numpy().view(np.uint32), d.npm)
+    sel, n_sel = d.select(s_dev, f32(e_np), alive_dev, k_q, k_e)
+    o_sel, o_n, o_alive = oracle.select_batch(s_dev.cpu().numpy().astype(np.float64),
+                                              e_np.astype(np.float64), alive_before, d.w["seq_len"],
+                                              k_q, k_e)
+    assert np.array_equal(sel.cpu().numpy(), o_sel)
+    assert np.array_equal(n_sel.cpu().numpy(), o_n)
+    got_alive = alive_dev.cpu().numpy().view(np.uint32)
+    want = alive_bytes_to_bits(o_alive)
+    assert np.array_equal(got_alive, want)
+    return sel, n_sel
+
+
+@pytest.mark.parametrize("which", ["tiny", "mid", "ties", "fewcand"])
+def test_select_bitexact_on_same_scores(which):
+    if which == "fewcand":     # fewer candidates than the budgets
+        w = gen.sparse_workload(2, 8, 2, 64 * 5 + 3, 8, 8, seed=2)
+    elif which == "tiny":
+        w = gen.tiny()
+    else:
+        w = gen.sparse_workload(4, 32, 8, 64 * 300 + 17, 24, 40, seed=11, outlier_p=0.01)
+    d = Dev(w)
+    s = d.scores()
+    e = w["evict"].copy()
+    if which == "ties":
+        s = torch.round(s * 2) / 2
+        e = np.round(e * 2) / 2
+        e[..., ::7] = -0.0
+        e[..., 3::7] = 0.0
+    alive = d.new_alive()
+    for step in range(3):
+        _check_select_bitexact(d, s, e, alive, w["k_q"], w["k_e"])
+        e = e + 0.3 * gen.normal_f32(1, 50 + step, e.size).reshape(e.shape)
+        if which == "ties":
+            e = np.round(e * 2) / 2
+    assert d.errors() == (0, 0)
+    d.close()
+
+
+def test_select_vs_oracle_scores_with_near_tie_rule():
+    w = gen.sparse_workload(4, 32, 8, 64 * 200 + 9, 16, 16, seed=13, outlier_p=0.01)
+    d = Dev(w)
+    sel, n_sel = d.select(d.scores(), f32(w["evict"]), d.new_alive(), w["k_q"], w["k_e"])
+    sel, n_sel = sel.cpu().numpy(), n_sel.cpu().numpy()
+    s_or = oracle.score_batch(w["q"], w["k_pool"], w["page_table"], w["seq_len"])
+    o_sel, o_n, o_alive = oracle.select_batch(s_or, w["evict"], np.ones(s_or.shape, np.uint8),
+                                              w["seq_len"], w["k_q"], w["k_e"])
+    local = (w["seq_len"] - 1) // 64
+    for b in range(w["B"]):
+        for h in range(w["Hk"]):
+            E = {p for p in range(local[b]) if o_alive[b, h, p]}
+            g = set(sel[b, h, :n_sel[b, h] - 1].tolist())
+            o = set(o_sel[b, h, :o_n[b, h] - 1].tolist())
+            assert E <= g, "eviction-head set ranks identical fp32 scores and must match"
+            cand = sorted((p for p in range(local[b]) if p not in E), key=lambda p: -s_or[b, h, p])
+            kth = s_or[b, h, cand[w["k_q"] - 1]]
+            for p in g ^ o:
+                assert abs(s_or[b, h, p] - kth) <= 1e-5 * abs(kth), (b, h, p)
+    d.close()
+
+
+# ------------------------------------------------------------------ sparse attention
+
+def _random_lists(w, rng, stride, lens=None):
+    B, Hk = w["B"], w["Hk"]
+    sel = np.full((B, Hk, stride), -1, np.int32)
+    n_sel = np.zeros((B, Hk), np.int32)
+    for b in range(B):
+        npg = (int(w["seq_len"][b]) + 63) // 64
+        for h in range(Hk):
+            n = int(rng.integers(0, min(stride, npg) + 1)) if lens is None else min(lens, npg)
+            pages = np.sort(rng.choice(npg, size=n, replace=False))
+            sel[b, h, :n] = pages
+            n_sel[b, h] = n
+    return sel, n_sel
+
+
+@pytest.mark.parametrize("B,Hq,Hk", [(1, 8, 2), (5, 16, 4), (3, 40, 8), (2, 16, 1), (4, 8, 8),
+                                     (2, 40, 4)])
+def test_sparse_attn_random_lists(B, Hq, Hk):
+    rng = np.random.default_rng(B * 100 + Hq + Hk)
+    w = gen.sparse_workload(B, Hq, Hk, 64 * 48, 8, 8, seed=B + Hq, outlier_p=0.01)
+    w["seq_len"] = rng.integers(1, 64 * 48 + 1, B).astype(np.int32)
+    w["seq_len"][0] = 64 * 48
+    d = Dev(w)
+    sel, n_sel = _random_lists(w, rng, stride=20)
+    out, lse = d.attn(i32(sel), i32(n_sel))
+    ro, rl = oracle.sparse_attn_batch(w["q"], w["k_pool"], w["v_pool"], w["page_table"], sel, n_sel,
+                                      w["seq_len"])
+    mx, mean = attn_errors(out.cpu().numpy(), ro)
+    assert mx <= ATTN_MAX and mean <= ATTN_MEAN, (mx, mean)
+    l = lse.cpu().numpy()
+    assert np.array_equal(np.isinf(l), np.isinf(rl))
+    fin = np.isfinite(rl)
+    assert np.abs(l[fin] - rl[fin]).max() <= LSE_TOL
+    assert d.errors() == (0, 0)
+    d.close()
+
+
+@pytest.mark.parametrize("B,n_pages", [(16, 65), (125, 2), (40, 33)])
+def test_sparse_attn_split_k_paths(B, n_pages):
+    """Units split over several CTAs (partial merge) and CTAs that cover many whole units."""
+    rng = np.random.default_rng(B)
+    w = gen.sparse_workload(B, 32, 8, 64 * 70 + 11, 8, 8, seed=B)
+    d = Dev(w, max_units=B * 8)
+    sel, n_sel = _random_lists(w, rng, stride=n_pages, lens=n_pages)
+    out, lse = d.attn(i32(sel), i32(n_sel))
+    ro, rl = oracle.sparse_attn_batch(w["q"], w["k_pool"], w["v_pool"], w["page_table"], sel, n_sel,
+                                      w["seq_len"])
+    mx, mean = attn_errors(out.cpu().numpy(), ro)
+    assert mx <= ATTN_MAX and mean <= ATTN_MEAN, (mx, mean)
+    assert np.abs(lse.cpu().numpy() - rl).max() <= LSE_TOL
+    # a second call reuses the arrival counters: must give the same bits
+    out2, lse2 = d.attn(i32(sel), i32(n_sel))
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    assert d.errors() == (0, 0)
+    d.close()
+
+
+def test_attn_never_reads_rows_past_valid():
+    w = gen.sparse_workload(2, 8, 2, 64 * 10 - 20, 4, 4, seed=21)
+    local_phys = w["page_table"][:, 9]
+    w_nan = dict(w)
+    w_nan["k_pool"] = w["k_pool"].copy()
+    w_nan["v_pool"] = w["v_pool"].copy()
+    for b in range(2):
+        w_nan["k_pool"][:, local_phys[b], 44:] = 0x7FC0     # bf16 NaN
+        w_nan["v_pool"][:, local_phys[b], 44:] = 0x7FC0
+    d = Dev(w_nan)
+    sel = np.tile(np.arange(10, dtype=np.int32), (2, 2, 1))
+    n_sel = np.full((2, 2), 10, np.int32)
+    out, lse = d.attn(i32(sel), i32(n_sel))
+    o = out.cpu().numpy()
+    assert np.isfinite(o).all() and np.isfinite(lse.cpu().numpy()).all()
+    ro, rl = oracle.sparse_attn_batch(w["q"], w["k_pool"], w["v_pool"], w["page_table"], sel, n_sel,
+                                      w["seq_len"])
+    assert attn_errors(o, ro)[0] <= ATTN_MAX
+    d.close()
+
+
+def test_bad_device_ids_set_error_bits_without_fault():
+    w = gen.sparse_workload(2, 8, 2, 64 * 10, 4, 4, seed=22)
+    d = Dev(w)
+    sel = np.tile(np.arange(10, dtype=np.int32), (2, 2, 1))
+    sel[0, 1, 3] = 10 ** 6
+    sel[1, 0, 0] = -5
+    n_sel = np.full((2, 2), 10, np.int32)
+    out, lse = d.attn(i32(sel), i32(n_sel))
+    st, bits = d.errors()
+    assert st == -4 and bits & spkv.DEVERR["PAGE_ID"]
+    ro, rl = oracle.sparse_attn_batch(w["q"], w["k_pool"], w["v_pool"], w["page_table"], sel, n_sel,
+                                      w["seq_len"], units=np.array([0, 3]))
+    o = out.cpu().numpy()
+    assert attn_errors(o[0, :4], ro[0, :4])[0] <= ATTN_MAX      # unit 0 untouched by the bad ids
+    assert attn_errors(o[1, 4:], ro[1, 4:])[0] <= ATTN_MAX      # unit 3
+    assert d.errors() == (0, 0)                                  # the word was cleared
+    d.close()
+
+
+# ------------------------------------------------------------------ lazy RoPE attention
+
+def _lazy_dev(w):
+    k_pool, v_pool = bf(w["k_pool"]), bf(w["v_pool"])
+    ksum = torch.zeros(w["Hk"], w["n_phys"], 4, 128, dtype=torch.float32, device=DEV)
+    cache = spkv.paged_kv_create(k_pool, v_pool, ksum, i32(w["page_cnt"]))
+    return cache, (k_pool, v_pool, ksum)
+
+
+def _words(phys, valid, slot):
+    ok = phys >= 0
+    words = np.zeros(phys.shape, np.uint32)
+    words[ok] = spkv.pack_page_words(phys[ok], valid[ok], slot[ok])
+    return words
+
+
+@pytest.mark.parametrize("seed,Hq,Hk", [(1, 16, 4), (2, 32, 8), (3, 8, 1)])
+def test_lazy_rope_vs_materialised_oracle(seed, Hq, Hk):
+    w = gen.lazy_rag(seed=seed, B=6, Hq=Hq, Hk=Hk, n_docs=20, docs_per_req=4, min_len=100, max_len=2000)
+    cache, keep = _lazy_dev(w)
+    words = _words(w["phys"], w["valid"], w["slot"])
+    B = w["B"]
+    out = torch.empty(B, Hq, 128, dtype=torch.float32, device=DEV)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=DEV)
+    spkv.lazy_rope_decode_attn(cache, bf(w["q"]), i32(w["qpos"]), u32_as_i32(words), i32(w["n_pages"]),
+                               i32(w["doc_pos"]), w["theta"], out, lse)
+    ro, rl = oracle.lazy_attn_batch(w["q"], w["k_pool"], w["v_pool"], w["phys"], w["valid"], w["slot"],
+                                    w["n_pages"], w["qpos"], w["doc_pos"], w["theta"], materialise=True)
+    mx, mean = attn_errors(out.cpu().numpy(), ro)
+    assert mx <= ATTN_MAX and mean <= ATTN_MEAN, (mx, mean)
+    assert np.abs(lse.cpu().numpy() - rl).max() <= LSE_TOL
+    assert spkv.get_device_error(cache) == (0, 0)
+    cache.close()
+
+
+def test_lazy_rope_per_head_page_lists():
+    w = gen.lazy_rag(seed=4, B=3, Hq=16, Hk=4, n_docs=10, docs_per_req=3, min_len=64, max_len=1500)
+    rng = np.random.default_rng(0)
+    B, Hk, npm = w["B"], w["Hk"], w["np_max"]
+    phys = np.full((B, Hk, npm), -1, np.int32)
+    valid = np.zeros((B, Hk, npm), np.int32)
+    slot = np.zeros((B, Hk, npm), np.int32)
+    n_pages = np.zeros(B, np.int32)
+    for b in range(B):
+        n = int(w["n_pages"][b])
+        keep = n // 2
+        n_pages[b] = keep
+        for h in range(Hk):
+            idx = np.sort(rng.choice(n, size=keep, replace=False))
+            phys[b, h, :keep] = w["phys"][b, idx]
+            valid[b, h, :keep] = w["valid"][b, idx]
+            slot[b, h, :keep] = w["slot"][b, idx]
+    cache, keep_alive = _lazy_dev(w)
+    words = _words(phys, valid, slot)
+    out = torch.empty(B, w["Hq"], 128, dtype=torch.float32, device=DEV)
+    lse = torch.empty(B, w["Hq"], dtype=torch.float32, device=DEV)
+    spkv.lazy_rope_decode_attn(cache, bf(w["q"]), i32(w["qpos"]), u32_as_i32(words), i32(n_pages),
+                               i32(w["doc_pos"]), w["theta"], out, lse)
+    ro, rl = oracle.lazy_attn_batch(w["q"], w["k_pool"], w["v_pool"], phys, valid, slot, n_pages,
+                                    w["qpos"], w["doc_pos"], w["theta"], materialise=True)
+    mx, mean = attn_errors(out.cpu().numpy(), ro)
+    assert mx <= ATTN_MAX and mean <= ATTN_MEAN, (mx, mean)
+    cache.close()
+
+
+# ------------------------------------------------------------------ residency bookkeeping
+
+@pytest.mark.parametrize("W", [1, 2])
+def test_setdiff_and_lru_trajectory_bitexact(W):
+    rng = np.random.default_rng(W)
+    U, n_slots, stride = 6, 64, 9
+    w = gen.tiny()
+    d = Dev(w)
+    resident = np.full((U, n_slots), -1, np.int32)
+    ts = np.full((U, n_slots), np.iinfo(np.int32).min, np.int32)
+    r_dev, t_dev = i32(resident), i32(ts)
+    for t in range(40):
+        sel = np.full((U, stride), -1, np.int32)
+        n_sel = np.zeros(U, np.int32)
+        for u in range(U):
+            n = int(rng.integers(0, stride + 1))
+            sel[u, :n] = np.sort(rng.choice(150, size=n, replace=False))
+            n_sel[u] = n
+        miss = torch.empty(U, stride, dtype=torch.int32, device=DEV)
+        nm = torch.empty(U, dtype=torch.int32, device=DEV)
+        slot = torch.empty(U, stride, dtype=torch.int32, device=DEV)
+        spkv.resident_setdiff(d.cache, r_dev, i32(sel), i32(n_sel), miss, nm, slot)
+        o_miss, o_nm, o_slot = oracle.setdiff_batch(resident, sel, n_sel)
+        assert np.array_equal(miss.cpu().numpy(), o_miss)
+        assert np.array_equal(nm.cpu().numpy(), o_nm)
+        assert np.array_equal(slot.cpu().numpy(), o_slot)
+        vic = torch.empty(U, stride, dtype=torch.int32, device=DEV)
+        hist = torch.empty(U, 64, dtype=torch.int32, device=DEV)
+        spkv.lru_bucket_update(d.cache, r_dev, t_dev, slot, i32(n_sel), miss, nm, t, W, vic, hist)
+        resident, ts, o_vic, o_hist = oracle.lru_batch(resident, ts, o_slot, n_sel, o_miss, o_nm, t, W)
+        assert np.array_equal(vic.cpu().numpy(), o_vic)
+        assert np.array_equal(hist.cpu().numpy(), o_hist)
+        assert np.array_equal(r_dev.cpu().numpy(), resident)
+        assert np.array_equal(t_dev.cpu().numpy(), ts)
+    assert d.errors() == (0, 0)
+    d.close()

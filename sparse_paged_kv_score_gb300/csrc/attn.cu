@@ -220,7 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int bc = __shfl_sync(0xffffffffu, my_uc, i);
         const int bh = __shfl_sync(0xffffffffu, head, i);
         if (jl >= STAGES) {
-          if (!mbar_wait(&S.empty[s], ((jl / STAGES) - 1) & 1)) {
+          // warp-uniform outcome even if lanes disagree at the time limit
+          if (!__all_sync(0xffffffffu, mbar_wait(&S.empty[s], ((jl / STAGES) - 1) & 1))) {
             if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
             ok = false;
             break;
@@ -424,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t stage0 = smem_u32(stages);
   for (int jl = 0; jl < n_local; ++jl) {
     const int s = jl % STAGES;
-    if (!mbar_wait(&S.full[s], (jl / STAGES) & 1)) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&S.full[s], (jl / STAGES) & 1))) {
       if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
       break;
     }

@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-lazy", action="store_true")
+    ap.add_argument("--batch", type=int, default=32,
+                    help="requests per step (32 = the Llama-3-8B-layer workload; smaller for profiling)")
     return ap.parse_args()
 
 
@@ -196,7 +198,7 @@ def run_native(args):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
 
-    w = gen.llama8b(seed=rank)
+    w = gen.llama8b(seed=rank, B=args.batch)
     B, Hq, Hk, npm = w["B"], w["Hq"], w["Hk"], w["np_max"]
     k_q, k_e = w["k_q"], w["k_e"]
     k = k_q + k_e
@@ -401,7 +403,7 @@ def run_native(args):
         units = np.arange(U, dtype=np.int32)
         dt, sb, thr = oracle_sample(w, units)
         cpu = {"value": sb / dt / 1e9, "unit": UNIT, "cores": thr, "kind": "oracle",
-               "sample": "one full step (all 256 units): score_blocks + select_topk + attention, fp64",
+               "sample": f"one full step (all {U} units): score_blocks + select_topk + attention, fp64",
                "ms_per_step": dt * 1e3}
 
     cache.close()

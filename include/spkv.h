@@ -211,6 +211,34 @@ int lru_bucket_update(spkv_cache_t cache, int32_t* resident, int32_t* ts, int n_
                       const int32_t* n_missing, int sel_stride, int n_units, int32_t t_now,
                       int bucket_width, int32_t* victims, int32_t* hist, void* stream);
 
+/* sparse_decode_attn without any allocation.  The pages this library follows have no
+ * counterpart for this entry point: it exists for callers that cannot allocate device memory
+ * (an engine that forbids cudaMalloc after start-up or owns all device memory through its own
+ * allocator, or code that must not create a handle, since paged_kv_create allocates).  It
+ * computes exactly what sparse_decode_attn computes, with the same kernel, but takes the pool
+ * directly instead of a handle and keeps its split-K scratch (partial results and arrival
+ * counters) in one fixed device array of SPKV_NOALLOC_SCRATCH_BYTES bytes that every GPU
+ * loading this library holds until the process exits.  The caller passes inputs and outputs.
+ *   k_pool, v_pool : device bf16 [n_kv_heads][n_phys_pages][64][128], 16-byte aligned
+ *   dev_err        : device uint32, receives SPKV_DEVERR_* bits (OR-ed in); may be NULL, in
+ *                    which case the bits go to a word inside the scratch that is not reported
+ *   other arguments: as sparse_decode_attn.
+ * Limits: B * n_kv_heads <= SPKV_NOALLOC_MAX_UNITS and Hq / n_kv_heads <= 16; larger calls
+ * return SPKV_EUNSUPPORTED before anything is launched.  No cudaMalloc, cudaFree or other
+ * allocating routine is called.  The first call on a device looks up the scratch's device
+ * address with that device current, so make it before any stream capture.  All calls on a
+ * device share the scratch, which keeps the last call's contents: each call clears the arrival
+ * counters (and the fallback error word) first, and calls whose kernels overlap on the GPU
+ * (unordered streams) race on it and must not be issued. */
+#define SPKV_NOALLOC_MAX_UNITS 512
+#define SPKV_NOALLOC_MAX_CTAS 160
+#define SPKV_NOALLOC_SCRATCH_BYTES 5593344
+int sparse_decode_attn_noalloc(const void* k_pool, const void* v_pool, int n_kv_heads,
+                               int64_t n_phys_pages, const void* q, int B, int Hq,
+                               const int32_t* page_table, int np_max, const int32_t* sel,
+                               const int32_t* n_sel, int sel_stride, const int32_t* seq_len,
+                               float* out, float* lse, uint32_t* dev_err, void* stream);
+
 /* Packs page words for lazy_rope_decode_attn on the host ([Lazy] "Technical implementation
  * 2. Decoding", bit-packed block id and offset):
  *   word = phys | (valid - 1) << 18 | doc_slot << 24,

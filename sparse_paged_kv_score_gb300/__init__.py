@@ -25,7 +25,8 @@ from ._abi import DEVERR, SpkvDesc, SpkvError, check, load
 
 __all__ = ["PagedKVCache", "paged_kv_create", "paged_kv_append", "score_blocks", "select_topk",
            "sparse_decode_attn", "lazy_rope_decode_attn", "resident_setdiff", "lru_bucket_update",
-           "pack_page_words", "get_device_error", "SpkvError", "DEVERR", "load"]
+           "sparse_decode_attn_noalloc", "pack_page_words", "get_device_error", "SpkvError", "DEVERR",
+           "load"]
 
 HEAD_DIM, PAGE, SUBBLOCK = 128, 64, 16
 
@@ -134,6 +135,31 @@ def sparse_decode_attn(cache: PagedKVCache, q, page_table, sel, n_sel, seq_len, 
         _t(n_sel, torch.int32, "n_sel", (B, cache.n_kv_heads)), stride,
         _t(seq_len, torch.int32, "seq_len", (B,)), _t(out, torch.float32, "out", (B, Hq, HEAD_DIM)),
         _t(lse, torch.float32, "lse", (B, Hq)), _stream(stream)))
+
+
+def sparse_decode_attn_noalloc(k_pool, v_pool, q, page_table, sel, n_sel, seq_len, out, lse, dev_err=None,
+                               stream=None):
+    """sparse_decode_attn for callers that cannot allocate device memory.
+
+    No handle and no allocation: the pool is passed directly and the split-K scratch is a
+    fixed device array inside the library (SPKV_NOALLOC_SCRATCH_BYTES per GPU, held until the
+    process exits).  At most 512 (request, kv head) units per call.  Calls on one device share
+    that scratch, so they must not overlap on the GPU.  ``dev_err`` is an optional int32 device
+    tensor of one element that receives the device error bits.
+    """
+    Hk, n_phys = k_pool.shape[0], k_pool.shape[1]
+    shp = (Hk, n_phys, PAGE, HEAD_DIM)
+    B, Hq = q.shape[0], q.shape[1]
+    np_max = page_table.shape[1]
+    stride = sel.shape[2]
+    err = None if dev_err is None else _t(dev_err, torch.int32, "dev_err", (1,))
+    check("sparse_decode_attn_noalloc", load().sparse_decode_attn_noalloc(
+        _t(k_pool, torch.bfloat16, "k_pool", shp), _t(v_pool, torch.bfloat16, "v_pool", shp), Hk, n_phys,
+        _t(q, torch.bfloat16, "q", (B, Hq, HEAD_DIM)), B, Hq,
+        _t(page_table, torch.int32, "page_table", (B, np_max)), np_max,
+        _t(sel, torch.int32, "sel", (B, Hk, stride)), _t(n_sel, torch.int32, "n_sel", (B, Hk)), stride,
+        _t(seq_len, torch.int32, "seq_len", (B,)), _t(out, torch.float32, "out", (B, Hq, HEAD_DIM)),
+        _t(lse, torch.float32, "lse", (B, Hq)), err, _stream(stream)))
 
 
 def lazy_rope_decode_attn(cache: PagedKVCache, q, qpos, meta, n_pages, doc_pos, theta: float, out, lse,

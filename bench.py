@@ -59,6 +59,21 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def measured_traffic():
+    """DRAM bytes per full attention launch from the committed ncu summary, or None when the
+    kernel source has changed since those counters were taken."""
+    import hashlib
+    import re
+    prof = os.path.join(ROOT, "profiles", "attn_split_kernel_llama8b_B8_full.md")
+    src = os.path.join(ROOT, "sparse_paged_kv_score_gb300", "csrc", "attn.cu")
+    if not (os.path.exists(prof) and os.path.exists(src)):
+        return None
+    m = re.search(r"bench-traffic: attn.cu=([0-9a-f]+) traffic_bytes_per_launch=(\d+)", open(prof).read())
+    if not m or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != m.group(1):
+        return None
+    return int(m.group(2))
+
+
 def step_bytes(w, k):
     """Algorithmic bytes of one step (one read of every operand, one write of every result)."""
     B, Hk, Hq, npm = w["B"], w["Hk"], w["Hq"], w["np_max"]
@@ -423,7 +438,8 @@ def run_native(args):
             "roofline": {"kernel": "sparse_decode_attn (attn_split_kernel)", "bound": "hbm",
                          "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "peak_kind": peak_kind, "us": attn_avg * 1e3,
-                         "bytes_per_launch": byts["attn_kv"], "traffic": None},
+                         "bytes_per_launch": byts["attn_kv"],
+                         "traffic": measured_traffic() if B == 32 else None},
             "lazy_attn": lazy,
             "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},

@@ -183,19 +183,25 @@ def nosa_traj(seed: int = 0, B: int = 16, steps: int = 64) -> dict:
     return w
 
 
-def traj_step_inputs(w: dict, t: int) -> dict:
+def traj_step_inputs(w: dict, t: int, prev_evict=None) -> dict:
     """Inputs that step t of a decode trajectory consumes.
 
-    The eviction scores follow a random walk (step std 0.1) starting from ``w['evict']``; the
-    query is fresh N(0,1); one new K and V row per (request, kv head) is appended.
+    The eviction scores follow a random walk (step std 0.1) starting from ``w['evict']``: pass the
+    previous step's scores as ``prev_evict`` (None at t = 0 or to replay the walk from the start).
+    The query is fresh N(0,1); one new K and V row per (request, kv head) is appended.
     """
     B, Hk, Hq, npm = w["B"], w["Hk"], w["Hq"], w["np_max"]
     seed = w["seed"]
-    e = w["evict"].astype(np.float64).copy()
-    for s in range(t + 1):
+    if prev_evict is None:
+        e = w["evict"].astype(np.float64).copy()
+        first = 0
+    else:
+        e = np.asarray(prev_evict, np.float64).copy()
+        first = t
+    for s in range(first, t + 1):
         e += normal_f64(seed, TAG_STEP_E + s, B * Hk * npm).reshape(B, Hk, npm) * 0.1
     return dict(
-        evict=e.astype(np.float32),
+        evict=e,
         q=rows_bf16(seed, TAG_STEP_Q + t, B * Hq).reshape(B, Hq, HEAD_DIM),
         k_new=rows_bf16(seed, TAG_STEP_K + t, B * Hk).reshape(B, Hk, HEAD_DIM),
         v_new=rows_bf16(seed, TAG_STEP_V + t, B * Hk).reshape(B, Hk, HEAD_DIM),

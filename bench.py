@@ -262,17 +262,13 @@ def run_native(args):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step(i, ev_attn=None):
+    def step(i):
         spkv.paged_kv_append(cache, app_phys, app_tok, knew[i], vnew[i])
         spkv.score_blocks(cache, qs[i], pt, seq, scores)
         spkv.select_topk(cache, scores, evs[i], alive, seq, k_q, k_e, sel, n_sel)
         spkv.resident_setdiff(cache, resident, sel, n_sel, missing, n_missing, slot)
         spkv.lru_bucket_update(cache, resident, ts, slot, n_sel.view(U), missing, n_missing, i, 1, victims, hist)
-        if ev_attn:
-            ev_attn[0].record(stream)
         spkv.sparse_decode_attn(cache, qs[i], pt, sel, n_sel, seq, out, lse)
-        if ev_attn:
-            ev_attn[1].record(stream)
 
     def barrier():
         torch.cuda.synchronize()
@@ -281,6 +277,19 @@ def run_native(args):
             dist.barrier()
             torch.cuda.synchronize()
 
+    def timed(fn, idx):
+        """Device time (ms) of fn(i) for i in idx, each bracketed by events, L2 flushed between."""
+        ev = []
+        for i in idx:
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn(i)
+            b_.record(stream)
+            flush.zero_()
+            ev.append((a, b_))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b_) for a, b_ in ev]
+
     for i in range(args.warmup):
         step(i)
         flush.zero_()
@@ -288,21 +297,23 @@ def run_native(args):
     if st != 0:
         raise RuntimeError(f"device error bits {bits} after warm-up")
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    # one CUDA graph per timed step (each step has its own inputs and LRU time)
+    timed_idx = list(range(args.warmup, args.warmup + args.steps))
+    graphs = {}
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    for i in timed_idx:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            step(i)
+        graphs[i] = g
+    torch.cuda.synchronize()
     barrier()
     with Clocks(local_rank) as clk:
-        for j in range(args.steps):
-            i = args.warmup + j
-            e0, ea0, ea1, e1 = ev[j]
-            e0.record(stream)
-            step(i, (ea0, ea1))
-            e1.record(stream)
-            flush.zero_()           # L2 flush between timed steps (outside the events)
+        step_ms = timed(lambda i: graphs[i].replay(), timed_idx)
         barrier()
-    step_ms = [a.elapsed_time(b) for a, _, _, b in ev]
-    attn_ms = [a.elapsed_time(b) for _, a, b, _ in ev]
+    eager_ms = statistics.mean(timed(step, timed_idx))
+    attn_ms = timed(lambda i: spkv.sparse_decode_attn(cache, qs[i], pt, sel, n_sel, seq, out, lse), timed_idx)
     ms = statistics.mean(step_ms)
     if world > 1:
         import torch.distributed as dist
@@ -340,19 +351,12 @@ def run_native(args):
         qpos = i32(np.full(B, L - 1, np.int32))
         lout = torch.empty_like(out)
         llse = torch.empty_like(lse)
-        for i in range(3):
+
+        def lazy_call(i):
             spkv.lazy_rope_decode_attn(cache, qs[i], qpos, meta, n_pages, doc_pos, 500000.0, lout, llse)
-            flush.zero_()
-        lt = []
-        for j in range(args.steps):
-            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            spkv.lazy_rope_decode_attn(cache, qs[j], qpos, meta, n_pages, doc_pos, 500000.0, lout, llse)
-            b_.record(stream)
-            flush.zero_()
-            lt.append((a, b_))
-        torch.cuda.synchronize()
-        lazy_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in lt)
+
+        timed(lazy_call, range(3))
+        lazy_ms = statistics.mean(timed(lazy_call, timed_idx))
         lazy_gbs = byts["attn_kv"] / (lazy_ms * 1e-3) / 1e9
         lazy = {"kernel": "lazy_rope_decode_attn (same 65 pages/head as 8 docs x 4096 tokens)",
                 "us": lazy_ms * 1e3, "achieved_GBps": lazy_gbs, "frac": lazy_gbs / peak,
@@ -432,6 +436,7 @@ def run_native(args):
             "config": {"workload": w["name"], "batch": B, "q_heads": Hq, "kv_heads": Hk, "context": L,
                        "page": 64, "subblock": 16, "k_q": k_q, "k_e": k_e, "resident_slots": N_SLOTS,
                        "step": "append+score+select+setdiff+lru+sparse_attn",
+                       "launch": "one CUDA graph per step (kernels chained by programmatic dependent launch)",
                        "bytes_per_step": {kk: int(v) for kk, v in byts.items()},
                        "l2": "256 MiB write between timed steps; step inputs (~0.8 GB) exceed L2",
                        "parallelism": f"replicas x{world}"},
@@ -444,6 +449,7 @@ def run_native(args):
             "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": 7 * args.steps,
+            "eager_ms_per_step": eager_ms,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
         }

@@ -152,7 +152,7 @@ int select_topk(spkv_cache_t cache, const float* q_scores, const float* evict_sc
  *   lse[b][h*G+g]    = log sum_t exp(q . k_t / sqrt(128))          (natural log)
  * over the tokens of pages sel[u][0 .. n_sel[u]); page p holds min(64, seq_len[b] - 64 p)
  * valid tokens (rows past that are never read into the result, even if they hold NaN).
- *   q          : device bf16 [B][Hq][128]
+ *   q          : device bf16 [B][Hq][128], 16-byte aligned
  *   page_table : device int32 [B][np_max]
  *   sel, n_sel : device int32 [B][n_kv_heads][sel_stride], [B][n_kv_heads]
  *   seq_len    : device int32 [B]
@@ -170,7 +170,7 @@ int sparse_decode_attn(spkv_cache_t cache, const void* q, int B, int Hq, const i
  * a document slot i; with P_i = doc_pos[b][i] and n = qpos[b] the page's keys are scored with
  * R(n - P_i) q, where R is the half-split RoPE rotation over pairs (x_j, x_{j+64}) with
  * frequencies theta^(-2j/128).  Stored keys carry only their document-local rotation.
- *   q        : device bf16 [B][Hq][128], not rotated
+ *   q        : device bf16 [B][Hq][128], not rotated, 16-byte aligned
  *   qpos     : device int32 [B]
  *   meta     : device uint32 [B][meta_heads][np_max]; meta_heads is 1 (one page list shared
  *              by all kv heads) or n_kv_heads
@@ -220,6 +220,7 @@ int lru_bucket_update(spkv_cache_t cache, int32_t* resident, int32_t* ts, int n_
  * counters) in one fixed device array of SPKV_NOALLOC_SCRATCH_BYTES bytes that every GPU
  * loading this library holds until the process exits.  The caller passes inputs and outputs.
  *   k_pool, v_pool : device bf16 [n_kv_heads][n_phys_pages][64][128], 16-byte aligned
+ *   q              : device bf16 [B][Hq][128], 16-byte aligned
  *   dev_err        : device uint32, receives SPKV_DEVERR_* bits (OR-ed in); may be NULL, in
  *                    which case the bits go to a word inside the scratch that is not reported
  *   other arguments: as sparse_decode_attn.

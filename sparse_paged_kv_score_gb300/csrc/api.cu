@@ -78,6 +78,15 @@ void fill_common(AttnParams& p, spkv_cache_t c, const void* q, int B, int Hq, fl
 
 }  // namespace
 
+namespace spkv {
+cudaError_t init_kernel_attributes() {
+  cudaError_t e;
+  if ((e = attn_init_attributes()) != cudaSuccess) return e;
+  if ((e = select_init_attributes()) != cudaSuccess) return e;
+  return resid_init_attributes();
+}
+}  // namespace spkv
+
 extern "C" {
 
 const char* spkv_status_string(int s) {
@@ -114,6 +123,10 @@ int paged_kv_create(const spkv_desc* desc, void* stream, spkv_cache_t* out) {
     return SPKV_ECUDA;
   }
   c->attn_grid = c->sm_count;
+  if (spkv::init_kernel_attributes() != cudaSuccess) {
+    delete c;
+    return SPKV_ECUDA;
+  }
   if (!encode_pool(&c->tmap_k, d.k_pool, n_ph) || !encode_pool(&c->tmap_v, d.v_pool, n_ph)) {
     delete c;
     return SPKV_ECUDA;
@@ -188,7 +201,7 @@ int sparse_decode_attn(spkv_cache_t c, const void* q, int B, int Hq, const int32
   if (st != SPKV_OK) return st;
   if (B == 0) return SPKV_OK;
   if (!q || !page_table || !sel || !n_sel || !seq_len || !out || !lse || np_max <= 0 || sel_stride <= 0 ||
-      !aligned(q, 4))
+      !aligned(q, 16))
     return SPKV_EINVAL;
   AttnParams p;
   fill_common(p, c, q, B, Hq, out, lse);
@@ -210,7 +223,7 @@ int lazy_rope_decode_attn(spkv_cache_t c, const void* q, int B, int Hq, const in
   if (st != SPKV_OK) return st;
   if (B == 0) return SPKV_OK;
   if (!q || !qpos || !meta || !n_pages || !doc_pos || !out || !lse || np_max <= 0 || max_docs <= 0 ||
-      !aligned(q, 4))
+      !aligned(q, 16))
     return SPKV_EINVAL;
   if (meta_heads != 1 && meta_heads != c->d.n_kv_heads) return SPKV_EINVAL;
   if (!(theta > 1.0f) || !std::isfinite(theta)) return SPKV_EINVAL;

@@ -8,19 +8,25 @@
 // accumulator, O / l at the end; rowmax and l are kept and returned as LSE.  Lazy form:
 // [LazyAttention] "Technical implementation 2. Decoding" and "Mathematical equivalence".
 //
-// GB300 design (one CTA per SM, persistent):
+// GB300 design (one CTA per SM, persistent, six warps):
 //   * Work balance: the pages of all units form one sequence of T pages; CTA i takes pages
 //     [i*T/N, (i+1)*T/N).  A unit split over several CTAs leaves one fp32 partial
 //     (max, sum, unnormalised O) per CTA in a workspace slot (unit + cta); the last CTA to
 //     finish a unit (atomic arrival counter, no waiting) merges the partials.
-//   * Data movement: a producer warp streams each page's K and V (2 x 16 KiB, head-major, one
-//     contiguous page each) with TMA tensor loads (128B swizzle) into a ring of shared-memory
-//     stages, completed on mbarriers; consumers release stages on a second barrier.
-//   * Math: four consumer warps each take 16 of the 64 tokens of every page.  Q.K^T runs on
+//   * Producer warp: streams each page's K and V (2 x 16 KiB, head-major, one contiguous page
+//     each) with TMA tensor loads (128B swizzle) into a ring of shared-memory stages, and with
+//     the first page of each unit a bulk copy of that unit's query rows; all complete on the
+//     stage's mbarrier.  Consumers release stages on a second mbarrier.
+//   * Four consumer warps each take 16 of the 64 tokens of every page.  Q.K^T runs on
 //     mma.sync m16n8k16 with the 16 keys as M and the GQA group (padded to 8) as N, so the
-//     group of G <= 8 query heads shares one tensor-core tile; P^T goes from the accumulator
-//     layout to the B-operand layout with movmatrix; P.V runs with V^T (ldmatrix.trans) as A.
-//     P is split into bf16 hi + lo parts (two MMAs) so the weights keep ~17 bits.
+//     group of query heads shares one tensor-core tile; P^T goes from the accumulator layout to
+//     the B-operand layout with movmatrix; P.V runs with V^T (ldmatrix.trans) as A.  P (and the
+//     rotated lazy query) is split into bf16 hi + lo parts so the weights keep ~17 bits.
+//   * Epilogue warp: at each unit switch the consumers hand their (max, sum, O) to a shared
+//     buffer and go on streaming; the epilogue warp merges the four states, writes the output or
+//     the split-K partial, and does the cross-CTA merge, off the consumers' critical path.
+//   * Launched with programmatic dependent launch: barrier set-up overlaps the previous kernel;
+//     griddepcontrol.wait precedes the first read of its outputs.
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -30,13 +36,19 @@ namespace spkv {
 namespace {
 
 constexpr int kConsumers = 4;
-constexpr int kThreads = (kConsumers + 1) * 32;
+constexpr int kProducerWarp = kConsumers;
+constexpr int kEpilogueWarp = kConsumers + 1;
+constexpr int kThreads = (kConsumers + 2) * 32;
 constexpr int kBoxBytes = 8192;                // 64 tokens x 64 dims x bf16
-constexpr int kStageBytes = 4 * kBoxBytes;     // K (2 boxes) + V (2 boxes) of one page-head
+constexpr int kKVBytes = 4 * kBoxBytes;        // K (2 boxes) + V (2 boxes) of one page-head
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Stage: K/V page image, then room for the query rows of the unit it starts.
+template <int NT>
+__host__ __device__ constexpr int stage_bytes() { return kKVBytes + NT * 8 * kHeadDim * 2; }
+
 struct __align__(16) StageMeta {
-  int unit;     // unit of this page
+  int unit;     // unit of this page (-1: none)
   int valid;    // valid tokens (0 = skip the page)
   int rel;      // lazy: query position - document offset
   int ustart;   // position of the unit's first page in the global page sequence
@@ -47,21 +59,23 @@ struct __align__(16) StageMeta {
 template <int NT>
 struct Smem {
   static constexpr int kG = NT * 8;
-  // combine area (one per consumer warp)
+  // hand-off buffer from the consumer warps to the epilogue warp
   float cm[kConsumers][kG];
   float cl[kConsumers][kG];
   float co[kConsumers][kG][kHeadDim];
+  int h_unit, h_ustart, h_ucount, h_last;
   uint64_t full[8];
   uint64_t empty[8];
+  uint64_t cfull;     // consumers -> epilogue (count kConsumers)
+  uint64_t cempty;    // epilogue -> consumers (count 1)
   StageMeta meta[8];
   int scan[kThreads];
   int u0, p0;
-  int last;
 };
 
 template <int NT, int STAGES>
 constexpr size_t smem_bytes() {
-  return 1024 /*align slack*/ + size_t(STAGES) * kStageBytes + sizeof(Smem<NT>);
+  return 1024 /*align slack*/ + size_t(STAGES) * stage_bytes<NT>() + sizeof(Smem<NT>);
 }
 
 __device__ __forceinline__ int unit_count(const AttnParams& p, bool lazy, int u) {
@@ -88,19 +102,33 @@ template <int NT, bool LAZY, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                       const __grid_constant__ AttnParams p) {
+  constexpr int kStage = stage_bytes<NT>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Smem<NT>& S = *reinterpret_cast<Smem<NT>*>(stages + size_t(STAGES) * kStageBytes);
+  Smem<NT>& S = *reinterpret_cast<Smem<NT>*>(stages + size_t(STAGES) * kStage);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int U = p.B * p.Hk;
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], kConsumers);
+    }
+    mbar_init(&S.cfull, kConsumers);
+    mbar_init(&S.cempty, 1);
+    fence_mbar_init();
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+  }
+  pdl_wait();      // the page lists and counts below are written by the previous kernel
+  pdl_trigger();
 
   // ---- 1. global page sequence: T = sum of unit counts; find this CTA's first unit
   const int c0 = static_cast<int>(int64_t(tid) * U / kThreads);
   const int c1 = static_cast<int>(int64_t(tid + 1) * U / kThreads);
   int csum = 0;
   for (int u = c0; u < c1; ++u) csum += unit_count(p, LAZY, u);
-  // block exclusive scan of csum
   int x = csum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -141,20 +169,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc += n;
     }
   }
-  if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], kConsumers);
-    }
-    fence_mbar_init();
-  }
   __syncthreads();
   const int n_local = static_cast<int>(hi - lo);
+  const int qbytes = p.G * kHeadDim * 2;
 
-  if (warp == kConsumers) {
+  if (warp == kProducerWarp) {
     // ================================================================ producer warp
     int u = S.u0, ustart = S.p0, ucnt = unit_count(p, LAZY, u);
     const uint64_t pol = LAZY ? l2_policy_evict_normal() : l2_policy_evict_first();
+    int last_unit = -1;
     bool ok = true;
     for (int64_t j0 = lo; j0 < hi && ok; j0 += 32) {
       const int64_t xpos = j0 + lane;
@@ -236,24 +259,115 @@ __global__ void __launch_bounds__(kThreads, 1)
           m.ucount = bc;
           m.pad0 = m.pad1 = m.pad2 = 0;
           S.meta[s] = m;
-          if (bv > 0) {
-            mbar_arrive_expect_tx(&S.full[s], kStageBytes);
-            uint8_t* dst = stages + size_t(s) * kStageBytes;
-            const int z = static_cast<int>(int64_t(bh) * p.n_phys + bp);
-            tma_load_3d(dst, &tmk, &S.full[s], 0, 0, z, pol);
-            tma_load_3d(dst + kBoxBytes, &tmk, &S.full[s], 64, 0, z, pol);
-            tma_load_3d(dst + 2 * kBoxBytes, &tmv, &S.full[s], 0, 0, z, pol);
-            tma_load_3d(dst + 3 * kBoxBytes, &tmv, &S.full[s], 64, 0, z, pol);
+          uint8_t* dst = stages + size_t(s) * kStage;
+          const bool new_unit = bu >= 0 && bu != last_unit;
+          const uint32_t tx = (bv > 0 ? kKVBytes : 0) + (new_unit ? qbytes : 0);
+          if (tx) {
+            mbar_arrive_expect_tx(&S.full[s], tx);
+            if (new_unit) {
+              const int b = bu / p.Hk, h = bu % p.Hk;
+              bulk_load(dst + kKVBytes,
+                        static_cast<const uint8_t*>(p.q) + (int64_t(b) * p.Hq + h * p.G) * (kHeadDim * 2),
+                        qbytes, &S.full[s]);
+            }
+            if (bv > 0) {
+              const int z = static_cast<int>(int64_t(bh) * p.n_phys + bp);
+              tma_load_3d(dst, &tmk, &S.full[s], 0, 0, z, pol);
+              tma_load_3d(dst + kBoxBytes, &tmk, &S.full[s], 64, 0, z, pol);
+              tma_load_3d(dst + 2 * kBoxBytes, &tmv, &S.full[s], 0, 0, z, pol);
+              tma_load_3d(dst + 3 * kBoxBytes, &tmv, &S.full[s], 64, 0, z, pol);
+            }
           } else {
             mbar_arrive(&S.full[s]);
           }
+          if (bu >= 0) last_unit = bu;
         }
         __syncwarp();
       }
     }
-    // Before leaving, make sure no TMA copy issued by this CTA is still in flight.
+    // Before leaving, make sure no copy issued by this CTA is still in flight.
     const int first = n_local > STAGES ? n_local - STAGES : 0;
     for (int jl = first; jl < n_local; ++jl) mbar_wait(&S.full[jl % STAGES], (jl / STAGES) & 1);
+    return;
+  }
+
+  if (warp == kEpilogueWarp) {
+    // ================================================================ epilogue warp
+    for (int k = 0;; ++k) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&S.cfull, k & 1))) {
+        if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
+        break;
+      }
+      const int u = S.h_unit, ustart = S.h_ustart, ucount = S.h_ucount, last = S.h_last;
+      if (u >= 0) {
+        const int b = u / p.Hk, h = u % p.Hk;
+        const int first = cta_of(ustart, T, N);
+        const int nparts = cta_of(int64_t(ustart) + ucount - 1, T, N) - first + 1;
+        const int64_t orow = int64_t(b) * p.Hq + h * p.G;
+        const int64_t slot = int64_t(u) + blockIdx.x;
+        for (int g = 0; g < p.G; ++g) {
+          float M = -CUDART_INF_F;
+#pragma unroll
+          for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, S.cm[w][g]);
+          float fw[kConsumers], L = 0.f;
+#pragma unroll
+          for (int w = 0; w < kConsumers; ++w) {
+            const float mw = S.cm[w][g];
+            fw[w] = mw == -CUDART_INF_F ? 0.f : exp2f(mw - M);
+            L += fw[w] * S.cl[w][g];
+          }
+#pragma unroll
+          for (int i = 0; i < kHeadDim / 32; ++i) {
+            const int d = lane + 32 * i;
+            float acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumers; ++w) acc += fw[w] * S.co[w][g][d];
+            if (nparts == 1) p.out[(orow + g) * kHeadDim + d] = L > 0.f ? acc / L : 0.f;
+            else p.ws_o[(slot * 16 + g) * kHeadDim + d] = acc;
+          }
+          if (lane == 0) {
+            if (nparts == 1) {
+              p.lse[orow + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
+            } else {
+              p.ws_m[slot * 16 + g] = M;
+              p.ws_l[slot * 16 + g] = L;
+            }
+          }
+        }
+        if (nparts > 1) {
+          __threadfence();
+          __syncwarp();
+          int lastcta = 0;
+          if (lane == 0) lastcta = atomicAdd(&p.ws_cnt[u], 1) == nparts - 1;
+          lastcta = __shfl_sync(0xffffffffu, lastcta, 0);
+          if (lastcta) {
+            __threadfence();
+            for (int g = 0; g < p.G; ++g) {
+              float M = -CUDART_INF_F;
+              for (int i = 0; i < nparts; ++i) M = fmaxf(M, __ldcg(&p.ws_m[(int64_t(u) + first + i) * 16 + g]));
+              float L = 0.f, acc[kHeadDim / 32] = {};
+              for (int i = 0; i < nparts; ++i) {
+                const int64_t sl = int64_t(u) + first + i;
+                const float mw = __ldcg(&p.ws_m[sl * 16 + g]);
+                const float f = mw == -CUDART_INF_F ? 0.f : exp2f(mw - M);
+                L += f * __ldcg(&p.ws_l[sl * 16 + g]);
+#pragma unroll
+                for (int j = 0; j < kHeadDim / 32; ++j)
+                  acc[j] += f * __ldcg(&p.ws_o[(sl * 16 + g) * kHeadDim + lane + 32 * j]);
+              }
+#pragma unroll
+              for (int j = 0; j < kHeadDim / 32; ++j)
+                p.out[(orow + g) * kHeadDim + lane + 32 * j] = L > 0.f ? acc[j] / L : 0.f;
+              if (lane == 0) p.lse[orow + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
+            }
+            if (lane == 0) p.ws_cnt[u] = 0;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.cempty);
+      if (last) break;
+    }
     return;
   }
 
@@ -267,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t qh[8][NT][2];                  // B fragments of q (bf16 hi part)
   uint32_t ql[LAZY ? 8 : 1][NT][2];       // lazy: bf16 lo part of the rotated query
   uint32_t qraw[LAZY ? 8 : 1][NT][2];     // lazy: unrotated query
-  int cur_u = -1, cur_us = 0, cur_uc = 0, cur_rel = 0;
+  int cur_u = -1, cur_us = 0, cur_uc = 0, cur_rel = 0, n_flush = 0;
   bool have_rel = false;
 
   auto reset_state = [&]() {
@@ -282,14 +396,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
-  auto load_q = [&](int u) {
-    const int b = u / p.Hk, h = u % p.Hk;
-    const uint32_t* qw = reinterpret_cast<const uint32_t*>(p.q);
+  // q fragments from the stage's query rows (rows g >= G read as zero).
+  auto load_q = [&](const uint8_t* qs) {
+    const uint32_t* qw = reinterpret_cast<const uint32_t*>(qs);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int g = nt * 8 + r;
       const bool live = g < p.G;
-      const int64_t row = (int64_t(b) * p.Hq + h * p.G + (live ? g : 0)) * (kHeadDim / 2);
+      const int row = (live ? g : 0) * (kHeadDim / 2);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const uint32_t w0 = live ? qw[row + ks * 8 + c] : 0u;
@@ -341,8 +455,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
-  // Merge the four warps' states for unit u and write the result or a split-K partial.
-  auto flush = [&](int u, int ustart, int ucount) {
+  // Hands this warp's state for unit u to the epilogue warp (which merges the four warps).
+  auto flush = [&](int u, int ustart, int ucount, int last) {
+    if (n_flush > 0) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&S.cempty, (n_flush - 1) & 1))) {
+        if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
+      }
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -363,62 +482,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           S.co[warp][nt * 8 + 2 * c + (e & 1)][16 * j + r + ((e >> 1) << 3)] = O[j][nt][e];
-    named_bar_sync(1, kConsumers * 32);
-
-    const int b = u / p.Hk, h = u % p.Hk;
-    const int d = tid;  // 0..127
-    const int first = cta_of(ustart, T, N);
-    const int nparts = cta_of(int64_t(ustart) + ucount - 1, T, N) - first + 1;
-    const int64_t orow = int64_t(b) * p.Hq + h * p.G;
-    const int64_t slot = int64_t(u) + blockIdx.x;
-    for (int g = 0; g < p.G; ++g) {
-      float M = -CUDART_INF_F;
-#pragma unroll
-      for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, S.cm[w][g]);
-      float L = 0.f, acc = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumers; ++w) {
-        const float mw = S.cm[w][g];
-        const float fw = mw == -CUDART_INF_F ? 0.f : exp2f(mw - M);
-        L += fw * S.cl[w][g];
-        acc += fw * S.co[w][g][d];
-      }
-      if (nparts == 1) {
-        p.out[(orow + g) * kHeadDim + d] = L > 0.f ? acc / L : 0.f;
-        if (d == 0) p.lse[orow + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
-      } else {
-        p.ws_o[(slot * 16 + g) * kHeadDim + d] = acc;
-        if (d == 0) {
-          p.ws_m[slot * 16 + g] = M;
-          p.ws_l[slot * 16 + g] = L;
-        }
-      }
+    if (warp == 0 && lane == 0) {
+      S.h_unit = u;
+      S.h_ustart = ustart;
+      S.h_ucount = ucount;
+      S.h_last = last;
     }
-    if (nparts > 1) {
-      __threadfence();
-      named_bar_sync(1, kConsumers * 32);
-      if (tid == 0) S.last = (atomicAdd(&p.ws_cnt[u], 1) == nparts - 1);
-      named_bar_sync(1, kConsumers * 32);
-      if (S.last) {
-        __threadfence();
-        for (int g = 0; g < p.G; ++g) {
-          float M = -CUDART_INF_F;
-          for (int i = 0; i < nparts; ++i) M = fmaxf(M, __ldcg(&p.ws_m[(int64_t(u) + first + i) * 16 + g]));
-          float L = 0.f, acc = 0.f;
-          for (int i = 0; i < nparts; ++i) {
-            const int64_t sl = int64_t(u) + first + i;
-            const float mw = __ldcg(&p.ws_m[sl * 16 + g]);
-            const float fw = mw == -CUDART_INF_F ? 0.f : exp2f(mw - M);
-            L += fw * __ldcg(&p.ws_l[sl * 16 + g]);
-            acc += fw * __ldcg(&p.ws_o[(sl * 16 + g) * kHeadDim + d]);
-          }
-          p.out[(orow + g) * kHeadDim + d] = L > 0.f ? acc / L : 0.f;
-          if (d == 0) p.lse[orow + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
-        }
-        if (tid == 0) p.ws_cnt[u] = 0;
-      }
-    }
-    named_bar_sync(1, kConsumers * 32);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.cfull);
+    ++n_flush;
   };
 
   reset_state();
@@ -436,12 +508,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       continue;
     }
     if (mt.unit != cur_u) {
-      if (cur_u >= 0) flush(cur_u, cur_us, cur_uc);
+      if (cur_u >= 0) flush(cur_u, cur_us, cur_uc, 0);
       cur_u = mt.unit;
       cur_us = mt.ustart;
       cur_uc = mt.ucount;
       reset_state();
-      load_q(cur_u);
+      load_q(stages + size_t(s) * kStage + kKVBytes);
       have_rel = false;
     }
     if (mt.valid > t0) {
@@ -450,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         cur_rel = mt.rel;
         have_rel = true;
       }
-      const uint32_t kb = stage0 + s * kStageBytes;
+      const uint32_t kb = stage0 + s * kStage;
       const uint32_t vb = kb + 2 * kBoxBytes;
       // ---- S^T = K q^T for my 16 keys
       float acc[NT][4];
@@ -534,31 +606,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.empty[s]);
   }
-  if (cur_u >= 0) flush(cur_u, cur_us, cur_uc);
+  // the last hand-off ends the epilogue warp (unit -1 when this warp saw no page)
+  flush(cur_u, cur_us, cur_uc, 1);
+}
+
+template <int NT, bool LAZY, int STAGES>
+cudaError_t set_attr() {
+  return cudaFuncSetAttribute(attn_split_kernel<NT, LAZY, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(smem_bytes<NT, STAGES>()));
 }
 
 template <int NT, bool LAZY, int STAGES>
 cudaError_t launch_one(const spkv_cache* c, const AttnParams& p, int grid, cudaStream_t st) {
-  auto kern = attn_split_kernel<NT, LAZY, STAGES>;
-  const size_t smem = smem_bytes<NT, STAGES>();
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, st>>>(c->tmap_k, c->tmap_v, p);
-  return cudaGetLastError();
+  return launch_pdl(attn_split_kernel<NT, LAZY, STAGES>, dim3(grid), dim3(kThreads), smem_bytes<NT, STAGES>(), st,
+                    c->tmap_k, c->tmap_v, p);
 }
+
+constexpr int kStages1 = 6;   // G <= 8: 6 stages of 34 KiB
+constexpr int kStages2 = 5;   // G <= 16: 5 stages of 36 KiB
 
 }  // namespace
 
+cudaError_t attn_init_attributes() {
+  cudaError_t e;
+  if ((e = set_attr<1, false, kStages1>()) != cudaSuccess) return e;
+  if ((e = set_attr<1, true, kStages1>()) != cudaSuccess) return e;
+  if ((e = set_attr<2, false, kStages2>()) != cudaSuccess) return e;
+  return set_attr<2, true, kStages2>();
+}
+
 size_t attn_smem_bytes(int G, bool lazy) {
   (void)lazy;
-  return G <= 8 ? smem_bytes<1, 6>() : smem_bytes<2, 5>();
+  return G <= 8 ? smem_bytes<1, kStages1>() : smem_bytes<2, kStages2>();
 }
 
 cudaError_t launch_attn(const spkv_cache* c, const AttnParams& p, bool lazy, int grid, cudaStream_t st) {
   if (p.G <= 8) {
-    return lazy ? launch_one<1, true, 6>(c, p, grid, st) : launch_one<1, false, 6>(c, p, grid, st);
+    return lazy ? launch_one<1, true, kStages1>(c, p, grid, st) : launch_one<1, false, kStages1>(c, p, grid, st);
   }
-  return lazy ? launch_one<2, true, 5>(c, p, grid, st) : launch_one<2, false, 5>(c, p, grid, st);
+  return lazy ? launch_one<2, true, kStages2>(c, p, grid, st) : launch_one<2, false, kStages2>(c, p, grid, st);
 }
 
 }  // namespace spkv

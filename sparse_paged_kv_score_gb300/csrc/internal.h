@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/spkv.h"
 
 struct spkv_cache {
@@ -24,6 +26,29 @@ struct spkv_cache {
 };
 
 namespace spkv {
+
+// Launches `k` with programmatic stream serialisation: the kernel may start while the previous
+// kernel of the stream finishes; every kernel of this library calls pdl_wait() before it reads
+// anything an earlier kernel wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
+}
+
+// Sets the dynamic shared-memory limits of every kernel once (at handle creation), so that no
+// launch path calls cudaFuncSetAttribute and every call can be captured in a CUDA graph.
+cudaError_t init_kernel_attributes();
 
 // Parameters of the split-K attention kernel (sparse and lazy forms).
 struct AttnParams {
@@ -74,5 +99,8 @@ cudaError_t launch_lru(uint32_t* err, int32_t* resident, int32_t* ts, int n_slot
 
 // Shared-memory bytes the attention kernel needs for a group size (used for limits checks).
 size_t attn_smem_bytes(int G, bool lazy);
+cudaError_t attn_init_attributes();
+cudaError_t select_init_attributes();
+cudaError_t resid_init_attributes();
 
 }  // namespace spkv

@@ -51,13 +51,16 @@ namespace {
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
 
-// Device address of g_noalloc_scratch on `dev` (looked up once per device, `dev` current).
+// Device address of g_noalloc_scratch on `dev` (looked up once per device, `dev` current); the
+// same first call sets the attention kernel's shared-memory limit on that device.
 cudaError_t scratch_address(int dev, unsigned char** out) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_addr[dev]) {
+    cudaError_t e = spkv::attn_init_attributes();
+    if (e != cudaSuccess) return e;
     void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
     if (!p) return cudaErrorInvalidSymbol;
     g_addr[dev] = p;
@@ -102,7 +105,7 @@ extern "C" int sparse_decode_attn_noalloc(const void* k_pool, const void* v_pool
     return SPKV_EINVAL;
   if (Hq % n_kv_heads != 0) return SPKV_EINVAL;
   if ((reinterpret_cast<uintptr_t>(k_pool) | reinterpret_cast<uintptr_t>(v_pool)) % 16 != 0 ||
-      reinterpret_cast<uintptr_t>(q) % 4 != 0)
+      reinterpret_cast<uintptr_t>(q) % 16 != 0)
     return SPKV_EINVAL;
   const int G = Hq / n_kv_heads;
   const int64_t n_ph = int64_t(n_kv_heads) * n_phys_pages;

@@ -45,6 +45,8 @@ __global__ void __launch_bounds__(kSdThreads)
                    const int32_t* __restrict__ n_sel, int stride, int32_t* __restrict__ missing,
                    int32_t* __restrict__ n_missing, int32_t* __restrict__ slot, uint32_t* err) {
   extern __shared__ int32_t sd[];
+  pdl_wait();
+  pdl_trigger();
   int32_t* ssel = sd;
   int32_t* sslot = sd + stride;
   const int u = blockIdx.x, tid = threadIdx.x;
@@ -99,6 +101,8 @@ __global__ void __launch_bounds__(kLruThreads)
   uint8_t* touched = lm + n_slots;
   int32_t* vic = reinterpret_cast<int32_t*>(lm + ((2 * n_slots + 15) & ~15));
   __shared__ int hist[64], hist_u[64], warp_tot[kLruThreads / 32];
+  pdl_wait();
+  pdl_trigger();
   const int u = blockIdx.x, tid = threadIdx.x;
   const int n = max(0, min(stride, n_sel[u]));
   int nm = max(0, min(stride, n_missing[u]));
@@ -171,16 +175,19 @@ __global__ void __launch_bounds__(kLruThreads)
 
 }  // namespace
 
+cudaError_t resid_init_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(setdiff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 4096 * 2 * 4);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(lru_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * 16384 + 4096 * 4);
+}
+
 cudaError_t launch_setdiff(uint32_t* err, const int32_t* resident, int n_slots, const int32_t* sel,
                            const int32_t* n_sel, int sel_stride, int n_units, int32_t* missing, int32_t* n_missing,
                            int32_t* slot, cudaStream_t st) {
   if (n_units == 0) return cudaSuccess;
   const size_t smem = size_t(sel_stride) * 2 * sizeof(int32_t);
-  cudaError_t e = cudaFuncSetAttribute(setdiff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  setdiff_kernel<<<n_units, kSdThreads, smem, st>>>(resident, n_slots, sel, n_sel, sel_stride, missing, n_missing, slot,
-                                                    err);
-  return cudaGetLastError();
+  return launch_pdl(setdiff_kernel, dim3(n_units), dim3(kSdThreads), smem, st, resident, n_slots, sel, n_sel,
+                    sel_stride, missing, n_missing, slot, err);
 }
 
 cudaError_t launch_lru(uint32_t* err, int32_t* resident, int32_t* ts, int n_slots, const int32_t* slot,
@@ -189,11 +196,8 @@ cudaError_t launch_lru(uint32_t* err, int32_t* resident, int32_t* ts, int n_slot
                        cudaStream_t st) {
   if (n_units == 0) return cudaSuccess;
   const size_t smem = size_t((2 * n_slots + 15) & ~15) + size_t(sel_stride) * sizeof(int32_t);
-  cudaError_t e = cudaFuncSetAttribute(lru_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  lru_kernel<<<n_units, kLruThreads, smem, st>>>(resident, ts, n_slots, slot, n_sel, missing, n_missing, sel_stride,
-                                                 t_now, bucket_width, victims, hist, err);
-  return cudaGetLastError();
+  return launch_pdl(lru_kernel, dim3(n_units), dim3(kLruThreads), smem, st, resident, ts, n_slots, slot, n_sel,
+                    missing, n_missing, sel_stride, t_now, bucket_width, victims, hist, err);
 }
 
 }  // namespace spkv

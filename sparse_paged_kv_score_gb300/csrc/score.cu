@@ -27,6 +27,8 @@ __global__ void __launch_bounds__(kWarps * 32)
     score_kernel(const uint32_t* __restrict__ q, const float* __restrict__ ksum, const int32_t* __restrict__ page_table,
                  const int32_t* __restrict__ seq_len, float* __restrict__ scores, int Hq, int Hk, int G, int np_max,
                  int64_t n_phys, float scale, uint32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   const int u = blockIdx.y, b = u / Hk, h = u % Hk;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   __shared__ float qs[kHeadDim];
@@ -93,9 +95,9 @@ cudaError_t launch_score(const spkv_cache* c, const void* q, int B, int Hq, cons
   const int G = Hq / Hk;
   dim3 grid((np_max + kPagesPerBlock - 1) / kPagesPerBlock, B * Hk);
   const float scale = static_cast<float>(1.0 / (16.0 * 11.313708498984760390));  // 1 / (16 sqrt(128))
-  score_kernel<<<grid, kWarps * 32, 0, st>>>(static_cast<const uint32_t*>(q), c->d.ksum, page_table, seq_len, scores,
-                                            Hq, Hk, G, np_max, c->d.n_phys_pages, scale, c->dev_err);
-  return cudaGetLastError();
+  return launch_pdl(score_kernel, grid, dim3(kWarps * 32), 0, st, static_cast<const uint32_t*>(q),
+                    static_cast<const float*>(c->d.ksum), page_table, seq_len, scores, Hq, Hk, G, np_max,
+                    static_cast<int64_t>(c->d.n_phys_pages), scale, c->dev_err);
 }
 
 }  // namespace spkv

@@ -147,6 +147,8 @@ __global__ void __launch_bounds__(kSelThreads)
   uint8_t* cand = sm + sizeof(uint32_t) * np_max;
   uint8_t* flags = cand + np_max;
   __shared__ SelShared sh;
+  pdl_wait();
+  pdl_trigger();
 
   const int u = blockIdx.x, b = u / Hk, tid = threadIdx.x;
   const int L = seq_len[b];
@@ -203,15 +205,16 @@ __global__ void __launch_bounds__(kSelThreads)
 
 }  // namespace
 
+cudaError_t select_init_attributes() {
+  return cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 32768 * 6);
+}
+
 cudaError_t launch_select(const spkv_cache* c, const float* qs, const float* es, uint32_t* alive, int B, int np_max,
                           const int32_t* seq_len, int k_q, int k_e, int32_t* sel, int32_t* n_sel, cudaStream_t st) {
   const int Hk = c->d.n_kv_heads;
   const size_t smem = size_t(np_max) * 6;
-  cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  select_kernel<<<B * Hk, kSelThreads, smem, st>>>(qs, es, alive, seq_len, Hk, np_max, k_q, k_e, sel, n_sel,
-                                                   c->dev_err);
-  return cudaGetLastError();
+  return launch_pdl(select_kernel, dim3(B * Hk), dim3(kSelThreads), smem, st, qs, es, alive, seq_len, Hk, np_max,
+                    k_q, k_e, sel, n_sel, c->dev_err);
 }
 
 }  // namespace spkv

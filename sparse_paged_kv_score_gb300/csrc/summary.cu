@@ -27,6 +27,8 @@ __device__ __forceinline__ float2 subblock_sum(const uint32_t* page_words, int j
 __global__ void __launch_bounds__(256) summary_build_kernel(const uint32_t* __restrict__ kpool, float* __restrict__ ksum,
                                                             const int32_t* __restrict__ page_cnt, int64_t n_ph,
                                                             int64_t n_phys) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t ph = int64_t(blockIdx.x) * 4 + threadIdx.x / 64;
   if (ph >= n_ph) return;
   const int i = threadIdx.x % 64;
@@ -44,6 +46,8 @@ __global__ void __launch_bounds__(256) append_write_kernel(uint32_t* __restrict_
                                                            const int32_t* __restrict__ tok, const uint32_t* __restrict__ k_new,
                                                            const uint32_t* __restrict__ v_new, int n_rows, int Hk,
                                                            int64_t n_phys, uint32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t item = int64_t(blockIdx.x) * 4 + threadIdx.x / 64;
   if (item >= int64_t(n_rows) * Hk) return;
   const int row = static_cast<int>(item / Hk), h = static_cast<int>(item % Hk);
@@ -65,6 +69,8 @@ __global__ void __launch_bounds__(256) append_sum_kernel(const uint32_t* __restr
                                                          const int32_t* __restrict__ page_cnt,
                                                          const int32_t* __restrict__ phys, const int32_t* __restrict__ tok,
                                                          int n_rows, int Hk, int64_t n_phys) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t item = int64_t(blockIdx.x) * 4 + threadIdx.x / 64;
   if (item >= int64_t(n_rows) * Hk) return;
   const int row = static_cast<int>(item / Hk), h = static_cast<int>(item % Hk);
@@ -84,9 +90,9 @@ cudaError_t launch_summary_build(const spkv_cache* c, cudaStream_t st) {
   const int64_t n_ph = int64_t(c->d.n_kv_heads) * c->d.n_phys_pages;
   if (n_ph == 0) return cudaSuccess;
   const int64_t blocks = (n_ph + 3) / 4;
-  summary_build_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-      static_cast<const uint32_t*>(c->d.k_pool), c->d.ksum, c->d.page_cnt, n_ph, c->d.n_phys_pages);
-  return cudaGetLastError();
+  return launch_pdl(summary_build_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
+                    static_cast<const uint32_t*>(c->d.k_pool), c->d.ksum, static_cast<const int32_t*>(c->d.page_cnt),
+                    n_ph, static_cast<int64_t>(c->d.n_phys_pages));
 }
 
 cudaError_t launch_append(const spkv_cache* c, const int32_t* phys, const int32_t* tok, const void* k_new,
@@ -94,16 +100,15 @@ cudaError_t launch_append(const spkv_cache* c, const int32_t* phys, const int32_
   if (n_rows == 0) return cudaSuccess;
   const int Hk = c->d.n_kv_heads;
   const int64_t blocks = (int64_t(n_rows) * Hk + 3) / 4;
-  append_write_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-      static_cast<uint32_t*>(c->d.k_pool), static_cast<uint32_t*>(c->d.v_pool), c->d.page_cnt, phys, tok,
-      static_cast<const uint32_t*>(k_new), static_cast<const uint32_t*>(v_new), n_rows, Hk, c->d.n_phys_pages,
-      c->dev_err);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(append_write_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
+                             static_cast<uint32_t*>(c->d.k_pool), static_cast<uint32_t*>(c->d.v_pool),
+                             c->d.page_cnt, phys, tok, static_cast<const uint32_t*>(k_new),
+                             static_cast<const uint32_t*>(v_new), n_rows, Hk, static_cast<int64_t>(c->d.n_phys_pages),
+                             c->dev_err);
   if (e != cudaSuccess) return e;
-  append_sum_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<const uint32_t*>(c->d.k_pool),
-                                                                     c->d.ksum, c->d.page_cnt, phys, tok, n_rows, Hk,
-                                                                     c->d.n_phys_pages);
-  return cudaGetLastError();
+  return launch_pdl(append_sum_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
+                    static_cast<const uint32_t*>(c->d.k_pool), c->d.ksum, static_cast<const int32_t*>(c->d.page_cnt),
+                    phys, tok, n_rows, Hk, static_cast<int64_t>(c->d.n_phys_pages));
 }
 
 }  // namespace spkv

@@ -75,7 +75,7 @@ typedef struct spkv_cache* spkv_cache_t; /* opaque, library-owned */
  *   page_cnt       : int32 [n_phys_pages]; valid tokens held by each physical page.  Read by
  *                    paged_kv_create, updated by paged_kv_append.
  *   max_units      : the largest B * n_kv_heads any call on this handle will use (sizes the
- *                    split-K workspace); 0 means 4096.
+ *                    split-K workspace); 0 means 4096, larger than 4096 is SPKV_EINVAL.
  */
 typedef struct {
   int32_t n_kv_heads;

@@ -73,6 +73,8 @@ void fill_common(AttnParams& p, spkv_cache_t c, const void* q, int B, int Hq, fl
   p.ws_l = c->ws_l;
   p.ws_o = c->ws_o;
   p.ws_cnt = c->ws_cnt;
+  p.ws_ctl = c->ws_cnt + c->max_units;
+  p.max_chunks = c->max_chunks;
   p.scale_log2 = static_cast<float>(1.4426950408889634074 / std::sqrt(128.0));
 }
 
@@ -107,7 +109,7 @@ int paged_kv_create(const spkv_desc* desc, void* stream, spkv_cache_t* out) {
   *out = nullptr;
   const spkv_desc& d = *desc;
   if (d.head_dim != 128 || d.page_tokens != 64 || d.subblock != 16) return SPKV_EUNSUPPORTED;
-  if (d.n_kv_heads <= 0 || d.n_phys_pages <= 0 || d.max_units < 0) return SPKV_EINVAL;
+  if (d.n_kv_heads <= 0 || d.n_phys_pages <= 0 || d.max_units < 0 || d.max_units > 4096) return SPKV_EINVAL;
   if (!d.k_pool || !d.v_pool || !d.ksum || !d.page_cnt) return SPKV_EINVAL;
   if (!aligned(d.k_pool, 16) || !aligned(d.v_pool, 16) || !aligned(d.ksum, 16)) return SPKV_EINVAL;
   const int64_t n_ph = int64_t(d.n_kv_heads) * d.n_phys_pages;
@@ -131,12 +133,13 @@ int paged_kv_create(const spkv_desc* desc, void* stream, spkv_cache_t* out) {
     delete c;
     return SPKV_ECUDA;
   }
-  c->ws_slots = int64_t(c->attn_grid) + c->max_units;
+  c->max_chunks = 16 * c->attn_grid;
+  c->ws_slots = int64_t(c->max_chunks) + c->max_units;
   bool ok = cudaMalloc(&c->dev_err, sizeof(uint32_t)) == cudaSuccess &&
             cudaMalloc(&c->ws_m, sizeof(float) * 16 * c->ws_slots) == cudaSuccess &&
             cudaMalloc(&c->ws_l, sizeof(float) * 16 * c->ws_slots) == cudaSuccess &&
             cudaMalloc(&c->ws_o, sizeof(float) * 16 * 128 * c->ws_slots) == cudaSuccess &&
-            cudaMalloc(&c->ws_cnt, sizeof(int32_t) * c->max_units) == cudaSuccess;
+            cudaMalloc(&c->ws_cnt, sizeof(int32_t) * (c->max_units + 2)) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     paged_kv_destroy(c);
@@ -144,7 +147,7 @@ int paged_kv_create(const spkv_desc* desc, void* stream, spkv_cache_t* out) {
   }
   cudaStream_t st = as_stream(stream);
   if (cudaMemsetAsync(c->dev_err, 0, sizeof(uint32_t), st) != cudaSuccess ||
-      cudaMemsetAsync(c->ws_cnt, 0, sizeof(int32_t) * c->max_units, st) != cudaSuccess ||
+      cudaMemsetAsync(c->ws_cnt, 0, sizeof(int32_t) * (c->max_units + 2), st) != cudaSuccess ||
       spkv::launch_summary_build(c, st) != cudaSuccess) {
     paged_kv_destroy(c);
     return SPKV_ECUDA;
@@ -211,6 +214,7 @@ int sparse_decode_attn(spkv_cache_t c, const void* q, int B, int Hq, const int32
   p.n_sel = n_sel;
   p.sel_stride = sel_stride;
   p.seq_len = seq_len;
+  p.min_chunk = (sel_stride + 254) / 255;
   const int64_t t_max = int64_t(B) * c->d.n_kv_heads * sel_stride;
   const int grid = static_cast<int>(t_max < c->attn_grid ? t_max : c->attn_grid);
   return status_of(spkv::launch_attn(c, p, false, grid, as_stream(stream)));
@@ -236,6 +240,7 @@ int lazy_rope_decode_attn(spkv_cache_t c, const void* q, int B, int Hq, const in
   p.n_pages = n_pages;
   p.doc_pos = doc_pos;
   p.max_docs = max_docs;
+  p.min_chunk = (np_max + 254) / 255;
   // turns per position of pair j: theta^(-2j/128) / (2 pi), as a 2^-64 fixed-point fraction
   for (int j = 0; j < 64; ++j) {
     const double f = std::pow(static_cast<double>(theta), -2.0 * j / 128.0) / (2.0 * 3.14159265358979323846);

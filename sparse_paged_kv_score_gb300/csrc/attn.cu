@@ -9,10 +9,12 @@
 // [LazyAttention] "Technical implementation 2. Decoding" and "Mathematical equivalence".
 //
 // GB300 design (one CTA per SM, persistent, six warps):
-//   * Work balance: the pages of all units form one sequence of T pages; CTA i takes pages
-//     [i*T/N, (i+1)*T/N).  A unit split over several CTAs leaves one fp32 partial
-//     (max, sum, unnormalised O) per CTA in a workspace slot (unit + cta); the last CTA to
-//     finish a unit (atomic arrival counter, no waiting) merges the partials.
+//   * Work balance: the pages of all units form one sequence of T pages, cut into fixed chunks
+//     of CH consecutive pages; CTAs take chunks from an atomic counter as they go, so SMs that
+//     stream faster take more.  A unit split over several chunks leaves one fp32 partial
+//     (max, sum, unnormalised O) per chunk in a workspace slot (unit + chunk); the last chunk to
+//     finish a unit (atomic arrival counter, no waiting) merges the partials.  The last CTA to
+//     leave resets the chunk counter for the next launch.
 //   * Producer warp: streams each page's K and V (2 x 16 KiB, head-major, one contiguous page
 //     each) with TMA tensor loads (128B swizzle) into a ring of shared-memory stages, and with
 //     the first page of each unit a bulk copy of that unit's query rows; all complete on the
@@ -47,13 +49,18 @@ constexpr float kLn2 = 0.6931471805599453f;
 template <int NT>
 __host__ __device__ constexpr int stage_bytes() { return kKVBytes + NT * 8 * kHeadDim * 2; }
 
+constexpr int kEnd = -2;   // StageMeta.unit of the stage that ends the CTA's page stream
+constexpr int kMaxUnits = 4096;   // (request, kv head) units per call
+constexpr int kMaxParts = 256;    // split-K partials per unit (the host sizes chunks to keep this)
+
 struct __align__(16) StageMeta {
-  int unit;     // unit of this page (-1: none)
+  int unit;     // unit of this page (-1: none, kEnd: no more pages)
   int valid;    // valid tokens (0 = skip the page)
   int rel;      // lazy: query position - document offset
   int ustart;   // position of the unit's first page in the global page sequence
   int ucount;   // pages of the unit
-  int pad0, pad1, pad2;
+  int chunk;    // chunk of the global page sequence this page belongs to
+  int pad0, pad1;
 };
 
 template <int NT>
@@ -63,14 +70,14 @@ struct Smem {
   float cm[kConsumers][kG];
   float cl[kConsumers][kG];
   float co[kConsumers][kG][kHeadDim];
-  int h_unit, h_ustart, h_ucount, h_last;
+  int h_unit, h_chunk, h_ustart, h_ucount, h_last, h_pad[3];
   uint64_t full[8];
   uint64_t empty[8];
   uint64_t cfull;     // consumers -> epilogue (count kConsumers)
   uint64_t cempty;    // epilogue -> consumers (count 1)
   StageMeta meta[8];
   int scan[kThreads];
-  int u0, p0;
+  int prefix[kMaxUnits + 1];   // first global page position of every unit, then T
 };
 
 template <int NT, int STAGES>
@@ -85,11 +92,6 @@ __device__ __forceinline__ int unit_count(const AttnParams& p, bool lazy, int u)
   }
   const int n = p.n_sel[u];
   return n < 0 ? 0 : (n > p.sel_stride ? p.sel_stride : n);
-}
-
-// CTA whose page range contains global page position x (ranges [i*T/N, (i+1)*T/N), T >= N).
-__device__ __forceinline__ int cta_of(int64_t x, int64_t T, int64_t N) {
-  return static_cast<int>(((x + 1) * N - 1) / T);
 }
 
 // Swizzled shared address of the 16-byte chunk `chunk` (0..15 across the 128 dims) of token
@@ -124,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();      // the page lists and counts below are written by the previous kernel
   pdl_trigger();
 
-  // ---- 1. global page sequence: T = sum of unit counts; find this CTA's first unit
+  // ---- 1. unit prefix table: prefix[u] = first global page position of unit u, prefix[U] = T
   const int c0 = static_cast<int>(int64_t(tid) * U / kThreads);
   const int c1 = static_cast<int>(int64_t(tid + 1) * U / kThreads);
   int csum = 0;
@@ -137,134 +139,127 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (lane == 31) S.scan[warp] = x;
   __syncthreads();
-  int wbase = 0, T = 0;
-  for (int w = 0; w < kThreads / 32; ++w) {
-    if (w < warp) wbase += S.scan[w];
-    T += S.scan[w];
+  int wbase = 0;
+  for (int w = 0; w < warp; ++w) wbase += S.scan[w];
+  {
+    int acc = wbase + x - csum;  // exclusive prefix of this thread's slice
+    for (int u = c0; u < c1; ++u) {
+      S.prefix[u] = acc;
+      acc += unit_count(p, LAZY, u);
+    }
+    if (c1 == U) S.prefix[U] = acc;
   }
-  const int cpre = wbase + x - csum;  // exclusive prefix of this thread's chunk
+  __syncthreads();
+  const int T = S.prefix[U];
 
   // units with no pages get out = 0, lse = -inf (spread over the CTAs)
   for (int u = blockIdx.x; u < U; u += gridDim.x) {
-    if (unit_count(p, LAZY, u) != 0) continue;
+    if (S.prefix[u + 1] != S.prefix[u]) continue;
     const int b = u / p.Hk, h = u % p.Hk;
     for (int i = tid; i < p.G * kHeadDim; i += kThreads)
       p.out[(int64_t(b) * p.Hq + h * p.G) * kHeadDim + i] = 0.f;
     if (tid < p.G) p.lse[int64_t(b) * p.Hq + h * p.G + tid] = -CUDART_INF_F;
   }
-
-  const int64_t N = T < static_cast<int>(gridDim.x) ? T : gridDim.x;
-  if (static_cast<int64_t>(blockIdx.x) >= N) return;
-  const int64_t lo = int64_t(blockIdx.x) * T / N;
-  const int64_t hi = int64_t(blockIdx.x + 1) * T / N;
-  if (csum > 0 && lo >= cpre && lo < cpre + csum) {
-    int acc = cpre;
-    for (int u = c0; u < c1; ++u) {
-      const int n = unit_count(p, LAZY, u);
-      if (lo < acc + n) {
-        S.u0 = u;
-        S.p0 = acc;
-        break;
-      }
-      acc += n;
-    }
-  }
-  __syncthreads();
-  const int n_local = static_cast<int>(hi - lo);
+  if (T == 0) return;
+  // chunk length: at most max_chunks chunks in all, and long enough that no unit spans more
+  // than kMaxParts chunks
+  const int CH = max((T + p.max_chunks - 1) / p.max_chunks, p.min_chunk);
+  const int n_chunks = (T + CH - 1) / CH;
   const int qbytes = p.G * kHeadDim * 2;
 
   if (warp == kProducerWarp) {
     // ================================================================ producer warp
-    int u = S.u0, ustart = S.p0, ucnt = unit_count(p, LAZY, u);
     const uint64_t pol = LAZY ? l2_policy_evict_normal() : l2_policy_evict_first();
-    int last_unit = -1;
+    int last_unit = -1, last_chunk = -1, jl = 0;
     bool ok = true;
-    for (int64_t j0 = lo; j0 < hi && ok; j0 += 32) {
-      const int64_t xpos = j0 + lane;
-      const bool need = xpos < hi;
-      int my_u = -1, my_k = 0, my_us = 0, my_uc = 0;
-      while (true) {
-        if (need && my_u < 0 && xpos < int64_t(ustart) + ucnt) {
-          my_u = u;
-          my_k = static_cast<int>(xpos - ustart);
-          my_us = ustart;
-          my_uc = ucnt;
+    while (ok) {
+      int c = 0;
+      if (lane == 0) c = atomicAdd(&p.ws_ctl[0], 1);
+      c = __shfl_sync(0xffffffffu, c, 0);
+      if (c >= n_chunks) break;
+      const int x0 = c * CH, x1 = min(T, x0 + CH);
+      for (int xb = x0; xb < x1 && ok; xb += 32) {
+        const int xpos = xb + lane;
+        const bool need = xpos < x1;
+        // unit of page position xpos: the last u with prefix[u] <= xpos (skips empty units)
+        int my_u = -1, my_k = 0, my_us = 0, my_uc = 0;
+        if (need) {
+          int lo = 0, hi = U;
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (S.prefix[mid] <= xpos) lo = mid;
+            else hi = mid;
+          }
+          my_u = lo;
+          my_us = S.prefix[lo];
+          my_uc = S.prefix[lo + 1] - my_us;
+          my_k = xpos - my_us;
         }
-        if (!__any_sync(0xffffffffu, need && my_u < 0)) break;
-        if (u >= U - 1) break;  // cannot happen: every position < T lies in a unit
-        ustart += ucnt;
-        do {
-          ++u;
-          ucnt = unit_count(p, LAZY, u);
-        } while (ucnt == 0 && u < U - 1);
-      }
-      // page info of position xpos
-      int phys = 0, valid = 0, rel = 0, head = 0;
-      if (need && my_u >= 0) {
-        const int b = my_u / p.Hk;
-        head = my_u % p.Hk;
-        uint32_t bad = 0;
-        if (!LAZY) {
-          const int lp = p.sel[int64_t(my_u) * p.sel_stride + my_k];
-          if (lp < 0 || lp >= p.np_max) {
-            bad |= SPKV_DEVERR_PAGE_ID;
+        int phys = 0, valid = 0, rel = 0, head = 0;
+        if (need) {
+          const int b = my_u / p.Hk;
+          head = my_u % p.Hk;
+          uint32_t bad = 0;
+          if (!LAZY) {
+            const int lp = p.sel[int64_t(my_u) * p.sel_stride + my_k];
+            if (lp < 0 || lp >= p.np_max) {
+              bad |= SPKV_DEVERR_PAGE_ID;
+            } else {
+              const int v = min(kPageTokens, p.seq_len[b] - kPageTokens * lp);
+              const int ph = p.page_table[int64_t(b) * p.np_max + lp];
+              if (v <= 0) bad |= SPKV_DEVERR_PAGE_ID;
+              else if (ph < 0 || ph >= p.n_phys) bad |= SPKV_DEVERR_PHYS;
+              else { phys = ph; valid = v; }
+            }
           } else {
-            const int v = min(kPageTokens, p.seq_len[b] - kPageTokens * lp);
-            const int ph = p.page_table[int64_t(b) * p.np_max + lp];
-            if (v <= 0) bad |= SPKV_DEVERR_PAGE_ID;
-            else if (ph < 0 || ph >= p.n_phys) bad |= SPKV_DEVERR_PHYS;
-            else { phys = ph; valid = v; }
+            const int mh = p.meta_heads == 1 ? 0 : head;
+            const uint32_t w = p.meta[(int64_t(b) * p.meta_heads + mh) * p.np_max + my_k];
+            const int ph = static_cast<int>(w & 0x3FFFFu);
+            const int v = static_cast<int>((w >> 18) & 63u) + 1;
+            const int sl = static_cast<int>(w >> 24);
+            if (ph >= p.n_phys) bad |= SPKV_DEVERR_PHYS;
+            else if (sl >= p.max_docs) bad |= SPKV_DEVERR_SLOT;
+            else {
+              phys = ph;
+              valid = v;
+              rel = p.qpos[b] - p.doc_pos[int64_t(b) * p.max_docs + sl];
+            }
           }
-        } else {
-          const int mh = p.meta_heads == 1 ? 0 : head;
-          const uint32_t w = p.meta[(int64_t(b) * p.meta_heads + mh) * p.np_max + my_k];
-          const int ph = static_cast<int>(w & 0x3FFFFu);
-          const int v = static_cast<int>((w >> 18) & 63u) + 1;
-          const int sl = static_cast<int>(w >> 24);
-          if (ph >= p.n_phys) bad |= SPKV_DEVERR_PHYS;
-          else if (sl >= p.max_docs) bad |= SPKV_DEVERR_SLOT;
-          else {
-            phys = ph;
-            valid = v;
-            rel = p.qpos[b] - p.doc_pos[int64_t(b) * p.max_docs + sl];
-          }
+          flag_error(p.err, bad);
         }
-        flag_error(p.err, bad);
-      }
-      const int cnt = static_cast<int>(hi - j0 < 32 ? hi - j0 : 32);
-      for (int i = 0; i < cnt; ++i) {
-        const int jl = static_cast<int>(j0 - lo) + i;
-        const int s = jl % STAGES;
-        const int bu = __shfl_sync(0xffffffffu, my_u, i);
-        const int bv = __shfl_sync(0xffffffffu, valid, i);
-        const int bp = __shfl_sync(0xffffffffu, phys, i);
-        const int br = __shfl_sync(0xffffffffu, rel, i);
-        const int bs = __shfl_sync(0xffffffffu, my_us, i);
-        const int bc = __shfl_sync(0xffffffffu, my_uc, i);
-        const int bh = __shfl_sync(0xffffffffu, head, i);
-        if (jl >= STAGES) {
-          // warp-uniform outcome even if lanes disagree at the time limit
-          if (!__all_sync(0xffffffffu, mbar_wait(&S.empty[s], ((jl / STAGES) - 1) & 1))) {
-            if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
-            ok = false;
-            break;
+        const int cnt = min(32, x1 - xb);
+        for (int i = 0; i < cnt; ++i, ++jl) {
+          const int s = jl % STAGES;
+          const int bu = __shfl_sync(0xffffffffu, my_u, i);
+          const int bv = __shfl_sync(0xffffffffu, valid, i);
+          const int bp = __shfl_sync(0xffffffffu, phys, i);
+          const int br = __shfl_sync(0xffffffffu, rel, i);
+          const int bs = __shfl_sync(0xffffffffu, my_us, i);
+          const int bc = __shfl_sync(0xffffffffu, my_uc, i);
+          const int bh = __shfl_sync(0xffffffffu, head, i);
+          if (jl >= STAGES) {
+            // warp-uniform outcome even if lanes disagree at the time limit
+            if (!__all_sync(0xffffffffu, mbar_wait(&S.empty[s], ((jl / STAGES) - 1) & 1))) {
+              if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
+              ok = false;
+              break;
+            }
           }
-        }
-        if (lane == 0) {
-          StageMeta m;
-          m.unit = bu;
-          m.valid = bv;
-          m.rel = br;
-          m.ustart = bs;
-          m.ucount = bc;
-          m.pad0 = m.pad1 = m.pad2 = 0;
-          S.meta[s] = m;
-          uint8_t* dst = stages + size_t(s) * kStage;
-          const bool new_unit = bu >= 0 && bu != last_unit;
-          const uint32_t tx = (bv > 0 ? kKVBytes : 0) + (new_unit ? qbytes : 0);
-          if (tx) {
+          if (lane == 0) {
+            StageMeta m;
+            m.unit = bu;
+            m.valid = bv;
+            m.rel = br;
+            m.ustart = bs;
+            m.ucount = bc;
+            m.chunk = c;
+            m.pad0 = m.pad1 = 0;
+            S.meta[s] = m;
+            uint8_t* dst = stages + size_t(s) * kStage;
+            const bool new_seg = bu != last_unit || c != last_chunk;
+            const uint32_t tx = (bv > 0 ? kKVBytes : 0) + (new_seg ? qbytes : 0);
             mbar_arrive_expect_tx(&S.full[s], tx);
-            if (new_unit) {
+            if (new_seg) {
               const int b = bu / p.Hk, h = bu % p.Hk;
               bulk_load(dst + kKVBytes,
                         static_cast<const uint8_t*>(p.q) + (int64_t(b) * p.Hq + h * p.G) * (kHeadDim * 2),
@@ -277,17 +272,33 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_3d(dst + 2 * kBoxBytes, &tmv, &S.full[s], 0, 0, z, pol);
               tma_load_3d(dst + 3 * kBoxBytes, &tmv, &S.full[s], 64, 0, z, pol);
             }
-          } else {
-            mbar_arrive(&S.full[s]);
+            last_unit = bu;
+            last_chunk = c;
           }
-          if (bu >= 0) last_unit = bu;
+          __syncwarp();
         }
-        __syncwarp();
+      }
+    }
+    // end of this CTA's page stream
+    if (ok) {
+      const int s = jl % STAGES;
+      bool free_stage = true;
+      if (jl >= STAGES) free_stage = __all_sync(0xffffffffu, mbar_wait(&S.empty[s], ((jl / STAGES) - 1) & 1));
+      if (free_stage) {
+        if (lane == 0) {
+          StageMeta m;
+          m.unit = kEnd;
+          m.valid = m.rel = m.ustart = m.ucount = m.chunk = m.pad0 = m.pad1 = 0;
+          S.meta[s] = m;
+          mbar_arrive(&S.full[s]);
+        }
+        ++jl;
+      } else if (lane == 0) {
+        flag_error(p.err, SPKV_DEVERR_TIMEOUT);
       }
     }
     // Before leaving, make sure no copy issued by this CTA is still in flight.
-    const int first = n_local > STAGES ? n_local - STAGES : 0;
-    for (int jl = first; jl < n_local; ++jl) mbar_wait(&S.full[jl % STAGES], (jl / STAGES) & 1);
+    for (int j = jl > STAGES ? jl - STAGES : 0; j < jl; ++j) mbar_wait(&S.full[j % STAGES], (j / STAGES) & 1);
     return;
   }
 
@@ -298,13 +309,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
         break;
       }
-      const int u = S.h_unit, ustart = S.h_ustart, ucount = S.h_ucount, last = S.h_last;
+      const int u = S.h_unit, chunk = S.h_chunk, ustart = S.h_ustart, ucount = S.h_ucount, last = S.h_last;
       if (u >= 0) {
         const int b = u / p.Hk, h = u % p.Hk;
-        const int first = cta_of(ustart, T, N);
-        const int nparts = cta_of(int64_t(ustart) + ucount - 1, T, N) - first + 1;
+        const int first = ustart / CH;
+        const int nparts = (ustart + ucount - 1) / CH - first + 1;
         const int64_t orow = int64_t(b) * p.Hq + h * p.G;
-        const int64_t slot = int64_t(u) + blockIdx.x;
+        const int64_t slot = int64_t(u) + chunk;
         for (int g = 0; g < p.G; ++g) {
           float M = -CUDART_INF_F;
 #pragma unroll
@@ -337,28 +348,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nparts > 1) {
           __threadfence();
           __syncwarp();
-          int lastcta = 0;
-          if (lane == 0) lastcta = atomicAdd(&p.ws_cnt[u], 1) == nparts - 1;
-          lastcta = __shfl_sync(0xffffffffu, lastcta, 0);
-          if (lastcta) {
+          int lastpart = 0;
+          if (lane == 0) lastpart = atomicAdd(&p.ws_cnt[u], 1) == nparts - 1;
+          lastpart = __shfl_sync(0xffffffffu, lastpart, 0);
+          if (lastpart) {
             __threadfence();
-            for (int g = 0; g < p.G; ++g) {
-              float M = -CUDART_INF_F;
-              for (int i = 0; i < nparts; ++i) M = fmaxf(M, __ldcg(&p.ws_m[(int64_t(u) + first + i) * 16 + g]));
-              float L = 0.f, acc[kHeadDim / 32] = {};
-              for (int i = 0; i < nparts; ++i) {
-                const int64_t sl = int64_t(u) + first + i;
+            // Merge the unit's partials (at most kMaxParts).  S.co is free scratch until cempty
+            // is signalled.  Lanes run over parts, so each round issues independent loads.
+            float* fw_s = &S.co[0][0][0];   // [g][kMaxParts]: weight of part i for query head g
+            float* lg_s = fw_s + Smem<NT>::kG * kMaxParts;
+            float mx[Smem<NT>::kG], ls[Smem<NT>::kG];
+#pragma unroll
+            for (int g = 0; g < Smem<NT>::kG; ++g) {
+              mx[g] = -CUDART_INF_F;
+              ls[g] = 0.f;
+            }
+            for (int i = lane; i < nparts; i += 32) {
+              const int64_t sl = int64_t(u) + first + i;
+#pragma unroll
+              for (int g = 0; g < Smem<NT>::kG; ++g)
+                if (g < p.G) mx[g] = fmaxf(mx[g], __ldcg(&p.ws_m[sl * 16 + g]));
+            }
+#pragma unroll
+            for (int g = 0; g < Smem<NT>::kG; ++g)
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], o));
+            for (int i = lane; i < nparts; i += 32) {
+              const int64_t sl = int64_t(u) + first + i;
+#pragma unroll
+              for (int g = 0; g < Smem<NT>::kG; ++g) {
+                if (g >= p.G) continue;
                 const float mw = __ldcg(&p.ws_m[sl * 16 + g]);
-                const float f = mw == -CUDART_INF_F ? 0.f : exp2f(mw - M);
-                L += f * __ldcg(&p.ws_l[sl * 16 + g]);
+                const float f = mw == -CUDART_INF_F ? 0.f : exp2f(mw - mx[g]);
+                fw_s[g * kMaxParts + i] = f;
+                ls[g] += f * __ldcg(&p.ws_l[sl * 16 + g]);
+              }
+            }
+#pragma unroll
+            for (int g = 0; g < Smem<NT>::kG; ++g)
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) ls[g] += __shfl_xor_sync(0xffffffffu, ls[g], o);
+            if (lane == 0) {
+#pragma unroll
+              for (int g = 0; g < Smem<NT>::kG; ++g) {
+                if (g >= p.G) continue;
+                lg_s[g] = ls[g];
+                p.lse[orow + g] = ls[g] > 0.f ? (mx[g] + log2f(ls[g])) * kLn2 : -CUDART_INF_F;
+              }
+            }
+            __syncwarp();
+            for (int g = 0; g < p.G; ++g) {
+              float acc[kHeadDim / 32] = {};
+              int i = 0;
+              for (; i + 4 <= nparts; i += 4) {
+                float v[4][kHeadDim / 32];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                  for (int j = 0; j < kHeadDim / 32; ++j)
+                    v[q][j] = __ldcg(&p.ws_o[((int64_t(u) + first + i + q) * 16 + g) * kHeadDim + lane + 32 * j]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                  for (int j = 0; j < kHeadDim / 32; ++j) acc[j] += fw_s[g * kMaxParts + i + q] * v[q][j];
+              }
+              for (; i < nparts; ++i)
 #pragma unroll
                 for (int j = 0; j < kHeadDim / 32; ++j)
-                  acc[j] += f * __ldcg(&p.ws_o[(sl * 16 + g) * kHeadDim + lane + 32 * j]);
-              }
+                  acc[j] += fw_s[g * kMaxParts + i] *
+                            __ldcg(&p.ws_o[((int64_t(u) + first + i) * 16 + g) * kHeadDim + lane + 32 * j]);
+              const float L = lg_s[g];
 #pragma unroll
               for (int j = 0; j < kHeadDim / 32; ++j)
                 p.out[(orow + g) * kHeadDim + lane + 32 * j] = L > 0.f ? acc[j] / L : 0.f;
-              if (lane == 0) p.lse[orow + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
             }
             if (lane == 0) p.ws_cnt[u] = 0;
           }
@@ -367,6 +429,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.cempty);
       if (last) break;
+    }
+    // the last CTA to leave resets the chunk counter for the next launch
+    if (lane == 0) {
+      __threadfence();
+      if (atomicAdd(&p.ws_ctl[1], 1) == static_cast<int>(gridDim.x) - 1) {
+        p.ws_ctl[0] = 0;
+        p.ws_ctl[1] = 0;
+        __threadfence();
+      }
     }
     return;
   }
@@ -381,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t qh[8][NT][2];                  // B fragments of q (bf16 hi part)
   uint32_t ql[LAZY ? 8 : 1][NT][2];       // lazy: bf16 lo part of the rotated query
   uint32_t qraw[LAZY ? 8 : 1][NT][2];     // lazy: unrotated query
-  int cur_u = -1, cur_us = 0, cur_uc = 0, cur_rel = 0, n_flush = 0;
+  int cur_u = -1, cur_c = -1, cur_us = 0, cur_uc = 0, cur_rel = 0, n_flush = 0;
   bool have_rel = false;
 
   auto reset_state = [&]() {
@@ -456,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   // Hands this warp's state for unit u to the epilogue warp (which merges the four warps).
-  auto flush = [&](int u, int ustart, int ucount, int last) {
+  auto flush = [&](int u, int chunk, int ustart, int ucount, int last) {
     if (n_flush > 0) {
       if (!__all_sync(0xffffffffu, mbar_wait(&S.cempty, (n_flush - 1) & 1))) {
         if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
@@ -484,6 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           S.co[warp][nt * 8 + 2 * c + (e & 1)][16 * j + r + ((e >> 1) << 3)] = O[j][nt][e];
     if (warp == 0 && lane == 0) {
       S.h_unit = u;
+      S.h_chunk = chunk;
       S.h_ustart = ustart;
       S.h_ucount = ucount;
       S.h_last = last;
@@ -495,21 +567,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   reset_state();
   const uint32_t stage0 = smem_u32(stages);
-  for (int jl = 0; jl < n_local; ++jl) {
+  for (int jl = 0;; ++jl) {
     const int s = jl % STAGES;
     if (!__all_sync(0xffffffffu, mbar_wait(&S.full[s], (jl / STAGES) & 1))) {
       if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
       break;
     }
     const StageMeta mt = S.meta[s];
+    if (mt.unit == kEnd) break;
     if (mt.unit < 0) {  // defensive: a position the producer could not place
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty[s]);
       continue;
     }
-    if (mt.unit != cur_u) {
-      if (cur_u >= 0) flush(cur_u, cur_us, cur_uc, 0);
+    if (mt.unit != cur_u || mt.chunk != cur_c) {
+      if (cur_u >= 0) flush(cur_u, cur_c, cur_us, cur_uc, 0);
       cur_u = mt.unit;
+      cur_c = mt.chunk;
       cur_us = mt.ustart;
       cur_uc = mt.ucount;
       reset_state();
@@ -607,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) mbar_arrive(&S.empty[s]);
   }
   // the last hand-off ends the epilogue warp (unit -1 when this warp saw no page)
-  flush(cur_u, cur_us, cur_uc, 1);
+  flush(cur_u, cur_c, cur_us, cur_uc, 1);
 }
 
 template <int NT, bool LAZY, int STAGES>
@@ -622,8 +696,8 @@ cudaError_t launch_one(const spkv_cache* c, const AttnParams& p, int grid, cudaS
                     c->tmap_k, c->tmap_v, p);
 }
 
-constexpr int kStages1 = 6;   // G <= 8: 6 stages of 34 KiB
-constexpr int kStages2 = 5;   // G <= 16: 5 stages of 36 KiB
+constexpr int kStages1 = 5;   // G <= 8: 5 stages of 34 KiB
+constexpr int kStages2 = 4;   // G <= 16: 4 stages of 36 KiB
 
 }  // namespace
 

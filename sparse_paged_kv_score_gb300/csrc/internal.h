@@ -19,10 +19,11 @@ struct spkv_cache {
   float* ws_m = nullptr;         // split-K partial row max   [slots][16]
   float* ws_l = nullptr;         // split-K partial row sum   [slots][16]
   float* ws_o = nullptr;         // split-K partial outputs   [slots][16][128]
-  int32_t* ws_cnt = nullptr;     // per-unit arrival counters [max_units], kept at 0 between calls
+  int32_t* ws_cnt = nullptr;     // per-unit arrival counters [max_units] + 2 chunk-scheduler words
   int64_t ws_slots = 0;
   int32_t max_units = 0;
   int attn_grid = 0;             // CTAs of the split-K attention kernel (one per SM)
+  int max_chunks = 0;            // chunks the attention kernel may cut its page sequence into
 };
 
 namespace spkv {
@@ -62,6 +63,9 @@ struct AttnParams {
   float* ws_l;
   float* ws_o;
   int32_t* ws_cnt;
+  int32_t* ws_ctl;               // [0] next chunk to hand out, [1] CTAs finished; both 0 between calls
+  int max_chunks;                // chunks of the page sequence at most (workspace slots = units + this)
+  int min_chunk;                 // smallest chunk length (keeps a unit's partials <= 256)
   // sparse form
   const int32_t* page_table;
   int np_max;

@@ -16,7 +16,8 @@
 //   * the first call on a device looks up the array's device address (cudaGetSymbolAddress)
 //     with that device current, so make that first call before any stream capture;
 //   * all calls on a device share the one array and it keeps the last call's contents; the
-//     arrival counters (and the fallback error word) are cleared at the start of every call;
+//     arrival counters, the chunk-scheduler words (and the fallback error word) are cleared at
+//     the start of every call;
 //     two calls whose kernels overlap on the GPU (different streams, no ordering) race on it;
 //   * nothing here calls cudaMalloc, cudaFree or any allocating routine.
 #include <cudaTypedefs.h>
@@ -132,6 +133,7 @@ extern "C" int sparse_decode_attn_noalloc(const void* k_pool, const void* v_pool
   const int64_t units = int64_t(B) * n_kv_heads;
   if (cudaMemsetAsync(cnt, 0, sizeof(int32_t) * units, st) != cudaSuccess) return SPKV_ECUDA;
   if (!dev_err && cudaMemsetAsync(err, 0, sizeof(uint32_t), st) != cudaSuccess) return SPKV_ECUDA;
+  if (cudaMemsetAsync(base + kOffErr + 16, 0, 2 * sizeof(int32_t), st) != cudaSuccess) return SPKV_ECUDA;
 
   spkv::AttnParams p;
   std::memset(&p, 0, sizeof(p));
@@ -148,6 +150,9 @@ extern "C" int sparse_decode_attn_noalloc(const void* k_pool, const void* v_pool
   p.ws_l = reinterpret_cast<float*>(base + kOffL);
   p.ws_o = reinterpret_cast<float*>(base + kOffO);
   p.ws_cnt = cnt;
+  p.ws_ctl = reinterpret_cast<int32_t*>(base + kOffErr + 16);   // inside the 256-byte first region
+  p.max_chunks = SPKV_NOALLOC_MAX_CTAS;
+  p.min_chunk = (sel_stride + 254) / 255;
   p.scale_log2 = static_cast<float>(1.4426950408889634074 / std::sqrt(128.0));
   p.page_table = page_table;
   p.np_max = np_max;

@@ -233,7 +233,7 @@ int lru_bucket_update(spkv_cache_t cache, int32_t* resident, int32_t* ts, int n_
  * (unordered streams) race on it and must not be issued. */
 #define SPKV_NOALLOC_MAX_UNITS 512
 #define SPKV_NOALLOC_MAX_CTAS 160
-#define SPKV_NOALLOC_SCRATCH_BYTES 5593344
+#define SPKV_NOALLOC_SCRATCH_BYTES 6924544
 int sparse_decode_attn_noalloc(const void* k_pool, const void* v_pool, int n_kv_heads,
                                int64_t n_phys_pages, const void* q, int B, int Hq,
                                const int32_t* page_table, int np_max, const int32_t* sel,

@@ -214,7 +214,7 @@ int sparse_decode_attn(spkv_cache_t c, const void* q, int B, int Hq, const int32
   p.n_sel = n_sel;
   p.sel_stride = sel_stride;
   p.seq_len = seq_len;
-  p.min_chunk = (sel_stride + 254) / 255;
+  p.min_chunk = (sel_stride + 125) / 126;
   const int64_t t_max = int64_t(B) * c->d.n_kv_heads * sel_stride;
   const int grid = static_cast<int>(t_max < c->attn_grid ? t_max : c->attn_grid);
   return status_of(spkv::launch_attn(c, p, false, grid, as_stream(stream)));
@@ -240,7 +240,7 @@ int lazy_rope_decode_attn(spkv_cache_t c, const void* q, int B, int Hq, const in
   p.n_pages = n_pages;
   p.doc_pos = doc_pos;
   p.max_docs = max_docs;
-  p.min_chunk = (np_max + 254) / 255;
+  p.min_chunk = (np_max + 125) / 126;
   // turns per position of pair j: theta^(-2j/128) / (2 pi), as a 2^-64 fixed-point fraction
   for (int j = 0; j < 64; ++j) {
     const double f = std::pow(static_cast<double>(theta), -2.0 * j / 128.0) / (2.0 * 3.14159265358979323846);

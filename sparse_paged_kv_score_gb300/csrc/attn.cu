@@ -9,12 +9,14 @@
 // [LazyAttention] "Technical implementation 2. Decoding" and "Mathematical equivalence".
 //
 // GB300 design (one CTA per SM, persistent, six warps):
-//   * Work balance: the pages of all units form one sequence of T pages, cut into fixed chunks
-//     of CH consecutive pages; CTAs take chunks from an atomic counter as they go, so SMs that
-//     stream faster take more.  A unit split over several chunks leaves one fp32 partial
-//     (max, sum, unnormalised O) per chunk in a workspace slot (unit + chunk); the last chunk to
-//     finish a unit (atomic arrival counter, no waiting) merges the partials.  The last CTA to
-//     leave resets the chunk counter for the next launch.
+//   * Work balance: the pages of all units form one sequence of T pages.  Each CTA first streams
+//     a static range (80% of the pages split evenly), then takes small chunks of the remaining
+//     20% from an atomic counter, so SMs that stream faster take more and all finish together.
+//     Static ranges and chunks ("segments") are numbered in page order; a unit split over
+//     several segments leaves one fp32 partial (max, sum, unnormalised O) per segment in a
+//     workspace slot (unit + segment); the last segment to finish a unit (atomic arrival
+//     counter, no waiting) merges the partials.  The last CTA to leave resets the chunk counter
+//     for the next launch.
 //   * Producer warp: streams each page's K and V (2 x 16 KiB, head-major, one contiguous page
 //     each) with TMA tensor loads (128B swizzle) into a ring of shared-memory stages, and with
 //     the first page of each unit a bulk copy of that unit's query rows; all complete on the
@@ -161,10 +163,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid < p.G) p.lse[int64_t(b) * p.Hq + h * p.G + tid] = -CUDART_INF_F;
   }
   if (T == 0) return;
-  // chunk length: at most max_chunks chunks in all, and long enough that no unit spans more
-  // than kMaxParts chunks
-  const int CH = max((T + p.max_chunks - 1) / p.max_chunks, p.min_chunk);
-  const int n_chunks = (T + CH - 1) / CH;
+  // Segments: static ranges of S0 pages (one per CTA, none when they would be shorter than
+  // min_chunk), then dynamic chunks of CH pages.  min_chunk keeps every unit within kMaxParts
+  // segments; the chunk count stays within the workspace (max_chunks - N chunks).
+  const int N = gridDim.x;
+  int S0 = static_cast<int>(int64_t(T) * 4 / (5 * int64_t(N)));
+  if (S0 < p.min_chunk) S0 = 0;
+  const int D0 = S0 * N;
+  const int T_dyn = T - D0;
+  const int CH = max(max((T_dyn + 2 * N - 1) / (2 * N), (T_dyn + p.max_chunks - N - 1) / (p.max_chunks - N)),
+                     p.min_chunk);
+  const int n_chunks = (T_dyn + CH - 1) / CH;
+  auto seg_of = [&](int x) { return x < D0 ? x / S0 : N + (x - D0) / CH; };
   const int qbytes = p.G * kHeadDim * 2;
 
   if (warp == kProducerWarp) {
@@ -172,12 +182,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol = LAZY ? l2_policy_evict_normal() : l2_policy_evict_first();
     int last_unit = -1, last_chunk = -1, jl = 0;
     bool ok = true;
-    while (ok) {
-      int c = 0;
-      if (lane == 0) c = atomicAdd(&p.ws_ctl[0], 1);
-      c = __shfl_sync(0xffffffffu, c, 0);
-      if (c >= n_chunks) break;
-      const int x0 = c * CH, x1 = min(T, x0 + CH);
+    for (int it = 0; ok; ++it) {
+      int c, x0, x1;   // segment id and its page range
+      if (it == 0 && S0 > 0) {
+        c = blockIdx.x;
+        x0 = blockIdx.x * S0;
+        x1 = x0 + S0;
+      } else {
+        int k = 0;
+        if (lane == 0) k = atomicAdd(&p.ws_ctl[0], 1);
+        k = __shfl_sync(0xffffffffu, k, 0);
+        if (k >= n_chunks) break;
+        c = N + k;
+        x0 = D0 + k * CH;
+        x1 = min(T, x0 + CH);
+      }
       for (int xb = x0; xb < x1 && ok; xb += 32) {
         const int xpos = xb + lane;
         const bool need = xpos < x1;
@@ -312,8 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int u = S.h_unit, chunk = S.h_chunk, ustart = S.h_ustart, ucount = S.h_ucount, last = S.h_last;
       if (u >= 0) {
         const int b = u / p.Hk, h = u % p.Hk;
-        const int first = ustart / CH;
-        const int nparts = (ustart + ucount - 1) / CH - first + 1;
+        const int first = seg_of(ustart);
+        const int nparts = seg_of(ustart + ucount - 1) - first + 1;
         const int64_t orow = int64_t(b) * p.Hq + h * p.G;
         const int64_t slot = int64_t(u) + chunk;
         for (int g = 0; g < p.G; ++g) {

@@ -65,7 +65,7 @@ struct AttnParams {
   int32_t* ws_cnt;
   int32_t* ws_ctl;               // [0] next chunk to hand out, [1] CTAs finished; both 0 between calls
   int max_chunks;                // chunks of the page sequence at most (workspace slots = units + this)
-  int min_chunk;                 // smallest chunk length (keeps a unit's partials <= 256)
+  int min_chunk;                 // smallest segment length (keeps a unit's partials <= 256)
   // sparse form
   const int32_t* page_table;
   int np_max;

@@ -31,7 +31,7 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int64_t kSlots = int64_t(SPKV_NOALLOC_MAX_CTAS) + SPKV_NOALLOC_MAX_UNITS;
+constexpr int64_t kSlots = int64_t(2 * SPKV_NOALLOC_MAX_CTAS) + SPKV_NOALLOC_MAX_UNITS;
 // Byte layout of the scratch array (each region 256-byte aligned).
 constexpr int64_t kOffErr = 0;
 constexpr int64_t kOffCnt = 256;
@@ -151,8 +151,8 @@ extern "C" int sparse_decode_attn_noalloc(const void* k_pool, const void* v_pool
   p.ws_o = reinterpret_cast<float*>(base + kOffO);
   p.ws_cnt = cnt;
   p.ws_ctl = reinterpret_cast<int32_t*>(base + kOffErr + 16);   // inside the 256-byte first region
-  p.max_chunks = SPKV_NOALLOC_MAX_CTAS;
-  p.min_chunk = (sel_stride + 254) / 255;
+  p.max_chunks = 2 * SPKV_NOALLOC_MAX_CTAS;
+  p.min_chunk = (sel_stride + 125) / 126;
   p.scale_log2 = static_cast<float>(1.4426950408889634074 / std::sqrt(128.0));
   p.page_table = page_table;
   p.np_max = np_max;

@@ -216,7 +216,7 @@ int lru_bucket_update(spkv_cache_t cache, int32_t* resident, int32_t* ts, int n_
  * (an engine that forbids cudaMalloc after start-up or owns all device memory through its own
  * allocator, or code that must not create a handle, since paged_kv_create allocates).  It
  * computes exactly what sparse_decode_attn computes, with the same kernel, but takes the pool
- * directly instead of a handle and keeps its split-K scratch (partial results and arrival
+ * directly instead of a handle and keeps its split-K scratch (partial results and their
  * counters) in one fixed device array of SPKV_NOALLOC_SCRATCH_BYTES bytes that every GPU
  * loading this library holds until the process exits.  The caller passes inputs and outputs.
  *   k_pool, v_pool : device bf16 [n_kv_heads][n_phys_pages][64][128], 16-byte aligned
@@ -233,7 +233,7 @@ int lru_bucket_update(spkv_cache_t cache, int32_t* resident, int32_t* ts, int n_
  * (unordered streams) race on it and must not be issued. */
 #define SPKV_NOALLOC_MAX_UNITS 512
 #define SPKV_NOALLOC_MAX_CTAS 160
-#define SPKV_NOALLOC_SCRATCH_BYTES 6924544
+#define SPKV_NOALLOC_SCRATCH_BYTES 6926592
 int sparse_decode_attn_noalloc(const void* k_pool, const void* v_pool, int n_kv_heads,
                                int64_t n_phys_pages, const void* q, int B, int Hq,
                                const int32_t* page_table, int np_max, const int32_t* sel,

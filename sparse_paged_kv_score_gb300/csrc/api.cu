@@ -72,8 +72,8 @@ void fill_common(AttnParams& p, spkv_cache_t c, const void* q, int B, int Hq, fl
   p.ws_m = c->ws_m;
   p.ws_l = c->ws_l;
   p.ws_o = c->ws_o;
-  p.ws_cnt = c->ws_cnt;
-  p.ws_ctl = c->ws_cnt + c->max_units;
+  p.ws_parts = c->ws_cnt;
+  p.ws_ctl = c->ws_cnt + 2 * c->max_units;
   p.max_chunks = c->max_chunks;
   p.scale_log2 = static_cast<float>(1.4426950408889634074 / std::sqrt(128.0));
 }
@@ -139,7 +139,7 @@ int paged_kv_create(const spkv_desc* desc, void* stream, spkv_cache_t* out) {
             cudaMalloc(&c->ws_m, sizeof(float) * 16 * c->ws_slots) == cudaSuccess &&
             cudaMalloc(&c->ws_l, sizeof(float) * 16 * c->ws_slots) == cudaSuccess &&
             cudaMalloc(&c->ws_o, sizeof(float) * 16 * 128 * c->ws_slots) == cudaSuccess &&
-            cudaMalloc(&c->ws_cnt, sizeof(int32_t) * (c->max_units + 2)) == cudaSuccess;
+            cudaMalloc(&c->ws_cnt, sizeof(int32_t) * (2 * c->max_units + 2)) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     paged_kv_destroy(c);
@@ -147,7 +147,7 @@ int paged_kv_create(const spkv_desc* desc, void* stream, spkv_cache_t* out) {
   }
   cudaStream_t st = as_stream(stream);
   if (cudaMemsetAsync(c->dev_err, 0, sizeof(uint32_t), st) != cudaSuccess ||
-      cudaMemsetAsync(c->ws_cnt, 0, sizeof(int32_t) * (c->max_units + 2), st) != cudaSuccess ||
+      cudaMemsetAsync(c->ws_cnt, 0, sizeof(int32_t) * (2 * c->max_units + 2), st) != cudaSuccess ||
       spkv::launch_summary_build(c, st) != cudaSuccess) {
     paged_kv_destroy(c);
     return SPKV_ECUDA;

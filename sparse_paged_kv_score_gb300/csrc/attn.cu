@@ -10,13 +10,12 @@
 //
 // GB300 design (one CTA per SM, persistent, six warps):
 //   * Work balance: the pages of all units form one sequence of T pages.  Each CTA first streams
-//     a static range (80% of the pages split evenly), then takes small chunks of the remaining
-//     20% from an atomic counter, so SMs that stream faster take more and all finish together.
+//     a static range (75% of the pages split evenly), then takes small chunks of the remaining
+//     25% from an atomic counter, so SMs that stream faster take more and all finish together.
 //     Static ranges and chunks ("segments") are numbered in page order; a unit split over
 //     several segments leaves one fp32 partial (max, sum, unnormalised O) per segment in a
-//     workspace slot (unit + segment); the last segment to finish a unit (atomic arrival
-//     counter, no waiting) merges the partials.  The last CTA to leave resets the chunk counter
-//     for the next launch.
+//     workspace slot (unit + segment), and a small second kernel (one CTA per unit, launched
+//     with programmatic dependent launch) merges them and resets the chunk counter.
 //   * Producer warp: streams each page's K and V (2 x 16 KiB, head-major, one contiguous page
 //     each) with TMA tensor loads (128B swizzle) into a ring of shared-memory stages, and with
 //     the first page of each unit a bulk copy of that unit's query rows; all complete on the
@@ -26,9 +25,9 @@
 //     group of query heads shares one tensor-core tile; P^T goes from the accumulator layout to
 //     the B-operand layout with movmatrix; P.V runs with V^T (ldmatrix.trans) as A.  P (and the
 //     rotated lazy query) is split into bf16 hi + lo parts so the weights keep ~17 bits.
-//   * Epilogue warp: at each unit switch the consumers hand their (max, sum, O) to a shared
-//     buffer and go on streaming; the epilogue warp merges the four states, writes the output or
-//     the split-K partial, and does the cross-CTA merge, off the consumers' critical path.
+//   * Epilogue warp: at each segment switch the consumers hand their (max, sum, O) to a shared
+//     buffer and go on streaming; the epilogue warp merges the four states and writes the
+//     output (unit within one segment) or the segment's partial, off the consumers' critical path.
 //   * Launched with programmatic dependent launch: barrier set-up overlaps the previous kernel;
 //     griddepcontrol.wait precedes the first read of its outputs.
 #include <math_constants.h>
@@ -53,7 +52,6 @@ __host__ __device__ constexpr int stage_bytes() { return kKVBytes + NT * 8 * kHe
 
 constexpr int kEnd = -2;   // StageMeta.unit of the stage that ends the CTA's page stream
 constexpr int kMaxUnits = 4096;   // (request, kv head) units per call
-constexpr int kMaxParts = 256;    // split-K partials per unit (the host sizes chunks to keep this)
 
 struct __align__(16) StageMeta {
   int unit;     // unit of this page (-1: none, kEnd: no more pages)
@@ -161,17 +159,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = tid; i < p.G * kHeadDim; i += kThreads)
       p.out[(int64_t(b) * p.Hq + h * p.G) * kHeadDim + i] = 0.f;
     if (tid < p.G) p.lse[int64_t(b) * p.Hq + h * p.G + tid] = -CUDART_INF_F;
+    if (tid == 0) p.ws_parts[2 * u] = p.ws_parts[2 * u + 1] = 0;
   }
   if (T == 0) return;
   // Segments: static ranges of S0 pages (one per CTA, none when they would be shorter than
-  // min_chunk), then dynamic chunks of CH pages.  min_chunk keeps every unit within kMaxParts
-  // segments; the chunk count stays within the workspace (max_chunks - N chunks).
+  // min_chunk), then dynamic chunks of CH pages.  min_chunk bounds the partials of a unit
+  // (about 250 at most); the chunk count stays within the workspace (max_chunks - N chunks).
   const int N = gridDim.x;
-  int S0 = static_cast<int>(int64_t(T) * 4 / (5 * int64_t(N)));
+  int S0 = static_cast<int>(int64_t(T) * 3 / (4 * int64_t(N)));
   if (S0 < p.min_chunk) S0 = 0;
   const int D0 = S0 * N;
   const int T_dyn = T - D0;
-  const int CH = max(max((T_dyn + 2 * N - 1) / (2 * N), (T_dyn + p.max_chunks - N - 1) / (p.max_chunks - N)),
+  const int CH = max(max((T_dyn + 6 * N - 1) / (6 * N), (T_dyn + p.max_chunks - N - 1) / (p.max_chunks - N)),
                      p.min_chunk);
   const int n_chunks = (T_dyn + CH - 1) / CH;
   auto seg_of = [&](int x) { return x < D0 ? x / S0 : N + (x - D0) / CH; };
@@ -364,99 +363,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (nparts > 1) {
-          __threadfence();
-          __syncwarp();
-          int lastpart = 0;
-          if (lane == 0) lastpart = atomicAdd(&p.ws_cnt[u], 1) == nparts - 1;
-          lastpart = __shfl_sync(0xffffffffu, lastpart, 0);
-          if (lastpart) {
-            __threadfence();
-            // Merge the unit's partials (at most kMaxParts).  S.co is free scratch until cempty
-            // is signalled.  Lanes run over parts, so each round issues independent loads.
-            float* fw_s = &S.co[0][0][0];   // [g][kMaxParts]: weight of part i for query head g
-            float* lg_s = fw_s + Smem<NT>::kG * kMaxParts;
-            float mx[Smem<NT>::kG], ls[Smem<NT>::kG];
-#pragma unroll
-            for (int g = 0; g < Smem<NT>::kG; ++g) {
-              mx[g] = -CUDART_INF_F;
-              ls[g] = 0.f;
-            }
-            for (int i = lane; i < nparts; i += 32) {
-              const int64_t sl = int64_t(u) + first + i;
-#pragma unroll
-              for (int g = 0; g < Smem<NT>::kG; ++g)
-                if (g < p.G) mx[g] = fmaxf(mx[g], __ldcg(&p.ws_m[sl * 16 + g]));
-            }
-#pragma unroll
-            for (int g = 0; g < Smem<NT>::kG; ++g)
-#pragma unroll
-              for (int o = 16; o > 0; o >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], o));
-            for (int i = lane; i < nparts; i += 32) {
-              const int64_t sl = int64_t(u) + first + i;
-#pragma unroll
-              for (int g = 0; g < Smem<NT>::kG; ++g) {
-                if (g >= p.G) continue;
-                const float mw = __ldcg(&p.ws_m[sl * 16 + g]);
-                const float f = mw == -CUDART_INF_F ? 0.f : exp2f(mw - mx[g]);
-                fw_s[g * kMaxParts + i] = f;
-                ls[g] += f * __ldcg(&p.ws_l[sl * 16 + g]);
-              }
-            }
-#pragma unroll
-            for (int g = 0; g < Smem<NT>::kG; ++g)
-#pragma unroll
-              for (int o = 16; o > 0; o >>= 1) ls[g] += __shfl_xor_sync(0xffffffffu, ls[g], o);
-            if (lane == 0) {
-#pragma unroll
-              for (int g = 0; g < Smem<NT>::kG; ++g) {
-                if (g >= p.G) continue;
-                lg_s[g] = ls[g];
-                p.lse[orow + g] = ls[g] > 0.f ? (mx[g] + log2f(ls[g])) * kLn2 : -CUDART_INF_F;
-              }
-            }
-            __syncwarp();
-            for (int g = 0; g < p.G; ++g) {
-              float acc[kHeadDim / 32] = {};
-              int i = 0;
-              for (; i + 4 <= nparts; i += 4) {
-                float v[4][kHeadDim / 32];
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-#pragma unroll
-                  for (int j = 0; j < kHeadDim / 32; ++j)
-                    v[q][j] = __ldcg(&p.ws_o[((int64_t(u) + first + i + q) * 16 + g) * kHeadDim + lane + 32 * j]);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-#pragma unroll
-                  for (int j = 0; j < kHeadDim / 32; ++j) acc[j] += fw_s[g * kMaxParts + i + q] * v[q][j];
-              }
-              for (; i < nparts; ++i)
-#pragma unroll
-                for (int j = 0; j < kHeadDim / 32; ++j)
-                  acc[j] += fw_s[g * kMaxParts + i] *
-                            __ldcg(&p.ws_o[((int64_t(u) + first + i) * 16 + g) * kHeadDim + lane + 32 * j]);
-              const float L = lg_s[g];
-#pragma unroll
-              for (int j = 0; j < kHeadDim / 32; ++j)
-                p.out[(orow + g) * kHeadDim + lane + 32 * j] = L > 0.f ? acc[j] / L : 0.f;
-            }
-            if (lane == 0) p.ws_cnt[u] = 0;
-          }
+        // the unit's first segment records where the combine kernel finds its partials
+        if (lane == 0 && chunk == first) {
+          p.ws_parts[2 * u] = first;
+          p.ws_parts[2 * u + 1] = nparts;
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.cempty);
       if (last) break;
-    }
-    // the last CTA to leave resets the chunk counter for the next launch
-    if (lane == 0) {
-      __threadfence();
-      if (atomicAdd(&p.ws_ctl[1], 1) == static_cast<int>(gridDim.x) - 1) {
-        p.ws_ctl[0] = 0;
-        p.ws_ctl[1] = 0;
-        __threadfence();
-      }
     }
     return;
   }
@@ -703,6 +618,52 @@ __global__ void __launch_bounds__(kThreads, 1)
   flush(cur_u, cur_c, cur_us, cur_uc, 1);
 }
 
+// Merges the split-K partials of every unit that spans several segments (one CTA per unit,
+// thread d owns output dimension d), then resets the chunk counter for the next launch.
+template <int NT>
+__global__ void __launch_bounds__(kHeadDim)
+    attn_combine_kernel(const __grid_constant__ AttnParams p) {
+  pdl_wait();
+  pdl_trigger();
+  const int u = blockIdx.x, d = threadIdx.x;
+  if (u == 0 && d == 0) p.ws_ctl[0] = 0;
+  const int first = p.ws_parts[2 * u], nparts = p.ws_parts[2 * u + 1];
+  if (nparts <= 1) return;
+  const int b = u / p.Hk, h = u % p.Hk;
+  const int64_t orow = int64_t(b) * p.Hq + h * p.G;
+  for (int g = 0; g < p.G; ++g) {
+    float M = -CUDART_INF_F;
+    for (int i = 0; i < nparts; ++i) M = fmaxf(M, p.ws_m[(int64_t(u) + first + i) * 16 + g]);
+    float L = 0.f, acc = 0.f;
+    int i = 0;
+    for (; i + 4 <= nparts; i += 4) {
+      float mw[4], lw[4], ow[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int64_t sl = int64_t(u) + first + i + q;
+        mw[q] = p.ws_m[sl * 16 + g];
+        lw[q] = p.ws_l[sl * 16 + g];
+        ow[q] = p.ws_o[(sl * 16 + g) * kHeadDim + d];
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float f = mw[q] == -CUDART_INF_F ? 0.f : exp2f(mw[q] - M);
+        L += f * lw[q];
+        acc += f * ow[q];
+      }
+    }
+    for (; i < nparts; ++i) {
+      const int64_t sl = int64_t(u) + first + i;
+      const float mw = p.ws_m[sl * 16 + g];
+      const float f = mw == -CUDART_INF_F ? 0.f : exp2f(mw - M);
+      L += f * p.ws_l[sl * 16 + g];
+      acc += f * p.ws_o[(sl * 16 + g) * kHeadDim + d];
+    }
+    p.out[(orow + g) * kHeadDim + d] = L > 0.f ? acc / L : 0.f;
+    if (d == 0) p.lse[orow + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
+  }
+}
+
 template <int NT, bool LAZY, int STAGES>
 cudaError_t set_attr() {
   return cudaFuncSetAttribute(attn_split_kernel<NT, LAZY, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -711,8 +672,10 @@ cudaError_t set_attr() {
 
 template <int NT, bool LAZY, int STAGES>
 cudaError_t launch_one(const spkv_cache* c, const AttnParams& p, int grid, cudaStream_t st) {
-  return launch_pdl(attn_split_kernel<NT, LAZY, STAGES>, dim3(grid), dim3(kThreads), smem_bytes<NT, STAGES>(), st,
-                    c->tmap_k, c->tmap_v, p);
+  cudaError_t e = launch_pdl(attn_split_kernel<NT, LAZY, STAGES>, dim3(grid), dim3(kThreads),
+                             smem_bytes<NT, STAGES>(), st, c->tmap_k, c->tmap_v, p);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(attn_combine_kernel<NT>, dim3(p.B * p.Hk), dim3(kHeadDim), 0, st, p);
 }
 
 constexpr int kStages1 = 5;   // G <= 8: 5 stages of 34 KiB

@@ -19,7 +19,7 @@ struct spkv_cache {
   float* ws_m = nullptr;         // split-K partial row max   [slots][16]
   float* ws_l = nullptr;         // split-K partial row sum   [slots][16]
   float* ws_o = nullptr;         // split-K partial outputs   [slots][16][128]
-  int32_t* ws_cnt = nullptr;     // per-unit arrival counters [max_units] + 2 chunk-scheduler words
+  int32_t* ws_cnt = nullptr;     // per unit (first segment, segments) [2 * max_units], then the chunk counter
   int64_t ws_slots = 0;
   int32_t max_units = 0;
   int attn_grid = 0;             // CTAs of the split-K attention kernel (one per SM)
@@ -62,8 +62,8 @@ struct AttnParams {
   float* ws_m;
   float* ws_l;
   float* ws_o;
-  int32_t* ws_cnt;
-  int32_t* ws_ctl;               // [0] next chunk to hand out, [1] CTAs finished; both 0 between calls
+  int32_t* ws_parts;             // per unit: first segment and number of segments (partials)
+  int32_t* ws_ctl;               // [0] next chunk to hand out; 0 between calls
   int max_chunks;                // chunks of the page sequence at most (workspace slots = units + this)
   int min_chunk;                 // smallest segment length (keeps a unit's partials <= 256)
   // sparse form

@@ -16,8 +16,8 @@
 //   * the first call on a device looks up the array's device address (cudaGetSymbolAddress)
 //     with that device current, so make that first call before any stream capture;
 //   * all calls on a device share the one array and it keeps the last call's contents; the
-//     arrival counters, the chunk-scheduler words (and the fallback error word) are cleared at
-//     the start of every call;
+//     chunk counter (and the fallback error word) are cleared at the start of every call, and
+//     every call rewrites the per-unit partial records before reading them;
 //     two calls whose kernels overlap on the GPU (different streams, no ordering) race on it;
 //   * nothing here calls cudaMalloc, cudaFree or any allocating routine.
 #include <cudaTypedefs.h>
@@ -35,7 +35,7 @@ constexpr int64_t kSlots = int64_t(2 * SPKV_NOALLOC_MAX_CTAS) + SPKV_NOALLOC_MAX
 // Byte layout of the scratch array (each region 256-byte aligned).
 constexpr int64_t kOffErr = 0;
 constexpr int64_t kOffCnt = 256;
-constexpr int64_t kOffM = kOffCnt + ((SPKV_NOALLOC_MAX_UNITS * 4 + 255) / 256) * 256;
+constexpr int64_t kOffM = kOffCnt + ((SPKV_NOALLOC_MAX_UNITS * 8 + 255) / 256) * 256;
 constexpr int64_t kOffL = kOffM + kSlots * 16 * 4;
 constexpr int64_t kOffO = kOffL + kSlots * 16 * 4;
 constexpr int64_t kScratchBytes = kOffO + kSlots * 16 * 128 * 4;
@@ -131,7 +131,6 @@ extern "C" int sparse_decode_attn_noalloc(const void* k_pool, const void* v_pool
   uint32_t* err = dev_err ? dev_err : reinterpret_cast<uint32_t*>(base + kOffErr);
   int32_t* cnt = reinterpret_cast<int32_t*>(base + kOffCnt);
   const int64_t units = int64_t(B) * n_kv_heads;
-  if (cudaMemsetAsync(cnt, 0, sizeof(int32_t) * units, st) != cudaSuccess) return SPKV_ECUDA;
   if (!dev_err && cudaMemsetAsync(err, 0, sizeof(uint32_t), st) != cudaSuccess) return SPKV_ECUDA;
   if (cudaMemsetAsync(base + kOffErr + 16, 0, 2 * sizeof(int32_t), st) != cudaSuccess) return SPKV_ECUDA;
 
@@ -149,7 +148,7 @@ extern "C" int sparse_decode_attn_noalloc(const void* k_pool, const void* v_pool
   p.ws_m = reinterpret_cast<float*>(base + kOffM);
   p.ws_l = reinterpret_cast<float*>(base + kOffL);
   p.ws_o = reinterpret_cast<float*>(base + kOffO);
-  p.ws_cnt = cnt;
+  p.ws_parts = cnt;
   p.ws_ctl = reinterpret_cast<int32_t*>(base + kOffErr + 16);   // inside the 256-byte first region
   p.max_chunks = 2 * SPKV_NOALLOC_MAX_CTAS;
   p.min_chunk = (sel_stride + 125) / 126;

@@ -181,6 +181,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol = LAZY ? l2_policy_evict_normal() : l2_policy_evict_first();
     int last_unit = -1, last_chunk = -1, jl = 0;
     bool ok = true;
+    // lane 0 keeps the next dynamic chunk index requested one segment ahead, so the atomic's
+    // latency overlaps the streaming of the current segment
+    int ahead = 0;
+    if (lane == 0 && n_chunks > 0) ahead = atomicAdd(&p.ws_ctl[0], 1);
     for (int it = 0; ok; ++it) {
       int c, x0, x1;   // segment id and its page range
       if (it == 0 && S0 > 0) {
@@ -188,10 +192,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         x0 = blockIdx.x * S0;
         x1 = x0 + S0;
       } else {
-        int k = 0;
-        if (lane == 0) k = atomicAdd(&p.ws_ctl[0], 1);
-        k = __shfl_sync(0xffffffffu, k, 0);
-        if (k >= n_chunks) break;
+        const int k = __shfl_sync(0xffffffffu, ahead, 0);
+        if (n_chunks == 0 || k >= n_chunks) break;
+        if (lane == 0) ahead = atomicAdd(&p.ws_ctl[0], 1);
         c = N + k;
         x0 = D0 + k * CH;
         x1 = min(T, x0 + CH);
@@ -618,46 +621,52 @@ __global__ void __launch_bounds__(kThreads, 1)
   flush(cur_u, cur_c, cur_us, cur_uc, 1);
 }
 
-// Merges the split-K partials of every unit that spans several segments (one CTA per unit,
-// thread d owns output dimension d), then resets the chunk counter for the next launch.
-template <int NT>
-__global__ void __launch_bounds__(kHeadDim)
+// Merges the split-K partials of every unit that spans several segments: one CTA per unit,
+// one thread per (query head, output dimension); an online (max, sum) merge over batches of
+// eight partials keeps eight independent loads in flight per thread.  Also resets the chunk
+// counter for the next launch.
+constexpr int kCombineHeads = 4;   // query heads per combine CTA pass (4 x 128 threads)
+
+__global__ void __launch_bounds__(kCombineHeads * kHeadDim)
     attn_combine_kernel(const __grid_constant__ AttnParams p) {
   pdl_wait();
   pdl_trigger();
-  const int u = blockIdx.x, d = threadIdx.x;
-  if (u == 0 && d == 0) p.ws_ctl[0] = 0;
+  const int u = blockIdx.x, d = threadIdx.x % kHeadDim;
+  if (u == 0 && threadIdx.x == 0) p.ws_ctl[0] = 0;
   const int first = p.ws_parts[2 * u], nparts = p.ws_parts[2 * u + 1];
   if (nparts <= 1) return;
   const int b = u / p.Hk, h = u % p.Hk;
   const int64_t orow = int64_t(b) * p.Hq + h * p.G;
-  for (int g = 0; g < p.G; ++g) {
-    float M = -CUDART_INF_F;
-    for (int i = 0; i < nparts; ++i) M = fmaxf(M, p.ws_m[(int64_t(u) + first + i) * 16 + g]);
-    float L = 0.f, acc = 0.f;
-    int i = 0;
-    for (; i + 4 <= nparts; i += 4) {
-      float mw[4], lw[4], ow[4];
+  for (int g = threadIdx.x / kHeadDim; g < p.G; g += kCombineHeads) {
+    float M = -CUDART_INF_F, L = 0.f, acc = 0.f;
+    for (int i0 = 0; i0 < nparts; i0 += 8) {
+      float mw[8], lw[8], ow[8];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int64_t sl = int64_t(u) + first + i + q;
-        mw[q] = p.ws_m[sl * 16 + g];
-        lw[q] = p.ws_l[sl * 16 + g];
-        ow[q] = p.ws_o[(sl * 16 + g) * kHeadDim + d];
+      for (int q = 0; q < 8; ++q) {
+        if (i0 + q < nparts) {
+          const int64_t sl = int64_t(u) + first + i0 + q;
+          mw[q] = p.ws_m[sl * 16 + g];
+          lw[q] = p.ws_l[sl * 16 + g];
+          ow[q] = p.ws_o[(sl * 16 + g) * kHeadDim + d];
+        } else {
+          mw[q] = -CUDART_INF_F;
+          lw[q] = ow[q] = 0.f;
+        }
       }
+      float mb = M;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float f = mw[q] == -CUDART_INF_F ? 0.f : exp2f(mw[q] - M);
+      for (int q = 0; q < 8; ++q) mb = fmaxf(mb, mw[q]);
+      if (mb == -CUDART_INF_F) continue;
+      const float r = exp2f(M - mb);     // M = -inf gives 0
+      L *= r;
+      acc *= r;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float f = mw[q] == -CUDART_INF_F ? 0.f : exp2f(mw[q] - mb);
         L += f * lw[q];
         acc += f * ow[q];
       }
-    }
-    for (; i < nparts; ++i) {
-      const int64_t sl = int64_t(u) + first + i;
-      const float mw = p.ws_m[sl * 16 + g];
-      const float f = mw == -CUDART_INF_F ? 0.f : exp2f(mw - M);
-      L += f * p.ws_l[sl * 16 + g];
-      acc += f * p.ws_o[(sl * 16 + g) * kHeadDim + d];
+      M = mb;
     }
     p.out[(orow + g) * kHeadDim + d] = L > 0.f ? acc / L : 0.f;
     if (d == 0) p.lse[orow + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
@@ -675,7 +684,7 @@ cudaError_t launch_one(const spkv_cache* c, const AttnParams& p, int grid, cudaS
   cudaError_t e = launch_pdl(attn_split_kernel<NT, LAZY, STAGES>, dim3(grid), dim3(kThreads),
                              smem_bytes<NT, STAGES>(), st, c->tmap_k, c->tmap_v, p);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_combine_kernel<NT>, dim3(p.B * p.Hk), dim3(kHeadDim), 0, st, p);
+  return launch_pdl(attn_combine_kernel, dim3(p.B * p.Hk), dim3(kCombineHeads * kHeadDim), 0, st, p);
 }
 
 constexpr int kStages1 = 5;   // G <= 8: 5 stages of 34 KiB

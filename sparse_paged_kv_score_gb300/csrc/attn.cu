@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     // ================================================================ producer warp
-    const uint64_t pol = LAZY ? l2_policy_evict_normal() : l2_policy_evict_first();
+    const uint64_t pol = l2_policy_evict_first();   // each page is read once per call
     int last_unit = -1, last_chunk = -1, jl = 0;
     bool ok = true;
     // lane 0 keeps the next dynamic chunk index requested one segment ahead, so the atomic's

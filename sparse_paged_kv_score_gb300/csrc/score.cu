@@ -31,6 +31,15 @@ __global__ void __launch_bounds__(kWarps * 32)
   pdl_trigger();
   const int u = blockIdx.y, b = u / Hk, h = u % Hk;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int p_begin = blockIdx.x * kPagesPerBlock;
+  const int p_end = min(np_max, p_begin + kPagesPerBlock);
+  // Each warp owns 8 consecutive pages: one load round for their physical ids (lanes 0..7,
+  // issued before the query sum so both latencies overlap), then two rounds of 4 pages x 4
+  // sub-blocks = 16 independent 16-byte loads per lane.
+  const int pw0 = p_begin + warp * 8;
+  int ph = 0;
+  if (lane < 8 && pw0 + lane < p_end) ph = page_table[int64_t(b) * np_max + pw0 + lane];
+  const int L = seq_len[b];
   __shared__ float qs[kHeadDim];
   if (tid < kHeadDim / 2) {
     float s0 = 0.f, s1 = 0.f;
@@ -44,45 +53,40 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
   __syncthreads();
   const float4 qv = reinterpret_cast<const float4*>(qs)[lane];
-  const int L = seq_len[b];
   const int local = L >= 1 ? (L - 1) / kPageTokens : 0;
   if (L < 1 && tid == 0 && blockIdx.x == 0) flag_error(err, SPKV_DEVERR_PAGE_ID);
-  const int p_begin = blockIdx.x * kPagesPerBlock;
-  const int p_end = min(np_max, p_begin + kPagesPerBlock);
   const float* plane = ksum + int64_t(h) * n_phys * (kNSub * kHeadDim);
   float* srow = scores + int64_t(u) * np_max;
-
-  // two pages per warp iteration keep 8 independent 16-byte loads in flight per lane
-  for (int p = p_begin + warp; p < p_end; p += 2 * kWarps) {
-    const int pp[2] = {p, p + kWarps};
-    float4 v[2][kNSub];
-    bool live[2];
+  bool okp = false;
+  if (lane < 8 && pw0 + lane < p_end && pw0 + lane < local) {
+    okp = ph >= 0 && ph < n_phys;
+    if (!okp) flag_error(err, SPKV_DEVERR_PHYS);
+  }
+  if (!okp) ph = 0;
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      live[k] = pp[k] < p_end && pp[k] < local;
-      int ph = 0;
-      if (live[k]) {
-        ph = page_table[int64_t(b) * np_max + pp[k]];
-        if (ph < 0 || ph >= n_phys) {
-          if (lane == 0) flag_error(err, SPKV_DEVERR_PHYS);
-          live[k] = false;
-        }
-      }
-      const float4* base = reinterpret_cast<const float4*>(plane + int64_t(ph) * (kNSub * kHeadDim));
+  for (int half = 0; half < 2; ++half) {
+    float4 v[4][kNSub];
+    bool live[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int src = half * 4 + k;
+      const int phk = __shfl_sync(0xffffffffu, ph, src);
+      live[k] = __shfl_sync(0xffffffffu, okp ? 1 : 0, src) != 0;
+      const float4* base = reinterpret_cast<const float4*>(plane + int64_t(phk) * (kNSub * kHeadDim));
 #pragma unroll
       for (int j = 0; j < kNSub; ++j)
         v[k][j] = live[k] ? __ldcs(base + j * (kHeadDim / 4) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      if (pp[k] >= p_end) continue;
+    for (int k = 0; k < 4; ++k) {
+      const int pg = pw0 + half * 4 + k;
       float best = -CUDART_INF_F;
 #pragma unroll
       for (int j = 0; j < kNSub; ++j) {
         const float d = warp_sum(v[k][j].x * qv.x + v[k][j].y * qv.y + v[k][j].z * qv.z + v[k][j].w * qv.w);
         best = fmaxf(best, d);
       }
-      if (lane == 0) srow[pp[k]] = live[k] ? best * scale : -CUDART_INF_F;
+      if (lane == 0 && pg < p_end) srow[pg] = live[k] ? best * scale : -CUDART_INF_F;
     }
   }
 }

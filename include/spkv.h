@@ -118,7 +118,7 @@ int paged_kv_append(spkv_cache_t cache, const int32_t* phys_page, const int32_t*
  *   scores[b][h][p] = max_j (sum_g q[b][h*G+g]) . ksum[h][page_table[b][p]][j] / (16 sqrt(128))
  * i.e. the sub-block scores of the G query heads of the group are summed before the max.
  * Entries p >= l_b are -inf.
- *   q          : device bf16 [B][Hq][128]
+ *   q          : device bf16 [B][Hq][128], 8-byte aligned
  *   page_table : device int32 [B][np_max], physical page of each logical page
  *   seq_len    : device int32 [B], tokens in each request's context (>= 1)
  *   scores     : device fp32 [B][n_kv_heads][np_max] (output) */

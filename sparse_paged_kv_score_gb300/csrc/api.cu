@@ -182,7 +182,7 @@ int score_blocks(spkv_cache_t c, const void* q, int B, int Hq, const int32_t* pa
   int st = check_group(c, B, Hq);
   if (st != SPKV_OK) return st;
   if (B == 0) return SPKV_OK;
-  if (!q || !page_table || !seq_len || !scores || np_max <= 0 || !aligned(q, 4)) return SPKV_EINVAL;
+  if (!q || !page_table || !seq_len || !scores || np_max <= 0 || !aligned(q, 8)) return SPKV_EINVAL;
   return status_of(spkv::launch_score(c, q, B, Hq, page_table, np_max, seq_len, scores, as_stream(stream)));
 }
 

@@ -123,8 +123,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
   }
-  pdl_wait();      // the page lists and counts below are written by the previous kernel
-  pdl_trigger();
+  // The page lists and counts below are written by the previous kernel.  This kernel does not
+  // trigger its dependent early: the combine kernel's CTAs would only sit on the SMs while the
+  // pages stream (CTA exit triggers it).
+  pdl_wait();
 
   // ---- 1. unit prefix table: prefix[u] = first global page position of unit u, prefix[U] = T
   const int c0 = static_cast<int>(int64_t(tid) * U / kThreads);

@@ -161,6 +161,17 @@ __device__ __forceinline__ uint32_t float_order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Adds 1 to hist[bin] for every active lane that passes `take`, with one shared-memory atomic per
+// distinct bin in the warp (lanes with equal bins are grouped by __match_any_sync).  Must be
+// called by all 32 lanes of the warp.
+__device__ __forceinline__ void warp_hist_add(int* hist, int bin, bool take) {
+  const unsigned active = __ballot_sync(0xffffffffu, take);
+  if (!take) return;
+  const unsigned peers = __match_any_sync(active, bin);
+  const int lane = threadIdx.x & 31;
+  if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+}
+
 __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bits) {
   if (bits) atomicOr(err, bits);
 }

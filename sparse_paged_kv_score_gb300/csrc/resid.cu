@@ -125,15 +125,17 @@ __global__ void __launch_bounds__(kLruThreads)
   }
   __syncthreads();
   // 2. buckets and histograms
-  for (int s = tid; s < n_slots; s += blockDim.x) {
+  for (int s0 = 0; s0 < n_slots; s0 += blockDim.x) {   // whole warps iterate together
+    const int s = s0 + tid;
     int bk = 63;
-    if (rrow[s] >= 0) {
+    const bool in = s < n_slots;
+    if (in && rrow[s] >= 0) {
       const int64_t age = int64_t(t_now) - trow[s];
       bk = age <= 0 ? 0 : static_cast<int>(age / W < 63 ? age / W : 63);
     }
-    bucket[s] = static_cast<uint8_t>(bk);
-    atomicAdd(&hist[bk], 1);
-    if (!touched[s]) atomicAdd(&hist_u[bk], 1);
+    if (in) bucket[s] = static_cast<uint8_t>(bk);
+    warp_hist_add(hist, bk, in);
+    warp_hist_add(hist_u, bk, in && !touched[s]);
   }
   __syncthreads();
   int avail = 0;

@@ -80,8 +80,11 @@ __device__ void block_topk(const uint32_t* keys, const uint8_t* cand, uint8_t* f
     for (int i = tid; i < 256; i += blockDim.x) sh.hist[i] = 0;
     __syncthreads();
     const uint32_t pre = static_cast<uint32_t>(sh.prefix);
-    for (int i = tid; i < n; i += blockDim.x)
-      if (cand[i] && (keys[i] & hmask) == (pre & hmask)) atomicAdd(&sh.hist[(keys[i] >> shift) & 255u], 1);
+    for (int i0 = 0; i0 < n; i0 += blockDim.x) {   // whole warps iterate together
+      const int i = i0 + tid;
+      const bool take = i < n && cand[i] && (keys[i] & hmask) == (pre & hmask);
+      warp_hist_add(sh.hist, take ? static_cast<int>((keys[i] >> shift) & 255u) : 0, take);
+    }
     __syncthreads();
     if (tid < 32) {
       // lane L owns bins 8*(31-L) .. 8*(31-L)+7, so lane 0 holds the largest bins
@@ -159,6 +162,14 @@ __global__ void __launch_bounds__(kSelThreads)
   const int64_t row = int64_t(u) * np_max;
   uint32_t* aw = alive + int64_t(u) * words;
 
+  // query-score keys of this thread's first pages, loaded now so the load overlaps Gamma_e
+  constexpr int kPre = 4;
+  uint32_t qkey[kPre];
+#pragma unroll
+  for (int r = 0; r < kPre; ++r) {
+    const int i = tid + r * blockDim.x;
+    qkey[r] = i < np_max ? float_order_key(qs[row + i]) : 0u;
+  }
   // ---- Gamma_e: top-k_e of the alive candidates by eviction score
   for (int i = tid; i < np_max; i += blockDim.x) {
     const bool a = (aw[i >> 5] >> (i & 31)) & 1u;
@@ -178,7 +189,15 @@ __global__ void __launch_bounds__(kSelThreads)
     if (clear) aw[w] = word & ~clear;
   }
   // ---- Gamma_q: top-k_q of the candidates outside E by query score
-  for (int i = tid; i < np_max; i += blockDim.x) {
+#pragma unroll
+  for (int r = 0; r < kPre; ++r) {
+    const int i = tid + r * blockDim.x;
+    if (i < np_max) {
+      cand[i] = (i < nc && !(flags[i] & kInE)) ? 1 : 0;
+      keys[i] = qkey[r];
+    }
+  }
+  for (int i = tid + kPre * blockDim.x; i < np_max; i += blockDim.x) {
     cand[i] = (i < nc && !(flags[i] & kInE)) ? 1 : 0;
     keys[i] = float_order_key(qs[row + i]);
   }

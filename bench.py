@@ -63,6 +63,23 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def rank_max(v: float, device) -> float:
+    """Max of v over the ranks of the default process group (v itself without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world: int, bytes_per_rank_step: float, ms_max: float) -> float:
+    """Whole-job GB/s of `world` independent replicas, each moving bytes_per_rank_step per step,
+    when the slowest rank takes ms_max per step (weak scaling: per-rank work is fixed)."""
+    return world * bytes_per_rank_step / (ms_max * 1e-3) / 1e9
+
+
 def measured_traffic():
     """DRAM bytes per full attention launch from the committed ncu summary, or None when the
     kernel source has changed since those counters were taken."""
@@ -326,19 +343,14 @@ def run_native(args):
         barrier()
     eager_ms = statistics.mean(timed(step, timed_idx))
     attn_ms = timed(lambda i: spkv.sparse_decode_attn(cache, qs[i], pt, sel, n_sel, seq, out, lse), timed_idx)
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = rank_max(statistics.mean(step_ms), dev)
     st, bits = spkv.get_device_error(cache)
     if st != 0:
         raise RuntimeError(f"device error bits {bits} in the timed region")
 
     byts = step_bytes(w, k)
     step_total = sum(v for kk, v in byts.items() if kk != "attn_kv")
-    value = world * step_total / (ms * 1e-3) / 1e9
+    value = replica_throughput(world, step_total, ms)
     attn_avg = statistics.mean(attn_ms)
     peak, peak_kind = peaks()
     achieved = byts["attn_kv"] / (attn_avg * 1e-3) / 1e9
@@ -457,13 +469,8 @@ def run_native(args):
         flush.zero_()
         eev.append((a, b_))
     barrier()
-    e2e_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in eev)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * step_total / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = rank_max(statistics.mean(a.elapsed_time(b_) for a, b_ in eev), dev)
+    e2e_value = replica_throughput(world, step_total, e2e_ms)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

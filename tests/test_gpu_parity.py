@@ -370,3 +370,71 @@ def test_setdiff_and_lru_trajectory_bitexact(W):
         assert np.array_equal(t_dev.cpu().numpy(), ts)
     assert d.errors() == (0, 0)
     d.close()
+
+
+# ------------------------------------------------------------------ more shapes and edge cases
+
+@pytest.mark.parametrize("Hq,Hk", [(32, 2), (24, 2), (12, 1)])
+def test_lazy_rope_large_groups(Hq, Hk):
+    """Group sizes 9..16 take the two-n-tile path of the kernel (16 query heads per tile)."""
+    w = gen.lazy_rag(seed=7, B=3, Hq=Hq, Hk=Hk, n_docs=8, docs_per_req=3, min_len=64, max_len=1200)
+    cache, keep = _lazy_dev(w)
+    words = _words(w["phys"], w["valid"], w["slot"])
+    B = w["B"]
+    out = torch.empty(B, Hq, 128, dtype=torch.float32, device=DEV)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=DEV)
+    spkv.lazy_rope_decode_attn(cache, bf(w["q"]), i32(w["qpos"]), u32_as_i32(words), i32(w["n_pages"]),
+                               i32(w["doc_pos"]), w["theta"], out, lse)
+    ro, rl = oracle.lazy_attn_batch(w["q"], w["k_pool"], w["v_pool"], w["phys"], w["valid"], w["slot"],
+                                    w["n_pages"], w["qpos"], w["doc_pos"], w["theta"], materialise=True)
+    mx, mean = attn_errors(out.cpu().numpy(), ro)
+    assert mx <= ATTN_MAX and mean <= ATTN_MEAN, (mx, mean)
+    assert np.abs(lse.cpu().numpy() - rl).max() <= LSE_TOL
+    cache.close()
+
+
+def test_all_units_empty():
+    w = gen.sparse_workload(3, 8, 2, 64 * 4, 2, 2, seed=1)
+    d = Dev(w)
+    sel = np.full((3, 2, 5), -1, np.int32)
+    n_sel = np.zeros((3, 2), np.int32)
+    out, lse = d.attn(i32(sel), i32(n_sel))
+    assert (out.cpu().numpy() == 0).all() and np.isneginf(lse.cpu().numpy()).all()
+    out2, lse2 = d.attn(i32(sel), i32(n_sel))     # the chunk counter must be intact
+    assert torch.equal(out, out2)
+    assert d.errors() == (0, 0)
+    d.close()
+
+
+def test_large_budgets_and_long_context_selection():
+    """k = 600 pages of 2047 candidates: several radix passes with many ties at the threshold."""
+    w = gen.sparse_workload(2, 8, 2, 64 * 2048, 300, 300, seed=17, extra_tokens=0)
+    d = Dev(w)
+    s = d.scores()
+    s = torch.round(s * 8) / 8                      # coarse scores: many exact ties
+    e = np.round(w["evict"] * 4) / 4
+    alive = d.new_alive()
+    sel, n_sel = _check_select_bitexact(d, s, e, alive, w["k_q"], w["k_e"])
+    out, lse = d.attn(sel, n_sel)
+    ro, rl = oracle.sparse_attn_batch(w["q"], w["k_pool"], w["v_pool"], w["page_table"], sel.cpu().numpy(),
+                                      n_sel.cpu().numpy(), w["seq_len"])
+    mx, mean = attn_errors(out.cpu().numpy(), ro)
+    assert mx <= ATTN_MAX and mean <= ATTN_MEAN, (mx, mean)
+    assert d.errors() == (0, 0)
+    d.close()
+
+
+def test_one_unit_many_pages_split_across_all_ctas():
+    """A single (request, kv head) unit of 2000 pages: the split-K merge of hundreds of parts."""
+    w = gen.sparse_workload(1, 4, 1, 64 * 2000 + 5, 8, 8, seed=23)
+    d = Dev(w)
+    n = 2001
+    sel = np.arange(n, dtype=np.int32).reshape(1, 1, n)
+    n_sel = np.full((1, 1), n, np.int32)
+    out, lse = d.attn(i32(sel), i32(n_sel))
+    ro, rl = oracle.sparse_attn_batch(w["q"], w["k_pool"], w["v_pool"], w["page_table"], sel, n_sel, w["seq_len"])
+    mx, mean = attn_errors(out.cpu().numpy(), ro)
+    assert mx <= ATTN_MAX and mean <= ATTN_MEAN, (mx, mean)
+    assert np.abs(lse.cpu().numpy() - rl).max() <= LSE_TOL
+    assert d.errors() == (0, 0)
+    d.close()

@@ -69,7 +69,7 @@ struct Smem {
   // hand-off buffer from the consumer warps to the epilogue warp
   float cm[kConsumers][kG];
   float cl[kConsumers][kG];
-  float co[kConsumers][kG][kHeadDim];
+  float co[kConsumers][kG][kHeadDim + 4];   // rows padded: the consumers' stores are conflict-free
   int h_unit, h_chunk, h_ustart, h_ucount, h_last, h_pad[3];
   uint64_t full[8];
   uint64_t empty[8];

@@ -506,7 +506,7 @@ def run_native(args):
             "lazy_rag": rag,
             "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": 7 * args.steps,
+            "gpu_launches": 8 * args.steps,
             "eager_ms_per_step": eager_ms,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,

@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-lazy", action="store_true")
     ap.add_argument("--no-rag", action="store_true", help="skip the lazy-RoPE RAG sub-measurement")
+    ap.add_argument("--no-offload", action="store_true",
+                    help="skip the offload sub-measurement (262k context, pool in pinned host memory)")
     ap.add_argument("--l2", default="none", choices=["none", "write"],
                     help="none: no flush, every step reads ~0.8 GB (> 129 MB L2); write: 256 MiB write "
                          "between timed steps")
@@ -216,6 +218,145 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------- GPU step
+
+def offload_leg(args, dev, stream, timed):
+    """Retrieve over the host link: the 262k-context workload (B8, Hq40/Hk8, 4096 pages per
+    request, k = 128) with the whole K/V pool in pinned host memory and 2048 device slots per
+    (request, kv head).  The pooled-key summaries stay on the device (built once from a device
+    copy of the pool); every page that attention reads comes from a slot."""
+    import torch
+    import gen
+    import sparse_paged_kv_score_gb300 as spkv
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+
+    def pinned(a):
+        t = torch.empty(a.shape, dtype=torch.int16, pin_memory=True)
+        t.numpy()[...] = a.view(np.int16)
+        return t.view(torch.bfloat16)
+
+    w = gen.long262k(seed=0)
+    B, Hq, Hk, npm = w["B"], w["Hq"], w["Hk"], w["np_max"]
+    U = B * Hk
+    k_q, k_e = w["k_q"], w["k_e"]
+    stride = k_q + k_e + 1
+    ns = w["n_slots"]
+    dk, dv = bf(w["k_pool"]), bf(w["v_pool"])
+    dks = torch.zeros(Hk, w["n_phys"], 4, 128, dtype=torch.float32, device=dev)
+    scache = spkv.paged_kv_create(dk, dv, dks, i32(gen.page_counts(w)), max_units=U)   # summaries
+    k_host, v_host = pinned(w["k_pool"]), pinned(w["v_pool"])
+    k_slots = torch.zeros(Hk, B * ns, 64, 128, dtype=torch.bfloat16, device=dev)
+    v_slots = torch.zeros_like(k_slots)
+    slots = spkv.paged_kv_create(k_slots, v_slots, None, None, max_units=U)
+    pt, seq = i32(w["page_table"]), i32(w["seq_len"])
+    n_iter = args.warmup + args.steps
+    qs = [bf(q) for q in gen.walk_queries(w, n_iter + 1)]
+    ev = torch.from_numpy(w["evict"].astype(np.float32)).to(dev)
+    scores = torch.empty(B, Hk, npm, dtype=torch.float32, device=dev)
+    alive = torch.full((B, Hk, (npm + 31) // 32), -1, dtype=torch.int32, device=dev)
+    sel = torch.empty(B, Hk, stride, dtype=torch.int32, device=dev)
+    n_sel = torch.empty(B, Hk, dtype=torch.int32, device=dev)
+    resident = torch.full((U, ns), -1, dtype=torch.int32, device=dev)
+    ts = torch.full((U, ns), np.iinfo(np.int32).min, dtype=torch.int32, device=dev)
+    missing = torch.empty(U, stride, dtype=torch.int32, device=dev)
+    n_missing = torch.empty(U, dtype=torch.int32, device=dev)
+    slot = torch.empty(U, stride, dtype=torch.int32, device=dev)
+    victims = torch.empty(U, stride, dtype=torch.int32, device=dev)
+    hist = torch.empty(U, 64, dtype=torch.int32, device=dev)
+    out = torch.empty(B, Hq, 128, dtype=torch.float32, device=dev)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+
+    def select_and_plan(i):
+        spkv.score_blocks(scache, qs[i], pt, seq, scores)
+        spkv.select_topk(scache, scores, ev, alive, seq, k_q, k_e, sel, n_sel)
+        spkv.resident_setdiff(scache, resident, sel, n_sel, missing, n_missing, slot)
+        spkv.lru_bucket_update(scache, resident, ts, slot, n_sel.view(U), missing, n_missing, i, 1, victims, hist)
+
+    def retrieve():
+        spkv.retrieve_pages(slots, k_host, v_host, pt, missing, n_missing, victims, slot, n_sel, ns)
+
+    def attend(i):
+        spkv.sparse_decode_attn_slots(slots, qs[i], sel, slot.view(B, Hk, stride), n_sel, ns, seq, out, lse)
+
+    # cold swap-in: every slot empty, so every selected page crosses the host link
+    select_and_plan(0)
+    slot0 = slot.clone()
+    cold_pages = int(n_missing.sum().item())
+    retrieve()
+    attend(0)
+
+    def cold(_):
+        slot.copy_(slot0)    # the slot list is completed in place; restore it (outside the events)
+
+    cold_ms = []
+    for r in range(3 + args.steps):
+        cold(r)
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        retrieve()
+        b_.record(stream)
+        torch.cuda.synchronize()
+        if r >= 3:
+            cold_ms.append(a.elapsed_time(b_))
+    cold_bytes = cold_pages * PAGE_BYTES
+    cold_avg = statistics.mean(cold_ms)
+    # copy-engine reference over the same link: one 1 GiB pinned -> device copy
+    src = torch.empty(1 << 29, dtype=torch.int16, pin_memory=True)
+    dst = torch.empty(1 << 29, dtype=torch.int16, device=dev)
+    for _ in range(2):
+        dst.copy_(src, non_blocking=True)
+    ce_ms = statistics.mean(timed(lambda i: dst.copy_(src, non_blocking=True), range(5)))
+    ce_gbs = (1 << 30) / (ce_ms * 1e-3) / 1e9
+    del src, dst
+
+    # steady offloaded decode steps (the query walks, so most selected pages stay resident)
+    step_ms, ret_ms, att_ms, miss = [], [], [], []
+    for i in range(1, n_iter + 1):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e[0].record(stream)
+        select_and_plan(i)
+        e[1].record(stream)
+        retrieve()
+        e[2].record(stream)
+        attend(i)
+        e[3].record(stream)
+        torch.cuda.synchronize()
+        if i > args.warmup:
+            step_ms.append(e[0].elapsed_time(e[3]))
+            ret_ms.append(e[1].elapsed_time(e[2]))
+            att_ms.append(e[2].elapsed_time(e[3]))
+            miss.append(int(n_missing.sum().item()))
+    for c in (scache, slots):
+        st, bits = spkv.get_device_error(c)
+        if st != 0:
+            raise RuntimeError(f"device error bits {bits} in the offload leg")
+    scache.close()
+    slots.close()
+    ms = statistics.mean(step_ms)
+    r_ms = statistics.mean(ret_ms)
+    attn_bytes = int(n_sel.sum().item()) * PAGE_BYTES
+    out_d = {
+        "workload": w["name"] + ", K/V pool (8.6 GB) in pinned host memory, 2048 device slots per unit",
+        "retrieve_cold": {"pages": cold_pages, "bytes": cold_bytes, "us": cold_avg * 1e3,
+                          "GBps": cold_bytes / (cold_avg * 1e-3) / 1e9,
+                          "bound": "host link (NVLink-C2C)", "peak": ce_gbs,
+                          "peak_kind": "measured copy-engine pinned-host-to-device copy of 1 GiB",
+                          "frac": cold_bytes / (cold_avg * 1e-3) / 1e9 / ce_gbs},
+        "step": {"launch": "eager, one call per kernel", "ms_per_step": ms, "queries_per_s": B / (ms * 1e-3),
+                 "missing_pages_per_step": statistics.mean(miss),
+                 "retrieve_us": r_ms * 1e3,
+                 "retrieve_GBps": statistics.mean(miss) * PAGE_BYTES / (r_ms * 1e-3) / 1e9,
+                 "attn_slots_us": statistics.mean(att_ms) * 1e3,
+                 "attn_slots_GBps": attn_bytes / (statistics.mean(att_ms) * 1e-3) / 1e9},
+    }
+    del dk, dv, dks, k_slots, v_slots, k_host, v_host
+    torch.cuda.empty_cache()
+    return out_d
+
 
 def run_native(args):
     import torch
@@ -422,6 +563,11 @@ def run_native(args):
                "note": "logical = every (request, head, page) read; shared hot documents hit in L2"}
         del rk, rv, rks, rmeta
 
+    # ---- offload: the 262k-context workload with its K/V pool in pinned host memory
+    offload = None
+    if not args.no_offload and rank == 0:
+        offload = offload_leg(args, dev, stream, timed)
+
     # ---- end to end through the public API: pinned host inputs in, outputs back, every step
     q_h = [torch.empty(B, Hq, 128, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     e_h = [torch.empty(B, Hk, npm, dtype=torch.float32).pin_memory() for _ in range(2)]
@@ -504,6 +650,7 @@ def run_native(args):
                          "traffic": measured_traffic() if B == 32 else None},
             "lazy_attn": lazy,
             "lazy_rag": rag,
+            "offload": offload,
             "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": 8 * args.steps,

@@ -8,6 +8,8 @@
  *   select_topk          per-KV-head top-k pages: eviction-head budget k_e + query budget k_q
  *   resident_setdiff     selected pages that are not resident (swap-in list)
  *   lru_bucket_update    64-bucket LRU recency update and victim choice
+ *   retrieve_pages       swap-in of the missing pages from a host pool into resident slots
+ *   sparse_decode_attn_slots  attention reading the selected pages from their resident slots
  *   sparse_decode_attn   split-K flash decoding over the selected pages
  *   lazy_rope_decode_attn  the same with deferred RoPE (query rotated once per document)
  *
@@ -76,6 +78,9 @@ typedef struct spkv_cache* spkv_cache_t; /* opaque, library-owned */
  *                    paged_kv_create, updated by paged_kv_append.
  *   max_units      : the largest B * n_kv_heads any call on this handle will use (sizes the
  *                    split-K workspace); 0 means 4096, larger than 4096 is SPKV_EINVAL.
+ * ksum and page_cnt may both be NULL: the handle then has no summaries (for a pool of resident
+ * slots that is attended but never scored, see retrieve_pages); score_blocks and
+ * paged_kv_append on it return SPKV_EINVAL.
  */
 typedef struct {
   int32_t n_kv_heads;
@@ -193,6 +198,44 @@ int lazy_rope_decode_attn(spkv_cache_t cache, const void* q, int B, int Hq, cons
 int resident_setdiff(spkv_cache_t cache, const int32_t* resident, int n_slots, const int32_t* sel,
                      const int32_t* n_sel, int sel_stride, int n_units, int32_t* missing,
                      int32_t* n_missing, int32_t* slot, void* stream);
+
+/* Retrieve: copies the selected pages that are not resident from the host pool into the
+ * resident slots the LRU update chose, and completes the slot list.  [NOSA] "Method 2: the
+ * NOSI system" (the full KV cache lives in host memory; a UVA host-to-device kernel moves the
+ * swapped-in blocks into their GPU slots); [Spin] 2A, the Retrieve operation.
+ * `cache` is a handle over the slot pool: its k_pool / v_pool hold, for kv head h, request b
+ * and slot s, the page at h * n_phys_pages + b * n_slots + s (B * n_slots <= n_phys_pages).
+ * Per unit u = (b, h), for j < n_missing[u]:
+ *   slot page (h, b, victims[u][j]) <- host page (h, page_table[b][missing[u][j]]), K and V;
+ * then the r-th entry of slot[u][0 .. n_sel[u]) that is -1 is set to victims[u][r].
+ *   k_host, v_host : bf16 [n_kv_heads][n_host_pages][64][128] in pinned host memory mapped
+ *                    into the device address space (cudaHostAlloc / cudaHostRegister), read
+ *                    through that address; 16-byte aligned
+ *   page_table     : device int32 [B][np_max], host page of each logical page
+ *   missing, n_missing : from resident_setdiff;  victims: from lru_bucket_update
+ *   slot           : device int32 [B][n_kv_heads][sel_stride] (in/out): resident_setdiff's
+ *                    slot list on entry, every selected page's slot on return
+ *   n_sel          : device int32 [B][n_kv_heads]
+ * Out-of-range ids and slots are skipped (SPKV_DEVERR_PAGE_ID / _PHYS / _SLOT); so is a slot
+ * list whose -1 entries do not number n_missing (SPKV_DEVERR_SLOT).  Requires
+ * B * n_kv_heads <= max_units of the handle. */
+int retrieve_pages(spkv_cache_t cache, const void* k_host, const void* v_host,
+                   int64_t n_host_pages, const int32_t* page_table, int np_max, int B,
+                   const int32_t* missing, const int32_t* n_missing, const int32_t* victims,
+                   int32_t* slot, const int32_t* n_sel, int sel_stride, int n_slots, void* stream);
+
+/* sparse_decode_attn reading every selected page from its resident slot ([NOSA] "Method 2",
+ * attention over the GPU buffer after the swap-in; [Spin] 2A, Attention on the fast tier).
+ * Same result as sparse_decode_attn, with page sel[u][i] of unit u = (b, h) read from slot page
+ * h * n_phys_pages + b * n_slots + slot[u][i] of the handle's pools (as retrieve_pages
+ * addresses them); sel still gives the logical page, hence the valid tokens.
+ *   slot : device int32 [B][n_kv_heads][sel_stride], 0 <= slot < n_slots (else the page is
+ *          skipped, SPKV_DEVERR_SLOT)
+ *   other arguments: as sparse_decode_attn.  B * n_slots <= n_phys_pages. */
+int sparse_decode_attn_slots(spkv_cache_t cache, const void* q, int B, int Hq,
+                             const int32_t* sel, const int32_t* slot, const int32_t* n_sel,
+                             int sel_stride, int n_slots, const int32_t* seq_len, float* out,
+                             float* lse, void* stream);
 
 /* Bucketed LRU update, [Spin] 2B "bucketed LRU policy" (pages grouped into 64 recency
  * buckets by timestamp; eviction without a global sort).  Per unit, at time t_now:

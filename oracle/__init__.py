@@ -64,6 +64,11 @@ def _l():
                                      i32, f64, i32, vp, i32, vp, vp, i32], None),
             "orc_setdiff_batch": ([vp, i32, vp, vp, i32, i32, vp, vp, vp, i32], None),
             "orc_lru_batch": ([vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, i32], None),
+            "orc_retrieve_unit": ([vp, vp, vp, vp, i32, vp, vp, i32, vp, vp], None),
+            "orc_retrieve_batch": ([i32, i32, vp, vp, i64, vp, i32, vp, vp, vp, vp, vp, i32, vp, vp, i64,
+                                    i32, i32], None),
+            "orc_slot_attn_batch": ([i32, i32, i32, vp, vp, vp, i64, vp, vp, vp, i32, i32, vp, vp, i32,
+                                     vp, vp, i32], None),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -281,3 +286,41 @@ def lru_batch(resident, ts, slot, n_sel, missing, n_missing, t: int, W: int, nth
     _l().orc_lru_batch(_p(resident), _p(ts), n_slots, _p(slot), _p(n_sel), _p(missing), _p(n_missing),
                        stride, U, int(t), int(W), _p(victims), _p(hist), nthreads)
     return resident, ts, victims, hist
+
+
+def retrieve_batch(k_host, v_host, page_table, missing, n_missing, victims, slot, n_sel, k_slots, v_slots,
+                   n_slots: int, nthreads: int = 0):
+    """Swap-in: copies missing pages into their victim slots of k_slots / v_slots (uint16
+    [Hk][n_slot_pages][64][128], modified in place).  slot is [B][Hk][stride] (or [U][stride]);
+    returns the completed slot list (same shape)."""
+    k_host, v_host = _c(k_host, np.uint16), _c(v_host, np.uint16)
+    if not (k_slots.dtype == np.uint16 and v_slots.dtype == np.uint16 and k_slots.flags.c_contiguous
+            and v_slots.flags.c_contiguous):
+        raise ValueError("k_slots / v_slots must be C-contiguous uint16 arrays (updated in place)")
+    page_table = _c(page_table, np.int32)
+    missing, n_missing, victims, n_sel = (_c(missing, np.int32), _c(n_missing, np.int32),
+                                          _c(victims, np.int32), _c(n_sel, np.int32))
+    out_slot = _c(slot, np.int32).copy()
+    Hk, n_host = k_host.shape[0], k_host.shape[1]
+    B, np_max = page_table.shape
+    stride = out_slot.shape[-1]
+    _l().orc_retrieve_batch(B, Hk, _p(k_host), _p(v_host), n_host, _p(page_table), np_max, _p(missing),
+                            _p(n_missing), _p(victims), _p(out_slot), _p(n_sel), stride, _p(k_slots),
+                            _p(v_slots), k_slots.shape[1], int(n_slots), nthreads)
+    return out_slot
+
+
+def slot_attn_batch(q, k_slots, v_slots, sel, slot, n_sel, seq_len, n_slots: int, units=None,
+                    nthreads: int = 0):
+    """Attention over the selected pages read from their slots; (out[B][Hq][128], lse[B][Hq])."""
+    q, k_slots, v_slots = _c(q, np.uint16), _c(k_slots, np.uint16), _c(v_slots, np.uint16)
+    sel, slot, n_sel, seq_len = _c(sel, np.int32), _c(slot, np.int32), _c(n_sel, np.int32), _c(seq_len, np.int32)
+    B, Hq, _ = q.shape
+    Hk = k_slots.shape[0]
+    out = np.zeros((B, Hq, D), np.float64)
+    lse = np.zeros((B, Hq), np.float64)
+    u = _units(units, B * Hk)
+    _l().orc_slot_attn_batch(B, Hq, Hk, _p(q), _p(k_slots), _p(v_slots), k_slots.shape[1], _p(sel), _p(slot),
+                             _p(n_sel), sel.shape[-1], int(n_slots), _p(seq_len), _p(u), u.shape[0], _p(out),
+                             _p(lse), nthreads)
+    return out, lse

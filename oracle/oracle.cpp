@@ -384,6 +384,30 @@ void orc_lru_unit(int32_t* resident, int32_t* ts, int n_slots, const int32_t* sl
   }
 }
 
+// ---------------------------------------------------------------- Retrieve (swap-in)
+// [NOSA] "Method 2: NOSI": the full KV cache lives in host memory and the selected blocks that
+// are not GPU-resident are copied into the buffer slots chosen for them; [Spin] 2A, Retrieve.
+// For one unit: for j < n_missing, slot page victims[j] receives host page pt_row[missing[j]]
+// (K and V planes of the unit's kv head); then the j-th entry of slot[0 .. n_sel) that is -1
+// (the j-th missing page, since the set difference lists them in selection order) becomes
+// victims[j].  kslots / vslots point at slot 0 of the unit's own slot range.
+void orc_retrieve_unit(const uint16_t* khost, const uint16_t* vhost, const int32_t* pt_row,
+                       const int32_t* missing, int n_missing, const int32_t* victims, int32_t* slot,
+                       int n_sel, uint16_t* kslots, uint16_t* vslots) {
+  const int64_t page_elems = static_cast<int64_t>(kPage) * kD;
+  for (int j = 0; j < n_missing; ++j) {
+    const int64_t src = static_cast<int64_t>(pt_row[missing[j]]) * page_elems;
+    const int64_t dst = static_cast<int64_t>(victims[j]) * page_elems;
+    for (int64_t e = 0; e < page_elems; ++e) {
+      kslots[dst + e] = khost[src + e];
+      vslots[dst + e] = vhost[src + e];
+    }
+  }
+  int j = 0;
+  for (int i = 0; i < n_sel; ++i)
+    if (slot[i] < 0) slot[i] = victims[j++];
+}
+
 // ---------------------------------------------------------------- batch drivers
 // The same functions applied to a list of (request, kv head) units, one unit per task on a
 // pool of `nthreads` threads (0 = all hardware threads).  Unit u = b * Hk + h.  Pools are
@@ -462,6 +486,51 @@ void orc_lazy_attn_batch(int B, int Hq, int Hk, const uint16_t* q, const uint16_
     else
       orc_attn_lazy_unit(q + qo * kD, G, kpool + plane, vpool + plane, phys + mo, valid + mo,
                          slot + mo, n_pages[b], qpos[b], dp, theta, out + qo * kD, lse + qo);
+  });
+}
+
+// Retrieve for every unit.  Host pools [Hk][n_host][64][128]; slot pools [Hk][n_slot_pages][64][128]
+// with unit (b, h)'s slots at pages b * n_slots .. b * n_slots + n_slots - 1 of plane h.
+void orc_retrieve_batch(int B, int Hk, const uint16_t* khost, const uint16_t* vhost, int64_t n_host,
+                        const int32_t* page_table, int np_max, const int32_t* missing,
+                        const int32_t* n_missing, const int32_t* victims, int32_t* slot,
+                        const int32_t* n_sel, int sel_stride, uint16_t* kslots, uint16_t* vslots,
+                        int64_t n_slot_pages, int n_slots, int nthreads) {
+  const int64_t page_elems = static_cast<int64_t>(kPage) * kD;
+  for_units(B * Hk, nthreads, [&](int u) {
+    const int b = u / Hk, h = u % Hk;
+    const int64_t so = static_cast<int64_t>(u) * sel_stride;
+    const int64_t hplane = static_cast<int64_t>(h) * n_host * page_elems;
+    const int64_t splane = (static_cast<int64_t>(h) * n_slot_pages + static_cast<int64_t>(b) * n_slots) *
+                           page_elems;
+    orc_retrieve_unit(khost + hplane, vhost + hplane, page_table + static_cast<int64_t>(b) * np_max,
+                      missing + so, n_missing[u], victims + so, slot + so, n_sel[u], kslots + splane,
+                      vslots + splane);
+  });
+}
+
+// Sparse attention reading the selected pages from their slots: page sel[u][j] of unit (b, h)
+// is slot page b * n_slots + slot[u][j] of plane h; its valid tokens follow from seq_len.
+void orc_slot_attn_batch(int B, int Hq, int Hk, const uint16_t* q, const uint16_t* kslots,
+                         const uint16_t* vslots, int64_t n_slot_pages, const int32_t* sel,
+                         const int32_t* slot, const int32_t* n_sel, int sel_stride, int n_slots,
+                         const int32_t* seq_len, const int32_t* units, int n_units, double* out,
+                         double* lse, int nthreads) {
+  (void)B;
+  const int G = Hq / Hk;
+  for_units(n_units, nthreads, [&](int i) {
+    const int u = units[i], b = u / Hk, h = u % Hk;
+    const int n = n_sel[u];
+    std::vector<int32_t> phys(n), valid(n);
+    for (int j = 0; j < n; ++j) {
+      const int64_t e = static_cast<int64_t>(u) * sel_stride + j;
+      phys[j] = b * n_slots + slot[e];
+      valid[j] = std::min(kPage, seq_len[b] - kPage * sel[e]);
+    }
+    const int64_t plane = static_cast<int64_t>(h) * n_slot_pages * kPage * kD;
+    const int64_t qo = (static_cast<int64_t>(b) * Hq + h * G);
+    orc_attn_unit(q + qo * kD, G, kslots + plane, vslots + plane, phys.data(), valid.data(), n,
+                  out + qo * kD, lse + qo);
   });
 }
 

@@ -13,6 +13,12 @@ computes.  Outputs are caller-allocated tensors, filled in place.
     lru_bucket_update(cache, resident, ts, slot, n_sel, missing, n_missing, t, 1, victims, hist)
     sparse_decode_attn(cache, q, page_table, sel, n_sel, seq_len, out, lse)
     lazy_rope_decode_attn(cache, q, qpos, meta, n_pages, doc_pos, theta, out, lse)
+
+With the full pool offloaded to pinned host memory and a slot pool on the device:
+
+    slots = paged_kv_create(k_slots, v_slots, None, None)
+    retrieve_pages(slots, k_host, v_host, page_table, missing, n_missing, victims, slot, n_sel, n_slots)
+    sparse_decode_attn_slots(slots, q, sel, slot, n_sel, n_slots, seq_len, out, lse)
 """
 from __future__ import annotations
 
@@ -25,6 +31,7 @@ from ._abi import DEVERR, SpkvDesc, SpkvError, check, load
 
 __all__ = ["PagedKVCache", "paged_kv_create", "paged_kv_append", "score_blocks", "select_topk",
            "sparse_decode_attn", "lazy_rope_decode_attn", "resident_setdiff", "lru_bucket_update",
+           "retrieve_pages", "sparse_decode_attn_slots",
            "sparse_decode_attn_noalloc", "pack_page_words", "get_device_error", "SpkvError", "DEVERR",
            "load"]
 
@@ -51,17 +58,37 @@ def _t(x: torch.Tensor, dtype, name: str, shape=None) -> int:
     return x.data_ptr()
 
 
+def _host(x: torch.Tensor, dtype, name: str, shape=None) -> int:
+    if not isinstance(x, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if x.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {x.dtype}")
+    if x.is_cuda or not x.is_pinned():
+        raise ValueError(f"{name}: must be a pinned host tensor")
+    if not x.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if shape is not None and tuple(x.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(x.shape)}")
+    return x.data_ptr()
+
+
 class PagedKVCache:
-    """Owns one library handle (``spkv_cache_t``) for a caller-owned pool."""
+    """Owns one library handle (``spkv_cache_t``) for a caller-owned pool.
+
+    ``ksum`` and ``page_cnt`` may both be None: a handle without summaries, for a pool of
+    resident slots that is only attended (``retrieve_pages``, ``sparse_decode_attn_slots``)."""
 
     def __init__(self, k_pool, v_pool, ksum, page_cnt, max_units: int = 0, stream=None):
         Hk, n_phys = k_pool.shape[0], k_pool.shape[1]
         shp = (Hk, n_phys, PAGE, HEAD_DIM)
+        if (ksum is None) != (page_cnt is None):
+            raise ValueError("ksum and page_cnt are given together or not at all")
         self.desc = SpkvDesc(Hk, HEAD_DIM, PAGE, SUBBLOCK, n_phys,
                              _t(k_pool, torch.bfloat16, "k_pool", shp),
                              _t(v_pool, torch.bfloat16, "v_pool", shp),
-                             _t(ksum, torch.float32, "ksum", (Hk, n_phys, 4, HEAD_DIM)),
-                             _t(page_cnt, torch.int32, "page_cnt", (n_phys,)), int(max_units))
+                             None if ksum is None else _t(ksum, torch.float32, "ksum", (Hk, n_phys, 4, HEAD_DIM)),
+                             None if page_cnt is None else _t(page_cnt, torch.int32, "page_cnt", (n_phys,)),
+                             int(max_units))
         self.n_kv_heads, self.n_phys = Hk, n_phys
         self.tensors = (k_pool, v_pool, ksum, page_cnt)   # keep the buffers alive
         h = ctypes.c_void_p()
@@ -135,6 +162,45 @@ def sparse_decode_attn(cache: PagedKVCache, q, page_table, sel, n_sel, seq_len, 
         _t(n_sel, torch.int32, "n_sel", (B, cache.n_kv_heads)), stride,
         _t(seq_len, torch.int32, "seq_len", (B,)), _t(out, torch.float32, "out", (B, Hq, HEAD_DIM)),
         _t(lse, torch.float32, "lse", (B, Hq)), _stream(stream)))
+
+
+def sparse_decode_attn_slots(cache: PagedKVCache, q, sel, slot, n_sel, n_slots: int, seq_len, out, lse,
+                             stream=None):
+    """sparse_decode_attn reading page sel[b][h][i] from slot page b * n_slots + slot[b][h][i]
+    of the handle's pools (the slot pool that ``retrieve_pages`` fills)."""
+    B, Hq = q.shape[0], q.shape[1]
+    stride = sel.shape[2]
+    check("sparse_decode_attn_slots", load().sparse_decode_attn_slots(
+        cache.handle, _t(q, torch.bfloat16, "q", (B, Hq, HEAD_DIM)), B, Hq,
+        _t(sel, torch.int32, "sel", (B, cache.n_kv_heads, stride)),
+        _t(slot, torch.int32, "slot", (B, cache.n_kv_heads, stride)),
+        _t(n_sel, torch.int32, "n_sel", (B, cache.n_kv_heads)), stride, int(n_slots),
+        _t(seq_len, torch.int32, "seq_len", (B,)), _t(out, torch.float32, "out", (B, Hq, HEAD_DIM)),
+        _t(lse, torch.float32, "lse", (B, Hq)), _stream(stream)))
+
+
+def retrieve_pages(cache: PagedKVCache, k_host, v_host, page_table, missing, n_missing, victims, slot, n_sel,
+                   n_slots: int, stream=None):
+    """Copies each unit's missing pages from the pinned host pool (k_host, v_host:
+    bf16 [Hk][n_host_pages][64][128]) into its victim slots of the handle's slot pool, and
+    fills the -1 entries of ``slot`` (in place) with those victims."""
+    Hk = cache.n_kv_heads
+    n_host = k_host.shape[1]
+    hshp = (Hk, n_host, PAGE, HEAD_DIM)
+    B, np_max = page_table.shape
+    stride = slot.shape[-1]
+    for name, x, want in (("missing", missing, B * Hk * stride), ("victims", victims, B * Hk * stride),
+                          ("slot", slot, B * Hk * stride), ("n_missing", n_missing, B * Hk),
+                          ("n_sel", n_sel, B * Hk)):
+        if x.numel() != want:
+            raise ValueError(f"{name}: expected {want} elements")
+    check("retrieve_pages", load().retrieve_pages(
+        cache.handle, _host(k_host, torch.bfloat16, "k_host", hshp),
+        _host(v_host, torch.bfloat16, "v_host", hshp), n_host,
+        _t(page_table, torch.int32, "page_table", (B, np_max)), np_max, B,
+        _t(missing, torch.int32, "missing"), _t(n_missing, torch.int32, "n_missing"),
+        _t(victims, torch.int32, "victims"), _t(slot, torch.int32, "slot"),
+        _t(n_sel, torch.int32, "n_sel"), stride, int(n_slots), _stream(stream)))
 
 
 def sparse_decode_attn_noalloc(k_pool, v_pool, q, page_table, sel, n_sel, seq_len, out, lse, dev_err=None,

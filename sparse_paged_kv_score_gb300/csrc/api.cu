@@ -110,7 +110,7 @@ int paged_kv_create(const spkv_desc* desc, void* stream, spkv_cache_t* out) {
   const spkv_desc& d = *desc;
   if (d.head_dim != 128 || d.page_tokens != 64 || d.subblock != 16) return SPKV_EUNSUPPORTED;
   if (d.n_kv_heads <= 0 || d.n_phys_pages <= 0 || d.max_units < 0 || d.max_units > 4096) return SPKV_EINVAL;
-  if (!d.k_pool || !d.v_pool || !d.ksum || !d.page_cnt) return SPKV_EINVAL;
+  if (!d.k_pool || !d.v_pool || !d.ksum != !d.page_cnt) return SPKV_EINVAL;
   if (!aligned(d.k_pool, 16) || !aligned(d.v_pool, 16) || !aligned(d.ksum, 16)) return SPKV_EINVAL;
   const int64_t n_ph = int64_t(d.n_kv_heads) * d.n_phys_pages;
   if (n_ph >= (int64_t(1) << 31)) return SPKV_EUNSUPPORTED;
@@ -148,7 +148,7 @@ int paged_kv_create(const spkv_desc* desc, void* stream, spkv_cache_t* out) {
   cudaStream_t st = as_stream(stream);
   if (cudaMemsetAsync(c->dev_err, 0, sizeof(uint32_t), st) != cudaSuccess ||
       cudaMemsetAsync(c->ws_cnt, 0, sizeof(int32_t) * (2 * c->max_units + 2), st) != cudaSuccess ||
-      spkv::launch_summary_build(c, st) != cudaSuccess) {
+      (d.ksum && spkv::launch_summary_build(c, st) != cudaSuccess)) {
     paged_kv_destroy(c);
     return SPKV_ECUDA;
   }
@@ -171,7 +171,7 @@ int spkv_sm_count(spkv_cache_t c) { return c ? c->sm_count : SPKV_EINVAL; }
 
 int paged_kv_append(spkv_cache_t c, const int32_t* phys_page, const int32_t* tok_in_page, const void* k_new,
                     const void* v_new, int n_rows, void* stream) {
-  if (!c || n_rows < 0) return SPKV_EINVAL;
+  if (!c || !c->d.ksum || n_rows < 0) return SPKV_EINVAL;
   if (n_rows == 0) return SPKV_OK;
   if (!phys_page || !tok_in_page || !k_new || !v_new || !aligned(k_new, 4) || !aligned(v_new, 4)) return SPKV_EINVAL;
   return status_of(spkv::launch_append(c, phys_page, tok_in_page, k_new, v_new, n_rows, as_stream(stream)));
@@ -181,6 +181,7 @@ int score_blocks(spkv_cache_t c, const void* q, int B, int Hq, const int32_t* pa
                  const int32_t* seq_len, float* scores, void* stream) {
   int st = check_group(c, B, Hq);
   if (st != SPKV_OK) return st;
+  if (!c->d.ksum) return SPKV_EINVAL;
   if (B == 0) return SPKV_OK;
   if (!q || !page_table || !seq_len || !scores || np_max <= 0 || !aligned(q, 8)) return SPKV_EINVAL;
   return status_of(spkv::launch_score(c, q, B, Hq, page_table, np_max, seq_len, scores, as_stream(stream)));
@@ -214,6 +215,31 @@ int sparse_decode_attn(spkv_cache_t c, const void* q, int B, int Hq, const int32
   p.n_sel = n_sel;
   p.sel_stride = sel_stride;
   p.seq_len = seq_len;
+  p.min_chunk = (sel_stride + 125) / 126;
+  const int64_t t_max = int64_t(B) * c->d.n_kv_heads * sel_stride;
+  const int grid = static_cast<int>(t_max < c->attn_grid ? t_max : c->attn_grid);
+  return status_of(spkv::launch_attn(c, p, false, grid, as_stream(stream)));
+}
+
+int sparse_decode_attn_slots(spkv_cache_t c, const void* q, int B, int Hq, const int32_t* sel, const int32_t* slot,
+                             const int32_t* n_sel, int sel_stride, int n_slots, const int32_t* seq_len, float* out,
+                             float* lse, void* stream) {
+  int st = check_group(c, B, Hq);
+  if (st != SPKV_OK) return st;
+  if (B == 0) return SPKV_OK;
+  if (!q || !sel || !slot || !n_sel || !seq_len || !out || !lse || sel_stride <= 0 || n_slots <= 0 ||
+      !aligned(q, 16))
+    return SPKV_EINVAL;
+  if (int64_t(B) * n_slots > c->d.n_phys_pages) return SPKV_EINVAL;
+  AttnParams p;
+  fill_common(p, c, q, B, Hq, out, lse);
+  p.np_max = 1 << 25;   // bounds the logical page id (64 * id stays within int); no page table here
+  p.sel = sel;
+  p.n_sel = n_sel;
+  p.sel_stride = sel_stride;
+  p.seq_len = seq_len;
+  p.slot = slot;
+  p.n_slots = n_slots;
   p.min_chunk = (sel_stride + 125) / 126;
   const int64_t t_max = int64_t(B) * c->d.n_kv_heads * sel_stride;
   const int grid = static_cast<int>(t_max < c->attn_grid ? t_max : c->attn_grid);
@@ -271,6 +297,36 @@ int lru_bucket_update(spkv_cache_t c, int32_t* resident, int32_t* ts, int n_slot
     return SPKV_EINVAL;
   return status_of(spkv::launch_lru(c->dev_err, resident, ts, n_slots, slot, n_sel, missing, n_missing, sel_stride,
                                     n_units, t_now, bucket_width, victims, hist, as_stream(stream)));
+}
+
+int retrieve_pages(spkv_cache_t c, const void* k_host, const void* v_host, int64_t n_host_pages,
+                   const int32_t* page_table, int np_max, int B, const int32_t* missing, const int32_t* n_missing,
+                   const int32_t* victims, int32_t* slot, const int32_t* n_sel, int sel_stride, int n_slots,
+                   void* stream) {
+  if (!c || B < 0) return SPKV_EINVAL;
+  if (B == 0) return SPKV_OK;
+  if (!k_host || !v_host || !page_table || !missing || !n_missing || !victims || !slot || !n_sel) return SPKV_EINVAL;
+  if (!aligned(k_host, 16) || !aligned(v_host, 16)) return SPKV_EINVAL;
+  if (n_host_pages <= 0 || np_max <= 0 || sel_stride <= 0 || sel_stride > 4096 || n_slots <= 0) return SPKV_EINVAL;
+  if (int64_t(B) * c->d.n_kv_heads > c->max_units) return SPKV_EINVAL;
+  if (int64_t(B) * n_slots > c->d.n_phys_pages) return SPKV_EINVAL;
+  // device address of the mapped host pool (the same address under unified addressing);
+  // looked up once per pool, so later calls (e.g. under stream capture) make no CUDA query
+  if (k_host != c->host_k || v_host != c->host_v) {
+    void* dk = nullptr;
+    void* dv = nullptr;
+    if (cudaHostGetDevicePointer(&dk, const_cast<void*>(k_host), 0) != cudaSuccess ||
+        cudaHostGetDevicePointer(&dv, const_cast<void*>(v_host), 0) != cudaSuccess) {
+      cudaGetLastError();
+      return SPKV_EINVAL;   // not pinned, device-mapped host memory
+    }
+    c->host_k = k_host;
+    c->host_v = v_host;
+    c->host_k_dev = dk;
+    c->host_v_dev = dv;
+  }
+  return status_of(spkv::launch_retrieve(c, c->host_k_dev, c->host_v_dev, n_host_pages, page_table, np_max, B, missing, n_missing,
+                                         victims, slot, n_sel, sel_stride, n_slots, as_stream(stream)));
 }
 
 int spkv_pack_page_words(const int32_t* phys, const int32_t* valid, const int32_t* doc_slot, int64_t n,

@@ -229,7 +229,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               bad |= SPKV_DEVERR_PAGE_ID;
             } else {
               const int v = min(kPageTokens, p.seq_len[b] - kPageTokens * lp);
-              const int ph = p.page_table[int64_t(b) * p.np_max + lp];
+              int ph;
+              if (p.slot) {
+                // resident-slot form: the page sits in slot s of this request's slot range
+                const int sl = p.slot[int64_t(my_u) * p.sel_stride + my_k];
+                ph = sl >= 0 && sl < p.n_slots ? b * p.n_slots + sl : -1;
+                if (ph < 0) bad |= SPKV_DEVERR_SLOT;
+              } else {
+                ph = p.page_table[int64_t(b) * p.np_max + lp];
+              }
               if (v <= 0) bad |= SPKV_DEVERR_PAGE_ID;
               else if (ph < 0 || ph >= p.n_phys) bad |= SPKV_DEVERR_PHYS;
               else { phys = ph; valid = v; }

@@ -24,6 +24,10 @@ struct spkv_cache {
   int32_t max_units = 0;
   int attn_grid = 0;             // CTAs of the split-K attention kernel (one per SM)
   int max_chunks = 0;            // chunks the attention kernel may cut its page sequence into
+  const void* host_k = nullptr;  // last host pool given to retrieve_pages and its device address
+  const void* host_v = nullptr;
+  const void* host_k_dev = nullptr;
+  const void* host_v_dev = nullptr;
 };
 
 namespace spkv {
@@ -73,6 +77,8 @@ struct AttnParams {
   const int32_t* n_sel;
   int sel_stride;
   const int32_t* seq_len;
+  const int32_t* slot;           // resident-slot form: slot of each selected page (else null)
+  int n_slots;                   // slots per (request, kv head); page = b * n_slots + slot
   // lazy form
   const int32_t* qpos;
   const uint32_t* meta;
@@ -96,6 +102,10 @@ cudaError_t launch_attn(const spkv_cache* c, const AttnParams& p, bool lazy, int
 cudaError_t launch_setdiff(uint32_t* err, const int32_t* resident, int n_slots, const int32_t* sel,
                            const int32_t* n_sel, int sel_stride, int n_units, int32_t* missing,
                            int32_t* n_missing, int32_t* slot, cudaStream_t st);
+cudaError_t launch_retrieve(const spkv_cache* c, const void* k_host, const void* v_host, int64_t n_host_pages,
+                            const int32_t* page_table, int np_max, int B, const int32_t* missing,
+                            const int32_t* n_missing, const int32_t* victims, int32_t* slot, const int32_t* n_sel,
+                            int sel_stride, int n_slots, cudaStream_t st);
 cudaError_t launch_lru(uint32_t* err, int32_t* resident, int32_t* ts, int n_slots, const int32_t* slot,
                        const int32_t* n_sel, const int32_t* missing, const int32_t* n_missing, int sel_stride,
                        int n_units, int32_t t_now, int bucket_width, int32_t* victims, int32_t* hist,

@@ -71,6 +71,57 @@ class Dev:
         self.cache.close()
 
 
+def host_bits(x):
+    """bf16 device tensor -> its uint16 bit patterns on the host."""
+    return x.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def pinned_bf16(a: np.ndarray) -> torch.Tensor:
+    t = torch.empty(a.shape, dtype=torch.int16, pin_memory=True)
+    t.numpy()[...] = a.view(np.int16)
+    return t.view(torch.bfloat16)
+
+
+class Offload:
+    """Host pool (pinned), device slot pool with its handle, and the residency tables."""
+
+    def __init__(self, d: Dev, n_slots: int):
+        w = d.w
+        self.d, self.n_slots = d, n_slots
+        self.B, self.Hk = w["B"], w["Hk"]
+        self.U = self.B * self.Hk
+        self.k_host, self.v_host = pinned_bf16(w["k_pool"]), pinned_bf16(w["v_pool"])
+        shp = (self.Hk, self.B * n_slots, 64, 128)
+        self.k_slots = torch.zeros(shp, dtype=torch.bfloat16, device=DEV)
+        self.v_slots = torch.zeros(shp, dtype=torch.bfloat16, device=DEV)
+        self.slots = spkv.paged_kv_create(self.k_slots, self.v_slots, None, None, max_units=self.U)
+        self.resident = i32(np.full((self.U, n_slots), -1, np.int32))
+        self.ts = i32(np.full((self.U, n_slots), np.iinfo(np.int32).min, np.int32))
+
+    def step(self, sel, n_sel, t, q):
+        U, stride = self.U, sel.shape[-1]
+        miss = torch.empty(U, stride, dtype=torch.int32, device=DEV)
+        nm = torch.empty(U, dtype=torch.int32, device=DEV)
+        slot = torch.empty(U, stride, dtype=torch.int32, device=DEV)
+        spkv.resident_setdiff(self.d.cache, self.resident, sel, n_sel, miss, nm, slot)
+        vic = torch.empty(U, stride, dtype=torch.int32, device=DEV)
+        hist = torch.empty(U, 64, dtype=torch.int32, device=DEV)
+        spkv.lru_bucket_update(self.d.cache, self.resident, self.ts, slot, n_sel.view(U), miss, nm, t, 1, vic,
+                               hist)
+        slot_before = slot.clone()
+        spkv.retrieve_pages(self.slots, self.k_host, self.v_host, self.d.pt, miss, nm, vic, slot, n_sel,
+                            self.n_slots)
+        B, Hq = q.shape[0], q.shape[1]
+        out = torch.empty(B, Hq, 128, dtype=torch.float32, device=DEV)
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=DEV)
+        spkv.sparse_decode_attn_slots(self.slots, q, sel, slot.view(sel.shape), n_sel, self.n_slots, self.d.L,
+                                      out, lse)
+        return dict(miss=miss, nm=nm, slot_before=slot_before, vic=vic, slot=slot, out=out, lse=lse)
+
+    def close(self):
+        self.slots.close()
+
+
 def alive_bits_to_bytes(words: np.ndarray, np_max: int) -> np.ndarray:
     w = words.astype(np.uint32)
     bits = (w[..., :, None] >> np.arange(32, dtype=np.uint32)) & 1

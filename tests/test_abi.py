@@ -33,7 +33,8 @@ def test_header_declares_the_decode_path():
     names = declared_functions()
     for f in ["paged_kv_create", "paged_kv_append", "score_blocks", "select_topk", "sparse_decode_attn",
               "lazy_rope_decode_attn", "resident_setdiff", "lru_bucket_update", "spkv_get_device_error",
-              "paged_kv_destroy", "spkv_status_string", "spkv_pack_page_words", "spkv_sm_count"]:
+              "paged_kv_destroy", "spkv_status_string", "spkv_pack_page_words", "spkv_sm_count",
+              "retrieve_pages", "sparse_decode_attn_slots"]:
         assert f in names
 
 
@@ -61,6 +62,13 @@ def test_host_argument_rejection_without_gpu(lib):
     assert lib.sparse_decode_attn(None, None, 1, 8, None, 1, None, None, 1, None, None, None, None) \
         == _abi.SPKV_EINVAL
     assert lib.paged_kv_destroy(None) == _abi.SPKV_EINVAL
+    assert lib.retrieve_pages(None, None, None, 1, None, 1, 1, None, None, None, None, None, 1, 1, None) \
+        == _abi.SPKV_EINVAL
+    assert lib.sparse_decode_attn_slots(None, None, 1, 8, None, None, None, 1, 1, None, None, None, None) \
+        == _abi.SPKV_EINVAL
+    # summaries are given together or not at all
+    d = _abi.SpkvDesc(8, 128, 64, 16, 16, 16, 16, 16, None, 0)
+    assert lib.paged_kv_create(ctypes.byref(d), None, ctypes.byref(out)) == _abi.SPKV_EINVAL
 
 
 def test_pack_page_words_matches_oracle_packing(lib):

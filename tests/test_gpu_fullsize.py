@@ -16,7 +16,7 @@ import torch
 import gen
 import oracle
 import sparse_paged_kv_score_gb300 as spkv
-from helpers import DEV, Dev, alive_bits_to_bytes, attn_errors, bf, f32, i32, u32_as_i32
+from helpers import DEV, Dev, Offload, alive_bits_to_bytes, attn_errors, bf, f32, host_bits, i32, u32_as_i32
 
 pytestmark = pytest.mark.gpu
 
@@ -246,6 +246,54 @@ def test_long262k_residency_trajectory():
     # the query walks slowly, so most selected pages stay resident from step to step
     assert hits[0] == 0.0 and np.mean(hits[1:]) > 0.5
     assert d.errors() == (0, 0)
+    d.close()
+
+
+def test_long262k_offload_trajectory():
+    """The same workload with the pool offloaded: pages come from pinned host memory into each
+    unit's 2048 slots (retrieve_pages) and attention reads them there."""
+    steps = 8
+    w = gen.long262k(seed=0)
+    B, Hk = w["B"], w["Hk"]
+    U = B * Hk
+    k_q, k_e = w["k_q"], w["k_e"]
+    stride = k_q + k_e + 1
+    n_slots = w["n_slots"]
+    qs = gen.walk_queries(w, steps)
+    d = Dev(w, max_units=U)
+    off = Offload(d, n_slots)
+    alive = d.new_alive()
+    ev = f32(w["evict"])
+    for t in range(steps):
+        q = bf(qs[t])
+        sel, n_sel = d.select(d.scores(q), ev, alive, k_q, k_e)
+        r = off.step(sel, n_sel, t, q)
+        out, lse = d.attn(sel, n_sel, q=q)
+        torch.cuda.synchronize()
+        assert torch.equal(r["out"], out) and torch.equal(r["lse"], lse)
+        sel_h, n_h = host(sel).reshape(U, stride), host(n_sel).reshape(U)
+        sl, res = host(r["slot"]), host(off.resident)
+        if t == 0:
+            assert np.array_equal(host(r["nm"]), n_h)   # empty buffers: everything is missing
+        for u in range(U):
+            n = n_h[u]
+            assert ((sl[u, :n] >= 0) & (sl[u, :n] < n_slots)).all() and len(set(sl[u, :n].tolist())) == n
+            assert np.array_equal(res[u, sl[u, :n]], sel_h[u, :n])
+        for u in (0, 29, 63):
+            b, h = divmod(u, Hk)
+            n = n_h[u]
+            rows = torch.from_numpy(b * n_slots + sl[u, :n].astype(np.int64)).to(DEV)
+            got_k = host_bits(off.k_slots[h].index_select(0, rows))
+            got_v = host_bits(off.v_slots[h].index_select(0, rows))
+            src = w["page_table"][b, sel_h[u, :n]]
+            assert np.array_equal(got_k, w["k_pool"][h, src]) and np.array_equal(got_v, w["v_pool"][h, src])
+        if t == steps - 1:
+            wq = dict(w)
+            wq["q"] = qs[t]
+            check_attn(wq, host(r["out"]), host(r["lse"]), host(sel), host(n_sel), units=np.array([0, 29, 63]))
+    assert d.errors() == (0, 0)
+    assert spkv.get_device_error(off.slots) == (0, 0)
+    off.close()
     d.close()
 
 

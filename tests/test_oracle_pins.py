@@ -416,3 +416,85 @@ def test_lru_empty_slots_are_oldest():
     r, t, vic, hist = oracle.lru_unit(r, t, [-1, -1, -1], 3, [10, 11, 12], 3, 3, 1, 3)
     # ages now: slot0 3, slot1 1, slot2 2, slot3 1 -> order 0, 2, 1
     assert vic.tolist() == [0, 2, 1] and hist[3] == 1 and hist[2] == 1 and hist[1] == 2
+
+
+# ------------------------------------------------------------------------------ retrieve (swap-in)
+
+def _offload_case(seed, B=2, Hk=2, G=2, npg=14, n_slots=6, stride=5):
+    """A small host pool, an empty slot pool and a page table with scattered host pages."""
+    rng = np.random.default_rng(seed)
+    n_host = B * npg + 3
+    k_host = gen.rows_bf16(seed, 901, Hk * n_host * 64).reshape(Hk, n_host, 64, 128)
+    v_host = gen.rows_bf16(seed, 902, Hk * n_host * 64).reshape(Hk, n_host, 64, 128)
+    pt = rng.permutation(n_host)[:B * npg].reshape(B, npg).astype(np.int32)
+    L = np.array([npg * 64 - int(rng.integers(0, 64)) for _ in range(B)], np.int32)
+    q = gen.rows_bf16(seed, 903, B * Hk * G).reshape(B, Hk * G, 128)
+    return rng, k_host, v_host, pt, L, q, n_slots, stride
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_retrieve_trajectory_invariants(seed):
+    """Over a trajectory of selections: every selected page ends up in its slot byte for byte,
+    only victim slots of the unit's own range change, the resident table names the slot's page,
+    and attention over the slots equals attention over the host pool exactly."""
+    rng, k_host, v_host, pt, L, q, n_slots, stride = _offload_case(seed)
+    B, npg = pt.shape
+    Hk = k_host.shape[0]
+    U = B * Hk
+    k_slots = np.zeros((Hk, B * n_slots, 64, 128), np.uint16)
+    v_slots = np.zeros_like(k_slots)
+    resident = np.full((U, n_slots), -1, np.int32)
+    ts = np.full((U, n_slots), np.iinfo(np.int32).min, np.int32)
+    for t in range(25):
+        sel = np.full((U, stride), -1, np.int32)
+        n_sel = rng.integers(1, stride + 1, U).astype(np.int32)
+        for u in range(U):
+            sel[u, :n_sel[u]] = np.sort(rng.choice(npg, size=n_sel[u], replace=False))
+        missing, nm, slot = oracle.setdiff_batch(resident, sel, n_sel)
+        resident, ts, victims, _ = oracle.lru_batch(resident, ts, slot, n_sel, missing, nm, t, 2)
+        k_before, v_before = k_slots.copy(), v_slots.copy()
+        full = oracle.retrieve_batch(k_host, v_host, pt, missing, nm, victims, slot, n_sel, k_slots,
+                                     v_slots, n_slots)
+        changed = set()
+        for h in range(Hk):
+            for p in range(B * n_slots):
+                if not (np.array_equal(k_slots[h, p], k_before[h, p])
+                        and np.array_equal(v_slots[h, p], v_before[h, p])):
+                    changed.add((h, p))
+        for u in range(U):
+            b, h = divmod(u, Hk)
+            n = n_sel[u]
+            assert (full[u, :n] >= 0).all() and (full[u, :n] < n_slots).all()
+            assert len(set(full[u, :n].tolist())) == n
+            hits = [i for i in range(n) if slot[u, i] >= 0]
+            assert all(full[u, i] == slot[u, i] for i in hits)
+            for i in range(n):
+                s = int(full[u, i])
+                assert resident[u, s] == sel[u, i]
+                hp = pt[b, sel[u, i]]
+                assert np.array_equal(k_slots[h, b * n_slots + s], k_host[h, hp])
+                assert np.array_equal(v_slots[h, b * n_slots + s], v_host[h, hp])
+        # the only pages written are the victims of each unit (content may coincide otherwise)
+        vict = {(u % Hk, (u // Hk) * n_slots + int(victims[u, j])) for u in range(U) for j in range(nm[u])}
+        assert changed <= vict
+        out_s, lse_s = oracle.slot_attn_batch(q, k_slots, v_slots, sel.reshape(B, Hk, stride),
+                                              full.reshape(B, Hk, stride), n_sel.reshape(B, Hk), L, n_slots)
+        out_h, lse_h = oracle.sparse_attn_batch(q, k_host, v_host, pt, sel.reshape(B, Hk, stride),
+                                                n_sel.reshape(B, Hk), L)
+        assert np.array_equal(out_s, out_h) and np.array_equal(lse_s, lse_h)
+
+
+def test_retrieve_hand_example():
+    """One unit, four slots, a hand-checked swap-in: selection [1, 4, 6], page 4 resident in
+    slot 2, victims 0 and 3 for pages 1 and 6."""
+    k_host = np.arange(1 * 8 * 64 * 128, dtype=np.uint16).reshape(1, 8, 64, 128)
+    v_host = (k_host + 7).astype(np.uint16)
+    pt = np.array([[7, 6, 5, 4, 3, 2, 1, 0]], np.int32)
+    k_slots = np.zeros((1, 4, 64, 128), np.uint16)
+    v_slots = np.zeros_like(k_slots)
+    slot = np.array([[-1, 2, -1, -1]], np.int32)
+    full = oracle.retrieve_batch(k_host, v_host, pt, [[1, 6, -1, -1]], [2], [[0, 3, -1, -1]], slot, [3],
+                                 k_slots, v_slots, 4)
+    assert full.tolist() == [[0, 2, 3, -1]]
+    assert np.array_equal(k_slots[0, 0], k_host[0, 6]) and np.array_equal(v_slots[0, 3], v_host[0, 1])
+    assert not k_slots[0, 1].any() and not k_slots[0, 2].any()

@@ -7,6 +7,8 @@ rows scaled x20), all rows of the hot path through the C ABI:
   paged_kv_append -> score_blocks -> select_topk -> resident_setdiff -> lru_bucket_update
   -> sparse_decode_attn
 
+(the three bookkeeping operations through select_resident_update, their one-kernel fused form).
+
 ``value`` is the step's algorithmic KV-cache bytes (pooled-key summaries scored + K/V pages
 attended + bookkeeping tables) divided by the device time of the step; ``queries_per_s`` is
 requests / step time.  ``roofline`` reports the dominant kernel (sparse_decode_attn) against
@@ -272,9 +274,8 @@ def offload_leg(args, dev, stream, timed):
 
     def select_and_plan(i):
         spkv.score_blocks(scache, qs[i], pt, seq, scores)
-        spkv.select_topk(scache, scores, ev, alive, seq, k_q, k_e, sel, n_sel)
-        spkv.resident_setdiff(scache, resident, sel, n_sel, missing, n_missing, slot)
-        spkv.lru_bucket_update(scache, resident, ts, slot, n_sel.view(U), missing, n_missing, i, 1, victims, hist)
+        spkv.select_resident_update(scache, scores, ev, alive, seq, k_q, k_e, sel, n_sel, resident, ts, i, 1,
+                                    missing, n_missing, slot, victims, hist)
 
     def retrieve():
         spkv.retrieve_pages(slots, k_host, v_host, pt, missing, n_missing, victims, slot, n_sel, ns)
@@ -435,9 +436,9 @@ def run_native(args):
     def step(i):
         spkv.paged_kv_append(cache, app_phys, app_tok, knew[i], vnew[i])
         spkv.score_blocks(cache, qs[i], pt, seq, scores)
-        spkv.select_topk(cache, scores, evs[i], alive, seq, k_q, k_e, sel, n_sel)
-        spkv.resident_setdiff(cache, resident, sel, n_sel, missing, n_missing, slot)
-        spkv.lru_bucket_update(cache, resident, ts, slot, n_sel.view(U), missing, n_missing, i, 1, victims, hist)
+        # select_topk + resident_setdiff + lru_bucket_update, fused into one kernel
+        spkv.select_resident_update(cache, scores, evs[i], alive, seq, k_q, k_e, sel, n_sel, resident, ts, i, 1,
+                                    missing, n_missing, slot, victims, hist)
         spkv.sparse_decode_attn(cache, qs[i], pt, sel, n_sel, seq, out, lse)
 
     def barrier():
@@ -593,10 +594,8 @@ def run_native(args):
         v_d.copy_(v_h[s_], non_blocking=True)
         spkv.paged_kv_append(cache, app_phys, app_tok, k_d, v_d)
         spkv.score_blocks(cache, q_d, pt, seq, scores)
-        spkv.select_topk(cache, scores, e_d, alive, seq, k_q, k_e, sel, n_sel)
-        spkv.resident_setdiff(cache, resident, sel, n_sel, missing, n_missing, slot)
-        spkv.lru_bucket_update(cache, resident, ts, slot, n_sel.view(U), missing, n_missing, 1000 + i, 1,
-                               victims, hist)
+        spkv.select_resident_update(cache, scores, e_d, alive, seq, k_q, k_e, sel, n_sel, resident, ts, 1000 + i,
+                                    1, missing, n_missing, slot, victims, hist)
         spkv.sparse_decode_attn(cache, q_d, pt, sel, n_sel, seq, out, lse)
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
@@ -637,7 +636,8 @@ def run_native(args):
             "config": {"workload": w["name"], "batch": B, "q_heads": Hq, "kv_heads": Hk, "context": L,
                        "page": 64, "subblock": 16, "k_q": k_q, "k_e": k_e, "resident_slots": N_SLOTS,
                        "step": "append+score+select+setdiff+lru+sparse_attn",
-                       "launch": "one CUDA graph per step (kernels chained by programmatic dependent launch)",
+                       "launch": ("one CUDA graph per step (kernels chained by programmatic dependent launch); "
+                                  "select + setdiff + lru as one fused kernel"),
                        "bytes_per_step": {kk: int(v) for kk, v in byts.items()},
                        "l2": ("no flush: each step reads ~0.81 GB of K/V pages and pooled-key sums, more "
                               "than the 129 MB L2, through evict-first loads" if args.l2 == "none" else
@@ -653,7 +653,7 @@ def run_native(args):
             "offload": offload,
             "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": 8 * args.steps,
+            "gpu_launches": 6 * args.steps,
             "eager_ms_per_step": eager_ms,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,

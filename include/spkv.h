@@ -8,6 +8,7 @@
  *   select_topk          per-KV-head top-k pages: eviction-head budget k_e + query budget k_q
  *   resident_setdiff     selected pages that are not resident (swap-in list)
  *   lru_bucket_update    64-bucket LRU recency update and victim choice
+ *   select_resident_update  select_topk + resident_setdiff + lru_bucket_update in one call
  *   retrieve_pages       swap-in of the missing pages from a host pool into resident slots
  *   sparse_decode_attn_slots  attention reading the selected pages from their resident slots
  *   sparse_decode_attn   split-K flash decoding over the selected pages
@@ -198,6 +199,22 @@ int lazy_rope_decode_attn(spkv_cache_t cache, const void* q, int B, int Hq, cons
 int resident_setdiff(spkv_cache_t cache, const int32_t* resident, int n_slots, const int32_t* sel,
                      const int32_t* n_sel, int sel_stride, int n_units, int32_t* missing,
                      int32_t* n_missing, int32_t* slot, void* stream);
+
+/* One decode step's selection and residency bookkeeping in one call: select_topk, then
+ * resident_setdiff, then lru_bucket_update, with results identical to those three calls made
+ * in turn with the same arguments (sel_stride = k_q + k_e + 1, n_units = B * n_kv_heads; the
+ * slot argument of lru_bucket_update is the slot list resident_setdiff writes).  Sources as for
+ * the three operations ([NOSA] "Method 1" and "Method 2: NOSI"; [Spin] 2B); the pages describe
+ * them separately, and fusing them is this library's choice: for np_max <= 1024 the whole step
+ * is one kernel (one CTA per unit, the selection in one warp's registers, the list handed over
+ * in shared memory, each unit's residency rows read once); longer contexts launch the three
+ * kernels in turn.  Argument rules and error behaviour: those of the three calls. */
+int select_resident_update(spkv_cache_t cache, const float* q_scores, const float* evict_scores,
+                           uint32_t* alive, int B, int np_max, const int32_t* seq_len, int k_q,
+                           int k_e, int32_t* sel, int32_t* n_sel, int32_t* resident, int32_t* ts,
+                           int n_slots, int32_t t_now, int bucket_width, int32_t* missing,
+                           int32_t* n_missing, int32_t* slot, int32_t* victims, int32_t* hist,
+                           void* stream);
 
 /* Retrieve: copies the selected pages that are not resident from the host pool into the
  * resident slots the LRU update chose, and completes the slot list.  [NOSA] "Method 2: the

@@ -31,7 +31,7 @@ from ._abi import DEVERR, SpkvDesc, SpkvError, check, load
 
 __all__ = ["PagedKVCache", "paged_kv_create", "paged_kv_append", "score_blocks", "select_topk",
            "sparse_decode_attn", "lazy_rope_decode_attn", "resident_setdiff", "lru_bucket_update",
-           "retrieve_pages", "sparse_decode_attn_slots",
+           "select_resident_update", "retrieve_pages", "sparse_decode_attn_slots",
            "sparse_decode_attn_noalloc", "pack_page_words", "get_device_error", "SpkvError", "DEVERR",
            "load"]
 
@@ -276,6 +276,32 @@ def lru_bucket_update(cache: PagedKVCache, resident, ts, slot, n_sel, missing, n
         _t(missing, torch.int32, "missing"), _t(n_missing, torch.int32, "n_missing"), stride, n_units,
         int(t_now), int(bucket_width), _t(victims, torch.int32, "victims"),
         _t(hist, torch.int32, "hist"), _stream(stream)))
+
+
+def select_resident_update(cache: PagedKVCache, q_scores, evict_scores, alive, seq_len, k_q: int, k_e: int, sel,
+                           n_sel, resident, ts, t_now: int, bucket_width: int, missing, n_missing, slot, victims,
+                           hist, stream=None):
+    """select_topk, resident_setdiff and lru_bucket_update in one call (identical results)."""
+    B, Hk, np_max = q_scores.shape
+    stride = k_q + k_e + 1
+    U = B * Hk
+    n_units, n_slots = resident.shape
+    if n_units != U:
+        raise ValueError(f"resident: expected {U} rows")
+    for name, x, want in (("ts", ts, U * n_slots), ("missing", missing, U * stride), ("n_missing", n_missing, U),
+                          ("slot", slot, U * stride), ("victims", victims, U * stride), ("hist", hist, U * 64)):
+        if x.numel() != want:
+            raise ValueError(f"{name}: expected {want} elements")
+    check("select_resident_update", load().select_resident_update(
+        cache.handle, _t(q_scores, torch.float32, "q_scores", (B, Hk, np_max)),
+        _t(evict_scores, torch.float32, "evict_scores", (B, Hk, np_max)),
+        _t(alive, torch.int32, "alive", (B, Hk, (np_max + 31) // 32)), B, np_max,
+        _t(seq_len, torch.int32, "seq_len", (B,)), int(k_q), int(k_e),
+        _t(sel, torch.int32, "sel", (B, Hk, stride)), _t(n_sel, torch.int32, "n_sel", (B, Hk)),
+        _t(resident, torch.int32, "resident"), _t(ts, torch.int32, "ts"), n_slots, int(t_now),
+        int(bucket_width), _t(missing, torch.int32, "missing"), _t(n_missing, torch.int32, "n_missing"),
+        _t(slot, torch.int32, "slot"), _t(victims, torch.int32, "victims"), _t(hist, torch.int32, "hist"),
+        _stream(stream)))
 
 
 def pack_page_words(phys, valid, doc_slot) -> np.ndarray:

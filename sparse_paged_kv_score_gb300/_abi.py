@@ -37,6 +37,8 @@ SIGNATURES = {
     "resident_setdiff": ([_vp, _vp, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp], _i32),
     "lru_bucket_update": ([_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp],
                           _i32),
+    "select_resident_update": ([_vp, _vp, _vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _i32,
+                                _i32, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "retrieve_pages": ([_vp, _vp, _vp, _i64, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp], _i32),
     "sparse_decode_attn_slots": ([_vp, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp], _i32),
     "sparse_decode_attn_noalloc": ([_vp, _vp, _i32, _i64, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _i32,

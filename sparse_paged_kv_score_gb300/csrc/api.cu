@@ -85,6 +85,7 @@ cudaError_t init_kernel_attributes() {
   cudaError_t e;
   if ((e = attn_init_attributes()) != cudaSuccess) return e;
   if ((e = select_init_attributes()) != cudaSuccess) return e;
+  if ((e = fused_init_attributes()) != cudaSuccess) return e;
   return resid_init_attributes();
 }
 }  // namespace spkv
@@ -327,6 +328,37 @@ int retrieve_pages(spkv_cache_t c, const void* k_host, const void* v_host, int64
   }
   return status_of(spkv::launch_retrieve(c, c->host_k_dev, c->host_v_dev, n_host_pages, page_table, np_max, B, missing, n_missing,
                                          victims, slot, n_sel, sel_stride, n_slots, as_stream(stream)));
+}
+
+int select_resident_update(spkv_cache_t c, const float* q_scores, const float* evict_scores, uint32_t* alive, int B,
+                           int np_max, const int32_t* seq_len, int k_q, int k_e, int32_t* sel, int32_t* n_sel,
+                           int32_t* resident, int32_t* ts, int n_slots, int32_t t_now, int bucket_width,
+                           int32_t* missing, int32_t* n_missing, int32_t* slot, int32_t* victims, int32_t* hist,
+                           void* stream) {
+  if (!c || B < 0) return SPKV_EINVAL;
+  const int64_t U = int64_t(B) * c->d.n_kv_heads;
+  if (U > 65535) return SPKV_EINVAL;
+  if (B == 0) return SPKV_OK;
+  if (!q_scores || !evict_scores || !alive || !seq_len || !sel || !n_sel || !resident || !ts || !missing ||
+      !n_missing || !slot || !victims || !hist)
+    return SPKV_EINVAL;
+  if (np_max <= 0 || np_max > 32768 || k_q < 0 || k_e < 0 || k_q + k_e + 1 > 4096) return SPKV_EINVAL;
+  if (n_slots <= 0 || n_slots > 16384 || bucket_width < 1) return SPKV_EINVAL;
+  cudaStream_t st = as_stream(stream);
+  const int stride = k_q + k_e + 1;
+  if (spkv::fused_supported(np_max))
+    return status_of(spkv::launch_select_resident(c, q_scores, evict_scores, alive, B, np_max, seq_len, k_q, k_e,
+                                                  sel, n_sel, resident, ts, n_slots, t_now, bucket_width, missing,
+                                                  n_missing, slot, victims, hist, st));
+  // longer contexts: the three kernels in turn (same results)
+  cudaError_t e = spkv::launch_select(c, q_scores, evict_scores, alive, B, np_max, seq_len, k_q, k_e, sel, n_sel, st);
+  if (e == cudaSuccess)
+    e = spkv::launch_setdiff(c->dev_err, resident, n_slots, sel, n_sel, stride, static_cast<int>(U), missing,
+                             n_missing, slot, st);
+  if (e == cudaSuccess)
+    e = spkv::launch_lru(c->dev_err, resident, ts, n_slots, slot, n_sel, missing, n_missing, stride,
+                         static_cast<int>(U), t_now, bucket_width, victims, hist, st);
+  return status_of(e);
 }
 
 int spkv_pack_page_words(const int32_t* phys, const int32_t* valid, const int32_t* doc_slot, int64_t n,

@@ -111,10 +111,18 @@ cudaError_t launch_lru(uint32_t* err, int32_t* resident, int32_t* ts, int n_slot
                        int n_units, int32_t t_now, int bucket_width, int32_t* victims, int32_t* hist,
                        cudaStream_t st);
 
+cudaError_t launch_select_resident(const spkv_cache* c, const float* qs, const float* es, uint32_t* alive, int B,
+                                   int np_max, const int32_t* seq_len, int k_q, int k_e, int32_t* sel,
+                                   int32_t* n_sel, int32_t* resident, int32_t* ts, int n_slots, int32_t t_now,
+                                   int W, int32_t* missing, int32_t* n_missing, int32_t* slot, int32_t* victims,
+                                   int32_t* hist, cudaStream_t st);
+bool fused_supported(int np_max);
+
 // Shared-memory bytes the attention kernel needs for a group size (used for limits checks).
 size_t attn_smem_bytes(int G, bool lazy);
 cudaError_t attn_init_attributes();
 cudaError_t select_init_attributes();
 cudaError_t resid_init_attributes();
+cudaError_t fused_init_attributes();
 
 }  // namespace spkv

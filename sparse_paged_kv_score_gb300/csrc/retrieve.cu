@@ -9,7 +9,8 @@
 // The kernel reads the pinned host pool through its device-mapped address (on GB300 the loads
 // cross NVLink-C2C) and writes each page into the victim slot the LRU update chose for it.  One
 // CTA copies one page-head (16 KiB of K and 16 KiB of V) with all of its 16-byte loads in flight
-// before the first store; the grid strides over (unit, missing index) pairs.  It also completes
+// before the first store; the grid strides over the missing pages of all units, numbered through
+// a per-unit prefix table that each CTA builds in shared memory.  It also completes
 // the per-page slot list in place, so attention can read every selected page from its slot.
 #include "common.cuh"
 #include "internal.h"
@@ -20,6 +21,7 @@ namespace {
 constexpr int kRtThreads = 256;
 constexpr int kVecPerPage = 16384 / 16;                 // uint4 per K (or V) page-head
 constexpr int kVecPerThread = kVecPerPage / kRtThreads;   // 4
+constexpr int kMaxUnits = 4096;                           // largest max_units of a handle
 
 __global__ void __launch_bounds__(kRtThreads)
     retrieve_kernel(const uint4* __restrict__ k_host, const uint4* __restrict__ v_host, int64_t n_host, int Hk,
@@ -28,16 +30,46 @@ __global__ void __launch_bounds__(kRtThreads)
                     int32_t* __restrict__ slot, const int32_t* __restrict__ n_sel, int stride, int n_units,
                     uint4* __restrict__ k_slots, uint4* __restrict__ v_slots, int64_t n_slot_pages, int n_slots,
                     uint32_t* err) {
+  __shared__ int prefix[kMaxUnits + 1];
+  __shared__ int warp_tot[kRtThreads / 32];
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+  // 0. prefix[u] = first copy item of unit u (every CTA builds the table; n_units <= 4096)
+  {
+    const int c0 = static_cast<int>(int64_t(tid) * n_units / kRtThreads);
+    const int c1 = static_cast<int>(int64_t(tid + 1) * n_units / kRtThreads);
+    int sum = 0;
+    for (int u = c0; u < c1; ++u) sum += max(0, min(stride, n_missing[u]));
+    int x = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    int acc = x - sum;
+    for (int w = 0; w < warp; ++w) acc += warp_tot[w];
+    for (int u = c0; u < c1; ++u) {
+      prefix[u] = acc;
+      acc += max(0, min(stride, n_missing[u]));
+    }
+    if (c1 == n_units) prefix[n_units] = acc;
+    __syncthreads();
+  }
+  const int n_items = prefix[n_units];
+
   // 1. copies: item w = (unit u, missing index j)
-  const int64_t n_items = int64_t(n_units) * stride;
-  for (int64_t w = blockIdx.x; w < n_items; w += gridDim.x) {
-    const int u = static_cast<int>(w / stride), j = static_cast<int>(w % stride);
-    const int nm = n_missing[u];
-    if (j >= nm) continue;
+  for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
+    int lo = 0, hi = n_units;   // last u with prefix[u] <= w
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (prefix[mid] <= w) lo = mid;
+      else hi = mid;
+    }
+    const int u = lo, j = w - prefix[lo];
     const int b = u / Hk, h = u % Hk;
     const int lp = missing[int64_t(u) * stride + j];
     const int vs = victims[int64_t(u) * stride + j];

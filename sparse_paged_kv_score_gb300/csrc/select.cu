@@ -5,13 +5,15 @@
 // eviction policy (a block not chosen by Gamma_e can never be chosen by it again), locality
 // guarantee, and ED-DMA (blocks ranked on pre-exp eviction scores; exp is never applied).
 //
-// One CTA per unit.  Each top-k is an exact radix select over 32-bit order-preserving keys of
+// Up to 1024 pages per unit: one warp per unit, scores in registers (warp form, below).
+// Longer contexts: one CTA per unit.  Each top-k is an exact radix select over 32-bit order-preserving keys of
 // the fp32 scores (4 passes of 8 bits, shared-memory histograms), followed by a page-ordered
 // pick among keys equal to the threshold, which realises the total order
 // (score descending, page ascending).  The union is emitted in ascending page order by a
 // block-wide scan, then the local page.
 #include "common.cuh"
 #include "internal.h"
+#include "select_warp.cuh"
 
 namespace spkv {
 namespace {
@@ -222,6 +224,20 @@ __global__ void __launch_bounds__(kSelThreads)
   }
 }
 
+// ---------------------------------------------------------------- warp form (np_max <= 32 R)
+// One warp per unit (warp_select_unit in select_warp.cuh), two units per 64-thread CTA.
+template <int R>
+__global__ void __launch_bounds__(64)
+    select_warp_kernel(const float* __restrict__ qs, const float* __restrict__ es, uint32_t* __restrict__ alive,
+                       const int32_t* __restrict__ seq_len, int Hk, int n_units, int np_max, int k_q, int k_e,
+                       int32_t* __restrict__ sel, int32_t* __restrict__ n_sel, uint32_t* err) {
+  pdl_wait();
+  pdl_trigger();
+  const int u = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (u >= n_units) return;
+  warp_select_unit<R>(qs, es, alive, seq_len, u, Hk, np_max, k_q, k_e, sel, n_sel, nullptr, err);
+}
+
 }  // namespace
 
 cudaError_t select_init_attributes() {
@@ -231,6 +247,22 @@ cudaError_t select_init_attributes() {
 cudaError_t launch_select(const spkv_cache* c, const float* qs, const float* es, uint32_t* alive, int B, int np_max,
                           const int32_t* seq_len, int k_q, int k_e, int32_t* sel, int32_t* n_sel, cudaStream_t st) {
   const int Hk = c->d.n_kv_heads;
+  const int U = B * Hk;
+  if (np_max <= 32 * 32) {
+    // warp form: two units per 64-thread CTA, all scores in registers
+    const dim3 grid((U + 1) / 2), block(64);
+    if (np_max <= 32 * 4)
+      return launch_pdl(select_warp_kernel<4>, grid, block, 0, st, qs, es, alive, seq_len, Hk, U, np_max, k_q, k_e,
+                        sel, n_sel, c->dev_err);
+    if (np_max <= 32 * 8)
+      return launch_pdl(select_warp_kernel<8>, grid, block, 0, st, qs, es, alive, seq_len, Hk, U, np_max, k_q, k_e,
+                        sel, n_sel, c->dev_err);
+    if (np_max <= 32 * 16)
+      return launch_pdl(select_warp_kernel<16>, grid, block, 0, st, qs, es, alive, seq_len, Hk, U, np_max, k_q,
+                        k_e, sel, n_sel, c->dev_err);
+    return launch_pdl(select_warp_kernel<32>, grid, block, 0, st, qs, es, alive, seq_len, Hk, U, np_max, k_q, k_e,
+                      sel, n_sel, c->dev_err);
+  }
   const size_t smem = size_t(np_max) * 6;
   return launch_pdl(select_kernel, dim3(B * Hk), dim3(kSelThreads), smem, st, qs, es, alive, seq_len, Hk, np_max,
                     k_q, k_e, sel, n_sel, c->dev_err);

@@ -16,7 +16,7 @@ import torch
 import gen
 import oracle
 import sparse_paged_kv_score_gb300 as spkv
-from helpers import DEV, Dev, alive_bits_to_bytes, attn_errors, bf, f32, i32, u32_as_i32
+from helpers import DEV, Dev, alive_bits_to_bytes, alive_bytes_to_bits, attn_errors, bf, f32, i32, u32_as_i32
 
 pytestmark = pytest.mark.gpu
 
@@ -145,6 +145,89 @@ def test_select_bitexact_on_same_scores(which):
         e = e + 0.3 * gen.normal_f32(1, 50 + step, e.size).reshape(e.shape)
         if which == "ties":
             e = np.round(e * 2) / 2
+    assert d.errors() == (0, 0)
+    d.close()
+
+
+@pytest.mark.parametrize("np_max", [1, 32, 33, 128, 129, 256, 257, 512, 513, 1000, 1024, 1025])
+def test_select_bitexact_across_context_sizes(np_max):
+    """Both selection forms (one warp per unit up to 1024 pages, one CTA per unit above) on
+    coarse scores with many exact ties, random alive masks, ragged contexts and budgets from 0
+    to more than the candidates."""
+    rng = np.random.default_rng(np_max)
+    w = gen.sparse_workload(3, 4, 2, 64 * np_max, 8, 8, seed=np_max)
+    w["seq_len"] = np.array([64 * np_max, max(1, 64 * np_max - 70), int(rng.integers(1, 64 * np_max + 1))],
+                            np.int32)
+    d = Dev(w)
+    shape = (w["B"], w["Hk"], np_max)
+    for k_q, k_e in [(8, 8), (0, 5), (5, 0), (np_max + 3, 2), (1, np_max)]:
+        s = np.round(rng.standard_normal(shape) * 2) / 2
+        s[rng.random(shape) < 0.1] = -0.0
+        alive = rng.random(shape) < 0.7
+        alive_dev = u32_as_i32(alive_bytes_to_bits(alive.astype(np.uint8)))
+        for step in range(2):
+            e = (np.round(rng.standard_normal(shape) * 3) / 3).astype(np.float32)
+            _check_select_bitexact(d, f32(s), e, alive_dev, k_q, k_e)
+    assert d.errors() == (0, 0)
+    d.close()
+
+
+@pytest.mark.parametrize("np_max, n_slots", [(96, 40), (512, 2048), (1000, 300), (1500, 700)])
+def test_select_resident_update_equals_three_calls(np_max, n_slots):
+    """The fused call (one kernel up to 1024 pages, three launches above) against select_topk +
+    resident_setdiff + lru_bucket_update on copies of the same state, and both against the oracle,
+    bit for bit, over a trajectory whose residency buffer fills and recycles."""
+    w = gen.sparse_workload(3, 8, 2, 64 * np_max - 5, 10, 6, seed=np_max)
+    d = Dev(w)
+    B, Hk = w["B"], w["Hk"]
+    U, k_q, k_e = B * Hk, w["k_q"], w["k_e"]
+    stride = k_q + k_e + 1
+    rng = np.random.default_rng(np_max)
+    shape = (B, Hk, np_max)
+
+    def state():
+        return dict(alive=d.new_alive(), resident=i32(np.full((U, n_slots), -1, np.int32)),
+                    ts=i32(np.full((U, n_slots), np.iinfo(np.int32).min, np.int32)))
+
+    def outputs():
+        z = lambda *sh: torch.empty(*sh, dtype=torch.int32, device=DEV)
+        return dict(sel=z(B, Hk, stride), n_sel=z(B, Hk), missing=z(U, stride), n_missing=z(U), slot=z(U, stride),
+                    victims=z(U, stride), hist=z(U, 64))
+
+    a, b = state(), state()
+    h_alive = np.ones(shape, np.uint8)
+    h_res = np.full((U, n_slots), -1, np.int32)
+    h_ts = np.full((U, n_slots), np.iinfo(np.int32).min, np.int32)
+    for t in range(8):
+        s = (np.round(rng.standard_normal(shape) * 4) / 4).astype(np.float32)
+        e = (np.round(rng.standard_normal(shape) * 4) / 4).astype(np.float32)
+        s_d, e_d = f32(s), f32(e)
+        fa, fb = outputs(), outputs()
+        spkv.select_resident_update(d.cache, s_d, e_d, a["alive"], d.L, k_q, k_e, fa["sel"], fa["n_sel"],
+                                    a["resident"], a["ts"], t, 2, fa["missing"], fa["n_missing"], fa["slot"],
+                                    fa["victims"], fa["hist"])
+        spkv.select_topk(d.cache, s_d, e_d, b["alive"], d.L, k_q, k_e, fb["sel"], fb["n_sel"])
+        spkv.resident_setdiff(d.cache, b["resident"], fb["sel"], fb["n_sel"], fb["missing"], fb["n_missing"],
+                              fb["slot"])
+        spkv.lru_bucket_update(d.cache, b["resident"], b["ts"], fb["slot"], fb["n_sel"].view(U), fb["missing"],
+                               fb["n_missing"], t, 2, fb["victims"], fb["hist"])
+        torch.cuda.synchronize()
+        for k in fa:
+            assert torch.equal(fa[k], fb[k]), k
+        for k in a:
+            assert torch.equal(a[k], b[k]), k
+        o_sel, o_n, h_alive = oracle.select_batch(s.astype(np.float64), e.astype(np.float64), h_alive,
+                                                  w["seq_len"], k_q, k_e)
+        o_miss, o_nm, o_slot = oracle.setdiff_batch(h_res, o_sel.reshape(U, stride), o_n.reshape(U))
+        h_res, h_ts, o_vic, o_hist = oracle.lru_batch(h_res, h_ts, o_slot, o_n.reshape(U), o_miss, o_nm, t, 2)
+        assert np.array_equal(fa["sel"].cpu().numpy(), o_sel) and np.array_equal(fa["n_sel"].cpu().numpy(), o_n)
+        assert np.array_equal(fa["missing"].cpu().numpy(), o_miss)
+        assert np.array_equal(fa["n_missing"].cpu().numpy(), o_nm)
+        assert np.array_equal(fa["slot"].cpu().numpy(), o_slot)
+        assert np.array_equal(fa["victims"].cpu().numpy(), o_vic)
+        assert np.array_equal(fa["hist"].cpu().numpy(), o_hist)
+        assert np.array_equal(a["resident"].cpu().numpy(), h_res) and np.array_equal(a["ts"].cpu().numpy(), h_ts)
+        assert np.array_equal(alive_bits_to_bytes(a["alive"].cpu().numpy().view(np.uint32), np_max), h_alive)
     assert d.errors() == (0, 0)
     d.close()
 

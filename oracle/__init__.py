@@ -64,6 +64,8 @@ def _l():
                                      i32, f64, i32, vp, i32, vp, vp, i32], None),
             "orc_setdiff_batch": ([vp, i32, vp, vp, i32, i32, vp, vp, vp, i32], None),
             "orc_lru_batch": ([vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, i32], None),
+            "orc_lazy_prefill_batch": ([i32, i32, i32, i32, vp, vp, vp, i64, vp, vp, vp, i32, vp, i32, vp, vp,
+                                        i32, f64, i32, vp, i32, vp, vp, i32], None),
             "orc_retrieve_unit": ([vp, vp, vp, vp, i32, vp, vp, i32, vp, vp], None),
             "orc_retrieve_batch": ([i32, i32, vp, vp, i64, vp, i32, vp, vp, vp, vp, vp, i32, vp, vp, i64,
                                     i32, i32], None),
@@ -323,4 +325,26 @@ def slot_attn_batch(q, k_slots, v_slots, sel, slot, n_sel, seq_len, n_slots: int
     _l().orc_slot_attn_batch(B, Hq, Hk, _p(q), _p(k_slots), _p(v_slots), k_slots.shape[1], _p(sel), _p(slot),
                              _p(n_sel), sel.shape[-1], int(n_slots), _p(seq_len), _p(u), u.shape[0], _p(out),
                              _p(lse), nthreads)
+    return out, lse
+
+
+def lazy_prefill_batch(q, k_pool, v_pool, phys, valid, slot, n_pages, qpos0, doc_pos, theta: float,
+                       materialise: bool = True, items=None, nthreads: int = 0):
+    """LazyAttention prefill: q [B][T][Hq][128] (bf16 bits); phys/valid/slot [B][meta_heads][np_max]
+    or [B][np_max].  Returns (out [B][T][Hq][128], lse [B][T][Hq]) in fp64 for the listed work
+    items ((b * T + t) * Hk + h; all when None)."""
+    q, k_pool, v_pool = _c(q, np.uint16), _c(k_pool, np.uint16), _c(v_pool, np.uint16)
+    if phys.ndim == 2:
+        phys, valid, slot = phys[:, None, :], valid[:, None, :], slot[:, None, :]
+    phys, valid, slot = _c(phys, np.int32), _c(valid, np.int32), _c(slot, np.int32)
+    n_pages, qpos0, doc_pos = _c(n_pages, np.int32), _c(qpos0, np.int32), _c(doc_pos, np.int32)
+    B, T, Hq, _ = q.shape
+    Hk, n_phys = k_pool.shape[0], k_pool.shape[1]
+    out = np.zeros((B, T, Hq, D), np.float64)
+    lse = np.zeros((B, T, Hq), np.float64)
+    it = _units(items, B * T * Hk)
+    _l().orc_lazy_prefill_batch(B, T, Hq, Hk, _p(q), _p(k_pool), _p(v_pool), n_phys, _p(phys), _p(valid),
+                                _p(slot), phys.shape[1], _p(n_pages), phys.shape[2], _p(qpos0), _p(doc_pos),
+                                doc_pos.shape[1], float(theta), int(bool(materialise)), _p(it), it.shape[0],
+                                _p(out), _p(lse), nthreads)
     return out, lse

@@ -489,6 +489,38 @@ void orc_lazy_attn_batch(int B, int Hq, int Hk, const uint16_t* q, const uint16_
   });
 }
 
+// LazyAttention prefill ([Lazy] "Technical implementation 1. Prefilling"): T new query rows
+// per request at absolute positions qpos0[b] + t attend over the request's cached document
+// pages (no mask: every cached key precedes the rows).  Row t is the single-query attention of
+// the functions above at position qpos0[b] + t, so the batch loops over rows.  q is
+// [B][T][Hq][128], out [B][T][Hq][128], lse [B][T][Hq]; a work item is (b, t, kv head h),
+// numbered ((b * T) + t) * Hk + h.
+void orc_lazy_prefill_batch(int B, int T, int Hq, int Hk, const uint16_t* q, const uint16_t* kpool,
+                            const uint16_t* vpool, int64_t n_phys, const int32_t* phys,
+                            const int32_t* valid, const int32_t* slot, int meta_heads,
+                            const int32_t* n_pages, int np_max, const int32_t* qpos0,
+                            const int32_t* doc_pos, int max_docs, double theta, int materialise,
+                            const int32_t* items, int n_items, double* out, double* lse, int nthreads) {
+  (void)B;
+  const int G = Hq / Hk;
+  for_units(n_items, nthreads, [&](int i) {
+    const int it = items[i];
+    const int h = it % Hk, bt = it / Hk, t = bt % T, b = bt / T;
+    const int mh = meta_heads == 1 ? 0 : h;
+    const int64_t mo = (static_cast<int64_t>(b) * meta_heads + mh) * np_max;
+    const int64_t plane = static_cast<int64_t>(h) * n_phys * kPage * kD;
+    const int64_t qo = static_cast<int64_t>(bt) * Hq + h * G;
+    const int32_t* dp = doc_pos + static_cast<int64_t>(b) * max_docs;
+    const int32_t pos = qpos0[b] + t;
+    if (materialise)
+      orc_attn_materialised_unit(q + qo * kD, G, kpool + plane, vpool + plane, phys + mo, valid + mo,
+                                 slot + mo, n_pages[b], pos, dp, theta, out + qo * kD, lse + qo);
+    else
+      orc_attn_lazy_unit(q + qo * kD, G, kpool + plane, vpool + plane, phys + mo, valid + mo,
+                         slot + mo, n_pages[b], pos, dp, theta, out + qo * kD, lse + qo);
+  });
+}
+
 // Retrieve for every unit.  Host pools [Hk][n_host][64][128]; slot pools [Hk][n_slot_pages][64][128]
 // with unit (b, h)'s slots at pages b * n_slots .. b * n_slots + n_slots - 1 of plane h.
 void orc_retrieve_batch(int B, int Hk, const uint16_t* khost, const uint16_t* vhost, int64_t n_host,

@@ -498,3 +498,77 @@ def test_retrieve_hand_example():
     assert full.tolist() == [[0, 2, 3, -1]]
     assert np.array_equal(k_slots[0, 0], k_host[0, 6]) and np.array_equal(v_slots[0, 3], v_host[0, 1])
     assert not k_slots[0, 1].any() and not k_slots[0, 2].any()
+
+
+# ------------------------------------------------------------------------------ lazy prefill
+
+def _prefill_case(seed, T=5, theta=10000.0):
+    w = gen.lazy_rag(seed=seed, B=2, Hq=4, Hk=2, n_docs=6, docs_per_req=3, min_len=70, max_len=200,
+                     theta=theta)
+    q = gen.rows_bf16(seed, 990, 2 * T * 4).reshape(2, T, 4, 128)
+    return w, q
+
+
+def _complex_rope_prefill(w, q, theta):
+    """Independent brute force: RoPE as multiplication of the complex numbers x_i + i x_(i+64) by
+    exp(i pos theta^(-i/64)); keys placed at their absolute positions; dense scipy softmax."""
+    B, T, Hq, _ = q.shape
+    Hk = w["Hk"]
+    G = Hq // Hk
+    freq = theta ** (-np.arange(64) / 64.0)
+    cplx = lambda x: x[..., :64] + 1j * x[..., 64:]
+    out = np.zeros((B, T, Hq, 128))
+    lse = np.zeros((B, T, Hq))
+    for b in range(B):
+        n = w["n_pages"][b]
+        for h in range(Hk):
+            ks, vs, kpos = [], [], []
+            for i in range(n):
+                rows = slice(0, w["valid"][b, i])
+                ks.append(f(w["k_pool"][h, w["phys"][b, i], rows]))
+                vs.append(f(w["v_pool"][h, w["phys"][b, i], rows]))
+                kpos += [w["doc_pos"][b, w["slot"][b, i]]] * w["valid"][b, i]
+            K, V, kpos = np.concatenate(ks), np.concatenate(vs), np.array(kpos, np.float64)
+            Kc = cplx(K) * np.exp(1j * kpos[:, None] * freq[None, :])   # keys carry doc-local rotation
+            for t in range(T):
+                pos = w["qpos"][b] + t
+                for g in range(G):
+                    qc = cplx(f(q[b, t, h * G + g])) * np.exp(1j * pos * freq)
+                    z = (qc.real @ Kc.real.T + qc.imag @ Kc.imag.T) / math.sqrt(128)
+                    out[b, t, h * G + g] = softmax(z) @ V
+                    lse[b, t, h * G + g] = logsumexp(z)
+    return out, lse
+
+
+@pytest.mark.parametrize("materialise", [True, False])
+def test_prefill_complex_rope_bruteforce(materialise):
+    w, q = _prefill_case(5)
+    out, lse = oracle.lazy_prefill_batch(q, w["k_pool"], w["v_pool"], w["phys"], w["valid"], w["slot"],
+                                         w["n_pages"], w["qpos"], w["doc_pos"], 10000.0, materialise=materialise)
+    ro, rl = _complex_rope_prefill(w, q, 10000.0)
+    assert np.abs(out - ro).max() < 1e-10 and np.abs(lse - rl).max() < 1e-10
+
+
+def test_prefill_depends_on_relative_positions_only():
+    """Moving the query rows and every document by the same offset changes nothing; moving one
+    document does."""
+    w, q = _prefill_case(6, T=3)
+    args = (w["k_pool"], w["v_pool"], w["phys"], w["valid"], w["slot"], w["n_pages"])
+    o1, l1 = oracle.lazy_prefill_batch(q, *args, w["qpos"], w["doc_pos"], 500000.0)
+    o2, l2 = oracle.lazy_prefill_batch(q, *args, w["qpos"] + 12345, w["doc_pos"] + 12345, 500000.0)
+    assert np.abs(o1 - o2).max() < 1e-9 and np.abs(l1 - l2).max() < 1e-9
+    dp = w["doc_pos"].copy()
+    dp[:, 1] += 7
+    o3, _ = oracle.lazy_prefill_batch(q, *args, w["qpos"], dp, 500000.0)
+    assert np.abs(o1 - o3).max() > 1e-4
+
+
+def test_prefill_rows_are_decode_queries():
+    """Row t of a prefill equals lazy decode attention with the query at qpos + t."""
+    w, q = _prefill_case(7, T=4)
+    out, lse = oracle.lazy_prefill_batch(q, w["k_pool"], w["v_pool"], w["phys"], w["valid"], w["slot"],
+                                         w["n_pages"], w["qpos"], w["doc_pos"], 500000.0, materialise=False)
+    for t in range(4):
+        od, ld = oracle.lazy_attn_batch(q[:, t], w["k_pool"], w["v_pool"], w["phys"], w["valid"], w["slot"],
+                                        w["n_pages"], w["qpos"] + t, w["doc_pos"], 500000.0, materialise=False)
+        assert np.array_equal(out[:, t], od) and np.array_equal(lse[:, t], ld)

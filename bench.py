@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-lazy", action="store_true")
     ap.add_argument("--no-rag", action="store_true", help="skip the lazy-RoPE RAG sub-measurement")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the LazyAttention prefill sub-measurement")
     ap.add_argument("--no-offload", action="store_true",
                     help="skip the offload sub-measurement (262k context, pool in pinned host memory)")
     ap.add_argument("--l2", default="none", choices=["none", "write"],
@@ -65,6 +66,14 @@ def peaks():
         d = json.load(open(p))
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def bf16_peak():
+    """Dense bf16 tensor throughput (TFLOP/s, burst) measured on this machine, else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p))["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
 
 
 def rank_max(v: float, device) -> float:
@@ -530,6 +539,7 @@ def run_native(args):
 
     # ---- lazy-RoPE dense decode over shared documents (64 requests x 8 Zipf-drawn documents)
     rag = None
+    prefill = None
     if not args.no_rag and rank == 0:
         wr = gen.lazy_rag(seed=0)
         Br, Hqr, Hkr = wr["B"], wr["Hq"], wr["Hk"]
@@ -552,6 +562,28 @@ def run_native(args):
         pages = int(wr["n_pages"].sum()) * Hkr
         logical = pages * PAGE_BYTES
         distinct = len(np.unique(wr["phys"][ok])) * Hkr * PAGE_BYTES
+        # LazyAttention prefill over the same cached documents: 128 new query rows per request
+        if not args.no_prefill:
+            Tq = 128
+            pq = bf(gen.rows_bf16(0, 7700, Br * Tq * Hqr).reshape(Br, Tq, Hqr, 128))
+            pout = torch.empty(Br, Tq, Hqr, 128, dtype=torch.float32, device=dev)
+            plse = torch.empty(Br, Tq, Hqr, dtype=torch.float32, device=dev)
+
+            def pre_call(i):
+                spkv.lazy_rope_prefill_attn(rcache, pq, rqpos, rmeta, rnp, rdoc, wr["theta"], pout, plse)
+
+            timed(pre_call, range(3))
+            pre_ms = statistics.mean(timed(pre_call, timed_idx))
+            keys = int(wr["qpos"].sum())          # cached tokens over all requests
+            flops = 4.0 * 128 * Tq * Hqr * keys   # QK^T and PV, 2 flops per multiply-add each
+            tflops = flops / (pre_ms * 1e-3) / 1e12
+            tpeak, tkind = bf16_peak()
+            prefill = {"kernel": "lazy_rope_prefill_attn (tcgen05.mma, TMEM accumulators, TMA pages)",
+                       "workload": "the RAG documents above, 128 new query rows per request (64 x 128 x 32 heads)",
+                       "us": pre_ms * 1e3, "flops": flops, "bound": "tensor", "achieved_TFLOPs": tflops,
+                       "peak": tpeak, "peak_kind": tkind + " bf16 dense (cuBLAS burst)", "frac": tflops / tpeak,
+                       "query_rows_per_s": Br * Tq / (pre_ms * 1e-3)}
+            del pq, pout, plse
         st, bits = spkv.get_device_error(rcache)
         if st != 0:
             raise RuntimeError(f"device error bits {bits} in the RAG leg")
@@ -650,6 +682,7 @@ def run_native(args):
                          "traffic": measured_traffic() if B == 32 else None},
             "lazy_attn": lazy,
             "lazy_rag": rag,
+            "lazy_prefill": prefill,
             "offload": offload,
             "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},

@@ -13,6 +13,7 @@
  *   sparse_decode_attn_slots  attention reading the selected pages from their resident slots
  *   sparse_decode_attn   split-K flash decoding over the selected pages
  *   lazy_rope_decode_attn  the same with deferred RoPE (query rotated once per document)
+ *   lazy_rope_prefill_attn a tile of new query rows over cached documents (tcgen05)
  *
  * Sources (web pages, cited by title and section):
  *   [NOSA] "NOSA: Native and Offloadable Sparse Attention", sections "Method 1: the NOSA
@@ -196,6 +197,27 @@ int lazy_rope_decode_attn(spkv_cache_t cache, const void* q, int B, int Hq, cons
  *   sel      : device int32 [n_units][sel_stride], strictly ascending in [0, n_sel)
  *   missing, slot : device int32 [n_units][sel_stride];  n_missing: device int32 [n_units]
  * n_slots <= 16384, sel_stride <= 4096. */
+/* LazyAttention prefill over cached documents, on the tcgen05 tensor cores ([Lazy]
+ * "Technical implementation 1. Prefilling" and "Mathematical equivalence").  Request b has T new
+ * query rows at absolute positions qpos0[b] + t; they attend over the request's cached document
+ * pages (page words and documents as in lazy_rope_decode_attn).  No mask is applied: every
+ * cached key precedes the rows (attention of the rows among themselves, if wanted, is the
+ * caller's, merged through lse).  For query head hq (kv head h = hq / G) and row t:
+ *   out[b][t][hq][:] = sum_k softmax_k(q'_k . key_k / sqrt(128)) v_k
+ *   lse[b][t][hq]    = log sum_k exp(q'_k . key_k / sqrt(128))                  (natural log)
+ * with q'_k = R(qpos0[b] + t - doc_pos[b][slot of key k]) q[b][t][hq], the same scores as keys
+ * rotated to their absolute positions.
+ *   q     : device bf16 [B][T][Hq][128], unrotated, 16-byte aligned
+ *   qpos0 : device int32 [B]
+ *   meta, meta_heads, n_pages, np_max, doc_pos, max_docs, theta: as lazy_rope_decode_attn
+ *   out   : device fp32 [B][T][Hq][128], 16-byte aligned;  lse: device fp32 [B][T][Hq]
+ * The rotated query and the softmax weights enter the tensor cores as bf16 (fp32 accumulation).
+ * A request with no pages gets out = 0 and lse = -inf.  B, Hq <= 65535. */
+int lazy_rope_prefill_attn(spkv_cache_t cache, const void* q, int B, int T, int Hq,
+                           const int32_t* qpos0, const uint32_t* meta, int meta_heads,
+                           const int32_t* n_pages, int np_max, const int32_t* doc_pos,
+                           int max_docs, float theta, float* out, float* lse, void* stream);
+
 int resident_setdiff(spkv_cache_t cache, const int32_t* resident, int n_slots, const int32_t* sel,
                      const int32_t* n_sel, int sel_stride, int n_units, int32_t* missing,
                      int32_t* n_missing, int32_t* slot, void* stream);

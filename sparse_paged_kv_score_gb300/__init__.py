@@ -31,7 +31,7 @@ from ._abi import DEVERR, SpkvDesc, SpkvError, check, load
 
 __all__ = ["PagedKVCache", "paged_kv_create", "paged_kv_append", "score_blocks", "select_topk",
            "sparse_decode_attn", "lazy_rope_decode_attn", "resident_setdiff", "lru_bucket_update",
-           "select_resident_update", "retrieve_pages", "sparse_decode_attn_slots",
+           "select_resident_update", "retrieve_pages", "sparse_decode_attn_slots", "lazy_rope_prefill_attn",
            "sparse_decode_attn_noalloc", "pack_page_words", "get_device_error", "SpkvError", "DEVERR",
            "load"]
 
@@ -242,6 +242,24 @@ def lazy_rope_decode_attn(cache: PagedKVCache, q, qpos, meta, n_pages, doc_pos, 
         meta_heads, _t(n_pages, torch.int32, "n_pages", (B,)), np_max,
         _t(doc_pos, torch.int32, "doc_pos", (B, max_docs)), max_docs, float(theta),
         _t(out, torch.float32, "out", (B, Hq, HEAD_DIM)), _t(lse, torch.float32, "lse", (B, Hq)),
+        _stream(stream)))
+
+
+def lazy_rope_prefill_attn(cache: PagedKVCache, q, qpos0, meta, n_pages, doc_pos, theta: float, out, lse,
+                           stream=None):
+    """LazyAttention prefill: q bf16 [B][T][Hq][128] rows at positions qpos0[b] + t over the cached
+    document pages; meta: int32 tensor of page words, [B][meta_heads][np_max] or [B][np_max]."""
+    B, T, Hq = q.shape[0], q.shape[1], q.shape[2]
+    if meta.dim() == 2:
+        meta = meta.unsqueeze(1)
+    meta_heads, np_max = meta.shape[1], meta.shape[2]
+    max_docs = doc_pos.shape[1]
+    check("lazy_rope_prefill_attn", load().lazy_rope_prefill_attn(
+        cache.handle, _t(q, torch.bfloat16, "q", (B, T, Hq, HEAD_DIM)), B, T, Hq,
+        _t(qpos0, torch.int32, "qpos0", (B,)), _t(meta, torch.int32, "meta", (B, meta_heads, np_max)),
+        meta_heads, _t(n_pages, torch.int32, "n_pages", (B,)), np_max,
+        _t(doc_pos, torch.int32, "doc_pos", (B, max_docs)), max_docs, float(theta),
+        _t(out, torch.float32, "out", (B, T, Hq, HEAD_DIM)), _t(lse, torch.float32, "lse", (B, T, Hq)),
         _stream(stream)))
 
 

@@ -86,6 +86,7 @@ cudaError_t init_kernel_attributes() {
   if ((e = attn_init_attributes()) != cudaSuccess) return e;
   if ((e = select_init_attributes()) != cudaSuccess) return e;
   if ((e = fused_init_attributes()) != cudaSuccess) return e;
+  if ((e = prefill_init_attributes()) != cudaSuccess) return e;
   return resid_init_attributes();
 }
 }  // namespace spkv
@@ -276,6 +277,47 @@ int lazy_rope_decode_attn(spkv_cache_t c, const void* q, int B, int Hq, const in
   const int64_t t_max = int64_t(B) * c->d.n_kv_heads * np_max;
   const int grid = static_cast<int>(t_max < c->attn_grid ? t_max : c->attn_grid);
   return status_of(spkv::launch_attn(c, p, true, grid, as_stream(stream)));
+}
+
+int lazy_rope_prefill_attn(spkv_cache_t c, const void* q, int B, int T, int Hq, const int32_t* qpos0,
+                           const uint32_t* meta, int meta_heads, const int32_t* n_pages, int np_max,
+                           const int32_t* doc_pos, int max_docs, float theta, float* out, float* lse, void* stream) {
+  if (!c || B < 0 || T < 0 || Hq <= 0) return SPKV_EINVAL;
+  const int Hk = c->d.n_kv_heads;
+  if (Hq % Hk != 0) return SPKV_EINVAL;
+  if (Hq / Hk > kMaxGroup) return SPKV_EUNSUPPORTED;
+  if (B == 0 || T == 0) return SPKV_OK;
+  if (!q || !qpos0 || !meta || !n_pages || !doc_pos || !out || !lse || np_max <= 0 || max_docs <= 0 ||
+      !aligned(q, 16) || !aligned(out, 16))
+    return SPKV_EINVAL;
+  if (meta_heads != 1 && meta_heads != Hk) return SPKV_EINVAL;
+  if (!(theta > 1.0f) || !std::isfinite(theta)) return SPKV_EINVAL;
+  if (B > 65535 || Hq > 65535) return SPKV_EINVAL;
+  spkv::PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = static_cast<const uint16_t*>(q);
+  p.out = out;
+  p.lse = lse;
+  p.B = B;
+  p.T = T;
+  p.Hq = Hq;
+  p.Hk = Hk;
+  p.G = Hq / Hk;
+  p.n_phys = c->d.n_phys_pages;
+  p.qpos0 = qpos0;
+  p.meta = meta;
+  p.meta_heads = meta_heads;
+  p.n_pages = n_pages;
+  p.np_max = np_max;
+  p.doc_pos = doc_pos;
+  p.max_docs = max_docs;
+  p.scale_log2 = static_cast<float>(1.4426950408889634074 / std::sqrt(128.0));
+  p.err = c->dev_err;
+  for (int j = 0; j < 64; ++j) {
+    const double f = std::pow(static_cast<double>(theta), -2.0 * j / 128.0) / (2.0 * 3.14159265358979323846);
+    p.phase_inc[j] = static_cast<uint64_t>(std::ldexp(f, 64));
+  }
+  return status_of(spkv::launch_prefill(c, p, as_stream(stream)));
 }
 
 int resident_setdiff(spkv_cache_t c, const int32_t* resident, int n_slots, const int32_t* sel, const int32_t* n_sel,

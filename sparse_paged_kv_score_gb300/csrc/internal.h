@@ -90,6 +90,25 @@ struct AttnParams {
   uint64_t phase_inc[64];        // RoPE pair j: turns per position, 2^-64 fixed point
 };
 
+// Parameters of the LazyAttention prefill kernel (tcgen05).
+struct PrefillParams {
+  const uint16_t* q;             // bf16 [B][T][Hq][128]
+  float* out;                    // [B][T][Hq][128]
+  float* lse;                    // [B][T][Hq]
+  int B, T, Hq, Hk, G;
+  int64_t n_phys;
+  const int32_t* qpos0;
+  const uint32_t* meta;
+  int meta_heads;
+  const int32_t* n_pages;
+  int np_max;
+  const int32_t* doc_pos;
+  int max_docs;
+  float scale_log2;
+  uint32_t* err;
+  uint64_t phase_inc[64];
+};
+
 cudaError_t launch_summary_build(const spkv_cache* c, cudaStream_t st);
 cudaError_t launch_append(const spkv_cache* c, const int32_t* phys, const int32_t* tok, const void* k_new,
                           const void* v_new, int n_rows, cudaStream_t st);
@@ -124,5 +143,7 @@ cudaError_t attn_init_attributes();
 cudaError_t select_init_attributes();
 cudaError_t resid_init_attributes();
 cudaError_t fused_init_attributes();
+cudaError_t prefill_init_attributes();
+cudaError_t launch_prefill(const spkv_cache* c, const PrefillParams& p, cudaStream_t st);
 
 }  // namespace spkv

@@ -1,0 +1,404 @@
+// LazyAttention prefill over cached documents, on the 5th-generation tensor cores.
+//
+// [Lazy] "LazyAttention", sections "Core idea: deferred positional encoding", "Technical
+// implementation 1. Prefilling" and "Mathematical equivalence": cached keys carry only their
+// document-local rotation, and a query at absolute position n scores the keys of document i
+// (placed at offset P_i) after one relative rotation by n - P_i; the result equals attention over
+// keys re-rotated to their absolute positions.  A tile of M = 128 query rows shares each K/V
+// page, so the rotation is a small cost next to the M x 64 x 128 products per page.
+//
+// The pages rotate the key block; here each query row is rotated instead, once per document
+// switch (a document spans tens of pages, so this is cheaper still, and the key tiles stay as
+// TMA wrote them).  Both give the same scores.
+//
+// One CTA per (request b, query head, tile of 128 query rows); six warps:
+//   warp 0     TMA producer: K and V of each page (two 64 x 64 bf16 boxes each, 128-byte
+//              swizzle) into a 4-stage ring;
+//   warp 1     MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM S buffers (M 128,
+//              N 64), then O += P_(j-1) V_(j-1) (M 128, N 128, V read MN-major); it also zeroes
+//              the V rows of a partial page so that P = 0 never meets garbage;
+//   warps 2-5  softmax: thread r owns query row r (TMEM lane r): it rotates its query row on
+//              document switches, reads its S row from TMEM, runs the online softmax in the
+//              log2 domain, writes its P row (bf16) as the A operand of the next PV MMA, and
+//              rescales its O row in TMEM only when the row maximum has grown by more than
+//              2^8 since the last rescale; at the end it normalises O and writes out and lse.
+// Hand-offs are mbarriers; every wait is bounded (SPKV_DEVERR_TIMEOUT), and the MMA issuer
+// drains its MMAs before TMEM is released.
+#include <math_constants.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tcgen05.cuh"
+
+namespace spkv {
+namespace {
+
+constexpr int kPM = 128;                      // query rows per tile (TMEM lanes)
+constexpr int kPStages = 4;                   // K/V page ring
+constexpr int kPThreads = 192;
+constexpr int kBox = 64 * 128;                // one 64 x 64 bf16 box, bytes
+constexpr int kPStageBytes = 4 * kBox;        // K (2 boxes) + V (2 boxes) of one page-head
+constexpr int kQBytes = 2 * kPM * 128;        // Q tile: two boxes of 128 rows x 128 B
+constexpr int kPBytes = kPM * 128;            // P tile: 128 rows x 64 bf16
+constexpr uint32_t kTmemCols = 256;           // O: columns 0..127; S buffers: 128..191, 192..255
+constexpr float kRescaleLog2 = 8.f;           // row-max growth (log2) tolerated before O is rescaled
+constexpr float kLn2 = 0.69314718055994530942f;
+
+struct PrefillSmem {
+  uint64_t full[kPStages], empty[kPStages];
+  uint64_t sfull[2], sfree[2], pready[2], pvdone[2];
+  uint64_t qready, drain;
+  uint32_t tmem_base;
+};
+
+constexpr size_t kPrefillSmem = 1024 + kQBytes + 2 * kPBytes + size_t(kPStages) * kPStageBytes + sizeof(PrefillSmem);
+
+struct PageInfo {
+  int phys, valid, slot;
+};
+
+__device__ __forceinline__ PageInfo page_info(const PrefillParams& p, int b, int h, int j) {
+  const int mh = p.meta_heads == 1 ? 0 : h;
+  const uint32_t w = p.meta[(int64_t(b) * p.meta_heads + mh) * p.np_max + j];
+  PageInfo r;
+  r.phys = static_cast<int>(w & 0x3FFFFu);
+  r.valid = static_cast<int>((w >> 18) & 63u) + 1;
+  r.slot = static_cast<int>(w >> 24);
+  if (r.phys >= p.n_phys || r.slot >= p.max_docs) {   // skipped page (flagged by the producer)
+    r.phys = 0;
+    r.valid = 0;
+    r.slot = 0;
+  }
+  return r;
+}
+
+// Bounded wait with one outcome for the whole warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+}
+
+__global__ void __launch_bounds__(kPThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                   const __grid_constant__ PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = base;
+  uint8_t* sP = base + kQBytes;
+  uint8_t* stages = sP + 2 * kPBytes;
+  PrefillSmem& S = *reinterpret_cast<PrefillSmem*>(stages + kPStages * kPStageBytes);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int mt = blockIdx.x, hq = blockIdx.y, b = blockIdx.z;
+  const int h = hq / p.G;
+
+  if (tid == 0) {
+    for (int s = 0; s < kPStages; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.sfull[i], 1);
+      mbar_init(&S.sfree[i], 4);
+      mbar_init(&S.pready[i], 4);
+      mbar_init(&S.pvdone[i], 1);
+    }
+    mbar_init(&S.qready, 4);
+    mbar_init(&S.drain, 1);
+    fence_mbar_init();
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+  }
+  if (warp == 1) {
+    tmem_alloc(&S.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = S.tmem_base;
+  pdl_wait();
+  const int n = max(0, min(p.n_pages[b], p.np_max));
+
+  if (warp == 0) {
+    // ================================================================ TMA producer
+    const uint64_t pol = l2_policy_evict_last();   // the group's query heads and other requests reuse pages
+    int j = 0;
+    for (; j < n; ++j) {
+      const int s = j % kPStages;
+      if (j >= kPStages && !warp_wait(&S.empty[s], ((j / kPStages) - 1) & 1)) {
+        if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
+        break;
+      }
+      if (lane == 0) {
+        const int mh = p.meta_heads == 1 ? 0 : h;
+        const uint32_t w = p.meta[(int64_t(b) * p.meta_heads + mh) * p.np_max + j];
+        if (static_cast<int64_t>(w & 0x3FFFFu) >= p.n_phys) flag_error(p.err, SPKV_DEVERR_PHYS);
+        else if (static_cast<int>(w >> 24) >= p.max_docs) flag_error(p.err, SPKV_DEVERR_SLOT);
+        const PageInfo pi = page_info(p, b, h, j);
+        if (pi.valid > 0) {
+          mbar_arrive_expect_tx(&S.full[s], kPStageBytes);
+          uint8_t* dst = stages + s * kPStageBytes;
+          const int z = static_cast<int>(int64_t(h) * p.n_phys + pi.phys);
+          tma_load_3d(dst, &tmk, &S.full[s], 0, 0, z, pol);
+          tma_load_3d(dst + kBox, &tmk, &S.full[s], 64, 0, z, pol);
+          tma_load_3d(dst + 2 * kBox, &tmv, &S.full[s], 0, 0, z, pol);
+          tma_load_3d(dst + 3 * kBox, &tmv, &S.full[s], 64, 0, z, pol);
+        } else {
+          mbar_arrive(&S.full[s]);
+        }
+      }
+      __syncwarp();
+    }
+    // no copy of this CTA may still be in flight when it exits
+    for (int i = j > kPStages ? j - kPStages : 0; i < j; ++i) mbar_wait(&S.full[i % kPStages], (i / kPStages) & 1);
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    constexpr uint32_t kIdS = umma_idesc_bf16(kPM, 64, false);
+    constexpr uint32_t kIdO = umma_idesc_bf16(kPM, 128, true);
+    bool ok = true;
+    auto issue_pv = [&](int jj) -> bool {
+      const int bb = jj & 1;
+      if (!warp_wait(&S.pready[bb], (jj >> 1) & 1)) return false;
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t pa = smem_u32(sP + bb * kPBytes);
+        const uint32_t va = smem_u32(stages + (jj % kPStages) * kPStageBytes + 2 * kBox);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_bf16(tbase, umma_desc_sw128(pa + 32 * k, 16, 1024), umma_desc_sw128(va + 2048 * k, 8192, 1024), kIdO,
+                    jj > 0 || k > 0);
+        umma_commit(&S.pvdone[bb]);
+        umma_commit(&S.empty[jj % kPStages]);
+      }
+      __syncwarp();
+      return true;
+    };
+    int prev_slot = -1, n_docs = 0;
+    for (int j = 0; j < n; ++j) {
+      const int s = j % kPStages, bb = j & 1;
+      const PageInfo pi = page_info(p, b, h, j);
+      if (!warp_wait(&S.full[s], (j / kPStages) & 1)) {
+        ok = false;
+        break;
+      }
+      if (pi.valid < 64) {
+        // rows past the valid tokens are multiplied by P = 0: make them exact zeros
+        uint8_t* vt = stages + s * kPStageBytes + 2 * kBox;
+        for (int i = lane; i < (64 - pi.valid) * 16; i += 32) {
+          const int row = pi.valid + (i >> 4), c = i & 15;
+          *reinterpret_cast<uint4*>(vt + (c >> 3) * kBox + row * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (pi.slot != prev_slot) {
+        prev_slot = pi.slot;
+        if (!warp_wait(&S.qready, n_docs & 1)) {
+          ok = false;
+          break;
+        }
+        ++n_docs;
+      }
+      if (j >= 2 && !warp_wait(&S.sfree[bb], ((j - 2) >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t qa = smem_u32(sQ), ka = smem_u32(stages + s * kPStageBytes);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          umma_bf16(tbase + 128 + 64 * bb, umma_desc_sw128(qa + (k >> 2) * (kPM * 128) + (k & 3) * 32, 16, 1024),
+                    umma_desc_sw128(ka + (k >> 2) * kBox + (k & 3) * 32, 16, 1024), kIdS, k > 0);
+        umma_commit(&S.sfull[bb]);
+      }
+      __syncwarp();
+      if (j >= 1 && !(ok = issue_pv(j - 1))) break;
+    }
+    if (ok && n > 0) ok = issue_pv(n - 1);
+    if (!ok && lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
+    // every MMA issued has completed before TMEM is released
+    if (lane == 0) umma_commit(&S.drain);
+    __syncwarp();
+    if (!warp_wait(&S.drain, 0) && lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
+  } else {
+    // ================================================================ softmax warps
+    const int quarter = warp & 3;              // TMEM lanes this warp may access
+    const int r = quarter * 32 + lane;         // query row of the tile
+    const int t = mt * kPM + r;
+    const bool live = t < p.T;
+    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint16_t* qrow = p.q + ((int64_t(b) * p.T + (live ? t : 0)) * p.Hq + hq) * kHeadDim;
+    const int pos = p.qpos0[b] + t;
+    const float scale = p.scale_log2;
+    float m = -CUDART_INF_F, l = 0.f;
+    int prev_slot = -1;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const int bb = j & 1;
+      const PageInfo pi = page_info(p, b, h, j);
+      if (pi.slot != prev_slot) {
+        // Document switch: every MMA that read the previous rotation has completed (its S
+        // row was read in the previous iteration), so row r of Q is rewritten as
+        // R(pos - doc_pos[slot]) q in bf16.
+        prev_slot = pi.slot;
+        const int rel = pos - p.doc_pos[int64_t(b) * p.max_docs + pi.slot];
+#pragma unroll 1
+        for (int cc = 0; cc < 8; ++cc) {
+          uint4 xa = make_uint4(0, 0, 0, 0), ya = make_uint4(0, 0, 0, 0);
+          if (live) {
+            xa = *reinterpret_cast<const uint4*>(qrow + 8 * cc);
+            ya = *reinterpret_cast<const uint4*>(qrow + 64 + 8 * cc);
+          }
+          const uint32_t xw[4] = {xa.x, xa.y, xa.z, xa.w}, yw[4] = {ya.x, ya.y, ya.z, ya.w};
+          uint32_t xo[4], yo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float sn[2], cs[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const int i = 8 * cc + 2 * e + k;   // pair index: dims i and i + 64
+              const uint64_t ph = static_cast<uint64_t>(static_cast<int64_t>(rel)) * p.phase_inc[i];
+              const float ang = static_cast<float>(static_cast<int32_t>(ph >> 32)) * 1.4629180792671596e-09f;
+              __sincosf(ang, &sn[k], &cs[k]);
+            }
+            const float x0 = bf16lo_to_f32(xw[e]), x1 = bf16hi_to_f32(xw[e]);
+            const float y0 = bf16lo_to_f32(yw[e]), y1 = bf16hi_to_f32(yw[e]);
+            xo[e] = pack_bf16x2(x0 * cs[0] - y0 * sn[0], x1 * cs[1] - y1 * sn[1]);
+            yo[e] = pack_bf16x2(y0 * cs[0] + x0 * sn[0], y1 * cs[1] + x1 * sn[1]);
+          }
+          const int off = r * 128 + ((cc ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(sQ + off) = make_uint4(xo[0], xo[1], xo[2], xo[3]);
+          *reinterpret_cast<uint4*>(sQ + kPM * 128 + off) = make_uint4(yo[0], yo[1], yo[2], yo[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.qready);
+      }
+      if (!warp_wait(&S.sfull[bb], (j >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sa[32], sb[32];   // S columns 0..31 and 32..63 of this row
+      tmem_ld32(lane_addr + 128 + 64 * bb, sa);
+      tmem_ld32(lane_addr + 128 + 64 * bb + 32, sb);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.sfree[bb]);
+      float mx = -CUDART_INF_F;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        if (c < pi.valid) mx = fmaxf(mx, __uint_as_float(sa[c]));
+        if (c + 32 < pi.valid) mx = fmaxf(mx, __uint_as_float(sb[c]));
+      }
+      const float m_page = mx * scale;
+      bool rescale = false;
+      float alpha = 1.f;
+      if (m == -CUDART_INF_F) {
+        m = m_page;   // nothing accumulated yet (O holds zeros or nothing)
+      } else if (m_page > m + kRescaleLog2) {
+        rescale = true;
+        alpha = exp2f(m - m_page);
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+        // O must hold every PV issued so far before it is scaled
+        if (!warp_wait(&S.pvdone[(j - 1) & 1], ((j - 1) >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int cb = 0; cb < 128; cb += 32) {
+          uint32_t o[32];
+          tmem_ld32(lane_addr + cb, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+          tmem_st32(lane_addr + cb, o);
+        }
+        tmem_wait_st();
+        if (rescale) {
+          l *= alpha;
+          m = m_page;
+        }
+      }
+      // the P buffer is free once the PV that read it two pages ago has completed
+      if (j >= 2 && !warp_wait(&S.pvdone[bb], ((j - 2) >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      uint8_t* prow = sP + bb * kPBytes + r * 128;
+      float lsum = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c0 = 8 * cc + 2 * e;
+          const float s0 = __uint_as_float(c0 < 32 ? sa[c0 & 31] : sb[c0 & 31]);
+          const float s1 = __uint_as_float(c0 + 1 < 32 ? sa[(c0 + 1) & 31] : sb[(c0 + 1) & 31]);
+          const float p0 = (c0 < pi.valid && m != -CUDART_INF_F) ? exp2f(s0 * scale - m) : 0.f;
+          const float p1 = (c0 + 1 < pi.valid && m != -CUDART_INF_F) ? exp2f(s1 * scale - m) : 0.f;
+          w4[e] = pack_bf16x2(p0, p1);
+          lsum += bf16lo_to_f32(w4[e]) + bf16hi_to_f32(w4[e]);   // sum what the MMA multiplies
+        }
+        *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      }
+      l += lsum;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.pready[bb]);
+    }
+    if (ok && n > 0) ok = warp_wait(&S.pvdone[(n - 1) & 1], ((n - 1) >> 1) & 1);
+    if (!ok && lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
+    tc_fence_after();
+    float* orow = p.out + ((int64_t(b) * p.T + (live ? t : 0)) * p.Hq + hq) * kHeadDim;
+    const bool have = ok && n > 0 && l > 0.f;
+    const float inv_l = have ? 1.f / l : 0.f;
+#pragma unroll 1
+    for (int cb = 0; cb < 128; cb += 32) {
+      uint32_t o[32] = {};
+      if (ok && n > 0) {   // TMEM holds O only once a PV has run
+        tmem_ld32(lane_addr + cb, o);
+        tmem_wait_ld();
+      }
+      if (live) {
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          float4 v;
+          v.x = have ? __uint_as_float(o[c]) * inv_l : 0.f;
+          v.y = have ? __uint_as_float(o[c + 1]) * inv_l : 0.f;
+          v.z = have ? __uint_as_float(o[c + 2]) * inv_l : 0.f;
+          v.w = have ? __uint_as_float(o[c + 3]) * inv_l : 0.f;
+          *reinterpret_cast<float4*>(orow + cb + c) = v;
+        }
+      }
+    }
+    if (live) p.lse[(int64_t(b) * p.T + t) * p.Hq + hq] = have ? (m + log2f(l)) * kLn2 : -CUDART_INF_F;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+}  // namespace
+
+size_t prefill_smem_bytes() { return kPrefillSmem; }
+
+cudaError_t prefill_init_attributes() {
+  return cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kPrefillSmem));
+}
+
+cudaError_t launch_prefill(const spkv_cache* c, const PrefillParams& p, cudaStream_t st) {
+  const dim3 grid((p.T + kPM - 1) / kPM, p.Hq, p.B);
+  return launch_pdl(prefill_kernel, grid, dim3(kPThreads), kPrefillSmem, st, c->tmap_k, c->tmap_v, p);
+}
+
+}  // namespace spkv

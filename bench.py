@@ -50,6 +50,10 @@ def parse():
     ap.add_argument("--no-lazy", action="store_true")
     ap.add_argument("--no-rag", action="store_true", help="skip the lazy-RoPE RAG sub-measurement")
     ap.add_argument("--no-prefill", action="store_true", help="skip the LazyAttention prefill sub-measurement")
+    ap.add_argument("--rag-batch", type=int, default=64,
+                    help="requests of the lazy-RoPE RAG workload (64 = the workload; smaller for profiling)")
+    ap.add_argument("--rag-docs", type=int, default=256,
+                    help="cached documents of the RAG workload (256 = the workload; smaller for profiling)")
     ap.add_argument("--no-offload", action="store_true",
                     help="skip the offload sub-measurement (262k context, pool in pinned host memory)")
     ap.add_argument("--l2", default="none", choices=["none", "write"],
@@ -541,7 +545,7 @@ def run_native(args):
     rag = None
     prefill = None
     if not args.no_rag and rank == 0:
-        wr = gen.lazy_rag(seed=0)
+        wr = gen.lazy_rag(seed=0, B=args.rag_batch, n_docs=args.rag_docs)
         Br, Hqr, Hkr = wr["B"], wr["Hq"], wr["Hk"]
         rk, rv = bf(wr["k_pool"]), bf(wr["v_pool"])
         rks = torch.zeros(Hkr, wr["n_phys"], 4, 128, dtype=torch.float32, device=dev)
@@ -579,7 +583,7 @@ def run_native(args):
             tflops = flops / (pre_ms * 1e-3) / 1e12
             tpeak, tkind = bf16_peak()
             prefill = {"kernel": "lazy_rope_prefill_attn (tcgen05.mma, TMEM accumulators, TMA pages)",
-                       "workload": "the RAG documents above, 128 new query rows per request (64 x 128 x 32 heads)",
+                       "workload": f"the RAG documents above, 128 new query rows per request ({Br} x 128 x 32 heads)",
                        "us": pre_ms * 1e3, "flops": flops, "bound": "tensor", "achieved_TFLOPs": tflops,
                        "peak": tpeak, "peak_kind": tkind + " bf16 dense (cuBLAS burst)", "frac": tflops / tpeak,
                        "query_rows_per_s": Br * Tq / (pre_ms * 1e-3)}
@@ -588,7 +592,8 @@ def run_native(args):
         if st != 0:
             raise RuntimeError(f"device error bits {bits} in the RAG leg")
         rcache.close()
-        rag = {"workload": "lazy-RoPE RAG decode B64 Hq32/Hk8, 8 Zipf(1.1) docs of 1024-4096 tokens",
+        rag = {"workload": f"lazy-RoPE RAG decode B{Br} Hq32/Hk8, 8 Zipf(1.1) docs of 1024-4096 tokens "
+                           f"(pool of {args.rag_docs} documents)",
                "us": rag_ms * 1e3, "logical_GBps": logical / (rag_ms * 1e-3) / 1e9,
                "distinct_page_GBps": distinct / (rag_ms * 1e-3) / 1e9,
                "logical_bytes": logical, "distinct_page_bytes": distinct,

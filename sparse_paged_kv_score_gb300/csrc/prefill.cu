@@ -11,17 +11,22 @@
 // switch (a document spans tens of pages, so this is cheaper still, and the key tiles stay as
 // TMA wrote them).  Both give the same scores.
 //
-// One CTA per (request b, query head, tile of 128 query rows); six warps:
+// One CTA per (request b, kv head h, pair of query heads of its group, tile of 128 query
+// rows): the two query heads are two 128-row tiles that share every K/V page, so each page
+// feeds twice the tensor-core work and two softmax warpgroups take turns (ten warps):
 //   warp 0     TMA producer: K and V of each page (two 64 x 64 bf16 boxes each, 128-byte
-//              swizzle) into a 4-stage ring;
-//   warp 1     MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM S buffers (M 128,
-//              N 64), then O += P_(j-1) V_(j-1) (M 128, N 128, V read MN-major); it also zeroes
-//              the V rows of a partial page so that P = 0 never meets garbage;
-//   warps 2-5  softmax: thread r owns query row r (TMEM lane r): it rotates its query row on
-//              document switches, reads its S row from TMEM, runs the online softmax in the
-//              log2 domain, writes its P row (bf16) as the A operand of the next PV MMA, and
-//              rescales its O row in TMEM only when the row maximum has grown by more than
-//              2^8 since the last rescale; at the end it normalises O and writes out and lse.
+//              swizzle) into a 3-stage ring;
+//   warp 1     MMA issuer (one thread): per tile x, S_x = Q_x K_j^T into one of two TMEM S
+//              buffers (M 128, N 64), then O_x += P_x V_(j-1) (M 128, N 128, V read MN-major);
+//              it also zeroes the V rows of a partial page so that P = 0 never meets garbage;
+//   warps 2-5, 6-9  softmax of tile 0 and tile 1: thread r owns query row r (TMEM lane r):
+//              it rotates its query row on document switches, reads its S row from TMEM,
+//              runs the online softmax in the log2 domain, writes its P row (bf16) as the A
+//              operand of a PV MMA (P double-buffered, so the softmax of page j never waits
+//              for the PV of page j - 1), and rescales its O row in TMEM only when the row
+//              maximum has grown by more than 2^8 since the last rescale; at the end it
+//              normalises O and writes out and lse.
+// Tensor memory holds all 512 columns: O of both tiles and two S buffers per tile.
 // Hand-offs are mbarriers; every wait is bounded (SPKV_DEVERR_TIMEOUT), and the MMA issuer
 // drains its MMAs before TMEM is released.
 #include <math_constants.h>
@@ -34,24 +39,30 @@ namespace spkv {
 namespace {
 
 constexpr int kPM = 128;                      // query rows per tile (TMEM lanes)
-constexpr int kPStages = 4;                   // K/V page ring
-constexpr int kPThreads = 192;
+constexpr int kTiles = 2;                     // query heads (tiles) per CTA
+constexpr int kPStages = 3;                   // K/V page ring
+constexpr int kPThreads = 64 + kTiles * 128;
 constexpr int kBox = 64 * 128;                // one 64 x 64 bf16 box, bytes
 constexpr int kPStageBytes = 4 * kBox;        // K (2 boxes) + V (2 boxes) of one page-head
 constexpr int kQBytes = 2 * kPM * 128;        // Q tile: two boxes of 128 rows x 128 B
 constexpr int kPBytes = kPM * 128;            // P tile: 128 rows x 64 bf16
-constexpr uint32_t kTmemCols = 256;           // O: columns 0..127; S buffers: 128..191, 192..255
+constexpr uint32_t kTmemCols = 512;           // O of tile x: 128 x .. ; S buffers from column 256
 constexpr float kRescaleLog2 = 8.f;           // row-max growth (log2) tolerated before O is rescaled
 constexpr float kLn2 = 0.69314718055994530942f;
 
+__host__ __device__ constexpr uint32_t o_col(int x) { return 128u * x; }
+__host__ __device__ constexpr uint32_t s_col(int x, int bb) { return 256u + 128u * x + 64u * bb; }
+
 struct PrefillSmem {
   uint64_t full[kPStages], empty[kPStages];
-  uint64_t sfull[2], sfree[2], pready[2], pvdone[2];
-  uint64_t qready, drain;
+  uint64_t sfull[kTiles][2], sfree[kTiles][2], pready[kTiles][2], pvdone[kTiles][2], qready[kTiles];
+  uint64_t drain;
   uint32_t tmem_base;
 };
 
-constexpr size_t kPrefillSmem = 1024 + kQBytes + 2 * kPBytes + size_t(kPStages) * kPStageBytes + sizeof(PrefillSmem);
+constexpr size_t kPrefillSmem =
+    1024 + size_t(kTiles) * (kQBytes + 2 * kPBytes) + size_t(kPStages) * kPStageBytes + sizeof(PrefillSmem);
+static_assert(kPrefillSmem <= 232448, "prefill shared memory exceeds the per-CTA limit");
 
 struct PageInfo {
   int phys, valid, slot;
@@ -77,31 +88,41 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __global__ void __launch_bounds__(kPThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                    const __grid_constant__ PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = base;
-  uint8_t* sP = base + kQBytes;
-  uint8_t* stages = sP + 2 * kPBytes;
+  uint8_t* sQ = base;                            // tile x at x * kQBytes
+  uint8_t* sP = base + kTiles * kQBytes;         // tile x, buffer bb at (2 x + bb) * kPBytes
+  uint8_t* stages = sP + 2 * kTiles * kPBytes;
   PrefillSmem& S = *reinterpret_cast<PrefillSmem*>(stages + kPStages * kPStageBytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int mt = blockIdx.x, hq = blockIdx.y, b = blockIdx.z;
-  const int h = hq / p.G;
+  const int mt = blockIdx.x, b = blockIdx.z;
+  const int pairs = (p.G + 1) / 2;
+  const int h = blockIdx.y / pairs, hq0 = h * p.G + 2 * (blockIdx.y % pairs);
+  const int n_tiles = min(kTiles, h * p.G + p.G - hq0);   // the last pair of an odd group has one head
 
   if (tid == 0) {
     for (int s = 0; s < kPStages; ++s) {
       mbar_init(&S.full[s], 1);
       mbar_init(&S.empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&S.sfull[i], 1);
-      mbar_init(&S.sfree[i], 4);
-      mbar_init(&S.pready[i], 4);
-      mbar_init(&S.pvdone[i], 1);
+    for (int x = 0; x < kTiles; ++x) {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&S.sfull[x][i], 1);
+        mbar_init(&S.sfree[x][i], 4);
+        mbar_init(&S.pready[x][i], 4);
+        mbar_init(&S.pvdone[x][i], 1);
+      }
+      mbar_init(&S.qready[x], 4);
     }
-    mbar_init(&S.qready, 4);
     mbar_init(&S.drain, 1);
     fence_mbar_init();
     prefetch_tensormap(&tmk);
@@ -120,7 +141,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
   if (warp == 0) {
     // ================================================================ TMA producer
-    const uint64_t pol = l2_policy_evict_last();   // the group's query heads and other requests reuse pages
+    const uint64_t pol = l2_policy_evict_last();   // the group's other query heads and other requests reuse pages
     int j = 0;
     for (; j < n; ++j) {
       const int s = j % kPStages;
@@ -155,25 +176,34 @@ __global__ void __launch_bounds__(kPThreads, 1)
     constexpr uint32_t kIdS = umma_idesc_bf16(kPM, 64, false);
     constexpr uint32_t kIdO = umma_idesc_bf16(kPM, 128, true);
     bool ok = true;
+    // Operand descriptors are formed once; a k step adds its byte offset / 16 to the start
+    // address field (every address here is below 256 KiB, so the field never overflows).
+    const uint64_t q_desc = umma_desc_sw128(smem_u32(sQ), 16, 1024);
+    const uint64_t p_desc = umma_desc_sw128(smem_u32(sP), 16, 1024);
+    const uint64_t k_desc = umma_desc_sw128(smem_u32(stages), 16, 1024);
+    const uint64_t v_desc = umma_desc_sw128(smem_u32(stages + 2 * kBox), 8192, 1024);
+    // O_x += P_x V_jj for every tile, then the page's stage is released
     auto issue_pv = [&](int jj) -> bool {
-      const int bb = jj & 1;
-      if (!warp_wait(&S.pready[bb], (jj >> 1) & 1)) return false;
-      if (lane == 0) {
-        tc_fence_after();
-        const uint32_t pa = smem_u32(sP + bb * kPBytes);
-        const uint32_t va = smem_u32(stages + (jj % kPStages) * kPStageBytes + 2 * kBox);
+      const int pb = jj & 1;
+      for (int x = 0; x < n_tiles; ++x) {
+        if (!warp_wait(&S.pready[x][pb], (jj >> 1) & 1)) return false;
+        if (lane == 0) {
+          tc_fence_after();
+          const uint64_t pa = p_desc + (((2 * x + pb) * kPBytes) >> 4);
+          const uint64_t va = v_desc + (((jj % kPStages) * kPStageBytes) >> 4);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          umma_bf16(tbase, umma_desc_sw128(pa + 32 * k, 16, 1024), umma_desc_sw128(va + 2048 * k, 8192, 1024), kIdO,
-                    jj > 0 || k > 0);
-        umma_commit(&S.pvdone[bb]);
-        umma_commit(&S.empty[jj % kPStages]);
+          for (int k = 0; k < 4; ++k)
+            umma_bf16(tbase + o_col(x), pa + 2 * k, va + 128 * k, kIdO, jj > 0 || k > 0);
+          umma_commit(&S.pvdone[x][pb]);
+        }
+        __syncwarp();
       }
+      if (lane == 0) umma_commit(&S.empty[jj % kPStages]);
       __syncwarp();
       return true;
     };
     int prev_slot = -1, n_docs = 0;
-    for (int j = 0; j < n; ++j) {
+    for (int j = 0; j < n && ok; ++j) {
       const int s = j % kPStages, bb = j & 1;
       const PageInfo pi = page_info(p, b, h, j);
       if (!warp_wait(&S.full[s], (j / kPStages) & 1)) {
@@ -190,28 +220,25 @@ __global__ void __launch_bounds__(kPThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
       }
-      if (pi.slot != prev_slot) {
-        prev_slot = pi.slot;
-        if (!warp_wait(&S.qready, n_docs & 1)) {
-          ok = false;
-          break;
-        }
-        ++n_docs;
-      }
-      if (j >= 2 && !warp_wait(&S.sfree[bb], ((j - 2) >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      if (lane == 0) {
-        tc_fence_after();
-        const uint32_t qa = smem_u32(sQ), ka = smem_u32(stages + s * kPStageBytes);
+      const bool new_doc = pi.slot != prev_slot;
+      prev_slot = pi.slot;
+      for (int x = 0; x < n_tiles && ok; ++x) {
+        if (new_doc && !warp_wait(&S.qready[x], n_docs & 1)) ok = false;
+        else if (j >= 2 && !warp_wait(&S.sfree[x][bb], ((j - 2) >> 1) & 1)) ok = false;
+        if (!ok) break;
+        if (lane == 0) {
+          tc_fence_after();
+          const uint64_t qa = q_desc + ((x * kQBytes) >> 4), ka = k_desc + ((s * kPStageBytes) >> 4);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          umma_bf16(tbase + 128 + 64 * bb, umma_desc_sw128(qa + (k >> 2) * (kPM * 128) + (k & 3) * 32, 16, 1024),
-                    umma_desc_sw128(ka + (k >> 2) * kBox + (k & 3) * 32, 16, 1024), kIdS, k > 0);
-        umma_commit(&S.sfull[bb]);
+          for (int k = 0; k < 8; ++k)
+            umma_bf16(tbase + s_col(x, bb), qa + (((k >> 2) * (kPM * 128) + (k & 3) * 32) >> 4),
+                      ka + (((k >> 2) * kBox + (k & 3) * 32) >> 4), kIdS, k > 0);
+          umma_commit(&S.sfull[x][bb]);
+        }
+        __syncwarp();
       }
-      __syncwarp();
+      if (!ok) break;
+      if (new_doc) ++n_docs;
       if (j >= 1 && !(ok = issue_pv(j - 1))) break;
     }
     if (ok && n > 0) ok = issue_pv(n - 1);
@@ -220,14 +247,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (lane == 0) umma_commit(&S.drain);
     __syncwarp();
     if (!warp_wait(&S.drain, 0) && lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
-  } else {
-    // ================================================================ softmax warps
+  } else if ((warp - 2) / 4 < n_tiles) {
+    // ================================================================ softmax warps of tile x
+    const int x = (warp - 2) / 4;
+    const int hq = hq0 + x;
     const int quarter = warp & 3;              // TMEM lanes this warp may access
     const int r = quarter * 32 + lane;         // query row of the tile
     const int t = mt * kPM + r;
     const bool live = t < p.T;
     const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint16_t* qrow = p.q + ((int64_t(b) * p.T + (live ? t : 0)) * p.Hq + hq) * kHeadDim;
+    uint8_t* qtile = sQ + x * kQBytes;
+    uint8_t* prow0 = sP + 2 * x * kPBytes + r * 128;   // P buffer bb of this row: + bb * kPBytes
     const int pos = p.qpos0[b] + t;
     const float scale = p.scale_log2;
     float m = -CUDART_INF_F, l = 0.f;
@@ -267,30 +298,31 @@ __global__ void __launch_bounds__(kPThreads, 1)
             yo[e] = pack_bf16x2(y0 * cs[0] + x0 * sn[0], y1 * cs[1] + x1 * sn[1]);
           }
           const int off = r * 128 + ((cc ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(sQ + off) = make_uint4(xo[0], xo[1], xo[2], xo[3]);
-          *reinterpret_cast<uint4*>(sQ + kPM * 128 + off) = make_uint4(yo[0], yo[1], yo[2], yo[3]);
+          *reinterpret_cast<uint4*>(qtile + off) = make_uint4(xo[0], xo[1], xo[2], xo[3]);
+          *reinterpret_cast<uint4*>(qtile + kPM * 128 + off) = make_uint4(yo[0], yo[1], yo[2], yo[3]);
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&S.qready);
+        if (lane == 0) mbar_arrive(&S.qready[x]);
       }
-      if (!warp_wait(&S.sfull[bb], (j >> 1) & 1)) {
+      if (!warp_wait(&S.sfull[x][bb], (j >> 1) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t sa[32], sb[32];   // S columns 0..31 and 32..63 of this row
-      tmem_ld32(lane_addr + 128 + 64 * bb, sa);
-      tmem_ld32(lane_addr + 128 + 64 * bb + 32, sb);
+      tmem_ld32(lane_addr + s_col(x, bb), sa);
+      tmem_ld32(lane_addr + s_col(x, bb) + 32, sb);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.sfree[bb]);
+      if (lane == 0) mbar_arrive(&S.sfree[x][bb]);
+      const int valid = pi.valid;
       float mx = -CUDART_INF_F;
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        if (c < pi.valid) mx = fmaxf(mx, __uint_as_float(sa[c]));
-        if (c + 32 < pi.valid) mx = fmaxf(mx, __uint_as_float(sb[c]));
+        mx = fmaxf(mx, c < valid ? __uint_as_float(sa[c]) : -CUDART_INF_F);
+        mx = fmaxf(mx, c + 32 < valid ? __uint_as_float(sb[c]) : -CUDART_INF_F);
       }
       const float m_page = mx * scale;
       bool rescale = false;
@@ -299,11 +331,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
         m = m_page;   // nothing accumulated yet (O holds zeros or nothing)
       } else if (m_page > m + kRescaleLog2) {
         rescale = true;
-        alpha = exp2f(m - m_page);
+        alpha = fast_exp2(m - m_page);
       }
       if (__any_sync(0xffffffffu, rescale)) {
         // O must hold every PV issued so far before it is scaled
-        if (!warp_wait(&S.pvdone[(j - 1) & 1], ((j - 1) >> 1) & 1)) {
+        if (!warp_wait(&S.pvdone[x][(j - 1) & 1], ((j - 1) >> 1) & 1)) {
           ok = false;
           break;
         }
@@ -311,11 +343,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll 1
         for (int cb = 0; cb < 128; cb += 32) {
           uint32_t o[32];
-          tmem_ld32(lane_addr + cb, o);
+          tmem_ld32(lane_addr + o_col(x) + cb, o);
           tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-          tmem_st32(lane_addr + cb, o);
+          tmem_st32(lane_addr + o_col(x) + cb, o);
         }
         tmem_wait_st();
         if (rescale) {
@@ -323,12 +355,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
           m = m_page;
         }
       }
-      // the P buffer is free once the PV that read it two pages ago has completed
-      if (j >= 2 && !warp_wait(&S.pvdone[bb], ((j - 2) >> 1) & 1)) {
+      // P buffer bb is free once the PV that read it two pages ago has completed
+      if (j >= 2 && !warp_wait(&S.pvdone[x][bb], ((j - 2) >> 1) & 1)) {
         ok = false;
         break;
       }
-      uint8_t* prow = sP + bb * kPBytes + r * 128;
+      uint8_t* prow = prow0 + bb * kPBytes;
+      const bool any = m != -CUDART_INF_F;
+      const float mneg = any ? -m : 0.f;
       float lsum = 0.f;
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc) {
@@ -338,10 +372,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
           const int c0 = 8 * cc + 2 * e;
           const float s0 = __uint_as_float(c0 < 32 ? sa[c0 & 31] : sb[c0 & 31]);
           const float s1 = __uint_as_float(c0 + 1 < 32 ? sa[(c0 + 1) & 31] : sb[(c0 + 1) & 31]);
-          const float p0 = (c0 < pi.valid && m != -CUDART_INF_F) ? exp2f(s0 * scale - m) : 0.f;
-          const float p1 = (c0 + 1 < pi.valid && m != -CUDART_INF_F) ? exp2f(s1 * scale - m) : 0.f;
+          const float p0 = (c0 < valid && any) ? fast_exp2(fmaf(s0, scale, mneg)) : 0.f;
+          const float p1 = (c0 + 1 < valid && any) ? fast_exp2(fmaf(s1, scale, mneg)) : 0.f;
+          lsum += p0 + p1;
           w4[e] = pack_bf16x2(p0, p1);
-          lsum += bf16lo_to_f32(w4[e]) + bf16hi_to_f32(w4[e]);   // sum what the MMA multiplies
         }
         *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
@@ -349,9 +383,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.pready[bb]);
+      if (lane == 0) mbar_arrive(&S.pready[x][bb]);
     }
-    if (ok && n > 0) ok = warp_wait(&S.pvdone[(n - 1) & 1], ((n - 1) >> 1) & 1);
+    if (ok && n > 0) ok = warp_wait(&S.pvdone[x][(n - 1) & 1], ((n - 1) >> 1) & 1);
     if (!ok && lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
     tc_fence_after();
     float* orow = p.out + ((int64_t(b) * p.T + (live ? t : 0)) * p.Hq + hq) * kHeadDim;
@@ -361,7 +395,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     for (int cb = 0; cb < 128; cb += 32) {
       uint32_t o[32] = {};
       if (ok && n > 0) {   // TMEM holds O only once a PV has run
-        tmem_ld32(lane_addr + cb, o);
+        tmem_ld32(lane_addr + o_col(x) + cb, o);
         tmem_wait_ld();
       }
       if (live) {
@@ -397,7 +431,8 @@ cudaError_t prefill_init_attributes() {
 }
 
 cudaError_t launch_prefill(const spkv_cache* c, const PrefillParams& p, cudaStream_t st) {
-  const dim3 grid((p.T + kPM - 1) / kPM, p.Hq, p.B);
+  const int pairs = (p.G + 1) / 2;
+  const dim3 grid((p.T + kPM - 1) / kPM, p.Hk * pairs, p.B);
   return launch_pdl(prefill_kernel, grid, dim3(kPThreads), kPrefillSmem, st, c->tmap_k, c->tmap_v, p);
 }
 

@@ -15,7 +15,7 @@
 // rows): the two query heads are two 128-row tiles that share every K/V page, so each page
 // feeds twice the tensor-core work and two softmax warpgroups take turns (ten warps):
 //   warp 0     TMA producer: K and V of each page (two 64 x 64 bf16 boxes each, 128-byte
-//              swizzle) into a 3-stage ring;
+//              swizzle) into a 3-stage ring, and L2 prefetches of the pages 8 beyond it;
 //   warp 1     MMA issuer (one thread): per tile x, S_x = Q_x K_j^T into one of two TMEM S
 //              buffers (M 128, N 64), then O_x += P_x V_(j-1) (M 128, N 128, V read MN-major);
 //              it also zeroes the V rows of a partial page so that P = 0 never meets garbage;
@@ -41,6 +41,7 @@ namespace {
 constexpr int kPM = 128;                      // query rows per tile (TMEM lanes)
 constexpr int kTiles = 2;                     // query heads (tiles) per CTA
 constexpr int kPStages = 3;                   // K/V page ring
+constexpr int kPrefetch = 8;                  // pages ahead of the ring that are fetched into L2
 constexpr int kPThreads = 64 + kTiles * 128;
 constexpr int kBox = 64 * 128;                // one 64 x 64 bf16 box, bytes
 constexpr int kPStageBytes = 4 * kBox;        // K (2 boxes) + V (2 boxes) of one page-head
@@ -142,9 +143,23 @@ __global__ void __launch_bounds__(kPThreads, 1)
   if (warp == 0) {
     // ================================================================ TMA producer
     const uint64_t pol = l2_policy_evict_last();   // the group's other query heads and other requests reuse pages
+    // A stage is held until the PV of its page completes, so the ring alone runs only a page or
+    // two ahead of the MMAs; pages further ahead are fetched into L2 so that their loads hit.
+    auto prefetch = [&](int jj) {
+      const PageInfo pi = page_info(p, b, h, jj);
+      if (pi.valid == 0) return;
+      const int z = static_cast<int>(int64_t(h) * p.n_phys + pi.phys);
+      tma_prefetch_l2_3d(&tmk, 0, 0, z);
+      tma_prefetch_l2_3d(&tmk, 64, 0, z);
+      tma_prefetch_l2_3d(&tmv, 0, 0, z);
+      tma_prefetch_l2_3d(&tmv, 64, 0, z);
+    };
+    if (lane == 0)
+      for (int jj = kPStages; jj < min(n, kPStages + kPrefetch); ++jj) prefetch(jj);
     int j = 0;
     for (; j < n; ++j) {
       const int s = j % kPStages;
+      if (lane == 0 && j + kPStages + kPrefetch < n) prefetch(j + kPStages + kPrefetch);
       if (j >= kPStages && !warp_wait(&S.empty[s], ((j / kPStages) - 1) & 1)) {
         if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
         break;
@@ -318,12 +333,25 @@ __global__ void __launch_bounds__(kPThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.sfree[x][bb]);
       const int valid = pi.valid;
-      float mx = -CUDART_INF_F;
+      float v[64];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        mx = fmaxf(mx, c < valid ? __uint_as_float(sa[c]) : -CUDART_INF_F);
-        mx = fmaxf(mx, c + 32 < valid ? __uint_as_float(sb[c]) : -CUDART_INF_F);
+        v[c] = __uint_as_float(sa[c]);
+        v[c + 32] = __uint_as_float(sb[c]);
       }
+      // row maximum over the valid columns, eight independent chains
+      float mx8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx8[k] = -CUDART_INF_F;
+      if (valid == 64) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], v[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], c < valid ? v[c] : -CUDART_INF_F);
+      }
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_page = mx * scale;
       bool rescale = false;
       float alpha = 1.f;
@@ -361,23 +389,27 @@ __global__ void __launch_bounds__(kPThreads, 1)
         break;
       }
       uint8_t* prow = prow0 + bb * kPBytes;
-      const bool any = m != -CUDART_INF_F;
-      const float mneg = any ? -m : 0.f;
-      float lsum = 0.f;
+      // p = 2^(s * scale - m), zero past the valid columns (and everywhere while m is -inf)
+      const bool full = valid == 64 && m != -CUDART_INF_F;
+      const float mneg = m != -CUDART_INF_F ? -m : 0.f;
+      const int lim = m != -CUDART_INF_F ? valid : 0;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float e = fast_exp2(fmaf(v[c], scale, mneg));
+        v[c] = full ? e : (c < lim ? e : 0.f);
+      }
+      float ls8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ls8[k] = 0.f;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) ls8[c & 7] += v[c];
+      const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc) {
-        uint32_t w4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c0 = 8 * cc + 2 * e;
-          const float s0 = __uint_as_float(c0 < 32 ? sa[c0 & 31] : sb[c0 & 31]);
-          const float s1 = __uint_as_float(c0 + 1 < 32 ? sa[(c0 + 1) & 31] : sb[(c0 + 1) & 31]);
-          const float p0 = (c0 < valid && any) ? fast_exp2(fmaf(s0, scale, mneg)) : 0.f;
-          const float p1 = (c0 + 1 < valid && any) ? fast_exp2(fmaf(s1, scale, mneg)) : 0.f;
-          lsum += p0 + p1;
-          w4[e] = pack_bf16x2(p0, p1);
-        }
-        *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        const uint4 w4 = make_uint4(pack_bf16x2(v[8 * cc], v[8 * cc + 1]), pack_bf16x2(v[8 * cc + 2], v[8 * cc + 3]),
+                                    pack_bf16x2(v[8 * cc + 4], v[8 * cc + 5]),
+                                    pack_bf16x2(v[8 * cc + 6], v[8 * cc + 7]));
+        *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) = w4;
       }
       l += lsum;
       fence_proxy_async_smem();

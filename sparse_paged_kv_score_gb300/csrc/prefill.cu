@@ -15,15 +15,16 @@
 // rows): the two query heads are two 128-row tiles that share every K/V page, so each page
 // feeds twice the tensor-core work and two softmax warpgroups take turns (ten warps):
 //   warp 0     TMA producer: K and V of each page (two 64 x 64 bf16 boxes each, 128-byte
-//              swizzle) into a 3-stage ring, and L2 prefetches of the pages 8 beyond it;
+//              swizzle) into a 5-stage ring, and L2 prefetches of the pages 8 beyond it;
 //   warp 1     MMA issuer (one thread): per tile x, S_x = Q_x K_j^T into one of two TMEM S
-//              buffers (M 128, N 64), then O_x += P_x V_(j-1) (M 128, N 128, V read MN-major);
+//              buffers (M 128, N 64), then O_x += P_x V_(j-1) (M 128, N 128) with P read from
+//              tensor memory and V from shared memory (MN-major);
 //              it also zeroes the V rows of a partial page so that P = 0 never meets garbage;
 //   warps 2-5, 6-9  softmax of tile 0 and tile 1: thread r owns query row r (TMEM lane r):
 //              it rotates its query row on document switches, reads its S row from TMEM,
-//              runs the online softmax in the log2 domain, writes its P row (bf16) as the A
-//              operand of a PV MMA (P double-buffered, so the softmax of page j never waits
-//              for the PV of page j - 1), and rescales its O row in TMEM only when the row
+//              runs the online softmax in the log2 domain, writes its P row (bf16 pairs) back
+//              over its S row in tensor memory as the A operand of the PV MMA (so P never
+//              crosses shared memory), and rescales its O row in TMEM only when the row
 //              maximum has grown by more than 2^8 since the last rescale; at the end it
 //              normalises O and writes out and lse.
 // Tensor memory holds all 512 columns: O of both tiles and two S buffers per tile.
@@ -40,14 +41,13 @@ namespace {
 
 constexpr int kPM = 128;                      // query rows per tile (TMEM lanes)
 constexpr int kTiles = 2;                     // query heads (tiles) per CTA
-constexpr int kPStages = 3;                   // K/V page ring
+constexpr int kPStages = 5;                   // K/V page ring
 constexpr int kPrefetch = 8;                  // pages ahead of the ring that are fetched into L2
 constexpr int kPThreads = 64 + kTiles * 128;
 constexpr int kBox = 64 * 128;                // one 64 x 64 bf16 box, bytes
 constexpr int kPStageBytes = 4 * kBox;        // K (2 boxes) + V (2 boxes) of one page-head
 constexpr int kQBytes = 2 * kPM * 128;        // Q tile: two boxes of 128 rows x 128 B
-constexpr int kPBytes = kPM * 128;            // P tile: 128 rows x 64 bf16
-constexpr uint32_t kTmemCols = 512;           // O of tile x: 128 x .. ; S buffers from column 256
+constexpr uint32_t kTmemCols = 512;           // O of tile x: 128 x .. ; S / P buffers from column 256
 constexpr float kRescaleLog2 = 8.f;           // row-max growth (log2) tolerated before O is rescaled
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -56,13 +56,13 @@ __host__ __device__ constexpr uint32_t s_col(int x, int bb) { return 256u + 128u
 
 struct PrefillSmem {
   uint64_t full[kPStages], empty[kPStages];
-  uint64_t sfull[kTiles][2], sfree[kTiles][2], pready[kTiles][2], pvdone[kTiles][2], qready[kTiles];
+  uint64_t sfull[kTiles][2], pready[kTiles][2], pvdone[kTiles][2], qready[kTiles];
   uint64_t drain;
   uint32_t tmem_base;
 };
 
 constexpr size_t kPrefillSmem =
-    1024 + size_t(kTiles) * (kQBytes + 2 * kPBytes) + size_t(kPStages) * kPStageBytes + sizeof(PrefillSmem);
+    1024 + size_t(kTiles) * kQBytes + size_t(kPStages) * kPStageBytes + sizeof(PrefillSmem);
 static_assert(kPrefillSmem <= 232448, "prefill shared memory exceeds the per-CTA limit");
 
 struct PageInfo {
@@ -101,8 +101,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;                            // tile x at x * kQBytes
-  uint8_t* sP = base + kTiles * kQBytes;         // tile x, buffer bb at (2 x + bb) * kPBytes
-  uint8_t* stages = sP + 2 * kTiles * kPBytes;
+  uint8_t* stages = base + kTiles * kQBytes;
   PrefillSmem& S = *reinterpret_cast<PrefillSmem*>(stages + kPStages * kPStageBytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int mt = blockIdx.x, b = blockIdx.z;
@@ -118,7 +117,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
     for (int x = 0; x < kTiles; ++x) {
       for (int i = 0; i < 2; ++i) {
         mbar_init(&S.sfull[x][i], 1);
-        mbar_init(&S.sfree[x][i], 4);
         mbar_init(&S.pready[x][i], 4);
         mbar_init(&S.pvdone[x][i], 1);
       }
@@ -194,7 +192,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // Operand descriptors are formed once; a k step adds its byte offset / 16 to the start
     // address field (every address here is below 256 KiB, so the field never overflows).
     const uint64_t q_desc = umma_desc_sw128(smem_u32(sQ), 16, 1024);
-    const uint64_t p_desc = umma_desc_sw128(smem_u32(sP), 16, 1024);
     const uint64_t k_desc = umma_desc_sw128(smem_u32(stages), 16, 1024);
     const uint64_t v_desc = umma_desc_sw128(smem_u32(stages + 2 * kBox), 8192, 1024);
     // O_x += P_x V_jj for every tile, then the page's stage is released
@@ -204,11 +201,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (!warp_wait(&S.pready[x][pb], (jj >> 1) & 1)) return false;
         if (lane == 0) {
           tc_fence_after();
-          const uint64_t pa = p_desc + (((2 * x + pb) * kPBytes) >> 4);
           const uint64_t va = v_desc + (((jj % kPStages) * kPStageBytes) >> 4);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            umma_bf16(tbase + o_col(x), pa + 2 * k, va + 128 * k, kIdO, jj > 0 || k > 0);
+          for (int k = 0; k < 4; ++k)   // P (bf16 pairs) sits in the first 32 columns of its S buffer
+            umma_bf16_tmem_a(tbase + o_col(x), tbase + s_col(x, pb) + 8 * k, va + 128 * k, kIdO, jj > 0 || k > 0);
           umma_commit(&S.pvdone[x][pb]);
         }
         __syncwarp();
@@ -238,8 +234,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const bool new_doc = pi.slot != prev_slot;
       prev_slot = pi.slot;
       for (int x = 0; x < n_tiles && ok; ++x) {
+        // S buffer bb held P of page j - 2: free once that PV has completed
         if (new_doc && !warp_wait(&S.qready[x], n_docs & 1)) ok = false;
-        else if (j >= 2 && !warp_wait(&S.sfree[x][bb], ((j - 2) >> 1) & 1)) ok = false;
+        else if (j >= 2 && !warp_wait(&S.pvdone[x][bb], ((j - 2) >> 1) & 1)) ok = false;
         if (!ok) break;
         if (lane == 0) {
           tc_fence_after();
@@ -273,7 +270,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint16_t* qrow = p.q + ((int64_t(b) * p.T + (live ? t : 0)) * p.Hq + hq) * kHeadDim;
     uint8_t* qtile = sQ + x * kQBytes;
-    uint8_t* prow0 = sP + 2 * x * kPBytes + r * 128;   // P buffer bb of this row: + bb * kPBytes
     const int pos = p.qpos0[b] + t;
     const float scale = p.scale_log2;
     float m = -CUDART_INF_F, l = 0.f;
@@ -329,9 +325,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
       tmem_ld32(lane_addr + s_col(x, bb), sa);
       tmem_ld32(lane_addr + s_col(x, bb) + 32, sb);
       tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.sfree[x][bb]);
       const int valid = pi.valid;
       float v[64];
 #pragma unroll
@@ -383,12 +376,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
           m = m_page;
         }
       }
-      // P buffer bb is free once the PV that read it two pages ago has completed
-      if (j >= 2 && !warp_wait(&S.pvdone[x][bb], ((j - 2) >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      uint8_t* prow = prow0 + bb * kPBytes;
       // p = 2^(s * scale - m), zero past the valid columns (and everywhere while m is -inf)
       const bool full = valid == 64 && m != -CUDART_INF_F;
       const float mneg = m != -CUDART_INF_F ? -m : 0.f;
@@ -404,15 +391,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
       for (int c = 0; c < 64; ++c) ls8[c & 7] += v[c];
       const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+      // P row (bf16 pairs) over the first half of this S buffer: the A operand of the PV MMA
+      uint32_t pw[32];
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        const uint4 w4 = make_uint4(pack_bf16x2(v[8 * cc], v[8 * cc + 1]), pack_bf16x2(v[8 * cc + 2], v[8 * cc + 3]),
-                                    pack_bf16x2(v[8 * cc + 4], v[8 * cc + 5]),
-                                    pack_bf16x2(v[8 * cc + 6], v[8 * cc + 7]));
-        *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) = w4;
-      }
+      for (int c = 0; c < 32; ++c) pw[c] = pack_bf16x2(v[2 * c], v[2 * c + 1]);
+      tmem_st32(lane_addr + s_col(x, bb), pw);
       l += lsum;
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.pready[x][bb]);

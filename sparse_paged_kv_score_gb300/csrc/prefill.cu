@@ -12,22 +12,25 @@
 // TMA wrote them).  Both give the same scores.
 //
 // One CTA per (request b, kv head h, pair of query heads of its group, tile of 128 query
-// rows): the two query heads are two 128-row tiles that share every K/V page, so each page
-// feeds twice the tensor-core work and two softmax warpgroups take turns (ten warps):
-//   warp 0     TMA producer: K and V of each page (two 64 x 64 bf16 boxes each, 128-byte
-//              swizzle) into a 5-stage ring, and L2 prefetches of the pages 8 beyond it;
-//   warp 1     MMA issuer (one thread): per tile x, S_x = Q_x K_j^T into one of two TMEM S
-//              buffers (M 128, N 64), then O_x += P_x V_(j-1) (M 128, N 128) with P read from
-//              tensor memory and V from shared memory (MN-major);
-//              it also zeroes the V rows of a partial page so that P = 0 never meets garbage;
+// rows): the two query heads are two 128-row tiles that share every K/V page.  Consecutive pages
+// of one document are taken in groups of two, so that a QK^T product is one N = 128 MMA tile.
+// Ten warps:
+//   warp 0     TMA producer: K and V of the group's pages (64 x 64 bf16 boxes, 128-byte swizzle;
+//              the two pages' rows stacked so each d-half is one 128-row tile) into a 2-stage
+//              ring, and L2 prefetches of the pages beyond it;
+//   warp 1     MMA issuer (one thread), per tile x in turn: O_x += P_x V_(g-1) (M 128, N 128,
+//              P read from tensor memory, V from shared memory as an MN-major operand), then
+//              S_x = Q_x K_g^T (M 128, N 64 or 128) into the same tensor-memory columns -- MMAs
+//              of one thread execute in issue order, so the PV has read P before the QK writes
+//              S; it also zeroes the V rows of a partial page so that P = 0 never meets garbage;
 //   warps 2-5, 6-9  softmax of tile 0 and tile 1: thread r owns query row r (TMEM lane r):
 //              it rotates its query row on document switches, reads its S row from TMEM,
 //              runs the online softmax in the log2 domain, writes its P row (bf16 pairs) back
-//              over its S row in tensor memory as the A operand of the PV MMA (so P never
-//              crosses shared memory), and rescales its O row in TMEM only when the row
-//              maximum has grown by more than 2^8 since the last rescale; at the end it
-//              normalises O and writes out and lse.
-// Tensor memory holds all 512 columns: O of both tiles and two S buffers per tile.
+//              over its S row as the A operand of the next PV MMA, and rescales its O row in
+//              TMEM only when the row maximum has grown by more than 2^8 since the last
+//              rescale; at the end it normalises O and writes out and lse.  While one tile's
+//              warps run their softmax, the tensor cores work on the other tile.
+// Tensor memory holds all 512 columns: O of both tiles and one S/P buffer of 128 per tile.
 // Hand-offs are mbarriers; every wait is bounded (SPKV_DEVERR_TIMEOUT), and the MMA issuer
 // drains its MMAs before TMEM is released.
 #include <math_constants.h>
@@ -41,28 +44,29 @@ namespace {
 
 constexpr int kPM = 128;                      // query rows per tile (TMEM lanes)
 constexpr int kTiles = 2;                     // query heads (tiles) per CTA
-constexpr int kPStages = 5;                   // K/V page ring
-constexpr int kPrefetch = 8;                  // pages ahead of the ring that are fetched into L2
+constexpr int kStages = 2;                    // page-group ring
+constexpr int kPrefetch = 8;                  // pages beyond the ring fetched into L2
 constexpr int kPThreads = 64 + kTiles * 128;
-constexpr int kBox = 64 * 128;                // one 64 x 64 bf16 box, bytes
-constexpr int kPStageBytes = 4 * kBox;        // K (2 boxes) + V (2 boxes) of one page-head
-constexpr int kQBytes = 2 * kPM * 128;        // Q tile: two boxes of 128 rows x 128 B
-constexpr uint32_t kTmemCols = 512;           // O of tile x: 128 x .. ; S / P buffers from column 256
+constexpr int kBox = 64 * 128;                // one page's 64 rows x 128 B (one d-half), bytes
+constexpr int kGBox = 2 * kBox;               // the group's rows of one d-half
+constexpr int kStageBytes = 4 * kGBox;        // K half 0, K half 1, V half 0, V half 1
+constexpr int kQBytes = 2 * kPM * 128;        // Q tile: two d-halves of 128 rows x 128 B
+constexpr uint32_t kTmemCols = 512;           // O of tile x at 128 x; S / P of tile x at 256 + 128 x
 constexpr float kRescaleLog2 = 8.f;           // row-max growth (log2) tolerated before O is rescaled
 constexpr float kLn2 = 0.69314718055994530942f;
 
 __host__ __device__ constexpr uint32_t o_col(int x) { return 128u * x; }
-__host__ __device__ constexpr uint32_t s_col(int x, int bb) { return 256u + 128u * x + 64u * bb; }
+__host__ __device__ constexpr uint32_t s_col(int x) { return 256u + 128u * x; }
 
 struct PrefillSmem {
-  uint64_t full[kPStages], empty[kPStages];
-  uint64_t sfull[kTiles][2], pready[kTiles][2], pvdone[kTiles][2], qready[kTiles];
+  uint64_t full[kStages], empty[kStages];
+  uint64_t sfull[kTiles], pready[kTiles], pvdone[kTiles], qready[kTiles];
   uint64_t drain;
   uint32_t tmem_base;
 };
 
 constexpr size_t kPrefillSmem =
-    1024 + size_t(kTiles) * kQBytes + size_t(kPStages) * kPStageBytes + sizeof(PrefillSmem);
+    1024 + size_t(kTiles) * kQBytes + size_t(kStages) * kStageBytes + sizeof(PrefillSmem);
 static_assert(kPrefillSmem <= 232448, "prefill shared memory exceeds the per-CTA limit");
 
 struct PageInfo {
@@ -84,6 +88,27 @@ __device__ __forceinline__ PageInfo page_info(const PrefillParams& p, int b, int
   return r;
 }
 
+// Page j and, when it exists and belongs to the same document, page j + 1.
+struct Group {
+  PageInfo a, b;
+  int size;
+};
+
+__device__ __forceinline__ Group group_at(const PrefillParams& p, int b, int h, int j, int n) {
+  Group g;
+  g.a = page_info(p, b, h, j);
+  g.size = 1;
+  g.b.phys = g.b.valid = g.b.slot = 0;
+  if (j + 1 < n) {
+    const PageInfo nb = page_info(p, b, h, j + 1);
+    if (nb.slot == g.a.slot) {
+      g.b = nb;
+      g.size = 2;
+    }
+  }
+  return g;
+}
+
 // Bounded wait with one outcome for the whole warp.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
@@ -102,7 +127,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;                            // tile x at x * kQBytes
   uint8_t* stages = base + kTiles * kQBytes;
-  PrefillSmem& S = *reinterpret_cast<PrefillSmem*>(stages + kPStages * kPStageBytes);
+  PrefillSmem& S = *reinterpret_cast<PrefillSmem*>(stages + kStages * kStageBytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int mt = blockIdx.x, b = blockIdx.z;
   const int pairs = (p.G + 1) / 2;
@@ -110,16 +135,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const int n_tiles = min(kTiles, h * p.G + p.G - hq0);   // the last pair of an odd group has one head
 
   if (tid == 0) {
-    for (int s = 0; s < kPStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&S.full[s], 1);
       mbar_init(&S.empty[s], 1);
     }
     for (int x = 0; x < kTiles; ++x) {
-      for (int i = 0; i < 2; ++i) {
-        mbar_init(&S.sfull[x][i], 1);
-        mbar_init(&S.pready[x][i], 4);
-        mbar_init(&S.pvdone[x][i], 1);
-      }
+      mbar_init(&S.sfull[x], 1);
+      mbar_init(&S.pready[x], 4);
+      mbar_init(&S.pvdone[x], 1);
       mbar_init(&S.qready[x], 4);
     }
     mbar_init(&S.drain, 1);
@@ -141,8 +164,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
   if (warp == 0) {
     // ================================================================ TMA producer
     const uint64_t pol = l2_policy_evict_last();   // the group's other query heads and other requests reuse pages
-    // A stage is held until the PV of its page completes, so the ring alone runs only a page or
-    // two ahead of the MMAs; pages further ahead are fetched into L2 so that their loads hit.
     auto prefetch = [&](int jj) {
       const PageInfo pi = page_info(p, b, h, jj);
       if (pi.valid == 0) return;
@@ -152,108 +173,128 @@ __global__ void __launch_bounds__(kPThreads, 1)
       tma_prefetch_l2_3d(&tmv, 0, 0, z);
       tma_prefetch_l2_3d(&tmv, 64, 0, z);
     };
-    if (lane == 0)
-      for (int jj = kPStages; jj < min(n, kPStages + kPrefetch); ++jj) prefetch(jj);
-    int j = 0;
-    for (; j < n; ++j) {
-      const int s = j % kPStages;
-      if (lane == 0 && j + kPStages + kPrefetch < n) prefetch(j + kPStages + kPrefetch);
-      if (j >= kPStages && !warp_wait(&S.empty[s], ((j / kPStages) - 1) & 1)) {
+    auto load_page = [&](uint8_t* st, int half_off, const PageInfo& pi, uint64_t* bar) {
+      const int z = static_cast<int>(int64_t(h) * p.n_phys + pi.phys);
+      tma_load_3d(st + half_off, &tmk, bar, 0, 0, z, pol);
+      tma_load_3d(st + kGBox + half_off, &tmk, bar, 64, 0, z, pol);
+      tma_load_3d(st + 2 * kGBox + half_off, &tmv, bar, 0, 0, z, pol);
+      tma_load_3d(st + 3 * kGBox + half_off, &tmv, bar, 64, 0, z, pol);
+    };
+    if (lane == 0) {
+      for (int jj = 0; jj < n; ++jj) {   // flag malformed page words once
+        const int mh = p.meta_heads == 1 ? 0 : h;
+        const uint32_t w = p.meta[(int64_t(b) * p.meta_heads + mh) * p.np_max + jj];
+        if (static_cast<int64_t>(w & 0x3FFFFu) >= p.n_phys) flag_error(p.err, SPKV_DEVERR_PHYS);
+        else if (static_cast<int>(w >> 24) >= p.max_docs) flag_error(p.err, SPKV_DEVERR_SLOT);
+      }
+      for (int jj = 2 * kStages; jj < min(n, 2 * kStages + kPrefetch); ++jj) prefetch(jj);
+    }
+    int g = 0, j = 0;
+    for (; j < n; ++g) {
+      const Group gr = group_at(p, b, h, j, n);
+      const int s = g % kStages;
+      if (g >= kStages && !warp_wait(&S.empty[s], ((g / kStages) - 1) & 1)) {
         if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
         break;
       }
       if (lane == 0) {
-        const int mh = p.meta_heads == 1 ? 0 : h;
-        const uint32_t w = p.meta[(int64_t(b) * p.meta_heads + mh) * p.np_max + j];
-        if (static_cast<int64_t>(w & 0x3FFFFu) >= p.n_phys) flag_error(p.err, SPKV_DEVERR_PHYS);
-        else if (static_cast<int>(w >> 24) >= p.max_docs) flag_error(p.err, SPKV_DEVERR_SLOT);
-        const PageInfo pi = page_info(p, b, h, j);
-        if (pi.valid > 0) {
-          mbar_arrive_expect_tx(&S.full[s], kPStageBytes);
-          uint8_t* dst = stages + s * kPStageBytes;
-          const int z = static_cast<int>(int64_t(h) * p.n_phys + pi.phys);
-          tma_load_3d(dst, &tmk, &S.full[s], 0, 0, z, pol);
-          tma_load_3d(dst + kBox, &tmk, &S.full[s], 64, 0, z, pol);
-          tma_load_3d(dst + 2 * kBox, &tmv, &S.full[s], 0, 0, z, pol);
-          tma_load_3d(dst + 3 * kBox, &tmv, &S.full[s], 64, 0, z, pol);
+        for (int jj = j + 2 * kStages + kPrefetch; jj < min(n, j + gr.size + 2 * kStages + kPrefetch); ++jj)
+          prefetch(jj);
+        uint8_t* st = stages + s * kStageBytes;
+        const uint32_t bytes = (gr.a.valid > 0 ? 4 * kBox : 0) + (gr.size == 2 && gr.b.valid > 0 ? 4 * kBox : 0);
+        if (bytes) {
+          mbar_arrive_expect_tx(&S.full[s], bytes);
+          if (gr.a.valid > 0) load_page(st, 0, gr.a, &S.full[s]);
+          if (gr.size == 2 && gr.b.valid > 0) load_page(st, kBox, gr.b, &S.full[s]);
         } else {
           mbar_arrive(&S.full[s]);
         }
       }
       __syncwarp();
+      j += gr.size;
     }
     // no copy of this CTA may still be in flight when it exits
-    for (int i = j > kPStages ? j - kPStages : 0; i < j; ++i) mbar_wait(&S.full[i % kPStages], (i / kPStages) & 1);
+    for (int i = g > kStages ? g - kStages : 0; i < g; ++i) mbar_wait(&S.full[i % kStages], (i / kStages) & 1);
   } else if (warp == 1) {
     // ================================================================ MMA issuer
-    constexpr uint32_t kIdS = umma_idesc_bf16(kPM, 64, false);
+    constexpr uint32_t kIdS64 = umma_idesc_bf16(kPM, 64, false);
+    constexpr uint32_t kIdS128 = umma_idesc_bf16(kPM, 128, false);
     constexpr uint32_t kIdO = umma_idesc_bf16(kPM, 128, true);
-    bool ok = true;
     // Operand descriptors are formed once; a k step adds its byte offset / 16 to the start
     // address field (every address here is below 256 KiB, so the field never overflows).
     const uint64_t q_desc = umma_desc_sw128(smem_u32(sQ), 16, 1024);
     const uint64_t k_desc = umma_desc_sw128(smem_u32(stages), 16, 1024);
-    const uint64_t v_desc = umma_desc_sw128(smem_u32(stages + 2 * kBox), 8192, 1024);
-    // O_x += P_x V_jj for every tile, then the page's stage is released
-    auto issue_pv = [&](int jj) -> bool {
-      const int pb = jj & 1;
-      for (int x = 0; x < n_tiles; ++x) {
-        if (!warp_wait(&S.pready[x][pb], (jj >> 1) & 1)) return false;
-        if (lane == 0) {
-          tc_fence_after();
-          const uint64_t va = v_desc + (((jj % kPStages) * kPStageBytes) >> 4);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)   // P (bf16 pairs) sits in the first 32 columns of its S buffer
-            umma_bf16_tmem_a(tbase + o_col(x), tbase + s_col(x, pb) + 8 * k, va + 128 * k, kIdO, jj > 0 || k > 0);
-          umma_commit(&S.pvdone[x][pb]);
-        }
-        __syncwarp();
+    const uint64_t v_desc = umma_desc_sw128(smem_u32(stages + 2 * kGBox), kGBox, 1024);
+    bool ok = true;
+    int prev_slot = -1, n_docs = 0, prev_size = 0, g = 0;
+    // O_x += P_x V of group gg (size sz): P in the first 32 sz columns of S_x
+    auto issue_pv = [&](int x, int gg, int sz) -> bool {
+      if (!warp_wait(&S.pready[x], gg & 1)) return false;
+      if (lane == 0) {
+        tc_fence_after();
+        const uint64_t va = v_desc + (((gg % kStages) * kStageBytes) >> 4);
+        for (int k = 0; k < 4 * sz; ++k)
+          umma_bf16_tmem_a(tbase + o_col(x), tbase + s_col(x) + 8 * k, va + 128 * k, kIdO, gg > 0 || k > 0);
+        umma_commit(&S.pvdone[x]);
       }
-      if (lane == 0) umma_commit(&S.empty[jj % kPStages]);
       __syncwarp();
       return true;
     };
-    int prev_slot = -1, n_docs = 0;
-    for (int j = 0; j < n && ok; ++j) {
-      const int s = j % kPStages, bb = j & 1;
-      const PageInfo pi = page_info(p, b, h, j);
-      if (!warp_wait(&S.full[s], (j / kPStages) & 1)) {
+    for (int j = 0; j < n && ok; ++g) {
+      const Group gr = group_at(p, b, h, j, n);
+      const int s = g % kStages;
+      if (!warp_wait(&S.full[s], (g / kStages) & 1)) {
         ok = false;
         break;
       }
-      if (pi.valid < 64) {
-        // rows past the valid tokens are multiplied by P = 0: make them exact zeros
-        uint8_t* vt = stages + s * kPStageBytes + 2 * kBox;
-        for (int i = lane; i < (64 - pi.valid) * 16; i += 32) {
-          const int row = pi.valid + (i >> 4), c = i & 15;
-          *reinterpret_cast<uint4*>(vt + (c >> 3) * kBox + row * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+      // rows past a page's valid tokens are multiplied by P = 0: make them exact zeros
+      for (int pg = 0; pg < gr.size; ++pg) {
+        const int valid = pg == 0 ? gr.a.valid : gr.b.valid;
+        if (valid == 64) continue;
+        uint8_t* vt = stages + s * kStageBytes + 2 * kGBox + pg * kBox;
+        for (int i = lane; i < (64 - valid) * 16; i += 32) {
+          const int row = valid + (i >> 4), c = i & 15;
+          *reinterpret_cast<uint4*>(vt + (c >> 3) * kGBox + row * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
-        fence_proxy_async_smem();
-        __syncwarp();
       }
-      const bool new_doc = pi.slot != prev_slot;
-      prev_slot = pi.slot;
+      fence_proxy_async_smem();
+      __syncwarp();
+      const bool new_doc = gr.a.slot != prev_slot;
+      prev_slot = gr.a.slot;
       for (int x = 0; x < n_tiles && ok; ++x) {
-        // S buffer bb held P of page j - 2: free once that PV has completed
-        if (new_doc && !warp_wait(&S.qready[x], n_docs & 1)) ok = false;
-        else if (j >= 2 && !warp_wait(&S.pvdone[x][bb], ((j - 2) >> 1) & 1)) ok = false;
-        if (!ok) break;
+        // PV of the previous group reads P_x from the columns the QK below overwrites; MMAs of
+        // one thread run in issue order
+        if (g >= 1 && !issue_pv(x, g - 1, prev_size)) {
+          ok = false;
+          break;
+        }
+        if (new_doc && !warp_wait(&S.qready[x], n_docs & 1)) {
+          ok = false;
+          break;
+        }
         if (lane == 0) {
           tc_fence_after();
-          const uint64_t qa = q_desc + ((x * kQBytes) >> 4), ka = k_desc + ((s * kPStageBytes) >> 4);
+          const uint64_t qa = q_desc + ((x * kQBytes) >> 4), ka = k_desc + ((s * kStageBytes) >> 4);
+          const uint32_t id = gr.size == 2 ? kIdS128 : kIdS64;
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            umma_bf16(tbase + s_col(x, bb), qa + (((k >> 2) * (kPM * 128) + (k & 3) * 32) >> 4),
-                      ka + (((k >> 2) * kBox + (k & 3) * 32) >> 4), kIdS, k > 0);
-          umma_commit(&S.sfull[x][bb]);
+            umma_bf16(tbase + s_col(x), qa + (((k >> 2) * (kPM * 128) + (k & 3) * 32) >> 4),
+                      ka + (((k >> 2) * kGBox + (k & 3) * 32) >> 4), id, k > 0);
+          umma_commit(&S.sfull[x]);
         }
         __syncwarp();
       }
       if (!ok) break;
+      if (g >= 1 && lane == 0) umma_commit(&S.empty[(g - 1) % kStages]);   // group g - 1 fully consumed
+      __syncwarp();
       if (new_doc) ++n_docs;
-      if (j >= 1 && !(ok = issue_pv(j - 1))) break;
+      prev_size = gr.size;
+      j += gr.size;
     }
-    if (ok && n > 0) ok = issue_pv(n - 1);
+    if (ok && g > 0) {
+      for (int x = 0; x < n_tiles && ok; ++x) ok = issue_pv(x, g - 1, prev_size);
+      if (ok && lane == 0) umma_commit(&S.empty[(g - 1) % kStages]);
+    }
     if (!ok && lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
     // every MMA issued has completed before TMEM is released
     if (lane == 0) umma_commit(&S.drain);
@@ -273,17 +314,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int pos = p.qpos0[b] + t;
     const float scale = p.scale_log2;
     float m = -CUDART_INF_F, l = 0.f;
-    int prev_slot = -1;
+    int prev_slot = -1, g = 0;
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      const int bb = j & 1;
-      const PageInfo pi = page_info(p, b, h, j);
-      if (pi.slot != prev_slot) {
+    for (int j = 0; j < n; ++g) {
+      const Group gr = group_at(p, b, h, j, n);
+      j += gr.size;
+      if (gr.a.slot != prev_slot) {
         // Document switch: every MMA that read the previous rotation has completed (its S
         // row was read in the previous iteration), so row r of Q is rewritten as
         // R(pos - doc_pos[slot]) q in bf16.
-        prev_slot = pi.slot;
-        const int rel = pos - p.doc_pos[int64_t(b) * p.max_docs + pi.slot];
+        prev_slot = gr.a.slot;
+        const int rel = pos - p.doc_pos[int64_t(b) * p.max_docs + gr.a.slot];
 #pragma unroll 1
         for (int cc = 0; cc < 8; ++cc) {
           uint4 xa = make_uint4(0, 0, 0, 0), ya = make_uint4(0, 0, 0, 0);
@@ -316,47 +357,53 @@ __global__ void __launch_bounds__(kPThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.qready[x]);
       }
-      if (!warp_wait(&S.sfull[x][bb], (j >> 1) & 1)) {
+      if (!warp_wait(&S.sfull[x], g & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sa[32], sb[32];   // S columns 0..31 and 32..63 of this row
-      tmem_ld32(lane_addr + s_col(x, bb), sa);
-      tmem_ld32(lane_addr + s_col(x, bb) + 32, sb);
-      tmem_wait_ld();
-      const int valid = pi.valid;
-      float v[64];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        v[c] = __uint_as_float(sa[c]);
-        v[c + 32] = __uint_as_float(sb[c]);
+      // S columns: page a in 0..63, page b in 64..127 (a group of one page fills only the first
+      // 64); kept as raw bits in four 32-column register blocks, overwritten by p in place
+      uint32_t s0[32], s1[32], s2[32], s3[32];
+      tmem_ld32(lane_addr + s_col(x), s0);
+      tmem_ld32(lane_addr + s_col(x) + 32, s1);
+      if (gr.size == 2) {
+        tmem_ld32(lane_addr + s_col(x) + 64, s2);
+        tmem_ld32(lane_addr + s_col(x) + 96, s3);
       }
-      // row maximum over the valid columns, eight independent chains
+      tmem_wait_ld();
+      const int va = gr.a.valid, vb = gr.size == 2 ? gr.b.valid : 0;
+      const bool full = va == 64 && vb == 64;
       float mx8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx8[k] = -CUDART_INF_F;
-      if (valid == 64) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], v[c]);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], c < valid ? v[c] : -CUDART_INF_F);
+      for (int c = 0; c < 32; ++c) {
+        if (full) {
+          mx8[c & 7] = fmaxf(mx8[c & 7], fmaxf(__uint_as_float(s0[c]), __uint_as_float(s1[c])));
+          mx8[c & 7] = fmaxf(mx8[c & 7], fmaxf(__uint_as_float(s2[c]), __uint_as_float(s3[c])));
+        } else {
+          mx8[c & 7] = fmaxf(mx8[c & 7], c < va ? __uint_as_float(s0[c]) : -CUDART_INF_F);
+          mx8[c & 7] = fmaxf(mx8[c & 7], c + 32 < va ? __uint_as_float(s1[c]) : -CUDART_INF_F);
+          mx8[c & 7] = fmaxf(mx8[c & 7], c < vb ? __uint_as_float(s2[c]) : -CUDART_INF_F);
+          mx8[c & 7] = fmaxf(mx8[c & 7], c + 32 < vb ? __uint_as_float(s3[c]) : -CUDART_INF_F);
+        }
       }
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float m_page = mx * scale;
+      const float m_grp = mx * scale;
       bool rescale = false;
       float alpha = 1.f;
       if (m == -CUDART_INF_F) {
-        m = m_page;   // nothing accumulated yet (O holds zeros or nothing)
-      } else if (m_page > m + kRescaleLog2) {
+        m = m_grp;   // nothing accumulated yet (O holds zeros or nothing)
+      } else if (m_grp > m + kRescaleLog2) {
         rescale = true;
-        alpha = fast_exp2(m - m_page);
+        alpha = fast_exp2(m - m_grp);
       }
       if (__any_sync(0xffffffffu, rescale)) {
-        // O must hold every PV issued so far before it is scaled
-        if (!warp_wait(&S.pvdone[x][(j - 1) & 1], ((j - 1) >> 1) & 1)) {
+        // O holds every PV issued before this group's QK (issue order): they have completed
+        // once S arrived, but wait for the previous group's PV explicitly
+        if (!warp_wait(&S.pvdone[x], (g - 1) & 1)) {
           ok = false;
           break;
         }
@@ -373,57 +420,76 @@ __global__ void __launch_bounds__(kPThreads, 1)
         tmem_wait_st();
         if (rescale) {
           l *= alpha;
-          m = m_page;
+          m = m_grp;
         }
       }
       // p = 2^(s * scale - m), zero past the valid columns (and everywhere while m is -inf)
-      const bool full = valid == 64 && m != -CUDART_INF_F;
-      const float mneg = m != -CUDART_INF_F ? -m : 0.f;
-      const int lim = m != -CUDART_INF_F ? valid : 0;
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float e = fast_exp2(fmaf(v[c], scale, mneg));
-        v[c] = full ? e : (c < lim ? e : 0.f);
-      }
+      const bool have_m = m != -CUDART_INF_F;
+      const float mneg = have_m ? -m : 0.f;
       float ls8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) ls8[k] = 0.f;
+      auto exp_block = [&](uint32_t (&sv)[32], int c0, int vlim) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c) ls8[c & 7] += v[c];
-      const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
-      // P row (bf16 pairs) over the first half of this S buffer: the A operand of the PV MMA
-      uint32_t pw[32];
+        for (int c = 0; c < 32; ++c) {
+          const float e = fast_exp2(fmaf(__uint_as_float(sv[c]), scale, mneg));
+          const float pv = (have_m && (full || c0 + c < vlim)) ? e : 0.f;
+          ls8[c & 7] += pv;
+          sv[c] = __float_as_uint(pv);
+        }
+      };
+      exp_block(s0, 0, va);
+      exp_block(s1, 32, va);
+      if (gr.size == 2) {
+        exp_block(s2, 0, vb);
+        exp_block(s3, 32, vb);
+      }
+      l += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+      // P row (bf16 pairs) over the first half of this S row: the A operand of the PV MMA
+      {
+        uint32_t pw[32];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) pw[c] = pack_bf16x2(v[2 * c], v[2 * c + 1]);
-      tmem_st32(lane_addr + s_col(x, bb), pw);
-      l += lsum;
+        for (int c = 0; c < 16; ++c) {
+          pw[c] = pack_bf16x2(__uint_as_float(s0[2 * c]), __uint_as_float(s0[2 * c + 1]));
+          pw[16 + c] = pack_bf16x2(__uint_as_float(s1[2 * c]), __uint_as_float(s1[2 * c + 1]));
+        }
+        tmem_st32(lane_addr + s_col(x), pw);
+        if (gr.size == 2) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            pw[c] = pack_bf16x2(__uint_as_float(s2[2 * c]), __uint_as_float(s2[2 * c + 1]));
+            pw[16 + c] = pack_bf16x2(__uint_as_float(s3[2 * c]), __uint_as_float(s3[2 * c + 1]));
+          }
+          tmem_st32(lane_addr + s_col(x) + 32, pw);
+        }
+      }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.pready[x][bb]);
+      if (lane == 0) mbar_arrive(&S.pready[x]);
     }
-    if (ok && n > 0) ok = warp_wait(&S.pvdone[x][(n - 1) & 1], ((n - 1) >> 1) & 1);
+    if (ok && g > 0) ok = warp_wait(&S.pvdone[x], (g - 1) & 1);
     if (!ok && lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
     tc_fence_after();
     float* orow = p.out + ((int64_t(b) * p.T + (live ? t : 0)) * p.Hq + hq) * kHeadDim;
-    const bool have = ok && n > 0 && l > 0.f;
+    const bool have = ok && g > 0 && l > 0.f;
     const float inv_l = have ? 1.f / l : 0.f;
 #pragma unroll 1
     for (int cb = 0; cb < 128; cb += 32) {
       uint32_t o[32] = {};
-      if (ok && n > 0) {   // TMEM holds O only once a PV has run
+      if (ok && g > 0) {   // TMEM holds O only once a PV has run
         tmem_ld32(lane_addr + o_col(x) + cb, o);
         tmem_wait_ld();
       }
       if (live) {
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
-          float4 v;
-          v.x = have ? __uint_as_float(o[c]) * inv_l : 0.f;
-          v.y = have ? __uint_as_float(o[c + 1]) * inv_l : 0.f;
-          v.z = have ? __uint_as_float(o[c + 2]) * inv_l : 0.f;
-          v.w = have ? __uint_as_float(o[c + 3]) * inv_l : 0.f;
-          *reinterpret_cast<float4*>(orow + cb + c) = v;
+          float4 w;
+          w.x = have ? __uint_as_float(o[c]) * inv_l : 0.f;
+          w.y = have ? __uint_as_float(o[c + 1]) * inv_l : 0.f;
+          w.z = have ? __uint_as_float(o[c + 2]) * inv_l : 0.f;
+          w.w = have ? __uint_as_float(o[c + 3]) * inv_l : 0.f;
+          *reinterpret_cast<float4*>(orow + cb + c) = w;
         }
       }
     }

@@ -363,31 +363,24 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       tc_fence_after();
       // S columns: page a in 0..63, page b in 64..127 (a group of one page fills only the first
-      // 64); kept as raw bits in four 32-column register blocks, overwritten by p in place
-      uint32_t s0[32], s1[32], s2[32], s3[32];
-      tmem_ld32(lane_addr + s_col(x), s0);
-      tmem_ld32(lane_addr + s_col(x) + 32, s1);
-      if (gr.size == 2) {
-        tmem_ld32(lane_addr + s_col(x) + 64, s2);
-        tmem_ld32(lane_addr + s_col(x) + 96, s3);
-      }
-      tmem_wait_ld();
+      // 64).  Two passes over tensor memory keep 32 columns in registers at a time: the row
+      // maximum first, then p, the row sum and P (bf16 pairs written over the columns already
+      // read: block k's 16 words land on columns 16 k .. 16 k + 15 <= 32 k).
       const int va = gr.a.valid, vb = gr.size == 2 ? gr.b.valid : 0;
       const bool full = va == 64 && vb == 64;
+      const int nblk = 2 * gr.size;
       float mx8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx8[k] = -CUDART_INF_F;
+#pragma unroll 1
+      for (int k = 0; k < nblk; ++k) {
+        uint32_t sv[32];
+        tmem_ld32(lane_addr + s_col(x) + 32 * k, sv);
+        tmem_wait_ld();
+        const int lim = (k < 2 ? va : vb) - 32 * (k & 1);   // valid columns of this block
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        if (full) {
-          mx8[c & 7] = fmaxf(mx8[c & 7], fmaxf(__uint_as_float(s0[c]), __uint_as_float(s1[c])));
-          mx8[c & 7] = fmaxf(mx8[c & 7], fmaxf(__uint_as_float(s2[c]), __uint_as_float(s3[c])));
-        } else {
-          mx8[c & 7] = fmaxf(mx8[c & 7], c < va ? __uint_as_float(s0[c]) : -CUDART_INF_F);
-          mx8[c & 7] = fmaxf(mx8[c & 7], c + 32 < va ? __uint_as_float(s1[c]) : -CUDART_INF_F);
-          mx8[c & 7] = fmaxf(mx8[c & 7], c < vb ? __uint_as_float(s2[c]) : -CUDART_INF_F);
-          mx8[c & 7] = fmaxf(mx8[c & 7], c + 32 < vb ? __uint_as_float(s3[c]) : -CUDART_INF_F);
-        }
+        for (int c = 0; c < 32; ++c)
+          mx8[c & 7] = fmaxf(mx8[c & 7], (full || c < lim) ? __uint_as_float(sv[c]) : -CUDART_INF_F);
       }
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
@@ -429,40 +422,26 @@ __global__ void __launch_bounds__(kPThreads, 1)
       float ls8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) ls8[k] = 0.f;
-      auto exp_block = [&](uint32_t (&sv)[32], int c0, int vlim) {
+#pragma unroll 1
+      for (int k = 0; k < nblk; ++k) {
+        uint32_t sv[32];
+        tmem_ld32(lane_addr + s_col(x) + 32 * k, sv);
+        tmem_wait_ld();
+        const int lim = have_m ? (k < 2 ? va : vb) - 32 * (k & 1) : 0;
+        uint32_t pw[16];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float e = fast_exp2(fmaf(__uint_as_float(sv[c]), scale, mneg));
-          const float pv = (have_m && (full || c0 + c < vlim)) ? e : 0.f;
-          ls8[c & 7] += pv;
-          sv[c] = __float_as_uint(pv);
+        for (int c = 0; c < 32; c += 2) {
+          const float e0 = fast_exp2(fmaf(__uint_as_float(sv[c]), scale, mneg));
+          const float e1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), scale, mneg));
+          const float p0 = (have_m && (full || c < lim)) ? e0 : 0.f;
+          const float p1 = (have_m && (full || c + 1 < lim)) ? e1 : 0.f;
+          ls8[c & 7] += p0;
+          ls8[(c + 1) & 7] += p1;
+          pw[c >> 1] = pack_bf16x2(p0, p1);
         }
-      };
-      exp_block(s0, 0, va);
-      exp_block(s1, 32, va);
-      if (gr.size == 2) {
-        exp_block(s2, 0, vb);
-        exp_block(s3, 32, vb);
+        tmem_st16(lane_addr + s_col(x) + 16 * k, pw);
       }
       l += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
-      // P row (bf16 pairs) over the first half of this S row: the A operand of the PV MMA
-      {
-        uint32_t pw[32];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          pw[c] = pack_bf16x2(__uint_as_float(s0[2 * c]), __uint_as_float(s0[2 * c + 1]));
-          pw[16 + c] = pack_bf16x2(__uint_as_float(s1[2 * c]), __uint_as_float(s1[2 * c + 1]));
-        }
-        tmem_st32(lane_addr + s_col(x), pw);
-        if (gr.size == 2) {
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            pw[c] = pack_bf16x2(__uint_as_float(s2[2 * c]), __uint_as_float(s2[2 * c + 1]));
-            pw[16 + c] = pack_bf16x2(__uint_as_float(s3[2 * c]), __uint_as_float(s3[2 * c + 1]));
-          }
-          tmem_st32(lane_addr + s_col(x) + 32, pw);
-        }
-      }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

@@ -75,7 +75,10 @@ typedef struct spkv_cache* spkv_cache_t; /* opaque, library-owned */
  *   k_pool, v_pool : bf16 [n_kv_heads][n_phys_pages][64][128]; one page of one head is
  *                    16 KiB contiguous ([Spin] 2B "per-head physical pages").  16-byte aligned.
  *   ksum           : fp32 [n_kv_heads][n_phys_pages][4][128]; per page and sub-block, the sum
- *                    of the valid keys (the library writes it; mean = ksum / count).
+ *                    of the valid keys (the library writes it; mean = ksum / count).  With
+ *                    ksum_bf16 = 1 it is bf16 of the same shape instead: the fp32 sum, formed in
+ *                    the same order, rounded once to bf16 (half the bytes for score_blocks to
+ *                    read; [Spin] 2C / cheaper scoring at long context).
  *   page_cnt       : int32 [n_phys_pages]; valid tokens held by each physical page.  Read by
  *                    paged_kv_create, updated by paged_kv_append.
  *   max_units      : the largest B * n_kv_heads any call on this handle will use (sizes the
@@ -92,9 +95,10 @@ typedef struct {
   int64_t n_phys_pages;
   void* k_pool;
   void* v_pool;
-  float* ksum;
+  void* ksum;
   int32_t* page_cnt;
   int32_t max_units;
+  int32_t ksum_bf16;    /* 0: fp32 summaries; 1: bf16 summaries */
 } spkv_desc;
 
 /* Creates a handle for the pool described by *desc (the struct is copied; the buffers are

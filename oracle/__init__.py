@@ -57,6 +57,8 @@ def _l():
             "orc_setdiff_unit": ([vp, i32, vp, i32, i32, vp, vp, vp], None),
             "orc_lru_unit": ([vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, vp, vp], None),
             "orc_score_batch": ([i32, i32, i32, vp, vp, i64, vp, i32, vp, vp, i32, vp, i32], None),
+            "orc_score_batch_ex": ([i32, i32, i32, vp, vp, i64, vp, i32, vp, vp, i32, i32, vp, i32], None),
+            "orc_round_bf16": ([f64], f64),
             "orc_select_batch": ([i32, vp, vp, vp, i32, vp, i32, i32, vp, vp, vp, i32, i32], None),
             "orc_sparse_attn_batch": ([i32, i32, i32, vp, vp, vp, i64, vp, i32, vp, vp, i32, vp, vp,
                                        i32, vp, vp, i32], None),
@@ -197,8 +199,13 @@ def _units(units, n):
     return _c(np.arange(n) if units is None else units, np.int32)
 
 
-def score_batch(q, k_pool, page_table, seq_len, units=None, nthreads: int = 0):
-    """Block scores [B][Hk][np_max] (fp64) for the listed units (others left 0)."""
+def round_bf16(x: float) -> float:
+    return _l().orc_round_bf16(float(x))
+
+
+def score_batch(q, k_pool, page_table, seq_len, units=None, nthreads: int = 0, summary_bf16: bool = False):
+    """Block scores [B][Hk][np_max] (fp64) for the listed units (others left 0); with
+    summary_bf16 the sub-block sums are rounded to bf16 before the means are taken."""
     q, k_pool = _c(q, np.uint16), _c(k_pool, np.uint16)
     page_table, seq_len = _c(page_table, np.int32), _c(seq_len, np.int32)
     B, Hq, _ = q.shape
@@ -206,8 +213,8 @@ def score_batch(q, k_pool, page_table, seq_len, units=None, nthreads: int = 0):
     np_max = page_table.shape[1]
     u = _units(units, B * Hk)
     s = np.zeros((B, Hk, np_max), np.float64)
-    _l().orc_score_batch(B, Hq, Hk, _p(q), _p(k_pool), n_phys, _p(page_table), np_max, _p(seq_len),
-                         _p(u), u.shape[0], _p(s), nthreads)
+    _l().orc_score_batch_ex(B, Hq, Hk, _p(q), _p(k_pool), n_phys, _p(page_table), np_max, _p(seq_len),
+                            _p(u), u.shape[0], int(bool(summary_bf16)), _p(s), nthreads)
     return s
 
 

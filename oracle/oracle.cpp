@@ -126,14 +126,26 @@ void orc_page_means(const uint16_t* page, int valid, double* mean, int32_t* cnt)
   }
 }
 
+// Round to the nearest bf16 (8 significant bits), ties to even: the value's binary significand
+// m in [1/2, 1) is scaled to [128, 256), rounded to an integer by rint (the default rounding
+// mode, nearest-even) and scaled back.  Finite, normal-range inputs.
+double orc_round_bf16(double x) {
+  if (x == 0.0 || !std::isfinite(x)) return x;
+  int e = 0;
+  const double m = std::frexp(x, &e);
+  return std::ldexp(std::rint(std::ldexp(m, 8)), e - 8);
+}
+
 // ---------------------------------------------------------------- A-2 block scores
 // [NOSA] "Block-wise implementation" (two-stage pooling: mean inside sub-blocks, then max to
 // the block) with reading R1 for the GQA group:
 //   s[p] = max_j  sum_g  (q_g . mean_{p,j}) / sqrt(128)
 // for every complete page p before the local page (R2); every other entry is -inf.
 // q: G rows of 128 bf16; kplane: the pool plane of this kv head, [n_phys][64][128].
-void orc_score_unit(const uint16_t* q, int G, const uint16_t* kplane, const int32_t* pt_row,
-                    int seq_len, int np_out, double* s) {
+// With summary_bf16 != 0 the stored summary is the sub-block sum rounded to bf16 (cheaper
+// scoring at long context, [Spin] 2C): mean = round_bf16(sum) / count.
+void orc_score_unit_ex(const uint16_t* q, int G, const uint16_t* kplane, const int32_t* pt_row,
+                       int seq_len, int np_out, int summary_bf16, double* s) {
   const int local = (seq_len - 1) / kPage;
   std::vector<double> mean(kNSub * kD);
   int32_t cnt[kNSub];
@@ -141,6 +153,10 @@ void orc_score_unit(const uint16_t* q, int G, const uint16_t* kplane, const int3
   for (int p = 0; p < np_out; ++p) {
     if (p >= local) { s[p] = kNegInf; continue; }
     orc_page_means(row_ptr(kplane, pt_row[p], 0), kPage, mean.data(), cnt);
+    if (summary_bf16)
+      for (int j = 0; j < kNSub; ++j)
+        for (int d = 0; d < kD; ++d)
+          if (cnt[j] > 0) mean[j * kD + d] = orc_round_bf16(mean[j * kD + d] * cnt[j]) / cnt[j];
     double best = kNegInf;
     for (int j = 0; j < kNSub; ++j) {
       double sum_g = 0.0;
@@ -153,6 +169,11 @@ void orc_score_unit(const uint16_t* q, int G, const uint16_t* kplane, const int3
     }
     s[p] = best;
   }
+}
+
+void orc_score_unit(const uint16_t* q, int G, const uint16_t* kplane, const int32_t* pt_row,
+                    int seq_len, int np_out, double* s) {
+  orc_score_unit_ex(q, G, kplane, pt_row, seq_len, np_out, 0, s);
 }
 
 // ---------------------------------------------------------------- A-3 selection
@@ -413,18 +434,24 @@ void orc_retrieve_unit(const uint16_t* khost, const uint16_t* vhost, const int32
 // pool of `nthreads` threads (0 = all hardware threads).  Unit u = b * Hk + h.  Pools are
 // [Hk][n_phys][64][128]; q is [B][Hq][128]; kv head h serves query heads h*G .. h*G+G-1.
 
-void orc_score_batch(int B, int Hq, int Hk, const uint16_t* q, const uint16_t* kpool, int64_t n_phys,
-                     const int32_t* page_table, int np_max, const int32_t* seq_len,
-                     const int32_t* units, int n_units, double* s, int nthreads) {
+void orc_score_batch_ex(int B, int Hq, int Hk, const uint16_t* q, const uint16_t* kpool, int64_t n_phys,
+                        const int32_t* page_table, int np_max, const int32_t* seq_len,
+                        const int32_t* units, int n_units, int summary_bf16, double* s, int nthreads) {
   (void)B;
   const int G = Hq / Hk;
   for_units(n_units, nthreads, [&](int i) {
     const int u = units[i], b = u / Hk, h = u % Hk;
-    orc_score_unit(q + (static_cast<int64_t>(b) * Hq + h * G) * kD, G,
-                   kpool + static_cast<int64_t>(h) * n_phys * kPage * kD,
-                   page_table + static_cast<int64_t>(b) * np_max, seq_len[b], np_max,
-                   s + static_cast<int64_t>(u) * np_max);
+    orc_score_unit_ex(q + (static_cast<int64_t>(b) * Hq + h * G) * kD, G,
+                      kpool + static_cast<int64_t>(h) * n_phys * kPage * kD,
+                      page_table + static_cast<int64_t>(b) * np_max, seq_len[b], np_max, summary_bf16,
+                      s + static_cast<int64_t>(u) * np_max);
   });
+}
+
+void orc_score_batch(int B, int Hq, int Hk, const uint16_t* q, const uint16_t* kpool, int64_t n_phys,
+                     const int32_t* page_table, int np_max, const int32_t* seq_len,
+                     const int32_t* units, int n_units, double* s, int nthreads) {
+  orc_score_batch_ex(B, Hq, Hk, q, kpool, n_phys, page_table, np_max, seq_len, units, n_units, 0, s, nthreads);
 }
 
 void orc_select_batch(int Hk, const double* s, const double* e, uint8_t* alive, int np_max,

@@ -75,7 +75,8 @@ def _host(x: torch.Tensor, dtype, name: str, shape=None) -> int:
 class PagedKVCache:
     """Owns one library handle (``spkv_cache_t``) for a caller-owned pool.
 
-    ``ksum`` and ``page_cnt`` may both be None: a handle without summaries, for a pool of
+    ``ksum`` is fp32, or bf16 for summaries rounded once to bf16 (half the bytes that
+    ``score_blocks`` reads).  ``ksum`` and ``page_cnt`` may both be None: a handle without summaries, for a pool of
     resident slots that is only attended (``retrieve_pages``, ``sparse_decode_attn_slots``)."""
 
     def __init__(self, k_pool, v_pool, ksum, page_cnt, max_units: int = 0, stream=None):
@@ -83,12 +84,14 @@ class PagedKVCache:
         shp = (Hk, n_phys, PAGE, HEAD_DIM)
         if (ksum is None) != (page_cnt is None):
             raise ValueError("ksum and page_cnt are given together or not at all")
+        ksum_bf16 = ksum is not None and ksum.dtype == torch.bfloat16   # bf16 summaries: half the scoring bytes
         self.desc = SpkvDesc(Hk, HEAD_DIM, PAGE, SUBBLOCK, n_phys,
                              _t(k_pool, torch.bfloat16, "k_pool", shp),
                              _t(v_pool, torch.bfloat16, "v_pool", shp),
-                             None if ksum is None else _t(ksum, torch.float32, "ksum", (Hk, n_phys, 4, HEAD_DIM)),
+                             None if ksum is None else _t(ksum, torch.bfloat16 if ksum_bf16 else torch.float32, "ksum",
+                                                          (Hk, n_phys, 4, HEAD_DIM)),
                              None if page_cnt is None else _t(page_cnt, torch.int32, "page_cnt", (n_phys,)),
-                             int(max_units))
+                             int(max_units), int(ksum_bf16))
         self.n_kv_heads, self.n_phys = Hk, n_phys
         self.tensors = (k_pool, v_pool, ksum, page_cnt)   # keep the buffers alive
         h = ctypes.c_void_p()

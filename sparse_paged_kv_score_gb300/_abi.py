@@ -23,7 +23,7 @@ class SpkvDesc(ctypes.Structure):
     _fields_ = [("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("page_tokens", ctypes.c_int32), ("subblock", ctypes.c_int32),
                 ("n_phys_pages", ctypes.c_int64), ("k_pool", _vp), ("v_pool", _vp),
-                ("ksum", _vp), ("page_cnt", _vp), ("max_units", ctypes.c_int32)]
+                ("ksum", _vp), ("page_cnt", _vp), ("max_units", ctypes.c_int32), ("ksum_bf16", ctypes.c_int32)]
 
 
 SIGNATURES = {

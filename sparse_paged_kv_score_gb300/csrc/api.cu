@@ -113,6 +113,7 @@ int paged_kv_create(const spkv_desc* desc, void* stream, spkv_cache_t* out) {
   if (d.head_dim != 128 || d.page_tokens != 64 || d.subblock != 16) return SPKV_EUNSUPPORTED;
   if (d.n_kv_heads <= 0 || d.n_phys_pages <= 0 || d.max_units < 0 || d.max_units > 4096) return SPKV_EINVAL;
   if (!d.k_pool || !d.v_pool || !d.ksum != !d.page_cnt) return SPKV_EINVAL;
+  if (d.ksum_bf16 != 0 && d.ksum_bf16 != 1) return SPKV_EINVAL;
   if (!aligned(d.k_pool, 16) || !aligned(d.v_pool, 16) || !aligned(d.ksum, 16)) return SPKV_EINVAL;
   const int64_t n_ph = int64_t(d.n_kv_heads) * d.n_phys_pages;
   if (n_ph >= (int64_t(1) << 31)) return SPKV_EUNSUPPORTED;

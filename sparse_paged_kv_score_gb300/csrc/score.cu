@@ -5,7 +5,8 @@
 // query-aware selection Gamma_q.  For unit (b, h) and a complete page p before the local page:
 //   s = max_j (sum_g q_g) . ksum[h][phys(p)][j] / (16 sqrt(128))
 // The group's sub-block scores are summed before the max; by linearity the kernel forms the
-// summed query once.  This pass is bound by HBM: it reads 2 KiB of fp32 summary per page-head.
+// summed query once.  This pass is bound by HBM: it reads 2 KiB of fp32 summary per page-head
+// (1 KiB with bf16 summaries: [Spin] 2C, cheaper scoring at long context).
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -14,8 +15,19 @@
 namespace spkv {
 namespace {
 
-constexpr int kPagesPerBlock = 64;
 constexpr int kWarps = 8;
+constexpr int kPagesPerWarp = 16;                         // load rounds of four (fp32) or eight (bf16) pages
+constexpr int kPagesPerBlock = kWarps * kPagesPerWarp;    // 128: a 512-page context is 4 CTAs per unit
+
+// Lane l's four summary values of sub-block row `row` (dims 4 l .. 4 l + 3), as fp32.
+template <bool BF16>
+__device__ __forceinline__ float4 load4(const void* ksum, int64_t row, int lane) {
+  if (BF16) {
+    const uint2 w = __ldcs(reinterpret_cast<const uint2*>(ksum) + row * (kHeadDim / 4) + lane);
+    return make_float4(bf16lo_to_f32(w.x), bf16hi_to_f32(w.x), bf16lo_to_f32(w.y), bf16hi_to_f32(w.y));
+  }
+  return __ldcs(reinterpret_cast<const float4*>(ksum) + row * (kHeadDim / 4) + lane);
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -23,8 +35,9 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+template <bool BF16>
 __global__ void __launch_bounds__(kWarps * 32)
-    score_kernel(const uint32_t* __restrict__ q, const float* __restrict__ ksum, const int32_t* __restrict__ page_table,
+    score_kernel(const uint32_t* __restrict__ q, const void* __restrict__ ksum, const int32_t* __restrict__ page_table,
                  const int32_t* __restrict__ seq_len, float* __restrict__ scores, int Hq, int Hk, int G, int np_max,
                  int64_t n_phys, float scale, uint32_t* err) {
   pdl_wait();
@@ -33,12 +46,14 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int p_begin = blockIdx.x * kPagesPerBlock;
   const int p_end = min(np_max, p_begin + kPagesPerBlock);
-  // Each warp owns 8 consecutive pages: one load round for their physical ids (lanes 0..7,
-  // issued before the query sum so both latencies overlap), then two rounds of 4 pages x 4
-  // sub-blocks = 16 independent 16-byte loads per lane.
-  const int pw0 = p_begin + warp * 8;
+  // Each warp owns 16 consecutive pages: one load round for their physical ids (lanes 0..15,
+  // issued before the query sum so both latencies overlap), then rounds of R pages x 4
+  // sub-blocks = 4 R independent loads per lane (R = 4 fp32 pages, 16 bytes each, or 8 bf16
+  // pages, 8 bytes each: 8 KiB in flight per warp either way).
+  constexpr int R = BF16 ? 8 : 4;
+  const int pw0 = p_begin + warp * kPagesPerWarp;
   int ph = 0;
-  if (lane < 8 && pw0 + lane < p_end) ph = page_table[int64_t(b) * np_max + pw0 + lane];
+  if (lane < kPagesPerWarp && pw0 + lane < p_end) ph = page_table[int64_t(b) * np_max + pw0 + lane];
   const int L = seq_len[b];
   __shared__ float qs[kHeadDim];
   if (tid < kHeadDim / 2) {
@@ -55,31 +70,31 @@ __global__ void __launch_bounds__(kWarps * 32)
   const float4 qv = reinterpret_cast<const float4*>(qs)[lane];
   const int local = L >= 1 ? (L - 1) / kPageTokens : 0;
   if (L < 1 && tid == 0 && blockIdx.x == 0) flag_error(err, SPKV_DEVERR_PAGE_ID);
-  const float* plane = ksum + int64_t(h) * n_phys * (kNSub * kHeadDim);
+  const int64_t plane_rows = int64_t(h) * n_phys * kNSub;   // first sub-block row of this head
   float* srow = scores + int64_t(u) * np_max;
   bool okp = false;
-  if (lane < 8 && pw0 + lane < p_end && pw0 + lane < local) {
+  if (lane < kPagesPerWarp && pw0 + lane < p_end && pw0 + lane < local) {
     okp = ph >= 0 && ph < n_phys;
     if (!okp) flag_error(err, SPKV_DEVERR_PHYS);
   }
   if (!okp) ph = 0;
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    float4 v[4][kNSub];
-    bool live[4];
+  for (int half = 0; half < kPagesPerWarp / R; ++half) {
+    float4 v[R][kNSub];
+    bool live[R];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int src = half * 4 + k;
+    for (int k = 0; k < R; ++k) {
+      const int src = half * R + k;
       const int phk = __shfl_sync(0xffffffffu, ph, src);
       live[k] = __shfl_sync(0xffffffffu, okp ? 1 : 0, src) != 0;
-      const float4* base = reinterpret_cast<const float4*>(plane + int64_t(phk) * (kNSub * kHeadDim));
+      const int64_t row0 = plane_rows + int64_t(phk) * kNSub;
 #pragma unroll
       for (int j = 0; j < kNSub; ++j)
-        v[k][j] = live[k] ? __ldcs(base + j * (kHeadDim / 4) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[k][j] = live[k] ? load4<BF16>(ksum, row0 + j, lane) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int pg = pw0 + half * 4 + k;
+    for (int k = 0; k < R; ++k) {
+      const int pg = pw0 + half * R + k;
       float best = -CUDART_INF_F;
 #pragma unroll
       for (int j = 0; j < kNSub; ++j) {
@@ -99,9 +114,9 @@ cudaError_t launch_score(const spkv_cache* c, const void* q, int B, int Hq, cons
   const int G = Hq / Hk;
   dim3 grid((np_max + kPagesPerBlock - 1) / kPagesPerBlock, B * Hk);
   const float scale = static_cast<float>(1.0 / (16.0 * 11.313708498984760390));  // 1 / (16 sqrt(128))
-  return launch_pdl(score_kernel, grid, dim3(kWarps * 32), 0, st, static_cast<const uint32_t*>(q),
-                    static_cast<const float*>(c->d.ksum), page_table, seq_len, scores, Hq, Hk, G, np_max,
-                    static_cast<int64_t>(c->d.n_phys_pages), scale, c->dev_err);
+  return launch_pdl(c->d.ksum_bf16 ? score_kernel<true> : score_kernel<false>, grid, dim3(kWarps * 32), 0, st,
+                    static_cast<const uint32_t*>(q), static_cast<const void*>(c->d.ksum), page_table, seq_len, scores,
+                    Hq, Hk, G, np_max, static_cast<int64_t>(c->d.n_phys_pages), scale, c->dev_err);
 }
 
 }  // namespace spkv

@@ -4,7 +4,8 @@
 // implementation: the selection score pools keys by their mean inside 16-token sub-blocks.
 // [NOSA] section "Method 2: NOSI", kernel fusion: pooling is produced where K is written.
 // We keep the fp32 *sum* of each sub-block's valid keys (mean = sum / count), written in a fixed
-// token order so that a create and any sequence of appends give bitwise the same sums.
+// token order so that a create and any sequence of appends give bitwise the same sums; a handle
+// with bf16 summaries stores that fp32 sum rounded once to bf16 (round to nearest even).
 #include "common.cuh"
 #include "internal.h"
 
@@ -23,8 +24,16 @@ __device__ __forceinline__ float2 subblock_sum(const uint32_t* page_words, int j
   return make_float2(s0, s1);
 }
 
+// Stores the sums of dims 2i, 2i+1 at element pair `pair` of the summary array (fp32 or bf16).
+template <bool BF16>
+__device__ __forceinline__ void store_pair(void* ksum, int64_t pair, float2 v) {
+  if (BF16) reinterpret_cast<uint32_t*>(ksum)[pair] = pack_bf16x2(v.x, v.y);
+  else reinterpret_cast<float2*>(ksum)[pair] = v;
+}
+
 // One group of 64 threads per page-head; thread i owns dims 2i, 2i+1.
-__global__ void __launch_bounds__(256) summary_build_kernel(const uint32_t* __restrict__ kpool, float* __restrict__ ksum,
+template <bool BF16>
+__global__ void __launch_bounds__(256) summary_build_kernel(const uint32_t* __restrict__ kpool, void* __restrict__ ksum,
                                                             const int32_t* __restrict__ page_cnt, int64_t n_ph,
                                                             int64_t n_phys) {
   pdl_wait();
@@ -34,9 +43,9 @@ __global__ void __launch_bounds__(256) summary_build_kernel(const uint32_t* __re
   const int i = threadIdx.x % 64;
   const int cnt = max(0, min(kPageTokens, page_cnt[ph % n_phys]));
   const uint32_t* pw = kpool + ph * (kPageTokens * kHeadDim / 2);
-  float2* out = reinterpret_cast<float2*>(ksum + ph * kNSub * kHeadDim);
 #pragma unroll
-  for (int j = 0; j < kNSub; ++j) out[j * (kHeadDim / 2) + i] = subblock_sum(pw, j, cnt, i);
+  for (int j = 0; j < kNSub; ++j)
+    store_pair<BF16>(ksum, (ph * kNSub + j) * (kHeadDim / 2) + i, subblock_sum(pw, j, cnt, i));
 }
 
 // Writes row r of every head into the pool and raises page_cnt.  One 64-thread group per
@@ -65,7 +74,8 @@ __global__ void __launch_bounds__(256) append_write_kernel(uint32_t* __restrict_
 }
 
 // Recomputes the sub-block sum that row r touched, for every head.
-__global__ void __launch_bounds__(256) append_sum_kernel(const uint32_t* __restrict__ kpool, float* __restrict__ ksum,
+template <bool BF16>
+__global__ void __launch_bounds__(256) append_sum_kernel(const uint32_t* __restrict__ kpool, void* __restrict__ ksum,
                                                          const int32_t* __restrict__ page_cnt,
                                                          const int32_t* __restrict__ phys, const int32_t* __restrict__ tok,
                                                          int n_rows, int Hk, int64_t n_phys) {
@@ -81,7 +91,7 @@ __global__ void __launch_bounds__(256) append_sum_kernel(const uint32_t* __restr
   const int cnt = max(0, min(kPageTokens, page_cnt[p]));
   const int64_t ph = int64_t(h) * n_phys + p;
   const uint32_t* pw = kpool + ph * (kPageTokens * kHeadDim / 2);
-  reinterpret_cast<float2*>(ksum + (ph * kNSub + j) * kHeadDim)[i] = subblock_sum(pw, j, cnt, i);
+  store_pair<BF16>(ksum, (ph * kNSub + j) * (kHeadDim / 2) + i, subblock_sum(pw, j, cnt, i));
 }
 
 }  // namespace
@@ -90,9 +100,9 @@ cudaError_t launch_summary_build(const spkv_cache* c, cudaStream_t st) {
   const int64_t n_ph = int64_t(c->d.n_kv_heads) * c->d.n_phys_pages;
   if (n_ph == 0) return cudaSuccess;
   const int64_t blocks = (n_ph + 3) / 4;
-  return launch_pdl(summary_build_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
-                    static_cast<const uint32_t*>(c->d.k_pool), c->d.ksum, static_cast<const int32_t*>(c->d.page_cnt),
-                    n_ph, static_cast<int64_t>(c->d.n_phys_pages));
+  return launch_pdl(c->d.ksum_bf16 ? summary_build_kernel<true> : summary_build_kernel<false>,
+                    dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, static_cast<const uint32_t*>(c->d.k_pool),
+                    c->d.ksum, static_cast<const int32_t*>(c->d.page_cnt), n_ph, static_cast<int64_t>(c->d.n_phys_pages));
 }
 
 cudaError_t launch_append(const spkv_cache* c, const int32_t* phys, const int32_t* tok, const void* k_new,
@@ -106,9 +116,10 @@ cudaError_t launch_append(const spkv_cache* c, const int32_t* phys, const int32_
                              static_cast<const uint32_t*>(v_new), n_rows, Hk, static_cast<int64_t>(c->d.n_phys_pages),
                              c->dev_err);
   if (e != cudaSuccess) return e;
-  return launch_pdl(append_sum_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
-                    static_cast<const uint32_t*>(c->d.k_pool), c->d.ksum, static_cast<const int32_t*>(c->d.page_cnt),
-                    phys, tok, n_rows, Hk, static_cast<int64_t>(c->d.n_phys_pages));
+  return launch_pdl(c->d.ksum_bf16 ? append_sum_kernel<true> : append_sum_kernel<false>,
+                    dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, static_cast<const uint32_t*>(c->d.k_pool),
+                    c->d.ksum, static_cast<const int32_t*>(c->d.page_cnt), phys, tok, n_rows, Hk,
+                    static_cast<int64_t>(c->d.n_phys_pages));
 }
 
 }  // namespace spkv

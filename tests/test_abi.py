@@ -56,9 +56,9 @@ def test_host_argument_rejection_without_gpu(lib):
     from sparse_paged_kv_score_gb300 import _abi
     out = ctypes.c_void_p()
     assert lib.paged_kv_create(None, None, ctypes.byref(out)) == _abi.SPKV_EINVAL
-    d = _abi.SpkvDesc(8, 64, 64, 16, 16, None, None, None, None, 0)
+    d = _abi.SpkvDesc(8, 64, 64, 16, 16, None, None, None, None, 0, 0)
     assert lib.paged_kv_create(ctypes.byref(d), None, ctypes.byref(out)) == _abi.SPKV_EUNSUPPORTED
-    d = _abi.SpkvDesc(8, 128, 64, 16, 16, None, None, None, None, 0)
+    d = _abi.SpkvDesc(8, 128, 64, 16, 16, None, None, None, None, 0, 0)
     assert lib.paged_kv_create(ctypes.byref(d), None, ctypes.byref(out)) == _abi.SPKV_EINVAL
     assert lib.sparse_decode_attn(None, None, 1, 8, None, 1, None, None, 1, None, None, None, None) \
         == _abi.SPKV_EINVAL
@@ -68,7 +68,9 @@ def test_host_argument_rejection_without_gpu(lib):
     assert lib.sparse_decode_attn_slots(None, None, 1, 8, None, None, None, 1, 1, None, None, None, None) \
         == _abi.SPKV_EINVAL
     # summaries are given together or not at all
-    d = _abi.SpkvDesc(8, 128, 64, 16, 16, 16, 16, 16, None, 0)
+    d = _abi.SpkvDesc(8, 128, 64, 16, 16, 16, 16, 16, None, 0, 0)
+    assert lib.paged_kv_create(ctypes.byref(d), None, ctypes.byref(out)) == _abi.SPKV_EINVAL
+    d = _abi.SpkvDesc(8, 128, 64, 16, 16, 16, 16, 16, 16, 0, 2)   # summary type flag out of range
     assert lib.paged_kv_create(ctypes.byref(d), None, ctypes.byref(out)) == _abi.SPKV_EINVAL
 
 

@@ -572,3 +572,43 @@ def test_prefill_rows_are_decode_queries():
         od, ld = oracle.lazy_attn_batch(q[:, t], w["k_pool"], w["v_pool"], w["phys"], w["valid"], w["slot"],
                                         w["n_pages"], w["qpos"] + t, w["doc_pos"], 500000.0, materialise=False)
         assert np.array_equal(out[:, t], od) and np.array_equal(lse[:, t], ld)
+
+
+# ------------------------------------------------------------------------------ bf16 summaries
+
+def test_round_bf16_matches_the_generator_rounding():
+    """fp64 -> bf16 round-to-nearest-even (frexp / rint) against the generator's fp32 bit
+    arithmetic, on fp32-exact values including exact ties."""
+    rng = np.random.default_rng(0)
+    x = (rng.standard_normal(20000) * 10.0 ** rng.integers(-3, 4, 20000)).astype(np.float32)
+    ties = (np.float32(1.0) + np.arange(1, 64, 2, dtype=np.float32) * np.float32(2.0 ** -8)).astype(np.float32)
+    x = np.concatenate([x, ties, -ties])
+    want = gen.bf16_to_f32(gen.f32_to_bf16(x)).astype(np.float64)
+    got = np.array([oracle.round_bf16(float(v)) for v in x])
+    assert np.array_equal(got, want)
+
+
+def test_scores_from_bf16_summaries_bruteforce():
+    """Keys with few significant bits (every fp32 sum exact): scores from bf16-rounded sums by
+    numpy against the oracle, then the distance to the fp32-summary scores stays within half a
+    bf16 ulp of each sum."""
+    rng = np.random.default_rng(3)
+    Hk, n_phys, G = 1, 6, 3
+    keys = (rng.integers(-40, 41, (Hk, n_phys, 64, 128)) / 8.0).astype(np.float32)
+    k_pool = gen.f32_to_bf16(keys)
+    q = gen.rows_bf16(3, 77, G).reshape(1, G, 128)
+    pt = np.arange(n_phys, dtype=np.int32).reshape(1, n_phys)
+    L = np.array([n_phys * 64], np.int32)
+    s16 = oracle.score_batch(q, k_pool, pt, L, summary_bf16=True)[0, 0]
+    s32 = oracle.score_batch(q, k_pool, pt, L)[0, 0]
+    sums = f(k_pool[0]).reshape(n_phys, 4, 16, 128).sum(2)                  # exact in fp32 here
+    means16 = gen.bf16_to_f32(gen.f32_to_bf16(sums.astype(np.float32))).astype(np.float64) / 16.0
+    qs = f(q[0]).sum(0)
+    want = (means16 @ qs).max(1) / math.sqrt(128)
+    want[n_phys - 1:] = -np.inf                                             # the local page and after
+    assert np.allclose(s16[:n_phys - 1], want[:n_phys - 1], rtol=0, atol=1e-12)
+    assert np.isneginf(s16[n_phys - 1])
+    bound = (np.abs(sums) * 2.0 ** -9 / 16.0) @ np.abs(qs) / math.sqrt(128)
+    diff = np.abs(s16[:n_phys - 1] - s32[:n_phys - 1])
+    assert (diff <= bound.max(1)[:n_phys - 1] + 1e-12).all()
+    assert diff.max() > 0                                                   # the rounding is real

@@ -29,11 +29,12 @@ def u32_as_i32(a) -> torch.Tensor:
 class Dev:
     """A sparse workload on the device with its library handle."""
 
-    def __init__(self, w: dict, page_cnt=None, max_units: int = 0):
+    def __init__(self, w: dict, page_cnt=None, max_units: int = 0, summary_bf16: bool = False):
         self.w = w
         self.B, self.Hq, self.Hk, self.npm = w["B"], w["Hq"], w["Hk"], w["np_max"]
         self.k_pool, self.v_pool = bf(w["k_pool"]), bf(w["v_pool"])
-        self.ksum = torch.zeros(self.Hk, w["n_phys"], 4, 128, dtype=torch.float32, device=DEV)
+        self.ksum = torch.zeros(self.Hk, w["n_phys"], 4, 128, device=DEV,
+                                dtype=torch.bfloat16 if summary_bf16 else torch.float32)
         cnt = gen.page_counts(w) if page_cnt is None else page_cnt
         self.cnt = i32(cnt)
         self.cache = spkv.paged_kv_create(self.k_pool, self.v_pool, self.ksum, self.cnt,

@@ -49,10 +49,11 @@ def test_summaries_match_oracle_means():
     d.close()
 
 
-def test_append_equals_rebuild():
+@pytest.mark.parametrize("summary_bf16", [False, True])
+def test_append_equals_rebuild(summary_bf16):
     B, Hk = 3, 2
     w = gen.sparse_workload(B, 8, Hk, 64 * 3 - 2, 4, 4, seed=5, extra_tokens=70)
-    d = Dev(w)
+    d = Dev(w, summary_bf16=summary_bf16)
     L = w["seq_len"].copy()
     for step in range(4):      # crosses the page boundary at 192
         phys = np.array([w["page_table"][b, L[b] // 64] for b in range(B)], np.int32)
@@ -69,7 +70,7 @@ def test_append_equals_rebuild():
     assert np.array_equal(d.k_pool.view(torch.int16).cpu().numpy().view(np.uint16), w["k_pool"])
     assert np.array_equal(d.v_pool.view(torch.int16).cpu().numpy().view(np.uint16), w["v_pool"])
     assert np.array_equal(d.cnt.cpu().numpy(), gen.page_counts(w))
-    fresh = Dev(w)      # summary build from scratch on the updated pool
+    fresh = Dev(w, summary_bf16=summary_bf16)      # summary build from scratch on the updated pool
     assert torch.equal(d.ksum, fresh.ksum), "append and create must give bitwise equal sums"
     assert d.errors() == (0, 0)
     d.close()
@@ -104,6 +105,35 @@ def test_score_blocks_vs_oracle(which):
     bound = _score_bound(w)
     diff = np.abs(s[fin] - ref[fin])
     assert (diff <= bound[fin]).all(), diff.max()
+    assert d.errors() == (0, 0)
+    d.close()
+
+
+@pytest.mark.parametrize("which", ["tiny", "mid"])
+def test_score_blocks_bf16_summaries_vs_oracle(which):
+    """bf16 summaries: the GPU rounds its fixed-order fp32 sum, the oracle the exact sum, so a
+    summary element may differ by one bf16 ulp (at most 2^-7 relative) on top of the fp32 bound."""
+    w = gen.tiny() if which == "tiny" else gen.sparse_workload(3, 32, 8, 64 * 40 + 5, 8, 8, seed=7,
+                                                                outlier_p=0.01)
+    d = Dev(w, summary_bf16=True)
+    assert d.ksum.dtype == torch.bfloat16
+    s = d.scores().cpu().numpy().astype(np.float64)
+    ref = oracle.score_batch(w["q"], w["k_pool"], w["page_table"], w["seq_len"], summary_bf16=True)
+    assert np.array_equal(np.isinf(s), np.isinf(ref))
+    fin = np.isfinite(ref)
+    q = f64(w["q"])
+    G = w["G"]
+    ulp = np.zeros_like(ref)
+    for b in range(w["B"]):
+        for h in range(w["Hk"]):
+            qs = np.abs(q[b, h * G:(h + 1) * G].sum(0))
+            m = np.abs(f64(w["k_pool"][h, w["page_table"][b]]).reshape(-1, 4, 16, 128).mean(2))
+            ulp[b, h] = 2.0 ** -7 * (m @ qs).max(1) / math.sqrt(128)
+    diff = np.abs(s[fin] - ref[fin])
+    assert (diff <= _score_bound(w)[fin] + ulp[fin]).all(), diff.max()
+    # and the bf16 scores stay close to the fp32-summary ones
+    s32 = oracle.score_batch(w["q"], w["k_pool"], w["page_table"], w["seq_len"])
+    assert np.abs(s[fin] - s32[fin]).max() <= (ulp[fin] + _score_bound(w)[fin]).max()
     assert d.errors() == (0, 0)
     d.close()
 

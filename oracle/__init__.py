@@ -68,6 +68,8 @@ def _l():
             "orc_lru_batch": ([vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, i32], None),
             "orc_lazy_prefill_batch": ([i32, i32, i32, i32, vp, vp, vp, i64, vp, vp, vp, i32, vp, i32, vp, vp,
                                         i32, f64, i32, vp, i32, vp, vp, i32], None),
+            "orc_column_scores_batch": ([i32, i32, i32, i32, vp, vp, i64, vp, i32, vp, i32, vp, i32, vp, i32],
+                                        None),
             "orc_retrieve_unit": ([vp, vp, vp, vp, i32, vp, vp, i32, vp, vp], None),
             "orc_retrieve_batch": ([i32, i32, vp, vp, i64, vp, i32, vp, vp, vp, vp, vp, i32, vp, vp, i64,
                                     i32, i32], None),
@@ -355,3 +357,17 @@ def lazy_prefill_batch(q, k_pool, v_pool, phys, valid, slot, n_pages, qpos0, doc
                                 doc_pos.shape[1], float(theta), int(bool(materialise)), _p(it), it.shape[0],
                                 _p(out), _p(lse), nthreads)
     return out, lse
+
+
+def column_scores_batch(q, k_pool, page_table, seq_len, n_out: int, items=None, nthreads: int = 0):
+    """PyramidKV-style score S per (request, query head): q [B][alpha][Hq][128] (bf16 bits) are the
+    prompt's last alpha rows; returns S [B][Hq][n_out] (fp64) for the listed items (b * Hq + hq)."""
+    q, k_pool = _c(q, np.uint16), _c(k_pool, np.uint16)
+    page_table, seq_len = _c(page_table, np.int32), _c(seq_len, np.int32)
+    B, alpha, Hq, _ = q.shape
+    Hk, n_phys = k_pool.shape[0], k_pool.shape[1]
+    S = np.zeros((B, Hq, n_out), np.float64)
+    it = _units(items, B * Hq)
+    _l().orc_column_scores_batch(B, Hq, Hk, alpha, _p(q), _p(k_pool), n_phys, _p(page_table), page_table.shape[1],
+                                 _p(seq_len), int(n_out), _p(it), it.shape[0], _p(S), nthreads)
+    return S

@@ -548,6 +548,54 @@ void orc_lazy_prefill_batch(int B, int T, int Hq, int Hk, const uint16_t* q, con
   });
 }
 
+// ---------------------------------------------------------------- column score S
+// [FA] "2. Attention modification" (the PyramidKV-style sparsification score, reading R16): the
+// last alpha rows of a prompt of n tokens, at positions n - alpha + j, attend causally over the
+// prompt's keys; with A[j][i] = softmax over i <= n - alpha + j of q_j . k_i / sqrt(128),
+//   S[i] = sum_j A[j][i]          (i < n; a key after a row's position gets nothing from it).
+// Computed the two-pass way the page describes: each row's log-sum-exp first (rowmax and l),
+// then every probability from it.  q: alpha rows of 128 bf16 (one query head); kplane: the pool
+// plane of its kv head; pt_row: the request's page table; S: n_out entries (>= n are 0).
+void orc_column_scores_unit(const uint16_t* q, int q_stride, int alpha, const uint16_t* kplane,
+                            const int32_t* pt_row, int n, int n_out, double* S) {
+  const double inv_sqrt_d = 1.0 / std::sqrt(static_cast<double>(kD));
+  for (int i = 0; i < n_out; ++i) S[i] = 0.0;
+  std::vector<double> z(n);
+  for (int j = 0; j < alpha; ++j) {
+    const int pos = n - alpha + j;
+    if (pos < 0) continue;
+    const uint16_t* qj = q + static_cast<int64_t>(j) * q_stride;
+    for (int i = 0; i <= pos; ++i) {
+      const uint16_t* k = row_ptr(kplane, pt_row[i / kPage], i % kPage);
+      double dot = 0.0;
+      for (int d = 0; d < kD; ++d) dot += from_bf16(qj[d]) * from_bf16(k[d]);
+      z[i] = dot * inv_sqrt_d;
+    }
+    double m = kNegInf;
+    for (int i = 0; i <= pos; ++i) m = std::max(m, z[i]);
+    double l = 0.0;
+    for (int i = 0; i <= pos; ++i) l += std::exp(z[i] - m);
+    const double lse = m + std::log(l);
+    for (int i = 0; i <= pos; ++i) S[i] += std::exp(z[i] - lse);
+  }
+}
+
+// Column scores for every (request, query head) listed: q is [B][alpha][Hq][128], S is
+// [B][Hq][n_out]; request b's prompt has seq_len[b] tokens in pages page_table[b][...].
+void orc_column_scores_batch(int B, int Hq, int Hk, int alpha, const uint16_t* q, const uint16_t* kpool,
+                             int64_t n_phys, const int32_t* page_table, int np_max, const int32_t* seq_len,
+                             int n_out, const int32_t* items, int n_items, double* S, int nthreads) {
+  (void)B;
+  const int G = Hq / Hk;
+  for_units(n_items, nthreads, [&](int i) {
+    const int it = items[i], b = it / Hq, hq = it % Hq, h = hq / G;
+    orc_column_scores_unit(q + (static_cast<int64_t>(b) * alpha * Hq + hq) * kD, Hq * kD, alpha,
+                           kpool + static_cast<int64_t>(h) * n_phys * kPage * kD,
+                           page_table + static_cast<int64_t>(b) * np_max, seq_len[b], n_out,
+                           S + static_cast<int64_t>(it) * n_out);
+  });
+}
+
 // Retrieve for every unit.  Host pools [Hk][n_host][64][128]; slot pools [Hk][n_slot_pages][64][128]
 // with unit (b, h)'s slots at pages b * n_slots .. b * n_slots + n_slots - 1 of plane h.
 void orc_retrieve_batch(int B, int Hk, const uint16_t* khost, const uint16_t* vhost, int64_t n_host,

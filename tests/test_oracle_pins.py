@@ -612,3 +612,46 @@ def test_scores_from_bf16_summaries_bruteforce():
     diff = np.abs(s16[:n_phys - 1] - s32[:n_phys - 1])
     assert (diff <= bound.max(1)[:n_phys - 1] + 1e-12).all()
     assert diff.max() > 0                                                   # the rounding is real
+
+
+# ------------------------------------------------------------------------------ column score S
+
+def _colscore_case(seed, B=2, Hq=4, Hk=2, n=200, alpha=9):
+    w = gen.sparse_workload(B, Hq, Hk, n, 4, 4, seed=seed)
+    q = gen.rows_bf16(seed, 555, B * alpha * Hq).reshape(B, alpha, Hq, 128)
+    return w, q
+
+
+def test_column_scores_scipy_bruteforce():
+    w, q = _colscore_case(1)
+    n, alpha = int(w["seq_len"][0]), q.shape[1]
+    S = oracle.column_scores_batch(q, w["k_pool"], w["page_table"], w["seq_len"], w["np_max"] * 64)
+    G = w["Hq"] // w["Hk"]
+    for b in range(w["B"]):
+        for hq in range(w["Hq"]):
+            h = hq // G
+            K = np.concatenate([f(w["k_pool"][h, w["page_table"][b, p]]) for p in range(w["np_max"])])[:n]
+            Q = f(q[b, :, hq])
+            Z = Q @ K.T / math.sqrt(128)
+            want = np.zeros(w["np_max"] * 64)
+            for j in range(alpha):
+                pos = n - alpha + j
+                want[:pos + 1] += softmax(Z[j, :pos + 1])
+            assert np.allclose(S[b, hq], want, rtol=1e-10, atol=1e-13)
+
+
+def test_column_scores_invariants():
+    """Each row's probabilities sum to one, so S sums to alpha; keys after row j's position get
+    nothing from it, so the last key collects only the last row; S >= 0; nothing past n."""
+    w, q = _colscore_case(2, n=64 * 3 + 17, alpha=20)
+    n, alpha = int(w["seq_len"][0]), q.shape[1]
+    S = oracle.column_scores_batch(q, w["k_pool"], w["page_table"], w["seq_len"], w["np_max"] * 64)
+    assert np.allclose(S.sum(-1), alpha, rtol=0, atol=1e-9)
+    assert (S >= 0).all() and (S[..., n:] == 0).all()
+    # the newest key is seen by the last row only: S[n-1] = A[alpha-1][n-1] < 1
+    assert (S[..., n - 1] < 1).all() and (S[..., n - 1] > 0).all()
+    # a window covering the whole prompt: every row sums to one over its own prefix
+    w2, q2 = _colscore_case(3, n=30, alpha=30)
+    S2 = oracle.column_scores_batch(q2, w2["k_pool"], w2["page_table"], w2["seq_len"], 64)
+    assert np.allclose(S2.sum(-1), 30, rtol=0, atol=1e-9)
+    assert (S2[..., 0] >= 1 - 1e-12).all()      # row 0 sits at position 0 and sees key 0 alone

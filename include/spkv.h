@@ -14,6 +14,7 @@
  *   sparse_decode_attn   split-K flash decoding over the selected pages
  *   lazy_rope_decode_attn  the same with deferred RoPE (query rotated once per document)
  *   lazy_rope_prefill_attn a tile of new query rows over cached documents (tcgen05)
+ *   attn_column_scores   PyramidKV-style key scores of a prompt's last rows (tcgen05)
  *
  * Sources (web pages, cited by title and section):
  *   [NOSA] "NOSA: Native and Offloadable Sparse Attention", sections "Method 1: the NOSA
@@ -221,6 +222,23 @@ int lazy_rope_prefill_attn(spkv_cache_t cache, const void* q, int B, int T, int 
                            const int32_t* qpos0, const uint32_t* meta, int meta_heads,
                            const int32_t* n_pages, int np_max, const int32_t* doc_pos,
                            int max_docs, float theta, float* out, float* lse, void* stream);
+
+/* The PyramidKV-style sparsification score S of a prompt's keys ([FA] "2. Attention
+ * modification": the sum of the softmax probabilities the last alpha rows give each key,
+ * computed from each row's maximum and sum in two passes, on the tcgen05 tensor cores).  For
+ * query head hq of request b, with n = seq_len[b] prompt tokens in pages page_table[b][..] of
+ * kv head hq / G, rows j < alpha at positions n - alpha + j and causal visibility:
+ *   scores[b][hq][i] = sum_j softmax_{i' <= n - alpha + j}(q_j . k_i' / sqrt(128))[i]   (i < n)
+ * and 0 for n <= i < 64 np_max.  The keys are read from the handle's pool; V is not used.
+ *   q          : device bf16 [B][alpha][Hq][128], the prompt's last alpha query rows (RoPE
+ *                already applied), 16-byte aligned
+ *   page_table : device int32 [B][np_max];  seq_len: device int32 [B] (alpha <= n <= 64 np_max,
+ *                else SPKV_DEVERR_PAGE_ID and the row is zeros)
+ *   scores     : device fp32 [B][Hq][64 np_max] (output)
+ * alpha <= 128 (else SPKV_EUNSUPPORTED).  B, Hq <= 65535. */
+int attn_column_scores(spkv_cache_t cache, const void* q, int B, int alpha, int Hq,
+                       const int32_t* page_table, int np_max, const int32_t* seq_len,
+                       float* scores, void* stream);
 
 int resident_setdiff(spkv_cache_t cache, const int32_t* resident, int n_slots, const int32_t* sel,
                      const int32_t* n_sel, int sel_stride, int n_units, int32_t* missing,

@@ -32,6 +32,7 @@ from ._abi import DEVERR, SpkvDesc, SpkvError, check, load
 __all__ = ["PagedKVCache", "paged_kv_create", "paged_kv_append", "score_blocks", "select_topk",
            "sparse_decode_attn", "lazy_rope_decode_attn", "resident_setdiff", "lru_bucket_update",
            "select_resident_update", "retrieve_pages", "sparse_decode_attn_slots", "lazy_rope_prefill_attn",
+           "attn_column_scores",
            "sparse_decode_attn_noalloc", "pack_page_words", "get_device_error", "SpkvError", "DEVERR",
            "load"]
 
@@ -263,6 +264,18 @@ def lazy_rope_prefill_attn(cache: PagedKVCache, q, qpos0, meta, n_pages, doc_pos
         meta_heads, _t(n_pages, torch.int32, "n_pages", (B,)), np_max,
         _t(doc_pos, torch.int32, "doc_pos", (B, max_docs)), max_docs, float(theta),
         _t(out, torch.float32, "out", (B, T, Hq, HEAD_DIM)), _t(lse, torch.float32, "lse", (B, T, Hq)),
+        _stream(stream)))
+
+
+def attn_column_scores(cache: PagedKVCache, q, page_table, seq_len, scores, stream=None):
+    """PyramidKV-style key scores: q bf16 [B][alpha][Hq][128] (the prompt's last alpha rows);
+    scores fp32 [B][Hq][64 np_max] (output)."""
+    B, alpha, Hq = q.shape[0], q.shape[1], q.shape[2]
+    np_max = page_table.shape[1]
+    check("attn_column_scores", load().attn_column_scores(
+        cache.handle, _t(q, torch.bfloat16, "q", (B, alpha, Hq, HEAD_DIM)), B, alpha, Hq,
+        _t(page_table, torch.int32, "page_table", (B, np_max)), np_max,
+        _t(seq_len, torch.int32, "seq_len", (B,)), _t(scores, torch.float32, "scores", (B, Hq, np_max * PAGE)),
         _stream(stream)))
 
 

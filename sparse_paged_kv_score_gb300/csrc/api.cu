@@ -87,6 +87,7 @@ cudaError_t init_kernel_attributes() {
   if ((e = select_init_attributes()) != cudaSuccess) return e;
   if ((e = fused_init_attributes()) != cudaSuccess) return e;
   if ((e = prefill_init_attributes()) != cudaSuccess) return e;
+  if ((e = colscore_init_attributes()) != cudaSuccess) return e;
   return resid_init_attributes();
 }
 }  // namespace spkv
@@ -319,6 +320,33 @@ int lazy_rope_prefill_attn(spkv_cache_t c, const void* q, int B, int T, int Hq, 
     p.phase_inc[j] = static_cast<uint64_t>(std::ldexp(f, 64));
   }
   return status_of(spkv::launch_prefill(c, p, as_stream(stream)));
+}
+
+int attn_column_scores(spkv_cache_t c, const void* q, int B, int alpha, int Hq, const int32_t* page_table,
+                       int np_max, const int32_t* seq_len, float* scores, void* stream) {
+  if (!c || B < 0 || Hq <= 0 || alpha < 0) return SPKV_EINVAL;
+  const int Hk = c->d.n_kv_heads;
+  if (Hq % Hk != 0) return SPKV_EINVAL;
+  if (alpha > 128 || Hq / Hk > kMaxGroup) return SPKV_EUNSUPPORTED;
+  if (B == 0) return SPKV_OK;
+  if (!q || !page_table || !seq_len || !scores || np_max <= 0 || alpha == 0 || !aligned(q, 16)) return SPKV_EINVAL;
+  if (B > 65535 || Hq > 65535) return SPKV_EINVAL;
+  spkv::ColScoreParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = static_cast<const uint16_t*>(q);
+  p.scores = scores;
+  p.B = B;
+  p.alpha = alpha;
+  p.Hq = Hq;
+  p.Hk = Hk;
+  p.G = Hq / Hk;
+  p.n_phys = c->d.n_phys_pages;
+  p.page_table = page_table;
+  p.np_max = np_max;
+  p.seq_len = seq_len;
+  p.scale_log2 = static_cast<float>(1.4426950408889634074 / std::sqrt(128.0));
+  p.err = c->dev_err;
+  return status_of(spkv::launch_colscore(c, p, as_stream(stream)));
 }
 
 int resident_setdiff(spkv_cache_t c, const int32_t* resident, int n_slots, const int32_t* sel, const int32_t* n_sel,

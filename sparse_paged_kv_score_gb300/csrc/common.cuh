@@ -154,6 +154,18 @@ __device__ __forceinline__ void named_bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// Named barrier that also ANDs a predicate over its n threads (every one gets the same answer).
+__device__ __forceinline__ bool named_bar_and(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.and.pred po, %2, %3, pi;\n"
+      " selp.u32 %0, 1, 0, po;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
 // Monotone map of an fp32 to uint32 (larger float -> larger key); -0.0 is mapped like +0.0.
 __device__ __forceinline__ uint32_t float_order_key(float f) {
   uint32_t u = __float_as_uint(f);

@@ -109,6 +109,19 @@ struct PrefillParams {
   uint64_t phase_inc[64];
 };
 
+// Parameters of the column-score kernel (PyramidKV-style score S).
+struct ColScoreParams {
+  const uint16_t* q;             // bf16 [B][alpha][Hq][128]: the last alpha rows of each prompt
+  float* scores;                 // [B][Hq][np_max * 64]
+  int B, alpha, Hq, Hk, G;
+  int64_t n_phys;
+  const int32_t* page_table;     // [B][np_max]
+  int np_max;
+  const int32_t* seq_len;        // prompt length n per request
+  float scale_log2;
+  uint32_t* err;
+};
+
 cudaError_t launch_summary_build(const spkv_cache* c, cudaStream_t st);
 cudaError_t launch_append(const spkv_cache* c, const int32_t* phys, const int32_t* tok, const void* k_new,
                           const void* v_new, int n_rows, cudaStream_t st);
@@ -144,6 +157,8 @@ cudaError_t select_init_attributes();
 cudaError_t resid_init_attributes();
 cudaError_t fused_init_attributes();
 cudaError_t prefill_init_attributes();
+cudaError_t colscore_init_attributes();
+cudaError_t launch_colscore(const spkv_cache* c, const ColScoreParams& p, cudaStream_t st);
 cudaError_t launch_prefill(const spkv_cache* c, const PrefillParams& p, cudaStream_t st);
 
 }  // namespace spkv

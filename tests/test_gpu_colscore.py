@@ -1,0 +1,80 @@
+"""GPU parity of the PyramidKV-style column score S (tcgen05) against the fp64 oracle.
+
+Both sides take every score from each row's log-sum-exp (two passes), the GPU in fp32 with
+bf16 operands that are exact inputs: each probability carries a relative error of a few 1e-6, so
+S matches to 1e-4 relative (plus 1e-6 absolute), and every row's probabilities still sum to one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+import sparse_paged_kv_score_gb300 as spkv
+from helpers import DEV, Dev, bf, i32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from sparse_paged_kv_score_gb300 import build
+    build.build()
+    spkv.load()
+
+
+def _run(w, q, seq_len=None):
+    d = Dev(w)
+    B, alpha, Hq = q.shape[0], q.shape[1], q.shape[2]
+    L = i32(w["seq_len"] if seq_len is None else seq_len)
+    out = torch.full((B, Hq, w["np_max"] * 64), float("nan"), dtype=torch.float32, device=DEV)
+    spkv.attn_column_scores(d.cache, bf(q), d.pt, L, out)
+    res = out.cpu().numpy()
+    err = d.errors()
+    d.close()
+    return res, err
+
+
+def _check(S, ref, alpha, n):
+    assert np.isfinite(S).all()
+    assert (np.abs(S - ref) <= 1e-4 * np.abs(ref) + 1e-6).all(), np.abs(S - ref).max()
+    assert np.allclose(S.sum(-1), np.minimum(alpha, n), rtol=1e-4, atol=0)
+
+
+@pytest.mark.parametrize("n,alpha,Hq,Hk", [(200, 9, 8, 2), (64 * 5, 64, 8, 2), (64 * 7 + 13, 128, 16, 4),
+                                           (130, 1, 4, 1), (64 * 3, 128, 40, 8), (64 * 9 + 1, 100, 8, 8)])
+def test_column_scores_vs_oracle(n, alpha, Hq, Hk):
+    w = gen.sparse_workload(2, Hq, Hk, n, 4, 4, seed=n + alpha)
+    q = gen.rows_bf16(n, 321, 2 * alpha * Hq).reshape(2, alpha, Hq, 128)
+    S, err = _run(w, q)
+    ref = oracle.column_scores_batch(q, w["k_pool"], w["page_table"], w["seq_len"], w["np_max"] * 64)
+    assert err == (0, 0)
+    _check(S, ref, alpha, n)
+
+
+def test_column_scores_ragged_prompts_and_rejected_request():
+    """Prompts of different lengths in one call; a prompt shorter than the window is rejected
+    (error bit, zero row) without disturbing the others."""
+    w = gen.sparse_workload(3, 8, 2, 64 * 6, 4, 4, seed=11)
+    alpha = 40
+    seq = np.array([64 * 6, 64 * 2 + 5, 20], np.int32)   # the last is shorter than alpha
+    q = gen.rows_bf16(11, 322, 3 * alpha * 8).reshape(3, alpha, 8, 128)
+    S, err = _run(w, q, seq)
+    assert err[1] == spkv.DEVERR["PAGE_ID"]
+    assert (S[2] == 0).all()
+    ref = oracle.column_scores_batch(q[:2], w["k_pool"], w["page_table"][:2], seq[:2], w["np_max"] * 64)
+    for b in range(2):
+        _check(S[b], ref[b], alpha, seq[b])
+
+
+def test_column_scores_full_context_sampled_heads():
+    """A 32768-token prompt (512 pages) with a 128-row window, sampled query heads."""
+    w = gen.sparse_workload(1, 32, 8, 32768, 4, 4, seed=12, outlier_p=0.01)
+    alpha = 128
+    q = gen.rows_bf16(12, 323, alpha * 32).reshape(1, alpha, 32, 128)
+    S, err = _run(w, q)
+    assert err == (0, 0)
+    items = np.array([0, 13, 31], np.int32)
+    ref = oracle.column_scores_batch(q, w["k_pool"], w["page_table"], w["seq_len"], w["np_max"] * 64, items=items)
+    for it in items:
+        _check(S[0, it], ref[0, it], alpha, 32768)

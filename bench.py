@@ -52,6 +52,10 @@ def parse():
     ap.add_argument("--no-prefill", action="store_true", help="skip the LazyAttention prefill sub-measurement")
     ap.add_argument("--no-bf16-summaries", action="store_true",
                     help="skip the step with bf16 pooled-key summaries")
+    ap.add_argument("--no-colscore", action="store_true",
+                    help="skip the PyramidKV-style column-score sub-measurement")
+    ap.add_argument("--col-batch", type=int, default=16,
+                    help="prompts of the column-score workload (5000 tokens, last 256 rows each)")
     ap.add_argument("--rag-batch", type=int, default=64,
                     help="requests of the lazy-RoPE RAG workload (64 = the workload; smaller for profiling)")
     ap.add_argument("--rag-docs", type=int, default=256,
@@ -642,6 +646,40 @@ def run_native(args):
         del graphs16
         cache16.close()
 
+    # ---- PyramidKV-style column score S: prompts of 5000 tokens, window of the last 256 rows
+    colsc = None
+    if not args.no_colscore and rank == 0:
+        Bc, nc, ac = args.col_batch, 5000, 256
+        npc = (nc + 63) // 64
+        ck = bf(gen.rows_bf16(0, 7800, Hk * Bc * npc * 64).reshape(Hk, Bc * npc, 64, 128))
+        ccache = spkv.paged_kv_create(ck, ck, None, None)           # V is not read by the score
+        cpt = i32(gen.permutation(0, 7801, Bc * npc).reshape(Bc, npc))
+        cseq = i32(np.full(Bc, nc, np.int32))
+        cq = bf(gen.rows_bf16(0, 7802, Bc * ac * Hq).reshape(Bc, ac, Hq, 128))
+        cs = torch.empty(Bc, Hq, npc * 64, dtype=torch.float32, device=dev)
+
+        def col_call(i):
+            spkv.attn_column_scores(ccache, cq, cpt, cseq, cs)
+
+        timed(col_call, range(3))
+        col_ms = statistics.mean(timed(col_call, timed_idx))
+        sums = cs.sum(-1)
+        if not torch.allclose(sums, torch.full_like(sums, float(ac)), rtol=1e-3):
+            raise RuntimeError("column scores do not sum to the window size")
+        st_c, bits_c = spkv.get_device_error(ccache)
+        if st_c != 0:
+            raise RuntimeError(f"device error bits {bits_c} in the column-score leg")
+        ccache.close()
+        cflops = 4.0 * 128 * ac * nc * Hq * Bc   # S = Q K^T over the window rows and all keys, in both passes
+        ctf = cflops / (col_ms * 1e-3) / 1e12
+        tpeak, tkind = bf16_peak()
+        colsc = {"kernel": "attn_column_scores (colscore_kernel: tcgen05.mma, TMA pages, two passes)",
+                 "workload": f"{Bc} prompts x {nc} tokens, window of the last {ac} rows, Hq {Hq} / Hk {Hk}",
+                 "us": col_ms * 1e3, "flops": cflops, "bound": "tensor", "achieved_TFLOPs": ctf,
+                 "peak": tpeak, "peak_kind": tkind + " bf16 dense (cuBLAS burst)", "frac": ctf / tpeak,
+                 "prompts_per_s": Bc / (col_ms * 1e-3), "launches": 2}
+        del ck, cq, cs
+
     # ---- offload: the 262k-context workload with its K/V pool in pinned host memory
     offload = None
     if not args.no_offload and rank == 0:
@@ -730,6 +768,7 @@ def run_native(args):
             "lazy_rag": rag,
             "lazy_prefill": prefill,
             "bf16_summaries": bf16_sum,
+            "column_scores": colsc,
             "offload": offload,
             "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},

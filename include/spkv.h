@@ -235,7 +235,9 @@ int lazy_rope_prefill_attn(spkv_cache_t cache, const void* q, int B, int T, int 
  *   page_table : device int32 [B][np_max];  seq_len: device int32 [B] (alpha <= n <= 64 np_max,
  *                else SPKV_DEVERR_PAGE_ID and the row is zeros)
  *   scores     : device fp32 [B][Hq][64 np_max] (output)
- * alpha <= 128 (else SPKV_EUNSUPPORTED).  B, Hq <= 65535. */
+ * alpha <= 1024 (else SPKV_EUNSUPPORTED), run as one launch per 128-row chunk of the window, the
+ * later chunks adding into scores (so scores must not alias another live buffer between them).
+ * B, Hq <= 65535. */
 int attn_column_scores(spkv_cache_t cache, const void* q, int B, int alpha, int Hq,
                        const int32_t* page_table, int np_max, const int32_t* seq_len,
                        float* scores, void* stream);

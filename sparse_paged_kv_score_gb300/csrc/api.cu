@@ -4,6 +4,7 @@
 
 #include <cmath>
 #include <cstdlib>
+#include <algorithm>
 #include <cstring>
 #include <new>
 
@@ -14,6 +15,7 @@ using spkv::AttnParams;
 namespace {
 
 constexpr int kMaxGroup = 16;
+constexpr int kMaxColumnRows = 1024;   // window rows of attn_column_scores (eight 128-row launches)
 constexpr int kMaxUnitsDefault = 4096;
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
@@ -327,7 +329,7 @@ int attn_column_scores(spkv_cache_t c, const void* q, int B, int alpha, int Hq, 
   if (!c || B < 0 || Hq <= 0 || alpha < 0) return SPKV_EINVAL;
   const int Hk = c->d.n_kv_heads;
   if (Hq % Hk != 0) return SPKV_EINVAL;
-  if (alpha > 128 || Hq / Hk > kMaxGroup) return SPKV_EUNSUPPORTED;
+  if (alpha > kMaxColumnRows || Hq / Hk > kMaxGroup) return SPKV_EUNSUPPORTED;
   if (B == 0) return SPKV_OK;
   if (!q || !page_table || !seq_len || !scores || np_max <= 0 || alpha == 0 || !aligned(q, 16)) return SPKV_EINVAL;
   if (B > 65535 || Hq > 65535) return SPKV_EINVAL;
@@ -346,7 +348,16 @@ int attn_column_scores(spkv_cache_t c, const void* q, int B, int alpha, int Hq, 
   p.seq_len = seq_len;
   p.scale_log2 = static_cast<float>(1.4426950408889634074 / std::sqrt(128.0));
   p.err = c->dev_err;
-  return status_of(spkv::launch_colscore(c, p, as_stream(stream)));
+  // one launch per 128-row chunk of the window: each row's softmax is its own, so the column sums
+  // of the chunks add; later chunks accumulate into the first one's result
+  for (int r0 = 0; r0 < alpha; r0 += 128) {
+    p.row0 = r0;
+    p.rows = std::min(128, alpha - r0);
+    p.accumulate = r0 > 0;
+    const int st = status_of(spkv::launch_colscore(c, p, as_stream(stream)));
+    if (st != SPKV_OK) return st;
+  }
+  return SPKV_OK;
 }
 
 int resident_setdiff(spkv_cache_t c, const int32_t* resident, int n_slots, const int32_t* sel, const int32_t* n_sel,

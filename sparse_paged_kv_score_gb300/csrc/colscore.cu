@@ -8,19 +8,27 @@
 // p = exp(q k - rowmax) / l in a second pass, with the loop order turned to k-major so that the
 // sum over rows stays in registers, and skips work the causal mask zeroes.
 //
-// One CTA per (request b, query head hq); the alpha (<= 128) rows are one M 128 tile.  Six warps:
+// One CTA per (request b, query head hq) and launch; a launch covers one chunk of up to 128 window
+// rows (one M 128 tile).  Every row's softmax is its own, so the chunks' column sums add: the first
+// launch writes them, later launches add theirs.  Eighteen warps:
 //   warp 0     TMA producer: the K rows of two consecutive pages (two 64 x 64 bf16 boxes each,
 //              128-byte swizzle, stacked into 128-row tiles) into a 3-stage ring, once for each
 //              pass;
 //   warp 1     MMA issuer (one thread): S = Q K^T (M 128 query rows, N 64 or 128 keys) into one
 //              of two TMEM buffers, in both passes; a stage is released as soon as its MMA
 //              completes (V is never needed);
-//   warps 2-5  thread r owns query row r (TMEM lane r).  Pass 1 keeps its causal row maximum and
-//              sum in the log2 domain (the row log-sum-exp).  Pass 2 turns its S row into
-//              probabilities 2^(s scale - lse) and writes them to a padded fp32 tile in shared
-//              memory; then thread r sums column r of that tile (key r of the pair) over the
-//              alpha rows -- the page's k-major loop order, with the transpose done in shared
-//              memory.
+//   warps 2-17 four column groups of 32 keys (warps 2-5, 6-9, 10-13, 14-17), one warp per TMEM
+//              lane quarter in each, so a thread owns query row r (TMEM lane r) on 32 keys of the
+//              pair.  Pass 1 keeps its causal row maximum and sum over its keys in the log2
+//              domain; the four groups merge into the row log-sum-exp once.  Pass 2 turns the S
+//              row into probabilities 2^(s scale - lse) and sums them over the rows (the page's
+//              k-major loop order, the transpose done in registers): a butterfly across the
+//              warp's 32 lanes leaves lane l with the sum of key l over its 32 rows, and the four
+//              lane quarters' sums are added in shared memory in a fixed order by whichever of
+//              the group's four warps finishes the job last (a counter per group and ring slot),
+//              so no warp waits for another.  Three ring slots suffice: a warp can only start job
+//              j + 3 after the MMA of job j + 3, which waits for every warp to have read job
+//              j + 1 from TMEM, i.e. to have finished job j.
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -31,9 +39,10 @@ namespace spkv {
 namespace {
 
 constexpr int kCM = 128;                    // tile rows: the window's query rows
-constexpr int kCStages = 3;
-constexpr int kPRow = kCM + 1;              // padded row of the probability tile (conflict-free)
-constexpr int kCThreads = 192;
+constexpr int kCStages = 4;
+constexpr int kCThreads = 576;
+constexpr int kMathThreads = 512;
+constexpr int kGroups = 4;                  // column groups of 32 keys in a page pair
 constexpr int kBox = 64 * 128;              // one page's 64 rows x 128 B (one d-half)
 constexpr int kGBox = 2 * kBox;             // two pages' rows of one d-half
 constexpr int kCStageBytes = 2 * kGBox;     // K half 0, K half 1 of a page pair
@@ -44,8 +53,11 @@ struct ColSmem {
   uint64_t full[kCStages], empty[kCStages];
   uint64_t dfull[2], dfree[2];
   uint64_t drain;
+  uint64_t mlready;                         // every group's (max, sum) rows are published
   uint32_t tmem_base;
-  float prob[kCM * kPRow];                  // pass 2: probabilities [query row][key], padded rows
+  float ml[kGroups][2][kCM];                // pass 1 -> 2: (max, sum) of each column group per row
+  float part[3][4][kCM];                    // pass 2: column sums of each lane quarter (32 rows), 3 slots
+  int cnt[3][kGroups];                      // pass 2: warps of a group done with a slot
 };
 
 constexpr size_t kColSmem = 1024 + kQBytes + size_t(kCStages) * kCStageBytes + sizeof(ColSmem);
@@ -79,9 +91,11 @@ __global__ void __launch_bounds__(kCThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S.dfull[i], 1);
-      mbar_init(&S.dfree[i], 4);
+      mbar_init(&S.dfree[i], kMathThreads / 32);
     }
     mbar_init(&S.drain, 1);
+    mbar_init(&S.mlready, kMathThreads / 32);
+    for (int i = 0; i < 3 * kGroups; ++i) (&S.cnt[0][0])[i] = 0;
     fence_mbar_init();
     prefetch_tensormap(&tmk);
   }
@@ -97,7 +111,8 @@ __global__ void __launch_bounds__(kCThreads, 1)
   for (int i = tid; i < kCM * 16; i += kCThreads) {
     const int r = i >> 4, c = i & 15;
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < p.alpha) v = *reinterpret_cast<const uint4*>(p.q + ((int64_t(b) * p.alpha + r) * p.Hq + hq) * kHeadDim + 8 * c);
+    if (r < p.rows)
+      v = *reinterpret_cast<const uint4*>(p.q + ((int64_t(b) * p.alpha + p.row0 + r) * p.Hq + hq) * kHeadDim + 8 * c);
     *reinterpret_cast<uint4*>(sQ + (c >> 3) * (kCM * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
   }
   fence_proxy_async_smem();
@@ -183,100 +198,146 @@ __global__ void __launch_bounds__(kCThreads, 1)
   } else {
     // ================================================================ math warps
     const int quarter = warp & 3;
+    const int grp = (warp - 2) >> 2;                 // column group: keys 32 grp .. 32 grp + 31 of the pair
     const int r = quarter * 32 + lane;               // TMEM lane: query row r
-    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
+    const int t = (warp - 2) * 32 + lane;            // 0 .. 511
+    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + 32 * grp;
     const float scale = p.scale_log2;
-    const int row_pos = n - p.alpha + r;             // position of query row r
+    const int row_min = n - p.alpha + p.row0;        // position of the chunk's first row
+    const int row_pos = row_min + r;                 // position of query row r
     float m = -CUDART_INF_F, l = 0.f, lse2 = CUDART_INF_F;
     bool ok = true;
     float* srow = p.scores + (int64_t(b) * p.Hq + hq) * (int64_t(p.np_max) * kPageTokens);
     for (int j = 0; j < n_jobs; ++j) {
       const int g = j % ng, bb = j & 1;
       const bool pass2 = j >= ng;
-      const int size = 2 * g + 1 < np_b ? 2 : 1;
-      const int key0 = 2 * g * kPageTokens;          // position of the pair's first key
-      const int ncol = 64 * size;
-      if (j == ng) lse2 = (r < p.alpha && l > 0.f) ? m + log2f(l) : CUDART_INF_F;   // pass 1 done
-      // all four math warps leave together (pass 2 synchronises them on a named barrier)
-      if (!named_bar_and(1, 128, warp_wait(&S.dfull[bb], (j >> 1) & 1))) {
+      const int key0 = 2 * g * kPageTokens + 32 * grp;   // position of this warp's first key
+      const bool live = key0 < n;                        // the pair's tail may lie past the prompt
+      if (j == ng) {                                     // pass 1 done: publish this group's (max, sum)
+        S.ml[grp][0][r] = m;
+        S.ml[grp][1][r] = l;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.mlready);
+      }
+      // warps meet only through mbarriers, whose waits are bounded: a warp that gives up leaves alone
+      bool got = warp_wait(&S.dfull[bb], (j >> 1) & 1);
+      if (j == ng) got = warp_wait(&S.mlready, 0) && got;
+      if (!got) {
         ok = false;
         break;
       }
+      if (j == ng) {
+        float mm = -CUDART_INF_F;
+#pragma unroll
+        for (int q = 0; q < kGroups; ++q) mm = fmaxf(mm, S.ml[q][0][r]);
+        float ll = 0.f;
+#pragma unroll
+        for (int q = 0; q < kGroups; ++q) {
+          const float mq = S.ml[q][0][r];
+          ll += mq == -CUDART_INF_F ? 0.f : S.ml[q][1][r] * fast_exp2(mq - mm);
+        }
+        lse2 = (r < p.rows && ll > 0.f) ? mm + log2f(ll) : CUDART_INF_F;
+      }
       tc_fence_after();
-      float ls8[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) ls8[k] = 0.f;
+      uint32_t sv[32];
+      if (live) {
+        tmem_ld32(lane_addr + 128 * bb, sv);
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.dfree[bb]);        // this warp's TMEM reads are done
+      // every row of the chunk sees every key of this group (all but the causal tail)
+      const bool full = key0 + 32 <= min(n, row_min + 1);
       if (!pass2) {
-        // the row maximum over the visible keys of this pair first, then the sum
-        float mx8[8];
+        if (!live) continue;
+        // the row maximum over the visible keys first (raw S; scale > 0), then the sum
+        float mx4[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = -CUDART_INF_F;
-        for (int c0 = 0; c0 < ncol; c0 += 32) {
-          uint32_t sv[32];
-          tmem_ld32(lane_addr + 128 * bb + c0, sv);
-          tmem_wait_ld();
+        for (int k = 0; k < 4; ++k) mx4[k] = -CUDART_INF_F;
+        if (full) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], __uint_as_float(sv[c]));
+        } else {
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const int key = key0 + c0 + c;
+            const int key = key0 + c;
             const bool vis = key < n && key <= row_pos;
-            mx8[c & 7] = fmaxf(mx8[c & 7], vis ? __uint_as_float(sv[c]) * scale : -CUDART_INF_F);
+            mx4[c & 3] = fmaxf(mx4[c & 3], vis ? __uint_as_float(sv[c]) : -CUDART_INF_F);
           }
         }
-        const float mb = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        const float mb = scale * fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         const float m_new = fmaxf(m, mb);
-        if (m_new != -CUDART_INF_F) {
-          l *= fast_exp2(m - m_new);   // m = -inf gives 0
-          m = m_new;
-        }
-        for (int c0 = 0; c0 < ncol; c0 += 32) {
-          uint32_t sv[32];
-          tmem_ld32(lane_addr + 128 * bb + c0, sv);
-          tmem_wait_ld();
+        if (m_new == -CUDART_INF_F) continue;          // nothing visible yet
+        float ls4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ls4[k] = 0.f;
+        if (full) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ls4[c & 3] += fast_exp2(fmaf(__uint_as_float(sv[c]), scale, -m_new));
+        } else {
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const int key = key0 + c0 + c;
-            const bool vis = key < n && key <= row_pos && m != -CUDART_INF_F;
-            ls8[c & 7] += vis ? fast_exp2(fmaf(__uint_as_float(sv[c]), scale, -m)) : 0.f;
+            const int key = key0 + c;
+            const bool vis = key < n && key <= row_pos;
+            ls4[c & 3] += vis ? fast_exp2(fmaf(__uint_as_float(sv[c]), scale, -m_new)) : 0.f;
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.dfree[bb]);
-        l += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+        l = l * fast_exp2(m - m_new) +                  // m = -inf gives 0
+            ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
+        m = m_new;
       } else {
-        // row r's probabilities of this pair into row r of the shared tile ...
-        float* prow = S.prob + r * kPRow;
-        for (int c0 = 0; c0 < ncol; c0 += 32) {
-          uint32_t sv[32];
-          tmem_ld32(lane_addr + 128 * bb + c0, sv);
-          tmem_wait_ld();
+        // row r's probabilities of these keys, summed over the warp's 32 rows by a butterfly:
+        // each step keeps half of the columns (the half named by one lane bit) and adds the
+        // partner lane's copy of them, so after five steps lane l holds key key0 + l
+        if (live) {
+          float v[32];                                     // rows past the chunk have lse2 = +inf
+          if (full) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int key = key0 + c0 + c;
-            const bool vis = key < n && key <= row_pos;   // rows >= alpha have lse2 = +inf
-            const float e = fast_exp2(fmaf(__uint_as_float(sv[c]), scale, -lse2));
-            prow[c0 + c] = vis ? e : 0.f;
+            for (int c = 0; c < 32; ++c) v[c] = fast_exp2(fmaf(__uint_as_float(sv[c]), scale, -lse2));
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const int key = key0 + c;
+              const bool vis = key < n && key <= row_pos;
+              const float e = fast_exp2(fmaf(__uint_as_float(sv[c]), scale, -lse2));
+              v[c] = vis ? e : 0.f;
+            }
+          }
+#pragma unroll
+          for (int w = 16; w >= 1; w >>= 1) {              // w = values kept after this step
+            const bool hi = (lane & w) != 0;
+#pragma unroll
+            for (int k = 0; k < w; ++k) {
+              const float send = hi ? v[k] : v[k + w];
+              const float keep = hi ? v[k + w] : v[k];
+              v[k] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+            }
+          }
+          const int slot = j % 3;
+          S.part[slot][quarter][32 * grp + lane] = v[0];
+          __syncwarp();
+          int last = 0;
+          if (lane == 0) {
+            __threadfence_block();                       // the partial sums before the count
+            last = atomicAdd(&S.cnt[slot][grp], 1) == 3;
+          }
+          if (__shfl_sync(0xffffffffu, last, 0)) {      // the group's last warp adds the four quarters
+            __threadfence_block();
+            const int cc = 32 * grp + lane;
+            const float sum = (S.part[slot][0][cc] + S.part[slot][1][cc]) + (S.part[slot][2][cc] + S.part[slot][3][cc]);
+            const int key = key0 + lane;                 // keys from n on are zeroed below
+            if (key < n) srow[key] = p.accumulate ? srow[key] + sum : sum;
+            __syncwarp();
+            if (lane == 0) S.cnt[slot][grp] = 0;        // reused three jobs later
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.dfree[bb]);
-        named_bar_sync(1, 128);
-        // ... then thread r sums column r (key key0 + r) over the alpha rows
-        if (r < ncol) {
-#pragma unroll 8
-          for (int row = 0; row < p.alpha; ++row) ls8[row & 7] += S.prob[row * kPRow + r];
-          const float sum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
-          const int key = key0 + r;
-          srow[key] = key < n ? sum : 0.f;
-        }
-        named_bar_sync(1, 128);   // the tile is rewritten by the next pair
       }
     }
     if (!ok && lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
-    // positions past the request's pages (all of them for a rejected request) are zero
-    for (int i = (valid_req ? np_b * kPageTokens : 0) + r; i < p.np_max * kPageTokens; i += kCM) srow[i] = 0.f;
+    // positions from the prompt's end on (all of them for a rejected request) are zero
+    if (!p.accumulate)
+      for (int i = (valid_req ? n : 0) + t; i < p.np_max * kPageTokens; i += kMathThreads) srow[i] = 0.f;
   }
 
   tc_fence_before();

@@ -114,6 +114,8 @@ struct ColScoreParams {
   const uint16_t* q;             // bf16 [B][alpha][Hq][128]: the last alpha rows of each prompt
   float* scores;                 // [B][Hq][np_max * 64]
   int B, alpha, Hq, Hk, G;
+  int row0, rows;                // this launch's chunk: window rows row0 .. row0 + rows - 1 (rows <= 128)
+  int accumulate;                // 0: write the chunk's sums (first chunk), 1: add them
   int64_t n_phys;
   const int32_t* page_table;     // [B][np_max]
   int np_max;

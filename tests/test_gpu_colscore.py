@@ -52,6 +52,30 @@ def test_column_scores_vs_oracle(n, alpha, Hq, Hk):
     _check(S, ref, alpha, n)
 
 
+@pytest.mark.parametrize("n,alpha", [(5000, 256), (64 * 4 + 7, 129), (64 * 6, 300)])
+def test_column_scores_windows_over_one_tile(n, alpha):
+    """Windows of more than 128 rows run as 128-row chunks whose column sums add; 5000 / 256 is
+    the prompt and window of the page's worked example."""
+    w = gen.sparse_workload(1, 8, 2, n, 4, 4, seed=n + alpha)
+    q = gen.rows_bf16(n, 324, alpha * 8).reshape(1, alpha, 8, 128)
+    S, err = _run(w, q)
+    items = np.array([0, 5], np.int32) if n > 1000 else None
+    ref = oracle.column_scores_batch(q, w["k_pool"], w["page_table"], w["seq_len"], w["np_max"] * 64, items=items)
+    assert err == (0, 0)
+    for it in (items if items is not None else range(8)):
+        _check(S[0, it], ref[0, it], alpha, n)
+
+
+def test_column_scores_window_limit():
+    w = gen.sparse_workload(1, 8, 2, 2048, 4, 4, seed=3)
+    d = Dev(w)
+    q = torch.zeros(1, 1025, 8, 128, dtype=torch.bfloat16, device=DEV)
+    out = torch.zeros(1, 8, w["np_max"] * 64, dtype=torch.float32, device=DEV)
+    with pytest.raises(spkv.SpkvError, match="UNSUPPORTED"):
+        spkv.attn_column_scores(d.cache, q, d.pt, i32(w["seq_len"]), out)
+    d.close()
+
+
 def test_column_scores_ragged_prompts_and_rejected_request():
     """Prompts of different lengths in one call; a prompt shorter than the window is rejected
     (error bit, zero row) without disturbing the others."""

@@ -425,8 +425,6 @@ def run_native(args):
     knew = [bf(gen.rows_bf16(rank, 9000 + i, U).reshape(B, Hk, 128)) for i in range(n_iter)]
     vnew = [bf(gen.rows_bf16(rank, 9500 + i, U).reshape(B, Hk, 128)) for i in range(n_iter)]
     # the step's own token sits at position L-1 (the last row of the local page)
-    app_phys = i32(w["page_table"][:, (L - 1) // 64])
-    app_tok = i32(np.full(B, (L - 1) % 64, np.int32))
 
     scores = torch.empty(B, Hk, npm, dtype=torch.float32, device=dev)
     alive = torch.full((B, Hk, (npm + 31) // 32), -1, dtype=torch.int32, device=dev)
@@ -453,8 +451,8 @@ def run_native(args):
     stream = torch.cuda.current_stream()
 
     def step(i):
-        spkv.paged_kv_append(cache, app_phys, app_tok, knew[i], vnew[i])
-        spkv.score_blocks(cache, qs[i], pt, seq, scores)
+        # the new token's K/V row at position L-1 and the block scores, one launch
+        spkv.decode_append_score(cache, knew[i], vnew[i], qs[i], pt, seq, scores)
         # select_topk + resident_setdiff + lru_bucket_update, fused into one kernel
         spkv.select_resident_update(cache, scores, evs[i], alive, seq, k_q, k_e, sel, n_sel, resident, ts, i, 1,
                                     missing, n_missing, slot, victims, hist)
@@ -616,8 +614,7 @@ def run_native(args):
         res16, ts16 = resident.clone(), ts.clone()
 
         def step16(i):
-            spkv.paged_kv_append(cache16, app_phys, app_tok, knew[i], vnew[i])
-            spkv.score_blocks(cache16, qs[i], pt, seq, scores)
+            spkv.decode_append_score(cache16, knew[i], vnew[i], qs[i], pt, seq, scores)
             spkv.select_resident_update(cache16, scores, evs[i], alive16, seq, k_q, k_e, sel, n_sel, res16, ts16,
                                         i, 1, missing, n_missing, slot, victims, hist)
             spkv.sparse_decode_attn(cache16, qs[i], pt, sel, n_sel, seq, out, lse)
@@ -708,8 +705,7 @@ def run_native(args):
         e_d.copy_(e_h[s_], non_blocking=True)
         k_d.copy_(k_h[s_], non_blocking=True)
         v_d.copy_(v_h[s_], non_blocking=True)
-        spkv.paged_kv_append(cache, app_phys, app_tok, k_d, v_d)
-        spkv.score_blocks(cache, q_d, pt, seq, scores)
+        spkv.decode_append_score(cache, k_d, v_d, q_d, pt, seq, scores)
         spkv.select_resident_update(cache, scores, e_d, alive, seq, k_q, k_e, sel, n_sel, resident, ts, 1000 + i,
                                     1, missing, n_missing, slot, victims, hist)
         spkv.sparse_decode_attn(cache, q_d, pt, sel, n_sel, seq, out, lse)
@@ -753,7 +749,7 @@ def run_native(args):
                        "page": 64, "subblock": 16, "k_q": k_q, "k_e": k_e, "resident_slots": N_SLOTS,
                        "step": "append+score+select+setdiff+lru+sparse_attn",
                        "launch": ("one CUDA graph per step (kernels chained by programmatic dependent launch); "
-                                  "select + setdiff + lru as one fused kernel"),
+                                  "append + score as one kernel, select + setdiff + lru as one fused kernel"),
                        "bytes_per_step": {kk: int(v) for kk, v in byts.items()},
                        "l2": ("no flush: each step reads ~0.81 GB of K/V pages and pooled-key sums, more "
                               "than the 129 MB L2, through evict-first loads" if args.l2 == "none" else
@@ -772,7 +768,7 @@ def run_native(args):
             "offload": offload,
             "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": 6 * args.steps,
+            "gpu_launches": 4 * args.steps,
             "eager_ms_per_step": eager_ms,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,

@@ -5,6 +5,7 @@
  *
  *   paged_kv_append      write the new token's K/V rows, refresh the pooled-key summaries
  *   score_blocks         block scores from the pooled keys (two-stage pooling)
+ *   decode_append_score  a decode step's paged_kv_append + score_blocks in one launch
  *   select_topk          per-KV-head top-k pages: eviction-head budget k_e + query budget k_q
  *   resident_setdiff     selected pages that are not resident (swap-in list)
  *   lru_bucket_update    64-bucket LRU recency update and victim choice
@@ -136,6 +137,22 @@ int paged_kv_append(spkv_cache_t cache, const int32_t* phys_page, const int32_t*
  *   scores     : device fp32 [B][n_kv_heads][np_max] (output) */
 int score_blocks(spkv_cache_t cache, const void* q, int B, int Hq, const int32_t* page_table,
                  int np_max, const int32_t* seq_len, float* scores, void* stream);
+
+/* A decode step's append and scoring in one launch: exactly paged_kv_append of each request's new
+ * row at position seq_len[b] - 1 (physical page page_table[b][(seq_len[b] - 1) / 64], row
+ * (seq_len[b] - 1) % 64, all kv heads), followed by score_blocks with the same arguments.  The two
+ * run concurrently, which is exact because score_blocks never reads a request's local page (the
+ * one holding position seq_len[b] - 1).  Requires that no two requests share that physical page
+ * (the usual copy-on-write rule for the page being written).  [NOSA] "Method 2: NOSI", kernel
+ * fusion: pooling produced where K is written.
+ *   k_new, v_new : device bf16 [B][n_kv_heads][128], 4-byte aligned
+ *   q, page_table, np_max, seq_len, scores : as score_blocks (seq_len counts the new token)
+ * A local page outside [0, n_phys_pages) sets SPKV_DEVERR_PHYS and that request's row is not
+ * written; (seq_len[b] - 1) / 64 >= np_max sets SPKV_DEVERR_PAGE_ID.  The handle must have
+ * summaries.  B * n_kv_heads <= 65535. */
+int decode_append_score(spkv_cache_t cache, const void* k_new, const void* v_new, const void* q, int B, int Hq,
+                        const int32_t* page_table, int np_max, const int32_t* seq_len, float* scores,
+                        void* stream);
 
 /* Dual top-k page selection, [NOSA] "Method 1": dual selection (Gamma_q query-aware,
  * Gamma_e query-agnostic eviction head), locality guarantee, ED-DMA (pages are ranked on the

@@ -29,7 +29,8 @@ import torch
 
 from ._abi import DEVERR, SpkvDesc, SpkvError, check, load
 
-__all__ = ["PagedKVCache", "paged_kv_create", "paged_kv_append", "score_blocks", "select_topk",
+__all__ = ["PagedKVCache", "paged_kv_create", "paged_kv_append", "score_blocks", "decode_append_score",
+           "select_topk",
            "sparse_decode_attn", "lazy_rope_decode_attn", "resident_setdiff", "lru_bucket_update",
            "select_resident_update", "retrieve_pages", "sparse_decode_attn_slots", "lazy_rope_prefill_attn",
            "attn_column_scores",
@@ -137,6 +138,20 @@ def score_blocks(cache: PagedKVCache, q, page_table, seq_len, scores, stream=Non
     np_max = page_table.shape[1]
     check("score_blocks", load().score_blocks(
         cache.handle, _t(q, torch.bfloat16, "q", (B, Hq, HEAD_DIM)), B, Hq,
+        _t(page_table, torch.int32, "page_table", (B, np_max)), np_max,
+        _t(seq_len, torch.int32, "seq_len", (B,)),
+        _t(scores, torch.float32, "scores", (B, cache.n_kv_heads, np_max)), _stream(stream)))
+
+
+def decode_append_score(cache: PagedKVCache, k_new, v_new, q, page_table, seq_len, scores, stream=None):
+    """paged_kv_append of each request's new row at position seq_len[b] - 1 (its local page) and
+    score_blocks, in one launch.  k_new, v_new: bf16 [B][Hk][128]."""
+    B, Hq = q.shape[0], q.shape[1]
+    np_max = page_table.shape[1]
+    shp = (B, cache.n_kv_heads, HEAD_DIM)
+    check("decode_append_score", load().decode_append_score(
+        cache.handle, _t(k_new, torch.bfloat16, "k_new", shp), _t(v_new, torch.bfloat16, "v_new", shp),
+        _t(q, torch.bfloat16, "q", (B, Hq, HEAD_DIM)), B, Hq,
         _t(page_table, torch.int32, "page_table", (B, np_max)), np_max,
         _t(seq_len, torch.int32, "seq_len", (B,)),
         _t(scores, torch.float32, "scores", (B, cache.n_kv_heads, np_max)), _stream(stream)))

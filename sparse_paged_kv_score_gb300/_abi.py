@@ -30,6 +30,7 @@ SIGNATURES = {
     "paged_kv_create": ([ctypes.POINTER(SpkvDesc), _vp, ctypes.POINTER(_vp)], _i32),
     "paged_kv_append": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp], _i32),
     "score_blocks": ([_vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _vp], _i32),
+    "decode_append_score": ([_vp, _vp, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _vp], _i32),
     "select_topk": ([_vp, _vp, _vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _vp, _vp], _i32),
     "sparse_decode_attn": ([_vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _vp], _i32),
     "lazy_rope_decode_attn": ([_vp, _vp, _i32, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _f32, _vp, _vp,

@@ -193,6 +193,18 @@ int score_blocks(spkv_cache_t c, const void* q, int B, int Hq, const int32_t* pa
   return status_of(spkv::launch_score(c, q, B, Hq, page_table, np_max, seq_len, scores, as_stream(stream)));
 }
 
+int decode_append_score(spkv_cache_t c, const void* k_new, const void* v_new, const void* q, int B, int Hq,
+                        const int32_t* page_table, int np_max, const int32_t* seq_len, float* scores, void* stream) {
+  int st = check_group(c, B, Hq);
+  if (st != SPKV_OK) return st;
+  if (!c->d.ksum) return SPKV_EINVAL;
+  if (B == 0) return SPKV_OK;
+  if (!q || !page_table || !seq_len || !scores || np_max <= 0 || !aligned(q, 8)) return SPKV_EINVAL;
+  if (!k_new || !v_new || !aligned(k_new, 4) || !aligned(v_new, 4)) return SPKV_EINVAL;
+  return status_of(spkv::launch_score(c, q, B, Hq, page_table, np_max, seq_len, scores, as_stream(stream), k_new,
+                                      v_new));
+}
+
 int select_topk(spkv_cache_t c, const float* q_scores, const float* evict_scores, uint32_t* alive, int B, int np_max,
                 const int32_t* seq_len, int k_q, int k_e, int32_t* sel, int32_t* n_sel, void* stream) {
   if (!c || B < 0) return SPKV_EINVAL;

@@ -127,8 +127,19 @@ struct ColScoreParams {
 cudaError_t launch_summary_build(const spkv_cache* c, cudaStream_t st);
 cudaError_t launch_append(const spkv_cache* c, const int32_t* phys, const int32_t* tok, const void* k_new,
                           const void* v_new, int n_rows, cudaStream_t st);
+// The fused decode append's pointers (k_new, v_new: bf16 [B][Hk][128] as 32-bit words).
+struct AppendRows {
+  uint32_t* kpool;
+  uint32_t* vpool;
+  int32_t* page_cnt;
+  const uint32_t* k_new;
+  const uint32_t* v_new;
+};
+
+// k_new == nullptr: scores only; else the decode append of each request's new row is fused in.
 cudaError_t launch_score(const spkv_cache* c, const void* q, int B, int Hq, const int32_t* page_table,
-                         int np_max, const int32_t* seq_len, float* scores, cudaStream_t st);
+                         int np_max, const int32_t* seq_len, float* scores, cudaStream_t st,
+                         const void* k_new = nullptr, const void* v_new = nullptr);
 cudaError_t launch_select(const spkv_cache* c, const float* qs, const float* es, uint32_t* alive, int B,
                           int np_max, const int32_t* seq_len, int k_q, int k_e, int32_t* sel, int32_t* n_sel,
                           cudaStream_t st);

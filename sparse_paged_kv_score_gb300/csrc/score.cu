@@ -7,10 +7,15 @@
 // The group's sub-block scores are summed before the max; by linearity the kernel forms the
 // summed query once.  This pass is bound by HBM: it reads 2 KiB of fp32 summary per page-head
 // (1 KiB with bf16 summaries: [Spin] 2C, cheaper scoring at long context).
+//
+// The fused decode form adds one block column that appends each request's new token (position
+// seq_len - 1, in the request's local page) and refreshes that sub-block's sum.  The scores never
+// read the local page, so doing both in one launch gives exactly append-then-score.
 #include <math_constants.h>
 
 #include "common.cuh"
 #include "internal.h"
+#include "summary.cuh"
 
 namespace spkv {
 namespace {
@@ -35,14 +40,50 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// The new K/V row of unit (b, h) into the request's local page, then that sub-block's sum again
+// (threads 0..63: thread i owns dims 2i, 2i+1).  Each request's local page is its own, so the
+// page count read here is the old one or already raised by head 0: the count used is the same.
 template <bool BF16>
+__device__ void append_local_row(const AppendRows& a, const int32_t* page_table, const int32_t* seq_len, void* ksum,
+                                 int np_max, int64_t n_phys, int b, int h, int Hk, uint32_t* err) {
+  const int i = threadIdx.x;
+  if (i >= kHeadDim / 2) return;
+  const int L = seq_len[b];
+  if (L < 1) return;                                  // flagged by the scoring blocks
+  const int pg = (L - 1) / kPageTokens, t = (L - 1) % kPageTokens;
+  if (pg >= np_max) {
+    if (i == 0) flag_error(err, SPKV_DEVERR_PAGE_ID);
+    return;
+  }
+  const int p = page_table[int64_t(b) * np_max + pg];
+  if (p < 0 || p >= n_phys) {
+    if (i == 0) flag_error(err, SPKV_DEVERR_PHYS);
+    return;
+  }
+  const int64_t ph = int64_t(h) * n_phys + p;
+  const int64_t src = (int64_t(b) * Hk + h) * (kHeadDim / 2) + i;
+  uint32_t* pw = a.kpool + ph * (kPageTokens * kHeadDim / 2);
+  pw[t * (kHeadDim / 2) + i] = a.k_new[src];
+  a.vpool[ph * (kPageTokens * kHeadDim / 2) + t * (kHeadDim / 2) + i] = a.v_new[src];
+  int cnt = a.page_cnt[p];
+  if (h == 0 && i == 0) atomicMax(&a.page_cnt[p], t + 1);
+  cnt = max(0, min(kPageTokens, max(cnt, t + 1)));
+  const int j = t / kSubblock;                        // this thread reads back its own word of row t
+  store_pair<BF16>(ksum, (ph * kNSub + j) * (kHeadDim / 2) + i, subblock_sum(pw, j, cnt, i));
+}
+
+template <bool BF16, bool APPEND>
 __global__ void __launch_bounds__(kWarps * 32)
     score_kernel(const uint32_t* __restrict__ q, const void* __restrict__ ksum, const int32_t* __restrict__ page_table,
                  const int32_t* __restrict__ seq_len, float* __restrict__ scores, int Hq, int Hk, int G, int np_max,
-                 int64_t n_phys, float scale, uint32_t* err) {
+                 int64_t n_phys, float scale, uint32_t* err, AppendRows app) {
   pdl_wait();
   pdl_trigger();
   const int u = blockIdx.y, b = u / Hk, h = u % Hk;
+  if (APPEND && blockIdx.x == gridDim.x - 1) {
+    append_local_row<BF16>(app, page_table, seq_len, const_cast<void*>(ksum), np_max, n_phys, b, h, Hk, err);
+    return;
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int p_begin = blockIdx.x * kPagesPerBlock;
   const int p_end = min(np_max, p_begin + kPagesPerBlock);
@@ -109,14 +150,20 @@ __global__ void __launch_bounds__(kWarps * 32)
 }  // namespace
 
 cudaError_t launch_score(const spkv_cache* c, const void* q, int B, int Hq, const int32_t* page_table, int np_max,
-                         const int32_t* seq_len, float* scores, cudaStream_t st) {
+                         const int32_t* seq_len, float* scores, cudaStream_t st, const void* k_new,
+                         const void* v_new) {
   const int Hk = c->d.n_kv_heads;
   const int G = Hq / Hk;
-  dim3 grid((np_max + kPagesPerBlock - 1) / kPagesPerBlock, B * Hk);
+  const bool append = k_new != nullptr;
+  dim3 grid((np_max + kPagesPerBlock - 1) / kPagesPerBlock + (append ? 1 : 0), B * Hk);
   const float scale = static_cast<float>(1.0 / (16.0 * 11.313708498984760390));  // 1 / (16 sqrt(128))
-  return launch_pdl(c->d.ksum_bf16 ? score_kernel<true> : score_kernel<false>, grid, dim3(kWarps * 32), 0, st,
-                    static_cast<const uint32_t*>(q), static_cast<const void*>(c->d.ksum), page_table, seq_len, scores,
-                    Hq, Hk, G, np_max, static_cast<int64_t>(c->d.n_phys_pages), scale, c->dev_err);
+  AppendRows app{static_cast<uint32_t*>(c->d.k_pool), static_cast<uint32_t*>(c->d.v_pool), c->d.page_cnt,
+                 static_cast<const uint32_t*>(k_new), static_cast<const uint32_t*>(v_new)};
+  auto kern = c->d.ksum_bf16 ? (append ? score_kernel<true, true> : score_kernel<true, false>)
+                             : (append ? score_kernel<false, true> : score_kernel<false, false>);
+  return launch_pdl(kern, grid, dim3(kWarps * 32), 0, st, static_cast<const uint32_t*>(q),
+                    static_cast<const void*>(c->d.ksum), page_table, seq_len, scores, Hq, Hk, G, np_max,
+                    static_cast<int64_t>(c->d.n_phys_pages), scale, c->dev_err, app);
 }
 
 }  // namespace spkv

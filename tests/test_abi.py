@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_header_declares_the_decode_path():
     names = declared_functions()
-    for f in ["paged_kv_create", "paged_kv_append", "score_blocks", "select_topk", "sparse_decode_attn",
+    for f in ["paged_kv_create", "paged_kv_append", "score_blocks", "decode_append_score", "select_topk", "sparse_decode_attn",
               "lazy_rope_decode_attn", "resident_setdiff", "lru_bucket_update", "spkv_get_device_error",
               "paged_kv_destroy", "spkv_status_string", "spkv_pack_page_words", "spkv_sm_count",
               "retrieve_pages", "sparse_decode_attn_slots", "select_resident_update",

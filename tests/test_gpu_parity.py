@@ -77,6 +77,61 @@ def test_append_equals_rebuild(summary_bf16):
     fresh.close()
 
 
+@pytest.mark.parametrize("summary_bf16", [False, True])
+def test_decode_append_score_equals_append_then_score(summary_bf16):
+    """The fused decode call gives bitwise the pools, page counts, summaries and scores of
+    paged_kv_append at position seq_len - 1 followed by score_blocks, over steps that cross a page
+    boundary (a token landing in row 0 of a fresh page)."""
+    B, Hk, Hq = 3, 2, 8
+    w = gen.sparse_workload(B, Hq, Hk, 64 * 3 - 2, 4, 4, seed=6, extra_tokens=70)
+    two, one = Dev(w, summary_bf16=summary_bf16), Dev(w, summary_bf16=summary_bf16)
+    L = w["seq_len"].copy()
+    for step in range(4):
+        L1 = L + 1                               # seq_len counts the new token
+        phys = np.array([w["page_table"][b, L[b] // 64] for b in range(B)], np.int32)
+        kn = bf(gen.rows_bf16(10, 100 + step, B * Hk).reshape(B, Hk, 128))
+        vn = bf(gen.rows_bf16(10, 200 + step, B * Hk).reshape(B, Hk, 128))
+        q = bf(gen.rows_bf16(10, 300 + step, B * Hq).reshape(B, Hq, 128))
+        s_two = torch.empty(B, Hk, w["np_max"], dtype=torch.float32, device=DEV)
+        s_one = torch.empty_like(s_two)
+        spkv.paged_kv_append(two.cache, i32(phys), i32((L % 64).astype(np.int32)), kn, vn)
+        spkv.score_blocks(two.cache, q, two.pt, i32(L1), s_two)
+        spkv.decode_append_score(one.cache, kn, vn, q, one.pt, i32(L1), s_one)
+        assert torch.equal(s_two, s_one)
+        L = L1
+    torch.cuda.synchronize()
+    assert torch.equal(two.k_pool.view(torch.int16), one.k_pool.view(torch.int16))
+    assert torch.equal(two.v_pool.view(torch.int16), one.v_pool.view(torch.int16))
+    assert torch.equal(two.cnt, one.cnt)
+    assert torch.equal(two.ksum, one.ksum)
+    assert two.errors() == (0, 0) and one.errors() == (0, 0)
+    two.close()
+    one.close()
+
+
+def test_decode_append_score_bad_local_page_flags_and_skips():
+    B, Hk, Hq = 3, 2, 8
+    w = gen.sparse_workload(B, Hq, Hk, 64 * 2 + 9, 4, 4, seed=8)
+    d = Dev(w)
+    before = d.k_pool.clone()
+    pt = w["page_table"].copy()
+    local = (w["seq_len"] - 1) // 64
+    pt[1, local[1]] = w["n_phys"]                # request 1's local page is out of range
+    kn = bf(gen.rows_bf16(11, 1, B * Hk).reshape(B, Hk, 128))
+    vn = bf(gen.rows_bf16(11, 2, B * Hk).reshape(B, Hk, 128))
+    s = torch.empty(B, Hk, w["np_max"], dtype=torch.float32, device=DEV)
+    spkv.decode_append_score(d.cache, kn, vn, d.q, i32(pt), d.L, s)
+    st, bits = d.errors()
+    assert bits == spkv.DEVERR["PHYS"]
+    changed = (d.k_pool.view(torch.int16) != before.view(torch.int16)).any(-1).nonzero().cpu().numpy()
+    # only the rows at position seq_len - 1 of requests 0 and 2 changed (every kv head)
+    want = sorted((h, int(w["page_table"][b, local[b]]), int((w["seq_len"][b] - 1) % 64))
+                  for b in (0, 2) for h in range(Hk))
+    assert sorted(map(tuple, changed.tolist())) == want
+    assert torch.equal(s, d.scores())            # scores are unaffected by the append
+    d.close()
+
+
 # ------------------------------------------------------------------ block scores
 
 def _score_bound(w):

@@ -255,6 +255,7 @@ def lazy_rag(seed: int = 0, B: int = 64, Hq: int = 32, Hk: int = 8, n_docs: int 
     phys = np.full((B, np_max), -1, np.int32)
     valid = np.zeros((B, np_max), np.int32)
     slot = np.zeros((B, np_max), np.int32)
+    page_start = np.zeros((B, np_max), np.int32)   # document-local position of each page's first token
     doc_pos = np.zeros((B, docs_per_req), np.int32)
     qpos = np.zeros(B, np.int32)
     for b in range(B):
@@ -266,6 +267,7 @@ def lazy_rag(seed: int = 0, B: int = 64, Hq: int = 32, Hk: int = 8, n_docs: int 
                 phys[b, j] = doc_phys[d][p]
                 valid[b, j] = min(PAGE, L - PAGE * p)
                 slot[b, j] = i
+                page_start[b, j] = PAGE * p
                 j += 1
             pos += L
         qpos[b] = pos
@@ -279,6 +281,6 @@ def lazy_rag(seed: int = 0, B: int = 64, Hq: int = 32, Hk: int = 8, n_docs: int 
             cnt[doc_phys[d][p]] = min(PAGE, int(doc_len[d]) - PAGE * p)
     return dict(name=f"lazy-RoPE RAG decode B{B} Hq{Hq}/Hk{Hk} {n_docs} docs x{docs_per_req} Zipf({zipf_s})",
                 B=B, Hq=Hq, Hk=Hk, G=Hq // Hk, D=HEAD_DIM, T=PAGE, n_phys=n_phys, np_max=np_max,
-                k_pool=k_pool, v_pool=v_pool, q=q, phys=phys, valid=valid, slot=slot,
+                k_pool=k_pool, v_pool=v_pool, q=q, phys=phys, valid=valid, slot=slot, page_start=page_start,
                 n_pages=n_pages, doc_pos=doc_pos, qpos=qpos, theta=theta, picks=picks,
                 doc_len=doc_len, page_cnt=cnt, max_docs=docs_per_req, seed=seed)

@@ -68,6 +68,8 @@ def _l():
             "orc_lru_batch": ([vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, i32], None),
             "orc_lazy_prefill_batch": ([i32, i32, i32, i32, vp, vp, vp, i64, vp, vp, vp, i32, vp, i32, vp, vp,
                                         i32, f64, i32, vp, i32, vp, vp, i32], None),
+            "orc_alibi_prefill_batch": ([i32, i32, i32, i32, vp, vp, vp, i64, vp, vp, vp, vp, i32, vp, i32, vp,
+                                         vp, i32, vp, vp, i32, vp, vp, i32], None),
             "orc_column_scores_batch": ([i32, i32, i32, i32, vp, vp, i64, vp, i32, vp, i32, vp, i32, vp, i32],
                                         None),
             "orc_retrieve_unit": ([vp, vp, vp, vp, i32, vp, vp, i32, vp, vp], None),
@@ -356,6 +358,30 @@ def lazy_prefill_batch(q, k_pool, v_pool, phys, valid, slot, n_pages, qpos0, doc
                                 _p(slot), phys.shape[1], _p(n_pages), phys.shape[2], _p(qpos0), _p(doc_pos),
                                 doc_pos.shape[1], float(theta), int(bool(materialise)), _p(it), it.shape[0],
                                 _p(out), _p(lse), nthreads)
+    return out, lse
+
+
+def alibi_prefill_batch(q, k_pool, v_pool, phys, valid, slot, page_start, n_pages, qpos0, doc_pos, slopes,
+                        items=None, nthreads: int = 0):
+    """ALiBi prefill over cached documents: like lazy_prefill_batch with the linear position bias
+    -slopes[hq] * (n - m) instead of the rotation; page_start (document-local position of each
+    listed page's first token) has the shape of phys; slopes [Hq] (fp32).  Returns (out, lse)."""
+    q, k_pool, v_pool = _c(q, np.uint16), _c(k_pool, np.uint16), _c(v_pool, np.uint16)
+    if phys.ndim == 2:
+        phys, valid, slot, page_start = phys[:, None, :], valid[:, None, :], slot[:, None, :], page_start[:, None, :]
+    phys, valid, slot, page_start = (_c(phys, np.int32), _c(valid, np.int32), _c(slot, np.int32),
+                                     _c(page_start, np.int32))
+    n_pages, qpos0, doc_pos = _c(n_pages, np.int32), _c(qpos0, np.int32), _c(doc_pos, np.int32)
+    slopes = _c(slopes, np.float32)
+    B, T, Hq, _ = q.shape
+    Hk, n_phys = k_pool.shape[0], k_pool.shape[1]
+    out = np.zeros((B, T, Hq, D), np.float64)
+    lse = np.zeros((B, T, Hq), np.float64)
+    it = _units(items, B * T * Hk)
+    _l().orc_alibi_prefill_batch(B, T, Hq, Hk, _p(q), _p(k_pool), _p(v_pool), n_phys, _p(phys), _p(valid),
+                                 _p(slot), _p(page_start), phys.shape[1], _p(n_pages), phys.shape[2], _p(qpos0),
+                                 _p(doc_pos), doc_pos.shape[1], _p(slopes), _p(it), it.shape[0], _p(out), _p(lse),
+                                 nthreads)
     return out, lse
 
 

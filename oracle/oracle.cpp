@@ -548,6 +548,73 @@ void orc_lazy_prefill_batch(int B, int T, int Hq, int Hk, const uint16_t* q, con
   });
 }
 
+// ---------------------------------------------------------------- ALiBi prefill
+// [Lazy] "Key contributions" 4 (the mechanism carries over to other relative position encodings,
+// ALiBi among them), reading R18: keys are stored with no positional transform; the key at
+// document-local position page_start[i] + t of document slot[i], placed at token offset
+// doc_pos[slot[i]], sits at m = doc_pos[slot[i]] + page_start[i] + t; the query row at position
+// n scores it as q . k / sqrt(128) - slope * (n - m) (the linear bias of ALiBi, one slope per
+// query head, natural-log units), and plain softmax attention follows.  No mask (as the RoPE
+// prefill).  q: G query heads of 128 bf16; slopes: their G slopes.
+void orc_alibi_attn_unit(const uint16_t* q, int G, const float* slopes, const uint16_t* kplane,
+                         const uint16_t* vplane, const int32_t* phys, const int32_t* valid, const int32_t* slot,
+                         const int32_t* page_start, int n_pages, int32_t qpos, const int32_t* doc_pos,
+                         double* out, double* lse) {
+  const double inv_sqrt_d = 1.0 / std::sqrt(static_cast<double>(kD));
+  std::vector<double> z;
+  for (int g = 0; g < G; ++g) {
+    const double slope = slopes[g];
+    z.clear();
+    for (int i = 0; i < n_pages; ++i)
+      for (int t = 0; t < valid[i]; ++t) {
+        const uint16_t* k = row_ptr(kplane, phys[i], t);
+        double dot = 0.0;
+        for (int d = 0; d < kD; ++d) dot += from_bf16(q[g * kD + d]) * from_bf16(k[d]);
+        const double m = static_cast<double>(doc_pos[slot[i]]) + page_start[i] + t;
+        z.push_back(dot * inv_sqrt_d - slope * (static_cast<double>(qpos) - m));
+      }
+    for (int d = 0; d < kD; ++d) out[g * kD + d] = 0.0;
+    if (z.empty()) {
+      lse[g] = kNegInf;
+      continue;
+    }
+    const double mx = *std::max_element(z.begin(), z.end());
+    double l = 0.0;
+    for (double x : z) l += std::exp(x - mx);
+    size_t idx = 0;
+    for (int i = 0; i < n_pages; ++i)
+      for (int t = 0; t < valid[i]; ++t, ++idx) {
+        const double w = std::exp(z[idx] - mx) / l;
+        const uint16_t* v = row_ptr(vplane, phys[i], t);
+        for (int d = 0; d < kD; ++d) out[g * kD + d] += w * from_bf16(v[d]);
+      }
+    lse[g] = mx + std::log(l);
+  }
+}
+
+// ALiBi prefill batch: the prefill of orc_lazy_prefill_batch with the bias above instead of the
+// rotation; page_start is [B][meta_heads][np_max] like phys, slopes is [Hq].
+void orc_alibi_prefill_batch(int B, int T, int Hq, int Hk, const uint16_t* q, const uint16_t* kpool,
+                             const uint16_t* vpool, int64_t n_phys, const int32_t* phys, const int32_t* valid,
+                             const int32_t* slot, const int32_t* page_start, int meta_heads,
+                             const int32_t* n_pages, int np_max, const int32_t* qpos0, const int32_t* doc_pos,
+                             int max_docs, const float* slopes, const int32_t* items, int n_items, double* out,
+                             double* lse, int nthreads) {
+  (void)B;
+  const int G = Hq / Hk;
+  for_units(n_items, nthreads, [&](int i) {
+    const int it = items[i];
+    const int h = it % Hk, bt = it / Hk, t = bt % T, b = bt / T;
+    const int mh = meta_heads == 1 ? 0 : h;
+    const int64_t mo = (static_cast<int64_t>(b) * meta_heads + mh) * np_max;
+    const int64_t plane = static_cast<int64_t>(h) * n_phys * kPage * kD;
+    const int64_t qo = static_cast<int64_t>(bt) * Hq + h * G;
+    orc_alibi_attn_unit(q + qo * kD, G, slopes + h * G, kpool + plane, vpool + plane, phys + mo, valid + mo,
+                        slot + mo, page_start + mo, n_pages[b], qpos0[b] + t,
+                        doc_pos + static_cast<int64_t>(b) * max_docs, out + qo * kD, lse + qo);
+  });
+}
+
 // ---------------------------------------------------------------- column score S
 // [FA] "2. Attention modification" (the PyramidKV-style sparsification score, reading R16): the
 // last alpha rows of a prompt of n tokens, at positions n - alpha + j, attend causally over the

@@ -574,6 +574,91 @@ def test_prefill_rows_are_decode_queries():
         assert np.array_equal(out[:, t], od) and np.array_equal(lse[:, t], ld)
 
 
+# ------------------------------------------------------------------------------ ALiBi prefill
+
+def _alibi_args(w):
+    return (w["k_pool"], w["v_pool"], w["phys"], w["valid"], w["slot"], w["page_start"], w["n_pages"])
+
+
+def _plain_prefill(w, q):
+    """Dense softmax attention over every listed key (no position term), scipy."""
+    B, T, Hq, _ = q.shape
+    G = Hq // w["Hk"]
+    out, lse = np.zeros((B, T, Hq, 128)), np.zeros((B, T, Hq))
+    for b in range(B):
+        n = w["n_pages"][b]
+        for h in range(w["Hk"]):
+            K = np.concatenate([f(w["k_pool"][h, w["phys"][b, i], :w["valid"][b, i]]) for i in range(n)])
+            V = np.concatenate([f(w["v_pool"][h, w["phys"][b, i], :w["valid"][b, i]]) for i in range(n)])
+            for t in range(T):
+                for g in range(G):
+                    z = K @ f(q[b, t, h * G + g]) / math.sqrt(128)
+                    out[b, t, h * G + g] = softmax(z) @ V
+                    lse[b, t, h * G + g] = logsumexp(z)
+    return out, lse
+
+
+def test_alibi_zero_slope_is_plain_attention_and_nonzero_slopes_are_not():
+    w, q = _prefill_case(8, T=3)
+    slopes = np.array([0.0, 0.05, 0.0, 0.25], np.float32)
+    out, lse = oracle.alibi_prefill_batch(q, *_alibi_args(w), w["qpos"], w["doc_pos"], slopes)
+    ro, rl = _plain_prefill(w, q)
+    for hq in (0, 2):
+        assert np.abs(out[:, :, hq] - ro[:, :, hq]).max() < 1e-10
+        assert np.abs(lse[:, :, hq] - rl[:, :, hq]).max() < 1e-10
+    for hq in (1, 3):
+        assert np.abs(out[:, :, hq] - ro[:, :, hq]).max() > 1e-3
+
+
+def test_alibi_two_equal_keys_closed_form():
+    """Two keys with the same K row at positions m0 < m1 and a query at n: their weights are in the
+    ratio exp(-s (n - m0)) : exp(-s (n - m1)), so out = (v0 + e^{s (m1 - m0)} v1) / (1 + e^{s (m1 - m0)})
+    and lse = q.k / sqrt(128) - s (n - m1) + log(1 + e^{-s (m1 - m0)})."""
+    k = gen.rows_bf16(9, 1, 1)[0]
+    v = gen.rows_bf16(9, 2, 2)
+    k_pool = np.zeros((1, 2, 64, 128), np.uint16)
+    v_pool = np.zeros((1, 2, 64, 128), np.uint16)
+    k_pool[0, 1, 0] = k_pool[0, 1, 1] = k                      # page 1 holds the two tokens
+    v_pool[0, 1, 0], v_pool[0, 1, 1] = v[0], v[1]
+    q = gen.rows_bf16(9, 3, 1).reshape(1, 1, 1, 128)
+    phys, valid, slot = np.array([[1]]), np.array([[2]]), np.array([[0]])
+    page_start, doc_pos, qpos = np.array([[10]]), np.array([[100]]), np.array([500])
+    s = 0.0625                                                 # exact in fp32
+    out, lse = oracle.alibi_prefill_batch(q, k_pool, v_pool, phys, valid, slot, page_start, np.array([1]), qpos,
+                                          doc_pos, np.array([s], np.float32))
+    m0, m1, n = 110.0, 111.0, 500.0
+    r = math.exp(s * (m1 - m0))
+    want = (f(v[0]) + r * f(v[1])) / (1 + r)
+    qk = float(f(q[0, 0, 0]) @ f(k)) / math.sqrt(128)
+    assert np.abs(out[0, 0, 0] - want).max() < 1e-12
+    assert abs(lse[0, 0, 0] - (qk - s * (n - m1) + math.log1p(math.exp(-s * (m1 - m0))))) < 1e-10
+
+
+def test_alibi_positions_not_list_order():
+    """Shifting the rows and every document by the same offset changes nothing (distance only);
+    listing the pages in another order changes nothing (positions come from doc_pos and
+    page_start); moving one page's start does."""
+    w, q = _prefill_case(10, T=2)
+    slopes = np.array([0.01, 0.03, 0.1, 0.5], np.float32)
+    o1, l1 = oracle.alibi_prefill_batch(q, *_alibi_args(w), w["qpos"], w["doc_pos"], slopes)
+    o2, l2 = oracle.alibi_prefill_batch(q, *_alibi_args(w), w["qpos"] + 777, w["doc_pos"] + 777, slopes)
+    assert np.abs(o1 - o2).max() < 1e-9 and np.abs(l1 - l2).max() < 1e-9
+    perm_w = dict(w)
+    for key in ("phys", "valid", "slot", "page_start"):
+        a = w[key].copy()
+        for b in range(w["B"]):
+            n = w["n_pages"][b]
+            a[b, :n] = w[key][b, gen.permutation(10, 40 + b, n)]
+        perm_w[key] = a
+    o3, l3 = oracle.alibi_prefill_batch(q, *_alibi_args(perm_w), w["qpos"], w["doc_pos"], slopes)
+    assert np.abs(o1 - o3).max() < 1e-12 and np.abs(l1 - l3).max() < 1e-12
+    ps = w["page_start"].copy()
+    ps[0, 1] += 5
+    moved = dict(w, page_start=ps)
+    o4, _ = oracle.alibi_prefill_batch(q, *_alibi_args(moved), w["qpos"], w["doc_pos"], slopes)
+    assert np.abs(o1 - o4).max() > 1e-6
+
+
 # ------------------------------------------------------------------------------ bf16 summaries
 
 def test_round_bf16_matches_the_generator_rounding():

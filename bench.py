@@ -586,11 +586,26 @@ def run_native(args):
             flops = 4.0 * 128 * Tq * Hqr * keys   # QK^T and PV, 2 flops per multiply-add each
             tflops = flops / (pre_ms * 1e-3) / 1e12
             tpeak, tkind = bf16_peak()
+            # the same prefill for ALiBi models: unrotated keys, bias -slope * distance
+            ok_pages = wr["phys"] >= 0
+            pstart = np.where(ok_pages, wr["page_start"], 0).astype(np.int32)
+            rps = i32(pstart)
+            slopes = torch.from_numpy((2.0 ** (-8.0 * (np.arange(Hqr) + 1) / Hqr)).astype(np.float32)).to(dev)
+
+            def alibi_call(i):
+                spkv.lazy_alibi_prefill_attn(rcache, pq, rqpos, rmeta, rnp, rps, rdoc, slopes, pout, plse)
+
+            timed(alibi_call, range(3))
+            al_ms = statistics.mean(timed(alibi_call, timed_idx))
+            al_tf = flops / (al_ms * 1e-3) / 1e12
             prefill = {"kernel": "lazy_rope_prefill_attn (tcgen05.mma, TMEM accumulators, TMA pages)",
                        "workload": f"the RAG documents above, 128 new query rows per request ({Br} x 128 x 32 heads)",
                        "us": pre_ms * 1e3, "flops": flops, "bound": "tensor", "achieved_TFLOPs": tflops,
                        "peak": tpeak, "peak_kind": tkind + " bf16 dense (cuBLAS burst)", "frac": tflops / tpeak,
-                       "query_rows_per_s": Br * Tq / (pre_ms * 1e-3)}
+                       "query_rows_per_s": Br * Tq / (pre_ms * 1e-3),
+                       "alibi": {"kernel": "lazy_alibi_prefill_attn (same kernel, bias instead of rotation)",
+                                 "slopes": "2^(-8 (h+1) / 32) per query head h", "us": al_ms * 1e3,
+                                 "achieved_TFLOPs": al_tf, "frac": al_tf / tpeak}}
             del pq, pout, plse
         st, bits = spkv.get_device_error(rcache)
         if st != 0:

@@ -15,6 +15,7 @@
  *   sparse_decode_attn   split-K flash decoding over the selected pages
  *   lazy_rope_decode_attn  the same with deferred RoPE (query rotated once per document)
  *   lazy_rope_prefill_attn a tile of new query rows over cached documents (tcgen05)
+ *   lazy_alibi_prefill_attn  the same for models with ALiBi position biases
  *   attn_column_scores   PyramidKV-style key scores of a prompt's last rows (tcgen05)
  *
  * Sources (web pages, cited by title and section):
@@ -239,6 +240,25 @@ int lazy_rope_prefill_attn(spkv_cache_t cache, const void* q, int B, int T, int 
                            const int32_t* qpos0, const uint32_t* meta, int meta_heads,
                            const int32_t* n_pages, int np_max, const int32_t* doc_pos,
                            int max_docs, float theta, float* out, float* lse, void* stream);
+
+/* The prefill above for ALiBi models ([Lazy] "Key contributions" 4: the mechanism carries over to
+ * other relative position encodings, ALiBi among them).  Keys are stored with no positional
+ * transform, so a cached document is reused at any offset as it is; the position enters only as
+ * the bias.  The key in row t of listed page j (document slot i, page_start[j] its document-local
+ * first position) sits at m = doc_pos[b][i] + page_start[j] + t, and for query row t' of request b
+ * (position n = qpos0[b] + t') and query head hq:
+ *   score = q . key / sqrt(128) - slopes[hq] * (n - m)
+ *   out[b][t'][hq][:] = sum softmax(score) v,  lse[b][t'][hq] = log sum exp(score)   (natural log)
+ * over every valid key of the request's listed pages (no mask, as lazy_rope_prefill_attn).
+ *   page_start : device int32 with the shape of meta ([B][meta_heads][np_max])
+ *   slopes     : device fp32 [Hq] (natural-log units per token of distance)
+ *   q, qpos0, meta, meta_heads, n_pages, np_max, doc_pos, max_docs, out, lse: as above
+ * The query and the softmax weights enter the tensor cores as bf16 (fp32 accumulation); the bias
+ * is added in fp32.  Errors as lazy_rope_prefill_attn.  B, Hq <= 65535. */
+int lazy_alibi_prefill_attn(spkv_cache_t cache, const void* q, int B, int T, int Hq, const int32_t* qpos0,
+                            const uint32_t* meta, int meta_heads, const int32_t* n_pages, int np_max,
+                            const int32_t* page_start, const int32_t* doc_pos, int max_docs,
+                            const float* slopes, float* out, float* lse, void* stream);
 
 /* The PyramidKV-style sparsification score S of a prompt's keys ([FA] "2. Attention
  * modification": the sum of the softmax probabilities the last alpha rows give each key,

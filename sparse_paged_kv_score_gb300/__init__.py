@@ -33,7 +33,7 @@ __all__ = ["PagedKVCache", "paged_kv_create", "paged_kv_append", "score_blocks",
            "select_topk",
            "sparse_decode_attn", "lazy_rope_decode_attn", "resident_setdiff", "lru_bucket_update",
            "select_resident_update", "retrieve_pages", "sparse_decode_attn_slots", "lazy_rope_prefill_attn",
-           "attn_column_scores",
+           "attn_column_scores", "lazy_alibi_prefill_attn",
            "sparse_decode_attn_noalloc", "pack_page_words", "get_device_error", "SpkvError", "DEVERR",
            "load"]
 
@@ -278,6 +278,27 @@ def lazy_rope_prefill_attn(cache: PagedKVCache, q, qpos0, meta, n_pages, doc_pos
         _t(qpos0, torch.int32, "qpos0", (B,)), _t(meta, torch.int32, "meta", (B, meta_heads, np_max)),
         meta_heads, _t(n_pages, torch.int32, "n_pages", (B,)), np_max,
         _t(doc_pos, torch.int32, "doc_pos", (B, max_docs)), max_docs, float(theta),
+        _t(out, torch.float32, "out", (B, T, Hq, HEAD_DIM)), _t(lse, torch.float32, "lse", (B, T, Hq)),
+        _stream(stream)))
+
+
+def lazy_alibi_prefill_attn(cache: PagedKVCache, q, qpos0, meta, n_pages, page_start, doc_pos, slopes, out, lse,
+                            stream=None):
+    """The prefill for ALiBi models: keys unrotated, bias -slopes[hq] * (n - m) with m = doc_pos[slot] +
+    page_start + row; page_start int32 with the shape of meta, slopes fp32 [Hq]."""
+    B, T, Hq = q.shape[0], q.shape[1], q.shape[2]
+    if meta.dim() == 2:
+        meta = meta.unsqueeze(1)
+    if page_start.dim() == 2:
+        page_start = page_start.unsqueeze(1)
+    meta_heads, np_max = meta.shape[1], meta.shape[2]
+    max_docs = doc_pos.shape[1]
+    check("lazy_alibi_prefill_attn", load().lazy_alibi_prefill_attn(
+        cache.handle, _t(q, torch.bfloat16, "q", (B, T, Hq, HEAD_DIM)), B, T, Hq,
+        _t(qpos0, torch.int32, "qpos0", (B,)), _t(meta, torch.int32, "meta", (B, meta_heads, np_max)),
+        meta_heads, _t(n_pages, torch.int32, "n_pages", (B,)), np_max,
+        _t(page_start, torch.int32, "page_start", (B, meta_heads, np_max)),
+        _t(doc_pos, torch.int32, "doc_pos", (B, max_docs)), max_docs, _t(slopes, torch.float32, "slopes", (Hq,)),
         _t(out, torch.float32, "out", (B, T, Hq, HEAD_DIM)), _t(lse, torch.float32, "lse", (B, T, Hq)),
         _stream(stream)))
 

@@ -336,6 +336,45 @@ int lazy_rope_prefill_attn(spkv_cache_t c, const void* q, int B, int T, int Hq, 
   return status_of(spkv::launch_prefill(c, p, as_stream(stream)));
 }
 
+int lazy_alibi_prefill_attn(spkv_cache_t c, const void* q, int B, int T, int Hq, const int32_t* qpos0,
+                            const uint32_t* meta, int meta_heads, const int32_t* n_pages, int np_max,
+                            const int32_t* page_start, const int32_t* doc_pos, int max_docs, const float* slopes,
+                            float* out, float* lse, void* stream) {
+  if (!c || B < 0 || T < 0 || Hq <= 0) return SPKV_EINVAL;
+  const int Hk = c->d.n_kv_heads;
+  if (Hq % Hk != 0) return SPKV_EINVAL;
+  if (Hq / Hk > kMaxGroup) return SPKV_EUNSUPPORTED;
+  if (B == 0 || T == 0) return SPKV_OK;
+  if (!q || !qpos0 || !meta || !n_pages || !page_start || !doc_pos || !slopes || !out || !lse || np_max <= 0 ||
+      max_docs <= 0 || !aligned(q, 16) || !aligned(out, 16))
+    return SPKV_EINVAL;
+  if (meta_heads != 1 && meta_heads != Hk) return SPKV_EINVAL;
+  if (B > 65535 || Hq > 65535) return SPKV_EINVAL;
+  spkv::PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = static_cast<const uint16_t*>(q);
+  p.out = out;
+  p.lse = lse;
+  p.B = B;
+  p.T = T;
+  p.Hq = Hq;
+  p.Hk = Hk;
+  p.G = Hq / Hk;
+  p.n_phys = c->d.n_phys_pages;
+  p.qpos0 = qpos0;
+  p.meta = meta;
+  p.meta_heads = meta_heads;
+  p.n_pages = n_pages;
+  p.np_max = np_max;
+  p.doc_pos = doc_pos;
+  p.max_docs = max_docs;
+  p.scale_log2 = static_cast<float>(1.4426950408889634074 / std::sqrt(128.0));
+  p.err = c->dev_err;
+  p.page_start = page_start;
+  p.slopes = slopes;   // phase_inc stays zero: the query is never rotated
+  return status_of(spkv::launch_prefill(c, p, as_stream(stream)));
+}
+
 int attn_column_scores(spkv_cache_t c, const void* q, int B, int alpha, int Hq, const int32_t* page_table,
                        int np_max, const int32_t* seq_len, float* scores, void* stream) {
   if (!c || B < 0 || Hq <= 0 || alpha < 0) return SPKV_EINVAL;

@@ -107,6 +107,8 @@ struct PrefillParams {
   float scale_log2;
   uint32_t* err;
   uint64_t phase_inc[64];
+  const int32_t* page_start;     // ALiBi form (slopes != null): document-local start of each listed page
+  const float* slopes;           // ALiBi form: [Hq] bias slopes (natural-log units); null for RoPE
 };
 
 // Parameters of the column-score kernel (PyramidKV-style score S).

@@ -120,6 +120,9 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// ALIBI: keys carry no rotation and the query rows are written once; each score gets the
+// linear bias -slope * (n - m), m = doc_pos[slot] + page_start + column.
+template <bool ALIBI>
 __global__ void __launch_bounds__(kPThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                    const __grid_constant__ PrefillParams p) {
@@ -259,7 +262,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       fence_proxy_async_smem();
       __syncwarp();
-      const bool new_doc = gr.a.slot != prev_slot;
+      const bool new_doc = ALIBI ? g == 0 : gr.a.slot != prev_slot;
       prev_slot = gr.a.slot;
       for (int x = 0; x < n_tiles && ok; ++x) {
         // PV of the previous group reads P_x from the columns the QK below overwrites; MMAs of
@@ -313,18 +316,27 @@ __global__ void __launch_bounds__(kPThreads, 1)
     uint8_t* qtile = sQ + x * kQBytes;
     const int pos = p.qpos0[b] + t;
     const float scale = p.scale_log2;
+    const float slope_l2 = ALIBI ? p.slopes[hq] * 1.4426950408889634f : 0.f;   // bias slope, log2 units
+    const int64_t ps_row = (int64_t(b) * p.meta_heads + (p.meta_heads == 1 ? 0 : h)) * p.np_max;
     float m = -CUDART_INF_F, l = 0.f;
     int prev_slot = -1, g = 0;
     bool ok = true;
     for (int j = 0; j < n; ++g) {
       const Group gr = group_at(p, b, h, j, n);
+      // ALiBi: the bias of column 0 of each page of the group (log2 units), slope (m - n)
+      float cb_a = 0.f, cb_b = 0.f;
+      if (ALIBI) {
+        const int dp = p.doc_pos[int64_t(b) * p.max_docs + gr.a.slot];
+        cb_a = slope_l2 * static_cast<float>(dp + p.page_start[ps_row + j] - pos);
+        if (gr.size == 2) cb_b = slope_l2 * static_cast<float>(dp + p.page_start[ps_row + j + 1] - pos);
+      }
       j += gr.size;
-      if (gr.a.slot != prev_slot) {
+      if (ALIBI ? g == 0 : gr.a.slot != prev_slot) {
         // Document switch: every MMA that read the previous rotation has completed (its S
         // row was read in the previous iteration), so row r of Q is rewritten as
-        // R(pos - doc_pos[slot]) q in bf16.
+        // R(pos - doc_pos[slot]) q in bf16 (ALiBi: q itself, once).
         prev_slot = gr.a.slot;
-        const int rel = pos - p.doc_pos[int64_t(b) * p.max_docs + gr.a.slot];
+        const int rel = ALIBI ? 0 : pos - p.doc_pos[int64_t(b) * p.max_docs + gr.a.slot];
 #pragma unroll 1
         for (int cc = 0; cc < 8; ++cc) {
           uint4 xa = make_uint4(0, 0, 0, 0), ya = make_uint4(0, 0, 0, 0);
@@ -378,13 +390,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
         tmem_ld32(lane_addr + s_col(x) + 32 * k, sv);
         tmem_wait_ld();
         const int lim = (k < 2 ? va : vb) - 32 * (k & 1);   // valid columns of this block
+        if (ALIBI) {   // the maximum of s scale + bias
+          const float cb = (k < 2 ? cb_a : cb_b) + slope_l2 * static_cast<float>(32 * (k & 1));
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          mx8[c & 7] = fmaxf(mx8[c & 7], (full || c < lim) ? __uint_as_float(sv[c]) : -CUDART_INF_F);
+          for (int c = 0; c < 32; ++c) {
+            const float a = fmaf(__uint_as_float(sv[c]), scale, fmaf(static_cast<float>(c), slope_l2, cb));
+            mx8[c & 7] = fmaxf(mx8[c & 7], (full || c < lim) ? a : -CUDART_INF_F);
+          }
+        } else {       // the maximum of s (scale > 0 is applied once below)
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            mx8[c & 7] = fmaxf(mx8[c & 7], (full || c < lim) ? __uint_as_float(sv[c]) : -CUDART_INF_F);
+        }
       }
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float m_grp = mx * scale;
+      const float m_grp = ALIBI ? mx : mx * scale;
       bool rescale = false;
       float alpha = 1.f;
       if (m == -CUDART_INF_F) {
@@ -428,11 +449,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
         tmem_ld32(lane_addr + s_col(x) + 32 * k, sv);
         tmem_wait_ld();
         const int lim = have_m ? (k < 2 ? va : vb) - 32 * (k & 1) : 0;
+        // ALiBi: column c adds c slope to the block's bias; RoPE: no bias
+        const float cbm = ALIBI ? (k < 2 ? cb_a : cb_b) + slope_l2 * static_cast<float>(32 * (k & 1)) + mneg : mneg;
         uint32_t pw[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          const float e0 = fast_exp2(fmaf(__uint_as_float(sv[c]), scale, mneg));
-          const float e1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), scale, mneg));
+          const float b0 = ALIBI ? fmaf(static_cast<float>(c), slope_l2, cbm) : mneg;
+          const float b1 = ALIBI ? fmaf(static_cast<float>(c + 1), slope_l2, cbm) : mneg;
+          const float e0 = fast_exp2(fmaf(__uint_as_float(sv[c]), scale, b0));
+          const float e1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), scale, b1));
           const float p0 = (have_m && (full || c < lim)) ? e0 : 0.f;
           const float p1 = (have_m && (full || c + 1 < lim)) ? e1 : 0.f;
           ls8[c & 7] += p0;
@@ -488,14 +513,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
 size_t prefill_smem_bytes() { return kPrefillSmem; }
 
 cudaError_t prefill_init_attributes() {
-  return cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kPrefillSmem));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(kPrefillSmem));
 }
 
 cudaError_t launch_prefill(const spkv_cache* c, const PrefillParams& p, cudaStream_t st) {
   const int pairs = (p.G + 1) / 2;
   const dim3 grid((p.T + kPM - 1) / kPM, p.Hk * pairs, p.B);
-  return launch_pdl(prefill_kernel, grid, dim3(kPThreads), kPrefillSmem, st, c->tmap_k, c->tmap_v, p);
+  return launch_pdl(p.slopes ? prefill_kernel<true> : prefill_kernel<false>, grid, dim3(kPThreads), kPrefillSmem, st,
+                    c->tmap_k, c->tmap_v, p);
 }
 
 }  // namespace spkv

@@ -35,7 +35,7 @@ def test_header_declares_the_decode_path():
               "lazy_rope_decode_attn", "resident_setdiff", "lru_bucket_update", "spkv_get_device_error",
               "paged_kv_destroy", "spkv_status_string", "spkv_pack_page_words", "spkv_sm_count",
               "retrieve_pages", "sparse_decode_attn_slots", "select_resident_update",
-              "lazy_rope_prefill_attn", "attn_column_scores"]:
+              "lazy_rope_prefill_attn", "lazy_alibi_prefill_attn", "attn_column_scores"]:
         assert f in names
 
 

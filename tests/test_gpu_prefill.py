@@ -150,3 +150,65 @@ def test_prefill_bad_page_words_flag_without_fault():
     assert bits == (spkv.DEVERR["PHYS"] | spkv.DEVERR["SLOT"])
     assert torch.isfinite(out).all()
     cache.close()
+
+
+# ------------------------------------------------------------------ ALiBi form
+
+def _slopes(Hq):
+    """A geometric set of slopes, one per query head (the values do not matter to parity)."""
+    return (2.0 ** (-8.0 * (np.arange(Hq) + 1) / Hq)).astype(np.float32)
+
+
+def _run_alibi(w, q, phys, valid, slot, page_start, n_pages, qpos0, doc_pos, slopes):
+    B, T, Hq = q.shape[0], q.shape[1], q.shape[2]
+    cache, keep = _cache(w)
+    words = _words(phys, valid, slot)
+    out = torch.full((B, T, Hq, 128), float("nan"), dtype=torch.float32, device=DEV)
+    lse = torch.full((B, T, Hq), float("nan"), dtype=torch.float32, device=DEV)
+    spkv.lazy_alibi_prefill_attn(cache, bf(q), i32(qpos0), u32_as_i32(words), i32(n_pages), i32(page_start),
+                                 i32(doc_pos), torch.from_numpy(slopes).to(DEV), out, lse)
+    o, l = out.cpu().numpy(), lse.cpu().numpy()
+    assert spkv.get_device_error(cache) == (0, 0)
+    cache.close()
+    return o, l
+
+
+@pytest.mark.parametrize("seed,Hq,Hk,T", [(11, 8, 2, 5), (12, 16, 4, 128), (13, 8, 8, 200), (14, 32, 2, 33)])
+def test_alibi_prefill_vs_oracle(seed, Hq, Hk, T):
+    """Tiles of 128 rows with ragged tails, group sizes 1..16, documents at unaligned offsets:
+    the bias spans hundreds of nats across a request, so the running maximum moves and O is
+    rescaled as nearer documents arrive."""
+    w = gen.lazy_rag(seed=seed, B=3, Hq=Hq, Hk=Hk, n_docs=12, docs_per_req=4, min_len=70, max_len=900)
+    q = _queries(seed, w["B"], T, Hq, 1.0)
+    sl = _slopes(Hq)
+    o, l = _run_alibi(w, q, w["phys"], w["valid"], w["slot"], w["page_start"], w["n_pages"], w["qpos"],
+                      w["doc_pos"], sl)
+    ro, rl = oracle.alibi_prefill_batch(q, w["k_pool"], w["v_pool"], w["phys"], w["valid"], w["slot"],
+                                        w["page_start"], w["n_pages"], w["qpos"], w["doc_pos"], sl)
+    _check(o, l, ro, rl)
+
+
+def test_alibi_prefill_per_head_page_order_and_empty_request():
+    """Positions come from doc_pos and page_start, not from the list order: per-kv-head page lists
+    in different orders give the oracle's result; a request without pages gives 0 and -inf."""
+    w = gen.lazy_rag(seed=15, B=3, Hq=8, Hk=2, n_docs=10, docs_per_req=3, min_len=64, max_len=700)
+    rng = np.random.default_rng(15)
+    B, Hk, npm = w["B"], w["Hk"], w["np_max"]
+    arrs = {k: np.zeros((B, Hk, npm), np.int32) for k in ("phys", "valid", "slot", "page_start")}
+    arrs["phys"][:] = -1
+    n_pages = w["n_pages"].copy()
+    n_pages[1] = 0
+    for b in range(B):
+        n = n_pages[b]
+        for h in range(Hk):
+            perm = rng.permutation(n) if h % 2 else np.arange(n)
+            for k in arrs:
+                arrs[k][b, h, :n] = w[k][b, perm]
+    q = _queries(15, B, 70, 8, 1.0)
+    sl = _slopes(8)
+    o, l = _run_alibi(w, q, arrs["phys"], arrs["valid"], arrs["slot"], arrs["page_start"], n_pages, w["qpos"],
+                      w["doc_pos"], sl)
+    ro, rl = oracle.alibi_prefill_batch(q, w["k_pool"], w["v_pool"], arrs["phys"], arrs["valid"], arrs["slot"],
+                                        arrs["page_start"], n_pages, w["qpos"], w["doc_pos"], sl)
+    assert (o[1] == 0).all() and np.isneginf(l[1]).all()
+    _check(o, l, ro, rl)

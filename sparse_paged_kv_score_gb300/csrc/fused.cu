@@ -5,9 +5,12 @@
 // three operations separately; running them as one kernel (one launch, each unit's tables read
 // once, the selected list handed over in shared memory) is this library's choice.
 //
-// One CTA of 256 threads per unit.  Warp 0 selects (warp form, scores in registers) while the
-// other warps clear the slot list and prefetch the unit's resident and timestamp rows into L2;
-// then all threads run the set-difference and LRU cores of resid.cuh on the list in shared memory.
+// One CTA of 256 threads per unit.  Up to 2048 slots, every thread first loads its eight slots'
+// resident ids and timestamps into registers (slot tid + 256 k), so the loads overlap the
+// selection and neither core reads the rows again; more slots, the other warps prefetch the rows
+// into L2 instead.  Warp 0 selects (warp form, scores in registers) while the other warps clear
+// the slot list; then all threads run the set-difference and LRU cores of resid.cuh on the list
+// in shared memory.
 #include "common.cuh"
 #include "internal.h"
 #include "resid.cuh"
@@ -17,13 +20,14 @@ namespace spkv {
 namespace {
 
 constexpr int kFuseThreads = 256;   // several CTAs per SM fit beside the selection warp's registers
+constexpr int kRegSlots = 8;        // slots per thread kept in registers (n_slots <= 2048)
 
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 template <int R>
-__global__ void __launch_bounds__(kFuseThreads)
+__global__ void __launch_bounds__(kFuseThreads, R >= 32 ? 1 : 2)
     select_resident_kernel(const float* __restrict__ qs, const float* __restrict__ es, uint32_t* __restrict__ alive,
                            const int32_t* __restrict__ seq_len, int Hk, int np_max, int k_q, int k_e,
                            int32_t* __restrict__ sel, int32_t* __restrict__ n_sel, int32_t* __restrict__ resident,
@@ -32,7 +36,7 @@ __global__ void __launch_bounds__(kFuseThreads)
                            int32_t* __restrict__ hist_out, uint32_t* err) {
   extern __shared__ __align__(16) uint8_t fm[];
   __shared__ int hist[64], hist_u[64], warp_tot[kFuseThreads / 32];
-  __shared__ int n_sh;
+  __shared__ int n_sh, nm_sh;
   pdl_wait();
   pdl_trigger();
   const int u = blockIdx.x, tid = threadIdx.x;
@@ -48,24 +52,51 @@ __global__ void __launch_bounds__(kFuseThreads)
   sm.warp_tot = warp_tot;
   int32_t* rrow = resident + int64_t(u) * n_slots;
   int32_t* trow = ts + int64_t(u) * n_slots;
+  const bool in_regs = n_slots <= kRegSlots * kFuseThreads;
+  int rid[kRegSlots], tsv[kRegSlots];
+  if (in_regs && tid >= 32) {   // warp 0 loads its share after the selection's loads
+#pragma unroll
+    for (int k = 0; k < kRegSlots; ++k) {
+      const int s = tid + k * kFuseThreads;
+      rid[k] = s < n_slots ? rrow[s] : -1;
+      tsv[k] = s < n_slots ? trow[s] : 0;
+    }
+  }
 
   if (tid < 32) {
     const int n = warp_select_unit<R>(qs, es, alive, seq_len, u, Hk, np_max, k_q, k_e, sel, n_sel, ssel, err);
     if (tid == 0) n_sh = n;
+    if (in_regs) {
+#pragma unroll
+      for (int k = 0; k < kRegSlots; ++k) {
+        const int s = tid + k * kFuseThreads;
+        rid[k] = s < n_slots ? rrow[s] : -1;
+        tsv[k] = s < n_slots ? trow[s] : 0;
+      }
+    }
   } else {
     for (int i = tid - 32; i < stride; i += kFuseThreads - 32) sslot[i] = -1;
-    const int lines = (n_slots * 4 + 127) / 128;   // 128-byte lines of each row
-    for (int l = tid - 32; l < 2 * lines; l += kFuseThreads - 32)
-      prefetch_l2(l < lines ? static_cast<const void*>(rrow + 32 * l) : static_cast<const void*>(trow + 32 * (l - lines)));
+    if (!in_regs) {
+      const int lines = (n_slots * 4 + 127) / 128;   // 128-byte lines of each row
+      for (int l = tid - 32; l < 2 * lines; l += kFuseThreads - 32)
+        prefetch_l2(l < lines ? static_cast<const void*>(rrow + 32 * l) : static_cast<const void*>(trow + 32 * (l - lines)));
+    }
   }
   __syncthreads();
   const int n = n_sh;
   int32_t* mrow = missing + int64_t(u) * stride;
-  setdiff_core(rrow, n_slots, ssel, n, stride, sslot, mrow, n_missing + u, slot + int64_t(u) * stride, err);
-  __syncthreads();   // the missing list and its length (global, this CTA's writes) are visible now
-  const int nm = n_missing[u];
-  lru_core(rrow, trow, n_slots, sslot, n, mrow, nm, stride, t_now, W, victims + int64_t(u) * stride,
-           hist_out + int64_t(u) * 64, sm, err);
+  if (in_regs) {
+    setdiff_core_regs(rid, ssel, n, stride, sslot, mrow, n_missing + u, slot + int64_t(u) * stride, &nm_sh, err);
+    __syncthreads();   // the missing list and its length are visible now
+    lru_core_regs(rid, tsv, rrow, trow, n_slots, sslot, n, mrow, nm_sh, stride, t_now, W,
+                  victims + int64_t(u) * stride, hist_out + int64_t(u) * 64, sm, err);
+  } else {
+    setdiff_core(rrow, n_slots, ssel, n, stride, sslot, mrow, n_missing + u, slot + int64_t(u) * stride, err);
+    __syncthreads();   // the missing list and its length (global, this CTA's writes) are visible now
+    const int nm = n_missing[u];
+    lru_core(rrow, trow, n_slots, sslot, n, mrow, nm, stride, t_now, W, victims + int64_t(u) * stride,
+             hist_out + int64_t(u) * 64, sm, err);
+  }
 }
 
 size_t fused_smem(int stride, int n_slots) { return size_t(3) * stride * 4 + size_t(2) * n_slots; }

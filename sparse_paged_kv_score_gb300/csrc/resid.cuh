@@ -38,6 +38,43 @@ __device__ __forceinline__ int block_excl_scan_i(int v, int* warp_tot, int* tota
   return base + x - v;
 }
 
+// Binary search of resident id `id` (slot s) in the ascending selected list; a hit records s.
+__device__ __forceinline__ void setdiff_probe(int id, int s, const int32_t* ssel, int n, int32_t* sslot,
+                                              uint32_t* err) {
+  if (id < 0) return;
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (ssel[mid] < id) lo = mid + 1;
+    else hi = mid;
+  }
+  if (lo < n && ssel[lo] == id && atomicCAS(&sslot[lo], -1, s) != -1) flag_error(err, SPKV_DEVERR_ORDER);
+}
+
+// Second half of the set difference (after the probes and a barrier): the slot list, the missing
+// list in ascending order (-1 padded) and its length, also to *nm_sh when it is not null.
+__device__ __forceinline__ void setdiff_finish(const int32_t* ssel, int n, int stride, const int32_t* sslot,
+                                               int32_t* __restrict__ mrow, int32_t* __restrict__ n_missing_u,
+                                               int32_t* __restrict__ orow, int* nm_sh) {
+  const int tid = threadIdx.x;
+  for (int i = tid; i < stride; i += blockDim.x) orow[i] = sslot[i];
+  if (tid < 32) {
+    int base = 0;
+    for (int i0 = 0; i0 < stride; i0 += 32) {
+      const int i = i0 + tid;
+      const bool miss = i < n && sslot[i] < 0;
+      const unsigned bal = __ballot_sync(0xffffffffu, miss);
+      if (miss) mrow[base + __popc(bal & ((1u << tid) - 1u))] = ssel[i];
+      base += __popc(bal);
+    }
+    for (int i = base + tid; i < stride; i += 32) mrow[i] = -1;
+    if (tid == 0) {
+      *n_missing_u = base;
+      if (nm_sh) *nm_sh = base;
+    }
+  }
+}
+
 // Set difference of one unit.  On entry (after a barrier): ssel[0..n) is the selected list in
 // ascending order and sslot[0..stride) == -1.  On return sslot[i] is the resident slot of
 // ssel[i] (or -1), and missing (ascending, -1 padded), *n_missing and slot are written.
@@ -55,33 +92,24 @@ __device__ __forceinline__ void setdiff_core(const int32_t* __restrict__ rrow, i
       id[k] = s < n_slots ? rrow[s] : -1;
     }
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      if (id[k] < 0) continue;
-      int lo = 0, hi = n;  // binary search in the ascending selected list
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (ssel[mid] < id[k]) lo = mid + 1;
-        else hi = mid;
-      }
-      if (lo < n && ssel[lo] == id[k]) {
-        if (atomicCAS(&sslot[lo], -1, s0 + k * static_cast<int>(blockDim.x)) != -1) flag_error(err, SPKV_DEVERR_ORDER);
-      }
-    }
+    for (int k = 0; k < kBatch; ++k) setdiff_probe(id[k], s0 + k * static_cast<int>(blockDim.x), ssel, n, sslot, err);
   }
   __syncthreads();
-  for (int i = tid; i < stride; i += blockDim.x) orow[i] = sslot[i];
-  if (tid < 32) {
-    int base = 0;
-    for (int i0 = 0; i0 < stride; i0 += 32) {
-      const int i = i0 + tid;
-      const bool miss = i < n && sslot[i] < 0;
-      const unsigned bal = __ballot_sync(0xffffffffu, miss);
-      if (miss) mrow[base + __popc(bal & ((1u << tid) - 1u))] = ssel[i];
-      base += __popc(bal);
-    }
-    for (int i = base + tid; i < stride; i += 32) mrow[i] = -1;
-    if (tid == 0) *n_missing_u = base;
-  }
+  setdiff_finish(ssel, n, stride, sslot, mrow, n_missing_u, orow, nullptr);
+}
+
+// The same with the unit's resident ids already in registers: rid[k] is slot tid + k blockDim
+// (-1 past n_slots).  Also leaves the missing count in *nm_sh (visible after a barrier).
+template <int P>
+__device__ __forceinline__ void setdiff_core_regs(const int (&rid)[P], const int32_t* ssel, int n, int stride,
+                                                  int32_t* sslot, int32_t* __restrict__ mrow,
+                                                  int32_t* __restrict__ n_missing_u, int32_t* __restrict__ orow,
+                                                  int* nm_sh, uint32_t* err) {
+#pragma unroll
+  for (int k = 0; k < P; ++k)
+    setdiff_probe(rid[k], static_cast<int>(threadIdx.x + k * blockDim.x), ssel, n, sslot, err);
+  __syncthreads();
+  setdiff_finish(ssel, n, stride, sslot, mrow, n_missing_u, orow, nm_sh);
 }
 
 // Shared-memory work space of lru_core.
@@ -94,17 +122,13 @@ struct LruSmem {
   int* warp_tot;      // [blockDim / 32]
 };
 
-// Bucketed LRU update of one unit at time t_now; srow[0..n) is the slot list (slot of each
-// selected page or -1), mrow[0..nm) the missing pages.  Needs no barrier before it.
-__device__ __forceinline__ void lru_core(int32_t* __restrict__ rrow, int32_t* __restrict__ trow, int n_slots,
-                                         const int32_t* srow, int n, const int32_t* mrow, int nm, int stride,
-                                         int32_t t_now, int W, int32_t* __restrict__ vrow,
-                                         int32_t* __restrict__ hist_row, const LruSmem& sm, uint32_t* err) {
+// LRU steps 0-1: clear the work space, then touch the hits (timestamp t_now).  Ends on a barrier.
+__device__ __forceinline__ void lru_touch(int32_t* __restrict__ trow, int n_slots, const int32_t* srow, int n,
+                                          int32_t t_now, const LruSmem& sm, uint32_t* err) {
   const int tid = threadIdx.x;
   for (int s = tid; s < n_slots; s += blockDim.x) sm.touched[s] = 0;
   if (tid < 64) sm.hist[tid] = sm.hist_u[tid] = 0;
   __syncthreads();
-  // 1. touch the hits
   for (int i = tid; i < n; i += blockDim.x) {
     const int s = srow[i];
     if (s < 0) continue;
@@ -116,39 +140,34 @@ __device__ __forceinline__ void lru_core(int32_t* __restrict__ rrow, int32_t* __
     sm.touched[s] = 1;
   }
   __syncthreads();
-  // 2. buckets and histograms (whole warps iterate together; a batch of slots is loaded first)
-  constexpr int kBatch = 4;
-  for (int s0 = 0; s0 < n_slots; s0 += kBatch * blockDim.x) {
-    int rv[kBatch], tv[kBatch];
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const int s = s0 + k * blockDim.x + tid;
-      const bool in = s < n_slots;
-      rv[k] = in ? rrow[s] : -1;
-      tv[k] = in ? trow[s] : 0;
-    }
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const int s = s0 + k * blockDim.x + tid;
-      const bool in = s < n_slots;
-      int bk = 63;
-      if (in && rv[k] >= 0) {
-        const int64_t age = int64_t(t_now) - tv[k];
-        bk = age <= 0 ? 0 : static_cast<int>(age / W < 63 ? age / W : 63);
-      }
-      if (in) sm.bucket[s] = static_cast<uint8_t>(bk);
-      warp_hist_add(sm.hist, bk, in);
-      warp_hist_add(sm.hist_u, bk, in && !sm.touched[s]);
-    }
+}
+
+// LRU step 2 for one slot: its bucket and the two histograms (whole warps call it together).
+__device__ __forceinline__ void lru_bucket_one(int s, bool in, int rv, int tv, int32_t t_now, int W,
+                                               const LruSmem& sm) {
+  int bk = 63;
+  if (in && rv >= 0) {
+    const int64_t age = int64_t(t_now) - tv;
+    bk = age <= 0 ? 0 : static_cast<int>(age / W < 63 ? age / W : 63);
   }
-  __syncthreads();
+  if (in) sm.bucket[s] = static_cast<uint8_t>(bk);
+  warp_hist_add(sm.hist, bk, in);
+  warp_hist_add(sm.hist_u, bk, in && !sm.touched[s]);
+}
+
+// LRU steps 3-4 (after the buckets and a barrier): victims are untouched slots, oldest bucket
+// first, ascending slot inside a bucket; the missing pages are installed in them.
+__device__ __forceinline__ void lru_pick_install(int32_t* __restrict__ rrow, int32_t* __restrict__ trow,
+                                                 int n_slots, const int32_t* mrow, int nm, int stride,
+                                                 int32_t t_now, int32_t* __restrict__ vrow,
+                                                 int32_t* __restrict__ hist_row, const LruSmem& sm, uint32_t* err) {
+  const int tid = threadIdx.x;
   int avail = 0;
   for (int k = 0; k < 64; ++k) avail += sm.hist_u[k];
   if (nm > avail) {
     if (tid == 0) flag_error(err, SPKV_DEVERR_CAPACITY);
     nm = avail;
   }
-  // 3. victims: untouched slots, oldest bucket first, ascending slot inside a bucket
   const int chunk = (n_slots + blockDim.x - 1) / blockDim.x;
   const int lo = min(n_slots, tid * chunk), hi = min(n_slots, lo + chunk);
   int filled = 0;
@@ -163,7 +182,6 @@ __device__ __forceinline__ void lru_core(int32_t* __restrict__ rrow, int32_t* __
     filled += min(total, nm - filled);
   }
   __syncthreads();
-  // 4. install the missing pages
   for (int i = tid; i < stride; i += blockDim.x) {
     if (i < nm) {
       const int s = sm.vic[i];
@@ -175,6 +193,54 @@ __device__ __forceinline__ void lru_core(int32_t* __restrict__ rrow, int32_t* __
     }
   }
   if (tid < 64) hist_row[tid] = sm.hist[tid];
+}
+
+// Bucketed LRU update of one unit at time t_now; srow[0..n) is the slot list (slot of each
+// selected page or -1), mrow[0..nm) the missing pages.  Needs no barrier before it.
+__device__ __forceinline__ void lru_core(int32_t* __restrict__ rrow, int32_t* __restrict__ trow, int n_slots,
+                                         const int32_t* srow, int n, const int32_t* mrow, int nm, int stride,
+                                         int32_t t_now, int W, int32_t* __restrict__ vrow,
+                                         int32_t* __restrict__ hist_row, const LruSmem& sm, uint32_t* err) {
+  const int tid = threadIdx.x;
+  lru_touch(trow, n_slots, srow, n, t_now, sm, err);
+  constexpr int kBatch = 4;   // a batch of slots is loaded before any is bucketed
+  for (int s0 = 0; s0 < n_slots; s0 += kBatch * blockDim.x) {
+    int rv[kBatch], tv[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int s = s0 + k * blockDim.x + tid;
+      const bool in = s < n_slots;
+      rv[k] = in ? rrow[s] : -1;
+      tv[k] = in ? trow[s] : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int s = s0 + k * blockDim.x + tid;
+      lru_bucket_one(s, s < n_slots, rv[k], tv[k], t_now, W, sm);
+    }
+  }
+  __syncthreads();
+  lru_pick_install(rrow, trow, n_slots, mrow, nm, stride, t_now, vrow, hist_row, sm, err);
+}
+
+// The same with the unit's rows in registers as read before the update: rid[k], tsv[k] are the
+// resident id and timestamp of slot tid + k blockDim.  A touched slot's timestamp is t_now, as
+// lru_touch has just written it.
+template <int P>
+__device__ __forceinline__ void lru_core_regs(const int (&rid)[P], const int (&tsv)[P], int32_t* __restrict__ rrow,
+                                              int32_t* __restrict__ trow, int n_slots, const int32_t* srow, int n,
+                                              const int32_t* mrow, int nm, int stride, int32_t t_now, int W,
+                                              int32_t* __restrict__ vrow, int32_t* __restrict__ hist_row,
+                                              const LruSmem& sm, uint32_t* err) {
+  lru_touch(trow, n_slots, srow, n, t_now, sm, err);
+#pragma unroll
+  for (int k = 0; k < P; ++k) {
+    const int s = static_cast<int>(threadIdx.x + k * blockDim.x);
+    const bool in = s < n_slots;
+    lru_bucket_one(s, in, rid[k], in && sm.touched[s] ? t_now : tsv[k], t_now, W, sm);
+  }
+  __syncthreads();
+  lru_pick_install(rrow, trow, n_slots, mrow, nm, stride, t_now, vrow, hist_row, sm, err);
 }
 
 }  // namespace spkv

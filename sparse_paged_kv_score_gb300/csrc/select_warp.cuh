@@ -16,7 +16,9 @@
 
 namespace spkv {
 
-// Per-lane bit masks over rows: bit r = page r * 32 + lane.
+// Per-lane bit masks over rows: bit r = page r * 32 + lane.  Keys of non-candidates must be 0:
+// every trial below has its own bit set, so a zero key never matches one and the search counts
+// candidates only without testing cand in every step.
 template <int R>
 __device__ __forceinline__ uint32_t warp_topk(const uint32_t (&key)[R], uint32_t cand, int k) {
   const int lane = threadIdx.x & 31;
@@ -28,10 +30,10 @@ __device__ __forceinline__ uint32_t warp_topk(const uint32_t (&key)[R], uint32_t
   for (int bit = 31; bit >= 0; --bit) {
     const uint32_t trial = prefix | (1u << bit);
     const uint32_t hmask = ~((1u << bit) - 1u);   // bits >= bit
-    int c = 0;
+    int c4[4] = {0, 0, 0, 0};   // four partial counts: short dependency chains
 #pragma unroll
-    for (int r = 0; r < R; ++r) c += ((cand >> r) & 1u) && ((key[r] & hmask) == trial);
-    c = __reduce_add_sync(0xffffffffu, c);
+    for (int r = 0; r < R; ++r) c4[r & 3] += (key[r] & hmask) == trial;
+    const int c = __reduce_add_sync(0xffffffffu, (c4[0] + c4[1]) + (c4[2] + c4[3]));
     if (c >= remaining) prefix = trial;
     else remaining -= c;
   }
@@ -62,14 +64,11 @@ __device__ __forceinline__ int warp_select_unit(const float* __restrict__ qs, co
                                                 int32_t* ssel, uint32_t* err) {
   const int lane = threadIdx.x & 31;
   const int b = u / Hk;
-  const int L = seq_len[b];
-  const int local = L >= 1 ? (L - 1) / kPageTokens : 0;
-  if (lane == 0 && (L < 1 || local >= np_max)) flag_error(err, SPKV_DEVERR_PAGE_ID);
-  const int nc = min(local, np_max);
   const int words = (np_max + 31) / 32;
   const int64_t row = int64_t(u) * np_max;
   uint32_t* aw = alive + int64_t(u) * words;
-
+  // every load first (one round trip), the checks after
+  const int L = seq_len[b];
   uint32_t ek[R], qk[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
@@ -78,6 +77,9 @@ __device__ __forceinline__ int warp_select_unit(const float* __restrict__ qs, co
     qk[r] = i < np_max ? float_order_key(qs[row + i]) : 0u;
   }
   const uint32_t my_word = lane < words ? aw[lane] : 0u;   // lane r holds alive word r
+  const int local = L >= 1 ? (L - 1) / kPageTokens : 0;
+  if (lane == 0 && (L < 1 || local >= np_max)) flag_error(err, SPKV_DEVERR_PAGE_ID);
+  const int nc = min(local, np_max);
   uint32_t in_range = 0, cand_e = 0;
 #pragma unroll
   for (int r = 0; r < R; ++r) {
@@ -87,6 +89,8 @@ __device__ __forceinline__ int warp_select_unit(const float* __restrict__ qs, co
     cand_e |= static_cast<uint32_t>(ok && ((word >> lane) & 1u)) << r;
   }
   // ---- Gamma_e, then every alive candidate outside it dies
+#pragma unroll
+  for (int r = 0; r < R; ++r) ek[r] = ((cand_e >> r) & 1u) ? ek[r] : 0u;
   const uint32_t in_e = warp_topk<R>(ek, cand_e, k_e);
   uint32_t my_clear = 0;
 #pragma unroll
@@ -96,7 +100,10 @@ __device__ __forceinline__ int warp_select_unit(const float* __restrict__ qs, co
   }
   if (lane < words && my_clear) aw[lane] = my_word & ~my_clear;
   // ---- Gamma_q over the candidates outside E
-  const uint32_t in_q = warp_topk<R>(qk, in_range & ~in_e, k_q);
+  const uint32_t cand_q = in_range & ~in_e;
+#pragma unroll
+  for (int r = 0; r < R; ++r) qk[r] = ((cand_q >> r) & 1u) ? qk[r] : 0u;
+  const uint32_t in_q = warp_topk<R>(qk, cand_q, k_q);
   // ---- ascending union, then the local page
   const int stride = k_e + k_q + 1;
   int32_t* out = sel + int64_t(u) * stride;

@@ -697,52 +697,74 @@ def run_native(args):
     if not args.no_offload and rank == 0:
         offload = offload_leg(args, dev, stream, timed)
 
-    # ---- end to end through the public API: pinned host inputs in, outputs back, every step
-    q_h = [torch.empty(B, Hq, 128, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    e_h = [torch.empty(B, Hk, npm, dtype=torch.float32).pin_memory() for _ in range(2)]
-    k_h = [torch.empty(B, Hk, 128, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    v_h = [torch.empty(B, Hk, 128, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    # ---- end to end through the public API: pinned host inputs in, outputs back, every step.
+    # A step's inputs (q, eviction scores, the new K and V rows) sit in one pinned host buffer
+    # and its outputs (O, LSE) in one device buffer, so each direction is a single copy; the API
+    # calls get typed views of the matching device buffers.
+    in_shapes = [((B, Hq, 128), torch.bfloat16), ((B, Hk, npm), torch.float32), ((B, Hk, 128), torch.bfloat16),
+                 ((B, Hk, 128), torch.bfloat16)]
+    in_bytes = [int(np.prod(sh)) * torch.tensor([], dtype=dt).element_size() for sh, dt in in_shapes]
+    in_off = np.concatenate([[0], np.cumsum(in_bytes)]).astype(int)   # every section a multiple of 256 B
+
+    def views(buf, offs, shapes):
+        return [buf[offs[j]:offs[j + 1]].view(dt).view(sh) for j, (sh, dt) in enumerate(shapes)]
+
+    in_h = [torch.empty(int(in_off[-1]), dtype=torch.uint8).pin_memory() for _ in range(2)]
     for s_ in range(2):
-        q_h[s_].copy_(qs[s_].cpu())
-        e_h[s_].copy_(evs[s_].cpu())
-        k_h[s_].copy_(knew[s_].cpu())
-        v_h[s_].copy_(vnew[s_].cpu())
-    out_h = torch.empty(B, Hq, 128, dtype=torch.float32).pin_memory()
-    lse_h = torch.empty(B, Hq, dtype=torch.float32).pin_memory()
-    q_d, e_d, k_d, v_d = torch.empty_like(qs[0]), torch.empty_like(evs[0]), torch.empty_like(knew[0]), \
-        torch.empty_like(vnew[0])
-    h2d = q_h[0].numel() * 2 + e_h[0].numel() * 4 + k_h[0].numel() * 2 + v_h[0].numel() * 2
-    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+        for dst, src in zip(views(in_h[s_], in_off, in_shapes), (qs[s_], evs[s_], knew[s_], vnew[s_])):
+            dst.copy_(src.cpu())
+    in_d = torch.empty(int(in_off[-1]), dtype=torch.uint8, device=dev)
+    q_d, e_d, k_d, v_d = views(in_d, in_off, in_shapes)
+    out_shapes = [((B, Hq, 128), torch.float32), ((B, Hq), torch.float32)]
+    out_off = np.array([0, B * Hq * 128 * 4, B * Hq * 129 * 4])
+    res_d = torch.empty(int(out_off[-1]), dtype=torch.uint8, device=dev)
+    res_h = torch.empty(int(out_off[-1]), dtype=torch.uint8).pin_memory()
+    out_e, lse_e = views(res_d, out_off, out_shapes)
+    h2d = int(in_off[-1])
+    d2h = int(out_off[-1])
 
     def e2e_step(i):
-        s_ = i % 2
-        q_d.copy_(q_h[s_], non_blocking=True)
-        e_d.copy_(e_h[s_], non_blocking=True)
-        k_d.copy_(k_h[s_], non_blocking=True)
-        v_d.copy_(v_h[s_], non_blocking=True)
+        in_d.copy_(in_h[i % 2], non_blocking=True)
         spkv.decode_append_score(cache, k_d, v_d, q_d, pt, seq, scores)
         spkv.select_resident_update(cache, scores, e_d, alive, seq, k_q, k_e, sel, n_sel, resident, ts, 1000 + i,
                                     1, missing, n_missing, slot, victims, hist)
-        spkv.sparse_decode_attn(cache, q_d, pt, sel, n_sel, seq, out, lse)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        spkv.sparse_decode_attn(cache, q_d, pt, sel, n_sel, seq, out_e, lse_e)
+        res_h.copy_(res_d, non_blocking=True)
+
+    def e2e_timed(run):
+        """Device time of each step from the first copy in to the result on the host; the host
+        waits for every step's result before it starts the next."""
+        eev = []
+        for i in range(args.steps):
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            run(i)
+            b_.record(stream)
+            b_.synchronize()
+            flush.zero_()
+            eev.append((a, b_))
+        return statistics.mean(a.elapsed_time(b_) for a, b_ in eev)
 
     for i in range(args.warmup):
         e2e_step(i)
         flush.zero_()
     barrier()
-    eev = []
+    e2e_eager_ms = rank_max(e2e_timed(e2e_step), dev)
+    # the same calls captured as one CUDA graph per step, the copies from and to pinned host
+    # memory included (each step keeps its own LRU time, as in the device-timed step)
+    e2e_graphs = {}
     for i in range(args.steps):
-        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        e2e_step(i)
-        b_.record(stream)
-        b_.synchronize()       # the host holds the step's result before the next step starts
-        flush.zero_()
-        eev.append((a, b_))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            e2e_step(i)
+        e2e_graphs[i] = g
+    torch.cuda.synchronize()
+    for i in range(min(args.warmup, args.steps)):
+        e2e_graphs[i].replay()
     barrier()
-    e2e_ms = rank_max(statistics.mean(a.elapsed_time(b_) for a, b_ in eev), dev)
+    e2e_ms = rank_max(e2e_timed(lambda i: e2e_graphs[i].replay()), dev)
     e2e_value = replica_throughput(world, step_total, e2e_ms)
+    del e2e_graphs
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -782,7 +804,10 @@ def run_native(args):
             "column_scores": colsc,
             "offload": offload,
             "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h,
+                    "launch": "one CUDA graph per step: copies in from pinned host memory, the API calls, "
+                              "copies out; the host waits for each step's result",
+                    "eager_ms_per_step": e2e_eager_ms},
             "gpu_launches": 4 * args.steps,
             "eager_ms_per_step": eager_ms,
             "clocks": clk.summary(),

@@ -275,7 +275,7 @@ def offload_leg(args, dev, stream, timed):
     slots = spkv.paged_kv_create(k_slots, v_slots, None, None, max_units=U)
     pt, seq = i32(w["page_table"]), i32(w["seq_len"])
     n_iter = args.warmup + args.steps
-    qs = [bf(q) for q in gen.walk_queries(w, n_iter + 1)]
+    qs = [bf(q) for q in gen.walk_queries(w, 2 * n_iter + 1)]   # eager steps, then graph-captured steps
     ev = torch.from_numpy(w["evict"].astype(np.float32)).to(dev)
     scores = torch.empty(B, Hk, npm, dtype=torch.float32, device=dev)
     alive = torch.full((B, Hk, (npm + 31) // 32), -1, dtype=torch.int32, device=dev)
@@ -350,6 +350,30 @@ def offload_leg(args, dev, stream, timed):
             ret_ms.append(e[1].elapsed_time(e[2]))
             att_ms.append(e[2].elapsed_time(e[3]))
             miss.append(int(n_missing.sum().item()))
+    # the walk goes on with each step captured as one CUDA graph (no events between its calls)
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    gsteps = list(range(n_iter + 1, 2 * n_iter + 1))
+    graphs = {}
+    for i in gsteps:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            select_and_plan(i)
+            retrieve()
+            attend(i)
+        graphs[i] = g
+    torch.cuda.synchronize()
+    gstep_ms, gmiss = [], []
+    for i in gsteps:
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        graphs[i].replay()
+        b_.record(stream)
+        torch.cuda.synchronize()
+        if i > n_iter + args.warmup:
+            gstep_ms.append(a.elapsed_time(b_))
+            gmiss.append(int(n_missing.sum().item()))
+    del graphs
     for c in (scache, slots):
         st, bits = spkv.get_device_error(c)
         if st != 0:
@@ -372,6 +396,9 @@ def offload_leg(args, dev, stream, timed):
                  "retrieve_GBps": statistics.mean(miss) * PAGE_BYTES / (r_ms * 1e-3) / 1e9,
                  "attn_slots_us": statistics.mean(att_ms) * 1e3,
                  "attn_slots_GBps": attn_bytes / (statistics.mean(att_ms) * 1e-3) / 1e9},
+        "step_graph": {"launch": "one CUDA graph per step", "ms_per_step": statistics.mean(gstep_ms),
+                       "queries_per_s": B / (statistics.mean(gstep_ms) * 1e-3),
+                       "missing_pages_per_step": statistics.mean(gmiss)},
     }
     del dk, dv, dks, k_slots, v_slots, k_host, v_host
     torch.cuda.empty_cache()

@@ -1,0 +1,90 @@
+"""The decode step captured as CUDA graphs (how bench.py and a serving loop run it) gives bitwise
+the results of the same calls launched one by one, step after step, including the residency
+state the steps carry forward."""
+import numpy as np
+import pytest
+import torch
+
+import gen
+import sparse_paged_kv_score_gb300 as spkv
+from helpers import DEV, bf, i32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from sparse_paged_kv_score_gb300 import build
+    build.build()
+    spkv.load()
+
+
+class _Step:
+    """One handle and its per-step state on the Llama-3-8B-layer shapes at batch 4."""
+
+    def __init__(self, w):
+        B, Hk, npm = w["B"], w["Hk"], w["np_max"]
+        self.k_pool, self.v_pool = bf(w["k_pool"]), bf(w["v_pool"])
+        self.ksum = torch.zeros(Hk, w["n_phys"], 4, 128, dtype=torch.float32, device=DEV)
+        self.cnt = i32(gen.page_counts(w))
+        U = B * Hk
+        self.cache = spkv.paged_kv_create(self.k_pool, self.v_pool, self.ksum, self.cnt, max_units=U)
+        self.pt, self.seq = i32(w["page_table"]), i32(w["seq_len"])
+        self.k_q, self.k_e = w["k_q"], w["k_e"]
+        stride = self.k_q + self.k_e + 1
+        self.scores = torch.empty(B, Hk, npm, dtype=torch.float32, device=DEV)
+        self.alive = torch.full((B, Hk, (npm + 31) // 32), -1, dtype=torch.int32, device=DEV)
+        self.sel = torch.empty(B, Hk, stride, dtype=torch.int32, device=DEV)
+        self.n_sel = torch.empty(B, Hk, dtype=torch.int32, device=DEV)
+        self.resident = torch.full((U, 256), -1, dtype=torch.int32, device=DEV)
+        self.ts = torch.full((U, 256), np.iinfo(np.int32).min, dtype=torch.int32, device=DEV)
+        self.missing = torch.empty(U, stride, dtype=torch.int32, device=DEV)
+        self.n_missing = torch.empty(U, dtype=torch.int32, device=DEV)
+        self.slot = torch.empty(U, stride, dtype=torch.int32, device=DEV)
+        self.victims = torch.empty(U, stride, dtype=torch.int32, device=DEV)
+        self.hist = torch.empty(U, 64, dtype=torch.int32, device=DEV)
+        self.out = torch.empty(B, w["Hq"], 128, dtype=torch.float32, device=DEV)
+        self.lse = torch.empty(B, w["Hq"], dtype=torch.float32, device=DEV)
+
+    def run(self, q, ev, kn, vn, t):
+        spkv.decode_append_score(self.cache, kn, vn, q, self.pt, self.seq, self.scores)
+        spkv.select_resident_update(self.cache, self.scores, ev, self.alive, self.seq, self.k_q, self.k_e, self.sel,
+                                    self.n_sel, self.resident, self.ts, t, 1, self.missing, self.n_missing,
+                                    self.slot, self.victims, self.hist)
+        spkv.sparse_decode_attn(self.cache, q, self.pt, self.sel, self.n_sel, self.seq, self.out, self.lse)
+
+    def state(self):
+        return [x.clone() for x in (self.out, self.lse, self.sel, self.n_sel, self.alive, self.resident, self.ts,
+                                    self.missing, self.victims, self.hist, self.ksum, self.k_pool, self.v_pool)]
+
+
+def test_graph_replayed_steps_equal_eager_steps():
+    w = gen.llama8b(seed=3, B=4)
+    B, Hq, Hk = w["B"], w["Hq"], w["Hk"]
+    n = 6
+    qs = [bf(gen.rows_bf16(3, 100 + i, B * Hq).reshape(B, Hq, 128)) for i in range(n)]
+    evs = [torch.from_numpy(gen.normal_f64(3, 200 + i, B * Hk * w["np_max"]).astype(np.float32)
+                            .reshape(B, Hk, w["np_max"])).to(DEV) for i in range(n)]
+    kn = [bf(gen.rows_bf16(3, 300 + i, B * Hk).reshape(B, Hk, 128)) for i in range(n)]
+    vn = [bf(gen.rows_bf16(3, 400 + i, B * Hk).reshape(B, Hk, 128)) for i in range(n)]
+    eager, graphed = _Step(w), _Step(w)
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    graphs = []
+    for i in range(n):                       # capture every step first (nothing runs while capturing)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            graphed.run(qs[i], evs[i], kn[i], vn[i], i)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    for i in range(n):
+        eager.run(qs[i], evs[i], kn[i], vn[i], i)
+        graphs[i].replay()
+        torch.cuda.synchronize()
+        for a, b in zip(eager.state(), graphed.state()):
+            assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
+                               b.view(torch.int16) if b.dtype == torch.bfloat16 else b), f"step {i}"
+    assert spkv.get_device_error(eager.cache) == (0, 0)
+    assert spkv.get_device_error(graphed.cache) == (0, 0)
+    eager.cache.close()
+    graphed.cache.close()

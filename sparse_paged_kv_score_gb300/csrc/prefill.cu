@@ -392,15 +392,24 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int lim = (k < 2 ? va : vb) - 32 * (k & 1);   // valid columns of this block
         if (ALIBI) {   // the maximum of s scale + bias
           const float cb = (k < 2 ? cb_a : cb_b) + slope_l2 * static_cast<float>(32 * (k & 1));
+          if (full) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float a = fmaf(__uint_as_float(sv[c]), scale, fmaf(static_cast<float>(c), slope_l2, cb));
-            mx8[c & 7] = fmaxf(mx8[c & 7], (full || c < lim) ? a : -CUDART_INF_F);
+            for (int c = 0; c < 32; ++c)
+              mx8[c & 7] = fmaxf(mx8[c & 7], fmaf(__uint_as_float(sv[c]), scale, fmaf(static_cast<float>(c), slope_l2, cb)));
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const float a = fmaf(__uint_as_float(sv[c]), scale, fmaf(static_cast<float>(c), slope_l2, cb));
+              mx8[c & 7] = fmaxf(mx8[c & 7], c < lim ? a : -CUDART_INF_F);
+            }
           }
-        } else {       // the maximum of s (scale > 0 is applied once below)
+        } else if (full) {   // the maximum of s (scale > 0 is applied once below); every column valid
+#pragma unroll
+          for (int c = 0; c < 32; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(sv[c]));
+        } else {
 #pragma unroll
           for (int c = 0; c < 32; ++c)
-            mx8[c & 7] = fmaxf(mx8[c & 7], (full || c < lim) ? __uint_as_float(sv[c]) : -CUDART_INF_F);
+            mx8[c & 7] = fmaxf(mx8[c & 7], c < lim ? __uint_as_float(sv[c]) : -CUDART_INF_F);
         }
       }
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
@@ -452,17 +461,30 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // ALiBi: column c adds c slope to the block's bias; RoPE: no bias
         const float cbm = ALIBI ? (k < 2 ? cb_a : cb_b) + slope_l2 * static_cast<float>(32 * (k & 1)) + mneg : mneg;
         uint32_t pw[16];
+        if (full && have_m) {   // every column valid: no masking
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float b0 = ALIBI ? fmaf(static_cast<float>(c), slope_l2, cbm) : mneg;
-          const float b1 = ALIBI ? fmaf(static_cast<float>(c + 1), slope_l2, cbm) : mneg;
-          const float e0 = fast_exp2(fmaf(__uint_as_float(sv[c]), scale, b0));
-          const float e1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), scale, b1));
-          const float p0 = (have_m && (full || c < lim)) ? e0 : 0.f;
-          const float p1 = (have_m && (full || c + 1 < lim)) ? e1 : 0.f;
-          ls8[c & 7] += p0;
-          ls8[(c + 1) & 7] += p1;
-          pw[c >> 1] = pack_bf16x2(p0, p1);
+          for (int c = 0; c < 32; c += 2) {
+            const float b0 = ALIBI ? fmaf(static_cast<float>(c), slope_l2, cbm) : mneg;
+            const float b1 = ALIBI ? fmaf(static_cast<float>(c + 1), slope_l2, cbm) : mneg;
+            const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c]), scale, b0));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), scale, b1));
+            ls8[c & 7] += p0;
+            ls8[(c + 1) & 7] += p1;
+            pw[c >> 1] = pack_bf16x2(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float b0 = ALIBI ? fmaf(static_cast<float>(c), slope_l2, cbm) : mneg;
+            const float b1 = ALIBI ? fmaf(static_cast<float>(c + 1), slope_l2, cbm) : mneg;
+            const float e0 = fast_exp2(fmaf(__uint_as_float(sv[c]), scale, b0));
+            const float e1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), scale, b1));
+            const float p0 = (have_m && c < lim) ? e0 : 0.f;
+            const float p1 = (have_m && c + 1 < lim) ? e1 : 0.f;
+            ls8[c & 7] += p0;
+            ls8[(c + 1) & 7] += p1;
+            pw[c >> 1] = pack_bf16x2(p0, p1);
+          }
         }
         tmem_st16(lane_addr + s_col(x) + 16 * k, pw);
       }

@@ -76,3 +76,42 @@ def test_4096_units_full_step_and_rejection_past_it():
     # and a handle cannot be made for more than 4096 units
     with pytest.raises(spkv.SpkvError, match="EINVAL"):
         spkv.paged_kv_create(d.k_pool, d.v_pool, d.ksum, d.cnt, max_units=U + 1)
+
+
+def test_selection_at_32768_pages_and_4096_entries():
+    """The CTA form of the selection at its largest context (32768 pages, 2M tokens) and largest
+    list (k_q + k_e + 1 = 4096), bit-exact with the oracle on the same scores; one page or one
+    list entry more is refused.  Selection reads only scores, so the pool is a tiny one."""
+    from helpers import alive_bits_to_bytes, alive_bytes_to_bits, u32_as_i32
+    small = gen.sparse_workload(2, 4, 2, 64 * 4, 1, 1, seed=5)
+    d = Dev(small)
+    B, Hk, npm = 2, 2, 32768
+    rng = np.random.default_rng(32768)
+    seq = np.array([64 * npm, 64 * npm - 1000], np.int32)
+    for k_q, k_e in [(64, 64), (2000, 2095)]:
+        s = (np.round(rng.standard_normal((B, Hk, npm)) * 8) / 8).astype(np.float32)   # many exact ties
+        e = (np.round(rng.standard_normal((B, Hk, npm)) * 4) / 4).astype(np.float32)
+        alive = rng.random((B, Hk, npm)) < 0.5
+        alive_dev = u32_as_i32(alive_bytes_to_bits(alive.astype(np.uint8)))
+        stride = k_q + k_e + 1
+        sel = torch.empty(B, Hk, stride, dtype=torch.int32, device=DEV)
+        n_sel = torch.empty(B, Hk, dtype=torch.int32, device=DEV)
+        spkv.select_topk(d.cache, f32(s), f32(e), alive_dev, i32(seq), k_q, k_e, sel, n_sel)
+        o_sel, o_n, o_alive = oracle.select_batch(s.astype(np.float64), e.astype(np.float64), alive.astype(np.uint8),
+                                                  seq, k_q, k_e)
+        assert np.array_equal(sel.cpu().numpy(), o_sel) and np.array_equal(n_sel.cpu().numpy(), o_n)
+        assert np.array_equal(alive_bits_to_bytes(alive_dev.cpu().numpy().view(np.uint32), npm), o_alive)
+    assert d.errors() == (0, 0)
+    # past either limit: refused before any launch
+    s1 = torch.zeros(B, Hk, npm + 1, dtype=torch.float32, device=DEV)
+    a1 = torch.zeros(B, Hk, (npm + 1 + 31) // 32, dtype=torch.int32, device=DEV)
+    sel1 = torch.empty(B, Hk, 3, dtype=torch.int32, device=DEV)
+    n1 = torch.empty(B, Hk, dtype=torch.int32, device=DEV)
+    with pytest.raises(spkv.SpkvError, match="EINVAL"):
+        spkv.select_topk(d.cache, s1, s1, a1, i32(seq), 1, 1, sel1, n1)
+    s2 = torch.zeros(B, Hk, 8192, dtype=torch.float32, device=DEV)
+    a2 = torch.zeros(B, Hk, 8192 // 32, dtype=torch.int32, device=DEV)
+    sel2 = torch.empty(B, Hk, 4097, dtype=torch.int32, device=DEV)
+    with pytest.raises(spkv.SpkvError, match="EINVAL"):
+        spkv.select_topk(d.cache, s2, s2, a2, i32(seq), 2000, 2096, sel2, n1)
+    d.close()

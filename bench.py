@@ -65,6 +65,9 @@ def parse():
     ap.add_argument("--l2", default="none", choices=["none", "write"],
                     help="none: no flush, every step reads ~0.8 GB (> 129 MB L2); write: 256 MiB write "
                          "between timed steps")
+    ap.add_argument("--bookkeeping", default="overlap", choices=["fused", "overlap"],
+                    help="fused: selection + set-difference + LRU in one kernel before attention; "
+                         "overlap: selection, then set-difference + LRU on a second stream beside attention")
     ap.add_argument("--batch", type=int, default=32,
                     help="requests per step (32 = the Llama-3-8B-layer workload; smaller for profiling)")
     return ap.parse_args()
@@ -477,13 +480,31 @@ def run_native(args):
     flush = _Flush()
     stream = torch.cuda.current_stream()
 
-    def step(i):
+    side = torch.cuda.Stream()
+
+    def run_step(c, q, k_new, v_new, ev, al, res, tsr, t, o, ls):
+        """One decode step through the public API on handle c."""
         # the new token's K/V row at position L-1 and the block scores, one launch
-        spkv.decode_append_score(cache, knew[i], vnew[i], qs[i], pt, seq, scores)
-        # select_topk + resident_setdiff + lru_bucket_update, fused into one kernel
-        spkv.select_resident_update(cache, scores, evs[i], alive, seq, k_q, k_e, sel, n_sel, resident, ts, i, 1,
-                                    missing, n_missing, slot, victims, hist)
-        spkv.sparse_decode_attn(cache, qs[i], pt, sel, n_sel, seq, out, lse)
+        spkv.decode_append_score(c, k_new, v_new, q, pt, seq, scores)
+        if args.bookkeeping == "fused":
+            # select_topk + resident_setdiff + lru_bucket_update, fused into one kernel
+            spkv.select_resident_update(c, scores, ev, al, seq, k_q, k_e, sel, n_sel, res, tsr, t, 1, missing,
+                                        n_missing, slot, victims, hist)
+            spkv.sparse_decode_attn(c, q, pt, sel, n_sel, seq, o, ls)
+        else:
+            # the selection, then the residency bookkeeping (which attention does not read) on a
+            # second stream while the pages stream; the step ends when both are done
+            spkv.select_topk(c, scores, ev, al, seq, k_q, k_e, sel, n_sel)
+            main = torch.cuda.current_stream()
+            side.wait_stream(main)
+            with torch.cuda.stream(side):
+                spkv.resident_setdiff(c, res, sel, n_sel, missing, n_missing, slot)
+                spkv.lru_bucket_update(c, res, tsr, slot, n_sel, missing, n_missing, t, 1, victims, hist)
+            spkv.sparse_decode_attn(c, q, pt, sel, n_sel, seq, o, ls)
+            main.wait_stream(side)
+
+    def step(i):
+        run_step(cache, qs[i], knew[i], vnew[i], evs[i], alive, resident, ts, i, out, lse)
 
     def barrier():
         torch.cuda.synchronize()
@@ -657,10 +678,7 @@ def run_native(args):
         res16, ts16 = resident.clone(), ts.clone()
 
         def step16(i):
-            spkv.decode_append_score(cache16, knew[i], vnew[i], qs[i], pt, seq, scores)
-            spkv.select_resident_update(cache16, scores, evs[i], alive16, seq, k_q, k_e, sel, n_sel, res16, ts16,
-                                        i, 1, missing, n_missing, slot, victims, hist)
-            spkv.sparse_decode_attn(cache16, qs[i], pt, sel, n_sel, seq, out, lse)
+            run_step(cache16, qs[i], knew[i], vnew[i], evs[i], alive16, res16, ts16, i, out, lse)
 
         for i in range(args.warmup):
             step16(i)
@@ -753,10 +771,7 @@ def run_native(args):
 
     def e2e_step(i):
         in_d.copy_(in_h[i % 2], non_blocking=True)
-        spkv.decode_append_score(cache, k_d, v_d, q_d, pt, seq, scores)
-        spkv.select_resident_update(cache, scores, e_d, alive, seq, k_q, k_e, sel, n_sel, resident, ts, 1000 + i,
-                                    1, missing, n_missing, slot, victims, hist)
-        spkv.sparse_decode_attn(cache, q_d, pt, sel, n_sel, seq, out_e, lse_e)
+        run_step(cache, q_d, k_d, v_d, e_d, alive, resident, ts, 1000 + i, out_e, lse_e)
         res_h.copy_(res_d, non_blocking=True)
 
     def e2e_timed(run):
@@ -815,7 +830,9 @@ def run_native(args):
                        "page": 64, "subblock": 16, "k_q": k_q, "k_e": k_e, "resident_slots": N_SLOTS,
                        "step": "append+score+select+setdiff+lru+sparse_attn",
                        "launch": ("one CUDA graph per step (kernels chained by programmatic dependent launch); "
-                                  "append + score as one kernel, select + setdiff + lru as one fused kernel"),
+                                  "append + score as one kernel; " +
+                                  ("select + setdiff + lru as one fused kernel" if args.bookkeeping == "fused" else
+                                   "select, then setdiff + lru on a second stream beside the attention")),
                        "bytes_per_step": {kk: int(v) for kk, v in byts.items()},
                        "l2": ("no flush: each step reads ~0.81 GB of K/V pages and pooled-key sums, more "
                               "than the 129 MB L2, through evict-first loads" if args.l2 == "none" else
@@ -837,7 +854,7 @@ def run_native(args):
                     "launch": "one CUDA graph per step: copies in from pinned host memory, the API calls, "
                               "copies out; the host waits for each step's result",
                     "eager_ms_per_step": e2e_eager_ms},
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": (4 if args.bookkeeping == "fused" else 6) * args.steps,
             "eager_ms_per_step": eager_ms,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,

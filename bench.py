@@ -735,7 +735,8 @@ def run_native(args):
                  "workload": f"{Bc} prompts x {nc} tokens, window of the last {ac} rows, Hq {Hq} / Hk {Hk}",
                  "us": col_ms * 1e3, "flops": cflops, "bound": "tensor", "achieved_TFLOPs": ctf,
                  "peak": tpeak, "peak_kind": tkind + " bf16 dense (cuBLAS burst)", "frac": ctf / tpeak,
-                 "prompts_per_s": Bc / (col_ms * 1e-3), "launches": 2}
+                 "prompts_per_s": Bc / (col_ms * 1e-3),
+                 "launches": "one memset and one kernel (both 128-row chunks of the window in one grid)"}
         del ck, cq, cs
 
     # ---- offload: the 262k-context workload with its K/V pool in pinned host memory

@@ -272,8 +272,10 @@ int lazy_alibi_prefill_attn(spkv_cache_t cache, const void* q, int B, int T, int
  *   page_table : device int32 [B][np_max];  seq_len: device int32 [B] (alpha <= n <= 64 np_max,
  *                else SPKV_DEVERR_PAGE_ID and the row is zeros)
  *   scores     : device fp32 [B][Hq][64 np_max] (output)
- * alpha <= 1024 (else SPKV_EUNSUPPORTED), run as one launch per 128-row chunk of the window, the
- * later chunks adding into scores (so scores must not alias another live buffer between them).
+ * alpha <= 1024 (else SPKV_EUNSUPPORTED).  The window runs in 128-row chunks whose column sums
+ * add: up to 256 rows, both chunks in one grid adding atomically onto a zeroed scores buffer (two
+ * addends onto zero give the same sum in either order, so results are reproducible); more rows,
+ * one launch per chunk, later chunks adding in order.
  * B, Hq <= 65535. */
 int attn_column_scores(spkv_cache_t cache, const void* q, int B, int alpha, int Hq,
                        const int32_t* page_table, int np_max, const int32_t* seq_len,

@@ -399,8 +399,15 @@ int attn_column_scores(spkv_cache_t c, const void* q, int B, int alpha, int Hq, 
   p.seq_len = seq_len;
   p.scale_log2 = static_cast<float>(1.4426950408889634074 / std::sqrt(128.0));
   p.err = c->dev_err;
-  // one launch per 128-row chunk of the window: each row's softmax is its own, so the column sums
-  // of the chunks add; later chunks accumulate into the first one's result
+  // each row's softmax is its own, so the column sums of 128-row chunks of the window add.  Two
+  // chunks run in one grid, adding atomically onto a zeroed result (two addends onto zero give
+  // the same sum in either order); more run as one launch per chunk, later ones adding in order.
+  if (alpha > 128 && alpha <= 256) {
+    const size_t bytes = size_t(B) * Hq * size_t(np_max) * 64 * sizeof(float);
+    if (cudaMemsetAsync(scores, 0, bytes, as_stream(stream)) != cudaSuccess) return SPKV_ECUDA;
+    p.chunks_in_grid = 2;
+    return status_of(spkv::launch_colscore(c, p, as_stream(stream)));
+  }
   for (int r0 = 0; r0 < alpha; r0 += 128) {
     p.row0 = r0;
     p.rows = std::min(128, alpha - r0);

@@ -82,6 +82,10 @@ __global__ void __launch_bounds__(kCThreads, 1)
   ColSmem& S = *reinterpret_cast<ColSmem*>(stages + kCStages * kCStageBytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hq = blockIdx.x, b = blockIdx.y;
+  // the chunk of window rows: this launch's, or blockIdx.z's when both chunks share one grid
+  const bool in_grid = p.chunks_in_grid > 1;
+  const int row0 = in_grid ? 128 * static_cast<int>(blockIdx.z) : p.row0;
+  const int rows = in_grid ? min(128, p.alpha - row0) : p.rows;
   const int h = hq / p.G;
 
   if (tid == 0) {
@@ -111,8 +115,8 @@ __global__ void __launch_bounds__(kCThreads, 1)
   for (int i = tid; i < kCM * 16; i += kCThreads) {
     const int r = i >> 4, c = i & 15;
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < p.rows)
-      v = *reinterpret_cast<const uint4*>(p.q + ((int64_t(b) * p.alpha + p.row0 + r) * p.Hq + hq) * kHeadDim + 8 * c);
+    if (r < rows)
+      v = *reinterpret_cast<const uint4*>(p.q + ((int64_t(b) * p.alpha + row0 + r) * p.Hq + hq) * kHeadDim + 8 * c);
     *reinterpret_cast<uint4*>(sQ + (c >> 3) * (kCM * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
   }
   fence_proxy_async_smem();
@@ -203,7 +207,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
     const int t = (warp - 2) * 32 + lane;            // 0 .. 511
     const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + 32 * grp;
     const float scale = p.scale_log2;
-    const int row_min = n - p.alpha + p.row0;        // position of the chunk's first row
+    const int row_min = n - p.alpha + row0;          // position of the chunk's first row
     const int row_pos = row_min + r;                 // position of query row r
     float m = -CUDART_INF_F, l = 0.f, lse2 = CUDART_INF_F;
     bool ok = true;
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
           const float mq = S.ml[q][0][r];
           ll += mq == -CUDART_INF_F ? 0.f : S.ml[q][1][r] * fast_exp2(mq - mm);
         }
-        lse2 = (r < p.rows && ll > 0.f) ? mm + log2f(ll) : CUDART_INF_F;
+        lse2 = (r < rows && ll > 0.f) ? mm + log2f(ll) : CUDART_INF_F;
       }
       tc_fence_after();
       uint32_t sv[32];
@@ -327,7 +331,10 @@ __global__ void __launch_bounds__(kCThreads, 1)
             const int cc = 32 * grp + lane;
             const float sum = (S.part[slot][0][cc] + S.part[slot][1][cc]) + (S.part[slot][2][cc] + S.part[slot][3][cc]);
             const int key = key0 + lane;                 // keys from n on are zeroed below
-            if (key < n) srow[key] = p.accumulate ? srow[key] + sum : sum;
+            if (key < n) {
+              if (in_grid) atomicAdd(&srow[key], sum);
+              else srow[key] = p.accumulate ? srow[key] + sum : sum;
+            }
             __syncwarp();
             if (lane == 0) S.cnt[slot][grp] = 0;        // reused three jobs later
           }
@@ -336,7 +343,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
     }
     if (!ok && lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
     // positions from the prompt's end on (all of them for a rejected request) are zero
-    if (!p.accumulate)
+    if (!p.accumulate && !in_grid)
       for (int i = (valid_req ? n : 0) + t; i < p.np_max * kPageTokens; i += kMathThreads) srow[i] = 0.f;
   }
 
@@ -355,7 +362,8 @@ cudaError_t colscore_init_attributes() {
 }
 
 cudaError_t launch_colscore(const spkv_cache* c, const ColScoreParams& p, cudaStream_t st) {
-  return launch_pdl(colscore_kernel, dim3(p.Hq, p.B), dim3(kCThreads), kColSmem, st, c->tmap_k, p);
+  return launch_pdl(colscore_kernel, dim3(p.Hq, p.B, p.chunks_in_grid > 1 ? p.chunks_in_grid : 1), dim3(kCThreads),
+                    kColSmem, st, c->tmap_k, p);
 }
 
 }  // namespace spkv

@@ -118,6 +118,8 @@ struct ColScoreParams {
   int B, alpha, Hq, Hk, G;
   int row0, rows;                // this launch's chunk: window rows row0 .. row0 + rows - 1 (rows <= 128)
   int accumulate;                // 0: write the chunk's sums (first chunk), 1: add them
+  int chunks_in_grid;            // 2: blockIdx.z is the chunk (rows 128 z ..), sums added atomically
+                                 // onto a zeroed row (two addends onto zero: order-independent)
   int64_t n_phys;
   const int32_t* page_table;     // [B][np_max]
   int np_max;

@@ -66,6 +66,25 @@ def test_column_scores_windows_over_one_tile(n, alpha):
         _check(S[0, it], ref[0, it], alpha, n)
 
 
+def test_column_scores_two_chunk_grid_is_reproducible():
+    """A window of 129..256 rows runs both 128-row chunks in one grid, adding onto a zeroed row; two
+    addends onto zero round the same in either order, so repeated calls agree bit for bit."""
+    w = gen.sparse_workload(2, 8, 2, 64 * 9 + 3, 4, 4, seed=33)
+    q = gen.rows_bf16(33, 325, 2 * 200 * 8).reshape(2, 200, 8, 128)
+    d = Dev(w)
+    outs = []
+    for _ in range(3):
+        out = torch.full((2, 8, w["np_max"] * 64), float("nan"), dtype=torch.float32, device=DEV)
+        spkv.attn_column_scores(d.cache, bf(q), d.pt, i32(w["seq_len"]), out)
+        outs.append(out.cpu().numpy())
+    assert d.errors() == (0, 0)
+    d.close()
+    assert all(np.array_equal(outs[0].view(np.uint32), o.view(np.uint32)) for o in outs[1:])
+    ref = oracle.column_scores_batch(q, w["k_pool"], w["page_table"], w["seq_len"], w["np_max"] * 64)
+    for b in range(2):
+        _check(outs[0][b], ref[b], 200, int(w["seq_len"][b]))
+
+
 def test_column_scores_window_limit():
     w = gen.sparse_workload(1, 8, 2, 2048, 4, 4, seed=3)
     d = Dev(w)

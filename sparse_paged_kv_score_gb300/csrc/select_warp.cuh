@@ -25,28 +25,39 @@ __device__ __forceinline__ uint32_t warp_topk(const uint32_t (&key)[R], uint32_t
   const int nc = __reduce_add_sync(0xffffffffu, __popc(cand));
   if (k <= 0) return 0u;
   if (nc <= k) return cand;
-  uint32_t prefix = 0;
-  int remaining = k;
-  for (int bit = 31; bit >= 0; --bit) {
+  // The k-th largest key starts with `prefix` (its bits under hmask), `remaining` of the
+  // candidates that start with it are still to be taken, and `in_group` candidates do.  Once the
+  // two are equal, every key of the group is taken and the search can stop.
+  uint32_t prefix = 0, hmask = 0;
+  int remaining = k, in_group = nc;
+  for (int bit = 31; bit >= 0 && in_group != remaining; --bit) {
     const uint32_t trial = prefix | (1u << bit);
-    const uint32_t hmask = ~((1u << bit) - 1u);   // bits >= bit
+    const uint32_t hm = ~((1u << bit) - 1u);   // bits >= bit
     int c4[4] = {0, 0, 0, 0};   // four partial counts: short dependency chains
 #pragma unroll
-    for (int r = 0; r < R; ++r) c4[r & 3] += (key[r] & hmask) == trial;
+    for (int r = 0; r < R; ++r) c4[r & 3] += (key[r] & hm) == trial;
     const int c = __reduce_add_sync(0xffffffffu, (c4[0] + c4[1]) + (c4[2] + c4[3]));
-    if (c >= remaining) prefix = trial;
-    else remaining -= c;
+    hmask = hm;
+    if (c >= remaining) {
+      prefix = trial;
+      in_group = c;
+    } else {
+      remaining -= c;
+      in_group -= c;
+    }
   }
-  // prefix is the k-th largest key; take every larger key and the first `remaining` equal ones
+  // take every key above the group, and the first `remaining` of the group in page order (all of
+  // it when the search stopped early; after all 32 bits the group is the keys equal to the k-th)
   uint32_t take = 0;
   int seen = 0;
   const uint32_t lt = (1u << lane) - 1u;
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     const bool c = (cand >> r) & 1u;
-    const bool eq = c && key[r] == prefix;
+    const uint32_t km = key[r] & hmask;
+    const bool eq = c && km == prefix;
     const unsigned bal = __ballot_sync(0xffffffffu, eq);
-    const bool pick = (c && key[r] > prefix) || (eq && seen + __popc(bal & lt) < remaining);
+    const bool pick = (c && km > prefix) || (eq && seen + __popc(bal & lt) < remaining);
     take |= static_cast<uint32_t>(pick) << r;
     seen += __popc(bal);
   }

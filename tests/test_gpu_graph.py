@@ -88,3 +88,56 @@ def test_graph_replayed_steps_equal_eager_steps():
     assert spkv.get_device_error(graphed.cache) == (0, 0)
     eager.cache.close()
     graphed.cache.close()
+
+
+def test_bookkeeping_beside_attention_equals_fused_schedule():
+    """The bench's default step runs the selection, then the set-difference and LRU update on a
+    second stream while the attention streams its pages (it does not read their results), joining
+    before the next step.  Over six steps, eagerly and replayed from CUDA graphs, every output and
+    the residency state equal the fused schedule's bit for bit."""
+    w = gen.llama8b(seed=4, B=4)
+    B, Hq, Hk = w["B"], w["Hq"], w["Hk"]
+    n = 6
+    qs = [bf(gen.rows_bf16(4, 100 + i, B * Hq).reshape(B, Hq, 128)) for i in range(n)]
+    evs = [torch.from_numpy(gen.normal_f64(4, 200 + i, B * Hk * w["np_max"]).astype(np.float32)
+                            .reshape(B, Hk, w["np_max"])).to(DEV) for i in range(n)]
+    kn = [bf(gen.rows_bf16(4, 300 + i, B * Hk).reshape(B, Hk, 128)) for i in range(n)]
+    vn = [bf(gen.rows_bf16(4, 400 + i, B * Hk).reshape(B, Hk, 128)) for i in range(n)]
+    side = torch.cuda.Stream()
+
+    def overlap(st, i):
+        spkv.decode_append_score(st.cache, kn[i], vn[i], qs[i], st.pt, st.seq, st.scores)
+        spkv.select_topk(st.cache, st.scores, evs[i], st.alive, st.seq, st.k_q, st.k_e, st.sel, st.n_sel)
+        main = torch.cuda.current_stream()
+        side.wait_stream(main)
+        with torch.cuda.stream(side):
+            spkv.resident_setdiff(st.cache, st.resident, st.sel, st.n_sel, st.missing, st.n_missing, st.slot)
+            spkv.lru_bucket_update(st.cache, st.resident, st.ts, st.slot, st.n_sel, st.missing, st.n_missing, i, 1,
+                                   st.victims, st.hist)
+        spkv.sparse_decode_attn(st.cache, qs[i], st.pt, st.sel, st.n_sel, st.seq, st.out, st.lse)
+        main.wait_stream(side)
+
+    fused, eager, graphed = _Step(w), _Step(w), _Step(w)
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    graphs = []
+    for i in range(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            overlap(graphed, i)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    for i in range(n):
+        fused.run(qs[i], evs[i], kn[i], vn[i], i)
+        overlap(eager, i)
+        graphs[i].replay()
+        torch.cuda.synchronize()
+        ref = fused.state() + [fused.missing.clone(), fused.n_missing.clone(), fused.slot.clone()]
+        for st in (eager, graphed):
+            got = st.state() + [st.missing.clone(), st.n_missing.clone(), st.slot.clone()]
+            for a, b in zip(ref, got):
+                assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
+                                   b.view(torch.int16) if b.dtype == torch.bfloat16 else b), f"step {i}"
+    for st in (fused, eager, graphed):
+        assert spkv.get_device_error(st.cache) == (0, 0)
+        st.cache.close()

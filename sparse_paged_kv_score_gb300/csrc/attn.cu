@@ -100,7 +100,11 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk) {
   return base + ((chunk >> 3) * kBoxBytes) + row * 128 + ((((chunk & 7) ^ (row & 7))) << 4);
 }
 
-template <int NT, bool LAZY, int STAGES>
+// PACK (groups of at most 4 query heads, NT == 1): the 8 columns of each MMA's query operand
+// hold the group's heads twice.  Columns 4..7 carry the bf16 lo part of what columns 0..3 carry
+// in hi (the rotated query in the lazy form, the probabilities P), so one MMA does the work of
+// the hi MMA and the lo MMA; the halves are added where a full value is needed.
+template <int NT, bool LAZY, bool PACK, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                       const __grid_constant__ AttnParams p) {
@@ -397,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float m[NT][2], lsum[NT][2];
   float O[8][NT][4];
   uint32_t qh[8][NT][2];                  // B fragments of q (bf16 hi part)
-  uint32_t ql[LAZY ? 8 : 1][NT][2];       // lazy: bf16 lo part of the rotated query
+  uint32_t ql[LAZY && !PACK ? 8 : 1][NT][2];   // lazy: bf16 lo part of the rotated query
   uint32_t qraw[LAZY ? 8 : 1][NT][2];     // lazy: unrotated query
   int cur_u = -1, cur_c = -1, cur_us = 0, cur_uc = 0, cur_rel = 0, n_flush = 0;
   bool have_rel = false;
@@ -419,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t* qw = reinterpret_cast<const uint32_t*>(qs);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int g = nt * 8 + r;
+      const int g = PACK ? (r & 3) : nt * 8 + r;
       const bool live = g < p.G;
       const int row = (live ? g : 0) * (kHeadDim / 2);
 #pragma unroll
@@ -464,10 +468,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           split_bf16(x1 * cs[1] - y1 * sn[1], xh1, xl1);
           split_bf16(y0 * cs[0] + x0 * sn[0], yh0, yl0);
           split_bf16(y1 * cs[1] + x1 * sn[1], yh1, yl1);
-          qh[ks][nt][wi] = pack_bf16x2(xh0, xh1);
-          ql[LAZY ? ks : 0][nt][wi] = pack_bf16x2(xl0, xl1);
-          qh[ks + 4][nt][wi] = pack_bf16x2(yh0, yh1);
-          ql[LAZY ? ks + 4 : 0][nt][wi] = pack_bf16x2(yl0, yl1);
+          if (PACK) {   // columns 0..3 (r < 4) take the hi part, columns 4..7 the lo part
+            const bool hi = r < 4;
+            qh[ks][nt][wi] = pack_bf16x2(hi ? xh0 : xl0, hi ? xh1 : xl1);
+            qh[ks + 4][nt][wi] = pack_bf16x2(hi ? yh0 : yl0, hi ? yh1 : yl1);
+          } else {
+            qh[ks][nt][wi] = pack_bf16x2(xh0, xh1);
+            ql[LAZY && !PACK ? ks : 0][nt][wi] = pack_bf16x2(xl0, xl1);
+            qh[ks + 4][nt][wi] = pack_bf16x2(yh0, yh1);
+            ql[LAZY && !PACK ? ks + 4 : 0][nt][wi] = pack_bf16x2(yl0, yl1);
+          }
         }
       }
     }
@@ -479,6 +489,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(&S.cempty, (n_flush - 1) & 1))) {
         if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
       }
+    }
+    if (PACK) {   // O = V^T P_hi (columns 0..3) + V^T P_lo (columns 4..7)
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) O[j][0][e] += __shfl_xor_sync(0xffffffffu, O[j][0][e], 2);
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -557,8 +573,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           mma_bf16_16816(acc[nt], a, qh[ks][nt][0], qh[ks][nt][1]);
-          if (LAZY) mma_bf16_16816(acc[nt], a, ql[LAZY ? ks : 0][nt][0], ql[LAZY ? ks : 0][nt][1]);
+          if (LAZY && !PACK) mma_bf16_16816(acc[nt], a, ql[LAZY && !PACK ? ks : 0][nt][0], ql[LAZY && !PACK ? ks : 0][nt][1]);
         }
+      }
+      if (LAZY && PACK) {
+        // hi-part scores (columns 0..3) + lo-part scores (columns 4..7), in both halves alike
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[0][e] += __shfl_xor_sync(0xffffffffu, acc[0][e], 2);
       }
       // ---- online softmax (log2 domain) on my 16 rows
       const bool row0_ok = t0 + r < mt.valid, row1_ok = t0 + r + 8 < mt.valid;
@@ -594,10 +615,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         split_bf16(pv[1], h1, l1);
         split_bf16(pv[2], h2, l2);
         split_bf16(pv[3], h3, l3);
-        bh[nt][0] = movmatrix_trans(pack_bf16x2(h0, h1));
-        bh[nt][1] = movmatrix_trans(pack_bf16x2(h2, h3));
-        bl[nt][0] = movmatrix_trans(pack_bf16x2(l0, l1));
-        bl[nt][1] = movmatrix_trans(pack_bf16x2(l2, l3));
+        if (PACK) {   // both column halves hold the same P: columns 0..3 keep hi, 4..7 lo
+          const bool hi = c < 2;
+          bh[nt][0] = movmatrix_trans(pack_bf16x2(hi ? h0 : l0, hi ? h1 : l1));
+          bh[nt][1] = movmatrix_trans(pack_bf16x2(hi ? h2 : l2, hi ? h3 : l3));
+        } else {
+          bh[nt][0] = movmatrix_trans(pack_bf16x2(h0, h1));
+          bh[nt][1] = movmatrix_trans(pack_bf16x2(h2, h3));
+          bl[nt][0] = movmatrix_trans(pack_bf16x2(l0, l1));
+          bl[nt][1] = movmatrix_trans(pack_bf16x2(l2, l3));
+        }
       }
       // ---- O^T += V^T P^T for my 16 keys
       const bool partial = mt.valid < t0 + 16;
@@ -620,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           mma_bf16_16816(O[j][nt], a, bh[nt][0], bh[nt][1]);
-          mma_bf16_16816(O[j][nt], a, bl[nt][0], bl[nt][1]);
+          if (!PACK) mma_bf16_16816(O[j][nt], a, bl[nt][0], bl[nt][1]);
         }
       }
     }
@@ -683,15 +710,15 @@ __global__ void __launch_bounds__(kCombineHeads * kHeadDim)
   }
 }
 
-template <int NT, bool LAZY, int STAGES>
+template <int NT, bool LAZY, bool PACK, int STAGES>
 cudaError_t set_attr() {
-  return cudaFuncSetAttribute(attn_split_kernel<NT, LAZY, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(attn_split_kernel<NT, LAZY, PACK, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(smem_bytes<NT, STAGES>()));
 }
 
-template <int NT, bool LAZY, int STAGES>
+template <int NT, bool LAZY, bool PACK, int STAGES>
 cudaError_t launch_one(const spkv_cache* c, const AttnParams& p, int grid, cudaStream_t st) {
-  cudaError_t e = launch_pdl(attn_split_kernel<NT, LAZY, STAGES>, dim3(grid), dim3(kThreads),
+  cudaError_t e = launch_pdl(attn_split_kernel<NT, LAZY, PACK, STAGES>, dim3(grid), dim3(kThreads),
                              smem_bytes<NT, STAGES>(), st, c->tmap_k, c->tmap_v, p);
   if (e != cudaSuccess) return e;
   return launch_pdl(attn_combine_kernel, dim3(p.B * p.Hk), dim3(kCombineHeads * kHeadDim), 0, st, p);
@@ -704,10 +731,11 @@ constexpr int kStages2 = 4;   // G <= 16: 4 stages of 36 KiB
 
 cudaError_t attn_init_attributes() {
   cudaError_t e;
-  if ((e = set_attr<1, false, kStages1>()) != cudaSuccess) return e;
-  if ((e = set_attr<1, true, kStages1>()) != cudaSuccess) return e;
-  if ((e = set_attr<2, false, kStages2>()) != cudaSuccess) return e;
-  return set_attr<2, true, kStages2>();
+  if ((e = set_attr<1, true, true, kStages1>()) != cudaSuccess) return e;
+  if ((e = set_attr<1, false, false, kStages1>()) != cudaSuccess) return e;
+  if ((e = set_attr<1, true, false, kStages1>()) != cudaSuccess) return e;
+  if ((e = set_attr<2, false, false, kStages2>()) != cudaSuccess) return e;
+  return set_attr<2, true, false, kStages2>();
 }
 
 size_t attn_smem_bytes(int G, bool lazy) {
@@ -716,10 +744,16 @@ size_t attn_smem_bytes(int G, bool lazy) {
 }
 
 cudaError_t launch_attn(const spkv_cache* c, const AttnParams& p, bool lazy, int grid, cudaStream_t st) {
+  // PACK only in the lazy form: it saves the lo MMAs of the rotated query and of P, and there
+  // the consumer arithmetic shows in the time; the stored-RoPE form streams at the same rate
+  // with or without it.
+  if (lazy && p.G <= 4) return launch_one<1, true, true, kStages1>(c, p, grid, st);
   if (p.G <= 8) {
-    return lazy ? launch_one<1, true, kStages1>(c, p, grid, st) : launch_one<1, false, kStages1>(c, p, grid, st);
+    return lazy ? launch_one<1, true, false, kStages1>(c, p, grid, st)
+                : launch_one<1, false, false, kStages1>(c, p, grid, st);
   }
-  return lazy ? launch_one<2, true, kStages2>(c, p, grid, st) : launch_one<2, false, kStages2>(c, p, grid, st);
+  return lazy ? launch_one<2, true, false, kStages2>(c, p, grid, st)
+              : launch_one<2, false, false, kStages2>(c, p, grid, st);
 }
 
 }  // namespace spkv

@@ -356,7 +356,7 @@ def _random_lists(w, rng, stride, lens=None):
 
 
 @pytest.mark.parametrize("B,Hq,Hk", [(1, 8, 2), (5, 16, 4), (3, 40, 8), (2, 16, 1), (4, 8, 8),
-                                     (2, 40, 4)])
+                                     (2, 40, 4), (3, 6, 2), (2, 6, 3)])
 def test_sparse_attn_random_lists(B, Hq, Hk):
     rng = np.random.default_rng(B * 100 + Hq + Hk)
     w = gen.sparse_workload(B, Hq, Hk, 64 * 48, 8, 8, seed=B + Hq, outlier_p=0.01)
@@ -453,7 +453,7 @@ def _words(phys, valid, slot):
     return words
 
 
-@pytest.mark.parametrize("seed,Hq,Hk", [(1, 16, 4), (2, 32, 8), (3, 8, 1)])
+@pytest.mark.parametrize("seed,Hq,Hk", [(1, 16, 4), (2, 32, 8), (3, 8, 1), (4, 12, 4), (5, 4, 4)])
 def test_lazy_rope_vs_materialised_oracle(seed, Hq, Hk):
     w = gen.lazy_rag(seed=seed, B=6, Hq=Hq, Hk=Hk, n_docs=20, docs_per_req=4, min_len=100, max_len=2000)
     cache, keep = _lazy_dev(w)

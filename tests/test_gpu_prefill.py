@@ -110,6 +110,50 @@ def test_prefill_long_documents_rescale_path():
     _check(np.array(sel_o), np.array(sel_l), np.array(sel_r), np.array(sel_rl))
 
 
+def test_prefill_row_maximum_growing_inside_a_page_group():
+    """A row's maximum jumping by more than 2^8 inside a group of two pages: keys set to zero
+    before, and keys scaled x3 in, the last 32 tokens of (A) a request's first page (the first
+    group's second 32-key block) and (B) the fourth page of another request's first document
+    (the second group's fourth block: O is rescaled there).  With keys three times the unit
+    scale, the bf16 rounding of the rotated query moves their scores three times as much, so
+    this case allows three times the attention and LSE tolerances."""
+    w = gen.lazy_rag(seed=13, B=3, Hq=8, Hk=2, n_docs=6, docs_per_req=3, min_len=300, max_len=900)
+    B = w["B"]
+    kp = gen.bf16_to_f32(w["k_pool"])
+
+    def first_doc(b):
+        n = int(w["n_pages"][b])
+        sl = w["slot"][b, :n]
+        end = next((i for i in range(1, n) if sl[i] != sl[0]), n)
+        return w["phys"][b, :end], w["valid"][b, :end]
+
+    pa, va = first_doc(0)
+    assert va[0] == 64
+    kp[:, pa[0], 0:32] = 0.0
+    kp[:, pa[0], 32:64] *= np.float32(3.0)
+    case_b = False
+    for b in range(1, B):
+        pb, vb = first_doc(b)
+        if len(pb) >= 4 and (vb[:4] == 64).all() and not set(pb[:4].tolist()) & set(pa.tolist()):
+            kp[:, pb[:3]] = 0.0
+            kp[:, pb[3], 0:32] = 0.0
+            kp[:, pb[3], 32:64] *= np.float32(3.0)
+            case_b = True
+            break
+    assert case_b
+    w["k_pool"] = gen.f32_to_bf16(kp)
+    q = _queries(13, B, 70, 8, 1.0)
+    o, l = _run(w, q, w["phys"], w["valid"], w["slot"], w["n_pages"], w["qpos"], w["doc_pos"])
+    ro, rl = oracle.lazy_prefill_batch(q, w["k_pool"], w["v_pool"], w["phys"], w["valid"], w["slot"],
+                                       w["n_pages"], w["qpos"], w["doc_pos"], w["theta"], materialise=True)
+    mx, mean = attn_errors(o, ro)
+    assert mx <= 3 * ATTN_MAX and mean <= 3 * ATTN_MEAN, (mx, mean)
+    rel = np.linalg.norm((o - ro).ravel()) / np.linalg.norm(ro.ravel())
+    assert rel <= REL_L2, rel
+    assert np.isfinite(l).all()
+    assert np.abs(l - rl).max() <= 3 * LSE_TOL
+
+
 def test_prefill_per_head_page_lists_and_empty_request():
     """Per-kv-head page lists in a different order per head, and a request without pages."""
     w = gen.lazy_rag(seed=6, B=3, Hq=8, Hk=2, n_docs=10, docs_per_req=3, min_len=64, max_len=700)

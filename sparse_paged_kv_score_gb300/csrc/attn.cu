@@ -738,11 +738,6 @@ cudaError_t attn_init_attributes() {
   return set_attr<2, true, false, kStages2>();
 }
 
-size_t attn_smem_bytes(int G, bool lazy) {
-  (void)lazy;
-  return G <= 8 ? smem_bytes<1, kStages1>() : smem_bytes<2, kStages2>();
-}
-
 cudaError_t launch_attn(const spkv_cache* c, const AttnParams& p, bool lazy, int grid, cudaStream_t st) {
   // PACK only in the lazy form: it saves the lo MMAs of the rotated query and of P, and there
   // the consumer arithmetic shows in the time; the stored-RoPE form streams at the same rate

@@ -168,7 +168,6 @@ cudaError_t launch_select_resident(const spkv_cache* c, const float* qs, const f
 bool fused_supported(int np_max);
 
 // Shared-memory bytes the attention kernel needs for a group size (used for limits checks).
-size_t attn_smem_bytes(int G, bool lazy);
 cudaError_t attn_init_attributes();
 cudaError_t select_init_attributes();
 cudaError_t resid_init_attributes();

@@ -532,8 +532,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
 }  // namespace
 
-size_t prefill_smem_bytes() { return kPrefillSmem; }
-
 cudaError_t prefill_init_attributes() {
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kPrefillSmem));

@@ -561,10 +561,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t kb = stage0 + s * kStage;
       const uint32_t vb = kb + 2 * kBoxBytes;
-      // ---- S^T = K q^T for my 16 keys
-      float acc[NT][4];
+      // ---- S^T = K q^T for my 16 keys.  Lazy form: even and odd k-steps accumulate
+      // separately (two dependent MMA chains of half the length), then add; the stored-RoPE form
+      // keeps one chain (it streams at the same rate either way)
+      float acc[NT][4], acc2[NT][4];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] = acc2[nt][e] = 0.f;
       const int krow = t0 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
@@ -572,9 +576,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         ldsm_x4(swz(kb, krow, 2 * ks + (lane >> 4)), a);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          mma_bf16_16816(acc[nt], a, qh[ks][nt][0], qh[ks][nt][1]);
-          if (LAZY && !PACK) mma_bf16_16816(acc[nt], a, ql[LAZY && !PACK ? ks : 0][nt][0], ql[LAZY && !PACK ? ks : 0][nt][1]);
+          float (&d)[4] = (LAZY && (ks & 1)) ? acc2[nt] : acc[nt];
+          mma_bf16_16816(d, a, qh[ks][nt][0], qh[ks][nt][1]);
+          if (LAZY && !PACK) mma_bf16_16816(d, a, ql[LAZY && !PACK ? ks : 0][nt][0], ql[LAZY && !PACK ? ks : 0][nt][1]);
         }
+      }
+      if (LAZY) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[nt][e] += acc2[nt][e];
       }
       if (LAZY && PACK) {
         // hi-part scores (columns 0..3) + lo-part scores (columns 4..7), in both halves alike

@@ -59,7 +59,9 @@ __host__ __device__ constexpr uint32_t o_col(int x) { return 128u * x; }
 __host__ __device__ constexpr uint32_t s_col(int x) { return 256u + 128u * x; }
 
 struct PrefillSmem {
-  uint64_t full[kStages], empty[kStages];
+  // K and V halves of each ring slot fill and free on their own: a slot's K is free once both
+  // tiles' QK have read it, its V once both tiles' PV have
+  uint64_t fullK[kStages], emptyK[kStages], fullV[kStages], emptyV[kStages];
   uint64_t sfull[kTiles], pready[kTiles], pvdone[kTiles], qready[kTiles];
   uint64_t drain;
   uint32_t tmem_base;
@@ -139,8 +141,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], 1);
+      mbar_init(&S.fullK[s], 1);
+      mbar_init(&S.emptyK[s], 1);
+      mbar_init(&S.fullV[s], 1);
+      mbar_init(&S.emptyV[s], 1);
     }
     for (int x = 0; x < kTiles; ++x) {
       mbar_init(&S.sfull[x], 1);
@@ -176,12 +180,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
       tma_prefetch_l2_3d(&tmv, 0, 0, z);
       tma_prefetch_l2_3d(&tmv, 64, 0, z);
     };
-    auto load_page = [&](uint8_t* st, int half_off, const PageInfo& pi, uint64_t* bar) {
+    // K (v = false) or V (v = true) rows of one page into the slot's half for page a or b
+    auto load_page = [&](uint8_t* st, int half_off, const PageInfo& pi, uint64_t* bar, bool v) {
       const int z = static_cast<int>(int64_t(h) * p.n_phys + pi.phys);
-      tma_load_3d(st + half_off, &tmk, bar, 0, 0, z, pol);
-      tma_load_3d(st + kGBox + half_off, &tmk, bar, 64, 0, z, pol);
-      tma_load_3d(st + 2 * kGBox + half_off, &tmv, bar, 0, 0, z, pol);
-      tma_load_3d(st + 3 * kGBox + half_off, &tmv, bar, 64, 0, z, pol);
+      uint8_t* dst = st + (v ? 2 * kGBox : 0) + half_off;
+      tma_load_3d(dst, v ? &tmv : &tmk, bar, 0, 0, z, pol);
+      tma_load_3d(dst + kGBox, v ? &tmv : &tmk, bar, 64, 0, z, pol);
     };
     if (lane == 0) {
       for (int jj = 0; jj < n; ++jj) {   // flag malformed page words once
@@ -196,28 +200,48 @@ __global__ void __launch_bounds__(kPThreads, 1)
     for (; j < n; ++g) {
       const Group gr = group_at(p, b, h, j, n);
       const int s = g % kStages;
-      if (g >= kStages && !warp_wait(&S.empty[s], ((g / kStages) - 1) & 1)) {
+      uint8_t* st = stages + s * kStageBytes;
+      const uint32_t bytes = (gr.a.valid > 0 ? 2 * kBox : 0) + (gr.size == 2 && gr.b.valid > 0 ? 2 * kBox : 0);
+      // K of the group, once both tiles' QK of the slot's previous group have completed
+      if (g >= kStages && !warp_wait(&S.emptyK[s], ((g / kStages) - 1) & 1)) {
         if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
         break;
       }
       if (lane == 0) {
         for (int jj = j + 2 * kStages + kPrefetch; jj < min(n, j + gr.size + 2 * kStages + kPrefetch); ++jj)
           prefetch(jj);
-        uint8_t* st = stages + s * kStageBytes;
-        const uint32_t bytes = (gr.a.valid > 0 ? 4 * kBox : 0) + (gr.size == 2 && gr.b.valid > 0 ? 4 * kBox : 0);
         if (bytes) {
-          mbar_arrive_expect_tx(&S.full[s], bytes);
-          if (gr.a.valid > 0) load_page(st, 0, gr.a, &S.full[s]);
-          if (gr.size == 2 && gr.b.valid > 0) load_page(st, kBox, gr.b, &S.full[s]);
+          mbar_arrive_expect_tx(&S.fullK[s], bytes);
+          if (gr.a.valid > 0) load_page(st, 0, gr.a, &S.fullK[s], false);
+          if (gr.size == 2 && gr.b.valid > 0) load_page(st, kBox, gr.b, &S.fullK[s], false);
         } else {
-          mbar_arrive(&S.full[s]);
+          mbar_arrive(&S.fullK[s]);
+        }
+      }
+      __syncwarp();
+      // V of the group, once both tiles' PV of the slot's previous group have completed
+      if (g >= kStages && !warp_wait(&S.emptyV[s], ((g / kStages) - 1) & 1)) {
+        if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
+        mbar_wait(&S.fullK[s], (g / kStages) & 1);   // this group's K copy must not be in flight at exit
+        break;
+      }
+      if (lane == 0) {
+        if (bytes) {
+          mbar_arrive_expect_tx(&S.fullV[s], bytes);
+          if (gr.a.valid > 0) load_page(st, 0, gr.a, &S.fullV[s], true);
+          if (gr.size == 2 && gr.b.valid > 0) load_page(st, kBox, gr.b, &S.fullV[s], true);
+        } else {
+          mbar_arrive(&S.fullV[s]);
         }
       }
       __syncwarp();
       j += gr.size;
     }
     // no copy of this CTA may still be in flight when it exits
-    for (int i = g > kStages ? g - kStages : 0; i < g; ++i) mbar_wait(&S.full[i % kStages], (i / kStages) & 1);
+    for (int i = g > kStages ? g - kStages : 0; i < g; ++i) {
+      mbar_wait(&S.fullK[i % kStages], (i / kStages) & 1);
+      mbar_wait(&S.fullV[i % kStages], (i / kStages) & 1);
+    }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
     constexpr uint32_t kIdS64 = umma_idesc_bf16(kPM, 64, false);
@@ -243,18 +267,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
       __syncwarp();
       return true;
     };
-    for (int j = 0; j < n && ok; ++g) {
-      const Group gr = group_at(p, b, h, j, n);
-      const int s = g % kStages;
-      if (!warp_wait(&S.full[s], (g / kStages) & 1)) {
-        ok = false;
-        break;
-      }
-      // rows past a page's valid tokens are multiplied by P = 0: make them exact zeros
-      for (int pg = 0; pg < gr.size; ++pg) {
-        const int valid = pg == 0 ? gr.a.valid : gr.b.valid;
+    // V of group gg (pages of gp) in its slot; rows past a page's valid tokens are multiplied by
+    // P = 0, so they are made exact zeros first
+    auto wait_v = [&](int gg, const Group& gp) -> bool {
+      if (!warp_wait(&S.fullV[gg % kStages], (gg / kStages) & 1)) return false;
+      for (int pg = 0; pg < gp.size; ++pg) {
+        const int valid = pg == 0 ? gp.a.valid : gp.b.valid;
         if (valid == 64) continue;
-        uint8_t* vt = stages + s * kStageBytes + 2 * kGBox + pg * kBox;
+        uint8_t* vt = stages + (gg % kStages) * kStageBytes + 2 * kGBox + pg * kBox;
         for (int i = lane; i < (64 - valid) * 16; i += 32) {
           const int row = valid + (i >> 4), c = i & 15;
           *reinterpret_cast<uint4*>(vt + (c >> 3) * kGBox + row * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
@@ -262,12 +282,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       fence_proxy_async_smem();
       __syncwarp();
+      return true;
+    };
+    Group prev_gr{};
+    for (int j = 0; j < n && ok; ++g) {
+      const Group gr = group_at(p, b, h, j, n);
+      const int s = g % kStages;
+      if (!warp_wait(&S.fullK[s], (g / kStages) & 1)) {
+        ok = false;
+        break;
+      }
       const bool new_doc = ALIBI ? g == 0 : gr.a.slot != prev_slot;
       prev_slot = gr.a.slot;
       for (int x = 0; x < n_tiles && ok; ++x) {
         // PV of the previous group reads P_x from the columns the QK below overwrites; MMAs of
         // one thread run in issue order
-        if (g >= 1 && !issue_pv(x, g - 1, prev_size)) {
+        if (g >= 1 && ((x == 0 && !wait_v(g - 1, prev_gr)) || !issue_pv(x, g - 1, prev_size))) {
           ok = false;
           break;
         }
@@ -288,15 +318,20 @@ __global__ void __launch_bounds__(kPThreads, 1)
         __syncwarp();
       }
       if (!ok) break;
-      if (g >= 1 && lane == 0) umma_commit(&S.empty[(g - 1) % kStages]);   // group g - 1 fully consumed
+      if (lane == 0) {
+        umma_commit(&S.emptyK[s]);                                 // both tiles' QK of group g
+        if (g >= 1) umma_commit(&S.emptyV[(g - 1) % kStages]);    // both tiles' PV of group g - 1
+      }
       __syncwarp();
       if (new_doc) ++n_docs;
+      prev_gr = gr;
       prev_size = gr.size;
       j += gr.size;
     }
     if (ok && g > 0) {
+      ok = wait_v(g - 1, prev_gr);
       for (int x = 0; x < n_tiles && ok; ++x) ok = issue_pv(x, g - 1, prev_size);
-      if (ok && lane == 0) umma_commit(&S.empty[(g - 1) % kStages]);
+      if (ok && lane == 0) umma_commit(&S.emptyV[(g - 1) % kStages]);
     }
     if (!ok && lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
     // every MMA issued has completed before TMEM is released

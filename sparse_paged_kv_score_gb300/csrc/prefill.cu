@@ -352,6 +352,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int pos = p.qpos0[b] + t;
     const float scale = p.scale_log2;
     const float slope_l2 = ALIBI ? p.slopes[hq] * 1.4426950408889634f : 0.f;   // bias slope, log2 units
+    float cslope[ALIBI ? 32 : 1];   // ALiBi: c slope for the 32 columns of a block
+#pragma unroll
+    for (int c = 0; c < (ALIBI ? 32 : 1); ++c) cslope[c] = static_cast<float>(c) * slope_l2;
     const int64_t ps_row = (int64_t(b) * p.meta_heads + (p.meta_heads == 1 ? 0 : h)) * p.np_max;
     float m = -CUDART_INF_F, l = 0.f;
     int prev_slot = -1, g = 0;
@@ -425,19 +428,24 @@ __global__ void __launch_bounds__(kPThreads, 1)
         tmem_ld32(lane_addr + s_col(x) + 32 * k, sv);
         tmem_wait_ld();
         const int lim = (k < 2 ? va : vb) - 32 * (k & 1);   // valid columns of this block
-        if (ALIBI) {   // the maximum of s scale + bias
+        if (ALIBI) {   // the maximum of s scale + bias: of s scale + c slope, plus the block's cb
           const float cb = (k < 2 ? cb_a : cb_b) + slope_l2 * static_cast<float>(32 * (k & 1));
+          float bm8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) bm8[e] = -CUDART_INF_F;
           if (full) {
 #pragma unroll
             for (int c = 0; c < 32; ++c)
-              mx8[c & 7] = fmaxf(mx8[c & 7], fmaf(__uint_as_float(sv[c]), scale, fmaf(static_cast<float>(c), slope_l2, cb)));
+              bm8[c & 7] = fmaxf(bm8[c & 7], fmaf(__uint_as_float(sv[c]), scale, cslope[ALIBI ? c : 0]));
           } else {
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-              const float a = fmaf(__uint_as_float(sv[c]), scale, fmaf(static_cast<float>(c), slope_l2, cb));
-              mx8[c & 7] = fmaxf(mx8[c & 7], c < lim ? a : -CUDART_INF_F);
+              const float a = fmaf(__uint_as_float(sv[c]), scale, cslope[ALIBI ? c : 0]);
+              bm8[c & 7] = fmaxf(bm8[c & 7], c < lim ? a : -CUDART_INF_F);
             }
           }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], bm8[e] + cb);
         } else if (full) {   // the maximum of s (scale > 0 is applied once below); every column valid
 #pragma unroll
           for (int c = 0; c < 32; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(sv[c]));

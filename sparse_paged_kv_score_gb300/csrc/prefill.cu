@@ -116,6 +116,22 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
+// Two fp32 lanes at once (Blackwell's packed f32x2 forms); each lane rounds as fma.rn.f32 /
+// add.rn.f32 would.
+__device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                          float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add_f32x2(float& d0, float& d1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %3};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -504,15 +520,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // ALiBi: column c adds c slope to the block's bias; RoPE: no bias
         const float cbm = ALIBI ? (k < 2 ? cb_a : cb_b) + slope_l2 * static_cast<float>(32 * (k & 1)) + mneg : mneg;
         uint32_t pw[16];
-        if (full && have_m) {   // every column valid: no masking
+        if (full && have_m) {   // every column valid: no masking; column pairs in packed f32x2 form
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
-            const float b0 = ALIBI ? fmaf(static_cast<float>(c), slope_l2, cbm) : mneg;
-            const float b1 = ALIBI ? fmaf(static_cast<float>(c + 1), slope_l2, cbm) : mneg;
-            const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c]), scale, b0));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), scale, b1));
-            ls8[c & 7] += p0;
-            ls8[(c + 1) & 7] += p1;
+            float b0 = mneg, b1 = mneg, e0, e1;
+            if (ALIBI)
+              fma_f32x2(b0, b1, static_cast<float>(c), static_cast<float>(c + 1), slope_l2, slope_l2, cbm, cbm);
+            fma_f32x2(e0, e1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), scale, scale, b0, b1);
+            const float p0 = fast_exp2(e0), p1 = fast_exp2(e1);
+            add_f32x2(ls8[c & 7], ls8[(c + 1) & 7], p0, p1);   // c even: two neighbouring sums
             pw[c >> 1] = pack_bf16x2(p0, p1);
           }
         } else {

@@ -278,7 +278,11 @@ __global__ void __launch_bounds__(kCThreads, 1)
         for (int k = 0; k < 4; ++k) ls4[k] = 0.f;
         if (full) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) ls4[c & 3] += fast_exp2(fmaf(__uint_as_float(sv[c]), scale, -m_new));
+          for (int c = 0; c < 32; c += 2) {   // column pairs in packed f32x2 form
+            float e0, e1;
+            fma_f32x2(e0, e1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), scale, scale, -m_new, -m_new);
+            add_f32x2(ls4[c & 3], ls4[(c + 1) & 3], fast_exp2(e0), fast_exp2(e1));   // c even: neighbouring sums
+          }
         } else {
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
@@ -298,7 +302,12 @@ __global__ void __launch_bounds__(kCThreads, 1)
           float v[32];                                     // rows past the chunk have lse2 = +inf
           if (full) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) v[c] = fast_exp2(fmaf(__uint_as_float(sv[c]), scale, -lse2));
+            for (int c = 0; c < 32; c += 2) {   // column pairs in packed f32x2 form
+              float e0, e1;
+              fma_f32x2(e0, e1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), scale, scale, -lse2, -lse2);
+              v[c] = fast_exp2(e0);
+              v[c + 1] = fast_exp2(e1);
+            }
           } else {
 #pragma unroll
             for (int c = 0; c < 32; ++c) {

@@ -16,8 +16,10 @@
 // of one document are taken in groups of two, so that a QK^T product is one N = 128 MMA tile.
 // Ten warps:
 //   warp 0     TMA producer: K and V of the group's pages (64 x 64 bf16 boxes, 128-byte swizzle;
-//              the two pages' rows stacked so each d-half is one 128-row tile) into a 2-stage
-//              ring, and L2 prefetches of the pages beyond it;
+//              the two pages' rows stacked so each d-half is one 128-row tile) into a 2-slot
+//              ring whose K and V halves fill and free on their own (a slot's K is reloaded once
+//              both tiles' QK have read it, its V once both PVs have), and L2 prefetches of the
+//              pages beyond it;
 //   warp 1     MMA issuer (one thread), per tile x in turn: O_x += P_x V_(g-1) (M 128, N 128,
 //              P read from tensor memory, V from shared memory as an MN-major operand), then
 //              S_x = Q_x K_g^T (M 128, N 64 or 128) into the same tensor-memory columns -- MMAs
@@ -44,7 +46,7 @@ namespace {
 
 constexpr int kPM = 128;                      // query rows per tile (TMEM lanes)
 constexpr int kTiles = 2;                     // query heads (tiles) per CTA
-constexpr int kStages = 2;                    // page-group ring
+constexpr int kStages = 2;                    // page-group ring slots (K and V halves freed apart)
 constexpr int kPrefetch = 8;                  // pages beyond the ring fetched into L2
 constexpr int kPThreads = 64 + kTiles * 128;
 constexpr int kBox = 64 * 128;                // one page's 64 rows x 128 B (one d-half), bytes

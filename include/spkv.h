@@ -366,16 +366,19 @@ int lru_bucket_update(spkv_cache_t cache, int32_t* resident, int32_t* ts, int n_
  * loading this library holds until the process exits.  The caller passes inputs and outputs.
  *   k_pool, v_pool : device bf16 [n_kv_heads][n_phys_pages][64][128], 16-byte aligned
  *   q              : device bf16 [B][Hq][128], 16-byte aligned
- *   dev_err        : device uint32, receives SPKV_DEVERR_* bits (OR-ed in); may be NULL, in
- *                    which case the bits go to a word inside the scratch that is not reported
+ *   dev_err        : device uint32 owned by the caller (required), receives SPKV_DEVERR_* bits
+ *                    (OR-ed in): out-of-range page ids and physical pages are skipped and
+ *                    reported only there, so the caller reads it after the call completes
  *   other arguments: as sparse_decode_attn.
+ * Every pointer above must be memory of the current device; any other (host memory, another
+ * device's memory) returns SPKV_EINVAL before anything is launched.
  * Limits: B * n_kv_heads <= SPKV_NOALLOC_MAX_UNITS and Hq / n_kv_heads <= 16; larger calls
  * return SPKV_EUNSUPPORTED before anything is launched.  No cudaMalloc, cudaFree or other
  * allocating routine is called.  The first call on a device looks up the scratch's device
  * address with that device current, so make it before any stream capture.  All calls on a
- * device share the scratch, which keeps the last call's contents: each call clears the arrival
- * counters (and the fallback error word) first, and calls whose kernels overlap on the GPU
- * (unordered streams) race on it and must not be issued. */
+ * device share the scratch, which keeps the last call's contents: each call clears the chunk
+ * counter first and rewrites every per-unit record it reads, and calls whose kernels overlap
+ * on the GPU (unordered streams) race on it and must not be issued. */
 #define SPKV_NOALLOC_MAX_UNITS 512
 #define SPKV_NOALLOC_MAX_CTAS 160
 #define SPKV_NOALLOC_SCRATCH_BYTES 6926592
@@ -403,6 +406,15 @@ int paged_kv_destroy(spkv_cache_t cache);
 
 /* Number of SMs the handle's kernels size their grids for (the device's SM count). */
 int spkv_sm_count(spkv_cache_t cache);
+
+/* Sets how long each bounded hand-off wait inside this handle's attention kernels
+ * (sparse_decode_attn, sparse_decode_attn_slots, lazy_rope_decode_attn) lasts before it gives up,
+ * in nanoseconds; the default is 1 s, far beyond any hand-off of a correct run.  A wait that gives
+ * up sets SPKV_DEVERR_TIMEOUT (reported as SPKV_ETIMEOUT by spkv_get_device_error); the CTA then
+ * waits for its own copies in flight (always with the full 1 s limit) and returns, and the call's
+ * outputs are undefined.  0 makes every wait that is not already complete give up at once, which
+ * exercises that error path without a fault.  Applies to calls made after it; ns <= 10^10. */
+int spkv_set_wait_limit(spkv_cache_t cache, uint64_t ns);
 
 /* A static string naming a status code. */
 const char* spkv_status_string(int status);

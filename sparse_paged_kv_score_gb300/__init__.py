@@ -105,6 +105,10 @@ class PagedKVCache:
     def sm_count(self) -> int:
         return load().spkv_sm_count(self.handle)
 
+    def set_wait_limit(self, ns: int) -> None:
+        """Limit (nanoseconds) of the attention kernels' bounded hand-off waits; 1 s by default."""
+        check("spkv_set_wait_limit", load().spkv_set_wait_limit(self.handle, int(ns)))
+
     def close(self):
         if self.handle:
             torch.cuda.synchronize()
@@ -222,29 +226,37 @@ def retrieve_pages(cache: PagedKVCache, k_host, v_host, page_table, missing, n_m
         _t(n_sel, torch.int32, "n_sel"), stride, int(n_slots), _stream(stream)))
 
 
-def sparse_decode_attn_noalloc(k_pool, v_pool, q, page_table, sel, n_sel, seq_len, out, lse, dev_err=None,
+def sparse_decode_attn_noalloc(k_pool, v_pool, q, page_table, sel, n_sel, seq_len, out, lse, dev_err,
                                stream=None):
     """sparse_decode_attn for callers that cannot allocate device memory.
 
     No handle and no allocation: the pool is passed directly and the split-K scratch is a
     fixed device array inside the library (SPKV_NOALLOC_SCRATCH_BYTES per GPU, held until the
     process exits).  At most 512 (request, kv head) units per call.  Calls on one device share
-    that scratch, so they must not overlap on the GPU.  ``dev_err`` is an optional int32 device
-    tensor of one element that receives the device error bits.
+    that scratch, so they must not overlap on the GPU.  ``dev_err`` (required) is an int32
+    device tensor of one element that receives the device error bits.  The call runs on the
+    device that holds ``k_pool`` (every tensor must be on it), on that device's current stream
+    unless ``stream`` is given.
     """
     Hk, n_phys = k_pool.shape[0], k_pool.shape[1]
     shp = (Hk, n_phys, PAGE, HEAD_DIM)
     B, Hq = q.shape[0], q.shape[1]
     np_max = page_table.shape[1]
     stride = sel.shape[2]
-    err = None if dev_err is None else _t(dev_err, torch.int32, "dev_err", (1,))
-    check("sparse_decode_attn_noalloc", load().sparse_decode_attn_noalloc(
-        _t(k_pool, torch.bfloat16, "k_pool", shp), _t(v_pool, torch.bfloat16, "v_pool", shp), Hk, n_phys,
-        _t(q, torch.bfloat16, "q", (B, Hq, HEAD_DIM)), B, Hq,
-        _t(page_table, torch.int32, "page_table", (B, np_max)), np_max,
-        _t(sel, torch.int32, "sel", (B, Hk, stride)), _t(n_sel, torch.int32, "n_sel", (B, Hk)), stride,
-        _t(seq_len, torch.int32, "seq_len", (B,)), _t(out, torch.float32, "out", (B, Hq, HEAD_DIM)),
-        _t(lse, torch.float32, "lse", (B, Hq)), err, _stream(stream)))
+    if dev_err is None:
+        raise ValueError("dev_err: an int32 device tensor of one element is required")
+    tensors = (k_pool, v_pool, q, page_table, sel, n_sel, seq_len, out, lse, dev_err)
+    if not all(isinstance(x, torch.Tensor) and x.device == k_pool.device for x in tensors):
+        raise ValueError("sparse_decode_attn_noalloc: every tensor must be on the device of k_pool")
+    with torch.cuda.device(k_pool.device):
+        check("sparse_decode_attn_noalloc", load().sparse_decode_attn_noalloc(
+            _t(k_pool, torch.bfloat16, "k_pool", shp), _t(v_pool, torch.bfloat16, "v_pool", shp), Hk, n_phys,
+            _t(q, torch.bfloat16, "q", (B, Hq, HEAD_DIM)), B, Hq,
+            _t(page_table, torch.int32, "page_table", (B, np_max)), np_max,
+            _t(sel, torch.int32, "sel", (B, Hk, stride)), _t(n_sel, torch.int32, "n_sel", (B, Hk)), stride,
+            _t(seq_len, torch.int32, "seq_len", (B,)), _t(out, torch.float32, "out", (B, Hq, HEAD_DIM)),
+            _t(lse, torch.float32, "lse", (B, Hq)), _t(dev_err, torch.int32, "dev_err", (1,)),
+            _stream(stream)))
 
 
 def lazy_rope_decode_attn(cache: PagedKVCache, q, qpos, meta, n_pages, doc_pos, theta: float, out, lse,

@@ -53,6 +53,7 @@ SIGNATURES = {
     "spkv_get_device_error": ([_vp, _vp, ctypes.POINTER(_u32)], _i32),
     "paged_kv_destroy": ([_vp], _i32),
     "spkv_sm_count": ([_vp], _i32),
+    "spkv_set_wait_limit": ([_vp, ctypes.c_uint64], _i32),
     "spkv_status_string": ([_i32], ctypes.c_char_p),
 }
 

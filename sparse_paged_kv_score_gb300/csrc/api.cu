@@ -78,6 +78,7 @@ void fill_common(AttnParams& p, spkv_cache_t c, const void* q, int B, int Hq, fl
   p.ws_ctl = c->ws_cnt + 2 * c->max_units;
   p.max_chunks = c->max_chunks;
   p.scale_log2 = static_cast<float>(1.4426950408889634074 / std::sqrt(128.0));
+  p.wait_ns = c->wait_ns;
 }
 
 }  // namespace
@@ -174,6 +175,12 @@ int paged_kv_destroy(spkv_cache_t c) {
 }
 
 int spkv_sm_count(spkv_cache_t c) { return c ? c->sm_count : SPKV_EINVAL; }
+
+int spkv_set_wait_limit(spkv_cache_t c, uint64_t ns) {
+  if (!c || ns > 10000000000ull) return SPKV_EINVAL;
+  c->wait_ns = ns;
+  return SPKV_OK;
+}
 
 int paged_kv_append(spkv_cache_t c, const int32_t* phys_page, const int32_t* tok_in_page, const void* k_new,
                     const void* v_new, int n_rows, void* stream) {

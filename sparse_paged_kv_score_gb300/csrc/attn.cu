@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int bh = __shfl_sync(0xffffffffu, head, i);
           if (jl >= STAGES) {
             // warp-uniform outcome even if lanes disagree at the time limit
-            if (!__all_sync(0xffffffffu, mbar_wait(&S.empty[s], ((jl / STAGES) - 1) & 1))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&S.empty[s], ((jl / STAGES) - 1) & 1, p.wait_ns))) {
               if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
               ok = false;
               break;
@@ -318,7 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       const int s = jl % STAGES;
       bool free_stage = true;
-      if (jl >= STAGES) free_stage = __all_sync(0xffffffffu, mbar_wait(&S.empty[s], ((jl / STAGES) - 1) & 1));
+      if (jl >= STAGES)
+        free_stage = __all_sync(0xffffffffu, mbar_wait(&S.empty[s], ((jl / STAGES) - 1) & 1, p.wait_ns));
       if (free_stage) {
         if (lane == 0) {
           StageMeta m;
@@ -332,7 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         flag_error(p.err, SPKV_DEVERR_TIMEOUT);
       }
     }
-    // Before leaving, make sure no copy issued by this CTA is still in flight.
+    // Before leaving, make sure no copy issued by this CTA is still in flight (always with the
+    // full limit: the copies themselves complete in microseconds).
     for (int j = jl > STAGES ? jl - STAGES : 0; j < jl; ++j) mbar_wait(&S.full[j % STAGES], (j / STAGES) & 1);
     return;
   }
@@ -340,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kEpilogueWarp) {
     // ================================================================ epilogue warp
     for (int k = 0;; ++k) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&S.cfull, k & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&S.cfull, k & 1, p.wait_ns))) {
         if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
         break;
       }
@@ -486,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Hands this warp's state for unit u to the epilogue warp (which merges the four warps).
   auto flush = [&](int u, int chunk, int ustart, int ucount, int last) {
     if (n_flush > 0) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&S.cempty, (n_flush - 1) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&S.cempty, (n_flush - 1) & 1, p.wait_ns))) {
         if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
       }
     }
@@ -532,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t stage0 = smem_u32(stages);
   for (int jl = 0;; ++jl) {
     const int s = jl % STAGES;
-    if (!__all_sync(0xffffffffu, mbar_wait(&S.full[s], (jl / STAGES) & 1))) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&S.full[s], (jl / STAGES) & 1, p.wait_ns))) {
       if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
       break;
     }

@@ -24,6 +24,7 @@ struct spkv_cache {
   int32_t max_units = 0;
   int attn_grid = 0;             // CTAs of the split-K attention kernel (one per SM)
   int max_chunks = 0;            // chunks the attention kernel may cut its page sequence into
+  uint64_t wait_ns = 1000000000ull;   // limit of the attention kernel's bounded hand-off waits
   const void* host_k = nullptr;  // last host pool given to retrieve_pages and its device address
   const void* host_v = nullptr;
   const void* host_k_dev = nullptr;
@@ -87,6 +88,7 @@ struct AttnParams {
   const int32_t* doc_pos;
   int max_docs;
   float scale_log2;              // log2(e) / sqrt(128)
+  uint64_t wait_ns;              // limit of each intra-CTA hand-off wait (0: give up unless complete)
   uint64_t phase_inc[64];        // RoPE pair j: turns per position, 2^-64 fixed point
 };
 

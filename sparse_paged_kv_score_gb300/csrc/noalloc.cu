@@ -16,9 +16,15 @@
 //   * the first call on a device looks up the array's device address (cudaGetSymbolAddress)
 //     with that device current, so make that first call before any stream capture;
 //   * all calls on a device share the one array and it keeps the last call's contents; the
-//     chunk counter (and the fallback error word) are cleared at the start of every call, and
-//     every call rewrites the per-unit partial records before reading them;
+//     chunk counter is cleared at the start of every call, and every call rewrites the per-unit
+//     partial records before reading them;
 //     two calls whose kernels overlap on the GPU (different streams, no ordering) race on it;
+//   * the caller's error word is required: a page id or physical page out of range is skipped
+//     and reported only there, so a call that could not report it would hand back wrong
+//     results with SPKV_OK;
+//   * every device pointer must belong to the current device (checked with
+//     cudaPointerGetAttributes, a lookup that allocates nothing): the scratch address, kernel
+//     attributes and tensor maps all follow the current device;
 //   * nothing here calls cudaMalloc, cudaFree or any allocating routine.
 #include <cudaTypedefs.h>
 
@@ -33,7 +39,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int64_t kSlots = int64_t(2 * SPKV_NOALLOC_MAX_CTAS) + SPKV_NOALLOC_MAX_UNITS;
 // Byte layout of the scratch array (each region 256-byte aligned).
-constexpr int64_t kOffErr = 0;
+constexpr int64_t kOffCtl = 0;     // the chunk counter (first word); the rest of the region is unused
 constexpr int64_t kOffCnt = 256;
 constexpr int64_t kOffM = kOffCnt + ((SPKV_NOALLOC_MAX_UNITS * 8 + 255) / 256) * 256;
 constexpr int64_t kOffL = kOffM + kSlots * 16 * 4;
@@ -82,6 +88,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// True when p is device (or managed) memory of device `dev`.  Host memory, unregistered or
+// pinned, and another device's memory are refused.
+bool on_device(const void* p, int dev) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) && a.device == dev;
+}
+
 bool encode(CUtensorMap* m, const void* base, int64_t n_page_heads) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -101,7 +118,8 @@ extern "C" int sparse_decode_attn_noalloc(const void* k_pool, const void* v_pool
                                           const int32_t* page_table, int np_max, const int32_t* sel,
                                           const int32_t* n_sel, int sel_stride, const int32_t* seq_len,
                                           float* out, float* lse, uint32_t* dev_err, void* stream) {
-  if (!k_pool || !v_pool || !q || !page_table || !sel || !n_sel || !seq_len || !out || !lse) return SPKV_EINVAL;
+  if (!k_pool || !v_pool || !q || !page_table || !sel || !n_sel || !seq_len || !out || !lse || !dev_err)
+    return SPKV_EINVAL;
   if (n_kv_heads <= 0 || n_phys_pages <= 0 || B < 0 || Hq <= 0 || np_max <= 0 || sel_stride <= 0)
     return SPKV_EINVAL;
   if (Hq % n_kv_heads != 0) return SPKV_EINVAL;
@@ -118,6 +136,11 @@ extern "C" int sparse_decode_attn_noalloc(const void* k_pool, const void* v_pool
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return SPKV_ECUDA;
+  for (const void* ptr : {k_pool, v_pool, q, static_cast<const void*>(page_table), static_cast<const void*>(sel),
+                          static_cast<const void*>(n_sel), static_cast<const void*>(seq_len),
+                          static_cast<const void*>(out), static_cast<const void*>(lse),
+                          static_cast<const void*>(dev_err)})
+    if (!on_device(ptr, dev)) return SPKV_EINVAL;
   unsigned char* base = nullptr;
   if (scratch_address(dev, &base) != cudaSuccess) return SPKV_ECUDA;
 
@@ -128,11 +151,9 @@ extern "C" int sparse_decode_attn_noalloc(const void* k_pool, const void* v_pool
   if (!encode(&c.tmap_k, k_pool, n_ph) || !encode(&c.tmap_v, v_pool, n_ph)) return SPKV_ECUDA;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  uint32_t* err = dev_err ? dev_err : reinterpret_cast<uint32_t*>(base + kOffErr);
   int32_t* cnt = reinterpret_cast<int32_t*>(base + kOffCnt);
   const int64_t units = int64_t(B) * n_kv_heads;
-  if (!dev_err && cudaMemsetAsync(err, 0, sizeof(uint32_t), st) != cudaSuccess) return SPKV_ECUDA;
-  if (cudaMemsetAsync(base + kOffErr + 16, 0, 2 * sizeof(int32_t), st) != cudaSuccess) return SPKV_ECUDA;
+  if (cudaMemsetAsync(base + kOffCtl, 0, 2 * sizeof(int32_t), st) != cudaSuccess) return SPKV_ECUDA;
 
   spkv::AttnParams p;
   std::memset(&p, 0, sizeof(p));
@@ -144,15 +165,16 @@ extern "C" int sparse_decode_attn_noalloc(const void* k_pool, const void* v_pool
   p.Hk = n_kv_heads;
   p.G = G;
   p.n_phys = n_phys_pages;
-  p.err = err;
+  p.err = dev_err;
   p.ws_m = reinterpret_cast<float*>(base + kOffM);
   p.ws_l = reinterpret_cast<float*>(base + kOffL);
   p.ws_o = reinterpret_cast<float*>(base + kOffO);
   p.ws_parts = cnt;
-  p.ws_ctl = reinterpret_cast<int32_t*>(base + kOffErr + 16);   // inside the 256-byte first region
+  p.ws_ctl = reinterpret_cast<int32_t*>(base + kOffCtl);
   p.max_chunks = 2 * SPKV_NOALLOC_MAX_CTAS;
   p.min_chunk = (sel_stride + 125) / 126;
   p.scale_log2 = static_cast<float>(1.4426950408889634074 / std::sqrt(128.0));
+  p.wait_ns = 1000000000ull;
   p.page_table = page_table;
   p.np_max = np_max;
   p.sel = sel;

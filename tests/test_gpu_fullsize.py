@@ -105,7 +105,7 @@ def test_llama8b_full_step():
     torch.cuda.synchronize()
     s_h, sel_h, n_h = host(s), host(sel), host(n_sel)
     rng = np.random.default_rng(0)
-    sample = np.sort(rng.choice(U, 24, replace=False))
+    sample = np.sort(rng.choice(U, U // 2, replace=False))     # half of the 256 units
     s_or = check_scores_sampled(w, s_h, sample)
     check_select_same_scores(w, s_h, w["evict"], np.ones((B, Hk, npm), np.uint8), k_q, k_e, sel_h, n_h,
                              alive_bits_to_bytes(host(alive).view(np.uint32), npm))
@@ -154,7 +154,7 @@ def test_llama8b_full_step():
     llse = torch.empty_like(lse)
     spkv.lazy_rope_decode_attn(d.cache, d.q, i32(qpos), u32_as_i32(words), i32(n_pages), i32(doc_pos),
                                500000.0, lout, llse)
-    lu = np.sort(rng.choice(U, 32, replace=False))
+    lu = np.sort(rng.choice(U, U // 2, replace=False))
     ro, rl = oracle.lazy_attn_batch(w["q"], w["k_pool"], w["v_pool"], phys_l, valid_l, slot_l, n_pages,
                                     qpos, doc_pos, 500000.0, materialise=True, units=lu)
     rows = np.concatenate([np.arange((u % Hk) * 4, (u % Hk + 1) * 4) + (u // Hk) * Hq for u in lu])
@@ -181,7 +181,7 @@ def test_lazy_rag_full_size_sampled():
     spkv.lazy_rope_decode_attn(cache, bf(w["q"]), i32(w["qpos"]), u32_as_i32(words), i32(w["n_pages"]),
                                i32(w["doc_pos"]), w["theta"], out, lse)
     torch.cuda.synchronize()
-    units = np.sort(np.random.default_rng(1).choice(B * Hk, 24, replace=False))
+    units = np.sort(np.random.default_rng(1).choice(B * Hk, B * Hk // 2, replace=False))   # half of 512
     ro, rl = oracle.lazy_attn_batch(w["q"], w["k_pool"], w["v_pool"], w["phys"], w["valid"], w["slot"],
                                     w["n_pages"], w["qpos"], w["doc_pos"], w["theta"], materialise=True,
                                     units=units)
@@ -238,10 +238,12 @@ def test_long262k_residency_trajectory():
         assert np.array_equal(host(vic), o_vic) and np.array_equal(host(hist), o_hist)
         assert np.array_equal(host(r_dev), resident) and np.array_equal(host(t_dev), ts)
         hits.append(1.0 - o_nm.sum() / n_h.sum())
-        if t in (0, steps - 1):
+        if t % 4 == 0 or t == steps - 1:
             wq = dict(w)
             wq["q"] = qs[t]
-            check_scores_sampled(wq, s_h, np.array([0, 13, 37, 63]))
+            # scores over 4096 pages per unit: half of the units at the ends, a few in between
+            su = np.arange(0, U, 2) if t in (0, steps - 1) else np.array([0, 13, 37, 63])
+            check_scores_sampled(wq, s_h, su)
             check_attn(wq, host(out), host(lse), sel_h, n_h)
     # the query walks slowly, so most selected pages stay resident from step to step
     assert hits[0] == 0.0 and np.mean(hits[1:]) > 0.5
@@ -299,7 +301,7 @@ def test_long262k_offload_trajectory():
 
 # ------------------------------------------------------------------ NOSA trajectory
 
-def _trajectory(w, steps, check_attn_steps):
+def _trajectory(w, steps, check_attn_steps, score_units=None, score_steps=()):
     B, Hk, npm = w["B"], w["Hk"], w["np_max"]
     k_q, k_e = w["k_q"], w["k_e"]
     k = k_q + k_e
@@ -354,7 +356,8 @@ def _trajectory(w, steps, check_attn_steps):
             wq = dict(w)
             wq["q"] = inp["q"]
             check_attn(wq, host(out), host(lse), sel_h, n_h)
-            check_scores_sampled(wq, s_h, np.array([0, 5, B * Hk - 1]))
+            su = score_units if t in score_steps else np.array([0, 5, B * Hk - 1])
+            check_scores_sampled(wq, s_h, su)
     assert d.errors() == (0, 0)
     d.close()
     return gammas
@@ -362,7 +365,8 @@ def _trajectory(w, steps, check_attn_steps):
 
 def test_nosa_trajectory_64_steps():
     w = gen.nosa_traj(seed=0)
-    g = _trajectory(w, 64, check_attn_steps=(0, 31, 63))
+    g = _trajectory(w, 64, check_attn_steps=tuple(range(0, 64, 4)) + (63,),
+                    score_units=np.arange(0, w["B"] * w["Hk"], 2), score_steps=(0, 31, 63))
     assert min(g) >= 0.75
 
 

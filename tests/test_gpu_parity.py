@@ -257,11 +257,14 @@ def test_select_bitexact_across_context_sizes(np_max):
     d.close()
 
 
-@pytest.mark.parametrize("np_max, n_slots", [(96, 40), (512, 2048), (1000, 300), (1500, 700)])
-def test_select_resident_update_equals_three_calls(np_max, n_slots):
+@pytest.mark.parametrize("np_max, n_slots, times", [(96, 40, None), (512, 2048, None), (1000, 300, None),
+                                                    (1500, 700, None), (96, 40, (0, 1, 9, 2, 3, 30, 4, 5)),
+                                                    (1500, 700, (0, 1, 9, 2, 3, 30, 4, 5))])
+def test_select_resident_update_equals_three_calls(np_max, n_slots, times):
     """The fused call (one kernel up to 1024 pages, three launches above) against select_topk +
     resident_setdiff + lru_bucket_update on copies of the same state, and both against the oracle,
-    bit for bit, over a trajectory whose residency buffer fills and recycles."""
+    bit for bit, over a trajectory whose residency buffer fills and recycles.  With `times`, the
+    clock steps back twice, so some slots carry timestamps later than t (age 0, bucket 0)."""
     w = gen.sparse_workload(3, 8, 2, 64 * np_max - 5, 10, 6, seed=np_max)
     d = Dev(w)
     B, Hk = w["B"], w["Hk"]
@@ -283,7 +286,9 @@ def test_select_resident_update_equals_three_calls(np_max, n_slots):
     h_alive = np.ones(shape, np.uint8)
     h_res = np.full((U, n_slots), -1, np.int32)
     h_ts = np.full((U, n_slots), np.iinfo(np.int32).min, np.int32)
-    for t in range(8):
+    saw_future = False
+    for t in (range(8) if times is None else times):
+        saw_future |= bool(((h_res >= 0) & (h_ts > t)).any())
         s = (np.round(rng.standard_normal(shape) * 4) / 4).astype(np.float32)
         e = (np.round(rng.standard_normal(shape) * 4) / 4).astype(np.float32)
         s_d, e_d = f32(s), f32(e)
@@ -313,6 +318,7 @@ def test_select_resident_update_equals_three_calls(np_max, n_slots):
         assert np.array_equal(fa["hist"].cpu().numpy(), o_hist)
         assert np.array_equal(a["resident"].cpu().numpy(), h_res) and np.array_equal(a["ts"].cpu().numpy(), h_ts)
         assert np.array_equal(alive_bits_to_bytes(a["alive"].cpu().numpy().view(np.uint32), np_max), h_alive)
+    assert saw_future == (times is not None)
     assert d.errors() == (0, 0)
     d.close()
 

@@ -369,12 +369,23 @@ def test_setdiff_python_sets(seed):
 
 # ------------------------------------------------------------------------------ bucketed LRU
 
+def _lru_bucket(res, stamp, t, W):
+    """Bucket of one slot, written out case by case: an empty slot is the oldest there is; a
+    slot stamped at or after t (a clock that stepped back, or a wrapped counter) is as recent
+    as a slot can be; otherwise whole bucket widths elapsed since the stamp, capped at 63."""
+    if res < 0:
+        return 63
+    if int(stamp) >= int(t):
+        return 0
+    return min(63, (int(t) - int(stamp)) // W)
+
+
 def _lru_bruteforce(resident, ts, slot, n_sel, missing, n_missing, t, W):
     resident, ts = resident.copy(), ts.copy()
     hits = {int(s) for s in slot[:n_sel] if s >= 0}
     for s in hits:
         ts[s] = t
-    bucket = [63 if resident[s] < 0 else min(63, (int(t) - int(ts[s])) // W) for s in range(len(ts))]
+    bucket = [_lru_bucket(resident[s], ts[s], t, W) for s in range(len(ts))]
     order = []
     for b in range(63, -1, -1):                 # oldest bucket first, slots ascending inside
         order += [s for s in range(len(ts)) if bucket[s] == b and s not in hits]
@@ -406,6 +417,44 @@ def test_lru_bruteforce_trajectory(W):
         assert set(sel[:n_sel].tolist()) <= set(r2.tolist())
         assert all(t2[s] == t for s in range(n_slots) if r2[s] in set(sel[:n_sel].tolist()))
         resident, ts = r2, t2
+
+
+@pytest.mark.parametrize("W", [1, 3])
+def test_lru_bruteforce_trajectory_with_clock_stepping_back(W):
+    """Times that jump back (and forward again) leave timestamps later than t; such a slot must
+    count as age 0 (bucket 0), not as a negative age."""
+    rng = np.random.default_rng(10 + W)
+    n_slots, stride = 20, 6
+    resident = np.full(n_slots, -1, np.int32)
+    ts = np.full(n_slots, np.iinfo(np.int32).min, np.int32)
+    times = [0, 1, 2, 40, 41, 3, 4, 90, 5, 6, 7, 200, 8, 9, 300, 10, 11, 12]
+    saw_future = False
+    for t in times:
+        n_sel = int(rng.integers(1, stride + 1))
+        sel = np.full(stride, -1, np.int32)
+        sel[:n_sel] = np.sort(rng.choice(35, size=n_sel, replace=False))
+        missing, nm, slot = oracle.setdiff_unit(resident, sel, n_sel, stride)
+        saw_future |= bool(((resident >= 0) & (ts > t)).any())
+        r2, t2, vic, hist = oracle.lru_unit(resident, ts, slot, n_sel, missing, nm, t, W, stride)
+        br, bt, bv, bh = _lru_bruteforce(resident, ts, slot, n_sel, missing, nm, t, W)
+        assert np.array_equal(r2, br) and np.array_equal(t2, bt)
+        assert vic[:nm].tolist() == bv and (vic[nm:] == -1).all()
+        assert np.array_equal(hist, bh) and hist.sum() == n_slots
+        resident, ts = r2, t2
+    assert saw_future
+
+
+def test_lru_future_timestamp_is_bucket_zero():
+    """Hand-checked: at t = 5 a slot stamped 10 is the newest (bucket 0), so it is evicted last."""
+    resident = np.array([1, 2, 3], np.int32)
+    ts = np.array([10, 3, 0], np.int32)
+    r, t2, vic, hist = oracle.lru_unit(resident, ts, [-1], 1, [7, 8, 9], 3, 5, 1, 3)
+    # ages: slot 0 in the future -> 0, slot 1 -> 2, slot 2 -> 5: oldest first is 2, 1, 0
+    assert vic.tolist() == [2, 1, 0]
+    assert hist[0] == 1 and hist[2] == 1 and hist[5] == 1 and hist.sum() == 3
+    r, t2, vic, hist = oracle.lru_unit(resident, ts, [-1], 1, [7], 1, 5, 3, 3)
+    # W = 3: ages 0, 2, 5 -> buckets 0, 0, 1; the bucket-1 slot goes first
+    assert vic.tolist() == [2, -1, -1] and hist[0] == 2 and hist[1] == 1
 
 
 def test_lru_empty_slots_are_oldest():

@@ -68,6 +68,8 @@ def parse():
     ap.add_argument("--bookkeeping", default="overlap", choices=["fused", "overlap"],
                     help="fused: selection + set-difference + LRU in one kernel before attention; "
                          "overlap: selection, then set-difference + LRU on a second stream beside attention")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the tiny and NOSA-trajectory workloads of the per-config report")
     ap.add_argument("--batch", type=int, default=32,
                     help="requests per step (32 = the Llama-3-8B-layer workload; smaller for profiling)")
     return ap.parse_args()
@@ -192,12 +194,15 @@ class Clocks:
 
 # ----------------------------------------------------------------------------- CPU oracle legs
 
-def oracle_sample(w, units, reps=1):
-    """Times the fp64 oracle on a sample of units of the step; returns (seconds, bytes, threads)."""
+def oracle_step(w, units, n_slots=N_SLOTS, residency=True, reps=1):
+    """Times the fp64 oracle on one decode step of the listed units: block scores, dual top-k
+    selection, sparse attention and (residency) the set-difference and LRU update against fresh
+    resident tables of n_slots slots.  Returns (seconds per step, threads)."""
     import oracle
     nthreads = os.cpu_count() or 1
     k_q, k_e = w["k_q"], w["k_e"]
     alive = np.ones((w["B"], w["Hk"], w["np_max"]), np.uint8)
+    stride = k_q + k_e + 1
     t0 = time.perf_counter()
     for _ in range(reps):
         s = oracle.score_batch(w["q"], w["k_pool"], w["page_table"], w["seq_len"], units=units,
@@ -206,11 +211,15 @@ def oracle_sample(w, units, reps=1):
                                             nthreads=nthreads)
         oracle.sparse_attn_batch(w["q"], w["k_pool"], w["v_pool"], w["page_table"], sel, n_sel,
                                  w["seq_len"], units=units, nthreads=nthreads)
-    dt = (time.perf_counter() - t0) / reps
-    b = step_bytes(w, k_q + k_e)
-    frac = len(units) / (w["B"] * w["Hk"])
-    sample_bytes = (b["score"] + b["select"] + b["attn"]) * frac
-    return dt, sample_bytes, nthreads
+        if residency:
+            U = len(units)
+            sel_u = sel.reshape(-1, stride)[units]
+            n_u = n_sel.reshape(-1)[units]
+            resident = np.full((U, n_slots), -1, np.int32)
+            ts = np.full((U, n_slots), np.iinfo(np.int32).min, np.int32)
+            miss, nm, slot = oracle.setdiff_batch(resident, sel_u, n_u, nthreads=nthreads)
+            oracle.lru_batch(resident, ts, slot, n_u, miss, nm, 0, 1, nthreads=nthreads)
+    return (time.perf_counter() - t0) / reps, nthreads
 
 
 def run_reference(args):
@@ -219,19 +228,19 @@ def run_reference(args):
         return
     import gen
     w = gen.llama8b(seed=0)
-    rng = np.random.default_rng(0)
-    n_units = 32
-    times, byts = [], 0.0
+    units = np.arange(w["B"] * w["Hk"], dtype=np.int32)
+    times = []
     thr = 1
     for i in range(args.warmup + args.steps):
-        units = np.sort(rng.choice(w["B"] * w["Hk"], size=n_units, replace=False)).astype(np.int32)
-        dt, sb, thr = oracle_sample(w, units)
+        dt, thr = oracle_step(w, units)
         if i >= args.warmup:
             times.append(dt)
-            byts = sb
     ms = 1e3 * statistics.mean(times)
+    b = step_bytes(w, w["k_q"] + w["k_e"])
+    byts = sum(v for kk, v in b.items() if kk != "attn_kv")
     value = byts / (ms * 1e-3) / 1e9
-    sample = f"{n_units} of 256 (request, kv head) units per step: score_blocks + select_topk + attention"
+    sample = ("the whole step, all 256 (request, kv head) units: block scores, dual top-k selection, sparse "
+              "attention, set-difference and LRU update (2048 slots), fp64")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -243,7 +252,288 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- GPU step
 
-def offload_leg(args, dev, stream, timed):
+def _dev_helpers(dev):
+    import torch
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+
+    return bf, i32
+
+
+def _parts(b, names):
+    return int(sum(b[n] for n in names))
+
+
+def _cpu_line(dt, byts, thr, sample, reps=1):
+    return {"value": byts / dt / 1e9, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample,
+            "ms_per_step": dt * 1e3}
+
+
+def _oracle_timed(fn, min_s=0.5):
+    """Seconds per call of fn() (the fp64 oracle), repeated until min_s of work has run."""
+    t0 = time.perf_counter()
+    fn()
+    dt = time.perf_counter() - t0
+    reps = max(0, int(min_s / max(dt, 1e-6)) - 1)
+    if reps:
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        dt = (time.perf_counter() - t0) / reps
+    return dt
+
+
+def tiny_leg(args, dev, timed, cap, peak, cpu_baseline):
+    """The tiny sparse-decode workload (batch 1, 8 q / 2 kv heads, context 4096, k = 16): one step
+    is the new token's append with the block scores (one launch), the dual top-k selection and
+    the sparse attention, each step one CUDA graph."""
+    import torch
+    import gen
+    import sparse_paged_kv_score_gb300 as spkv
+    bf, i32 = _dev_helpers(dev)
+    w = gen.tiny(seed=0)
+    B, Hq, Hk, npm = w["B"], w["Hq"], w["Hk"], w["np_max"]
+    k_q, k_e = w["k_q"], w["k_e"]
+    stride = k_q + k_e + 1
+    U = B * Hk
+    k_pool, v_pool = bf(w["k_pool"]), bf(w["v_pool"])
+    ksum = torch.zeros(Hk, w["n_phys"], 4, 128, dtype=torch.float32, device=dev)
+    cache = spkv.paged_kv_create(k_pool, v_pool, ksum, i32(gen.page_counts(w)), max_units=U)
+    pt, seq = i32(w["page_table"]), i32(w["seq_len"])
+    n_iter = args.warmup + args.steps
+    qs = [bf(gen.rows_bf16(0, 7000 + i, B * Hq).reshape(B, Hq, 128)) for i in range(n_iter)]
+    evs = [torch.from_numpy(w["evict"]).to(dev) for _ in range(n_iter)]
+    kn = [bf(gen.rows_bf16(0, 9000 + i, U).reshape(B, Hk, 128)) for i in range(n_iter)]
+    vn = [bf(gen.rows_bf16(0, 9500 + i, U).reshape(B, Hk, 128)) for i in range(n_iter)]
+    scores = torch.empty(B, Hk, npm, dtype=torch.float32, device=dev)
+    alive = torch.full((B, Hk, (npm + 31) // 32), -1, dtype=torch.int32, device=dev)
+    sel = torch.empty(B, Hk, stride, dtype=torch.int32, device=dev)
+    n_sel = torch.empty(B, Hk, dtype=torch.int32, device=dev)
+    out = torch.empty(B, Hq, 128, dtype=torch.float32, device=dev)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+
+    def step(i):
+        spkv.decode_append_score(cache, kn[i], vn[i], qs[i], pt, seq, scores)
+        spkv.select_topk(cache, scores, evs[i], alive, seq, k_q, k_e, sel, n_sel)
+        spkv.sparse_decode_attn(cache, qs[i], pt, sel, n_sel, seq, out, lse)
+
+    for i in range(args.warmup):
+        step(i)
+    idx = list(range(args.warmup, n_iter))
+    graphs = {}
+    for i in idx:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            step(i)
+        graphs[i] = g
+    torch.cuda.synchronize()
+    ms = statistics.median(timed(lambda i: graphs[i].replay(), idx))
+    st, bits = spkv.get_device_error(cache)
+    if st != 0:
+        raise RuntimeError(f"device error bits {bits} in the tiny leg")
+    cache.close()
+    byts = _parts(step_bytes(w, k_q + k_e), ("append", "score", "select", "attn"))
+    gbs = byts / (ms * 1e-3) / 1e9
+    res = {"workload": w["name"], "step": "append+score, select, sparse attention (3 launches + combine)",
+           "us_per_step": ms * 1e3, "bytes_per_step": byts, "GBps": gbs, "pct_hbm_peak": 100 * gbs / peak,
+           "queries_per_s": B / (ms * 1e-3), "launch": "one CUDA graph per step", "stat": "median"}
+    if cpu_baseline:
+        units = np.arange(U, dtype=np.int32)
+        thr = os.cpu_count() or 1
+        dt = _oracle_timed(lambda: oracle_step(w, units, residency=False))
+        res["cpu_baseline"] = _cpu_line(dt, byts, thr, "the whole step (both units), fp64")
+    return res
+
+
+def traj_leg(args, dev, timed, cap, peak, cpu_baseline):
+    """The NOSA trajectory (batch 16, 32 q / 8 kv heads, context 65536 growing by one token per
+    step, k = 64 with k_e = 48, k_q = 16): 64 consecutive decode steps, each the new token's append
+    with the block scores, the dual top-k selection (eviction scores on a random walk) and the
+    sparse attention, one CUDA graph per step.  The trajectory runs once untimed (warm-up), its
+    state is reset, and runs again timed; the locality gamma(t) is read from the timed steps'
+    selections afterwards."""
+    import torch
+    import gen
+    import sparse_paged_kv_score_gb300 as spkv
+    bf, i32 = _dev_helpers(dev)
+    w = gen.nosa_traj(seed=0)
+    B, Hq, Hk, npm, steps = w["B"], w["Hq"], w["Hk"], w["np_max"], w["steps"]
+    k_q, k_e = w["k_q"], w["k_e"]
+    k = k_q + k_e
+    stride = k + 1
+    U = B * Hk
+    L0 = w["seq_len"].copy()
+    k_pool, v_pool = bf(w["k_pool"]), bf(w["v_pool"])
+    ksum = torch.zeros(Hk, w["n_phys"], 4, 128, dtype=torch.float32, device=dev)
+    cnt0 = i32(gen.page_counts(w))
+    cnt = cnt0.clone()
+    cache = spkv.paged_kv_create(k_pool, v_pool, ksum, cnt, max_units=U)
+    pt = i32(w["page_table"])
+    inps, e_walk = [], None
+    for t in range(steps):
+        inp = gen.traj_step_inputs(w, t, e_walk)
+        e_walk = inp["evict"]
+        inps.append(dict(q=bf(inp["q"]), ev=torch.from_numpy(e_walk.astype(np.float32)).to(dev),
+                         kn=bf(inp["k_new"]), vn=bf(inp["v_new"]), seq=i32(L0 + t + 1)))
+        if t == 0:
+            inp0 = inp
+    scores = torch.empty(B, Hk, npm, dtype=torch.float32, device=dev)
+    alive = torch.full((B, Hk, (npm + 31) // 32), -1, dtype=torch.int32, device=dev)
+    sels = [torch.empty(B, Hk, stride, dtype=torch.int32, device=dev) for _ in range(steps)]
+    nsels = [torch.empty(B, Hk, dtype=torch.int32, device=dev) for _ in range(steps)]
+    out = torch.empty(B, Hq, 128, dtype=torch.float32, device=dev)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+
+    def step(t):
+        x = inps[t]
+        spkv.decode_append_score(cache, x["kn"], x["vn"], x["q"], pt, x["seq"], scores)
+        spkv.select_topk(cache, scores, x["ev"], alive, x["seq"], k_q, k_e, sels[t], nsels[t])
+        spkv.sparse_decode_attn(cache, x["q"], pt, sels[t], nsels[t], x["seq"], out, lse)
+
+    graphs = []
+    for t in range(steps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            step(t)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    for g in graphs:          # warm-up: the whole trajectory once
+        g.replay()
+    torch.cuda.synchronize()
+    alive.fill_(-1)           # back to the initial state (the local page's summaries are never scored)
+    cnt.copy_(cnt0)
+    torch.cuda.synchronize()
+    ms_all = timed(lambda t: graphs[t].replay(), range(steps))
+    st, bits = spkv.get_device_error(cache)
+    if st != 0:
+        raise RuntimeError(f"device error bits {bits} in the trajectory leg")
+    sel_h = [x.cpu().numpy() for x in sels]
+    n_h = [x.cpu().numpy() for x in nsels]
+    gammas = []
+    for t in range(1, steps):
+        local = (L0 + t) // 64
+        for b in range(B):
+            for h in range(Hk):
+                prev = set(sel_h[t - 1][b, h, :n_h[t - 1][b, h]].tolist())
+                cur = set(sel_h[t][b, h, :n_h[t][b, h]].tolist()) - {int(local[b])}
+                gammas.append(len(cur & prev) / k)
+    del graphs
+    cache.close()
+    wb = dict(w, seq_len=L0 + 1)
+    byts = _parts(step_bytes(wb, k), ("append", "score", "select", "attn"))
+    ms = statistics.mean(ms_all)
+    gbs = byts / (ms * 1e-3) / 1e9
+    res = {"workload": w["name"], "step": "append+score, select, sparse attention; 64 steps in a row",
+           "ms_per_step": ms, "ms_per_step_median": statistics.median(ms_all), "bytes_per_step": byts,
+           "GBps": gbs, "pct_hbm_peak": 100 * gbs / peak, "queries_per_s": B / (ms * 1e-3),
+           "gamma_min": min(gammas), "gamma_mean": statistics.mean(gammas), "gamma_bound": k_e / k,
+           "launch": "one CUDA graph per step"}
+    if cpu_baseline:
+        # the oracle on the trajectory's first step (its query, eviction scores and appended row)
+        phys = w["page_table"][np.arange(B), L0 // 64]
+        for b in range(B):
+            w["k_pool"][:, phys[b], L0[b] % 64] = inp0["k_new"][b]
+            w["v_pool"][:, phys[b], L0[b] % 64] = inp0["v_new"][b]
+        w1 = dict(w, q=inp0["q"], evict=inp0["evict"], seq_len=L0 + 1)
+        units = np.arange(U, dtype=np.int32)
+        dt = _oracle_timed(lambda: oracle_step(w1, units, residency=False), min_s=0.0)
+        res["cpu_baseline"] = _cpu_line(dt, byts, os.cpu_count() or 1,
+                                        f"the trajectory's first step, all {U} units, fp64")
+    del k_pool, v_pool, ksum
+    torch.cuda.empty_cache()
+    return res
+
+
+def resident262k_leg(args, dev, timed, cap, peak, cpu_baseline, w, scache, qs, q_host0):
+    """The 262k-context workload with its whole pool resident on the device (batch 8, 40 q / 8 kv
+    heads, 4096 pages per request, k = 128): one step is the block scores, the selection with the
+    set-difference against each unit's 2048-slot resident buffer and the 64-bucket LRU update
+    (select_resident_update: three kernels at this context), and the sparse attention, one CUDA
+    graph per step along the query walk.  The set-difference and the LRU update are also timed
+    alone on further eager steps."""
+    import torch
+    import sparse_paged_kv_score_gb300 as spkv
+    bf, i32 = _dev_helpers(dev)
+    B, Hq, Hk, npm = w["B"], w["Hq"], w["Hk"], w["np_max"]
+    U = B * Hk
+    k_q, k_e = w["k_q"], w["k_e"]
+    stride = k_q + k_e + 1
+    ns = w["n_slots"]
+    pt, seq = i32(w["page_table"]), i32(w["seq_len"])
+    ev = torch.from_numpy(w["evict"].astype(np.float32)).to(dev)
+    scores = torch.empty(B, Hk, npm, dtype=torch.float32, device=dev)
+    alive = torch.full((B, Hk, (npm + 31) // 32), -1, dtype=torch.int32, device=dev)
+    sel = torch.empty(B, Hk, stride, dtype=torch.int32, device=dev)
+    n_sel = torch.empty(B, Hk, dtype=torch.int32, device=dev)
+    resident = torch.full((U, ns), -1, dtype=torch.int32, device=dev)
+    ts = torch.full((U, ns), np.iinfo(np.int32).min, dtype=torch.int32, device=dev)
+    missing, slot, victims = (torch.empty(U, stride, dtype=torch.int32, device=dev) for _ in range(3))
+    n_missing = torch.empty(U, dtype=torch.int32, device=dev)
+    hist = torch.empty(U, 64, dtype=torch.int32, device=dev)
+    out = torch.empty(B, Hq, 128, dtype=torch.float32, device=dev)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+    n_iter = args.warmup + args.steps
+
+    def step(i):
+        spkv.score_blocks(scache, qs[i], pt, seq, scores)
+        spkv.select_resident_update(scache, scores, ev, alive, seq, k_q, k_e, sel, n_sel, resident, ts, i, 1,
+                                    missing, n_missing, slot, victims, hist)
+        spkv.sparse_decode_attn(scache, qs[i], pt, sel, n_sel, seq, out, lse)
+
+    for i in range(args.warmup):
+        step(i)
+    idx = list(range(args.warmup, n_iter))
+    graphs = {}
+    for i in idx:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            step(i)
+        graphs[i] = g
+    torch.cuda.synchronize()
+    ms_all = timed(lambda i: graphs[i].replay(), idx)
+    del graphs
+    # the bookkeeping alone, on further steps of the walk (events between the calls)
+    sd_us, lru_us, miss = [], [], []
+    st_ = torch.cuda.current_stream()
+    for i in range(n_iter, n_iter + max(args.steps, 5)):
+        spkv.score_blocks(scache, qs[i], pt, seq, scores)
+        spkv.select_topk(scache, scores, ev, alive, seq, k_q, k_e, sel, n_sel)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(st_)
+        spkv.resident_setdiff(scache, resident, sel, n_sel, missing, n_missing, slot)
+        e[1].record(st_)
+        spkv.lru_bucket_update(scache, resident, ts, slot, n_sel, missing, n_missing, i, 1, victims, hist)
+        e[2].record(st_)
+        torch.cuda.synchronize()
+        sd_us.append(e[0].elapsed_time(e[1]) * 1e3)
+        lru_us.append(e[1].elapsed_time(e[2]) * 1e3)
+        miss.append(int(n_missing.sum().item()))
+    st, bits = spkv.get_device_error(scache)
+    if st != 0:
+        raise RuntimeError(f"device error bits {bits} in the resident 262k leg")
+    byts = _parts(step_bytes(w, k_q + k_e), ("score", "select", "setdiff", "lru", "attn"))
+    ms = statistics.mean(ms_all)
+    gbs = byts / (ms * 1e-3) / 1e9
+    res = {"workload": w["name"] + ", pool resident on the device",
+           "step": "score, select + set-difference + LRU (2048 slots), sparse attention",
+           "ms_per_step": ms, "ms_per_step_median": statistics.median(ms_all), "bytes_per_step": byts,
+           "GBps": gbs, "pct_hbm_peak": 100 * gbs / peak, "queries_per_s": B / (ms * 1e-3),
+           "resident_setdiff_us": statistics.median(sd_us), "lru_bucket_update_us": statistics.median(lru_us),
+           "missing_pages_per_step": statistics.mean(miss), "launch": "one CUDA graph per step"}
+    if cpu_baseline:
+        units = np.arange(U, dtype=np.int32)
+        w1 = dict(w, q=q_host0)
+        dt = _oracle_timed(lambda: oracle_step(w1, units, n_slots=ns), min_s=0.0)
+        res["cpu_baseline"] = _cpu_line(dt, byts, os.cpu_count() or 1,
+                                        f"one whole step (all {U} units) at the walk's first query, fp64")
+    return res
+
+
+def offload_leg(args, dev, stream, timed, cap, peak, cpu_baseline):
     """Retrieve over the host link: the 262k-context workload (B8, Hq40/Hk8, 4096 pages per
     request, k = 128) with the whole K/V pool in pinned host memory and 2048 device slots per
     (request, kv head).  The pooled-key summaries stay on the device (built once from a device
@@ -278,7 +568,10 @@ def offload_leg(args, dev, stream, timed):
     slots = spkv.paged_kv_create(k_slots, v_slots, None, None, max_units=U)
     pt, seq = i32(w["page_table"]), i32(w["seq_len"])
     n_iter = args.warmup + args.steps
-    qs = [bf(q) for q in gen.walk_queries(w, 2 * n_iter + 1)]   # eager steps, then graph-captured steps
+    walk = gen.walk_queries(w, 2 * n_iter + max(args.steps, 5) + 1)
+    qs = [bf(q) for q in walk]   # eager steps, then graph-captured steps
+    # the same workload with its pool resident on the device (the handle over the device pool)
+    resident = resident262k_leg(args, dev, timed, cap, peak, cpu_baseline, w, scache, qs, walk[0])
     ev = torch.from_numpy(w["evict"].astype(np.float32)).to(dev)
     scores = torch.empty(B, Hk, npm, dtype=torch.float32, device=dev)
     alive = torch.full((B, Hk, (npm + 31) // 32), -1, dtype=torch.int32, device=dev)
@@ -405,7 +698,7 @@ def offload_leg(args, dev, stream, timed):
     }
     del dk, dv, dks, k_slots, v_slots, k_host, v_host
     torch.cuda.empty_cache()
-    return out_d
+    return out_d, resident
 
 
 def run_native(args):
@@ -561,6 +854,7 @@ def run_native(args):
     value = replica_throughput(world, step_total, ms)
     attn_avg = statistics.mean(attn_ms)
     peak, peak_kind = peaks()
+    cpu_on = rank == 0 and world == 1 and not args.no_cpu_baseline
     achieved = byts["attn_kv"] / (attn_avg * 1e-3) / 1e9
 
     # ---- lazy-RoPE attention on the same selected pages (8 documents x 4096 tokens)
@@ -664,9 +958,20 @@ def run_native(args):
                            f"(pool of {args.rag_docs} documents)",
                "us": rag_ms * 1e3, "logical_GBps": logical / (rag_ms * 1e-3) / 1e9,
                "distinct_page_GBps": distinct / (rag_ms * 1e-3) / 1e9,
+               "distinct_page_frac": distinct / (rag_ms * 1e-3) / 1e9 / peak,
                "logical_bytes": logical, "distinct_page_bytes": distinct,
                "queries_per_s": Br / (rag_ms * 1e-3),
                "note": "logical = every (request, head, page) read; shared hot documents hit in L2"}
+        if cpu_on:
+            import oracle
+            su = np.sort(np.random.default_rng(0).choice(Br * Hkr, 64, replace=False)).astype(np.int32)
+            thr = os.cpu_count() or 1
+            dt = _oracle_timed(lambda: oracle.lazy_attn_batch(
+                wr["q"], wr["k_pool"], wr["v_pool"], wr["phys"], wr["valid"], wr["slot"], wr["n_pages"], wr["qpos"],
+                wr["doc_pos"], wr["theta"], materialise=False, units=su, nthreads=thr), min_s=0.0)
+            su_bytes = int(wr["n_pages"][su // Hkr].sum()) * PAGE_BYTES
+            rag["cpu_baseline"] = _cpu_line(dt, su_bytes, thr, "64 of the 512 (request, kv head) units, lazy form, "
+                                                               "fp64; logical bytes of those units")
         del rk, rv, rks, rmeta
 
     # ---- cheaper scoring: the same step with bf16 pooled-key summaries (half the scoring bytes)
@@ -724,25 +1029,61 @@ def run_native(args):
         sums = cs.sum(-1)
         if not torch.allclose(sums, torch.full_like(sums, float(ac)), rtol=1e-3):
             raise RuntimeError("column scores do not sum to the window size")
+        # the method's own work: one S = Q K^T over the window rows and every key (the rows' maximum
+        # and sum come from the attention that already ran)
+        cflops = 2.0 * 128 * ac * nc * Hq * Bc
+        ctf = cflops / (col_ms * 1e-3) / 1e12
+        tpeak, tkind = bf16_peak()
+        # the form that takes each window row's log-sum-exp from that attention: the rows' LSE is
+        # prepared here with plain torch on the device (input set-up, outside the timed region)
+        kk = ck.view(Hk, Bc * npc * 64, 128)
+        lse_in = torch.empty(Bc, ac, Hq, dtype=torch.float32, device=dev)
+        pos = torch.arange(nc, device=dev)
+        for b in range(Bc):
+            rows = (cpt[b].long()[:, None] * 64 + torch.arange(64, device=dev)[None, :]).reshape(-1)[:nc]
+            for h in range(Hk):
+                kb = kk[h, rows].float()
+                z = torch.einsum("ahd,kd->ahk", cq[b, :, h * (Hq // Hk):(h + 1) * (Hq // Hk)].float(), kb)
+                z = z / float(np.sqrt(128.0))
+                vis = pos[None, :] <= (nc - ac + torch.arange(ac, device=dev))[:, None]
+                z = z.masked_fill(~vis[:, None, :], float("-inf"))
+                lse_in[b, :, h * (Hq // Hk):(h + 1) * (Hq // Hk)] = torch.logsumexp(z, dim=-1)
+        csl = torch.empty_like(cs)
+
+        def col_lse_call(i):
+            spkv.attn_column_scores_lse(ccache, cq, lse_in, cpt, cseq, csl)
+
+        timed(col_lse_call, range(3))
+        coll_ms = statistics.mean(timed(col_lse_call, timed_idx))
+        if not torch.allclose(csl, cs, rtol=1e-3, atol=1e-5):
+            raise RuntimeError("column scores from the given LSE differ from the two-pass form")
         st_c, bits_c = spkv.get_device_error(ccache)
         if st_c != 0:
             raise RuntimeError(f"device error bits {bits_c} in the column-score leg")
-        ccache.close()
-        cflops = 4.0 * 128 * ac * nc * Hq * Bc   # S = Q K^T over the window rows and all keys, in both passes
-        ctf = cflops / (col_ms * 1e-3) / 1e12
-        tpeak, tkind = bf16_peak()
+        ctf_l = cflops / (coll_ms * 1e-3) / 1e12
         colsc = {"kernel": "attn_column_scores (colscore_kernel: tcgen05.mma, TMA pages, two passes)",
                  "workload": f"{Bc} prompts x {nc} tokens, window of the last {ac} rows, Hq {Hq} / Hk {Hk}",
-                 "us": col_ms * 1e3, "flops": cflops, "bound": "tensor", "achieved_TFLOPs": ctf,
+                 "us": col_ms * 1e3, "flops": cflops,
+                 "flops_def": "2 * 128 * window rows * prompt tokens * Hq * prompts (one Q K^T pass)",
+                 "bound": "tensor", "achieved_TFLOPs": ctf,
                  "peak": tpeak, "peak_kind": tkind + " bf16 dense (cuBLAS burst)", "frac": ctf / tpeak,
                  "prompts_per_s": Bc / (col_ms * 1e-3),
-                 "launches": "one memset and one kernel (both 128-row chunks of the window in one grid)"}
-        del ck, cq, cs
+                 "launches": "one memset and one kernel (both 128-row chunks of the window in one grid)",
+                 "given_lse": {"kernel": "attn_column_scores_lse (the probability pass alone)",
+                               "us": coll_ms * 1e3, "achieved_TFLOPs": ctf_l, "frac": ctf_l / tpeak}}
+        ccache.close()
+        del ck, cq, cs, csl, lse_in
 
     # ---- offload: the 262k-context workload with its K/V pool in pinned host memory
-    offload = None
+    offload, resident = None, None
     if not args.no_offload and rank == 0:
-        offload = offload_leg(args, dev, stream, timed)
+        offload, resident = offload_leg(args, dev, stream, timed, cap, peak, cpu_on)
+
+    # ---- the other workloads of the per-config report
+    tiny, traj = None, None
+    if not args.no_configs and rank == 0:
+        tiny = tiny_leg(args, dev, timed, cap, peak, cpu_on)
+        traj = traj_leg(args, dev, timed, cap, peak, cpu_on)
 
     # ---- end to end through the public API: pinned host inputs in, outputs back, every step.
     # A step's inputs (q, eviction scores, the new K and V rows) sit in one pinned host buffer
@@ -813,9 +1154,10 @@ def run_native(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         units = np.arange(U, dtype=np.int32)
-        dt, sb, thr = oracle_sample(w, units)
-        cpu = {"value": sb / dt / 1e9, "unit": UNIT, "cores": thr, "kind": "oracle",
-               "sample": f"one full step (all {U} units): score_blocks + select_topk + attention, fp64",
+        dt, thr = oracle_step(w, units)
+        cpu = {"value": step_total / dt / 1e9, "unit": UNIT, "cores": thr, "kind": "oracle",
+               "sample": (f"one whole step (all {U} units): block scores, dual top-k selection, sparse attention, "
+                          f"set-difference and LRU update ({N_SLOTS} slots), fp64"),
                "ms_per_step": dt * 1e3}
 
     cache.close()
@@ -850,6 +1192,18 @@ def run_native(args):
             "bf16_summaries": bf16_sum,
             "column_scores": colsc,
             "offload": offload,
+            "per_config": {
+                "1_tiny": tiny,
+                "2_llama8b": {"workload": w["name"], "ms_per_step": ms, "GBps": value,
+                              "pct_hbm_peak": 100.0 * (step_total / (ms * 1e-3) / 1e9) / peak,
+                              "queries_per_s": world * B / (ms * 1e-3), "sparse_decode_attn_us": attn_avg * 1e3,
+                              "sparse_decode_attn_frac": achieved / peak,
+                              "lazy_rope_decode_attn_frac": lazy["frac"] if lazy else None,
+                              "cpu_baseline": cpu},
+                "3_lazy_rag": rag,
+                "4_long262k_resident": resident,
+                "5_nosa_traj": traj,
+            },
             "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
                     "launch": "one CUDA graph per step: copies in from pinned host memory, the API calls, "

@@ -38,6 +38,7 @@ _lib = None
 # Stream tags: one independent random stream per tensor kind.
 TAG_K, TAG_V, TAG_Q, TAG_E, TAG_PERM = 1, 2, 3, 4, 5
 TAG_DOC_LEN, TAG_DOC_PICK, TAG_DOC_PERM = 6, 7, 8
+TAG_SELF_K, TAG_SELF_V, TAG_ROWS_Q = 9, 10, 11
 TAG_STEP_E, TAG_STEP_Q, TAG_STEP_K, TAG_STEP_V = 1000, 2000, 3000, 4000
 
 
@@ -284,3 +285,53 @@ def lazy_rag(seed: int = 0, B: int = 64, Hq: int = 32, Hk: int = 8, n_docs: int 
                 k_pool=k_pool, v_pool=v_pool, q=q, phys=phys, valid=valid, slot=slot, page_start=page_start,
                 n_pages=n_pages, doc_pos=doc_pos, qpos=qpos, theta=theta, picks=picks,
                 doc_len=doc_len, page_cnt=cnt, max_docs=docs_per_req, seed=seed)
+
+
+def prefill_step(seed: int = 0, B: int = 3, T: int = 128, Hq: int = 8, Hk: int = 2, n_docs: int = 12,
+                 docs_per_req: int = 4, min_len: int = 70, max_len: int = 900, theta: float = 500000.0,
+                 cached: bool = True) -> dict:
+    """A prompt's prefill step: each request's cached documents (the ``lazy_rag`` layout, none when
+    ``cached`` is False) followed by its T new rows' own K/V in ceil(T/64) fresh pages, listed last as
+    one more document placed at the first new row's position ``qpos0`` (the cached length); its pages
+    have document-local starts 0, 64, ...  ``q`` holds the new rows' queries [B][T][Hq][128].  The new
+    keys stand for keys that carry the rotation of their position inside the prompt."""
+    if cached:
+        w = lazy_rag(seed, B, Hq, Hk, n_docs, docs_per_req, min_len, max_len, theta=theta)
+    else:
+        w = dict(name="", B=B, Hq=Hq, Hk=Hk, G=Hq // Hk, D=HEAD_DIM, T=PAGE, n_phys=0, np_max=0,
+                 k_pool=np.zeros((Hk, 0, PAGE, HEAD_DIM), np.uint16), v_pool=np.zeros((Hk, 0, PAGE, HEAD_DIM), np.uint16),
+                 phys=np.zeros((B, 0), np.int32), valid=np.zeros((B, 0), np.int32), slot=np.zeros((B, 0), np.int32),
+                 page_start=np.zeros((B, 0), np.int32), n_pages=np.zeros(B, np.int32),
+                 doc_pos=np.zeros((B, 0), np.int32), qpos=np.zeros(B, np.int32), theta=theta,
+                 page_cnt=np.zeros(0, np.int32), max_docs=0, seed=seed)
+    n_self = (T + PAGE - 1) // PAGE
+    n_old = w["n_phys"]
+    n_phys = n_old + B * n_self
+    rows = Hk * B * n_self * PAGE
+    k_new = rows_bf16(seed, TAG_SELF_K, rows).reshape(Hk, B * n_self, PAGE, HEAD_DIM)
+    v_new = rows_bf16(seed, TAG_SELF_V, rows).reshape(Hk, B * n_self, PAGE, HEAD_DIM)
+    k_pool = np.concatenate([w["k_pool"], k_new], axis=1)
+    v_pool = np.concatenate([w["v_pool"], v_new], axis=1)
+    np_max = int((w["n_pages"] + n_self).max())
+    slot_self = w["max_docs"]
+    arrs = {}
+    for key, fill in (("phys", -1), ("valid", 0), ("slot", 0), ("page_start", 0)):
+        a = np.full((B, np_max), fill, np.int32)
+        a[:, :w[key].shape[1]] = w[key]
+        arrs[key] = a
+    cnt = np.concatenate([w["page_cnt"], np.zeros(B * n_self, np.int32)])
+    for b in range(B):
+        j0 = int(w["n_pages"][b])
+        for p in range(n_self):
+            ph = n_old + b * n_self + p
+            arrs["phys"][b, j0 + p] = ph
+            arrs["valid"][b, j0 + p] = min(PAGE, T - PAGE * p)
+            arrs["slot"][b, j0 + p] = slot_self
+            arrs["page_start"][b, j0 + p] = PAGE * p
+            cnt[ph] = min(PAGE, T - PAGE * p)
+    doc_pos = np.concatenate([w["doc_pos"], w["qpos"][:, None]], axis=1).astype(np.int32)
+    q = rows_bf16(seed, TAG_ROWS_Q, B * T * Hq).reshape(B, T, Hq, HEAD_DIM)
+    return dict(name=f"prefill step B{B} T{T} Hq{Hq}/Hk{Hk}", B=B, T=T, Hq=Hq, Hk=Hk, G=Hq // Hk, n_phys=n_phys,
+                np_max=np_max, k_pool=k_pool, v_pool=v_pool, q=q, n_pages=(w["n_pages"] + n_self).astype(np.int32),
+                doc_pos=doc_pos, qpos0=w["qpos"].astype(np.int32), theta=theta, page_cnt=cnt,
+                max_docs=slot_self + 1, seed=seed, **arrs)

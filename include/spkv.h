@@ -15,8 +15,10 @@
  *   sparse_decode_attn   split-K flash decoding over the selected pages
  *   lazy_rope_decode_attn  the same with deferred RoPE (query rotated once per document)
  *   lazy_rope_prefill_attn a tile of new query rows over cached documents (tcgen05)
- *   lazy_alibi_prefill_attn  the same for models with ALiBi position biases
+ *   lazy_rope_prefill_step   the same plus the new rows' causal attention among themselves
+ *   lazy_alibi_prefill_attn  the prefill step for models with ALiBi position biases
  *   attn_column_scores   PyramidKV-style key scores of a prompt's last rows (tcgen05)
+ *   attn_column_scores_lse  the same from row log-sum-exps the attention already produced
  *
  * Sources (web pages, cited by title and section):
  *   [NOSA] "NOSA: Native and Offloadable Sparse Attention", sections "Method 1: the NOSA
@@ -241,6 +243,25 @@ int lazy_rope_prefill_attn(spkv_cache_t cache, const void* q, int B, int T, int 
                            const int32_t* n_pages, int np_max, const int32_t* doc_pos,
                            int max_docs, float theta, float* out, float* lse, void* stream);
 
+/* The whole prefill step of a prompt: lazy_rope_prefill_attn plus the new rows' causal attention
+ * among themselves, in one softmax ([Lazy] "Technical implementation 1. Prefilling": the prompt's
+ * tile attends to the cached documents after one relative rotation each; its own keys complete
+ * the step).  Every listed key has an absolute position m = doc_pos[b][slot] + page_start[j] + t
+ * (row t of listed page j), and query row t' of request b (position n = qpos0[b] + t') attends
+ * to the keys with m <= n.  The caller lists the new rows' own K/V (written with paged_kv_append,
+ * keys carrying the rotation of their position within the prompt, 0 .. T-1) as one more document
+ * placed at doc_pos = qpos0[b], after the cached documents: cached keys all precede the rows, the
+ * rows' own keys are seen causally, and out / lse are the complete prefill attention.
+ *   page_start : device int32 with the shape of meta ([B][meta_heads][np_max]), the document-local
+ *                position of each listed page's first token
+ *   every other argument: as lazy_rope_prefill_attn (which equals this call when no key lies
+ *   after any row).
+ * A row that sees no key gets out = 0 and lse = -inf.  page_start NULL is SPKV_EINVAL. */
+int lazy_rope_prefill_step(spkv_cache_t cache, const void* q, int B, int T, int Hq, const int32_t* qpos0,
+                           const uint32_t* meta, int meta_heads, const int32_t* n_pages, int np_max,
+                           const int32_t* page_start, const int32_t* doc_pos, int max_docs, float theta,
+                           float* out, float* lse, void* stream);
+
 /* The prefill above for ALiBi models ([Lazy] "Key contributions" 4: the mechanism carries over to
  * other relative position encodings, ALiBi among them).  Keys are stored with no positional
  * transform, so a cached document is reused at any offset as it is; the position enters only as
@@ -249,7 +270,9 @@ int lazy_rope_prefill_attn(spkv_cache_t cache, const void* q, int B, int T, int 
  * (position n = qpos0[b] + t') and query head hq:
  *   score = q . key / sqrt(128) - slopes[hq] * (n - m)
  *   out[b][t'][hq][:] = sum softmax(score) v,  lse[b][t'][hq] = log sum exp(score)   (natural log)
- * over every valid key of the request's listed pages (no mask, as lazy_rope_prefill_attn).
+ * over every valid key of the request's listed pages at a position m <= n (keys after the row
+ * are masked, as in lazy_rope_prefill_step: cached documents are seen whole, and the new rows'
+ * own keys listed as a document placed at qpos0[b] make this the whole prefill step).
  *   page_start : device int32 with the shape of meta ([B][meta_heads][np_max])
  *   slopes     : device fp32 [Hq] (natural-log units per token of distance)
  *   q, qpos0, meta, meta_heads, n_pages, np_max, doc_pos, max_docs, out, lse: as above
@@ -280,6 +303,18 @@ int lazy_alibi_prefill_attn(spkv_cache_t cache, const void* q, int B, int T, int
 int attn_column_scores(spkv_cache_t cache, const void* q, int B, int alpha, int Hq,
                        const int32_t* page_table, int np_max, const int32_t* seq_len,
                        float* scores, void* stream);
+
+/* attn_column_scores with each window row's log-sum-exp supplied by the caller, as the
+ * attention that already computed rowmax and l over the same keys returns it ([FA] "2. Attention
+ * modification": the FlashAttention pass outputs rowmax and l, and the score adds only the
+ * probability pass).  The kernel skips its first pass and computes
+ *   scores[b][hq][i] = sum over rows j with i <= n - alpha + j of exp(q_j . k_i / sqrt(128) - lse[b][j][hq])
+ * which equals attn_column_scores when lse is each row's own log-sum-exp over its visible keys.
+ *   lse : device fp32 [B][alpha][Hq], natural log, finite (not checked)
+ * Every other argument, limit and error: as attn_column_scores; lse NULL is SPKV_EINVAL. */
+int attn_column_scores_lse(spkv_cache_t cache, const void* q, const float* lse, int B, int alpha, int Hq,
+                           const int32_t* page_table, int np_max, const int32_t* seq_len, float* scores,
+                           void* stream);
 
 int resident_setdiff(spkv_cache_t cache, const int32_t* resident, int n_slots, const int32_t* sel,
                      const int32_t* n_sel, int sel_stride, int n_units, int32_t* missing,

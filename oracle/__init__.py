@@ -72,6 +72,10 @@ def _l():
                                          vp, i32, vp, vp, i32, vp, vp, i32], None),
             "orc_column_scores_batch": ([i32, i32, i32, i32, vp, vp, i64, vp, i32, vp, i32, vp, i32, vp, i32],
                                         None),
+            "orc_prefill_step_batch": ([i32, i32, i32, i32, vp, vp, vp, i64, vp, vp, vp, vp, i32, vp, i32, vp, vp,
+                                        i32, f64, i32, vp, i32, vp, vp, i32], None),
+            "orc_column_scores_given_lse_batch": ([i32, i32, i32, i32, vp, vp, vp, i64, vp, i32, vp, i32, vp, i32,
+                                                   vp, i32], None),
             "orc_retrieve_unit": ([vp, vp, vp, vp, i32, vp, vp, i32, vp, vp], None),
             "orc_retrieve_batch": ([i32, i32, vp, vp, i64, vp, i32, vp, vp, vp, vp, vp, i32, vp, vp, i64,
                                     i32, i32], None),
@@ -361,6 +365,32 @@ def lazy_prefill_batch(q, k_pool, v_pool, phys, valid, slot, n_pages, qpos0, doc
     return out, lse
 
 
+def prefill_step_batch(q, k_pool, v_pool, phys, valid, slot, page_start, n_pages, qpos0, doc_pos, theta: float,
+                       mode: str = "materialised", items=None, nthreads: int = 0):
+    """The whole RoPE prefill step: rows at positions qpos0[b] + t over every listed key at a position
+    m = doc_pos[slot] + page_start + row <= the row's position (the rows' own keys listed as a document
+    placed at qpos0).  mode: "materialised" (keys rotated to their positions), "lazy" (query rotated
+    per document) or "lazy_bf16q" (the lazy form with the rotated query rounded to bf16).
+    Arrays as lazy_prefill_batch, page_start with the shape of phys.  Returns (out, lse)."""
+    modes = {"materialised": 0, "lazy": 1, "lazy_bf16q": 2}
+    q, k_pool, v_pool = _c(q, np.uint16), _c(k_pool, np.uint16), _c(v_pool, np.uint16)
+    if phys.ndim == 2:
+        phys, valid, slot, page_start = phys[:, None, :], valid[:, None, :], slot[:, None, :], page_start[:, None, :]
+    phys, valid, slot, page_start = (_c(phys, np.int32), _c(valid, np.int32), _c(slot, np.int32),
+                                     _c(page_start, np.int32))
+    n_pages, qpos0, doc_pos = _c(n_pages, np.int32), _c(qpos0, np.int32), _c(doc_pos, np.int32)
+    B, T, Hq, _ = q.shape
+    Hk, n_phys = k_pool.shape[0], k_pool.shape[1]
+    out = np.zeros((B, T, Hq, D), np.float64)
+    lse = np.zeros((B, T, Hq), np.float64)
+    it = _units(items, B * T * Hk)
+    _l().orc_prefill_step_batch(B, T, Hq, Hk, _p(q), _p(k_pool), _p(v_pool), n_phys, _p(phys), _p(valid), _p(slot),
+                                _p(page_start), phys.shape[1], _p(n_pages), phys.shape[2], _p(qpos0), _p(doc_pos),
+                                doc_pos.shape[1], float(theta), modes[mode], _p(it), it.shape[0], _p(out), _p(lse),
+                                nthreads)
+    return out, lse
+
+
 def alibi_prefill_batch(q, k_pool, v_pool, phys, valid, slot, page_start, n_pages, qpos0, doc_pos, slopes,
                         items=None, nthreads: int = 0):
     """ALiBi prefill over cached documents: like lazy_prefill_batch with the linear position bias
@@ -396,4 +426,22 @@ def column_scores_batch(q, k_pool, page_table, seq_len, n_out: int, items=None, 
     it = _units(items, B * Hq)
     _l().orc_column_scores_batch(B, Hq, Hk, alpha, _p(q), _p(k_pool), n_phys, _p(page_table), page_table.shape[1],
                                  _p(seq_len), int(n_out), _p(it), it.shape[0], _p(S), nthreads)
+    return S
+
+
+def column_scores_given_lse_batch(q, lse, k_pool, page_table, seq_len, n_out: int, items=None, nthreads: int = 0):
+    """The column score with each window row's log-sum-exp given: lse [B][alpha][Hq] (natural log);
+    S[b][hq][i] = sum over the rows j that see key i of exp(q_j . k_i / sqrt(128) - lse[b][j][hq])."""
+    q, k_pool = _c(q, np.uint16), _c(k_pool, np.uint16)
+    lse = _c(lse, np.float64)
+    page_table, seq_len = _c(page_table, np.int32), _c(seq_len, np.int32)
+    B, alpha, Hq, _ = q.shape
+    if lse.shape != (B, alpha, Hq):
+        raise ValueError("lse must be [B][alpha][Hq]")
+    Hk, n_phys = k_pool.shape[0], k_pool.shape[1]
+    S = np.zeros((B, Hq, n_out), np.float64)
+    it = _units(items, B * Hq)
+    _l().orc_column_scores_given_lse_batch(B, Hq, Hk, alpha, _p(q), _p(lse), _p(k_pool), n_phys, _p(page_table),
+                                           page_table.shape[1], _p(seq_len), int(n_out), _p(it), it.shape[0],
+                                           _p(S), nthreads)
     return S

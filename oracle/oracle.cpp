@@ -32,6 +32,9 @@
 //   R7 packed page word: phys[0:18) | (valid-1)[18:24) | doc slot[24:32).
 //   R8 LRU: bucket = min(63, max(0, t - ts) / W); empty slots are bucket 63; hits are
 //      touched first; victims are untouched slots in (bucket desc, slot asc) order.
+//   R19 prefill step: a prompt row at position n attends to every listed key at a position
+//      m <= n; the rows' own keys are listed as a document placed at the first row's position.
+//   R20 the prefill's rotated query enters the tensor cores rounded to bf16 (oracle mode 2).
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -548,30 +551,124 @@ void orc_lazy_prefill_batch(int B, int T, int Hq, int Hk, const uint16_t* q, con
   });
 }
 
+// ---------------------------------------------------------------- the whole RoPE prefill step
+// [Lazy] "Technical implementation 1. Prefilling" with reading R19: the prompt's T new rows at
+// positions n0 + t attend over every listed key whose absolute position does not come after the
+// row, m = doc_pos[slot[i]] + page_start[i] + t <= n.  Cached documents all precede n0, so they are
+// seen whole; the rows' own keys, listed as one more document placed at n0 (their document-local
+// positions 0 .. T-1), give the causal attention of the rows among themselves in the same softmax.
+// mode 0 (materialised, the plain definition): each stored key, which carries its document-local
+// rotation, is copied and rotated by R(doc_pos[slot]) to its absolute position, the query by
+// R(n), then softmax attention over the visible copies.
+// mode 1 (lazy): keys as stored, the query rotated by R(n - doc_pos[slot]) for each document.
+// mode 2: mode 1 with the rotated query rounded to bf16 (nearest, ties to even) before the dot
+// products -- the precision at which the rotated query enters the tensor cores (reading R20).
+void orc_attn_step_unit(const uint16_t* q, int G, const uint16_t* kplane, const uint16_t* vplane,
+                        const int32_t* phys, const int32_t* valid, const int32_t* slot, const int32_t* page_start,
+                        int n_pages, int32_t qpos, const int32_t* doc_pos, double theta, int mode, double* out,
+                        double* lse) {
+  const double inv_sqrt_d = 1.0 / std::sqrt(static_cast<double>(kD));
+  std::vector<double> z;
+  std::vector<const uint16_t*> vrow;
+  double qin[kD], qrot[kD], kin[kD], krot[kD];
+  for (int g = 0; g < G; ++g) {
+    for (int d = 0; d < kD; ++d) qin[d] = from_bf16(q[g * kD + d]);
+    if (mode == 0) orc_rope(qin, static_cast<double>(qpos), theta, qrot);
+    z.clear();
+    vrow.clear();
+    int cur_slot = -1;
+    for (int i = 0; i < n_pages; ++i) {
+      if (mode != 0 && slot[i] != cur_slot) {
+        cur_slot = slot[i];
+        orc_rope(qin, static_cast<double>(qpos) - doc_pos[cur_slot], theta, qrot);
+        if (mode == 2)
+          for (int d = 0; d < kD; ++d) qrot[d] = orc_round_bf16(qrot[d]);
+      }
+      for (int t = 0; t < valid[i]; ++t) {
+        const int64_t m = static_cast<int64_t>(doc_pos[slot[i]]) + page_start[i] + t;
+        if (m > qpos) continue;   // a key after the row is not attended
+        const uint16_t* k = row_ptr(kplane, phys[i], t);
+        for (int d = 0; d < kD; ++d) kin[d] = from_bf16(k[d]);
+        const double* kk = kin;
+        if (mode == 0) {
+          orc_rope(kin, static_cast<double>(doc_pos[slot[i]]), theta, krot);
+          kk = krot;
+        }
+        double dot = 0.0;
+        for (int d = 0; d < kD; ++d) dot += qrot[d] * kk[d];
+        z.push_back(dot * inv_sqrt_d);
+        vrow.push_back(row_ptr(vplane, phys[i], t));
+      }
+    }
+    for (int d = 0; d < kD; ++d) out[g * kD + d] = 0.0;
+    if (z.empty()) {
+      lse[g] = kNegInf;
+      continue;
+    }
+    const double mx = *std::max_element(z.begin(), z.end());
+    double l = 0.0;
+    for (double x : z) l += std::exp(x - mx);
+    for (size_t r = 0; r < z.size(); ++r) {
+      const double w = std::exp(z[r] - mx) / l;
+      for (int d = 0; d < kD; ++d) out[g * kD + d] += w * from_bf16(vrow[r][d]);
+    }
+    lse[g] = mx + std::log(l);
+  }
+}
+
+// The step for every (request, row, kv head) work item listed, numbered ((b * T) + t) * Hk + h;
+// arrays as in orc_lazy_prefill_batch plus page_start ([B][meta_heads][np_max], the document-local
+// position of each listed page's first token).
+void orc_prefill_step_batch(int B, int T, int Hq, int Hk, const uint16_t* q, const uint16_t* kpool,
+                            const uint16_t* vpool, int64_t n_phys, const int32_t* phys, const int32_t* valid,
+                            const int32_t* slot, const int32_t* page_start, int meta_heads, const int32_t* n_pages,
+                            int np_max, const int32_t* qpos0, const int32_t* doc_pos, int max_docs, double theta,
+                            int mode, const int32_t* items, int n_items, double* out, double* lse, int nthreads) {
+  (void)B;
+  const int G = Hq / Hk;
+  for_units(n_items, nthreads, [&](int i) {
+    const int it = items[i];
+    const int h = it % Hk, bt = it / Hk, t = bt % T, b = bt / T;
+    const int mh = meta_heads == 1 ? 0 : h;
+    const int64_t mo = (static_cast<int64_t>(b) * meta_heads + mh) * np_max;
+    const int64_t plane = static_cast<int64_t>(h) * n_phys * kPage * kD;
+    const int64_t qo = static_cast<int64_t>(bt) * Hq + h * G;
+    orc_attn_step_unit(q + qo * kD, G, kpool + plane, vpool + plane, phys + mo, valid + mo, slot + mo,
+                       page_start + mo, n_pages[b], qpos0[b] + t, doc_pos + static_cast<int64_t>(b) * max_docs,
+                       theta, mode, out + qo * kD, lse + qo);
+  });
+}
+
 // ---------------------------------------------------------------- ALiBi prefill
 // [Lazy] "Key contributions" 4 (the mechanism carries over to other relative position encodings,
 // ALiBi among them), reading R18: keys are stored with no positional transform; the key at
 // document-local position page_start[i] + t of document slot[i], placed at token offset
 // doc_pos[slot[i]], sits at m = doc_pos[slot[i]] + page_start[i] + t; the query row at position
 // n scores it as q . k / sqrt(128) - slope * (n - m) (the linear bias of ALiBi, one slope per
-// query head, natural-log units), and plain softmax attention follows.  No mask (as the RoPE
-// prefill).  q: G query heads of 128 bf16; slopes: their G slopes.
+// query head, natural-log units), and plain softmax attention follows over the keys that do not
+// come after the row (m <= n; reading R19): cached documents all precede the rows, and the rows'
+// own keys listed as a document at offset n0 give the causal part of the prefill step.
+// q: G query heads of 128 bf16; slopes: their G slopes.
 void orc_alibi_attn_unit(const uint16_t* q, int G, const float* slopes, const uint16_t* kplane,
                          const uint16_t* vplane, const int32_t* phys, const int32_t* valid, const int32_t* slot,
                          const int32_t* page_start, int n_pages, int32_t qpos, const int32_t* doc_pos,
                          double* out, double* lse) {
   const double inv_sqrt_d = 1.0 / std::sqrt(static_cast<double>(kD));
   std::vector<double> z;
+  std::vector<const uint16_t*> vrow;
   for (int g = 0; g < G; ++g) {
     const double slope = slopes[g];
     z.clear();
+    vrow.clear();
     for (int i = 0; i < n_pages; ++i)
       for (int t = 0; t < valid[i]; ++t) {
+        const double m = static_cast<double>(doc_pos[slot[i]]) + page_start[i] + t;
+        if (m > qpos) continue;   // a key after the row is not attended
         const uint16_t* k = row_ptr(kplane, phys[i], t);
         double dot = 0.0;
         for (int d = 0; d < kD; ++d) dot += from_bf16(q[g * kD + d]) * from_bf16(k[d]);
-        const double m = static_cast<double>(doc_pos[slot[i]]) + page_start[i] + t;
         z.push_back(dot * inv_sqrt_d - slope * (static_cast<double>(qpos) - m));
+        vrow.push_back(row_ptr(vplane, phys[i], t));
       }
     for (int d = 0; d < kD; ++d) out[g * kD + d] = 0.0;
     if (z.empty()) {
@@ -581,13 +678,10 @@ void orc_alibi_attn_unit(const uint16_t* q, int G, const float* slopes, const ui
     const double mx = *std::max_element(z.begin(), z.end());
     double l = 0.0;
     for (double x : z) l += std::exp(x - mx);
-    size_t idx = 0;
-    for (int i = 0; i < n_pages; ++i)
-      for (int t = 0; t < valid[i]; ++t, ++idx) {
-        const double w = std::exp(z[idx] - mx) / l;
-        const uint16_t* v = row_ptr(vplane, phys[i], t);
-        for (int d = 0; d < kD; ++d) out[g * kD + d] += w * from_bf16(v[d]);
-      }
+    for (size_t r = 0; r < z.size(); ++r) {
+      const double w = std::exp(z[r] - mx) / l;
+      for (int d = 0; d < kD; ++d) out[g * kD + d] += w * from_bf16(vrow[r][d]);
+    }
     lse[g] = mx + std::log(l);
   }
 }
@@ -660,6 +754,47 @@ void orc_column_scores_batch(int B, int Hq, int Hk, int alpha, const uint16_t* q
                            kpool + static_cast<int64_t>(h) * n_phys * kPage * kD,
                            page_table + static_cast<int64_t>(b) * np_max, seq_len[b], n_out,
                            S + static_cast<int64_t>(it) * n_out);
+  });
+}
+
+// The same score with each row's log-sum-exp given instead of computed ([FA] "2. Attention
+// modification": the FlashAttention pass already produced rowmax and l, so the score needs only
+// the probability pass).  With lse_j the natural-log LSE the caller supplies for row j,
+//   S[i] = sum over rows j with i <= n - alpha + j of exp(q_j . k_i / sqrt(128) - lse_j).
+// When lse_j is the row's own log-sum-exp this is orc_column_scores_unit exactly.
+void orc_column_scores_given_lse_unit(const uint16_t* q, int q_stride, int alpha, const double* lse,
+                                      int lse_stride, const uint16_t* kplane, const int32_t* pt_row, int n,
+                                      int n_out, double* S) {
+  const double inv_sqrt_d = 1.0 / std::sqrt(static_cast<double>(kD));
+  for (int i = 0; i < n_out; ++i) S[i] = 0.0;
+  for (int j = 0; j < alpha; ++j) {
+    const int pos = n - alpha + j;
+    if (pos < 0) continue;
+    const uint16_t* qj = q + static_cast<int64_t>(j) * q_stride;
+    const double lj = lse[static_cast<int64_t>(j) * lse_stride];
+    for (int i = 0; i <= pos; ++i) {
+      const uint16_t* k = row_ptr(kplane, pt_row[i / kPage], i % kPage);
+      double dot = 0.0;
+      for (int d = 0; d < kD; ++d) dot += from_bf16(qj[d]) * from_bf16(k[d]);
+      S[i] += std::exp(dot * inv_sqrt_d - lj);
+    }
+  }
+}
+
+// Batch driver of the given-LSE form: lse is [B][alpha][Hq] (natural log), the rest as above.
+void orc_column_scores_given_lse_batch(int B, int Hq, int Hk, int alpha, const uint16_t* q, const double* lse,
+                                       const uint16_t* kpool, int64_t n_phys, const int32_t* page_table,
+                                       int np_max, const int32_t* seq_len, int n_out, const int32_t* items,
+                                       int n_items, double* S, int nthreads) {
+  (void)B;
+  const int G = Hq / Hk;
+  for_units(n_items, nthreads, [&](int i) {
+    const int it = items[i], b = it / Hq, hq = it % Hq, h = hq / G;
+    orc_column_scores_given_lse_unit(q + (static_cast<int64_t>(b) * alpha * Hq + hq) * kD, Hq * kD, alpha,
+                                     lse + static_cast<int64_t>(b) * alpha * Hq + hq, Hq,
+                                     kpool + static_cast<int64_t>(h) * n_phys * kPage * kD,
+                                     page_table + static_cast<int64_t>(b) * np_max, seq_len[b], n_out,
+                                     S + static_cast<int64_t>(it) * n_out);
   });
 }
 

@@ -33,7 +33,8 @@ __all__ = ["PagedKVCache", "paged_kv_create", "paged_kv_append", "score_blocks",
            "select_topk",
            "sparse_decode_attn", "lazy_rope_decode_attn", "resident_setdiff", "lru_bucket_update",
            "select_resident_update", "retrieve_pages", "sparse_decode_attn_slots", "lazy_rope_prefill_attn",
-           "attn_column_scores", "lazy_alibi_prefill_attn",
+           "lazy_rope_prefill_step",
+           "attn_column_scores", "attn_column_scores_lse", "lazy_alibi_prefill_attn",
            "sparse_decode_attn_noalloc", "pack_page_words", "get_device_error", "SpkvError", "DEVERR",
            "load"]
 
@@ -294,6 +295,28 @@ def lazy_rope_prefill_attn(cache: PagedKVCache, q, qpos0, meta, n_pages, doc_pos
         _stream(stream)))
 
 
+def lazy_rope_prefill_step(cache: PagedKVCache, q, qpos0, meta, n_pages, page_start, doc_pos, theta: float, out,
+                           lse, stream=None):
+    """The whole RoPE prefill step: lazy_rope_prefill_attn over every listed key at a position
+    doc_pos[slot] + page_start + row <= the query row's position (the new rows' own pages listed as a
+    document placed at qpos0 give their causal attention); page_start int32 with the shape of meta."""
+    B, T, Hq = q.shape[0], q.shape[1], q.shape[2]
+    if meta.dim() == 2:
+        meta = meta.unsqueeze(1)
+    if page_start.dim() == 2:
+        page_start = page_start.unsqueeze(1)
+    meta_heads, np_max = meta.shape[1], meta.shape[2]
+    max_docs = doc_pos.shape[1]
+    check("lazy_rope_prefill_step", load().lazy_rope_prefill_step(
+        cache.handle, _t(q, torch.bfloat16, "q", (B, T, Hq, HEAD_DIM)), B, T, Hq,
+        _t(qpos0, torch.int32, "qpos0", (B,)), _t(meta, torch.int32, "meta", (B, meta_heads, np_max)),
+        meta_heads, _t(n_pages, torch.int32, "n_pages", (B,)), np_max,
+        _t(page_start, torch.int32, "page_start", (B, meta_heads, np_max)),
+        _t(doc_pos, torch.int32, "doc_pos", (B, max_docs)), max_docs, float(theta),
+        _t(out, torch.float32, "out", (B, T, Hq, HEAD_DIM)), _t(lse, torch.float32, "lse", (B, T, Hq)),
+        _stream(stream)))
+
+
 def lazy_alibi_prefill_attn(cache: PagedKVCache, q, qpos0, meta, n_pages, page_start, doc_pos, slopes, out, lse,
                             stream=None):
     """The prefill for ALiBi models: keys unrotated, bias -slopes[hq] * (n - m) with m = doc_pos[slot] +
@@ -322,6 +345,19 @@ def attn_column_scores(cache: PagedKVCache, q, page_table, seq_len, scores, stre
     np_max = page_table.shape[1]
     check("attn_column_scores", load().attn_column_scores(
         cache.handle, _t(q, torch.bfloat16, "q", (B, alpha, Hq, HEAD_DIM)), B, alpha, Hq,
+        _t(page_table, torch.int32, "page_table", (B, np_max)), np_max,
+        _t(seq_len, torch.int32, "seq_len", (B,)), _t(scores, torch.float32, "scores", (B, Hq, np_max * PAGE)),
+        _stream(stream)))
+
+
+def attn_column_scores_lse(cache: PagedKVCache, q, lse, page_table, seq_len, scores, stream=None):
+    """attn_column_scores from the window rows' log-sum-exp lse fp32 [B][alpha][Hq] (natural log),
+    as the attention over the same keys returns it; only the probability pass runs."""
+    B, alpha, Hq = q.shape[0], q.shape[1], q.shape[2]
+    np_max = page_table.shape[1]
+    check("attn_column_scores_lse", load().attn_column_scores_lse(
+        cache.handle, _t(q, torch.bfloat16, "q", (B, alpha, Hq, HEAD_DIM)),
+        _t(lse, torch.float32, "lse", (B, alpha, Hq)), B, alpha, Hq,
         _t(page_table, torch.int32, "page_table", (B, np_max)), np_max,
         _t(seq_len, torch.int32, "seq_len", (B,)), _t(scores, torch.float32, "scores", (B, Hq, np_max * PAGE)),
         _stream(stream)))

@@ -37,9 +37,12 @@ SIGNATURES = {
                                _vp], _i32),
     "lazy_rope_prefill_attn": ([_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _f32, _vp,
                                 _vp, _vp], _i32),
+    "lazy_rope_prefill_step": ([_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _vp, _i32, _f32, _vp,
+                                _vp, _vp], _i32),
     "lazy_alibi_prefill_attn": ([_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _vp, _i32, _vp,
                                  _vp, _vp, _vp], _i32),
     "attn_column_scores": ([_vp, _vp, _i32, _i32, _i32, _vp, _i32, _vp, _vp, _vp], _i32),
+    "attn_column_scores_lse": ([_vp, _vp, _vp, _i32, _i32, _i32, _vp, _i32, _vp, _vp, _vp], _i32),
     "resident_setdiff": ([_vp, _vp, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp], _i32),
     "lru_bucket_update": ([_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp],
                           _i32),

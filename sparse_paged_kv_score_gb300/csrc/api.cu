@@ -302,9 +302,10 @@ int lazy_rope_decode_attn(spkv_cache_t c, const void* q, int B, int Hq, const in
   return status_of(spkv::launch_attn(c, p, true, grid, as_stream(stream)));
 }
 
-int lazy_rope_prefill_attn(spkv_cache_t c, const void* q, int B, int T, int Hq, const int32_t* qpos0,
-                           const uint32_t* meta, int meta_heads, const int32_t* n_pages, int np_max,
-                           const int32_t* doc_pos, int max_docs, float theta, float* out, float* lse, void* stream) {
+static int rope_prefill(spkv_cache_t c, const void* q, int B, int T, int Hq, const int32_t* qpos0,
+                        const uint32_t* meta, int meta_heads, const int32_t* n_pages, int np_max,
+                        const int32_t* page_start, const int32_t* doc_pos, int max_docs, float theta, float* out,
+                        float* lse, void* stream) {
   if (!c || B < 0 || T < 0 || Hq <= 0) return SPKV_EINVAL;
   const int Hk = c->d.n_kv_heads;
   if (Hq % Hk != 0) return SPKV_EINVAL;
@@ -336,11 +337,29 @@ int lazy_rope_prefill_attn(spkv_cache_t c, const void* q, int B, int T, int Hq, 
   p.max_docs = max_docs;
   p.scale_log2 = static_cast<float>(1.4426950408889634074 / std::sqrt(128.0));
   p.err = c->dev_err;
+  p.page_start = page_start;
+  p.causal = page_start != nullptr;
   for (int j = 0; j < 64; ++j) {
     const double f = std::pow(static_cast<double>(theta), -2.0 * j / 128.0) / (2.0 * 3.14159265358979323846);
     p.phase_inc[j] = static_cast<uint64_t>(std::ldexp(f, 64));
   }
   return status_of(spkv::launch_prefill(c, p, as_stream(stream)));
+}
+
+int lazy_rope_prefill_attn(spkv_cache_t c, const void* q, int B, int T, int Hq, const int32_t* qpos0,
+                           const uint32_t* meta, int meta_heads, const int32_t* n_pages, int np_max,
+                           const int32_t* doc_pos, int max_docs, float theta, float* out, float* lse, void* stream) {
+  return rope_prefill(c, q, B, T, Hq, qpos0, meta, meta_heads, n_pages, np_max, nullptr, doc_pos, max_docs, theta,
+                      out, lse, stream);
+}
+
+int lazy_rope_prefill_step(spkv_cache_t c, const void* q, int B, int T, int Hq, const int32_t* qpos0,
+                           const uint32_t* meta, int meta_heads, const int32_t* n_pages, int np_max,
+                           const int32_t* page_start, const int32_t* doc_pos, int max_docs, float theta, float* out,
+                           float* lse, void* stream) {
+  if (!page_start) return SPKV_EINVAL;
+  return rope_prefill(c, q, B, T, Hq, qpos0, meta, meta_heads, n_pages, np_max, page_start, doc_pos, max_docs,
+                      theta, out, lse, stream);
 }
 
 int lazy_alibi_prefill_attn(spkv_cache_t c, const void* q, int B, int T, int Hq, const int32_t* qpos0,
@@ -382,8 +401,8 @@ int lazy_alibi_prefill_attn(spkv_cache_t c, const void* q, int B, int T, int Hq,
   return status_of(spkv::launch_prefill(c, p, as_stream(stream)));
 }
 
-int attn_column_scores(spkv_cache_t c, const void* q, int B, int alpha, int Hq, const int32_t* page_table,
-                       int np_max, const int32_t* seq_len, float* scores, void* stream) {
+static int column_scores(spkv_cache_t c, const void* q, const float* lse_in, int B, int alpha, int Hq,
+                  const int32_t* page_table, int np_max, const int32_t* seq_len, float* scores, void* stream) {
   if (!c || B < 0 || Hq <= 0 || alpha < 0) return SPKV_EINVAL;
   const int Hk = c->d.n_kv_heads;
   if (Hq % Hk != 0) return SPKV_EINVAL;
@@ -404,6 +423,7 @@ int attn_column_scores(spkv_cache_t c, const void* q, int B, int alpha, int Hq, 
   p.page_table = page_table;
   p.np_max = np_max;
   p.seq_len = seq_len;
+  p.lse_in = lse_in;
   p.scale_log2 = static_cast<float>(1.4426950408889634074 / std::sqrt(128.0));
   p.err = c->dev_err;
   // each row's softmax is its own, so the column sums of 128-row chunks of the window add.  Two
@@ -423,6 +443,18 @@ int attn_column_scores(spkv_cache_t c, const void* q, int B, int alpha, int Hq, 
     if (st != SPKV_OK) return st;
   }
   return SPKV_OK;
+}
+
+int attn_column_scores(spkv_cache_t c, const void* q, int B, int alpha, int Hq, const int32_t* page_table,
+                       int np_max, const int32_t* seq_len, float* scores, void* stream) {
+  return column_scores(c, q, nullptr, B, alpha, Hq, page_table, np_max, seq_len, scores, stream);
+}
+
+int attn_column_scores_lse(spkv_cache_t c, const void* q, const float* lse, int B, int alpha, int Hq,
+                           const int32_t* page_table, int np_max, const int32_t* seq_len, float* scores,
+                           void* stream) {
+  if (!lse) return SPKV_EINVAL;
+  return column_scores(c, q, lse, B, alpha, Hq, page_table, np_max, seq_len, scores, stream);
 }
 
 int resident_setdiff(spkv_cache_t c, const int32_t* resident, int n_slots, const int32_t* sel, const int32_t* n_sel,

@@ -8,6 +8,9 @@
 // p = exp(q k - rowmax) / l in a second pass, with the loop order turned to k-major so that the
 // sum over rows stays in registers, and skips work the causal mask zeroes.
 //
+// With the rows' log-sum-exp given (the attention that produced rowmax and l returns it), the first
+// pass is skipped and each row's LSE is read instead; the rest is the same.
+//
 // One CTA per (request b, query head hq) and launch; a launch covers one chunk of up to 128 window
 // rows (one M 128 tile).  Every row's softmax is its own, so the chunks' column sums add: the first
 // launch writes them, later launches add theirs.  Eighteen warps:
@@ -126,7 +129,10 @@ __global__ void __launch_bounds__(kCThreads, 1)
   const uint32_t tbase = S.tmem_base;
   const bool valid_req = n >= p.alpha && n <= p.np_max * kPageTokens;
   const int ng = valid_req ? (np_b + 1) / 2 : 0;   // page pairs
-  const int n_jobs = 2 * ng;                       // pass 1, then pass 2
+  // pass 1 (each row's maximum and sum), then pass 2 (the probabilities); with the rows'
+  // log-sum-exp given by the caller, pass 2 alone
+  const int p1 = p.lse_in ? 0 : ng;
+  const int n_jobs = p1 + ng;
 
   if (warp == 0) {
     // ================================================================ TMA producer
@@ -210,14 +216,16 @@ __global__ void __launch_bounds__(kCThreads, 1)
     const int row_min = n - p.alpha + row0;          // position of the chunk's first row
     const int row_pos = row_min + r;                 // position of query row r
     float m = -CUDART_INF_F, l = 0.f, lse2 = CUDART_INF_F;
+    if (p.lse_in && r < rows)      // the caller's natural-log LSE in the log2 domain of the scores
+      lse2 = p.lse_in[(int64_t(b) * p.alpha + row0 + r) * p.Hq + hq] * 1.4426950408889634f;
     bool ok = true;
     float* srow = p.scores + (int64_t(b) * p.Hq + hq) * (int64_t(p.np_max) * kPageTokens);
     for (int j = 0; j < n_jobs; ++j) {
       const int g = j % ng, bb = j & 1;
-      const bool pass2 = j >= ng;
+      const bool pass2 = j >= p1;
       const int key0 = 2 * g * kPageTokens + 32 * grp;   // position of this warp's first key
       const bool live = key0 < n;                        // the pair's tail may lie past the prompt
-      if (j == ng) {                                     // pass 1 done: publish this group's (max, sum)
+      if (p1 > 0 && j == p1) {                           // pass 1 done: publish this group's (max, sum)
         S.ml[grp][0][r] = m;
         S.ml[grp][1][r] = l;
         __syncwarp();
@@ -225,12 +233,12 @@ __global__ void __launch_bounds__(kCThreads, 1)
       }
       // warps meet only through mbarriers, whose waits are bounded: a warp that gives up leaves alone
       bool got = warp_wait(&S.dfull[bb], (j >> 1) & 1);
-      if (j == ng) got = warp_wait(&S.mlready, 0) && got;
+      if (p1 > 0 && j == p1) got = warp_wait(&S.mlready, 0) && got;
       if (!got) {
         ok = false;
         break;
       }
-      if (j == ng) {
+      if (p1 > 0 && j == p1) {
         float mm = -CUDART_INF_F;
 #pragma unroll
         for (int q = 0; q < kGroups; ++q) mm = fmaxf(mm, S.ml[q][0][r]);

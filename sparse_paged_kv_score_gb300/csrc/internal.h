@@ -109,8 +109,10 @@ struct PrefillParams {
   float scale_log2;
   uint32_t* err;
   uint64_t phase_inc[64];
-  const int32_t* page_start;     // ALiBi form (slopes != null): document-local start of each listed page
+  const int32_t* page_start;     // ALiBi form and RoPE step: document-local start of each listed page
   const float* slopes;           // ALiBi form: [Hq] bias slopes (natural-log units); null for RoPE
+  int causal;                    // RoPE step: keys at positions after a row are masked (needs page_start);
+                                 // the ALiBi form always masks them
 };
 
 // Parameters of the column-score kernel (PyramidKV-style score S).
@@ -126,6 +128,7 @@ struct ColScoreParams {
   const int32_t* page_table;     // [B][np_max]
   int np_max;
   const int32_t* seq_len;        // prompt length n per request
+  const float* lse_in;           // [B][alpha][Hq] natural-log LSE of each window row, or null (pass 1 runs)
   float scale_log2;
   uint32_t* err;
 };

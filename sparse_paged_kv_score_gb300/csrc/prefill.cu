@@ -363,12 +363,23 @@ __global__ void __launch_bounds__(kPThreads, 1)
     bool ok = true;
     for (int j = 0; j < n; ++g) {
       const Group gr = group_at(p, b, h, j, n);
+      // columns of each page this row attends: its valid tokens, and with page positions known
+      // (ALiBi, or the RoPE step) only keys at positions m <= pos: column c of a page whose first
+      // token sits at m0 is visible while m0 + c <= pos (cached documents precede every row; the
+      // rows' own document, placed at qpos0, is the causal part)
+      int va = gr.a.valid, vb = gr.size == 2 ? gr.b.valid : 0;
       // ALiBi: the bias of column 0 of each page of the group (log2 units), slope (m - n)
       float cb_a = 0.f, cb_b = 0.f;
-      if (ALIBI) {
+      if (ALIBI || p.causal) {
         const int dp = p.doc_pos[int64_t(b) * p.max_docs + gr.a.slot];
-        cb_a = slope_l2 * static_cast<float>(dp + p.page_start[ps_row + j] - pos);
-        if (gr.size == 2) cb_b = slope_l2 * static_cast<float>(dp + p.page_start[ps_row + j + 1] - pos);
+        const int m0a = dp + p.page_start[ps_row + j];
+        const int m0b = gr.size == 2 ? dp + p.page_start[ps_row + j + 1] : 0;
+        if (ALIBI) {
+          cb_a = slope_l2 * static_cast<float>(m0a - pos);
+          if (gr.size == 2) cb_b = slope_l2 * static_cast<float>(m0b - pos);
+        }
+        va = min(va, max(0, pos - m0a + 1));
+        if (gr.size == 2) vb = min(vb, max(0, pos - m0b + 1));
       }
       j += gr.size;
       if (ALIBI ? g == 0 : gr.a.slot != prev_slot) {
@@ -418,7 +429,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
       // 64).  Two passes over tensor memory keep 32 columns in registers at a time: the row
       // maximum first, then p, the row sum and P (bf16 pairs written over the columns already
       // read: block k's 16 words land on columns 16 k .. 16 k + 15 <= 32 k).
-      const int va = gr.a.valid, vb = gr.size == 2 ? gr.b.valid : 0;
       const bool full = va == 64 && vb == 64;
       const int nblk = 2 * gr.size;
       float mx8[8];

@@ -121,3 +121,59 @@ def test_column_scores_full_context_sampled_heads():
     ref = oracle.column_scores_batch(q, w["k_pool"], w["page_table"], w["seq_len"], w["np_max"] * 64, items=items)
     for it in items:
         _check(S[0, it], ref[0, it], alpha, 32768)
+
+
+def _window_lse(w, q):
+    """Each window row's log-sum-exp over its visible keys, in numpy fp64 from the bf16 inputs,
+    rounded to fp32 as an attention call returns it: [B][alpha][Hq]."""
+    B, alpha, Hq = q.shape[0], q.shape[1], q.shape[2]
+    G = Hq // w["Hk"]
+    out = np.zeros((B, alpha, Hq), np.float32)
+    for b in range(B):
+        n = int(w["seq_len"][b])
+        for hq in range(Hq):
+            K = gen.bf16_to_f32(w["k_pool"][hq // G, w["page_table"][b]]).reshape(-1, 128)[:n].astype(np.float64)
+            Z = gen.bf16_to_f32(q[b, :, hq]).astype(np.float64) @ K.T / np.sqrt(128.0)
+            for j in range(alpha):
+                z = Z[j, :n - alpha + j + 1]
+                m = z.max()
+                out[b, j, hq] = m + np.log(np.exp(z - m).sum())
+    return out
+
+
+@pytest.mark.parametrize("n,alpha,Hq,Hk", [(200, 9, 8, 2), (64 * 7 + 13, 128, 16, 4), (64 * 4 + 7, 129, 8, 2),
+                                           (64 * 6, 300, 8, 2), (5000, 256, 8, 2)])
+def test_column_scores_from_given_lse_vs_oracle(n, alpha, Hq, Hk):
+    """The probability pass alone, from each row's LSE as an attention call would return it (fp32):
+    against the oracle's given-LSE form on the same fp32 LSE, and against the two-pass GPU form."""
+    w = gen.sparse_workload(2, Hq, Hk, n, 4, 4, seed=n + 7 * alpha)
+    q = gen.rows_bf16(n, 326, 2 * alpha * Hq).reshape(2, alpha, Hq, 128)
+    lse = _window_lse(w, q)
+    d = Dev(w)
+    out = torch.full((2, Hq, w["np_max"] * 64), float("nan"), dtype=torch.float32, device=DEV)
+    spkv.attn_column_scores_lse(d.cache, bf(q), torch.from_numpy(lse).to(DEV), d.pt, i32(w["seq_len"]), out)
+    two = torch.full_like(out, float("nan"))
+    spkv.attn_column_scores(d.cache, bf(q), d.pt, i32(w["seq_len"]), two)
+    S, S2 = out.cpu().numpy(), two.cpu().numpy()
+    assert d.errors() == (0, 0)
+    d.close()
+    items = np.array([0, Hq + 3], np.int32) if n > 1000 else None
+    ref = oracle.column_scores_given_lse_batch(q, lse.astype(np.float64), w["k_pool"], w["page_table"],
+                                               w["seq_len"], w["np_max"] * 64, items=items)
+    for it in (items if items is not None else range(2 * Hq)):
+        b, hq = divmod(int(it), Hq)
+        _check(S[b, hq], ref[b, hq], alpha, n)
+    assert np.allclose(S, S2, rtol=1e-4, atol=1e-6)
+
+
+def test_column_scores_lse_argument_checks():
+    w = gen.sparse_workload(1, 8, 2, 256, 4, 4, seed=3)
+    d = Dev(w)
+    q = torch.zeros(1, 8, 8, 128, dtype=torch.bfloat16, device=DEV)
+    out = torch.zeros(1, 8, w["np_max"] * 64, dtype=torch.float32, device=DEV)
+    lib = spkv.load()
+    st = lib.attn_column_scores_lse(d.cache.handle, q.data_ptr(), None, 1, 8, 8, d.pt.data_ptr(), w["np_max"],
+                                    i32(w["seq_len"]).data_ptr(), out.data_ptr(),
+                                    torch.cuda.current_stream().cuda_stream)
+    assert st == -1
+    d.close()

@@ -623,6 +623,145 @@ def test_prefill_rows_are_decode_queries():
         assert np.array_equal(out[:, t], od) and np.array_equal(lse[:, t], ld)
 
 
+# ------------------------------------------------------------------------------ prefill step (causal)
+
+def _step_bruteforce(w, theta, slopes=None):
+    """Independent brute force of the whole prefill step: every listed key gets its absolute
+    position m = doc_pos[slot] + page_start + row; a row at position n attends to the keys with
+    m <= n.  RoPE: complex rotation (keys by doc_pos, since they carry their document-local
+    rotation; the query by n).  ALiBi (slopes given): no rotation, bias -slope (n - m).  scipy
+    softmax / logsumexp over the visible keys."""
+    q = w["q"]
+    B, T, Hq, _ = q.shape
+    Hk = w["Hk"]
+    G = Hq // Hk
+    freq = theta ** (-np.arange(64) / 64.0)
+    cplx = lambda x: x[..., :64] + 1j * x[..., 64:]
+    out, lse = np.zeros((B, T, Hq, 128)), np.zeros((B, T, Hq))
+    for b in range(B):
+        n_p = w["n_pages"][b]
+        for h in range(Hk):
+            ks, vs, mpos, dpos = [], [], [], []
+            for i in range(n_p):
+                v = w["valid"][b, i]
+                ks.append(f(w["k_pool"][h, w["phys"][b, i], :v]))
+                vs.append(f(w["v_pool"][h, w["phys"][b, i], :v]))
+                d = w["doc_pos"][b, w["slot"][b, i]]
+                mpos += [d + w["page_start"][b, i] + r for r in range(v)]
+                dpos += [d] * v
+            K, V = np.concatenate(ks), np.concatenate(vs)
+            mpos, dpos = np.array(mpos, np.float64), np.array(dpos, np.float64)
+            Kc = cplx(K) * np.exp(1j * dpos[:, None] * freq[None, :])
+            for t in range(T):
+                n = w["qpos0"][b] + t
+                vis = mpos <= n
+                for g in range(G):
+                    hq = h * G + g
+                    if slopes is None:
+                        qc = cplx(f(q[b, t, hq])) * np.exp(1j * n * freq)
+                        z = (qc.real @ Kc.real.T + qc.imag @ Kc.imag.T) / math.sqrt(128)
+                    else:
+                        z = K @ f(q[b, t, hq]) / math.sqrt(128) - float(slopes[hq]) * (n - mpos)
+                    out[b, t, hq] = softmax(z[vis]) @ V[vis]
+                    lse[b, t, hq] = logsumexp(z[vis])
+    return out, lse
+
+
+def _step_args(w):
+    return (w["q"], w["k_pool"], w["v_pool"], w["phys"], w["valid"], w["slot"], w["page_start"], w["n_pages"],
+            w["qpos0"], w["doc_pos"])
+
+
+@pytest.mark.parametrize("mode", ["materialised", "lazy"])
+def test_prefill_step_scipy_bruteforce(mode):
+    """Cached documents plus the rows' own keys (T = 70 spans two self pages): the causal mask by
+    absolute position, against the independent brute force."""
+    w = gen.prefill_step(seed=21, B=2, T=70, Hq=4, Hk=2, n_docs=4, docs_per_req=2, min_len=64, max_len=200,
+                         theta=10000.0)
+    out, lse = oracle.prefill_step_batch(*_step_args(w), 10000.0, mode=mode)
+    ro, rl = _step_bruteforce(w, 10000.0)
+    assert np.abs(out - ro).max() < 1e-10 and np.abs(lse - rl).max() < 1e-10
+
+
+def test_prefill_step_without_cached_documents_closed_forms():
+    """Only the rows' own keys: row 0 sees key 0 alone, so its output is V of key 0 and its LSE
+    the single score; a key after row t never changes row t."""
+    w = gen.prefill_step(seed=22, B=2, T=20, Hq=2, Hk=1, theta=500000.0, cached=False)
+    out, lse = oracle.prefill_step_batch(*_step_args(w), 500000.0)
+    for b in range(2):
+        v0 = f(w["v_pool"][0, w["phys"][b, 0], 0])
+        for hq in range(2):
+            assert np.abs(out[b, 0, hq] - v0).max() < 1e-12
+            k0 = f(w["k_pool"][0, w["phys"][b, 0], 0])
+            # row 0 and key 0 both sit at position 0 of the prompt: R(0) on both
+            assert abs(lse[b, 0, hq] - float(f(w["q"][b, 0, hq]) @ k0) / math.sqrt(128)) < 1e-12
+    w2 = dict(w)
+    kp, vp = w["k_pool"].copy(), w["v_pool"].copy()
+    kp[0, w["phys"][0, 0], 11:] = gen.rows_bf16(5, 77, 64 - 11)
+    vp[0, w["phys"][0, 0], 11:] = gen.rows_bf16(5, 78, 64 - 11)
+    w2["k_pool"], w2["v_pool"] = kp, vp
+    out2, lse2 = oracle.prefill_step_batch(*_step_args(w2), 500000.0)
+    assert np.array_equal(out2[0, :11], out[0, :11]) and np.array_equal(lse2[0, :11], lse[0, :11])
+    assert np.abs(out2[0, 11:] - out[0, 11:]).max() > 1e-3
+
+
+def test_prefill_step_equals_cached_prefill_when_nothing_follows_the_rows():
+    """Without the rows' own pages every key precedes every row: the step is the cached-document
+    prefill."""
+    w = gen.prefill_step(seed=23, B=2, T=6, Hq=4, Hk=2, n_docs=5, docs_per_req=2, min_len=64, max_len=300)
+    n_cached = w["n_pages"] - 1
+    args = (w["q"], w["k_pool"], w["v_pool"], w["phys"], w["valid"], w["slot"])
+    o1, l1 = oracle.prefill_step_batch(*args, w["page_start"], n_cached, w["qpos0"], w["doc_pos"], w["theta"])
+    o2, l2 = oracle.lazy_prefill_batch(*args, n_cached, w["qpos0"], w["doc_pos"], w["theta"], materialise=True)
+    assert np.abs(o1 - o2).max() < 1e-12 and np.abs(l1 - l2).max() < 1e-12
+
+
+def _np_bf16(x):
+    """Nearest bf16 (ties to even) of fp64 values, by scaling the significand to 8 bits."""
+    m, e = np.frexp(np.asarray(x, np.float64))
+    return np.ldexp(np.rint(m * 256.0), e - 8)
+
+
+def test_prefill_step_bf16_rotated_query_mode():
+    """Mode lazy_bf16q rounds each document's rotated query to bf16: against a numpy brute force
+    that does the same (numpy RoPE, numpy rounding), and different from the exact lazy form."""
+    w = gen.prefill_step(seed=24, B=1, T=3, Hq=2, Hk=1, n_docs=3, docs_per_req=2, min_len=64, max_len=150,
+                         theta=10000.0)
+    out, lse = oracle.prefill_step_batch(*_step_args(w), 10000.0, mode="lazy_bf16q")
+    exact, _ = oracle.prefill_step_batch(*_step_args(w), 10000.0, mode="lazy")
+    freq = 10000.0 ** (-np.arange(64) / 64.0)
+    n_p = w["n_pages"][0]
+    for t in range(3):
+        n = w["qpos0"][0] + t
+        for hq in range(2):
+            zs, vs = [], []
+            for i in range(n_p):
+                d = w["doc_pos"][0, w["slot"][0, i]]
+                a = (n - d) * freq
+                x = f(w["q"][0, t, hq])
+                qr = np.concatenate([x[:64] * np.cos(a) - x[64:] * np.sin(a), x[64:] * np.cos(a) + x[:64] * np.sin(a)])
+                qr = _np_bf16(qr)
+                for r in range(w["valid"][0, i]):
+                    if d + w["page_start"][0, i] + r > n:
+                        continue
+                    zs.append(qr @ f(w["k_pool"][0, w["phys"][0, i], r]) / math.sqrt(128))
+                    vs.append(f(w["v_pool"][0, w["phys"][0, i], r]))
+            zs = np.array(zs)
+            assert np.abs(out[0, t, hq] - softmax(zs) @ np.array(vs)).max() < 1e-10
+            assert abs(lse[0, t, hq] - logsumexp(zs)) < 1e-10
+    assert np.abs(out - exact).max() > 1e-6          # the rounding is real
+
+
+def test_alibi_step_scipy_bruteforce():
+    """The ALiBi prefill with the rows' own keys listed: causal by position, brute force."""
+    w = gen.prefill_step(seed=25, B=2, T=70, Hq=4, Hk=2, n_docs=4, docs_per_req=2, min_len=64, max_len=200)
+    slopes = np.array([0.01, 0.05, 0.2, 0.0], np.float32)
+    out, lse = oracle.alibi_prefill_batch(w["q"], w["k_pool"], w["v_pool"], w["phys"], w["valid"], w["slot"],
+                                          w["page_start"], w["n_pages"], w["qpos0"], w["doc_pos"], slopes)
+    ro, rl = _step_bruteforce(w, 10000.0, slopes=slopes)
+    assert np.abs(out - ro).max() < 1e-10 and np.abs(lse - rl).max() < 1e-10
+
+
 # ------------------------------------------------------------------------------ ALiBi prefill
 
 def _alibi_args(w):
@@ -772,6 +911,36 @@ def test_column_scores_scipy_bruteforce():
                 pos = n - alpha + j
                 want[:pos + 1] += softmax(Z[j, :pos + 1])
             assert np.allclose(S[b, hq], want, rtol=1e-10, atol=1e-13)
+
+
+def test_column_scores_given_lse_scipy_bruteforce():
+    """The given-LSE form against numpy: with each row's exact log-sum-exp (scipy) it is the
+    softmax column sum; adding c to a row's LSE scales that row's contribution by exp(-c)."""
+    w, q = _colscore_case(4, n=64 * 2 + 45, alpha=13)
+    n, alpha = int(w["seq_len"][0]), q.shape[1]
+    G = w["Hq"] // w["Hk"]
+    lse = np.zeros((w["B"], alpha, w["Hq"]))
+    want = np.zeros((w["B"], w["Hq"], w["np_max"] * 64))
+    shift = np.linspace(-0.7, 1.3, alpha)                 # a different shift per row
+    want_shift = np.zeros_like(want)
+    for b in range(w["B"]):
+        for hq in range(w["Hq"]):
+            h = hq // G
+            K = np.concatenate([f(w["k_pool"][h, w["page_table"][b, p]]) for p in range(w["np_max"])])[:n]
+            Z = f(q[b, :, hq]) @ K.T / math.sqrt(128)
+            for j in range(alpha):
+                pos = n - alpha + j
+                lse[b, j, hq] = logsumexp(Z[j, :pos + 1])
+                p = softmax(Z[j, :pos + 1])
+                want[b, hq, :pos + 1] += p
+                want_shift[b, hq, :pos + 1] += p * math.exp(-shift[j])
+    S = oracle.column_scores_given_lse_batch(q, lse, w["k_pool"], w["page_table"], w["seq_len"], w["np_max"] * 64)
+    assert np.allclose(S, want, rtol=1e-10, atol=1e-13)
+    assert np.allclose(S, oracle.column_scores_batch(q, w["k_pool"], w["page_table"], w["seq_len"],
+                                                     w["np_max"] * 64), rtol=1e-10, atol=1e-13)
+    S2 = oracle.column_scores_given_lse_batch(q, lse + shift[None, :, None], w["k_pool"], w["page_table"],
+                                              w["seq_len"], w["np_max"] * 64)
+    assert np.allclose(S2, want_shift, rtol=1e-10, atol=1e-13)
 
 
 def test_column_scores_invariants():

@@ -571,7 +571,7 @@ def offload_leg(args, dev, stream, timed, cap, peak, cpu_baseline):
     walk = gen.walk_queries(w, 2 * n_iter + max(args.steps, 5) + 1)
     qs = [bf(q) for q in walk]   # eager steps, then graph-captured steps
     # the same workload with its pool resident on the device (the handle over the device pool)
-    resident = resident262k_leg(args, dev, timed, cap, peak, cpu_baseline, w, scache, qs, walk[0])
+    res_leg = resident262k_leg(args, dev, timed, cap, peak, cpu_baseline, w, scache, qs, walk[0])
     ev = torch.from_numpy(w["evict"].astype(np.float32)).to(dev)
     scores = torch.empty(B, Hk, npm, dtype=torch.float32, device=dev)
     alive = torch.full((B, Hk, (npm + 31) // 32), -1, dtype=torch.int32, device=dev)
@@ -698,7 +698,7 @@ def offload_leg(args, dev, stream, timed, cap, peak, cpu_baseline):
     }
     del dk, dv, dks, k_slots, v_slots, k_host, v_host
     torch.cuda.empty_cache()
-    return out_d, resident
+    return out_d, res_leg
 
 
 def run_native(args):
@@ -1075,9 +1075,9 @@ def run_native(args):
         del ck, cq, cs, csl, lse_in
 
     # ---- offload: the 262k-context workload with its K/V pool in pinned host memory
-    offload, resident = None, None
+    offload, resident262k = None, None
     if not args.no_offload and rank == 0:
-        offload, resident = offload_leg(args, dev, stream, timed, cap, peak, cpu_on)
+        offload, resident262k = offload_leg(args, dev, stream, timed, cap, peak, cpu_on)
 
     # ---- the other workloads of the per-config report
     tiny, traj = None, None
@@ -1201,7 +1201,7 @@ def run_native(args):
                               "lazy_rope_decode_attn_frac": lazy["frac"] if lazy else None,
                               "cpu_baseline": cpu},
                 "3_lazy_rag": rag,
-                "4_long262k_resident": resident,
+                "4_long262k_resident": resident262k,
                 "5_nosa_traj": traj,
             },
             "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,

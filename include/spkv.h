@@ -19,6 +19,8 @@
  *   lazy_alibi_prefill_attn  the prefill step for models with ALiBi position biases
  *   attn_column_scores   PyramidKV-style key scores of a prompt's last rows (tcgen05)
  *   attn_column_scores_lse  the same from row log-sum-exps the attention already produced
+ *   score_blocks_dir, sparse_decode_attn_dir, retrieve_pages_dir  the same calls through a
+ *                        two-level page directory (spkv_pagemap_* manages one)
  *
  * Sources (web pages, cited by title and section):
  *   [NOSA] "NOSA: Native and Offloadable Sparse Attention", sections "Method 1: the NOSA
@@ -431,7 +433,90 @@ int sparse_decode_attn_noalloc(const void* k_pool, const void* v_pool, int n_kv_
 int spkv_pack_page_words(const int32_t* phys, const int32_t* valid, const int32_t* doc_slot,
                          int64_t n, uint32_t* words);
 
-/* Waits for `stream`, then reads and clears the handle's device error word into *bits.
+/* ---------------------------------------------------------------------------------------------
+ * Two-level page directory ([Spin] "Unifying Sparse Attention with Hierarchical Memory for
+ * Scalable Long-Context LLM Serving", section 2C "Hierarchical metadata management": a small
+ * GPU-resident top-level directory points to second-level segments that are allocated on demand in
+ * CPU memory, so metadata grows with the pages actually in use rather than with the logical address
+ * space; latency-critical metadata stays on the GPU, bulk metadata moves to the CPU).
+ *
+ * The logical-to-physical page table of a request is split into segments of 2^seg_shift page ids.
+ * Directory entry e = dir[b][p >> seg_shift] locates the segment holding logical page p:
+ *   e >= 0   device tier: segment e of dev_segs (the GPU-resident cache of hot segments)
+ *   e <= -2  host tier: host segment h = -2 - e, in pinned host memory read in place by the kernels
+ *            (over NVLink-C2C on GB300): chunk h >> chunk_shift of host_chunks, segment
+ *            h & (2^chunk_shift - 1) of that chunk
+ *   e == -1  unmapped: no page of that range exists (a lookup there reports SPKV_DEVERR_PHYS)
+ * and the physical page is entry p & (2^seg_shift - 1) of that segment.  A lookup gives exactly the
+ * page a flat page_table[b][p] with the same contents gives, so the *_dir calls below return
+ * bit for bit what their flat-table forms return.  (spkv_pagemap_* builds and maintains one.) */
+typedef struct {
+  const int32_t* dir;                 /* device int32 [B][n_dir] */
+  const int32_t* dev_segs;            /* device int32 [n_dev_segs][2^seg_shift] */
+  const int32_t* const* host_chunks;  /* device array of the device addresses of pinned, mapped host
+                                         chunks, each int32 [2^chunk_shift][2^seg_shift] */
+  int32_t n_dir;                      /* directory entries per request (>= ceil(np_max / 2^seg_shift)) */
+  int32_t seg_shift;                  /* 4 .. 12 */
+  int32_t n_dev_segs;
+  int32_t chunk_shift;                /* 0 .. 16 */
+  int64_t n_host_segs;
+} spkv_page_dir;
+
+/* score_blocks with the page table given as a two-level directory (contents as above; np_max still
+ * bounds the logical pages).  Every other argument, result and error: as score_blocks. */
+int score_blocks_dir(spkv_cache_t cache, const void* q, int B, int Hq, const spkv_page_dir* dir, int np_max,
+                     const int32_t* seq_len, float* scores, void* stream);
+
+/* sparse_decode_attn with the page table given as a two-level directory. */
+int sparse_decode_attn_dir(spkv_cache_t cache, const void* q, int B, int Hq, const spkv_page_dir* dir, int np_max,
+                           const int32_t* sel, const int32_t* n_sel, int sel_stride, const int32_t* seq_len,
+                           float* out, float* lse, void* stream);
+
+/* retrieve_pages with the (host-page) table given as a two-level directory. */
+int retrieve_pages_dir(spkv_cache_t cache, const void* k_host, const void* v_host, int64_t n_host_pages,
+                       const spkv_page_dir* dir, int np_max, int B, const int32_t* missing,
+                       const int32_t* n_missing, const int32_t* victims, int32_t* slot, const int32_t* n_sel,
+                       int sel_stride, int n_slots, void* stream);
+
+/* A page-directory manager (host side, [Spin] 2C).  It owns the device directory, a device cache of
+ * n_dev_segs hot segments and the host segments, which it allocates on demand (pinned, mapped host
+ * memory, 2^chunk_shift segments per allocation) the first time a page of their range is mapped.
+ * spkv_pagemap_map and spkv_pagemap_promote change the host state at once; spkv_pagemap_sync
+ * enqueues on `stream` the copies that bring the device directory and the device-tier segments up to
+ * date and waits for them.  Host-tier segments are read in place by the kernels, so map only pages
+ * that no enqueued, unfinished kernel reads (for example between decode steps).  One thread at a time
+ * per manager.  Errors: SPKV_EINVAL for bad arguments, SPKV_ENOMEM when an allocation fails,
+ * SPKV_ECUDA for a failed copy. */
+typedef struct spkv_pagemap* spkv_pagemap_t;
+
+/* B requests of up to np_max logical pages, segments of 2^seg_shift ids (4 .. 12), n_dev_segs >= 0
+ * device-tier slots.  Allocates the device directory (all entries unmapped) and the device slots. */
+int spkv_pagemap_create(int B, int np_max, int seg_shift, int n_dev_segs, spkv_pagemap_t* out);
+
+/* Logical pages [first_page, first_page + n) of request b get the physical ids phys[0 .. n) (host
+ * int32; -1 unmaps a page).  Host segments of the range are allocated on demand. */
+int spkv_pagemap_map(spkv_pagemap_t pm, int b, int first_page, int n, const int32_t* phys);
+
+/* Moves the segment of request b that holds logical page `page` to the device tier: a free device
+ * slot, else the slot promoted longest ago, whose segment returns to the host tier.  The segment
+ * must be mapped (SPKV_EINVAL otherwise); promoting a device-tier segment renews it. */
+int spkv_pagemap_promote(spkv_pagemap_t pm, int b, int page);
+
+/* Brings the device directory and the device-tier segments up to date (copies on `stream`, then
+ * waits for the stream). */
+int spkv_pagemap_sync(spkv_pagemap_t pm, void* stream);
+
+/* The directory view that the *_dir calls take (valid until the next map / promote / sync). */
+int spkv_pagemap_view(spkv_pagemap_t pm, spkv_page_dir* out);
+
+/* Metadata bytes: on the device (directory, device-tier slots, chunk table) and in host memory
+ * (allocated host segments). */
+int spkv_pagemap_bytes(spkv_pagemap_t pm, int64_t* device_bytes, int64_t* host_bytes);
+
+/* Frees everything the manager allocated (the caller ensures no kernel still reads it). */
+int spkv_pagemap_destroy(spkv_pagemap_t pm);
+
+/* Waits for `stream`, then reads and clears the handle's device error word into *bits./* Waits for `stream`, then reads and clears the handle's device error word into *bits.
  * Returns SPKV_OK when it was zero, SPKV_EDEVICE otherwise (SPKV_ECUDA if the wait failed). */
 int spkv_get_device_error(spkv_cache_t cache, void* stream, uint32_t* bits);
 

@@ -72,6 +72,7 @@ def _l():
                                          vp, i32, vp, vp, i32, vp, vp, i32], None),
             "orc_column_scores_batch": ([i32, i32, i32, i32, vp, vp, i64, vp, i32, vp, i32, vp, i32, vp, i32],
                                         None),
+            "orc_dir_to_table": ([i32, i32, vp, i32, i32, vp, i32, vp, i64, vp], None),
             "orc_prefill_step_batch": ([i32, i32, i32, i32, vp, vp, vp, i64, vp, vp, vp, vp, i32, vp, i32, vp, vp,
                                         i32, f64, i32, vp, i32, vp, vp, i32], None),
             "orc_column_scores_given_lse_batch": ([i32, i32, i32, i32, vp, vp, vp, i64, vp, i32, vp, i32, vp, i32,
@@ -445,3 +446,18 @@ def column_scores_given_lse_batch(q, lse, k_pool, page_table, seq_len, n_out: in
                                            page_table.shape[1], _p(seq_len), int(n_out), _p(it), it.shape[0],
                                            _p(S), nthreads)
     return S
+
+
+def dir_to_table(dir_, shift: int, dev_segs, host_segs, np_max: int):
+    """The flat page table [B][np_max] a two-level directory describes: dir_ [B][n_dir] (entries
+    >= 0 device segment, <= -2 host segment -2 - e, -1 unmapped), dev_segs [n_dev][2^shift],
+    host_segs [n_host][2^shift]."""
+    dir_ = _c(dir_, np.int32)
+    seg = 1 << shift
+    dev_segs = _c(np.asarray(dev_segs).reshape(-1, seg), np.int32)
+    host_segs = _c(np.asarray(host_segs).reshape(-1, seg), np.int32)
+    B, n_dir = dir_.shape
+    out = np.zeros((B, np_max), np.int32)
+    _l().orc_dir_to_table(B, int(np_max), _p(dir_), n_dir, int(shift), _p(dev_segs), dev_segs.shape[0],
+                          _p(host_segs), host_segs.shape[0], _p(out))
+    return out

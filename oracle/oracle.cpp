@@ -432,6 +432,30 @@ void orc_retrieve_unit(const uint16_t* khost, const uint16_t* vhost, const int32
     if (slot[i] < 0) slot[i] = victims[j++];
 }
 
+// ---------------------------------------------------------------- two-level page directory
+// [Spin] 2C "Hierarchical metadata management": the page table of a request is split into
+// segments of 2^shift page ids; a directory entry per segment says where that segment lives:
+// e >= 0 the device tier (segment e of dev_segs), e <= -2 the host tier (segment -2 - e of
+// host_segs), e == -1 nowhere (every page of the range unmapped).  Logical page p of request b is
+// entry p mod 2^shift of the segment named by dir[b][p / 2^shift]; -1 when unmapped or when the
+// entry names a segment that does not exist.  Writes the flat table [B][np_max].
+void orc_dir_to_table(int B, int np_max, const int32_t* dir, int n_dir, int shift, const int32_t* dev_segs,
+                      int n_dev, const int32_t* host_segs, int64_t n_host, int32_t* table) {
+  const int seg = 1 << shift;
+  for (int b = 0; b < B; ++b)
+    for (int p = 0; p < np_max; ++p) {
+      int32_t v = -1;
+      const int s = p / seg;
+      if (s < n_dir) {
+        const int32_t e = dir[static_cast<int64_t>(b) * n_dir + s];
+        if (e >= 0 && e < n_dev) v = dev_segs[static_cast<int64_t>(e) * seg + p % seg];
+        if (e <= -2 && -static_cast<int64_t>(e) - 2 < n_host)
+          v = host_segs[(-static_cast<int64_t>(e) - 2) * seg + p % seg];
+      }
+      table[static_cast<int64_t>(b) * np_max + p] = v;
+    }
+}
+
 // ---------------------------------------------------------------- batch drivers
 // The same functions applied to a list of (request, kv head) units, one unit per task on a
 // pool of `nthreads` threads (0 = all hardware threads).  Unit u = b * Hk + h.  Pools are

@@ -27,7 +27,7 @@ import ctypes
 import numpy as np
 import torch
 
-from ._abi import DEVERR, SpkvDesc, SpkvError, check, load
+from ._abi import DEVERR, SpkvDesc, SpkvError, SpkvPageDir, check, load
 
 __all__ = ["PagedKVCache", "paged_kv_create", "paged_kv_append", "score_blocks", "decode_append_score",
            "select_topk",
@@ -36,6 +36,7 @@ __all__ = ["PagedKVCache", "paged_kv_create", "paged_kv_append", "score_blocks",
            "lazy_rope_prefill_step",
            "attn_column_scores", "attn_column_scores_lse", "lazy_alibi_prefill_attn",
            "sparse_decode_attn_noalloc", "pack_page_words", "get_device_error", "SpkvError", "DEVERR",
+           "PageMap", "score_blocks_dir", "sparse_decode_attn_dir", "retrieve_pages_dir",
            "load"]
 
 HEAD_DIM, PAGE, SUBBLOCK = 128, 64, 16
@@ -420,6 +421,97 @@ def select_resident_update(cache: PagedKVCache, q_scores, evict_scores, alive, s
         int(bucket_width), _t(missing, torch.int32, "missing"), _t(n_missing, torch.int32, "n_missing"),
         _t(slot, torch.int32, "slot"), _t(victims, torch.int32, "victims"), _t(hist, torch.int32, "hist"),
         _stream(stream)))
+
+
+class PageMap:
+    """A two-level page directory ([Spin] 2C) managed by the library: a GPU directory of segments of
+    2^seg_shift page ids, host segments allocated on demand in pinned memory, and n_dev_segs device
+    slots for hot segments.  ``map`` and ``promote`` change the host state; ``sync`` brings the device
+    up to date (and waits for the stream).  Pass the PageMap to the *_dir calls."""
+
+    def __init__(self, B: int, np_max: int, seg_shift: int = 8, n_dev_segs: int = 0):
+        h = ctypes.c_void_p()
+        check("spkv_pagemap_create", load().spkv_pagemap_create(int(B), int(np_max), int(seg_shift),
+                                                                int(n_dev_segs), ctypes.byref(h)))
+        self.handle, self.B, self.np_max, self.seg_shift = h, B, np_max, seg_shift
+
+    def map(self, b: int, first_page: int, phys) -> None:
+        """Logical pages first_page .. of request b get the ids in phys (host int32; -1 unmaps)."""
+        phys = np.ascontiguousarray(phys, np.int32)
+        check("spkv_pagemap_map", load().spkv_pagemap_map(self.handle, int(b), int(first_page), phys.size,
+                                                          phys.ctypes.data))
+
+    def promote(self, b: int, page: int) -> None:
+        check("spkv_pagemap_promote", load().spkv_pagemap_promote(self.handle, int(b), int(page)))
+
+    def sync(self, stream=None) -> None:
+        check("spkv_pagemap_sync", load().spkv_pagemap_sync(self.handle, _stream(stream)))
+
+    def view(self) -> SpkvPageDir:
+        v = SpkvPageDir()
+        check("spkv_pagemap_view", load().spkv_pagemap_view(self.handle, ctypes.byref(v)))
+        return v
+
+    def nbytes(self):
+        """(device bytes, host bytes) of the directory's metadata."""
+        d, h = ctypes.c_int64(), ctypes.c_int64()
+        check("spkv_pagemap_bytes", load().spkv_pagemap_bytes(self.handle, ctypes.byref(d), ctypes.byref(h)))
+        return int(d.value), int(h.value)
+
+    def close(self):
+        if self.handle:
+            torch.cuda.synchronize()
+            check("spkv_pagemap_destroy", load().spkv_pagemap_destroy(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            if self.handle:
+                load().spkv_pagemap_destroy(self.handle)
+                self.handle = None
+        except Exception:
+            pass
+
+
+def score_blocks_dir(cache: PagedKVCache, q, pagemap: PageMap, seq_len, scores, stream=None):
+    """score_blocks with the page table given by a PageMap."""
+    B, Hq = q.shape[0], q.shape[1]
+    v = pagemap.view()
+    np_max = pagemap.np_max
+    check("score_blocks_dir", load().score_blocks_dir(
+        cache.handle, _t(q, torch.bfloat16, "q", (B, Hq, HEAD_DIM)), B, Hq, ctypes.byref(v), np_max,
+        _t(seq_len, torch.int32, "seq_len", (B,)),
+        _t(scores, torch.float32, "scores", (B, cache.n_kv_heads, np_max)), _stream(stream)))
+
+
+def sparse_decode_attn_dir(cache: PagedKVCache, q, pagemap: PageMap, sel, n_sel, seq_len, out, lse, stream=None):
+    """sparse_decode_attn with the page table given by a PageMap."""
+    B, Hq = q.shape[0], q.shape[1]
+    stride = sel.shape[2]
+    v = pagemap.view()
+    check("sparse_decode_attn_dir", load().sparse_decode_attn_dir(
+        cache.handle, _t(q, torch.bfloat16, "q", (B, Hq, HEAD_DIM)), B, Hq, ctypes.byref(v), pagemap.np_max,
+        _t(sel, torch.int32, "sel", (B, cache.n_kv_heads, stride)),
+        _t(n_sel, torch.int32, "n_sel", (B, cache.n_kv_heads)), stride,
+        _t(seq_len, torch.int32, "seq_len", (B,)), _t(out, torch.float32, "out", (B, Hq, HEAD_DIM)),
+        _t(lse, torch.float32, "lse", (B, Hq)), _stream(stream)))
+
+
+def retrieve_pages_dir(cache: PagedKVCache, k_host, v_host, pagemap: PageMap, missing, n_missing, victims, slot,
+                       n_sel, n_slots: int, stream=None):
+    """retrieve_pages with the host-page table given by a PageMap."""
+    Hk = cache.n_kv_heads
+    n_host = k_host.shape[1]
+    hshp = (Hk, n_host, PAGE, HEAD_DIM)
+    B = pagemap.B
+    stride = slot.shape[-1]
+    v = pagemap.view()
+    check("retrieve_pages_dir", load().retrieve_pages_dir(
+        cache.handle, _host(k_host, torch.bfloat16, "k_host", hshp),
+        _host(v_host, torch.bfloat16, "v_host", hshp), n_host, ctypes.byref(v), pagemap.np_max, B,
+        _t(missing, torch.int32, "missing"), _t(n_missing, torch.int32, "n_missing"),
+        _t(victims, torch.int32, "victims"), _t(slot, torch.int32, "slot"),
+        _t(n_sel, torch.int32, "n_sel"), stride, int(n_slots), _stream(stream)))
 
 
 def pack_page_words(phys, valid, doc_slot) -> np.ndarray:

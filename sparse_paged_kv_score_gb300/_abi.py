@@ -26,6 +26,14 @@ class SpkvDesc(ctypes.Structure):
                 ("ksum", _vp), ("page_cnt", _vp), ("max_units", ctypes.c_int32), ("ksum_bf16", ctypes.c_int32)]
 
 
+class SpkvPageDir(ctypes.Structure):
+    _fields_ = [("dir", _vp), ("dev_segs", _vp), ("host_chunks", _vp), ("n_dir", ctypes.c_int32),
+                ("seg_shift", ctypes.c_int32), ("n_dev_segs", ctypes.c_int32), ("chunk_shift", ctypes.c_int32),
+                ("n_host_segs", ctypes.c_int64)]
+
+
+_pd = ctypes.POINTER(SpkvPageDir)
+
 SIGNATURES = {
     "paged_kv_create": ([ctypes.POINTER(SpkvDesc), _vp, ctypes.POINTER(_vp)], _i32),
     "paged_kv_append": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp], _i32),
@@ -53,6 +61,16 @@ SIGNATURES = {
     "sparse_decode_attn_noalloc": ([_vp, _vp, _i32, _i64, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _i32,
                                     _vp, _vp, _vp, _vp, _vp], _i32),
     "spkv_pack_page_words": ([_vp, _vp, _vp, _i64, _vp], _i32),
+    "score_blocks_dir": ([_vp, _vp, _i32, _i32, _pd, _i32, _vp, _vp, _vp], _i32),
+    "sparse_decode_attn_dir": ([_vp, _vp, _i32, _i32, _pd, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _vp], _i32),
+    "retrieve_pages_dir": ([_vp, _vp, _vp, _i64, _pd, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp], _i32),
+    "spkv_pagemap_create": ([_i32, _i32, _i32, _i32, ctypes.POINTER(_vp)], _i32),
+    "spkv_pagemap_map": ([_vp, _i32, _i32, _i32, _vp], _i32),
+    "spkv_pagemap_promote": ([_vp, _i32, _i32], _i32),
+    "spkv_pagemap_sync": ([_vp, _vp], _i32),
+    "spkv_pagemap_view": ([_vp, _pd], _i32),
+    "spkv_pagemap_bytes": ([_vp, ctypes.POINTER(_i64), ctypes.POINTER(_i64)], _i32),
+    "spkv_pagemap_destroy": ([_vp], _i32),
     "spkv_get_device_error": ([_vp, _vp, ctypes.POINTER(_u32)], _i32),
     "paged_kv_destroy": ([_vp], _i32),
     "spkv_sm_count": ([_vp], _i32),

@@ -479,13 +479,14 @@ int lru_bucket_update(spkv_cache_t c, int32_t* resident, int32_t* ts, int n_slot
                                     n_units, t_now, bucket_width, victims, hist, as_stream(stream)));
 }
 
-int retrieve_pages(spkv_cache_t c, const void* k_host, const void* v_host, int64_t n_host_pages,
-                   const int32_t* page_table, int np_max, int B, const int32_t* missing, const int32_t* n_missing,
-                   const int32_t* victims, int32_t* slot, const int32_t* n_sel, int sel_stride, int n_slots,
-                   void* stream) {
+static int retrieve_common(spkv_cache_t c, const void* k_host, const void* v_host, int64_t n_host_pages,
+                           const int32_t* page_table, const spkv::PageDir* pd, int np_max, int B,
+                           const int32_t* missing, const int32_t* n_missing, const int32_t* victims, int32_t* slot,
+                           const int32_t* n_sel, int sel_stride, int n_slots, void* stream) {
   if (!c || B < 0) return SPKV_EINVAL;
   if (B == 0) return SPKV_OK;
-  if (!k_host || !v_host || !page_table || !missing || !n_missing || !victims || !slot || !n_sel) return SPKV_EINVAL;
+  if (!k_host || !v_host || (!page_table && !pd) || !missing || !n_missing || !victims || !slot || !n_sel)
+    return SPKV_EINVAL;
   if (!aligned(k_host, 16) || !aligned(v_host, 16)) return SPKV_EINVAL;
   if (n_host_pages <= 0 || np_max <= 0 || sel_stride <= 0 || sel_stride > 4096 || n_slots <= 0) return SPKV_EINVAL;
   if (int64_t(B) * c->d.n_kv_heads > c->max_units) return SPKV_EINVAL;
@@ -506,7 +507,16 @@ int retrieve_pages(spkv_cache_t c, const void* k_host, const void* v_host, int64
     c->host_v_dev = dv;
   }
   return status_of(spkv::launch_retrieve(c, c->host_k_dev, c->host_v_dev, n_host_pages, page_table, np_max, B, missing, n_missing,
-                                         victims, slot, n_sel, sel_stride, n_slots, as_stream(stream)));
+                                         victims, slot, n_sel, sel_stride, n_slots, as_stream(stream), pd));
+}
+
+int retrieve_pages(spkv_cache_t c, const void* k_host, const void* v_host, int64_t n_host_pages,
+                   const int32_t* page_table, int np_max, int B, const int32_t* missing, const int32_t* n_missing,
+                   const int32_t* victims, int32_t* slot, const int32_t* n_sel, int sel_stride, int n_slots,
+                   void* stream) {
+  if (!page_table) return SPKV_EINVAL;
+  return retrieve_common(c, k_host, v_host, n_host_pages, page_table, nullptr, np_max, B, missing, n_missing, victims,
+                         slot, n_sel, sel_stride, n_slots, stream);
 }
 
 int select_resident_update(spkv_cache_t c, const float* q_scores, const float* evict_scores, uint32_t* alive, int B,
@@ -538,6 +548,70 @@ int select_resident_update(spkv_cache_t c, const float* q_scores, const float* e
     e = spkv::launch_lru(c->dev_err, resident, ts, n_slots, slot, n_sel, missing, n_missing, stride,
                          static_cast<int>(U), t_now, bucket_width, victims, hist, st);
   return status_of(e);
+}
+
+// Checks a directory description and converts it to the kernels' view.
+static int dir_view(const spkv_page_dir* d, int np_max, spkv::PageDir* out) {
+  if (!d || !d->dir || d->seg_shift < 4 || d->seg_shift > 12 || d->chunk_shift < 0 || d->chunk_shift > 16 ||
+      d->n_dev_segs < 0 || d->n_host_segs < 0 || (d->n_dev_segs > 0 && !d->dev_segs) ||
+      (d->n_host_segs > 0 && !d->host_chunks))
+    return SPKV_EINVAL;
+  if (int64_t(d->n_dir) << d->seg_shift < np_max) return SPKV_EINVAL;   // the directory must cover np_max pages
+  out->dir = d->dir;
+  out->dev = d->dev_segs;
+  out->chunks = d->host_chunks;
+  out->n_dir = d->n_dir;
+  out->shift = d->seg_shift;
+  out->n_dev = d->n_dev_segs;
+  out->chunk_shift = d->chunk_shift;
+  out->n_host = d->n_host_segs;
+  return SPKV_OK;
+}
+
+int score_blocks_dir(spkv_cache_t c, const void* q, int B, int Hq, const spkv_page_dir* dir, int np_max,
+                     const int32_t* seq_len, float* scores, void* stream) {
+  int st = check_group(c, B, Hq);
+  if (st != SPKV_OK) return st;
+  if (!c->d.ksum) return SPKV_EINVAL;
+  if (B == 0) return SPKV_OK;
+  if (!q || !seq_len || !scores || np_max <= 0 || !aligned(q, 8)) return SPKV_EINVAL;
+  spkv::PageDir pd;
+  if ((st = dir_view(dir, np_max, &pd)) != SPKV_OK) return st;
+  return status_of(spkv::launch_score(c, q, B, Hq, nullptr, np_max, seq_len, scores, as_stream(stream), nullptr,
+                                      nullptr, &pd));
+}
+
+int sparse_decode_attn_dir(spkv_cache_t c, const void* q, int B, int Hq, const spkv_page_dir* dir, int np_max,
+                           const int32_t* sel, const int32_t* n_sel, int sel_stride, const int32_t* seq_len,
+                           float* out, float* lse, void* stream) {
+  int st = check_group(c, B, Hq);
+  if (st != SPKV_OK) return st;
+  if (B == 0) return SPKV_OK;
+  if (!q || !sel || !n_sel || !seq_len || !out || !lse || np_max <= 0 || sel_stride <= 0 || !aligned(q, 16))
+    return SPKV_EINVAL;
+  AttnParams p;
+  fill_common(p, c, q, B, Hq, out, lse);
+  if ((st = dir_view(dir, np_max, &p.pd)) != SPKV_OK) return st;
+  p.np_max = np_max;
+  p.sel = sel;
+  p.n_sel = n_sel;
+  p.sel_stride = sel_stride;
+  p.seq_len = seq_len;
+  p.min_chunk = (sel_stride + 125) / 126;
+  const int64_t t_max = int64_t(B) * c->d.n_kv_heads * sel_stride;
+  const int grid = static_cast<int>(t_max < c->attn_grid ? t_max : c->attn_grid);
+  return status_of(spkv::launch_attn(c, p, false, grid, as_stream(stream)));
+}
+
+int retrieve_pages_dir(spkv_cache_t c, const void* k_host, const void* v_host, int64_t n_host_pages,
+                       const spkv_page_dir* dir, int np_max, int B, const int32_t* missing, const int32_t* n_missing,
+                       const int32_t* victims, int32_t* slot, const int32_t* n_sel, int sel_stride, int n_slots,
+                       void* stream) {
+  spkv::PageDir pd;
+  const int st = dir_view(dir, np_max, &pd);
+  if (st != SPKV_OK) return st;
+  return retrieve_common(c, k_host, v_host, n_host_pages, nullptr, &pd, np_max, B, missing, n_missing, victims, slot,
+                         n_sel, sel_stride, n_slots, stream);
 }
 
 int spkv_pack_page_words(const int32_t* phys, const int32_t* valid, const int32_t* doc_slot, int64_t n,

@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ph = sl >= 0 && sl < p.n_slots ? b * p.n_slots + sl : -1;
                 if (ph < 0) bad |= SPKV_DEVERR_SLOT;
               } else {
-                ph = p.page_table[int64_t(b) * p.np_max + lp];
+                ph = page_lookup(p.page_table, p.np_max, p.pd, b, lp);
               }
               if (v <= 0) bad |= SPKV_DEVERR_PAGE_ID;
               else if (ph < 0 || ph >= p.n_phys) bad |= SPKV_DEVERR_PHYS;

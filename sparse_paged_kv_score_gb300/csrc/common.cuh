@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include "../../include/spkv.h"
+#include "internal.h"
 
 namespace spkv {
 
@@ -216,6 +217,25 @@ __device__ __forceinline__ void warp_hist_add(int* hist, int bin, bool take) {
 
 __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bits) {
   if (bits) atomicOr(err, bits);
+}
+
+// Physical page of logical page p (0 <= p < np_max) of request b: page_table[b][p], or through the
+// two-level directory when pd.dir is set ([Spin] 2C): the directory entry of p's segment names a
+// device-tier segment (>= 0), a host-tier segment (<= -2, read in place from pinned host memory)
+// or nothing (-1); the page id is the segment's entry p mod 2^shift.  -1 when unmapped or when an
+// entry is out of range (callers report SPKV_DEVERR_PHYS for any id outside the pool).
+__device__ __forceinline__ int page_lookup(const int32_t* page_table, int np_max, const PageDir& pd, int b, int p) {
+  if (!pd.dir) return page_table[int64_t(b) * np_max + p];
+  const int s = p >> pd.shift;
+  if (s >= pd.n_dir) return -1;
+  const int e = pd.dir[int64_t(b) * pd.n_dir + s];
+  const int64_t o = p & ((1 << pd.shift) - 1);
+  if (e >= 0) return e < pd.n_dev ? pd.dev[(int64_t(e) << pd.shift) + o] : -1;
+  if (e == -1) return -1;
+  const int64_t h = -int64_t(e) - 2;
+  if (h >= pd.n_host) return -1;
+  const int32_t* chunk = pd.chunks[h >> pd.chunk_shift];
+  return chunk[((h & ((int64_t(1) << pd.chunk_shift) - 1)) << pd.shift) + o];
 }
 
 }  // namespace spkv

@@ -33,6 +33,16 @@ struct spkv_cache {
 
 namespace spkv {
 
+// Device view of a two-level page directory (spkv_page_dir); dir == nullptr means the call uses a
+// flat page table instead.
+struct PageDir {
+  const int32_t* dir;            // [B][n_dir]: >= 0 device segment, <= -2 host segment -2 - e, -1 unmapped
+  const int32_t* dev;            // device-tier segments [n_dev][1 << shift]
+  const int32_t* const* chunks;  // device addresses of the host chunks, each [1 << chunk_shift][1 << shift]
+  int n_dir, shift, n_dev, chunk_shift;
+  int64_t n_host;
+};
+
 // Launches `k` with programmatic stream serialisation: the kernel may start while the previous
 // kernel of the stream finishes; every kernel of this library calls pdl_wait() before it reads
 // anything an earlier kernel wrote.
@@ -78,6 +88,7 @@ struct AttnParams {
   const int32_t* n_sel;
   int sel_stride;
   const int32_t* seq_len;
+  PageDir pd;                    // two-level page directory (pd.dir null: page_table)
   const int32_t* slot;           // resident-slot form: slot of each selected page (else null)
   int n_slots;                   // slots per (request, kv head); page = b * n_slots + slot
   // lazy form
@@ -148,7 +159,7 @@ struct AppendRows {
 // k_new == nullptr: scores only; else the decode append of each request's new row is fused in.
 cudaError_t launch_score(const spkv_cache* c, const void* q, int B, int Hq, const int32_t* page_table,
                          int np_max, const int32_t* seq_len, float* scores, cudaStream_t st,
-                         const void* k_new = nullptr, const void* v_new = nullptr);
+                         const void* k_new = nullptr, const void* v_new = nullptr, const PageDir* pd = nullptr);
 cudaError_t launch_select(const spkv_cache* c, const float* qs, const float* es, uint32_t* alive, int B,
                           int np_max, const int32_t* seq_len, int k_q, int k_e, int32_t* sel, int32_t* n_sel,
                           cudaStream_t st);
@@ -159,7 +170,7 @@ cudaError_t launch_setdiff(uint32_t* err, const int32_t* resident, int n_slots, 
 cudaError_t launch_retrieve(const spkv_cache* c, const void* k_host, const void* v_host, int64_t n_host_pages,
                             const int32_t* page_table, int np_max, int B, const int32_t* missing,
                             const int32_t* n_missing, const int32_t* victims, int32_t* slot, const int32_t* n_sel,
-                            int sel_stride, int n_slots, cudaStream_t st);
+                            int sel_stride, int n_slots, cudaStream_t st, const PageDir* pd = nullptr);
 cudaError_t launch_lru(uint32_t* err, int32_t* resident, int32_t* ts, int n_slots, const int32_t* slot,
                        const int32_t* n_sel, const int32_t* missing, const int32_t* n_missing, int sel_stride,
                        int n_units, int32_t t_now, int bucket_width, int32_t* victims, int32_t* hist,

@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(kRtThreads)
                     const int32_t* __restrict__ n_missing, const int32_t* __restrict__ victims,
                     int32_t* __restrict__ slot, const int32_t* __restrict__ n_sel, int stride, int n_units,
                     uint4* __restrict__ k_slots, uint4* __restrict__ v_slots, int64_t n_slot_pages, int n_slots,
-                    uint32_t* err) {
+                    uint32_t* err, PageDir pd) {
   __shared__ int prefix[kMaxUnits + 1];
   __shared__ int warp_tot[kRtThreads / 32];
   pdl_wait();
@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kRtThreads)
     int64_t hp = -1;
     if (lp < 0 || lp >= np_max) bad |= SPKV_DEVERR_PAGE_ID;
     else {
-      hp = page_table[int64_t(b) * np_max + lp];
+      hp = page_lookup(page_table, np_max, pd, b, lp);
       if (hp < 0 || hp >= n_host) bad |= SPKV_DEVERR_PHYS;
     }
     if (vs < 0 || vs >= n_slots) bad |= SPKV_DEVERR_SLOT;
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kRtThreads)
 cudaError_t launch_retrieve(const spkv_cache* c, const void* k_host, const void* v_host, int64_t n_host_pages,
                             const int32_t* page_table, int np_max, int B, const int32_t* missing,
                             const int32_t* n_missing, const int32_t* victims, int32_t* slot, const int32_t* n_sel,
-                            int sel_stride, int n_slots, cudaStream_t st) {
+                            int sel_stride, int n_slots, cudaStream_t st, const PageDir* pd) {
   const int Hk = c->d.n_kv_heads;
   const int n_units = B * Hk;
   const int64_t items = int64_t(n_units) * sel_stride;
@@ -140,7 +140,7 @@ cudaError_t launch_retrieve(const spkv_cache* c, const void* k_host, const void*
   return launch_pdl(retrieve_kernel, dim3(grid), dim3(kRtThreads), 0, st, static_cast<const uint4*>(k_host),
                     static_cast<const uint4*>(v_host), n_host_pages, Hk, page_table, np_max, missing, n_missing,
                     victims, slot, n_sel, sel_stride, n_units, static_cast<uint4*>(c->d.k_pool),
-                    static_cast<uint4*>(c->d.v_pool), c->d.n_phys_pages, n_slots, c->dev_err);
+                    static_cast<uint4*>(c->d.v_pool), c->d.n_phys_pages, n_slots, c->dev_err, pd ? *pd : PageDir{});
 }
 
 }  // namespace spkv

@@ -44,8 +44,9 @@ __device__ __forceinline__ float warp_sum(float v) {
 // (threads 0..63: thread i owns dims 2i, 2i+1).  Each request's local page is its own, so the
 // page count read here is the old one or already raised by head 0: the count used is the same.
 template <bool BF16>
-__device__ void append_local_row(const AppendRows& a, const int32_t* page_table, const int32_t* seq_len, void* ksum,
-                                 int np_max, int64_t n_phys, int b, int h, int Hk, uint32_t* err) {
+__device__ void append_local_row(const AppendRows& a, const int32_t* page_table, const PageDir& pd,
+                                 const int32_t* seq_len, void* ksum, int np_max, int64_t n_phys, int b, int h, int Hk,
+                                 uint32_t* err) {
   const int i = threadIdx.x;
   if (i >= kHeadDim / 2) return;
   const int L = seq_len[b];
@@ -55,7 +56,7 @@ __device__ void append_local_row(const AppendRows& a, const int32_t* page_table,
     if (i == 0) flag_error(err, SPKV_DEVERR_PAGE_ID);
     return;
   }
-  const int p = page_table[int64_t(b) * np_max + pg];
+  const int p = page_lookup(page_table, np_max, pd, b, pg);
   if (p < 0 || p >= n_phys) {
     if (i == 0) flag_error(err, SPKV_DEVERR_PHYS);
     return;
@@ -76,12 +77,12 @@ template <bool BF16, bool APPEND>
 __global__ void __launch_bounds__(kWarps * 32)
     score_kernel(const uint32_t* __restrict__ q, const void* __restrict__ ksum, const int32_t* __restrict__ page_table,
                  const int32_t* __restrict__ seq_len, float* __restrict__ scores, int Hq, int Hk, int G, int np_max,
-                 int64_t n_phys, float scale, uint32_t* err, AppendRows app) {
+                 int64_t n_phys, float scale, uint32_t* err, AppendRows app, PageDir pd) {
   pdl_wait();
   pdl_trigger();
   const int u = blockIdx.y, b = u / Hk, h = u % Hk;
   if (APPEND && blockIdx.x == gridDim.x - 1) {
-    append_local_row<BF16>(app, page_table, seq_len, const_cast<void*>(ksum), np_max, n_phys, b, h, Hk, err);
+    append_local_row<BF16>(app, page_table, pd, seq_len, const_cast<void*>(ksum), np_max, n_phys, b, h, Hk, err);
     return;
   }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -94,7 +95,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   constexpr int R = BF16 ? 8 : 4;
   const int pw0 = p_begin + warp * kPagesPerWarp;
   int ph = 0;
-  if (lane < kPagesPerWarp && pw0 + lane < p_end) ph = page_table[int64_t(b) * np_max + pw0 + lane];
+  if (lane < kPagesPerWarp && pw0 + lane < p_end) ph = page_lookup(page_table, np_max, pd, b, pw0 + lane);
   const int L = seq_len[b];
   __shared__ float qs[kHeadDim];
   if (tid < kHeadDim / 2) {
@@ -151,7 +152,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 
 cudaError_t launch_score(const spkv_cache* c, const void* q, int B, int Hq, const int32_t* page_table, int np_max,
                          const int32_t* seq_len, float* scores, cudaStream_t st, const void* k_new,
-                         const void* v_new) {
+                         const void* v_new, const PageDir* pd) {
   const int Hk = c->d.n_kv_heads;
   const int G = Hq / Hk;
   const bool append = k_new != nullptr;
@@ -163,7 +164,7 @@ cudaError_t launch_score(const spkv_cache* c, const void* q, int B, int Hq, cons
                              : (append ? score_kernel<false, true> : score_kernel<false, false>);
   return launch_pdl(kern, grid, dim3(kWarps * 32), 0, st, static_cast<const uint32_t*>(q),
                     static_cast<const void*>(c->d.ksum), page_table, seq_len, scores, Hq, Hk, G, np_max,
-                    static_cast<int64_t>(c->d.n_phys_pages), scale, c->dev_err, app);
+                    static_cast<int64_t>(c->d.n_phys_pages), scale, c->dev_err, app, pd ? *pd : PageDir{});
 }
 
 }  // namespace spkv

@@ -958,3 +958,65 @@ def test_column_scores_invariants():
     S2 = oracle.column_scores_batch(q2, w2["k_pool"], w2["page_table"], w2["seq_len"], 64)
     assert np.allclose(S2.sum(-1), 30, rtol=0, atol=1e-9)
     assert (S2[..., 0] >= 1 - 1e-12).all()      # row 0 sits at position 0 and sees key 0 alone
+
+
+# ------------------------------------------------------------------------------ two-level page directory
+
+def _split_table(table, shift, rng, dev_frac):
+    """A directory for a flat table, built independently: each segment that holds a mapped page gets
+    a host copy; a random share of them also a device copy (the directory then names the device)."""
+    B, npm = table.shape
+    seg = 1 << shift
+    n_dir = (npm + seg - 1) // seg
+    dir_ = np.full((B, n_dir), -1, np.int32)
+    host, dev = [], []
+    for b in range(B):
+        for s_ in range(n_dir):
+            chunk = np.full(seg, -1, np.int32)
+            part = table[b, s_ * seg:(s_ + 1) * seg]
+            chunk[:len(part)] = part
+            if (chunk < 0).all():
+                continue
+            if rng.random() < dev_frac:
+                dir_[b, s_] = len(dev)
+                dev.append(chunk)
+            else:
+                dir_[b, s_] = -2 - len(host)
+                host.append(chunk)
+    z = np.zeros((1, seg), np.int32)
+    return dir_, (np.array(dev) if dev else z), (np.array(host) if host else z)
+
+
+@pytest.mark.parametrize("shift,dev_frac", [(4, 0.0), (8, 0.5), (6, 1.0)])
+def test_dir_lookup_equals_flat_table(shift, dev_frac):
+    rng = np.random.default_rng(shift)
+    B, npm = 5, 1000
+    table = rng.integers(0, 50000, (B, npm)).astype(np.int32)
+    table[1, 300:700] = -1                 # an unmapped stretch spanning whole segments
+    table[3, 950:] = -1
+    d, dev, host = _split_table(table, shift, rng, dev_frac)
+    assert np.array_equal(oracle.dir_to_table(d, shift, dev, host, npm), table)
+    # entries naming segments that do not exist read as unmapped
+    bad = d.copy()
+    bad[0, 0] = 10 ** 6
+    bad[2, 1] = -2 - 10 ** 6
+    t2 = oracle.dir_to_table(bad, shift, dev, host, npm)
+    seg = 1 << shift
+    assert (t2[0, :seg] == -1).all() and (t2[2, seg:2 * seg] == -1).all()
+    assert np.array_equal(t2[4], table[4])
+
+
+def test_dir_metadata_follows_the_pages_in_use():
+    """Only segments with a mapped page exist: a 1M-page logical space with 3 x 4096 pages in use
+    needs about 3 x 16 segments of 256 ids, whatever the logical size."""
+    shift, npm = 8, 1 << 20
+    table = np.full((3, npm), -1, np.int32)
+    for b, start in enumerate((0, 5000, 900_000)):
+        table[b, start:start + 4096] = np.arange(4096) + 4096 * b
+    d, dev, host = _split_table(table, shift, np.random.default_rng(0), 0.0)
+    n_segs = int((d != -1).sum())
+    # 4096 pages fill 16 aligned segments; the ranges starting at 5000 and 900000 are not aligned
+    # to 256 and touch 17 each
+    assert n_segs == 16 + 17 + 17
+    assert host.shape[0] * (1 << shift) * 4 < table.nbytes / 200    # 50 KiB of segments for 12 MiB of flat table
+    assert np.array_equal(oracle.dir_to_table(d, shift, dev, host, npm), table)

@@ -512,6 +512,45 @@ def resident262k_leg(args, dev, timed, cap, peak, cpu_baseline, w, scache, qs, q
         sd_us.append(e[0].elapsed_time(e[1]) * 1e3)
         lru_us.append(e[1].elapsed_time(e[2]) * 1e3)
         miss.append(int(n_missing.sum().item()))
+    # the same step with the page table as a two-level directory ([Spin] 2C): every segment on the
+    # device tier, then every segment on the host tier (read in place over the host link)
+    pdir = {}
+    shift = 8
+    n_segs = B * ((npm + (1 << shift) - 1) >> shift)
+    for tier in ("device", "host"):
+        pm = spkv.PageMap(B, npm, seg_shift=shift, n_dev_segs=n_segs if tier == "device" else 0)
+        for b in range(B):
+            pm.map(b, 0, w["page_table"][b])
+            if tier == "device":
+                for p0 in range(0, npm, 1 << shift):
+                    pm.promote(b, p0)
+        pm.sync()
+
+        def dstep(i):
+            spkv.score_blocks_dir(scache, qs[i], pm, seq, scores)
+            spkv.select_resident_update(scache, scores, ev, alive, seq, k_q, k_e, sel, n_sel, resident, ts, i, 1,
+                                        missing, n_missing, slot, victims, hist)
+            spkv.sparse_decode_attn_dir(scache, qs[i], pm, sel, n_sel, seq, out, lse)
+
+        dstep(0)
+        graphs = {}
+        for i in idx:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                dstep(i)
+            graphs[i] = g
+        torch.cuda.synchronize()
+        dms = timed(lambda i: graphs[i].replay(), idx)
+        sc_us = statistics.median(timed(lambda i: spkv.score_blocks_dir(scache, qs[i], pm, seq, scores), idx)) * 1e3
+        del graphs
+        dev_b, host_b = pm.nbytes()
+        pdir[tier + "_tier"] = {"ms_per_step": statistics.mean(dms), "score_blocks_us": sc_us,
+                                "metadata_device_bytes": dev_b, "metadata_host_bytes": host_b}
+        pm.close()
+    pdir["flat_page_table_bytes"] = B * npm * 4
+    pdir["flat_score_blocks_us"] = statistics.median(
+        timed(lambda i: spkv.score_blocks(scache, qs[i], pt, seq, scores), idx)) * 1e3
+    pdir["segment_ids"] = 1 << shift
     st, bits = spkv.get_device_error(scache)
     if st != 0:
         raise RuntimeError(f"device error bits {bits} in the resident 262k leg")
@@ -523,7 +562,8 @@ def resident262k_leg(args, dev, timed, cap, peak, cpu_baseline, w, scache, qs, q
            "ms_per_step": ms, "ms_per_step_median": statistics.median(ms_all), "bytes_per_step": byts,
            "GBps": gbs, "pct_hbm_peak": 100 * gbs / peak, "queries_per_s": B / (ms * 1e-3),
            "resident_setdiff_us": statistics.median(sd_us), "lru_bucket_update_us": statistics.median(lru_us),
-           "missing_pages_per_step": statistics.mean(miss), "launch": "one CUDA graph per step"}
+           "missing_pages_per_step": statistics.mean(miss), "launch": "one CUDA graph per step",
+           "page_directory": pdir}
     if cpu_baseline:
         units = np.arange(U, dtype=np.int32)
         w1 = dict(w, q=q_host0)

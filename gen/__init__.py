@@ -280,7 +280,12 @@ def lazy_rag(seed: int = 0, B: int = 64, Hq: int = 32, Hk: int = 8, n_docs: int 
     for d in range(n_docs):
         for p in range(int(doc_pages[d])):
             cnt[doc_phys[d][p]] = min(PAGE, int(doc_len[d]) - PAGE * p)
+    doc_first = np.concatenate([[0], np.cumsum(doc_pages)]).astype(np.int32)
+    doc_phys = np.concatenate(doc_phys).astype(np.int32)
+    doc_valid = np.concatenate([np.minimum(PAGE, int(doc_len[d]) - PAGE * np.arange(int(doc_pages[d])))
+                                for d in range(n_docs)]).astype(np.int32)
     return dict(name=f"lazy-RoPE RAG decode B{B} Hq{Hq}/Hk{Hk} {n_docs} docs x{docs_per_req} Zipf({zipf_s})",
+                doc_first=doc_first, doc_phys=doc_phys, doc_valid=doc_valid,
                 B=B, Hq=Hq, Hk=Hk, G=Hq // Hk, D=HEAD_DIM, T=PAGE, n_phys=n_phys, np_max=np_max,
                 k_pool=k_pool, v_pool=v_pool, q=q, phys=phys, valid=valid, slot=slot, page_start=page_start,
                 n_pages=n_pages, doc_pos=doc_pos, qpos=qpos, theta=theta, picks=picks,

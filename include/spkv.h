@@ -14,6 +14,7 @@
  *   sparse_decode_attn_slots  attention reading the selected pages from their resident slots
  *   sparse_decode_attn   split-K flash decoding over the selected pages
  *   lazy_rope_decode_attn  the same with deferred RoPE (query rotated once per document)
+ *   lazy_rope_decode_attn_docs  the same over shared cached documents, scheduled by document
  *   lazy_rope_prefill_attn a tile of new query rows over cached documents (tcgen05)
  *   lazy_rope_prefill_step   the same plus the new rows' causal attention among themselves
  *   lazy_alibi_prefill_attn  the prefill step for models with ALiBi position biases
@@ -215,6 +216,41 @@ int lazy_rope_decode_attn(spkv_cache_t cache, const void* q, int B, int Hq, cons
                           const uint32_t* meta, int meta_heads, const int32_t* n_pages, int np_max,
                           const int32_t* doc_pos, int max_docs, float theta, float* out,
                           float* lse, void* stream);
+
+/* Lazy-RoPE decode attention over shared cached documents, scheduled document by document.
+ * [Lazy] "Core idea: deferred positional encoding" (a cached document, stored with only its
+ * document-local rotation, is reused at any position) and "Technical implementation 2. Decoding"
+ * (the query is rotated once per document by the relative offset).  The result is exactly
+ * lazy_rope_decode_attn's for a request whose page list is its documents' pages in slot order:
+ * request b holds document req_docs[b][i] (the plan's) in slot i, placed at token offset
+ * doc_pos[b][i]; document d's pages are doc_pages[doc_first[d] .. doc_first[d+1]) (page words as
+ * spkv_pack_page_words makes them; the slot field is ignored).  Each job of the plan streams one
+ * document's pages of one kv head once for the query rows of up to 16 / G requests holding it,
+ * each rotated by its own offset qpos[b] - doc_pos[b][i], so a document shared by many requests is
+ * read once per job rather than once per request; every (request, query head) then merges the
+ * partial results of its documents.
+ *   plan      : from lazy_docs_plan_create on this handle (B, Hq, max_docs and req_docs come from it)
+ *   q         : device bf16 [B][Hq][128], not rotated, 16-byte aligned
+ *   qpos      : device int32 [B];  doc_pos: device int32 [B][max_docs]
+ *   doc_pages : device uint32 page words;  doc_first: device int32 [n_docs + 1] (as given to the plan)
+ *   out, lse  : as lazy_rope_decode_attn (a request without documents gets 0 and -inf).
+ * A plan serves one stream at a time (its job counter and partials are reused by every call). */
+typedef struct spkv_doc_plan* spkv_doc_plan_t;
+int lazy_rope_decode_attn_docs(spkv_cache_t cache, spkv_doc_plan_t plan, const void* q, const int32_t* qpos,
+                               const uint32_t* doc_pages, const int32_t* doc_first, const int32_t* doc_pos,
+                               float theta, float* out, float* lse, void* stream);
+
+/* Builds the document-major schedule on the host (the decode batch's document composition changes
+ * far less often than every step, so one plan serves many steps):
+ *   req_docs  : host int32 [B][max_docs], the document in each slot of each request, -1 for none
+ *   doc_first : host int32 [n_docs + 1], the layout of the document page words (page counts)
+ * Allocates the plan's device buffers (jobs, occurrences, one partial record per occurrence and
+ * query head).  SPKV_EINVAL for a document id outside [-1, n_docs) or a decreasing doc_first. */
+int lazy_docs_plan_create(spkv_cache_t cache, int B, int Hq, const int32_t* req_docs, int max_docs, int n_docs,
+                          const int32_t* doc_first, spkv_doc_plan_t* out);
+/* Number of jobs in the plan. */
+int lazy_docs_plan_jobs(spkv_doc_plan_t plan);
+int lazy_docs_plan_destroy(spkv_doc_plan_t plan);
 
 /* Set-difference of selected vs GPU-resident pages, [NOSA] "Method 2: NOSI", optimised
  * memory layout (custom kernel computing set differences for block swapping).  Per unit:

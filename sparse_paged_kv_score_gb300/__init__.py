@@ -36,7 +36,8 @@ __all__ = ["PagedKVCache", "paged_kv_create", "paged_kv_append", "score_blocks",
            "lazy_rope_prefill_step",
            "attn_column_scores", "attn_column_scores_lse", "lazy_alibi_prefill_attn",
            "sparse_decode_attn_noalloc", "pack_page_words", "get_device_error", "SpkvError", "DEVERR",
-           "PageMap", "score_blocks_dir", "sparse_decode_attn_dir", "retrieve_pages_dir",
+           "PageMap", "score_blocks_dir", "sparse_decode_attn_dir", "retrieve_pages_dir", "DocPlan",
+           "lazy_rope_decode_attn_docs",
            "load"]
 
 HEAD_DIM, PAGE, SUBBLOCK = 128, 64, 16
@@ -276,6 +277,52 @@ def lazy_rope_decode_attn(cache: PagedKVCache, q, qpos, meta, n_pages, doc_pos, 
         _t(doc_pos, torch.int32, "doc_pos", (B, max_docs)), max_docs, float(theta),
         _t(out, torch.float32, "out", (B, Hq, HEAD_DIM)), _t(lse, torch.float32, "lse", (B, Hq)),
         _stream(stream)))
+
+
+class DocPlan:
+    """Document-major schedule of lazy-RoPE decode over shared cached documents (built on the host
+    from req_docs: host int32 [B][max_docs], -1 for an empty slot; doc_first: host int32
+    [n_docs + 1]).  Reused by every lazy_rope_decode_attn_docs call of that batch composition."""
+
+    def __init__(self, cache: PagedKVCache, Hq: int, req_docs, doc_first):
+        req_docs = np.ascontiguousarray(req_docs, np.int32)
+        doc_first = np.ascontiguousarray(doc_first, np.int32)
+        B, max_docs = req_docs.shape
+        h = ctypes.c_void_p()
+        check("lazy_docs_plan_create", load().lazy_docs_plan_create(
+            cache.handle, B, int(Hq), req_docs.ctypes.data, max_docs, doc_first.size - 1, doc_first.ctypes.data,
+            ctypes.byref(h)))
+        self.handle, self.B, self.Hq, self.max_docs = h, B, int(Hq), max_docs
+
+    @property
+    def n_jobs(self) -> int:
+        return load().lazy_docs_plan_jobs(self.handle)
+
+    def close(self):
+        if self.handle:
+            torch.cuda.synchronize()
+            check("lazy_docs_plan_destroy", load().lazy_docs_plan_destroy(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            if self.handle:
+                load().lazy_docs_plan_destroy(self.handle)
+                self.handle = None
+        except Exception:
+            pass
+
+
+def lazy_rope_decode_attn_docs(cache: PagedKVCache, plan: DocPlan, q, qpos, doc_pages, doc_first, doc_pos,
+                               theta: float, out, lse, stream=None):
+    """lazy_rope_decode_attn over shared documents, grouped by document.  doc_pages: int32 tensor of the
+    uint32 page words of every document; doc_first: int32 [n_docs + 1]; doc_pos: int32 [B][max_docs]."""
+    B, Hq = plan.B, plan.Hq
+    check("lazy_rope_decode_attn_docs", load().lazy_rope_decode_attn_docs(
+        cache.handle, plan.handle, _t(q, torch.bfloat16, "q", (B, Hq, HEAD_DIM)), _t(qpos, torch.int32, "qpos", (B,)),
+        _t(doc_pages, torch.int32, "doc_pages"), _t(doc_first, torch.int32, "doc_first"),
+        _t(doc_pos, torch.int32, "doc_pos", (B, plan.max_docs)), float(theta),
+        _t(out, torch.float32, "out", (B, Hq, HEAD_DIM)), _t(lse, torch.float32, "lse", (B, Hq)), _stream(stream)))
 
 
 def lazy_rope_prefill_attn(cache: PagedKVCache, q, qpos0, meta, n_pages, doc_pos, theta: float, out, lse,

@@ -61,6 +61,10 @@ SIGNATURES = {
     "sparse_decode_attn_noalloc": ([_vp, _vp, _i32, _i64, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _i32,
                                     _vp, _vp, _vp, _vp, _vp], _i32),
     "spkv_pack_page_words": ([_vp, _vp, _vp, _i64, _vp], _i32),
+    "lazy_docs_plan_create": ([_vp, _i32, _i32, _vp, _i32, _i32, _vp, ctypes.POINTER(_vp)], _i32),
+    "lazy_docs_plan_jobs": ([_vp], _i32),
+    "lazy_docs_plan_destroy": ([_vp], _i32),
+    "lazy_rope_decode_attn_docs": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _vp, _vp, _vp], _i32),
     "score_blocks_dir": ([_vp, _vp, _i32, _i32, _pd, _i32, _vp, _vp, _vp], _i32),
     "sparse_decode_attn_dir": ([_vp, _vp, _i32, _i32, _pd, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _vp], _i32),
     "retrieve_pages_dir": ([_vp, _vp, _vp, _i64, _pd, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp], _i32),

@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 SO = os.path.join(HERE, "libspkv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "attn.cu", "score.cu", "select.cu", "summary.cu", "resid.cu", "fused.cu", "prefill.cu", "colscore.cu", "retrieve.cu", "noalloc.cu", "pagemap.cu"]
+SOURCES = ["api.cu", "attn.cu", "score.cu", "select.cu", "summary.cu", "resid.cu", "fused.cu", "prefill.cu", "colscore.cu", "retrieve.cu", "noalloc.cu", "pagemap.cu", "docplan.cu"]
 
 
 def _nvcc() -> str:

@@ -76,6 +76,7 @@ struct Smem {
   uint64_t cfull;     // consumers -> epilogue (count kConsumers)
   uint64_t cempty;    // epilogue -> consumers (count 1)
   StageMeta meta[8];
+  int srel[8][16];          // document-major form: each query row's rotation offset, per stage
   int scan[kThreads];
   int prefix[kMaxUnits + 1];   // first global page position of every unit, then T
 };
@@ -104,7 +105,11 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk) {
 // hold the group's heads twice.  Columns 4..7 carry the bf16 lo part of what columns 0..3 carry
 // in hi (the rotated query in the lazy form, the probabilities P), so one MMA does the work of
 // the hi MMA and the lo MMA; the halves are added where a full value is needed.
-template <int NT, bool LAZY, bool PACK, int STAGES>
+// DOCS (document-major lazy form, LAZY set): a unit is a job of the plan -- one document, one kv
+// head and up to 16 / G of the requests that hold the document -- whose query rows (G per request,
+// each with its own rotation offset) share every page of the document; jobs come from a queue, are
+// never split, and leave one partial (max, sum, O) per query row, merged per request afterwards.
+template <int NT, bool LAZY, bool PACK, int STAGES, bool DOCS = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                       const __grid_constant__ AttnParams p) {
@@ -132,53 +137,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   // pages stream (CTA exit triggers it).
   pdl_wait();
 
-  // ---- 1. unit prefix table: prefix[u] = first global page position of unit u, prefix[U] = T
-  const int c0 = static_cast<int>(int64_t(tid) * U / kThreads);
-  const int c1 = static_cast<int>(int64_t(tid + 1) * U / kThreads);
-  int csum = 0;
-  for (int u = c0; u < c1; ++u) csum += unit_count(p, LAZY, u);
-  int x = csum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) S.scan[warp] = x;
-  __syncthreads();
-  int wbase = 0;
-  for (int w = 0; w < warp; ++w) wbase += S.scan[w];
-  {
-    int acc = wbase + x - csum;  // exclusive prefix of this thread's slice
-    for (int u = c0; u < c1; ++u) {
-      S.prefix[u] = acc;
-      acc += unit_count(p, LAZY, u);
-    }
-    if (c1 == U) S.prefix[U] = acc;
-  }
-  __syncthreads();
-  const int T = S.prefix[U];
-
-  // units with no pages get out = 0, lse = -inf (spread over the CTAs)
-  for (int u = blockIdx.x; u < U; u += gridDim.x) {
-    if (S.prefix[u + 1] != S.prefix[u]) continue;
-    const int b = u / p.Hk, h = u % p.Hk;
-    for (int i = tid; i < p.G * kHeadDim; i += kThreads)
-      p.out[(int64_t(b) * p.Hq + h * p.G) * kHeadDim + i] = 0.f;
-    if (tid < p.G) p.lse[int64_t(b) * p.Hq + h * p.G + tid] = -CUDART_INF_F;
-    if (tid == 0) p.ws_parts[2 * u] = p.ws_parts[2 * u + 1] = 0;
-  }
-  if (T == 0) return;
-  // Segments: static ranges of S0 pages (one per CTA, none when they would be shorter than
-  // min_chunk), then dynamic chunks of CH pages.  min_chunk bounds the partials of a unit
-  // (about 250 at most); the chunk count stays within the workspace (max_chunks - N chunks).
   const int N = gridDim.x;
-  int S0 = static_cast<int>(int64_t(T) * 3 / (4 * int64_t(N)));
-  if (S0 < p.min_chunk) S0 = 0;
-  const int D0 = S0 * N;
-  const int T_dyn = T - D0;
-  const int CH = max(max((T_dyn + 6 * N - 1) / (6 * N), (T_dyn + p.max_chunks - N - 1) / (p.max_chunks - N)),
-                     p.min_chunk);
-  const int n_chunks = (T_dyn + CH - 1) / CH;
+  int T = 0, S0 = 0, D0 = 0, CH = 1, n_chunks = 0;
+  if (!DOCS) {
+    // ---- 1. unit prefix table: prefix[u] = first global page position of unit u, prefix[U] = T
+    const int c0 = static_cast<int>(int64_t(tid) * U / kThreads);
+    const int c1 = static_cast<int>(int64_t(tid + 1) * U / kThreads);
+    int csum = 0;
+    for (int u = c0; u < c1; ++u) csum += unit_count(p, LAZY, u);
+    int x = csum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) S.scan[warp] = x;
+    __syncthreads();
+    int wbase = 0;
+    for (int w = 0; w < warp; ++w) wbase += S.scan[w];
+    {
+      int acc = wbase + x - csum;  // exclusive prefix of this thread's slice
+      for (int u = c0; u < c1; ++u) {
+        S.prefix[u] = acc;
+        acc += unit_count(p, LAZY, u);
+      }
+      if (c1 == U) S.prefix[U] = acc;
+    }
+    __syncthreads();
+    T = S.prefix[U];
+
+    // units with no pages get out = 0, lse = -inf (spread over the CTAs)
+    for (int u = blockIdx.x; u < U; u += gridDim.x) {
+      if (S.prefix[u + 1] != S.prefix[u]) continue;
+      const int b = u / p.Hk, h = u % p.Hk;
+      for (int i = tid; i < p.G * kHeadDim; i += kThreads)
+        p.out[(int64_t(b) * p.Hq + h * p.G) * kHeadDim + i] = 0.f;
+      if (tid < p.G) p.lse[int64_t(b) * p.Hq + h * p.G + tid] = -CUDART_INF_F;
+      if (tid == 0) p.ws_parts[2 * u] = p.ws_parts[2 * u + 1] = 0;
+    }
+    if (T == 0) return;
+    // Segments: static ranges of S0 pages (one per CTA, none when they would be shorter than
+    // min_chunk), then dynamic chunks of CH pages.  min_chunk bounds the partials of a unit
+    // (about 250 at most); the chunk count stays within the workspace (max_chunks - N chunks).
+    S0 = static_cast<int>(int64_t(T) * 3 / (4 * int64_t(N)));
+    if (S0 < p.min_chunk) S0 = 0;
+    D0 = S0 * N;
+    const int T_dyn = T - D0;
+    CH = max(max((T_dyn + 6 * N - 1) / (6 * N), (T_dyn + p.max_chunks - N - 1) / (p.max_chunks - N)), p.min_chunk);
+    n_chunks = (T_dyn + CH - 1) / CH;
+  }
   auto seg_of = [&](int x) { return x < D0 ? x / S0 : N + (x - D0) / CH; };
   const int qbytes = p.G * kHeadDim * 2;
 
@@ -187,11 +194,85 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol = l2_policy_evict_first();   // each page is read once per call
     int last_unit = -1, last_chunk = -1, jl = 0;
     bool ok = true;
-    // lane 0 keeps the next dynamic chunk index requested one segment ahead, so the atomic's
-    // latency overlaps the streaming of the current segment
+    // lane 0 keeps the next dynamic chunk index (DOCS: the next job) requested one segment ahead,
+    // so the atomic's latency overlaps the streaming of the current segment
     int ahead = 0;
-    if (lane == 0 && n_chunks > 0) ahead = atomicAdd(&p.ws_ctl[0], 1);
-    for (int it = 0; ok; ++it) {
+    if (lane == 0 && (DOCS || n_chunks > 0)) ahead = atomicAdd(&p.ws_ctl[0], 1);
+    while (DOCS && ok) {
+      const int job = __shfl_sync(0xffffffffu, ahead, 0);
+      if (job >= p.n_jobs) break;
+      if (lane == 0) ahead = atomicAdd(&p.ws_ctl[0], 1);
+      const int4 jb = p.jobs[job];              // document, kv head, first occurrence, occurrences
+      const int pg0 = p.doc_first[jb.x];
+      const int npg = max(0, p.doc_first[jb.x + 1] - pg0);
+      const int nrows = jb.w * p.G;
+      // lane o < occurrences: occurrence o's request and rotation offset (query position minus
+      // the document's placement in that request)
+      int ob = 0, orel = 0;
+      if (lane < jb.w) {
+        const int2 oc = p.occ[jb.z + lane];     // request, document slot
+        ob = oc.x;
+        orel = p.qpos[oc.x] - p.doc_pos[int64_t(oc.x) * p.max_docs + oc.y];
+      }
+      const int row_rel = __shfl_sync(0xffffffffu, orel, min(lane / p.G, 31));   // query row = lane
+      const int steps = max(npg, 1);            // a document without pages still hands over empty results
+      for (int xb = 0; xb < steps && ok; xb += 32) {
+        int phys = 0, valid = 0;
+        if (xb + lane < npg) {
+          const uint32_t w = p.doc_pages[pg0 + xb + lane];
+          const int ph = static_cast<int>(w & 0x3FFFFu);
+          if (ph >= p.n_phys) flag_error(p.err, SPKV_DEVERR_PHYS);
+          else {
+            phys = ph;
+            valid = static_cast<int>((w >> 18) & 63u) + 1;
+          }
+        }
+        const int cnt = min(32, steps - xb);
+        for (int i = 0; i < cnt; ++i, ++jl) {
+          const int s = jl % STAGES;
+          const int bv = __shfl_sync(0xffffffffu, valid, i);
+          const int bp = __shfl_sync(0xffffffffu, phys, i);
+          if (jl >= STAGES) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&S.empty[s], ((jl / STAGES) - 1) & 1, p.wait_ns))) {
+              if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
+              ok = false;
+              break;
+            }
+          }
+          const bool first = xb + i == 0;
+          uint8_t* dst = stages + size_t(s) * kStage;
+          if (first && lane < 16) S.srel[s][lane] = row_rel;
+          __syncwarp();
+          if (lane == 0) {
+            StageMeta m;
+            m.unit = job;
+            m.valid = bv;
+            m.rel = 0;
+            m.ustart = 0;
+            m.ucount = npg;
+            m.chunk = 0;
+            m.pad0 = nrows;
+            m.pad1 = 0;
+            S.meta[s] = m;
+            mbar_arrive_expect_tx(&S.full[s], (bv > 0 ? kKVBytes : 0) + (first ? nrows * kHeadDim * 2 : 0));
+          }
+          __syncwarp();
+          if (first && lane < jb.w)   // the G query rows of occurrence `lane`, one bulk copy each
+            bulk_load(dst + kKVBytes + lane * p.G * kHeadDim * 2,
+                      static_cast<const uint8_t*>(p.q) + (int64_t(ob) * p.Hq + jb.y * p.G) * (kHeadDim * 2),
+                      p.G * kHeadDim * 2, &S.full[s]);
+          if (lane == 0 && bv > 0) {
+            const int z = static_cast<int>(int64_t(jb.y) * p.n_phys + bp);
+            tma_load_3d(dst, &tmk, &S.full[s], 0, 0, z, pol);
+            tma_load_3d(dst + kBoxBytes, &tmk, &S.full[s], 64, 0, z, pol);
+            tma_load_3d(dst + 2 * kBoxBytes, &tmv, &S.full[s], 0, 0, z, pol);
+            tma_load_3d(dst + 3 * kBoxBytes, &tmv, &S.full[s], 64, 0, z, pol);
+          }
+          __syncwarp();
+        }
+      }
+    }
+    for (int it = 0; !DOCS && ok; ++it) {
       int c, x0, x1;   // segment id and its page range
       if (it == 0 && S0 > 0) {
         c = blockIdx.x;
@@ -347,7 +428,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       const int u = S.h_unit, chunk = S.h_chunk, ustart = S.h_ustart, ucount = S.h_ucount, last = S.h_last;
-      if (u >= 0) {
+      if (DOCS && u >= 0) {
+        const int4 jb = p.jobs[u];
+        for (int g = 0; g < jb.w * p.G; ++g) {
+          float M = -CUDART_INF_F;
+#pragma unroll
+          for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, S.cm[w][g]);
+          float fw[kConsumers], L = 0.f;
+#pragma unroll
+          for (int w = 0; w < kConsumers; ++w) {
+            const float mw = S.cm[w][g];
+            fw[w] = mw == -CUDART_INF_F ? 0.f : exp2f(mw - M);
+            L += fw[w] * S.cl[w][g];
+          }
+          // row of (occurrence, query head of the kv head's group) in the plan's partials
+          const int64_t row = int64_t(jb.z + g / p.G) * p.Hq + jb.y * p.G + g % p.G;
+#pragma unroll
+          for (int i = 0; i < kHeadDim / 32; ++i) {
+            const int d = lane + 32 * i;
+            float acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumers; ++w) acc += fw[w] * S.co[w][g][d];
+            p.part_o[row * kHeadDim + d] = acc;
+          }
+          if (lane == 0) {
+            p.part_m[row] = M;
+            p.part_l[row] = L;
+          }
+        }
+      } else if (u >= 0) {
         const int b = u / p.Hk, h = u % p.Hk;
         const int first = seg_of(ustart);
         const int nparts = seg_of(ustart + ucount - 1) - first + 1;
@@ -406,6 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t ql[LAZY && !PACK ? 8 : 1][NT][2];   // lazy: bf16 lo part of the rotated query
   uint32_t qraw[LAZY ? 8 : 1][NT][2];     // lazy: unrotated query
   int cur_u = -1, cur_c = -1, cur_us = 0, cur_uc = 0, cur_rel = 0, n_flush = 0;
+  int col_rel[NT];                        // rotation offset of each query column (DOCS: per row)
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) col_rel[nt] = 0;
   bool have_rel = false;
 
   auto reset_state = [&]() {
@@ -420,13 +532,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
-  // q fragments from the stage's query rows (rows g >= G read as zero).
-  auto load_q = [&](const uint8_t* qs) {
+  // q fragments from the stage's query rows (rows g >= rows read as zero).
+  auto load_q = [&](const uint8_t* qs, int rows) {
     const uint32_t* qw = reinterpret_cast<const uint32_t*>(qs);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int g = PACK ? (r & 3) : nt * 8 + r;
-      const bool live = g < p.G;
+      const bool live = g < rows;
       const int row = (live ? g : 0) * (kHeadDim / 2);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
@@ -447,21 +559,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   // angle of pair i is rel * theta_i; its fraction of a turn is formed exactly modulo 1 as a
   // 64-bit fixed-point product (phase accumulator), so the angle handed to __sincosf lies in
   // [-pi, pi) with ~1e-9 rad error however large rel * theta_i is.
-  auto rotate_q = [&](int rel) {
+  auto rotate_q = [&](const int (&rel)[NT]) {
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
       for (int wi = 0; wi < 2; ++wi) {
-        float sn[2], cs[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int i = 16 * ks + 2 * c + 8 * wi + e;   // pair index: dims i and i + 64
-          const uint64_t ph = static_cast<uint64_t>(static_cast<int64_t>(rel)) * p.phase_inc[i];
-          const float ang = static_cast<float>(static_cast<int32_t>(ph >> 32)) * 1.4629180792671596e-09f;
-          __sincosf(ang, &sn[e], &cs[e]);
-        }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
+          float sn[2], cs[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int i = 16 * ks + 2 * c + 8 * wi + e;   // pair index: dims i and i + 64
+            const uint64_t ph = static_cast<uint64_t>(static_cast<int64_t>(rel[nt])) * p.phase_inc[i];
+            const float ang = static_cast<float>(static_cast<int32_t>(ph >> 32)) * 1.4629180792671596e-09f;
+            __sincosf(ang, &sn[e], &cs[e]);
+          }
           const uint32_t wx = qraw[LAZY ? ks : 0][nt][wi], wy = qraw[LAZY ? ks + 4 : 0][nt][wi];
           const float x0 = bf16lo_to_f32(wx), x1 = bf16hi_to_f32(wx);
           const float y0 = bf16lo_to_f32(wy), y1 = bf16hi_to_f32(wy);
@@ -552,12 +664,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       cur_us = mt.ustart;
       cur_uc = mt.ucount;
       reset_state();
-      load_q(stages + size_t(s) * kStage + kKVBytes);
+      load_q(stages + size_t(s) * kStage + kKVBytes, DOCS ? mt.pad0 : p.G);
+      if (DOCS) {   // the job's query rows each carry their own offset (one document: fixed for the job)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) col_rel[nt] = S.srel[s][nt * 8 + r];
+      }
       have_rel = false;
     }
     if (mt.valid > t0) {
-      if (LAZY && (!have_rel || mt.rel != cur_rel)) {
-        rotate_q(mt.rel);
+      if (LAZY && (!have_rel || (!DOCS && mt.rel != cur_rel))) {
+        if (!DOCS) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) col_rel[nt] = mt.rel;
+        }
+        rotate_q(col_rel);
         cur_rel = mt.rel;
         have_rel = true;
       }
@@ -723,10 +843,55 @@ __global__ void __launch_bounds__(kCombineHeads * kHeadDim)
   }
 }
 
-template <int NT, bool LAZY, bool PACK, int STAGES>
+// Document-major form: merges, for each request and query head, the partials its documents' jobs
+// left (one per document slot, in slot order), and resets the job counter for the next launch.
+__global__ void __launch_bounds__(kCombineHeads * kHeadDim)
+    attn_docs_combine_kernel(const __grid_constant__ AttnParams p) {
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.x, d = threadIdx.x % kHeadDim;
+  if (b == 0 && threadIdx.x == 0) p.ws_ctl[0] = 0;
+  for (int hq = threadIdx.x / kHeadDim; hq < p.Hq; hq += kCombineHeads) {
+    float M = -CUDART_INF_F, L = 0.f, acc = 0.f;
+    for (int i0 = 0; i0 < p.max_docs; i0 += 8) {
+      float mw[8], lw[8], ow[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int o = i0 + k < p.max_docs ? p.req_occ[int64_t(b) * p.max_docs + i0 + k] : -1;
+        if (o >= 0) {
+          const int64_t row = int64_t(o) * p.Hq + hq;
+          mw[k] = p.part_m[row];
+          lw[k] = p.part_l[row];
+          ow[k] = p.part_o[row * kHeadDim + d];
+        } else {
+          mw[k] = -CUDART_INF_F;
+          lw[k] = ow[k] = 0.f;
+        }
+      }
+      float mb = M;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mb = fmaxf(mb, mw[k]);
+      if (mb == -CUDART_INF_F) continue;
+      const float r = exp2f(M - mb);     // M = -inf gives 0
+      L *= r;
+      acc *= r;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float f = mw[k] == -CUDART_INF_F ? 0.f : exp2f(mw[k] - mb);
+        L += f * lw[k];
+        acc += f * ow[k];
+      }
+      M = mb;
+    }
+    p.out[(int64_t(b) * p.Hq + hq) * kHeadDim + d] = L > 0.f ? acc / L : 0.f;
+    if (d == 0) p.lse[int64_t(b) * p.Hq + hq] = L > 0.f ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
+  }
+}
+
+template <int NT, bool LAZY, bool PACK, int STAGES, bool DOCS = false>
 cudaError_t set_attr() {
-  return cudaFuncSetAttribute(attn_split_kernel<NT, LAZY, PACK, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(smem_bytes<NT, STAGES>()));
+  return cudaFuncSetAttribute(attn_split_kernel<NT, LAZY, PACK, STAGES, DOCS>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes<NT, STAGES>()));
 }
 
 template <int NT, bool LAZY, bool PACK, int STAGES>
@@ -748,7 +913,15 @@ cudaError_t attn_init_attributes() {
   if ((e = set_attr<1, false, false, kStages1>()) != cudaSuccess) return e;
   if ((e = set_attr<1, true, false, kStages1>()) != cudaSuccess) return e;
   if ((e = set_attr<2, false, false, kStages2>()) != cudaSuccess) return e;
+  if ((e = set_attr<2, true, false, kStages2, true>()) != cudaSuccess) return e;
   return set_attr<2, true, false, kStages2>();
+}
+
+cudaError_t launch_attn_docs(const spkv_cache* c, const AttnParams& p, int grid, cudaStream_t st) {
+  cudaError_t e = launch_pdl(attn_split_kernel<2, true, false, kStages2, true>, dim3(grid), dim3(kThreads),
+                             smem_bytes<2, kStages2>(), st, c->tmap_k, c->tmap_v, p);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(attn_docs_combine_kernel, dim3(p.B), dim3(kCombineHeads * kHeadDim), 0, st, p);
 }
 
 cudaError_t launch_attn(const spkv_cache* c, const AttnParams& p, bool lazy, int grid, cudaStream_t st) {

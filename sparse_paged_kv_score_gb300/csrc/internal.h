@@ -98,6 +98,16 @@ struct AttnParams {
   const int32_t* n_pages;
   const int32_t* doc_pos;
   int max_docs;
+  // document-major lazy form (a plan's jobs)
+  const int4* jobs;              // [n_jobs]: document, kv head, first occurrence, occurrences
+  int n_jobs;
+  const int2* occ;               // [occurrences]: request, document slot
+  const int32_t* req_occ;        // [B][max_docs]: occurrence of each (request, slot), -1 for none
+  const uint32_t* doc_pages;     // page words (phys | (valid - 1) << 18) of every document, by document
+  const int32_t* doc_first;      // [documents + 1]: first page word of each document
+  float* part_m;                 // [occurrences][Hq] row max (log2 domain), sum and unnormalised O
+  float* part_l;
+  float* part_o;
   float scale_log2;              // log2(e) / sqrt(128)
   uint64_t wait_ns;              // limit of each intra-CTA hand-off wait (0: give up unless complete)
   uint64_t phase_inc[64];        // RoPE pair j: turns per position, 2^-64 fixed point
@@ -164,6 +174,7 @@ cudaError_t launch_select(const spkv_cache* c, const float* qs, const float* es,
                           int np_max, const int32_t* seq_len, int k_q, int k_e, int32_t* sel, int32_t* n_sel,
                           cudaStream_t st);
 cudaError_t launch_attn(const spkv_cache* c, const AttnParams& p, bool lazy, int grid, cudaStream_t st);
+cudaError_t launch_attn_docs(const spkv_cache* c, const AttnParams& p, int grid, cudaStream_t st);
 cudaError_t launch_setdiff(uint32_t* err, const int32_t* resident, int n_slots, const int32_t* sel,
                            const int32_t* n_sel, int sel_stride, int n_units, int32_t* missing,
                            int32_t* n_missing, int32_t* slot, cudaStream_t st);

@@ -114,7 +114,9 @@ def test_docs_vs_oracle(seed, Hq, Hk):
     w = gen.lazy_rag(seed=seed, B=12, Hq=Hq, Hk=Hk, n_docs=9, docs_per_req=4, min_len=70, max_len=900)
     res = _run_both(w, w["picks"], w["doc_pos"], w["qpos"], w["q"])
     _check(w, w["q"], w["doc_pos"], res)
-    assert res[-1] < w["B"] * w["Hk"] * 4      # shared documents: fewer jobs than (request, head, slot)s
+    # shared documents: fewer jobs than (request, kv head, slot)s once a job holds several requests
+    opj = max(1, 16 // (Hq // Hk))
+    assert res[-1] <= w["B"] * w["Hk"] * 4 and (opj == 1 or res[-1] < w["B"] * w["Hk"] * 4)
 
 
 def test_docs_empty_slots_duplicates_and_empty_documents():

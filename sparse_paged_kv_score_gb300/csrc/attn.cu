@@ -38,17 +38,24 @@
 namespace spkv {
 namespace {
 
-constexpr int kConsumers = 4;
-constexpr int kProducerWarp = kConsumers;
-constexpr int kEpilogueWarp = kConsumers + 1;
-constexpr int kThreads = (kConsumers + 2) * 32;
 constexpr int kBoxBytes = 8192;                // 64 tokens x 64 dims x bf16
 constexpr int kKVBytes = 4 * kBoxBytes;        // K (2 boxes) + V (2 boxes) of one page-head
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kDocRows = 16;                   // query rows of a document-major job
+
+// Warps: kCons consumers, then the producer warp and the epilogue warp.  The document-major form
+// runs two groups of four consumers over each page, one group per 8 of the job's 16 query rows, so
+// every SM sub-partition has two consumer warps to switch between.
+template <bool DOCS>
+struct Cfg {
+  static constexpr int kCons = DOCS ? 8 : 4;
+  static constexpr int kThreads = (kCons + 2) * 32;
+};
+constexpr int kThreads = Cfg<false>::kThreads;
 
 // Stage: K/V page image, then room for the query rows of the unit it starts.
-template <int NT>
-__host__ __device__ constexpr int stage_bytes() { return kKVBytes + NT * 8 * kHeadDim * 2; }
+template <int NT, bool DOCS = false>
+__host__ __device__ constexpr int stage_bytes() { return kKVBytes + (DOCS ? kDocRows : NT * 8) * kHeadDim * 2; }
 
 constexpr int kEnd = -2;   // StageMeta.unit of the stage that ends the CTA's page stream
 constexpr int kMaxUnits = 4096;   // (request, kv head) units per call
@@ -63,17 +70,17 @@ struct __align__(16) StageMeta {
   int pad0, pad1;
 };
 
-template <int NT>
+template <int NT, int KC>
 struct Smem {
   static constexpr int kG = NT * 8;
   // hand-off buffer from the consumer warps to the epilogue warp
-  float cm[kConsumers][kG];
-  float cl[kConsumers][kG];
-  float co[kConsumers][kG][kHeadDim + 4];   // rows padded: the consumers' stores are conflict-free
+  float cm[KC][kG];
+  float cl[KC][kG];
+  float co[KC][kG][kHeadDim + 4];   // rows padded: the consumers' stores are conflict-free
   int h_unit, h_chunk, h_ustart, h_ucount, h_last, h_pad[3];
   uint64_t full[8];
   uint64_t empty[8];
-  uint64_t cfull;     // consumers -> epilogue (count kConsumers)
+  uint64_t cfull;     // consumers -> epilogue (count: the consumer warps)
   uint64_t cempty;    // epilogue -> consumers (count 1)
   StageMeta meta[8];
   int srel[8][16];          // document-major form: each query row's rotation offset, per stage
@@ -81,9 +88,9 @@ struct Smem {
   int prefix[kMaxUnits + 1];   // first global page position of every unit, then T
 };
 
-template <int NT, int STAGES>
+template <int NT, int STAGES, bool DOCS = false>
 constexpr size_t smem_bytes() {
-  return 1024 /*align slack*/ + size_t(STAGES) * stage_bytes<NT>() + sizeof(Smem<NT>);
+  return 1024 /*align slack*/ + size_t(STAGES) * stage_bytes<NT, DOCS>() + sizeof(Smem<NT, Cfg<DOCS>::kCons>);
 }
 
 __device__ __forceinline__ int unit_count(const AttnParams& p, bool lazy, int u) {
@@ -110,13 +117,16 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk) {
 // each with its own rotation offset) share every page of the document; jobs come from a queue, are
 // never split, and leave one partial (max, sum, O) per query row, merged per request afterwards.
 template <int NT, bool LAZY, bool PACK, int STAGES, bool DOCS = false>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<DOCS>::kThreads, 1)
     attn_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                       const __grid_constant__ AttnParams p) {
-  constexpr int kStage = stage_bytes<NT>();
+  constexpr int kConsumers = Cfg<DOCS>::kCons;
+  constexpr int kProducerWarp = kConsumers;
+  constexpr int kEpilogueWarp = kConsumers + 1;
+  constexpr int kStage = stage_bytes<NT, DOCS>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Smem<NT>& S = *reinterpret_cast<Smem<NT>*>(stages + size_t(STAGES) * kStage);
+  Smem<NT, kConsumers>& S = *reinterpret_cast<Smem<NT, kConsumers>*>(stages + size_t(STAGES) * kStage);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int U = p.B * p.Hk;
@@ -431,15 +441,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (DOCS && u >= 0) {
         const int4 jb = p.jobs[u];
         for (int g = 0; g < jb.w * p.G; ++g) {
+          // row g was handled by the four warps of group g / 8, in their column g % 8
+          const int w0 = (g >> 3) * 4, col = g & 7;
           float M = -CUDART_INF_F;
 #pragma unroll
-          for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, S.cm[w][g]);
-          float fw[kConsumers], L = 0.f;
+          for (int w = 0; w < 4; ++w) M = fmaxf(M, S.cm[w0 + w][col]);
+          float fw[4], L = 0.f;
 #pragma unroll
-          for (int w = 0; w < kConsumers; ++w) {
-            const float mw = S.cm[w][g];
+          for (int w = 0; w < 4; ++w) {
+            const float mw = S.cm[w0 + w][col];
             fw[w] = mw == -CUDART_INF_F ? 0.f : exp2f(mw - M);
-            L += fw[w] * S.cl[w][g];
+            L += fw[w] * S.cl[w0 + w][col];
           }
           // row of (occurrence, query head of the kv head's group) in the plan's partials
           const int64_t row = int64_t(jb.z + g / p.G) * p.Hq + jb.y * p.G + g % p.G;
@@ -448,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int d = lane + 32 * i;
             float acc = 0.f;
 #pragma unroll
-            for (int w = 0; w < kConsumers; ++w) acc += fw[w] * S.co[w][g][d];
+            for (int w = 0; w < 4; ++w) acc += fw[w] * S.co[w0 + w][col][d];
             p.part_o[row * kHeadDim + d] = acc;
           }
           if (lane == 0) {
@@ -506,7 +518,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ================================================================== consumer warps
   const int r = lane >> 2, c = lane & 3;
-  const int t0 = warp * 16;
+  // tokens t0 .. t0 + 15 of every page; DOCS: consumer group `grp` takes query rows 8 grp .. 8 grp + 7
+  const int t0 = (warp & 3) * 16;
+  const int grp_row = DOCS ? (warp >> 2) * 8 : 0;
   const float scale = p.scale_log2;
 
   float m[NT][2], lsum[NT][2];
@@ -537,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t* qw = reinterpret_cast<const uint32_t*>(qs);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int g = PACK ? (r & 3) : nt * 8 + r;
+      const int g = PACK ? (r & 3) : grp_row + nt * 8 + r;
       const bool live = g < rows;
       const int row = (live ? g : 0) * (kHeadDim / 2);
 #pragma unroll
@@ -667,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       load_q(stages + size_t(s) * kStage + kKVBytes, DOCS ? mt.pad0 : p.G);
       if (DOCS) {   // the job's query rows each carry their own offset (one document: fixed for the job)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) col_rel[nt] = S.srel[s][nt * 8 + r];
+        for (int nt = 0; nt < NT; ++nt) col_rel[nt] = S.srel[s][grp_row + nt * 8 + r];
       }
       have_rel = false;
     }
@@ -891,7 +905,8 @@ __global__ void __launch_bounds__(kCombineHeads * kHeadDim)
 template <int NT, bool LAZY, bool PACK, int STAGES, bool DOCS = false>
 cudaError_t set_attr() {
   return cudaFuncSetAttribute(attn_split_kernel<NT, LAZY, PACK, STAGES, DOCS>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes<NT, STAGES>()));
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(smem_bytes<NT, STAGES, DOCS>()));
 }
 
 template <int NT, bool LAZY, bool PACK, int STAGES>
@@ -904,6 +919,7 @@ cudaError_t launch_one(const spkv_cache* c, const AttnParams& p, int grid, cudaS
 
 constexpr int kStages1 = 5;   // G <= 8: 5 stages of 34 KiB
 constexpr int kStages2 = 4;   // G <= 16: 4 stages of 36 KiB
+constexpr int kStagesD = 4;   // document-major: 4 stages of 36 KiB (16 query rows), eight consumer warps
 
 }  // namespace
 
@@ -913,13 +929,13 @@ cudaError_t attn_init_attributes() {
   if ((e = set_attr<1, false, false, kStages1>()) != cudaSuccess) return e;
   if ((e = set_attr<1, true, false, kStages1>()) != cudaSuccess) return e;
   if ((e = set_attr<2, false, false, kStages2>()) != cudaSuccess) return e;
-  if ((e = set_attr<2, true, false, kStages2, true>()) != cudaSuccess) return e;
+  if ((e = set_attr<1, true, false, kStagesD, true>()) != cudaSuccess) return e;
   return set_attr<2, true, false, kStages2>();
 }
 
 cudaError_t launch_attn_docs(const spkv_cache* c, const AttnParams& p, int grid, cudaStream_t st) {
-  cudaError_t e = launch_pdl(attn_split_kernel<2, true, false, kStages2, true>, dim3(grid), dim3(kThreads),
-                             smem_bytes<2, kStages2>(), st, c->tmap_k, c->tmap_v, p);
+  cudaError_t e = launch_pdl(attn_split_kernel<1, true, false, kStagesD, true>, dim3(grid),
+                             dim3(Cfg<true>::kThreads), smem_bytes<1, kStagesD, true>(), st, c->tmap_k, c->tmap_v, p);
   if (e != cudaSuccess) return e;
   return launch_pdl(attn_docs_combine_kernel, dim3(p.B), dim3(kCombineHeads * kHeadDim), 0, st, p);
 }

@@ -70,7 +70,7 @@ struct __align__(16) StageMeta {
   int pad0, pad1;
 };
 
-template <int NT, int KC>
+template <int NT, int KC, int NPREFIX = kMaxUnits + 1>
 struct Smem {
   static constexpr int kG = NT * 8;
   // hand-off buffer from the consumer warps to the epilogue warp
@@ -85,12 +85,13 @@ struct Smem {
   StageMeta meta[8];
   int srel[8][16];          // document-major form: each query row's rotation offset, per stage
   int scan[kThreads];
-  int prefix[kMaxUnits + 1];   // first global page position of every unit, then T
+  int prefix[NPREFIX];         // first global page position of every unit, then T (not used by DOCS)
 };
 
 template <int NT, int STAGES, bool DOCS = false>
 constexpr size_t smem_bytes() {
-  return 1024 /*align slack*/ + size_t(STAGES) * stage_bytes<NT, DOCS>() + sizeof(Smem<NT, Cfg<DOCS>::kCons>);
+  return 1024 /*align slack*/ + size_t(STAGES) * stage_bytes<NT, DOCS>() +
+         sizeof(Smem<NT, Cfg<DOCS>::kCons, DOCS ? 1 : kMaxUnits + 1>);
 }
 
 __device__ __forceinline__ int unit_count(const AttnParams& p, bool lazy, int u) {
@@ -126,7 +127,8 @@ __global__ void __launch_bounds__(Cfg<DOCS>::kThreads, 1)
   constexpr int kStage = stage_bytes<NT, DOCS>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Smem<NT, kConsumers>& S = *reinterpret_cast<Smem<NT, kConsumers>*>(stages + size_t(STAGES) * kStage);
+  using SmemT = Smem<NT, kConsumers, DOCS ? 1 : kMaxUnits + 1>;
+  SmemT& S = *reinterpret_cast<SmemT*>(stages + size_t(STAGES) * kStage);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int U = p.B * p.Hk;
@@ -919,7 +921,7 @@ cudaError_t launch_one(const spkv_cache* c, const AttnParams& p, int grid, cudaS
 
 constexpr int kStages1 = 5;   // G <= 8: 5 stages of 34 KiB
 constexpr int kStages2 = 4;   // G <= 16: 4 stages of 36 KiB
-constexpr int kStagesD = 4;   // document-major: 4 stages of 36 KiB (16 query rows), eight consumer warps
+constexpr int kStagesD = 5;   // document-major: 5 stages of 36 KiB (16 query rows), eight consumer warps
 
 }  // namespace
 

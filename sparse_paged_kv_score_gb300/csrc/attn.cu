@@ -144,6 +144,8 @@ __global__ void __launch_bounds__(Cfg<DOCS>::kThreads, 1)
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
   }
+  // No warp touches a barrier before thread 0 has initialised it.
+  __syncthreads();
   // The page lists and counts below are written by the previous kernel.  This kernel does not
   // trigger its dependent early: the combine kernel's CTAs would only sit on the SMs while the
   // pages stream (CTA exit triggers it).

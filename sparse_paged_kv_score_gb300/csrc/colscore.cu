@@ -13,28 +13,25 @@
 //
 // One CTA per (request b, query head hq) and launch; a launch covers one chunk of up to 128 window
 // rows (one M 128 tile).  Every row's softmax is its own, so the chunks' column sums add: the first
-// launch writes them, later launches add theirs.  Ten warps:
+// launch writes them, later launches add theirs.  Eighteen warps:
 //   warp 0     TMA producer: the K rows of two consecutive pages (two 64 x 64 bf16 boxes each,
-//              128-byte swizzle, stacked into 128-row tiles) into a 4-stage ring, once for each
+//              128-byte swizzle, stacked into 128-row tiles) into a 3-stage ring, once for each
 //              pass;
 //   warp 1     MMA issuer (one thread): S = Q K^T (M 128 query rows, N 64 or 128 keys) into one
 //              of two TMEM buffers, in both passes; a stage is released as soon as its MMA
 //              completes (V is never needed);
-//   warps 2-9  two column groups of 64 keys (warps 2-5, 6-9), one warp per TMEM lane quarter in
-//              each, so a thread owns query row r (TMEM lane r) on 64 keys of the pair.  Each warp
-//              issues the tensor-memory loads of the next job before it computes the current one
-//              (two register buffers in turn), so the loads land while it computes.  Pass 1 keeps
-//              its causal row maximum and sum over its keys in the log2 domain; the two groups
-//              merge into the row log-sum-exp once.  Pass 2 turns the S row into probabilities
-//              2^(s scale - lse) and sums them over the rows (the page's k-major loop order, the
-//              transpose done in registers): a butterfly across the warp's 32 lanes leaves lane l
-//              with the sum of key l over its 32 rows, per 32-key chunk, and the four lane
-//              quarters' sums are added in shared memory in a fixed order by whichever of the
-//              group's four warps finishes the job last (a counter per group and ring slot), so
-//              no warp waits for another.  Three slots suffice: a warp can start job j + 2 only
-//              after the MMA of job j + 2, which waits for every warp to have read job j from
-//              TMEM, and it cannot load job j + 3 before every warp has read job j + 1, which each
-//              does after finishing job j.
+//   warps 2-17 four column groups of 32 keys (warps 2-5, 6-9, 10-13, 14-17), one warp per TMEM
+//              lane quarter in each, so a thread owns query row r (TMEM lane r) on 32 keys of the
+//              pair.  Pass 1 keeps its causal row maximum and sum over its keys in the log2
+//              domain; the four groups merge into the row log-sum-exp once.  Pass 2 turns the S
+//              row into probabilities 2^(s scale - lse) and sums them over the rows (the page's
+//              k-major loop order, the transpose done in registers): a butterfly across the
+//              warp's 32 lanes leaves lane l with the sum of key l over its 32 rows, and the four
+//              lane quarters' sums are added in shared memory in a fixed order by whichever of
+//              the group's four warps finishes the job last (a counter per group and ring slot),
+//              so no warp waits for another.  Three ring slots suffice: a warp can only start job
+//              j + 3 after the MMA of job j + 3, which waits for every warp to have read job
+//              j + 1 from TMEM, i.e. to have finished job j.
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -46,9 +43,9 @@ namespace {
 
 constexpr int kCM = 128;                    // tile rows: the window's query rows
 constexpr int kCStages = 4;
-constexpr int kCThreads = 320;
-constexpr int kMathThreads = 256;
-constexpr int kGroups = 2;                  // column groups of 64 keys in a page pair
+constexpr int kCThreads = 576;
+constexpr int kMathThreads = 512;
+constexpr int kGroups = 4;                  // column groups of 32 keys in a page pair
 constexpr int kBox = 64 * 128;              // one page's 64 rows x 128 B (one d-half)
 constexpr int kGBox = 2 * kBox;             // two pages' rows of one d-half
 constexpr int kCStageBytes = 2 * kGBox;     // K half 0, K half 1 of a page pair
@@ -63,7 +60,7 @@ struct ColSmem {
   uint32_t tmem_base;
   float ml[kGroups][2][kCM];                // pass 1 -> 2: (max, sum) of each column group per row
   float part[3][4][kCM];                    // pass 2: column sums of each lane quarter (32 rows), 3 slots
-  int cnt[3][kGroups];                      // pass 2: warps of a group done with a slot (of 4)
+  int cnt[3][kGroups];                      // pass 2: warps of a group done with a slot
 };
 
 constexpr size_t kColSmem = 1024 + kQBytes + size_t(kCStages) * kCStageBytes + sizeof(ColSmem);
@@ -210,14 +207,11 @@ __global__ void __launch_bounds__(kCThreads, 1)
     if (!warp_wait(&S.drain, 0) && lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
   } else {
     // ================================================================ math warps
-    // Warp w (2..9) owns TMEM lane quarter w % 4 (query rows 32 (w % 4) ..) and column group
-    // grp = (w - 2) / 4 (keys 64 grp .. 64 grp + 63 of the pair, two 32-key chunks).  The loads of
-    // job j + 1 are issued before job j is computed, so they land while it is.
     const int quarter = warp & 3;
-    const int grp = (warp - 2) >> 2;
+    const int grp = (warp - 2) >> 2;                 // column group: keys 32 grp .. 32 grp + 31 of the pair
     const int r = quarter * 32 + lane;               // TMEM lane: query row r
-    const int t = (warp - 2) * 32 + lane;            // 0 .. 255
-    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + 64 * grp;
+    const int t = (warp - 2) * 32 + lane;            // 0 .. 511
+    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + 32 * grp;
     const float scale = p.scale_log2;
     const int row_min = n - p.alpha + row0;          // position of the chunk's first row
     const int row_pos = row_min + r;                 // position of query row r
@@ -226,34 +220,49 @@ __global__ void __launch_bounds__(kCThreads, 1)
       lse2 = p.lse_in[(int64_t(b) * p.alpha + row0 + r) * p.Hq + hq] * 1.4426950408889634f;
     bool ok = true;
     float* srow = p.scores + (int64_t(b) * p.Hq + hq) * (int64_t(p.np_max) * kPageTokens);
-    uint32_t bufX[32], bufY[32];
-
-    // the pass-1 -> pass-2 switch: publish this group's (max, sum) and take every group's
-    auto to_pass2 = [&]() -> bool {
-      S.ml[grp][0][r] = m;
-      S.ml[grp][1][r] = l;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.mlready);
-      if (!warp_wait(&S.mlready, 0)) return false;
-      float mm = -CUDART_INF_F;
-#pragma unroll
-      for (int q = 0; q < kGroups; ++q) mm = fmaxf(mm, S.ml[q][0][r]);
-      float ll = 0.f;
-#pragma unroll
-      for (int q = 0; q < kGroups; ++q) {
-        const float mq = S.ml[q][0][r];
-        ll += mq == -CUDART_INF_F ? 0.f : S.ml[q][1][r] * fast_exp2(mq - mm);
+    for (int j = 0; j < n_jobs; ++j) {
+      const int g = j % ng, bb = j & 1;
+      const bool pass2 = j >= p1;
+      const int key0 = 2 * g * kPageTokens + 32 * grp;   // position of this warp's first key
+      const bool live = key0 < n;                        // the pair's tail may lie past the prompt
+      if (p1 > 0 && j == p1) {                           // pass 1 done: publish this group's (max, sum)
+        S.ml[grp][0][r] = m;
+        S.ml[grp][1][r] = l;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.mlready);
       }
-      lse2 = (r < rows && ll > 0.f) ? mm + log2f(ll) : CUDART_INF_F;
-      return true;
-    };
-    // chunk h (32 keys) of job j, its S values in sv
-    auto chunk = [&](int j, int h, const uint32_t (&sv)[32]) {
-      const int key0 = 2 * (j % ng) * kPageTokens + 64 * grp + 32 * h;   // this chunk's first key
-      if (key0 >= n) return;                                           // the pair's tail past the prompt
-      // every row of the chunk sees every key of these 32 (all but the causal tail)
+      // warps meet only through mbarriers, whose waits are bounded: a warp that gives up leaves alone
+      bool got = warp_wait(&S.dfull[bb], (j >> 1) & 1);
+      if (p1 > 0 && j == p1) got = warp_wait(&S.mlready, 0) && got;
+      if (!got) {
+        ok = false;
+        break;
+      }
+      if (p1 > 0 && j == p1) {
+        float mm = -CUDART_INF_F;
+#pragma unroll
+        for (int q = 0; q < kGroups; ++q) mm = fmaxf(mm, S.ml[q][0][r]);
+        float ll = 0.f;
+#pragma unroll
+        for (int q = 0; q < kGroups; ++q) {
+          const float mq = S.ml[q][0][r];
+          ll += mq == -CUDART_INF_F ? 0.f : S.ml[q][1][r] * fast_exp2(mq - mm);
+        }
+        lse2 = (r < rows && ll > 0.f) ? mm + log2f(ll) : CUDART_INF_F;
+      }
+      tc_fence_after();
+      uint32_t sv[32];
+      if (live) {
+        tmem_ld32(lane_addr + 128 * bb, sv);
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.dfree[bb]);        // this warp's TMEM reads are done
+      // every row of the chunk sees every key of this group (all but the causal tail)
       const bool full = key0 + 32 <= min(n, row_min + 1);
-      if (j < p1) {
+      if (!pass2) {
+        if (!live) continue;
         // the row maximum over the visible keys first (raw S; scale > 0), then the sum
         float mx4[4];
 #pragma unroll
@@ -271,7 +280,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
         }
         const float mb = scale * fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         const float m_new = fmaxf(m, mb);
-        if (m_new == -CUDART_INF_F) return;            // nothing visible yet
+        if (m_new == -CUDART_INF_F) continue;          // nothing visible yet
         float ls4[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) ls4[k] = 0.f;
@@ -297,103 +306,59 @@ __global__ void __launch_bounds__(kCThreads, 1)
         // row r's probabilities of these keys, summed over the warp's 32 rows by a butterfly:
         // each step keeps half of the columns (the half named by one lane bit) and adds the
         // partner lane's copy of them, so after five steps lane l holds key key0 + l
-        float v[32];                                     // rows past the chunk have lse2 = +inf
-        if (full) {
+        if (live) {
+          float v[32];                                     // rows past the chunk have lse2 = +inf
+          if (full) {
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {   // column pairs in packed f32x2 form
-            float e0, e1;
-            fma_f32x2(e0, e1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), scale, scale, -lse2, -lse2);
-            v[c] = fast_exp2(e0);
-            v[c + 1] = fast_exp2(e1);
+            for (int c = 0; c < 32; c += 2) {   // column pairs in packed f32x2 form
+              float e0, e1;
+              fma_f32x2(e0, e1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), scale, scale, -lse2, -lse2);
+              v[c] = fast_exp2(e0);
+              v[c + 1] = fast_exp2(e1);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const int key = key0 + c;
+              const bool vis = key < n && key <= row_pos;
+              const float e = fast_exp2(fmaf(__uint_as_float(sv[c]), scale, -lse2));
+              v[c] = vis ? e : 0.f;
+            }
           }
-        } else {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int key = key0 + c;
-            const bool vis = key < n && key <= row_pos;
-            const float e = fast_exp2(fmaf(__uint_as_float(sv[c]), scale, -lse2));
-            v[c] = vis ? e : 0.f;
+          for (int w = 16; w >= 1; w >>= 1) {              // w = values kept after this step
+            const bool hi = (lane & w) != 0;
+#pragma unroll
+            for (int k = 0; k < w; ++k) {
+              const float send = hi ? v[k] : v[k + w];
+              const float keep = hi ? v[k + w] : v[k];
+              v[k] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+            }
           }
-        }
-#pragma unroll
-        for (int w = 16; w >= 1; w >>= 1) {              // w = values kept after this step
-          const bool hi = (lane & w) != 0;
-#pragma unroll
-          for (int k = 0; k < w; ++k) {
-            const float send = hi ? v[k] : v[k + w];
-            const float keep = hi ? v[k + w] : v[k];
-            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+          const int slot = j % 3;
+          S.part[slot][quarter][32 * grp + lane] = v[0];
+          __syncwarp();
+          int last = 0;
+          if (lane == 0) {
+            __threadfence_block();                       // the partial sums before the count
+            last = atomicAdd(&S.cnt[slot][grp], 1) == 3;
           }
-        }
-        S.part[j % 3][quarter][64 * grp + 32 * h + lane] = v[0];
-      }
-    };
-    // pass 2, end of job j: the group's last warp to finish adds the four quarters of its 64 keys
-    auto finish_job = [&](int j) {
-      const int slot = j % 3;
-      __syncwarp();
-      int last = 0;
-      if (lane == 0) {
-        __threadfence_block();                         // the partial sums before the count
-        last = atomicAdd(&S.cnt[slot][grp], 1) == 3;
-      }
-      if (__shfl_sync(0xffffffffu, last, 0)) {
-        __threadfence_block();
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int cc = 64 * grp + 32 * h + lane;
-          const float sum = (S.part[slot][0][cc] + S.part[slot][1][cc]) + (S.part[slot][2][cc] + S.part[slot][3][cc]);
-          const int key = 2 * (j % ng) * kPageTokens + cc;   // keys from n on are zeroed below
-          if (key < n) {
-            if (in_grid) atomicAdd(&srow[key], sum);
-            else srow[key] = p.accumulate ? srow[key] + sum : sum;
+          if (__shfl_sync(0xffffffffu, last, 0)) {      // the group's last warp adds the four quarters
+            __threadfence_block();
+            const int cc = 32 * grp + lane;
+            const float sum = (S.part[slot][0][cc] + S.part[slot][1][cc]) + (S.part[slot][2][cc] + S.part[slot][3][cc]);
+            const int key = key0 + lane;                 // keys from n on are zeroed below
+            if (key < n) {
+              if (in_grid) atomicAdd(&srow[key], sum);
+              else srow[key] = p.accumulate ? srow[key] + sum : sum;
+            }
+            __syncwarp();
+            if (lane == 0) S.cnt[slot][grp] = 0;        // reused three jobs later
           }
         }
-        __syncwarp();
-        if (lane == 0) S.cnt[slot][grp] = 0;          // reused three jobs later
-      }
-    };
-    // tensor-memory load of chunk h of job j (issued; tmem_wait_ld makes it usable)
-    auto load = [&](int j, int h, uint32_t (&sv)[32]) {
-      tc_fence_after();
-      tmem_ld32(lane_addr + 128 * (j & 1) + 32 * h, sv);
-    };
-
-    // software pipeline over 32-key chunks, two register buffers in turn: the next chunk loads
-    // while the current one is computed (chunk 1 of a job during chunk 0, chunk 0 of the next job
-    // during chunk 1).  A warp can be at most two jobs ahead of the slowest warp of its group (the
-    // MMA of job j + 2 waits for every warp to have read job j), so three partial-sum slots suffice.
-    if (n_jobs > 0) {
-      ok = warp_wait(&S.dfull[0], 0);
-      if (ok) {
-        load(0, 0, bufX);
-        tmem_wait_ld();
       }
     }
-    for (int j = 0; j < n_jobs && ok; ++j) {
-      if (p1 > 0 && j == p1 && !to_pass2()) {
-        ok = false;
-        break;
-      }
-      load(j, 1, bufY);
-      chunk(j, 0, bufX);
-      tmem_wait_ld();                                  // both chunks of job j are in registers
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.dfree[j & 1]);     // its TMEM buffer goes back to the MMA thread
-      const bool more = j + 1 < n_jobs;
-      if (more) {
-        if (!warp_wait(&S.dfull[(j + 1) & 1], ((j + 1) >> 1) & 1)) ok = false;
-        else load(j + 1, 0, bufX);
-      }
-      chunk(j, 1, bufY);
-      if (j >= p1) finish_job(j);
-      if (more && ok) tmem_wait_ld();
-    }
-    if (!ok) {
-      tmem_wait_ld();                                  // no load of this warp may still be in flight
-      if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
-    }
+    if (!ok && lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
     // positions from the prompt's end on (all of them for a rejected request) are zero
     if (!p.accumulate && !in_grid)
       for (int i = (valid_req ? n : 0) + t; i < p.np_max * kPageTokens; i += kMathThreads) srow[i] = 0.f;

@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(Cfg<DOCS>::kThreads, 1)
             StageMeta m;
             m.unit = job;
             m.valid = bv;
-            m.rel = 0;
+            m.rel = xb + i;           // the page's index within the job
             m.ustart = 0;
             m.ucount = npg;
             m.chunk = 0;
@@ -660,8 +660,148 @@ __global__ void __launch_bounds__(Cfg<DOCS>::kThreads, 1)
     ++n_flush;
   };
 
-  reset_state();
   const uint32_t stage0 = smem_u32(stages);
+  if (DOCS) {
+    // Document-major consumers take a job's pages two at a time (the last of an odd count alone,
+    // its partner then the same stage with no valid token): one row max, one correction exp and
+    // one rescale of O per 32 keys, and four independent Q.K^T chains and eight P.V chains.  The
+    // job's query offsets are fixed, so its rotated query is formed once, at the job's start.
+    reset_state();
+    int cur_job = -1;
+    int jl = 0;
+    const int krow = t0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int vrow = t0 + (lane & 7) + ((lane >> 4) & 1) * 8;
+    const int vsel = (lane >> 3) & 1;
+    for (;;) {
+      const int s = jl % STAGES;
+      if (!__all_sync(0xffffffffu, mbar_wait(&S.full[s], (jl / STAGES) & 1, p.wait_ns))) {
+        if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
+        break;
+      }
+      const StageMeta mt = S.meta[s];
+      if (mt.unit == kEnd) break;
+      if (mt.unit != cur_job) {
+        if (cur_job >= 0) flush(cur_job, 0, 0, 0, 0);
+        cur_job = mt.unit;
+        reset_state();
+        load_q(stages + size_t(s) * kStage + kKVBytes, mt.pad0);
+        col_rel[0] = S.srel[s][grp_row + r];
+        rotate_q(col_rel);
+      }
+      const bool two = mt.rel + 1 < mt.ucount;   // the producer streams a job's pages in order
+      const int s2 = two ? (jl + 1) % STAGES : s;
+      int v2 = 0;
+      if (two) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&S.full[s2], ((jl + 1) / STAGES) & 1, p.wait_ns))) {
+          if (lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
+          break;
+        }
+        v2 = S.meta[s2].valid;
+      }
+      const int vld[2] = {mt.valid, v2};
+      if (vld[0] > t0 || vld[1] > t0) {
+        const uint32_t kb[2] = {stage0 + s * kStage, stage0 + s2 * kStage};
+        // ---- S^T = K q^T for my 16 keys of both pages (even / odd k-steps in separate chains)
+        float acc[2][2][4];
+#pragma unroll
+        for (int pg = 0; pg < 2; ++pg)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[pg][h][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+          for (int pg = 0; pg < 2; ++pg) {
+            uint32_t a[4];
+            ldsm_x4(swz(kb[pg], krow, 2 * ks + (lane >> 4)), a);
+            mma_bf16_16816(acc[pg][ks & 1], a, qh[ks][0][0], qh[ks][0][1]);
+            mma_bf16_16816(acc[pg][ks & 1], a, ql[LAZY && !PACK ? ks : 0][0][0],
+                           ql[LAZY && !PACK ? ks : 0][0][1]);
+          }
+        }
+        // ---- online softmax (log2 domain) over the 32 keys
+        float sv[2][4];
+#pragma unroll
+        for (int pg = 0; pg < 2; ++pg) {
+          const bool ok0 = t0 + r < vld[pg], ok1 = t0 + r + 8 < vld[pg];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float x = (acc[pg][0][e] + acc[pg][1][e]) * scale;
+            sv[pg][e] = (e < 2 ? ok0 : ok1) ? x : -CUDART_INF_F;
+          }
+        }
+        float pv[2][4];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          float mx = fmaxf(fmaxf(sv[0][cc], sv[0][cc + 2]), fmaxf(sv[1][cc], sv[1][cc + 2]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float mnew = fmaxf(m[0][cc], mx);   // finite: key t0 of one page is valid
+          const float alpha = exp2f(m[0][cc] - mnew);
+          m[0][cc] = mnew;
+#pragma unroll
+          for (int pg = 0; pg < 2; ++pg) {
+            pv[pg][cc] = exp2f(sv[pg][cc] - mnew);
+            pv[pg][cc + 2] = exp2f(sv[pg][cc + 2] - mnew);
+          }
+          lsum[0][cc] = lsum[0][cc] * alpha + ((pv[0][cc] + pv[0][cc + 2]) + (pv[1][cc] + pv[1][cc + 2]));
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            O[j][0][cc] *= alpha;
+            O[j][0][cc + 2] *= alpha;
+          }
+        }
+        uint32_t bh[2][2], bl[2][2];
+#pragma unroll
+        for (int pg = 0; pg < 2; ++pg) {
+          float h0, l0, h1, l1, h2, l2, h3, l3;
+          split_bf16(pv[pg][0], h0, l0);
+          split_bf16(pv[pg][1], h1, l1);
+          split_bf16(pv[pg][2], h2, l2);
+          split_bf16(pv[pg][3], h3, l3);
+          bh[pg][0] = movmatrix_trans(pack_bf16x2(h0, h1));
+          bh[pg][1] = movmatrix_trans(pack_bf16x2(h2, h3));
+          bl[pg][0] = movmatrix_trans(pack_bf16x2(l0, l1));
+          bl[pg][1] = movmatrix_trans(pack_bf16x2(l2, l3));
+        }
+        // ---- O^T += V^T P^T for my 16 keys of both pages (rows past the valid count masked:
+        // their P is 0, but the page image may hold any bits there)
+        uint32_t mlo[2], mhi[2];
+#pragma unroll
+        for (int pg = 0; pg < 2; ++pg) {
+          const int ta = t0 + 2 * c, tb = t0 + 8 + 2 * c;
+          mlo[pg] = (ta < vld[pg] ? 0x0000FFFFu : 0u) | (ta + 1 < vld[pg] ? 0xFFFF0000u : 0u);
+          mhi[pg] = (tb < vld[pg] ? 0x0000FFFFu : 0u) | (tb + 1 < vld[pg] ? 0xFFFF0000u : 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+#pragma unroll
+          for (int pg = 0; pg < 2; ++pg) {
+            uint32_t a[4];
+            ldsm_x4_trans(swz(kb[pg] + 2 * kBoxBytes, vrow, 2 * j + vsel), a);
+            a[0] &= mlo[pg];
+            a[1] &= mlo[pg];
+            a[2] &= mhi[pg];
+            a[3] &= mhi[pg];
+            mma_bf16_16816(O[j][0], a, bh[pg][0], bh[pg][1]);
+            mma_bf16_16816(O[j][0], a, bl[pg][0], bl[pg][1]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&S.empty[s]);
+        if (two) mbar_arrive(&S.empty[s2]);
+      }
+      jl += two ? 2 : 1;
+    }
+    flush(cur_job, 0, 0, 0, 1);
+    return;
+  }
+
+  reset_state();
   for (int jl = 0;; ++jl) {
     const int s = jl % STAGES;
     if (!__all_sync(0xffffffffu, mbar_wait(&S.full[s], (jl / STAGES) & 1, p.wait_ns))) {

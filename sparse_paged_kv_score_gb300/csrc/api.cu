@@ -50,6 +50,21 @@ bool encode_pool(CUtensorMap* m, void* base, int64_t n_page_heads) {
   return r == CUDA_SUCCESS;
 }
 
+// Window rows [B][alpha][Hq][128] bf16 as a 4-D tensor (d, hq, row, b); box 64 x 1 x 256 x 1 with
+// 128-byte swizzle (one box is 256 rows of one head's 64-dim half, rows past alpha read as zero).
+bool encode_rows(CUtensorMap* m, const void* q, int B, int alpha, int Hq) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {128, static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(alpha), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {256, static_cast<cuuint64_t>(Hq) * 256, static_cast<cuuint64_t>(alpha) * Hq * 256};
+  cuuint32_t box[4] = {64, 1, 256, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int check_group(spkv_cache_t c, int B, int Hq) {
   if (!c || B < 0 || Hq <= 0) return SPKV_EINVAL;
   const int Hk = c->d.n_kv_heads;
@@ -426,6 +441,23 @@ static int column_scores(spkv_cache_t c, const void* q, const float* lse_in, int
   p.lse_in = lse_in;
   p.scale_log2 = static_cast<float>(1.4426950408889634074 / std::sqrt(128.0));
   p.err = c->dev_err;
+  // Given LSE: the keys-as-M kernel, 256 window rows per launch (later launches add in order).
+  // The tile table of a launch lives in shared memory and counts tiles in 32 bits.
+  if (lse_in && B <= spkv::colscore_lse_max_requests() &&
+      int64_t(B) * Hq * ((int64_t(np_max) + 1) / 2) < (int64_t(1) << 31)) {
+    CUtensorMap tmq;
+    if (!encode_rows(&tmq, q, B, alpha, Hq)) return SPKV_ECUDA;
+    const int64_t tiles = int64_t(B) * Hq * ((int64_t(np_max) + 1) / 2);
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tiles, c->sm_count)));
+    for (int r0 = 0; r0 < alpha; r0 += 256) {
+      p.row0 = r0;
+      p.rows = std::min(256, alpha - r0);
+      p.accumulate = r0 > 0;
+      const int st = status_of(spkv::launch_colscore_lse(c, p, tmq, grid, as_stream(stream)));
+      if (st != SPKV_OK) return st;
+    }
+    return SPKV_OK;
+  }
   // each row's softmax is its own, so the column sums of 128-row chunks of the window add.  Two
   // chunks run in one grid, adding atomically onto a zeroed result (two addends onto zero give
   // the same sum in either order); more run as one launch per chunk, later ones adding in order.

@@ -372,10 +372,411 @@ __global__ void __launch_bounds__(kCThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Given-LSE form with the product turned around: S^T = K Q^T, the keys of a page pair as M (128
+// TMEM lanes) and up to 256 window rows as N (TMEM columns).  A thread then owns one key and sums
+// its probabilities over the rows in its own registers: per score one fused multiply-add, one exp2
+// and one add, with no cross-lane reduction.  Both operands are the same K-major 128-byte-swizzled
+// tiles as above, K from the paged pool by TMA and the window rows by one 4-D TMA load per
+// (request, query head).  Every MMA is M 128 x N 256 (a pair with one page leaves lanes 64..127
+// holding keys past the prompt, which are never read).
+//
+// Persistent: the (request, query head, page pair) tiles of all requests form one sequence (a
+// table of per-request tile offsets in shared memory); CTA c takes a contiguous range of it, so
+// the query heads of one kv head (the same pages) run side by side on neighbouring CTAs.  A tile's
+// column sums are complete within the CTA (all the launch's rows are in one N 256 tile): plain
+// stores, no atomics, bit-reproducible.  Eighteen warps:
+//   warp 0     TMA producer: the page pairs into a 4-stage ring; each (request, head)'s rows' LSE
+//              (log2 domain) into one of two shared buffers;
+//   warp 1     MMA issuer: loads the window rows of each (request, head) once every MMA reading
+//              the previous ones has completed, then 8 MMAs per pair into one of two 256-column
+//              TMEM accumulators;
+//   warps 2-9  four lane quarters (32 keys) x two column groups (128 rows): each thread loads its
+//              key's 128 scores from TMEM at once (freeing the accumulator early), sums them over
+//              the rows; the two groups' sums meet in shared memory and the quarter's last warp to
+//              finish adds them in a fixed order and stores the key's score.  (Ten warps: a thread
+//              may hold 168 registers, enough for the 128 loaded scores.)
+constexpr int kTRows = 256;                       // window rows per launch (N)
+constexpr int kTStages = 4;
+constexpr int kTThreads = 320;
+constexpr int kTMathWarps = 8;
+constexpr int kTMaxB = 4096;                      // requests per launch (the tile table)
+constexpr int kTQBytes = 2 * kTRows * 128;        // the rows' two 64-dim halves
+constexpr uint32_t kTTmemCols = 512;              // two 256-column accumulators
+
+struct ColTSmem {
+  uint64_t full[kTStages], empty[kTStages];
+  uint64_t dfull[2], dfree[2];
+  uint64_t qfull, qfree;
+  uint64_t lfull[2], lfree[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int scan[kTThreads / 32];
+  alignas(16) float lse[2][kTRows];               // log2-domain LSE of each row, +inf past the chunk (read as float4)
+  float part[3][2][128];                          // [slot][column group][key of the pair]
+  int cnt[3][4];                                  // [slot][lane quarter]: column groups done
+  int tile_pre[kTMaxB + 1];                       // Hq x (page pairs of the requests before b)
+};
+
+constexpr size_t kColTSmem = 1024 + kTQBytes + size_t(kTStages) * kCStageBytes + sizeof(ColTSmem);
+static_assert(kColTSmem <= 232448, "column-score (given LSE) shared memory exceeds the per-CTA limit");
+static_assert(offsetof(ColTSmem, lse) % 16 == 0, "the LSE rows are read as 16-byte vectors");
+
+// Position in the tile sequence: request b, query head hq, pair g of the request's tb pairs.
+struct TileWalk {
+  int b = 0, hq = 0, g = 0, tb = 0;
+  __device__ void start(const int* pre, int B, int Hq, int x) {
+    int lo = 0, hi = B;                           // the last b with pre[b] <= x (then pre[b + 1] > x)
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (pre[mid] <= x) lo = mid;
+      else hi = mid;
+    }
+    b = lo;
+    tb = (pre[b + 1] - pre[b]) / Hq;
+    const int off = x - pre[b];
+    hq = off / tb;
+    g = off % tb;
+  }
+  __device__ void next(const int* pre, int B, int Hq) {
+    if (++g < tb) return;
+    g = 0;
+    if (++hq < Hq) return;
+    hq = 0;
+    do {
+      ++b;
+    } while (b < B && pre[b + 1] == pre[b]);
+    tb = b < B ? (pre[b + 1] - pre[b]) / Hq : 0;
+  }
+};
+
+__device__ __forceinline__ int request_pairs(const ColScoreParams& p, int b) {
+  const int n = p.seq_len[b];
+  if (n < p.alpha || n > p.np_max * kPageTokens) return 0;
+  return ((n + kPageTokens - 1) / kPageTokens + 1) / 2;
+}
+
+// Sum over 32 rows (columns cb .. cb + 31 of this thread's key) of 2^(s scale - lse), rows before
+// `thr` excluded (they precede the key).
+__device__ __forceinline__ float key_rows_sum(const uint32_t (&sv)[32], const float* lse, int cb, int thr,
+                                              float scale) {
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  if (thr <= cb) {
+#pragma unroll
+    for (int c = 0; c < 32; c += 4) {
+      const float4 l = *reinterpret_cast<const float4*>(lse + cb + c);
+      float e0, e1, e2, e3;
+      fma_f32x2(e0, e1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), scale, scale, -l.x, -l.y);
+      fma_f32x2(e2, e3, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]), scale, scale, -l.z, -l.w);
+      add_f32x2(a0, a1, fast_exp2(e0), fast_exp2(e1));
+      add_f32x2(a2, a3, fast_exp2(e2), fast_exp2(e3));
+    }
+  } else if (thr < cb + 32) {
+#pragma unroll
+    for (int c = 0; c < 32; c += 4) {
+      const float4 l = *reinterpret_cast<const float4*>(lse + cb + c);
+      const float lv[4] = {l.x, l.y, l.z, l.w};
+      float e[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        e[i] = cb + c + i >= thr ? fast_exp2(fmaf(__uint_as_float(sv[c + i]), scale, -lv[i])) : 0.f;
+      add_f32x2(a0, a1, e[0], e[1]);
+      add_f32x2(a2, a3, e[2], e[3]);
+    }
+  }
+  return (a0 + a1) + (a2 + a3);
+}
+
+__global__ void __launch_bounds__(kTThreads, 1)
+    colscore_lse_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
+                        const __grid_constant__ ColScoreParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = base;
+  uint8_t* stages = base + kTQBytes;
+  ColTSmem& S = *reinterpret_cast<ColTSmem*>(stages + kTStages * kCStageBytes);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < kTStages; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.dfull[i], 1);
+      mbar_init(&S.dfree[i], kTMathWarps);
+      mbar_init(&S.lfull[i], 32);
+      mbar_init(&S.lfree[i], kTMathWarps);
+    }
+    mbar_init(&S.qfull, 1);
+    mbar_init(&S.qfree, 1);
+    mbar_init(&S.drain, 1);
+    for (int i = 0; i < 3 * 4; ++i) (&S.cnt[0][0])[i] = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmq);
+  }
+  if (warp == 1) {
+    tmem_alloc(&S.tmem_base, kTTmemCols);
+    tmem_relinquish();
+  }
+  pdl_wait();
+  // tile table: tile_pre[b] = Hq x (page pairs of requests 0 .. b - 1), one slice of requests per thread
+  {
+    const int per = (p.B + kTThreads - 1) / kTThreads;
+    const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
+    int sum = 0;
+    for (int b = b0; b < b1; ++b) {
+      const int t = request_pairs(p, b);
+      if (t == 0 && blockIdx.x == 0) flag_error(p.err, SPKV_DEVERR_PAGE_ID);
+      sum += p.Hq * t;
+    }
+    int x = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) S.scan[warp] = x;
+    __syncthreads();
+    int wbase = 0;
+    for (int w = 0; w < warp; ++w) wbase += S.scan[w];
+    int acc = wbase + x - sum;
+    for (int b = b0; b < b1; ++b) {
+      S.tile_pre[b] = acc;
+      acc += p.Hq * request_pairs(p, b);
+    }
+    if (tid == kTThreads - 1) S.tile_pre[p.B] = wbase + x;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = S.tmem_base;
+  const int X = S.tile_pre[p.B];
+  const int x0 = static_cast<int>(int64_t(blockIdx.x) * X / gridDim.x);
+  const int x1 = static_cast<int>(int64_t(blockIdx.x + 1) * X / gridDim.x);
+  const int njobs = x1 - x0;
+
+  if (warp == 0) {
+    // ================================================================ TMA producer
+    const uint64_t pol = l2_policy_evict_last();   // the kv head's other query heads read the same pages
+    TileWalk w;
+    if (njobs > 0) w.start(S.tile_pre, p.B, p.Hq, x0);
+    int k = -1, j = 0, np_b = 0;
+    bool ok = true;
+    for (; j < njobs; ++j, w.next(S.tile_pre, p.B, p.Hq)) {
+      if (j == 0 || w.g == 0) {
+        ++k;
+        np_b = (p.seq_len[w.b] + kPageTokens - 1) / kPageTokens;
+        if (k >= 2 && !warp_wait(&S.lfree[k & 1], ((k - 2) >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        for (int i = lane; i < kTRows; i += 32)
+          S.lse[k & 1][i] = i < p.rows ? p.lse_in[(int64_t(w.b) * p.alpha + p.row0 + i) * p.Hq + w.hq] *
+                                             1.4426950408889634f
+                                       : CUDART_INF_F;
+        mbar_arrive(&S.lfull[k & 1]);
+      }
+      const int s = j % kTStages;
+      if (j >= kTStages && !warp_wait(&S.empty[s], ((j / kTStages) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        uint32_t bytes = 0;
+        int ph[2] = {-1, -1};
+        for (int q = 0; q < 2; ++q) {
+          const int pg = 2 * w.g + q;
+          if (pg >= np_b) continue;
+          const int v = p.page_table[int64_t(w.b) * p.np_max + pg];
+          if (v < 0 || v >= p.n_phys) {
+            flag_error(p.err, SPKV_DEVERR_PHYS);
+            continue;
+          }
+          ph[q] = v;
+          bytes += 2 * kBox;
+        }
+        uint8_t* st = stages + s * kCStageBytes;
+        const int h = w.hq / p.G;
+        if (bytes) {
+          mbar_arrive_expect_tx(&S.full[s], bytes);
+          for (int q = 0; q < 2; ++q) {
+            if (ph[q] < 0) continue;
+            const int z = static_cast<int>(int64_t(h) * p.n_phys + ph[q]);
+            tma_load_3d(st + q * kBox, &tmk, &S.full[s], 0, 0, z, pol);
+            tma_load_3d(st + kGBox + q * kBox, &tmk, &S.full[s], 64, 0, z, pol);
+          }
+        } else {
+          mbar_arrive(&S.full[s]);
+        }
+      }
+      __syncwarp();
+    }
+    if (!ok && lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
+    for (int i = j > kTStages ? j - kTStages : 0; i < j; ++i) mbar_wait(&S.full[i % kTStages], (i / kTStages) & 1);
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    constexpr uint32_t kId = umma_idesc_bf16(128, kTRows, false);   // M = keys, N = rows
+    const uint64_t q_desc = umma_desc_sw128(smem_u32(sQ), 16, 1024);
+    const uint64_t k_desc = umma_desc_sw128(smem_u32(stages), 16, 1024);
+    const uint64_t qpol = l2_policy_evict_first();
+    TileWalk w;
+    if (njobs > 0) w.start(S.tile_pre, p.B, p.Hq, x0);
+    int k = -1;
+    bool ok = true, q_pending = false;
+    for (int j = 0; j < njobs && ok; ++j, w.next(S.tile_pre, p.B, p.Hq)) {
+      if (j == 0 || w.g == 0) {
+        ++k;
+        if (k >= 1) {   // every MMA reading the previous rows completes before they are replaced
+          if (lane == 0) umma_commit(&S.qfree);
+          __syncwarp();
+          if (!warp_wait(&S.qfree, (k - 1) & 1)) {
+            ok = false;
+            break;
+          }
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&S.qfull, kTQBytes);
+          tma_load_4d(sQ, &tmq, &S.qfull, 0, w.hq, p.row0, w.b, qpol);
+          tma_load_4d(sQ + kTQBytes / 2, &tmq, &S.qfull, 64, w.hq, p.row0, w.b, qpol);
+        }
+        q_pending = true;
+        __syncwarp();
+        if (!warp_wait(&S.qfull, k & 1)) {
+          ok = false;
+          break;
+        }
+        q_pending = false;
+      }
+      const int s = j % kTStages, bb = j & 1;
+      if (!warp_wait(&S.full[s], (j / kTStages) & 1)) ok = false;
+      else if (j >= 2 && !warp_wait(&S.dfree[bb], ((j - 2) >> 1) & 1)) ok = false;
+      if (!ok) break;
+      if (lane == 0) {
+        tc_fence_after();
+        const uint64_t ka = k_desc + ((s * kCStageBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ko = ka + (((kk >> 2) * kGBox + (kk & 3) * 32) >> 4);
+          const uint64_t qo = q_desc + (((kk >> 2) * (kTQBytes / 2) + (kk & 3) * 32) >> 4);
+          umma_bf16(tbase + kTRows * bb, ko, qo, kId, kk > 0);   // S^T = K Q^T
+        }
+        umma_commit(&S.empty[s]);
+        umma_commit(&S.dfull[bb]);
+      }
+      __syncwarp();
+    }
+    if (!ok && lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
+    if (q_pending) mbar_wait(&S.qfull, k & 1);     // a row copy in flight lands before the CTA leaves
+    if (lane == 0) umma_commit(&S.drain);
+    __syncwarp();
+    if (!warp_wait(&S.drain, 0) && lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
+  } else {
+    // ================================================================ math warps
+    const int quarter = warp & 3;                  // TMEM lanes 32 quarter .. (keys of the pair)
+    const int grp = (warp - 2) >> 2;               // rows 128 grp .. 128 grp + 127
+    const int kt = 32 * quarter + lane;            // this thread's key within the pair
+    const int cb = 128 * grp;
+    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + cb;
+    const float scale = p.scale_log2;
+    const int nq = min(4, max(0, (p.rows - cb + 31) / 32));   // 32-column quarters holding rows of this launch
+    TileWalk w;
+    if (njobs > 0) w.start(S.tile_pre, p.B, p.Hq, x0);
+    int k = -1, n = 0, first_pos = 0;
+    float* srow = p.scores;
+    bool ok = true;
+    for (int j = 0; j < njobs; ++j, w.next(S.tile_pre, p.B, p.Hq)) {
+      if (j == 0 || w.g == 0) {
+        if (k >= 0) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.lfree[k & 1]);
+        }
+        ++k;
+        if (!warp_wait(&S.lfull[k & 1], (k >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        n = p.seq_len[w.b];
+        first_pos = n - p.alpha + p.row0;           // position of the launch's first row
+        srow = p.scores + (int64_t(w.b) * p.Hq + w.hq) * (int64_t(p.np_max) * kPageTokens);
+      }
+      const int bb = j & 1;
+      if (!warp_wait(&S.dfull[bb], (j >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sv[4][32];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (i < nq) tmem_ld32(lane_addr + kTRows * bb + 32 * i, sv[i]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.dfree[bb]);   // this warp's TMEM reads are done
+      const int key = 2 * w.g * kPageTokens + kt;
+      float sum = 0.f;
+      if (key < n) {
+        const int thr = key - first_pos;           // rows before thr precede the key
+        const float* lse = S.lse[k & 1];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (i < nq) sum += key_rows_sum(sv[i], lse, cb + 32 * i, thr, scale);
+      }
+      const int slot = j % 3;
+      S.part[slot][grp][kt] = sum;
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) {
+        __threadfence_block();                     // the partial sums before the count
+        last = atomicAdd(&S.cnt[slot][quarter], 1) == 1;
+      }
+      if (__shfl_sync(0xffffffffu, last, 0)) {    // the quarter's last group adds the two in order
+        __threadfence_block();
+        const float tot = S.part[slot][0][kt] + S.part[slot][1][kt];
+        if (key < n) srow[key] = p.accumulate ? srow[key] + tot : tot;
+        else if (!p.accumulate && key < p.np_max * kPageTokens) srow[key] = 0.f;
+        __syncwarp();
+        if (lane == 0) S.cnt[slot][quarter] = 0;  // reused three pairs later
+      }
+    }
+    if (!ok && lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
+    // positions past each (request, head)'s last pair (all of a rejected request's) are zero
+    if (!p.accumulate) {
+      const int t = tid - 64;
+      for (int u = blockIdx.x; u < p.B * p.Hq; u += gridDim.x) {
+        const int b = u / p.Hq;
+        const int from = 2 * kPageTokens * ((S.tile_pre[b + 1] - S.tile_pre[b]) / p.Hq);
+        float* row = p.scores + int64_t(u) * (int64_t(p.np_max) * kPageTokens);
+        for (int i = from + t; i < p.np_max * kPageTokens; i += kTMathWarps * 32) row[i] = 0.f;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTTmemCols);
+  }
+}
+
 }  // namespace
 
 cudaError_t colscore_init_attributes() {
-  return cudaFuncSetAttribute(colscore_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kColSmem));
+  cudaError_t e = cudaFuncSetAttribute(colscore_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kColSmem));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(colscore_lse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kColTSmem));
+}
+
+int colscore_lse_max_requests() { return kTMaxB; }
+
+cudaError_t launch_colscore_lse(const spkv_cache* c, const ColScoreParams& p, const CUtensorMap& tmq, int grid,
+                                cudaStream_t st) {
+  return launch_pdl(colscore_lse_kernel, dim3(grid), dim3(kTThreads), kColTSmem, st, c->tmap_k, tmq, p);
 }
 
 cudaError_t launch_colscore(const spkv_cache* c, const ColScoreParams& p, cudaStream_t st) {

@@ -141,7 +141,8 @@ struct ColScoreParams {
   const uint16_t* q;             // bf16 [B][alpha][Hq][128]: the last alpha rows of each prompt
   float* scores;                 // [B][Hq][np_max * 64]
   int B, alpha, Hq, Hk, G;
-  int row0, rows;                // this launch's chunk: window rows row0 .. row0 + rows - 1 (rows <= 128)
+  int row0, rows;                // this launch's chunk: window rows row0 .. row0 + rows - 1 (rows <= 128;
+                                 // <= 256 in the given-LSE kernel)
   int accumulate;                // 0: write the chunk's sums (first chunk), 1: add them
   int chunks_in_grid;            // 2: blockIdx.z is the chunk (rows 128 z ..), sums added atomically
                                  // onto a zeroed row (two addends onto zero: order-independent)
@@ -202,6 +203,12 @@ cudaError_t fused_init_attributes();
 cudaError_t prefill_init_attributes();
 cudaError_t colscore_init_attributes();
 cudaError_t launch_colscore(const spkv_cache* c, const ColScoreParams& p, cudaStream_t st);
+// Given-LSE column scores, keys as M: rows row0 .. row0 + rows - 1 (rows <= 256) of the window,
+// tmq the window rows [B][alpha][Hq][128] as a 4-D tensor (d, hq, row, b), box 64 x 1 x 256 x 1,
+// 128-byte swizzle; grid persistent CTAs.  At most colscore_lse_max_requests() requests.
+int colscore_lse_max_requests();
+cudaError_t launch_colscore_lse(const spkv_cache* c, const ColScoreParams& p, const CUtensorMap& tmq, int grid,
+                                cudaStream_t st);
 cudaError_t launch_prefill(const spkv_cache* c, const PrefillParams& p, cudaStream_t st);
 
 }  // namespace spkv

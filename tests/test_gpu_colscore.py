@@ -177,3 +177,58 @@ def test_column_scores_lse_argument_checks():
                                     torch.cuda.current_stream().cuda_stream)
     assert st == -1
     d.close()
+
+
+def test_column_scores_lse_ragged_rejected_and_reproducible():
+    """The keys-as-M form over a ragged batch: prompts of different lengths (tile counts), one shorter
+    than the window (rejected: error bit, zero row), persistent CTAs whose tile ranges cut through
+    (request, head) pairs; repeated calls agree bit for bit, and every valid row matches the oracle."""
+    w = gen.sparse_workload(5, 8, 2, 64 * 11, 4, 4, seed=41)
+    alpha = 40
+    seq = np.array([64 * 6, 64 * 2 + 5, 20, 64 * 11, 64 * 3], np.int32)
+    q = gen.rows_bf16(41, 327, 5 * alpha * 8).reshape(5, alpha, 8, 128)
+    wl = dict(w, seq_len=np.where(seq >= alpha, seq, alpha).astype(np.int32))
+    lse = _window_lse(wl, q)
+    lse[2] = 0.0
+    d = Dev(w)
+    outs = []
+    for _ in range(2):
+        out = torch.full((5, 8, w["np_max"] * 64), float("nan"), dtype=torch.float32, device=DEV)
+        spkv.attn_column_scores_lse(d.cache, bf(q), torch.from_numpy(lse).to(DEV), d.pt, i32(seq), out)
+        outs.append(out.cpu().numpy())
+    st, bits = d.errors()
+    d.close()
+    assert bits == spkv.DEVERR["PAGE_ID"]
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    S = outs[0]
+    assert (S[2] == 0).all()
+    keep = np.array([0, 1, 3, 4])
+    ref = oracle.column_scores_given_lse_batch(q[keep], lse[keep].astype(np.float64), w["k_pool"],
+                                               w["page_table"][keep], seq[keep], w["np_max"] * 64)
+    for i, b in enumerate(keep):
+        for hq in range(8):
+            _check(S[b, hq], ref[i, hq], alpha, int(seq[b]))
+
+
+def test_column_scores_lse_beyond_the_tile_table():
+    """More requests than the keys-as-M form's tile table holds (4096): the call runs the row-major
+    kernel's probability pass instead, with the same results."""
+    B, alpha = 4100, 4
+    w = gen.sparse_workload(B, 4, 1, 64 + 9, 2, 2, seed=43)
+    q = gen.rows_bf16(43, 328, B * alpha * 4).reshape(B, alpha, 4, 128)
+    items = np.array([0, 4 * 4095 + 1, 4 * 4099 + 3], np.int32)
+    lse = np.zeros((B, alpha, 4), np.float32)
+    sub = np.array([0, 4095, 4099])
+    wl = dict(w, seq_len=w["seq_len"][sub], page_table=w["page_table"][sub])
+    lse[sub] = _window_lse(wl, q[sub])
+    d = Dev(w)
+    out = torch.full((B, 4, w["np_max"] * 64), float("nan"), dtype=torch.float32, device=DEV)
+    spkv.attn_column_scores_lse(d.cache, bf(q), torch.from_numpy(lse).to(DEV), d.pt, i32(w["seq_len"]), out)
+    S = out.cpu().numpy()
+    assert d.errors() == (0, 0)
+    d.close()
+    ref = oracle.column_scores_given_lse_batch(q, lse.astype(np.float64), w["k_pool"], w["page_table"],
+                                               w["seq_len"], w["np_max"] * 64, items=items)
+    for it in items:
+        b, hq = divmod(int(it), 4)
+        _check(S[b, hq], ref[b, hq], alpha, int(w["seq_len"][b]))

@@ -391,11 +391,11 @@ __global__ void __launch_bounds__(kCThreads, 1)
 //   warp 1     MMA issuer: loads the window rows of each (request, head) once every MMA reading
 //              the previous ones has completed, then 8 MMAs per pair into one of two 256-column
 //              TMEM accumulators;
-//   warps 2-9  four lane quarters (32 keys) x two column groups (128 rows): each thread loads its
-//              key's 128 scores from TMEM at once (freeing the accumulator early), sums them over
-//              the rows; the two groups' sums meet in shared memory and the quarter's last warp to
-//              finish adds them in a fixed order and stores the key's score.  (Ten warps: a thread
-//              may hold 168 registers, enough for the 128 loaded scores.)
+//   warps 2-9  two groups of four warps (one per TMEM lane quarter: 32 keys), group q taking the
+//              pairs j with j % 2 == q (accumulator q): a thread reads its key's scores for all
+//              the launch's rows, 64 columns at a time, and sums them in a fixed order, so the two
+//              warps on each SM sub-partition work on different pairs (one loads while the other
+//              computes) and every key's score is complete in one thread.
 constexpr int kTRows = 256;                       // window rows per launch (N)
 constexpr int kTStages = 4;
 constexpr int kTThreads = 320;
@@ -413,8 +413,6 @@ struct ColTSmem {
   uint32_t tmem_base;
   int scan[kTThreads / 32];
   alignas(16) float lse[2][kTRows];               // log2-domain LSE of each row, +inf past the chunk (read as float4)
-  float part[3][2][128];                          // [slot][column group][key of the pair]
-  int cnt[3][4];                                  // [slot][lane quarter]: column groups done
   int tile_pre[kTMaxB + 1];                       // Hq x (page pairs of the requests before b)
 };
 
@@ -504,14 +502,13 @@ __global__ void __launch_bounds__(kTThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S.dfull[i], 1);
-      mbar_init(&S.dfree[i], kTMathWarps);
+      mbar_init(&S.dfree[i], kTMathWarps / 2);   // the four warps of group i
       mbar_init(&S.lfull[i], 32);
       mbar_init(&S.lfree[i], kTMathWarps);
     }
     mbar_init(&S.qfull, 1);
     mbar_init(&S.qfree, 1);
     mbar_init(&S.drain, 1);
-    for (int i = 0; i < 3 * 4; ++i) (&S.cnt[0][0])[i] = 0;
     fence_mbar_init();
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmq);
@@ -675,19 +672,18 @@ __global__ void __launch_bounds__(kTThreads, 1)
   } else {
     // ================================================================ math warps
     const int quarter = warp & 3;                  // TMEM lanes 32 quarter .. (keys of the pair)
-    const int grp = (warp - 2) >> 2;               // rows 128 grp .. 128 grp + 127
+    const int grp = (warp - 2) >> 2;               // pairs j with j % 2 == grp (accumulator grp)
     const int kt = 32 * quarter + lane;            // this thread's key within the pair
-    const int cb = 128 * grp;
-    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + cb;
+    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + kTRows * grp;
     const float scale = p.scale_log2;
-    const int nq = min(4, max(0, (p.rows - cb + 31) / 32));   // 32-column quarters holding rows of this launch
+    const int rounds = (p.rows + 63) / 64;         // 64-column rounds holding rows of this launch
     TileWalk w;
     if (njobs > 0) w.start(S.tile_pre, p.B, p.Hq, x0);
     int k = -1, n = 0, first_pos = 0;
     float* srow = p.scores;
     bool ok = true;
     for (int j = 0; j < njobs; ++j, w.next(S.tile_pre, p.B, p.Hq)) {
-      if (j == 0 || w.g == 0) {
+      if (j == 0 || w.g == 0) {                    // every warp follows every (request, head) switch
         if (k >= 0) {
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.lfree[k & 1]);
@@ -701,45 +697,33 @@ __global__ void __launch_bounds__(kTThreads, 1)
         first_pos = n - p.alpha + p.row0;           // position of the launch's first row
         srow = p.scores + (int64_t(w.b) * p.Hq + w.hq) * (int64_t(p.np_max) * kPageTokens);
       }
-      const int bb = j & 1;
-      if (!warp_wait(&S.dfull[bb], (j >> 1) & 1)) {
+      if ((j & 1) != grp) continue;
+      if (!warp_wait(&S.dfull[grp], (j >> 1) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sv[4][32];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (i < nq) tmem_ld32(lane_addr + kTRows * bb + 32 * i, sv[i]);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.dfree[bb]);   // this warp's TMEM reads are done
       const int key = 2 * w.g * kPageTokens + kt;
+      const int thr = key - first_pos;             // rows before thr precede the key
+      const float* lse = S.lse[k & 1];
       float sum = 0.f;
-      if (key < n) {
-        const int thr = key - first_pos;           // rows before thr precede the key
-        const float* lse = S.lse[k & 1];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (i < nq) sum += key_rows_sum(sv[i], lse, cb + 32 * i, thr, scale);
+      for (int rd = 0; rd < rounds; ++rd) {
+        uint32_t sv[2][32];
+        tmem_ld32(lane_addr + 64 * rd, sv[0]);
+        tmem_ld32(lane_addr + 64 * rd + 32, sv[1]);
+        tmem_wait_ld();
+        if (rd == rounds - 1) {                    // this warp's last read of the accumulator
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.dfree[grp]);
+        }
+        if (key < n) {
+          sum += key_rows_sum(sv[0], lse, 64 * rd, thr, scale);
+          sum += key_rows_sum(sv[1], lse, 64 * rd + 32, thr, scale);
+        }
       }
-      const int slot = j % 3;
-      S.part[slot][grp][kt] = sum;
-      __syncwarp();
-      int last = 0;
-      if (lane == 0) {
-        __threadfence_block();                     // the partial sums before the count
-        last = atomicAdd(&S.cnt[slot][quarter], 1) == 1;
-      }
-      if (__shfl_sync(0xffffffffu, last, 0)) {    // the quarter's last group adds the two in order
-        __threadfence_block();
-        const float tot = S.part[slot][0][kt] + S.part[slot][1][kt];
-        if (key < n) srow[key] = p.accumulate ? srow[key] + tot : tot;
-        else if (!p.accumulate && key < p.np_max * kPageTokens) srow[key] = 0.f;
-        __syncwarp();
-        if (lane == 0) S.cnt[slot][quarter] = 0;  // reused three pairs later
-      }
+      if (key < n) srow[key] = p.accumulate ? srow[key] + sum : sum;
+      else if (!p.accumulate && key < p.np_max * kPageTokens) srow[key] = 0.f;
     }
     if (!ok && lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
     // positions past each (request, head)'s last pair (all of a rejected request's) are zero

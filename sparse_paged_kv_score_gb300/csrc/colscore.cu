@@ -398,8 +398,9 @@ __global__ void __launch_bounds__(kCThreads, 1)
 //              computes) and every key's score is complete in one thread.
 constexpr int kTRows = 256;                       // window rows per launch (N)
 constexpr int kTStages = 4;
-constexpr int kTThreads = 320;
-constexpr int kTMathWarps = 8;
+constexpr int kTThreads = 576;
+constexpr int kTMathWarps = 16;
+constexpr int kRoundCols = 32;                    // TMEM columns a math thread reads per wait
 constexpr int kTMaxB = 4096;                      // requests per launch (the tile table)
 constexpr int kTQBytes = 2 * kTRows * 128;        // the rows' two 64-dim halves
 constexpr uint32_t kTTmemCols = 512;              // two 256-column accumulators
@@ -413,6 +414,8 @@ struct ColTSmem {
   uint32_t tmem_base;
   int scan[kTThreads / 32];
   alignas(16) float lse[2][kTRows];               // log2-domain LSE of each row, +inf past the chunk (read as float4)
+  float part[2][3][2][128];                       // [group][slot][row half][key]: each half's sums
+  int cnt[2][3][4];                               // [group][slot][lane quarter]: halves done
   int tile_pre[kTMaxB + 1];                       // Hq x (page pairs of the requests before b)
 };
 
@@ -502,13 +505,14 @@ __global__ void __launch_bounds__(kTThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S.dfull[i], 1);
-      mbar_init(&S.dfree[i], kTMathWarps / 2);   // the four warps of group i
+      mbar_init(&S.dfree[i], kTMathWarps / 2);   // the eight warps of group i
       mbar_init(&S.lfull[i], 32);
       mbar_init(&S.lfree[i], kTMathWarps);
     }
     mbar_init(&S.qfull, 1);
     mbar_init(&S.qfree, 1);
     mbar_init(&S.drain, 1);
+    for (int i = 0; i < 2 * 3 * 4; ++i) (&S.cnt[0][0][0])[i] = 0;
     fence_mbar_init();
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmq);
@@ -671,12 +675,15 @@ __global__ void __launch_bounds__(kTThreads, 1)
     if (!warp_wait(&S.drain, 0) && lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
   } else {
     // ================================================================ math warps
+    const int mw = warp - 2;                       // 0 .. 15
     const int quarter = warp & 3;                  // TMEM lanes 32 quarter .. (keys of the pair)
-    const int grp = (warp - 2) >> 2;               // pairs j with j % 2 == grp (accumulator grp)
+    const int grp = mw >> 3;                       // pairs j with j % 2 == grp (accumulator grp)
+    const int half = (mw >> 2) & 1;                // rows 128 half .. 128 half + 127
     const int kt = 32 * quarter + lane;            // this thread's key within the pair
-    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + kTRows * grp;
+    const int cb = 128 * half;
+    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + kTRows * grp + cb;
     const float scale = p.scale_log2;
-    const int rounds = (p.rows + 63) / 64;         // 64-column rounds holding rows of this launch
+    const int rounds = min(128, max(0, p.rows - cb) + kRoundCols - 1) / kRoundCols;   // rounds holding rows
     TileWalk w;
     if (njobs > 0) w.start(S.tile_pre, p.B, p.Hq, x0);
     int k = -1, n = 0, first_pos = 0;
@@ -707,10 +714,15 @@ __global__ void __launch_bounds__(kTThreads, 1)
       const int thr = key - first_pos;             // rows before thr precede the key
       const float* lse = S.lse[k & 1];
       float sum = 0.f;
+      if (rounds == 0) {                           // no rows of this launch in this half
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.dfree[grp]);
+      }
       for (int rd = 0; rd < rounds; ++rd) {
-        uint32_t sv[2][32];
-        tmem_ld32(lane_addr + 64 * rd, sv[0]);
-        tmem_ld32(lane_addr + 64 * rd + 32, sv[1]);
+        uint32_t sv[kRoundCols / 32][32];
+#pragma unroll
+        for (int i = 0; i < kRoundCols / 32; ++i) tmem_ld32(lane_addr + kRoundCols * rd + 32 * i, sv[i]);
         tmem_wait_ld();
         if (rd == rounds - 1) {                    // this warp's last read of the accumulator
           tc_fence_before();
@@ -718,12 +730,28 @@ __global__ void __launch_bounds__(kTThreads, 1)
           if (lane == 0) mbar_arrive(&S.dfree[grp]);
         }
         if (key < n) {
-          sum += key_rows_sum(sv[0], lse, 64 * rd, thr, scale);
-          sum += key_rows_sum(sv[1], lse, 64 * rd + 32, thr, scale);
+#pragma unroll
+          for (int i = 0; i < kRoundCols / 32; ++i) sum += key_rows_sum(sv[i], lse, cb + kRoundCols * rd + 32 * i, thr, scale);
         }
       }
-      if (key < n) srow[key] = p.accumulate ? srow[key] + sum : sum;
-      else if (!p.accumulate && key < p.np_max * kPageTokens) srow[key] = 0.f;
+      // the two halves' sums of a key meet in shared memory; the second to arrive adds them in
+      // order and stores the score
+      const int slot = (j >> 1) % 3;
+      S.part[grp][slot][half][kt] = sum;
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) {
+        __threadfence_block();                     // the partial sums before the count
+        last = atomicAdd(&S.cnt[grp][slot][quarter], 1) == 1;
+      }
+      if (__shfl_sync(0xffffffffu, last, 0)) {
+        __threadfence_block();
+        const float tot = S.part[grp][slot][0][kt] + S.part[grp][slot][1][kt];
+        if (key < n) srow[key] = p.accumulate ? srow[key] + tot : tot;
+        else if (!p.accumulate && key < p.np_max * kPageTokens) srow[key] = 0.f;
+        __syncwarp();
+        if (lane == 0) S.cnt[grp][slot][quarter] = 0;   // reused three of the group's pairs later
+      }
     }
     if (!ok && lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
     // positions past each (request, head)'s last pair (all of a rejected request's) are zero

@@ -384,18 +384,20 @@ __global__ void __launch_bounds__(kCThreads, 1)
 // Persistent: the (request, query head, page pair) tiles of all requests form one sequence (a
 // table of per-request tile offsets in shared memory); CTA c takes a contiguous range of it, so
 // the query heads of one kv head (the same pages) run side by side on neighbouring CTAs.  A tile's
-// column sums are complete within the CTA (all the launch's rows are in one N 256 tile): plain
-// stores, no atomics, bit-reproducible.  Eighteen warps:
+// column sums are complete within the CTA (all the launch's rows are in one N 256 tile): the
+// scores are plain stores (no atomic adds), bit-reproducible.  Eighteen warps:
 //   warp 0     TMA producer: the page pairs into a 4-stage ring; each (request, head)'s rows' LSE
 //              (log2 domain) into one of two shared buffers;
 //   warp 1     MMA issuer: loads the window rows of each (request, head) once every MMA reading
 //              the previous ones has completed, then 8 MMAs per pair into one of two 256-column
 //              TMEM accumulators;
-//   warps 2-9  two groups of four warps (one per TMEM lane quarter: 32 keys), group q taking the
-//              pairs j with j % 2 == q (accumulator q): a thread reads its key's scores for all
-//              the launch's rows, 64 columns at a time, and sums them in a fixed order, so the two
-//              warps on each SM sub-partition work on different pairs (one loads while the other
-//              computes) and every key's score is complete in one thread.
+//   warps 2-17 two groups of eight, group q taking the pairs j with j % 2 == q (accumulator q),
+//              each group one warp per (TMEM lane quarter: 32 keys, half of the rows: 128): a
+//              thread reads its key's scores for its rows 32 columns at a time and sums them in a
+//              fixed order; the two halves' sums meet in shared memory and the second to finish
+//              adds them.  Four warps share each SM sub-partition, on two pairs in different
+//              phases, so one computes while another waits for its tensor-memory load (a warp's
+//              wait covers all its outstanding loads, so it cannot overlap its own).
 constexpr int kTRows = 256;                       // window rows per launch (N)
 constexpr int kTStages = 4;
 constexpr int kTThreads = 576;

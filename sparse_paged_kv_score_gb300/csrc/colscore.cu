@@ -451,6 +451,10 @@ struct TileWalk {
     } while (b < B && pre[b + 1] == pre[b]);
     tb = b < B ? (pre[b + 1] - pre[b]) / Hq : 0;
   }
+  // The page pair of step g: odd query heads take the request's pairs last to first, so a CTA that
+  // moves on to the next head of the same kv head starts on the pages it read most recently (still
+  // in L2).
+  __device__ int pair() const { return (hq & 1) ? tb - 1 - g : g; }
 };
 
 __device__ __forceinline__ int request_pairs(const ColScoreParams& p, int b) {
@@ -590,7 +594,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
         uint32_t bytes = 0;
         int ph[2] = {-1, -1};
         for (int q = 0; q < 2; ++q) {
-          const int pg = 2 * w.g + q;
+          const int pg = 2 * w.pair() + q;
           if (pg >= np_b) continue;
           const int v = p.page_table[int64_t(w.b) * p.np_max + pg];
           if (v < 0 || v >= p.n_phys) {
@@ -712,7 +716,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
         break;
       }
       tc_fence_after();
-      const int key = 2 * w.g * kPageTokens + kt;
+      const int key = 2 * w.pair() * kPageTokens + kt;
       const int thr = key - first_pos;             // rows before thr precede the key
       const float* lse = S.lse[k & 1];
       float sum = 0.f;

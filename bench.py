@@ -1124,15 +1124,16 @@ def run_native(args):
         if st_c != 0:
             raise RuntimeError(f"device error bits {bits_c} in the column-score leg")
         ctf_l = cflops / (coll_ms * 1e-3) / 1e12
-        colsc = {"kernel": "attn_column_scores (colscore_kernel: tcgen05.mma, TMA pages, two passes)",
+        colsc = {"kernel": "attn_column_scores (colscore_kernel pass 1: each row's LSE; colscore_lse_kernel: the "
+                           "probabilities with keys as M; tcgen05.mma, TMA pages)",
                  "workload": f"{Bc} prompts x {nc} tokens, window of the last {ac} rows, Hq {Hq} / Hk {Hk}",
                  "us": col_ms * 1e3, "flops": cflops,
                  "flops_def": "2 * 128 * window rows * prompt tokens * Hq * prompts (one Q K^T pass)",
                  "bound": "tensor", "achieved_TFLOPs": ctf,
                  "peak": tpeak, "peak_kind": tkind + " bf16 dense (cuBLAS burst)", "frac": ctf / tpeak,
                  "prompts_per_s": Bc / (col_ms * 1e-3),
-                 "launches": "one memset and one kernel (both 128-row chunks of the window in one grid)",
-                 "given_lse": {"kernel": "attn_column_scores_lse (the probability pass alone)",
+                 "launches": "two kernels (the LSE of both 128-row chunks in one grid, then the probability pass)",
+                 "given_lse": {"kernel": "attn_column_scores_lse (colscore_lse_kernel: the probability pass alone)",
                                "us": coll_ms * 1e3, "achieved_TFLOPs": ctf_l, "frac": ctf_l / tpeak}}
         ccache.close()
         del ck, cq, cs, csl, lse_in

@@ -333,10 +333,15 @@ int lazy_alibi_prefill_attn(spkv_cache_t cache, const void* q, int B, int T, int
  *   page_table : device int32 [B][np_max];  seq_len: device int32 [B] (alpha <= n <= 64 np_max,
  *                else SPKV_DEVERR_PAGE_ID and the row is zeros)
  *   scores     : device fp32 [B][Hq][64 np_max] (output)
- * alpha <= 1024 (else SPKV_EUNSUPPORTED).  The window runs in 128-row chunks whose column sums
- * add: up to 256 rows, both chunks in one grid adding atomically onto a zeroed scores buffer (two
- * addends onto zero give the same sum in either order, so results are reproducible); more rows,
- * one launch per chunk, later chunks adding in order.
+ * alpha <= 1024 (else SPKV_EUNSUPPORTED).  Two launches: the first computes each window row's
+ * log-sum-exp into the handle's split-K workspace (128-row chunks in one grid), the second the
+ * probabilities with a page pair's keys as the MMA's M and up to 256 window rows as N, each key's
+ * sum over the rows formed by one thread in a fixed order (results are reproducible); windows of
+ * more than 256 rows add later 256-row launches in order.  Past 4096 requests, or when the
+ * workspace cannot hold B * alpha * Hq values, one launch runs both passes with the rows as M
+ * (128-row chunks whose column sums add: up to 256 rows, both chunks in one grid adding atomically
+ * onto a zeroed scores buffer, two addends onto zero giving the same sum in either order; more
+ * rows, one launch per chunk, adding in order).
  * B, Hq <= 65535. */
 int attn_column_scores(spkv_cache_t cache, const void* q, int B, int alpha, int Hq,
                        const int32_t* page_table, int np_max, const int32_t* seq_len,
@@ -345,7 +350,7 @@ int attn_column_scores(spkv_cache_t cache, const void* q, int B, int alpha, int 
 /* attn_column_scores with each window row's log-sum-exp supplied by the caller, as the
  * attention that already computed rowmax and l over the same keys returns it ([FA] "2. Attention
  * modification": the FlashAttention pass outputs rowmax and l, and the score adds only the
- * probability pass).  The kernel skips its first pass and computes
+ * probability pass).  Only the probability launch runs, and it computes
  *   scores[b][hq][i] = sum over rows j with i <= n - alpha + j of exp(q_j . k_i / sqrt(128) - lse[b][j][hq])
  * which equals attn_column_scores when lse is each row's own log-sum-exp over its visible keys.
  *   lse : device fp32 [B][alpha][Hq], natural log, finite (not checked)

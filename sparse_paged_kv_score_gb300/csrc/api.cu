@@ -441,12 +441,26 @@ static int column_scores(spkv_cache_t c, const void* q, const float* lse_in, int
   p.lse_in = lse_in;
   p.scale_log2 = static_cast<float>(1.4426950408889634074 / std::sqrt(128.0));
   p.err = c->dev_err;
-  // Given LSE: the keys-as-M kernel, 256 window rows per launch (later launches add in order).
-  // The tile table of a launch lives in shared memory and counts tiles in 32 bits.
-  if (lse_in && B <= spkv::colscore_lse_max_requests() &&
+  // The keys-as-M probability kernel, 256 window rows per launch (later launches add in order),
+  // from the caller's LSE or, without one, from a pass-1 launch of the row-major kernel that writes
+  // each row's log2-domain LSE into the handle's split-K workspace (one stream per handle).  The
+  // tile table of a launch lives in shared memory and counts tiles in 32 bits.
+  const bool ws_fits = int64_t(B) * alpha * Hq <= int64_t(16) * 128 * c->ws_slots;
+  if ((lse_in || ws_fits) && B <= spkv::colscore_lse_max_requests() &&
       int64_t(B) * Hq * ((int64_t(np_max) + 1) / 2) < (int64_t(1) << 31)) {
     CUtensorMap tmq;
     if (!encode_rows(&tmq, q, B, alpha, Hq)) return SPKV_ECUDA;
+    if (!lse_in) {
+      spkv::ColScoreParams p1 = p;
+      p1.lse_out = c->ws_o;
+      p1.row0 = 0;
+      p1.rows = std::min(128, alpha);
+      p1.chunks_in_grid = (alpha + 127) / 128;
+      const int st = status_of(spkv::launch_colscore(c, p1, as_stream(stream)));
+      if (st != SPKV_OK) return st;
+      p.lse_in = c->ws_o;
+      p.lse_is_log2 = 1;
+    }
     const int64_t tiles = int64_t(B) * Hq * ((int64_t(np_max) + 1) / 2);
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tiles, c->sm_count)));
     for (int r0 = 0; r0 < alpha; r0 += 256) {

@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
   // pass 1 (each row's maximum and sum), then pass 2 (the probabilities); with the rows'
   // log-sum-exp given by the caller, pass 2 alone
   const int p1 = p.lse_in ? 0 : ng;
-  const int n_jobs = p1 + ng;
+  const int n_jobs = p1 + (p.lse_out ? 0 : ng);   // lse_out: pass 1 alone
 
   if (warp == 0) {
     // ================================================================ TMA producer
@@ -220,6 +220,20 @@ __global__ void __launch_bounds__(kCThreads, 1)
       lse2 = p.lse_in[(int64_t(b) * p.alpha + row0 + r) * p.Hq + hq] * 1.4426950408889634f;
     bool ok = true;
     float* srow = p.scores + (int64_t(b) * p.Hq + hq) * (int64_t(p.np_max) * kPageTokens);
+    // the four groups' (max, sum) of row r merged into its log-sum-exp, log2 domain (+inf for rows
+    // past the chunk or with nothing visible)
+    auto merge_lse = [&]() -> float {
+      float mm = -CUDART_INF_F;
+#pragma unroll
+      for (int q = 0; q < kGroups; ++q) mm = fmaxf(mm, S.ml[q][0][r]);
+      float ll = 0.f;
+#pragma unroll
+      for (int q = 0; q < kGroups; ++q) {
+        const float mq = S.ml[q][0][r];
+        ll += mq == -CUDART_INF_F ? 0.f : S.ml[q][1][r] * fast_exp2(mq - mm);
+      }
+      return (r < rows && ll > 0.f) ? mm + log2f(ll) : CUDART_INF_F;
+    };
     for (int j = 0; j < n_jobs; ++j) {
       const int g = j % ng, bb = j & 1;
       const bool pass2 = j >= p1;
@@ -238,18 +252,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
         ok = false;
         break;
       }
-      if (p1 > 0 && j == p1) {
-        float mm = -CUDART_INF_F;
-#pragma unroll
-        for (int q = 0; q < kGroups; ++q) mm = fmaxf(mm, S.ml[q][0][r]);
-        float ll = 0.f;
-#pragma unroll
-        for (int q = 0; q < kGroups; ++q) {
-          const float mq = S.ml[q][0][r];
-          ll += mq == -CUDART_INF_F ? 0.f : S.ml[q][1][r] * fast_exp2(mq - mm);
-        }
-        lse2 = (r < rows && ll > 0.f) ? mm + log2f(ll) : CUDART_INF_F;
-      }
+      if (p1 > 0 && j == p1) lse2 = merge_lse();
       tc_fence_after();
       uint32_t sv[32];
       if (live) {
@@ -358,9 +361,18 @@ __global__ void __launch_bounds__(kCThreads, 1)
         }
       }
     }
+    if (p.lse_out) {
+      // pass 1 alone: each row's log-sum-exp (log2 domain) for a later probability pass
+      S.ml[grp][0][r] = m;
+      S.ml[grp][1][r] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.mlready);
+      if (!warp_wait(&S.mlready, 0)) ok = false;
+      else if (grp == 0 && r < rows) p.lse_out[(int64_t(b) * p.alpha + row0 + r) * p.Hq + hq] = merge_lse();
+    }
     if (!ok && lane == 0) flag_error(p.err, SPKV_DEVERR_TIMEOUT);
     // positions from the prompt's end on (all of them for a rejected request) are zero
-    if (!p.accumulate && !in_grid)
+    if (!p.accumulate && !in_grid && !p.lse_out)
       for (int i = (valid_req ? n : 0) + t; i < p.np_max * kPageTokens; i += kMathThreads) srow[i] = 0.f;
   }
 
@@ -581,7 +593,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
         }
         for (int i = lane; i < kTRows; i += 32)
           S.lse[k & 1][i] = i < p.rows ? p.lse_in[(int64_t(w.b) * p.alpha + p.row0 + i) * p.Hq + w.hq] *
-                                             1.4426950408889634f
+                                             (p.lse_is_log2 ? 1.f : 1.4426950408889634f)
                                        : CUDART_INF_F;
         mbar_arrive(&S.lfull[k & 1]);
       }

@@ -151,6 +151,8 @@ struct ColScoreParams {
   int np_max;
   const int32_t* seq_len;        // prompt length n per request
   const float* lse_in;           // [B][alpha][Hq] natural-log LSE of each window row, or null (pass 1 runs)
+  int lse_is_log2;               // lse_in holds log2-domain values (written by a pass-1 launch)
+  float* lse_out;                // colscore_kernel: pass 1 alone, each row's log2-domain LSE to [B][alpha][Hq]
   float scale_log2;
   uint32_t* err;
 };

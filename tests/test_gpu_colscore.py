@@ -211,8 +211,9 @@ def test_column_scores_lse_ragged_rejected_and_reproducible():
 
 
 def test_column_scores_lse_beyond_the_tile_table():
-    """More requests than the keys-as-M form's tile table holds (4096): the call runs the row-major
-    kernel's probability pass instead, with the same results."""
+    """More requests than the keys-as-M form's tile table holds (4096): both forms run the row-major
+    kernel instead (the given-LSE form its probability pass, the other both passes in one launch),
+    with the same results."""
     B, alpha = 4100, 4
     w = gen.sparse_workload(B, 4, 1, 64 + 9, 2, 2, seed=43)
     q = gen.rows_bf16(43, 328, B * alpha * 4).reshape(B, alpha, 4, 128)
@@ -224,11 +225,15 @@ def test_column_scores_lse_beyond_the_tile_table():
     d = Dev(w)
     out = torch.full((B, 4, w["np_max"] * 64), float("nan"), dtype=torch.float32, device=DEV)
     spkv.attn_column_scores_lse(d.cache, bf(q), torch.from_numpy(lse).to(DEV), d.pt, i32(w["seq_len"]), out)
-    S = out.cpu().numpy()
+    two = torch.full_like(out, float("nan"))
+    spkv.attn_column_scores(d.cache, bf(q), d.pt, i32(w["seq_len"]), two)
+    S, S2 = out.cpu().numpy(), two.cpu().numpy()
     assert d.errors() == (0, 0)
     d.close()
     ref = oracle.column_scores_given_lse_batch(q, lse.astype(np.float64), w["k_pool"], w["page_table"],
                                                w["seq_len"], w["np_max"] * 64, items=items)
+    ref2 = oracle.column_scores_batch(q, w["k_pool"], w["page_table"], w["seq_len"], w["np_max"] * 64, items=items)
     for it in items:
         b, hq = divmod(int(it), 4)
         _check(S[b, hq], ref[b, hq], alpha, int(w["seq_len"][b]))
+        _check(S2[b, hq], ref2[b, hq], alpha, int(w["seq_len"][b]))

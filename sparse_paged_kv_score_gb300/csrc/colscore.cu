@@ -50,11 +50,11 @@ constexpr int kBox = 64 * 128;              // one page's 64 rows x 128 B (one d
 constexpr int kGBox = 2 * kBox;             // two pages' rows of one d-half
 constexpr int kCStageBytes = 2 * kGBox;     // K half 0, K half 1 of a page pair
 constexpr int kQBytes = 2 * kCM * 128;
-constexpr uint32_t kTmemCols = 256;         // two 128-column buffers
+constexpr uint32_t kTmemCols = 512;         // two 128-column buffers (four in the LSE-only mode)
 
 struct ColSmem {
   uint64_t full[kCStages], empty[kCStages];
-  uint64_t dfull[2], dfree[2];
+  uint64_t dfull[4], dfree[4];
   uint64_t drain;
   uint64_t mlready;                         // every group's (max, sum) rows are published
   uint32_t tmem_base;
@@ -96,9 +96,10 @@ __global__ void __launch_bounds__(kCThreads, 1)
       mbar_init(&S.full[s], 1);
       mbar_init(&S.empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 4; ++i) {
       mbar_init(&S.dfull[i], 1);
-      mbar_init(&S.dfree[i], kMathThreads / 32);
+      // LSE-only mode: buffer i is read by the four warps of group i alone
+      mbar_init(&S.dfree[i], p.lse_out ? 4 : kMathThreads / 32);
     }
     mbar_init(&S.drain, 1);
     mbar_init(&S.mlready, kMathThreads / 32);
@@ -181,11 +182,12 @@ __global__ void __launch_bounds__(kCThreads, 1)
     const uint64_t q_desc = umma_desc_sw128(smem_u32(sQ), 16, 1024);
     const uint64_t k_desc = umma_desc_sw128(smem_u32(stages), 16, 1024);
     bool ok = true;
+    const int nbuf = p.lse_out ? 4 : 2;               // accumulators in rotation
     for (int j = 0; j < n_jobs && ok; ++j) {
-      const int s = j % kCStages, g = j % ng, bb = j & 1;
+      const int s = j % kCStages, g = j % ng, bb = j % nbuf;
       const int size = 2 * g + 1 < np_b ? 2 : 1;
       if (!warp_wait(&S.full[s], (j / kCStages) & 1)) ok = false;
-      else if (j >= 2 && !warp_wait(&S.dfree[bb], ((j - 2) >> 1) & 1)) ok = false;
+      else if (j >= nbuf && !warp_wait(&S.dfree[bb], ((j - nbuf) / nbuf) & 1)) ok = false;
       if (!ok) break;
       if (lane == 0) {
         tc_fence_after();
@@ -234,7 +236,82 @@ __global__ void __launch_bounds__(kCThreads, 1)
       }
       return (r < rows && ll > 0.f) ? mm + log2f(ll) : CUDART_INF_F;
     };
-    for (int j = 0; j < n_jobs; ++j) {
+    // One 32-key block of row r's scores (keys key0 ..) into its running maximum and sum (log2
+    // domain), visible keys only.
+    auto absorb = [&](const uint32_t (&sv)[32], int key0) {
+      const bool full = key0 + 32 <= min(n, row_min + 1);   // every row of the chunk sees them
+      // the row maximum over the visible keys first (raw S; scale > 0), then the sum
+      float mx4[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mx4[k] = -CUDART_INF_F;
+      if (full) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], __uint_as_float(sv[c]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int key = key0 + c;
+          const bool vis = key < n && key <= row_pos;
+          mx4[c & 3] = fmaxf(mx4[c & 3], vis ? __uint_as_float(sv[c]) : -CUDART_INF_F);
+        }
+      }
+      const float mb = scale * fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      const float m_new = fmaxf(m, mb);
+      if (m_new == -CUDART_INF_F) return;             // nothing visible yet
+      float ls4[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) ls4[k] = 0.f;
+      if (full) {
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {   // column pairs in packed f32x2 form
+          float e0, e1;
+          fma_f32x2(e0, e1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), scale, scale, -m_new, -m_new);
+          add_f32x2(ls4[c & 3], ls4[(c + 1) & 3], fast_exp2(e0), fast_exp2(e1));   // c even: neighbouring sums
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int key = key0 + c;
+          const bool vis = key < n && key <= row_pos;
+          ls4[c & 3] += vis ? fast_exp2(fmaf(__uint_as_float(sv[c]), scale, -m_new)) : 0.f;
+        }
+      }
+      l = l * fast_exp2(m - m_new) +                  // m = -inf gives 0
+          ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
+      m = m_new;
+    };
+    if (p.lse_out) {
+      // LSE-only: group grp takes the pairs j with j % 4 == grp (accumulator grp), a thread all 128
+      // keys of its row in each, 32 columns per tensor-memory wait, so the four groups work on
+      // different pairs (one warp's load overlaps another's arithmetic)
+      const uint32_t gaddr = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + 128 * grp;
+      for (int j = grp; j < n_jobs; j += 4) {
+        if (!warp_wait(&S.dfull[grp], (j >> 2) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int kb = 2 * j * kPageTokens;           // the pair's first key
+        const int rounds = min(4, max(0, (n - kb + 31) / 32));
+        if (rounds == 0) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.dfree[grp]);
+        }
+        for (int rd = 0; rd < rounds; ++rd) {
+          uint32_t sv[32];
+          tmem_ld32(gaddr + 32 * rd, sv);
+          tmem_wait_ld();
+          if (rd == rounds - 1) {                     // this warp's last read of the accumulator
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.dfree[grp]);
+          }
+          absorb(sv, kb + 32 * rd);
+        }
+      }
+    }
+    for (int j = 0; j < (p.lse_out ? 0 : n_jobs); ++j) {
       const int g = j % ng, bb = j & 1;
       const bool pass2 = j >= p1;
       const int key0 = 2 * g * kPageTokens + 32 * grp;   // position of this warp's first key
@@ -265,46 +342,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
       // every row of the chunk sees every key of this group (all but the causal tail)
       const bool full = key0 + 32 <= min(n, row_min + 1);
       if (!pass2) {
-        if (!live) continue;
-        // the row maximum over the visible keys first (raw S; scale > 0), then the sum
-        float mx4[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) mx4[k] = -CUDART_INF_F;
-        if (full) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], __uint_as_float(sv[c]));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int key = key0 + c;
-            const bool vis = key < n && key <= row_pos;
-            mx4[c & 3] = fmaxf(mx4[c & 3], vis ? __uint_as_float(sv[c]) : -CUDART_INF_F);
-          }
-        }
-        const float mb = scale * fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        const float m_new = fmaxf(m, mb);
-        if (m_new == -CUDART_INF_F) continue;          // nothing visible yet
-        float ls4[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) ls4[k] = 0.f;
-        if (full) {
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {   // column pairs in packed f32x2 form
-            float e0, e1;
-            fma_f32x2(e0, e1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), scale, scale, -m_new, -m_new);
-            add_f32x2(ls4[c & 3], ls4[(c + 1) & 3], fast_exp2(e0), fast_exp2(e1));   // c even: neighbouring sums
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int key = key0 + c;
-            const bool vis = key < n && key <= row_pos;
-            ls4[c & 3] += vis ? fast_exp2(fmaf(__uint_as_float(sv[c]), scale, -m_new)) : 0.f;
-          }
-        }
-        l = l * fast_exp2(m - m_new) +                  // m = -inf gives 0
-            ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
-        m = m_new;
+        if (live) absorb(sv, key0);
       } else {
         // row r's probabilities of these keys, summed over the warp's 32 rows by a butterfly:
         // each step keeps half of the columns (the half named by one lane bit) and adds the

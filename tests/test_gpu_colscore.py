@@ -42,7 +42,8 @@ def _check(S, ref, alpha, n):
 
 
 @pytest.mark.parametrize("n,alpha,Hq,Hk", [(200, 9, 8, 2), (64 * 5, 64, 8, 2), (64 * 7 + 13, 128, 16, 4),
-                                           (130, 1, 4, 1), (64 * 3, 128, 40, 8), (64 * 9 + 1, 100, 8, 8)])
+                                           (130, 1, 4, 1), (64 * 3, 128, 40, 8), (64 * 9 + 1, 100, 8, 8),
+                                           (128, 128, 8, 2), (200, 200, 8, 2)])
 def test_column_scores_vs_oracle(n, alpha, Hq, Hk):
     w = gen.sparse_workload(2, Hq, Hk, n, 4, 4, seed=n + alpha)
     q = gen.rows_bf16(n, 321, 2 * alpha * Hq).reshape(2, alpha, Hq, 128)
@@ -142,7 +143,8 @@ def _window_lse(w, q):
 
 
 @pytest.mark.parametrize("n,alpha,Hq,Hk", [(200, 9, 8, 2), (64 * 7 + 13, 128, 16, 4), (64 * 4 + 7, 129, 8, 2),
-                                           (64 * 6, 300, 8, 2), (5000, 256, 8, 2)])
+                                           (64 * 6, 300, 8, 2), (5000, 256, 8, 2), (256, 256, 8, 2),
+                                           (64 * 5 + 3, 64 * 5 + 3, 16, 4)])
 def test_column_scores_from_given_lse_vs_oracle(n, alpha, Hq, Hk):
     """The probability pass alone, from each row's LSE as an attention call would return it (fp32):
     against the oracle's given-LSE form on the same fp32 LSE, and against the two-pass GPU form."""

@@ -949,56 +949,57 @@ __global__ void __launch_bounds__(Cfg<DOCS>::kThreads, 1)
   flush(cur_u, cur_c, cur_us, cur_uc, 1);
 }
 
-// Merges the split-K partials of every unit that spans several segments: one CTA per unit,
-// one thread per (query head, output dimension); an online (max, sum) merge over batches of
-// eight partials keeps eight independent loads in flight per thread.  Also resets the chunk
-// counter for the next launch.
-constexpr int kCombineHeads = 4;   // query heads per combine CTA pass (4 x 128 threads)
+// Merges the split-K partials of every unit that spans several segments: one CTA per unit and
+// group of up to four query heads (a group of five or more heads spreads over several CTAs instead
+// of looping), one thread per (query head, output dimension); an online (max, sum) merge over
+// batches of eight partials keeps eight independent loads in flight per thread.  Also resets the
+// chunk counter for the next launch.
+constexpr int kCombineHeads = 4;   // query heads per combine CTA (4 x 128 threads)
+constexpr int kCombineBatch = 8;   // partials loaded per round
 
 __global__ void __launch_bounds__(kCombineHeads * kHeadDim)
     attn_combine_kernel(const __grid_constant__ AttnParams p) {
   pdl_wait();
   pdl_trigger();
   const int u = blockIdx.x, d = threadIdx.x % kHeadDim;
-  if (u == 0 && threadIdx.x == 0) p.ws_ctl[0] = 0;
+  if (u == 0 && blockIdx.y == 0 && threadIdx.x == 0) p.ws_ctl[0] = 0;
+  const int g = blockIdx.y * kCombineHeads + threadIdx.x / kHeadDim;
   const int first = p.ws_parts[2 * u], nparts = p.ws_parts[2 * u + 1];
-  if (nparts <= 1) return;
+  if (nparts <= 1 || g >= p.G) return;
   const int b = u / p.Hk, h = u % p.Hk;
   const int64_t orow = int64_t(b) * p.Hq + h * p.G;
-  for (int g = threadIdx.x / kHeadDim; g < p.G; g += kCombineHeads) {
-    float M = -CUDART_INF_F, L = 0.f, acc = 0.f;
-    for (int i0 = 0; i0 < nparts; i0 += 8) {
-      float mw[8], lw[8], ow[8];
+  float M = -CUDART_INF_F, L = 0.f, acc = 0.f;
+  for (int i0 = 0; i0 < nparts; i0 += kCombineBatch) {
+    float mw[kCombineBatch], lw[kCombineBatch], ow[kCombineBatch];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        if (i0 + q < nparts) {
-          const int64_t sl = int64_t(u) + first + i0 + q;
-          mw[q] = p.ws_m[sl * 16 + g];
-          lw[q] = p.ws_l[sl * 16 + g];
-          ow[q] = p.ws_o[(sl * 16 + g) * kHeadDim + d];
-        } else {
-          mw[q] = -CUDART_INF_F;
-          lw[q] = ow[q] = 0.f;
-        }
+    for (int q = 0; q < kCombineBatch; ++q) {
+      if (i0 + q < nparts) {
+        const int64_t sl = int64_t(u) + first + i0 + q;
+        mw[q] = p.ws_m[sl * 16 + g];
+        lw[q] = p.ws_l[sl * 16 + g];
+        ow[q] = p.ws_o[(sl * 16 + g) * kHeadDim + d];
+      } else {
+        mw[q] = -CUDART_INF_F;
+        lw[q] = ow[q] = 0.f;
       }
-      float mb = M;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) mb = fmaxf(mb, mw[q]);
-      if (mb == -CUDART_INF_F) continue;
-      const float r = exp2f(M - mb);     // M = -inf gives 0
-      L *= r;
-      acc *= r;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float f = mw[q] == -CUDART_INF_F ? 0.f : exp2f(mw[q] - mb);
-        L += f * lw[q];
-        acc += f * ow[q];
-      }
-      M = mb;
     }
-    p.out[(orow + g) * kHeadDim + d] = L > 0.f ? acc / L : 0.f;
-    if (d == 0) p.lse[orow + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
+    float mb = M;
+#pragma unroll
+    for (int q = 0; q < kCombineBatch; ++q) mb = fmaxf(mb, mw[q]);
+    if (mb == -CUDART_INF_F) continue;
+    const float r = exp2f(M - mb);     // M = -inf gives 0
+    L *= r;
+    acc *= r;
+#pragma unroll
+    for (int q = 0; q < kCombineBatch; ++q) {
+      const float f = mw[q] == -CUDART_INF_F ? 0.f : exp2f(mw[q] - mb);
+      L += f * lw[q];
+      acc += f * ow[q];
+    }
+    M = mb;
   }
+  p.out[(orow + g) * kHeadDim + d] = L > 0.f ? acc / L : 0.f;
+  if (d == 0) p.lse[orow + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
 }
 
 // Document-major form: merges, for each request and query head, the partials its documents' jobs
@@ -1058,7 +1059,8 @@ cudaError_t launch_one(const spkv_cache* c, const AttnParams& p, int grid, cudaS
   cudaError_t e = launch_pdl(attn_split_kernel<NT, LAZY, PACK, STAGES>, dim3(grid), dim3(kThreads),
                              smem_bytes<NT, STAGES>(), st, c->tmap_k, c->tmap_v, p);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_combine_kernel, dim3(p.B * p.Hk), dim3(kCombineHeads * kHeadDim), 0, st, p);
+  return launch_pdl(attn_combine_kernel, dim3(p.B * p.Hk, (p.G + kCombineHeads - 1) / kCombineHeads),
+                    dim3(kCombineHeads * kHeadDim), 0, st, p);
 }
 
 constexpr int kStages1 = 5;   // G <= 8: 5 stages of 34 KiB

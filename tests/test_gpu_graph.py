@@ -141,3 +141,55 @@ def test_bookkeeping_beside_attention_equals_fused_schedule():
     for st in (fused, eager, graphed):
         assert spkv.get_device_error(st.cache) == (0, 0)
         st.cache.close()
+
+
+def test_document_major_decode_and_column_scores_in_graphs():
+    """The document-major lazy decode (whose plan carries a job counter from call to call) and both
+    column-score forms (whose calls build a tensor map of the window rows on the host) captured as
+    CUDA graphs and replayed several times give bitwise what the eager calls give."""
+    from helpers import u32_as_i32
+    w = gen.lazy_rag(seed=21, B=10, Hq=8, Hk=2, n_docs=8, docs_per_req=3, min_len=100, max_len=700)
+    B, Hq, Hk = w["B"], w["Hq"], w["Hk"]
+    k_pool, v_pool = bf(w["k_pool"]), bf(w["v_pool"])
+    cache = spkv.paged_kv_create(k_pool, v_pool, None, None, max_units=B * Hk)
+    plan = spkv.DocPlan(cache, Hq, w["picks"], w["doc_first"])
+    words = u32_as_i32(spkv.pack_page_words(w["doc_phys"], w["doc_valid"], np.zeros_like(w["doc_phys"])))
+    q, qpos, df, dp = bf(w["q"]), i32(w["qpos"]), i32(w["doc_first"]), i32(w["doc_pos"])
+    out = torch.empty(B, Hq, 128, dtype=torch.float32, device=DEV)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=DEV)
+    # column scores over request 0's first document's pages as a prompt (window 40 rows)
+    sw = gen.sparse_workload(3, Hq, Hk, 64 * 7 + 9, 4, 4, seed=22)
+    ck = bf(sw["k_pool"])
+    ccache = spkv.paged_kv_create(ck, ck, None, None)
+    alpha = 40
+    cq = bf(gen.rows_bf16(22, 329, 3 * alpha * Hq).reshape(3, alpha, Hq, 128))
+    cpt, cseq = i32(sw["page_table"]), i32(sw["seq_len"])
+    clse = torch.from_numpy(np.random.default_rng(3).normal(6.0, 1.0, (3, alpha, Hq)).astype(np.float32)).to(DEV)
+    s1 = torch.empty(3, Hq, sw["np_max"] * 64, dtype=torch.float32, device=DEV)
+    s2 = torch.empty_like(s1)
+
+    def calls():
+        spkv.lazy_rope_decode_attn_docs(cache, plan, q, qpos, words, df, dp, w["theta"], out, lse)
+        spkv.attn_column_scores(ccache, cq, cpt, cseq, s1)
+        spkv.attn_column_scores_lse(ccache, cq, clse, cpt, cseq, s2)
+
+    calls()
+    torch.cuda.synchronize()
+    eager = [x.clone() for x in (out, lse, s1, s2)]
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=side):
+        calls()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for x in (out, lse, s1, s2):
+            x.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(eager, (out, lse, s1, s2)):
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    assert spkv.get_device_error(cache) == (0, 0) and spkv.get_device_error(ccache) == (0, 0)
+    plan.close()
+    cache.close()
+    ccache.close()

@@ -115,3 +115,41 @@ def test_selection_at_32768_pages_and_4096_entries():
     with pytest.raises(spkv.SpkvError, match="EINVAL"):
         spkv.select_topk(d.cache, s2, s2, a2, i32(seq), 2000, 2096, sel2, n1)
     d.close()
+
+
+@pytest.mark.parametrize("np_max", [1025, 1536, 2047, 2048, 2049, 4095, 4096, 5000, 8192, 8193, 16384, 16385, 20000])
+def test_selection_cta_form_across_sizes(np_max):
+    """The CTA form of the selection (more than 1024 pages: 512 threads of 4, 8, 16 or 32 pages,
+    then 1024 threads of 32) at the edges of each page-per-thread size, bit-exact with the oracle on
+    the same scores: coarse scores with many exact ties and -0.0, random alive masks, ragged
+    contexts, budgets from 0 to more than the candidates.  Sizes that are not a multiple of 4, and
+    score rows that start off a 16-byte boundary, take the per-element loads."""
+    from helpers import alive_bits_to_bytes, alive_bytes_to_bits, u32_as_i32
+    small = gen.sparse_workload(3, 4, 2, 64 * 4, 1, 1, seed=6)
+    d = Dev(small)
+    B, Hk = 3, 2
+    rng = np.random.default_rng(np_max)
+    seq = np.array([64 * np_max, max(1, 64 * np_max - 70), int(rng.integers(1, 64 * np_max + 1))], np.int32)
+    for k_q, k_e, offset in [(64, 64, 0), (0, 7, 0), (9, 0, 1), (min(np_max + 3, 4093), 2, 0), (300, 200, 1)]:
+        s = (np.round(rng.standard_normal((B, Hk, np_max)) * 2) / 2).astype(np.float32)
+        s[rng.random(s.shape) < 0.1] = -0.0
+        e = (np.round(rng.standard_normal((B, Hk, np_max)) * 3) / 3).astype(np.float32)
+        alive = rng.random((B, Hk, np_max)) < 0.7
+        alive_dev = u32_as_i32(alive_bytes_to_bits(alive.astype(np.uint8)))
+        # offset 1: both score rows start one float past a 16-byte boundary
+        sb = torch.zeros(B * Hk * np_max + 4, dtype=torch.float32, device=DEV)
+        eb = torch.zeros_like(sb)
+        s_dev = sb[offset:offset + B * Hk * np_max].view(B, Hk, np_max)
+        e_dev = eb[offset:offset + B * Hk * np_max].view(B, Hk, np_max)
+        s_dev.copy_(f32(s))
+        e_dev.copy_(f32(e))
+        stride = k_q + k_e + 1
+        sel = torch.empty(B, Hk, stride, dtype=torch.int32, device=DEV)
+        n_sel = torch.empty(B, Hk, dtype=torch.int32, device=DEV)
+        spkv.select_topk(d.cache, s_dev, e_dev, alive_dev, i32(seq), k_q, k_e, sel, n_sel)
+        o_sel, o_n, o_alive = oracle.select_batch(s.astype(np.float64), e.astype(np.float64), alive.astype(np.uint8),
+                                                  seq, k_q, k_e)
+        assert np.array_equal(sel.cpu().numpy(), o_sel) and np.array_equal(n_sel.cpu().numpy(), o_n)
+        assert np.array_equal(alive_bits_to_bytes(alive_dev.cpu().numpy().view(np.uint32), np_max), o_alive)
+    assert d.errors() == (0, 0)
+    d.close()
